@@ -1,0 +1,420 @@
+/*
+ * lla_oracle.c -- plain, slow fp64 CPU oracle for log-linear attention in its
+ * Log-Linear Mamba-2 form.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg load this library.  The CUDA library never
+ * includes, links or calls anything in this directory, and this file includes
+ * nothing from the CUDA library.
+ *
+ * Sources (page titles, sections):
+ *   "Log-Linear Attention" (gist.science 2506.04761), technical summary
+ *     §2.2 "数学的定式化": the output is a lambda-weighted sum over levels of
+ *     q_t^T S_t^(l), with the prefix [0,t) split into at most L disjoint
+ *     Fenwick-tree buckets, one hidden state per bucket.
+ *   same page, §2.3 "効率的なアルゴリズム": the decode form is recurrent and
+ *     touches O(log T) states per step.
+ *   same page, §3: the Mamba-2 instance ("Log-Linear Mamba-2"): a scalar
+ *     per-head gate g_t <= 0, G = cumsum(g), decay exp(G_t - G_s).
+ *
+ * Conventions (readings where the pages are silent):
+ *   - positions are 0-based; the buckets of query t partition [0, t);
+ *   - level of a key s for query t is bit_length(t XOR s): 0 for s == t, and
+ *     for s < t the level l >= 1 bucket has 2^(l-1) members;
+ *   - G_t = sum_{r<=t} g_r (inclusive), so the diagonal term has decay 1;
+ *   - L = 1 + bit_length(T-1) weights per token; lambda is [B,H,T,L].
+ *
+ * Every array is C-contiguous fp64.  Layouts:
+ *   q [B,H,T,dk], k [B,H,T,dk], v [B,H,T,dv], g [B,H,T], lam [B,H,T,L],
+ *   out [B,H,T,dv].
+ * Functions return 0 on success and a negative number on a bad argument.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Number of binary digits of x (0 for x == 0), by repeated halving. */
+static int bit_length(uint64_t x)
+{
+    int n = 0;
+    while (x) {
+        n++;
+        x >>= 1;
+    }
+    return n;
+}
+
+/* Number of trailing zero bits of x > 0, by repeated halving. */
+static int trailing_zeros(uint64_t x)
+{
+    int n = 0;
+    while ((x & 1u) == 0u) {
+        n++;
+        x >>= 1;
+    }
+    return n;
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+int oracle_level(int64_t t, int64_t s)
+{
+    return bit_length((uint64_t)(t ^ s));
+}
+
+/* Inclusive running sum of one head's gates: G_t = g_0 + ... + g_t. */
+static void cumsum(const double *g, int64_t T, double *G)
+{
+    double acc = 0.0;
+    for (int64_t t = 0; t < T; t++) {
+        acc += g[t];
+        G[t] = acc;
+    }
+}
+
+static double dot(const double *a, const double *b, int64_t n)
+{
+    double acc = 0.0;
+    for (int64_t i = 0; i < n; i++)
+        acc += a[i] * b[i];
+    return acc;
+}
+
+/*
+ * The defining double sum ("Log-Linear Attention" §2.2 with the Mamba-2 gate
+ * of §3), written out term by term:
+ *     o_t = sum_{s<=t} lam_t[level(t,s)] * exp(G_t - G_s) * (q_t . k_s) * v_s
+ * O(T^2 (dk+dv)) per (batch, head).
+ */
+int oracle_naive(const double *q, const double *k, const double *v,
+                 const double *g, const double *lam, double *out,
+                 int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv,
+                 int64_t L)
+{
+    if (B < 0 || H < 0 || T < 0 || dk <= 0 || dv <= 0 || L <= 0)
+        return -1;
+    if (T > 0 && bit_length((uint64_t)(T - 1)) > L - 1)
+        return -2;
+    int64_t BH = B * H;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t bh = 0; bh < BH; bh++) {
+        const double *qh = q + bh * T * dk;
+        const double *kh = k + bh * T * dk;
+        const double *vh = v + bh * T * dv;
+        const double *gh = g + bh * T;
+        const double *lh = lam + bh * T * L;
+        double *oh = out + bh * T * dv;
+        double *G = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+        if (!G) {
+            bad |= 1;
+            continue;
+        }
+        cumsum(gh, T, G);
+        for (int64_t t = 0; t < T; t++) {
+            double *o = oh + t * dv;
+            for (int64_t j = 0; j < dv; j++)
+                o[j] = 0.0;
+            for (int64_t s = 0; s <= t; s++) {
+                int lev = oracle_level(t, s);
+                double w = lh[t * L + lev] * exp(G[t] - G[s]) *
+                           dot(qh + t * dk, kh + s * dk, dk);
+                const double *vs = vh + s * dv;
+                for (int64_t j = 0; j < dv; j++)
+                    o[j] += w * vs[j];
+            }
+        }
+        free(G);
+    }
+    return bad ? -3 : 0;
+}
+
+/*
+ * Per-token Fenwick recurrence ("Log-Linear Attention" §2.2 buckets, §2.3
+ * recurrent decode), with the decay applied eagerly to every live state.
+ *
+ * Before token t, slot l (l >= 1) holds, when live, the state of one Fenwick
+ * bucket of [0, t):  S_l = sum_{s in bucket} exp(G_{t-1} - G_s) k_s v_s^T.
+ * Step t:
+ *   1. decay every live slot by exp(g_t)   (now decayed to t);
+ *   2. o_t = lam_t[0] (q_t.k_t) v_t + sum_{live l} lam_t[l] q_t^T S_l;
+ *   3. Fenwick insert of token t, a binary-counter carry: the new bucket
+ *      joins token t with the live slots 1..m, m = trailing zeros of t+1;
+ *      slots 1..m are emptied and slot m+1 receives the merged state.
+ * The slots' liveness is tracked with explicit flags, not derived from bits
+ * of t, so that the test suite can check it against the binary digits of t.
+ * If live_count_out is non-NULL it receives, per (b,h,t), the number of live
+ * slots read at step 2.
+ */
+int oracle_fenwick(const double *q, const double *k, const double *v,
+                   const double *g, const double *lam, double *out,
+                   int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv,
+                   int64_t L, int32_t *live_count_out)
+{
+    if (B < 0 || H < 0 || T < 0 || dk <= 0 || dv <= 0 || L <= 0)
+        return -1;
+    if (T > 0 && bit_length((uint64_t)(T - 1)) > L - 1)
+        return -2;
+    /* slots 1..L: the carry after the last token may reach level
+       bit_length(T) = L when T is a power of two. */
+    const int64_t nslot = L + 1;
+    int64_t BH = B * H;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t bh = 0; bh < BH; bh++) {
+        const double *qh = q + bh * T * dk;
+        const double *kh = k + bh * T * dk;
+        const double *vh = v + bh * T * dv;
+        const double *gh = g + bh * T;
+        const double *lh = lam + bh * T * L;
+        double *oh = out + bh * T * dv;
+        double *S = (double *)calloc((size_t)(nslot * dk * dv), sizeof(double));
+        double *merged = (double *)malloc(sizeof(double) * (size_t)(dk * dv));
+        int *live = (int *)calloc((size_t)nslot, sizeof(int));
+        if (!S || !merged || !live) {
+            free(S);
+            free(merged);
+            free(live);
+            bad |= 1;
+            continue;
+        }
+        for (int64_t t = 0; t < T; t++) {
+            const double *qt = qh + t * dk;
+            const double *kt = kh + t * dk;
+            const double *vt = vh + t * dv;
+            const double *lt = lh + t * L;
+            double *o = oh + t * dv;
+            double decay = exp(gh[t]);
+            /* 1. decay */
+            for (int64_t l = 1; l < nslot; l++) {
+                if (!live[l])
+                    continue;
+                double *Sl = S + l * dk * dv;
+                for (int64_t e = 0; e < dk * dv; e++)
+                    Sl[e] *= decay;
+            }
+            /* 2. read-out */
+            double diag = lt[0] * dot(qt, kt, dk);
+            for (int64_t j = 0; j < dv; j++)
+                o[j] = diag * vt[j];
+            int nlive = 0;
+            for (int64_t l = 1; l < nslot; l++) {
+                if (!live[l])
+                    continue;
+                nlive++;
+                if (l >= L) {
+                    bad |= 2; /* a live bucket without a lambda entry */
+                    continue;
+                }
+                const double *Sl = S + l * dk * dv;
+                for (int64_t j = 0; j < dv; j++) {
+                    double acc = 0.0;
+                    for (int64_t i = 0; i < dk; i++)
+                        acc += qt[i] * Sl[i * dv + j];
+                    o[j] += lt[l] * acc;
+                }
+            }
+            if (live_count_out)
+                live_count_out[bh * T + t] = nlive;
+            /* 3. insert token t */
+            int m = trailing_zeros((uint64_t)(t + 1));
+            if (m + 1 >= nslot) {
+                bad |= 4;
+                continue;
+            }
+            for (int64_t i = 0; i < dk; i++)
+                for (int64_t j = 0; j < dv; j++)
+                    merged[i * dv + j] = kt[i] * vt[j];
+            for (int64_t l = 1; l <= m; l++) {
+                if (!live[l]) {
+                    bad |= 8; /* a carry through an empty slot */
+                    continue;
+                }
+                const double *Sl = S + l * dk * dv;
+                for (int64_t e = 0; e < dk * dv; e++)
+                    merged[e] += Sl[e];
+                live[l] = 0;
+            }
+            if (live[m + 1])
+                bad |= 16; /* the carry target must be empty */
+            memcpy(S + (m + 1) * dk * dv, merged, sizeof(double) * (size_t)(dk * dv));
+            live[m + 1] = 1;
+        }
+        free(S);
+        free(merged);
+        free(live);
+    }
+    return bad ? -(8 + bad) : 0;
+}
+
+/*
+ * One decode step on a lazily decayed level state (the recurrent form of
+ * "Log-Linear Attention" §2.3).  The state of one (batch, head):
+ *   S [Ls, dk, dv]: slot i holds level i+1;
+ *   d [Ls]:         log-decay; the level's true state is exp(d) * S.
+ * Slot i is live for token index t iff bit i of t is set.  The step:
+ *   1. d_l += g for every live slot;
+ *   2. o = lam[0] (q.k) v + sum_{live l} lam[l] exp(d_l) q^T S_l;
+ *   3. m = trailing zeros of t+1:
+ *        S_{m+1} = k v^T + sum_{l=1..m} exp(d_l) S_l,  d_{m+1} = 0.
+ * Arguments for one batch of independent (batch, head) pairs, C-contiguous:
+ *   S [B,H,Ls,dk,dv], d [B,H,Ls], q,k [B,H,dk], v [B,H,dv], g [B,H],
+ *   lam [B,H,Ls+1], out [B,H,dv], pos [B] (token index t of the step).
+ * Returns -4 if some t has bit_length(t+1) > Ls (the state has no room).
+ */
+int oracle_decode_step(double *S, double *d, const double *q, const double *k,
+                       const double *v, const double *g, const double *lam,
+                       double *out, const int64_t *pos, int64_t B, int64_t H,
+                       int64_t dk, int64_t dv, int64_t Ls)
+{
+    if (B < 0 || H < 0 || dk <= 0 || dv <= 0 || Ls <= 0)
+        return -1;
+    for (int64_t b = 0; b < B; b++)
+        if (pos[b] < 0 || bit_length((uint64_t)(pos[b] + 1)) > Ls)
+            return -4;
+    int64_t BH = B * H;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t bh = 0; bh < BH; bh++) {
+        int64_t t = pos[bh / H];
+        double *Sh = S + bh * Ls * dk * dv;
+        double *dh = d + bh * Ls;
+        const double *qh = q + bh * dk;
+        const double *kh = k + bh * dk;
+        const double *vh = v + bh * dv;
+        const double *lh = lam + bh * (Ls + 1);
+        double *o = out + bh * dv;
+        for (int64_t i = 0; i < Ls; i++)
+            if ((t >> i) & 1)
+                dh[i] += g[bh];
+        double diag = lh[0] * dot(qh, kh, dk);
+        for (int64_t j = 0; j < dv; j++)
+            o[j] = diag * vh[j];
+        for (int64_t i = 0; i < Ls; i++) {
+            if (!((t >> i) & 1))
+                continue;
+            double w = lh[i + 1] * exp(dh[i]);
+            const double *Si = Sh + i * dk * dv;
+            for (int64_t j = 0; j < dv; j++) {
+                double acc = 0.0;
+                for (int64_t r = 0; r < dk; r++)
+                    acc += qh[r] * Si[r * dv + j];
+                o[j] += w * acc;
+            }
+        }
+        int m = trailing_zeros((uint64_t)(t + 1));
+        double *Snew = Sh + (int64_t)m * dk * dv;
+        /* the target slot m is dead for t (bit m of t is 0), so it can be
+           overwritten only after the sources 0..m-1 are folded in */
+        double *acc = (double *)malloc(sizeof(double) * (size_t)(dk * dv));
+        for (int64_t r = 0; r < dk; r++)
+            for (int64_t j = 0; j < dv; j++)
+                acc[r * dv + j] = kh[r] * vh[j];
+        for (int64_t i = 0; i < m; i++) {
+            double w = exp(dh[i]);
+            const double *Si = Sh + i * dk * dv;
+            for (int64_t e = 0; e < dk * dv; e++)
+                acc[e] += w * Si[e];
+        }
+        memcpy(Snew, acc, sizeof(double) * (size_t)(dk * dv));
+        dh[m] = 0.0;
+        free(acc);
+    }
+    return 0;
+}
+
+/*
+ * The decode state of one prefix, straight from the definition: for query
+ * index pos, every key s < pos goes to level l = bit_length(pos XOR s) >= 1,
+ * decayed to the last prefix token pos-1:
+ *     S_l = sum_{s<pos, level(pos,s)=l} exp(G_{pos-1} - G_s) k_s v_s^T,
+ * stored in slot l-1 with log-decay 0.  Slots with no member are zero.
+ * Arguments: k [B,H,Tp,dk], v [B,H,Tp,dv], g [B,H,Tp] hold prefixes of
+ * length Tp >= max(pos); pos [B]; S out [B,H,Ls,dk,dv]; d out [B,H,Ls].
+ */
+int oracle_state_closed_form(const double *k, const double *v, const double *g,
+                             const int64_t *pos, double *S, double *d,
+                             int64_t B, int64_t H, int64_t Tp, int64_t dk,
+                             int64_t dv, int64_t Ls)
+{
+    if (B < 0 || H < 0 || Tp < 0 || dk <= 0 || dv <= 0 || Ls <= 0)
+        return -1;
+    for (int64_t b = 0; b < B; b++)
+        if (pos[b] < 0 || pos[b] > Tp || bit_length((uint64_t)pos[b]) > Ls)
+            return -4;
+    int64_t BH = B * H;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t bh = 0; bh < BH; bh++) {
+        int64_t p = pos[bh / H];
+        const double *kh = k + bh * Tp * dk;
+        const double *vh = v + bh * Tp * dv;
+        const double *gh = g + bh * Tp;
+        double *Sh = S + bh * Ls * dk * dv;
+        double *dh = d + bh * Ls;
+        memset(Sh, 0, sizeof(double) * (size_t)(Ls * dk * dv));
+        for (int64_t i = 0; i < Ls; i++)
+            dh[i] = 0.0;
+        /* G_{p-1} - G_s = g_{s+1} + ... + g_{p-1}, accumulated backwards */
+        double tail = 0.0;
+        for (int64_t s = p - 1; s >= 0; s--) {
+            int lev = oracle_level(p, s);
+            double w = exp(tail);
+            double *Sl = Sh + (int64_t)(lev - 1) * dk * dv;
+            const double *ks = kh + s * dk;
+            const double *vs = vh + s * dv;
+            for (int64_t r = 0; r < dk; r++)
+                for (int64_t j = 0; j < dv; j++)
+                    Sl[r * dv + j] += w * ks[r] * vs[j];
+            tail += gh[s];
+        }
+    }
+    return 0;
+}
+
+/*
+ * Plain gated linear attention (the Mamba-2 scalar-gate scan the pages build
+ * on): one state, S_t = exp(g_t) S_{t-1} + k_t v_t^T, o_t = S_t^T q_t.
+ * Log-linear attention with every lambda equal to 1 reduces to this.
+ */
+int oracle_ssd(const double *q, const double *k, const double *v,
+               const double *g, double *out, int64_t B, int64_t H, int64_t T,
+               int64_t dk, int64_t dv)
+{
+    if (B < 0 || H < 0 || T < 0 || dk <= 0 || dv <= 0)
+        return -1;
+    int64_t BH = B * H;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t bh = 0; bh < BH; bh++) {
+        const double *qh = q + bh * T * dk;
+        const double *kh = k + bh * T * dk;
+        const double *vh = v + bh * T * dv;
+        const double *gh = g + bh * T;
+        double *oh = out + bh * T * dv;
+        double *S = (double *)calloc((size_t)(dk * dv), sizeof(double));
+        for (int64_t t = 0; t < T; t++) {
+            double a = exp(gh[t]);
+            for (int64_t r = 0; r < dk; r++)
+                for (int64_t j = 0; j < dv; j++)
+                    S[r * dv + j] = a * S[r * dv + j] + kh[t * dk + r] * vh[t * dv + j];
+            for (int64_t j = 0; j < dv; j++) {
+                double acc = 0.0;
+                for (int64_t r = 0; r < dk; r++)
+                    acc += qh[t * dk + r] * S[r * dv + j];
+                oh[t * dv + j] = acc;
+            }
+        }
+        free(S);
+    }
+    return 0;
+}

@@ -1,0 +1,264 @@
+"""Pins of the fp64 oracle against facts fixed by the pages and by mathematics,
+not against the oracle itself.
+
+Page "Log-Linear Attention" (gist.science 2506.04761), technical summary:
+  §2.2  the output is sum_l lambda_t^(l) q_t^T S_t^(l), the prefix [0,t) split
+        into <= L disjoint Fenwick buckets;
+  §2.3  decoding is recurrent with O(log T) states;
+  §3    the Mamba-2 instance with a scalar gate.
+Page "Adaptive memory decay for Log-Linear Attention", §LambdaMLPSoftplus:
+  softplus(0.54) is about 1.0 (the lambda initialisation the workloads centre on).
+
+Each test below would fail on a plausible slip in the oracle: a wrong level
+index (bucket tests, hand table), an exclusive instead of inclusive gate sum or
+a sign error in the decay (hand-expanded T=3 case, SSD reduction), a dropped
+diagonal or level term (lambda = e_l tests), a transposed state (decode replay
+and closed-form state against the double sum).
+"""
+
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rand_inputs(B, H, T, dk, dv, seed, g_scale=1.0, L=None):
+    rng = np.random.default_rng(seed)
+    L = oracle.num_levels(T) if L is None else L
+    q = rng.standard_normal((B, H, T, dk)) / math.sqrt(dk)
+    k = rng.standard_normal((B, H, T, dk))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((B, H, T, dv))
+    g = -np.log1p(np.exp(rng.standard_normal((B, H, T)))) * g_scale
+    lam = np.log1p(np.exp(0.54 + 0.3 * rng.standard_normal((B, H, T, L))))
+    return q, k, v, g, lam
+
+
+def fenwick_buckets(t):
+    """Buckets of [0,t) by peeling the lowest set bit of the Fenwick index:
+    j = t, t - lowbit(t), ...; bucket [j - lowbit(j), j) has lowbit(j) keys.
+    Returns a list of (first, end, size)."""
+    out = []
+    j = t
+    while j > 0:
+        low = j & -j
+        out.append((j - low, j, low))
+        j -= low
+    return out
+
+
+def relerr(a, b):
+    return np.max(np.abs(a - b)) / max(1.0, np.max(np.abs(b)))
+
+
+# ---------------------------------------------------------------- levels
+
+def test_level_table_T8_golden():
+    rows = {}
+    with open(os.path.join(GOLDEN, "fenwick_levels_T8.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            t, rest = line.split(":")
+            rows[int(t)] = [int(x) for x in rest.split()]
+    assert sorted(rows) == list(range(8))
+    for t, levels in rows.items():
+        assert [oracle.level(t, s) for s in range(t + 1)] == levels
+
+
+@pytest.mark.parametrize("T", list(range(1, 17)))
+def test_levels_are_fenwick_buckets(T):
+    for t in range(T):
+        buckets = fenwick_buckets(t)
+        # the buckets partition [0, t), finer near t, at most L-1 of them
+        covered = sorted(s for a, b, _ in buckets for s in range(a, b))
+        assert covered == list(range(t))
+        assert len(buckets) == bin(t).count("1")
+        assert len(buckets) <= oracle.num_levels(T) - 1
+        sizes = [n for _, _, n in buckets]
+        assert sizes == sorted(sizes)
+        for a, b, n in buckets:
+            lev = n.bit_length()  # 2^(l-1) keys <-> level l
+            for s in range(a, b):
+                assert oracle.level(t, s) == lev
+        assert oracle.level(t, t) == 0
+
+
+def test_num_levels_of_the_workloads():
+    assert [oracle.num_levels(T) for T in (256, 2048, 8192, 32768, 65536)] == \
+        [9, 12, 14, 16, 17]
+    assert oracle.num_levels(1) == 1
+
+
+# ---------------------------------------------------------- hand expansion
+
+def test_hand_expanded_T3():
+    """o_2 written out by hand from the definition: keys 0 and 1 form the
+    level-2 bucket of query 2; key 2 is the diagonal.  G is the inclusive
+    running sum, so key 1 decays by exp(g_2) and key 0 by exp(g_1 + g_2)."""
+    q, k, v, g, lam = rand_inputs(1, 1, 3, 4, 5, seed=11, L=3)
+    q0, k0, v0, g0, l0 = q[0, 0], k[0, 0], v[0, 0], g[0, 0], lam[0, 0]
+    o = oracle.naive(q, k, v, g, lam)[0, 0]
+    o0 = l0[0, 0] * (q0[0] @ k0[0]) * v0[0]
+    o1 = l0[1, 0] * (q0[1] @ k0[1]) * v0[1] + \
+        l0[1, 1] * math.exp(g0[1]) * (q0[1] @ k0[0]) * v0[0]
+    o2 = l0[2, 0] * (q0[2] @ k0[2]) * v0[2] + l0[2, 2] * (
+        math.exp(g0[1] + g0[2]) * (q0[2] @ k0[0]) * v0[0] +
+        math.exp(g0[2]) * (q0[2] @ k0[1]) * v0[1])
+    np.testing.assert_allclose(o[0], o0, rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(o[1], o1, rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(o[2], o2, rtol=1e-13, atol=1e-15)
+    # lambda entries at levels with no bucket are ignored
+    lam2 = lam.copy()
+    lam2[0, 0, 2, 1] = 1e6
+    lam2[0, 0, 1, 2] = -7.0
+    np.testing.assert_allclose(oracle.naive(q, k, v, g, lam2)[0, 0], o, rtol=1e-14)
+
+
+# ------------------------------------------------ two independent derivations
+
+@pytest.mark.parametrize("B,H,T,dk,dv", [(1, 1, 1, 4, 4), (2, 3, 64, 8, 8), (1, 2, 100, 5, 7),
+                                         (1, 1, 257, 6, 3), (1, 1, 512, 4, 4)])
+def test_naive_equals_fenwick_recurrence(B, H, T, dk, dv):
+    q, k, v, g, lam = rand_inputs(B, H, T, dk, dv, seed=T)
+    a = oracle.naive(q, k, v, g, lam)
+    b, live = oracle.fenwick(q, k, v, g, lam, return_live_counts=True)
+    assert relerr(b, a) <= 1e-10
+    # the recurrent form touches popcount(t) <= bit_length(t) states (§2.3)
+    for t in range(T):
+        assert (live[..., t] == bin(t).count("1")).all()
+        assert bin(t).count("1") <= max(t, 0).bit_length()
+
+
+def test_naive_equals_fenwick_slow_decay():
+    q, k, v, g, lam = rand_inputs(1, 2, 300, 8, 8, seed=3, g_scale=0.01)
+    assert relerr(oracle.fenwick(q, k, v, g, lam), oracle.naive(q, k, v, g, lam)) <= 1e-10
+
+
+# ------------------------------------------------------------- reductions
+
+def test_lambda_one_is_gated_linear_attention():
+    """Every lambda = 1: the Fenwick levels merge back into the single-state
+    Mamba-2 scan S_t = e^{g_t} S_{t-1} + k_t v_t^T, o_t = S_t^T q_t."""
+    q, k, v, g, lam = rand_inputs(2, 2, 200, 6, 5, seed=5)
+    ones = np.ones_like(lam)
+    ref = oracle.ssd(q, k, v, g)
+    assert relerr(oracle.naive(q, k, v, g, ones), ref) <= 1e-10
+    assert relerr(oracle.fenwick(q, k, v, g, ones), ref) <= 1e-10
+
+
+def test_no_decay_lambda_one_is_causal_linear_attention():
+    q, k, v, g, lam = rand_inputs(1, 1, 50, 7, 6, seed=6)
+    zeros = np.zeros_like(g)
+    ones = np.ones_like(lam)
+    Q, K, V = q[0, 0], k[0, 0], v[0, 0]
+    ref = np.tril(Q @ K.T) @ V
+    assert relerr(oracle.naive(q, k, v, zeros, ones)[0, 0], ref) <= 1e-12
+    assert relerr(oracle.fenwick(q, k, v, zeros, ones)[0, 0], ref) <= 1e-12
+    assert relerr(oracle.ssd(q, k, v, zeros)[0, 0], ref) <= 1e-12
+
+
+def test_level0_only_is_the_diagonal():
+    q, k, v, g, lam = rand_inputs(1, 2, 40, 6, 4, seed=7)
+    lam0 = np.zeros_like(lam)
+    lam0[..., 0] = lam[..., 0]
+    ref = lam[..., 0:1] * np.sum(q * k, axis=-1, keepdims=True) * v
+    assert relerr(oracle.naive(q, k, v, g, lam0), ref) <= 1e-13
+    assert relerr(oracle.fenwick(q, k, v, g, lam0), ref) <= 1e-13
+
+
+@pytest.mark.parametrize("lev", [1, 2, 3, 4, 5])
+def test_single_level_is_its_bucket_sum(lev):
+    """lambda = e_l: the output is the decayed sum over the level-l Fenwick
+    bucket of [0,t), the bucket taken from lowest-bit peeling."""
+    T = 40
+    q, k, v, g, lam = rand_inputs(1, 1, T, 5, 3, seed=8 + lev)
+    e = np.zeros_like(lam)
+    e[..., lev] = 1.0
+    G = np.cumsum(g[0, 0])
+    ref = np.zeros((T, 3))
+    for t in range(T):
+        for a, b, n in fenwick_buckets(t):
+            if n.bit_length() != lev:
+                continue
+            for s in range(a, b):
+                ref[t] += math.exp(G[t] - G[s]) * (q[0, 0, t] @ k[0, 0, s]) * v[0, 0, s]
+    assert relerr(oracle.naive(q, k, v, g, e)[0, 0], ref) <= 1e-12
+    assert relerr(oracle.fenwick(q, k, v, g, e)[0, 0], ref) <= 1e-12
+
+
+def test_linear_in_lambda():
+    q, k, v, g, lam = rand_inputs(1, 2, 64, 4, 4, seed=9)
+    L = lam.shape[-1]
+    total = np.zeros_like(oracle.naive(q, k, v, g, lam))
+    for lev in range(L):
+        part = np.zeros_like(lam)
+        part[..., lev] = lam[..., lev]
+        total += oracle.naive(q, k, v, g, part)
+    assert relerr(total, oracle.naive(q, k, v, g, lam)) <= 1e-12
+
+
+# ------------------------------------------------------------------ decode
+
+def test_decode_replay_reproduces_the_double_sum():
+    B, H, T, dk, dv = 2, 2, 70, 6, 5
+    q, k, v, g, lam = rand_inputs(B, H, T, dk, dv, seed=12)
+    Ls = (T).bit_length()  # room for the carry after the last token
+    L = lam.shape[-1]
+    ref = oracle.naive(q, k, v, g, lam)
+    S = np.zeros((B, H, Ls, dk, dv))
+    d = np.zeros((B, H, Ls))
+    for t in range(T):
+        lam_t = np.zeros((B, H, Ls + 1))
+        lam_t[..., :L] = lam[:, :, t]
+        o = oracle.decode_step(S, d, q[:, :, t], k[:, :, t], v[:, :, t], g[:, :, t], lam_t,
+                               np.full(B, t))
+        assert relerr(o, ref[:, :, t]) <= 1e-10
+    # after T tokens the lazily decayed state equals the bucket states of [0,T)
+    S_cf, d_cf = oracle.state_closed_form(k, v, g, np.full(B, T), Ls)
+    live = np.array([(T >> i) & 1 for i in range(Ls)], bool)
+    true_state = np.exp(d)[..., None, None] * S
+    assert relerr(true_state[:, :, live], S_cf[:, :, live]) <= 1e-10
+    assert np.all(S_cf[:, :, ~live] == 0)
+
+
+def test_decode_from_closed_form_state_mid_sequence():
+    """Start decode at a position p taken from the closed-form state and
+    check the next outputs against the double sum."""
+    B, H, T, dk, dv = 3, 1, 90, 4, 4
+    q, k, v, g, lam = rand_inputs(B, H, T, dk, dv, seed=13)
+    ref = oracle.naive(q, k, v, g, lam)
+    L = lam.shape[-1]
+    Ls = T.bit_length()
+    pos = np.array([37, 64, 81])
+    S, d = oracle.state_closed_form(k, v, g, pos, Ls)
+    for step in range(T - 81):
+        p = pos + step
+        lam_t = np.zeros((B, H, Ls + 1))
+        bidx = np.arange(B)
+        lam_t[..., :L] = lam[bidx, :, p]
+        o = oracle.decode_step(S, d, q[bidx, :, p], k[bidx, :, p], v[bidx, :, p],
+                               g[bidx, :, p], lam_t, p)
+        assert relerr(o, ref[bidx, :, p]) <= 1e-10
+
+
+def test_decode_rejects_a_state_without_room():
+    S = np.zeros((1, 1, 3, 2, 2))
+    d = np.zeros((1, 1, 3))
+    z = np.zeros((1, 1, 2))
+    with pytest.raises(RuntimeError):  # bit_length(7 + 1) = 4 > 3 slots
+        oracle.decode_step(S, d, z, z, z, np.zeros((1, 1)), np.zeros((1, 1, 4)), [7])
+
+
+# ------------------------------------------------------- lambda's centre
+
+def test_softplus_centre_is_one():
+    """Page "Adaptive memory decay for Log-Linear Attention": the bias 0.54
+    makes softplus start near 1.0."""
+    assert abs(math.log1p(math.exp(0.54)) - 0.99916) < 5e-6
