@@ -1,0 +1,411 @@
+#!/usr/bin/env python
+"""Throughput of the log-linear attention forward (and decode) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl lla|reference]
+
+One step = one lla_fwd over the T=32768 workload (B=1, H=16, dk=dv=128,
+chunk 64, bf16 q/k/v, fp32 g/lambda/out), inputs resident in HBM.  Rank 0
+prints one JSON line.  With N > 1 (torchrun) every rank runs its own copy of
+the workload on its GPU (independent (batch, head) units: weak scaling, no
+collective on the data path); time is the max over ranks.
+
+--impl reference times the fp64 CPU oracle (its Fenwick recurrent form, the
+O(T log T) one) on a bounded sample of the same workload, on this host's
+cores, in the same unit.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from log_linear_attention_chunkwise_gb300 import workloads as W  # noqa: E402
+
+METRIC = "log-linear attn fwd tokens/s & TFLOP/s at T=8K–32K; decode HBM GB/s"
+WORKLOAD = "bf16_T32768_slowdecay"
+
+
+# ----------------------------------------------------------------- helpers
+
+def fwd_flops(cfg: W.FwdConfig) -> float:
+    """Algorithmic flops of one chunked forward at the workload's chunk size:
+    causal half of the intra-chunk products, the chunk states, the Fenwick
+    read-out (popcount(i) states per chunk i) and the node scan."""
+    C, N, dk, dv = cfg.chunk, cfg.T // cfg.chunk, cfg.dk, cfg.dv
+    intra = N * C * (C + 1) / 2 * 2 * (dk + dv)
+    state = N * 2 * C * dk * dv
+    readout = sum(bin(i).count("1") for i in range(N)) * 2 * C * dk * dv
+    scan = sum(1 + ((j & -j).bit_length() - 1) for j in range(1, N)) * 2 * dk * dv
+    return cfg.B * cfg.H * (intra + state + readout + scan)
+
+
+def fwd_bytes(cfg: W.FwdConfig, out_bytes: int = 4) -> float:
+    """Compulsory HBM bytes of one forward: read q, k, v, g, lambda; write out."""
+    e = torch.empty(0, dtype=cfg.dtype).element_size()
+    per_tok = 2 * cfg.dk * e + cfg.dv * e + 4 + 4 * cfg.L + cfg.dv * out_bytes
+    return cfg.B * cfg.H * cfg.T * per_tok
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "log_linear_attention_chunkwise_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(kernel_digest: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, or None when the kernel sources changed since the capture."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None, None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("source_digest") != kernel_digest:
+        return None, d.get("kernel")
+    return d.get("bytes_per_launch"), d.get("kernel")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except FileNotFoundError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), util=float(parts[4]),
+                                 hw=parts[6], hwt=parts[7], swt=parts[8], swp=parts[9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        load = [r for r in rows if r["util"] >= 50] or rows
+        reasons = set()
+        for r in load:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in load),
+                "sm_max_mhz": max(r["smax"] for r in rows), "reasons": sorted(reasons),
+                "samples_under_load": len(load)}
+
+
+# ------------------------------------------------------------- our arm
+
+def run_lla(args, rank, world, local_rank):
+    from log_linear_attention_chunkwise_gb300 import binding
+    binding.load()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    cfg = W.FWD_CONFIGS[WORKLOAD]
+    x = W.make_fwd_inputs(cfg)
+    xd = {n: t.to(dev) for n, t in x.items()}
+    out = torch.empty((cfg.B, cfg.H, cfg.T, cfg.dv), dtype=torch.float32, device=dev)
+    need = binding.fwd_workspace_bytes(cfg.B, cfg.H, cfg.T, cfg.dk, cfg.dv, cfg.chunk, cfg.dtype)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    launches_per_call = binding.load().lla_fwd_launches(
+        cfg.B, cfg.H, cfg.T, cfg.dk, cfg.dv, cfg.chunk, binding.LLA_BF16, binding.LLA_F32)
+
+    def step():
+        binding.fwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["lam"], chunk=cfg.chunk, out=out,
+                    workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        torch.cuda.synchronize(dev)
+        t_start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    per_launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    tokens = cfg.tokens * world
+    value = tokens / (ms_per_step / 1e3)
+
+    # end to end through the public call with pinned host buffers
+    hx = {n: t.pin_memory() for n, t in x.items()}
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in hx.values())
+    d2h = hout.numel() * hout.element_size()
+
+    def e2e_step():
+        for n in xd:
+            xd[n].copy_(hx[n], non_blocking=True)
+        step()
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_steps = max(3, min(args.steps, 10))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = a.elapsed_time(b) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    hbm_peak, bf16_peak, bf16_sus, peak_src = load_peaks()
+    nbytes = fwd_bytes(cfg)
+    flops = fwd_flops(cfg)
+    achieved_gbs = nbytes / (per_launch_ms / 1e3) / 1e9
+    tflops = flops / (per_launch_ms / 1e3) / 1e12
+    traffic, traffic_kernel = load_traffic(source_digest())
+    res = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; q,k,v bf16, g,lambda fp32)",
+        "config": {"workload": f"{WORKLOAD}: B=1 H=16 T=32768 dk=dv=128 chunk=64 bf16 in, fp32 out",
+                   "global_batch": cfg.B * world, "seq_len": cfg.T,
+                   "parallelism": f"replicas over (batch, head) units x{world}",
+                   "l2": "inputs (436 MB) larger than L2, no flush"},
+        "tflops": tflops, "tflops_frac_of_bf16_peak": tflops / bf16_peak,
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved_gbs / hbm_peak, "traffic": traffic,
+                     "kernel": "lla_fwd (all launches of one call)",
+                     "algorithmic_bytes_per_launch": nbytes, "algorithmic_flops_per_launch": flops,
+                     "per_launch_ms": per_launch_ms,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"},
+        "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_call * args.steps,
+        "clocks": clk.summary(),
+    }
+    del hx, hout
+    if rank == 0 and not args.skip_decode:
+        res["decode"] = run_decode(dev, args)
+    if rank == 0 and not args.skip_cpu:
+        res["cpu_baseline"] = cpu_baseline(x, cfg, args.cpu_tokens)
+    res["context"] = ("pages: a Triton kernel overtakes FlashAttention-2 from about 8K tokens "
+                      "(hardware not named)")
+    return res
+
+
+def decode_bytes(cfg: W.DecodeConfig, pos) -> float:
+    slot = cfg.dk * cfg.dv * 4
+    total = 0.0
+    for p in pos:
+        p = int(p)
+        total += (bin(p).count("1") + 1) * slot
+    vec = (2 * cfg.dk + cfg.dv) * 2 + 4 + 4 * (cfg.Ls + 1) + cfg.dv * 4 + 2 * 4 * cfg.Ls
+    return cfg.H * total + cfg.batch * cfg.H * vec + cfg.batch * 8
+
+
+def run_decode(dev, args):
+    from log_linear_attention_chunkwise_gb300 import binding
+    cfg = W.DECODE_CONFIG
+    pos0 = W.make_decode_positions(cfg)
+    Bn, H, dk, dv, Ls = cfg.batch, cfg.H, cfg.dk, cfg.dv, cfg.Ls
+    S = torch.empty((Bn, H, Ls, dk, dv), device=dev)
+    D = torch.empty((Bn, H, Ls), device=dev)
+    for b in range(Bn):
+        n = int(pos0[b])
+        pre = W.make_decode_prefix(cfg, pos0, n, device=dev, seqs=[b])
+        binding.prefill_state(pre["k"], pre["v"], pre["g"], Ls, state=S[b:b + 1],
+                              logdecay=D[b:b + 1])
+        del pre
+    steps = W.make_decode_steps(cfg, device=dev)
+    out = torch.empty((cfg.steps, Bn, H, dv), device=dev)
+    pos = (pos0[None, :] + torch.arange(cfg.steps)[:, None]).to(dev).contiguous()
+    S0, D0 = S.clone(), D.clone()
+    stream = torch.cuda.Stream(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for s in range(2):  # warm the kernels before capture
+            binding.decode_step(S, D, steps["q"][s], steps["k"][s], steps["v"][s], steps["g"][s],
+                                steps["lam"][s], pos[s], out=out[s], stream=stream)
+        torch.cuda.synchronize(dev)
+        S.copy_(S0)
+        D.copy_(D0)
+        with torch.cuda.graph(graph, stream=stream):
+            for s in range(cfg.steps):
+                binding.decode_step(S, D, steps["q"][s], steps["k"][s], steps["v"][s],
+                                    steps["g"][s], steps["lam"][s], pos[s], out=out[s],
+                                    stream=torch.cuda.current_stream())
+    reps = 5
+    times = []
+    for r in range(reps + 1):
+        S.copy_(S0)
+        D.copy_(D0)
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        if r > 0:
+            times.append(a.elapsed_time(b) / cfg.steps)
+    us = statistics.median(times) * 1e3
+    nbytes = statistics.mean(decode_bytes(cfg, pos0 + s) for s in range(cfg.steps))
+    gbs = nbytes / (us / 1e6) / 1e9
+    hbm_peak = load_peaks()[0]
+    return {"workload": "decode: 64 seqs, H=16, dk=dv=128, Ls=17 fp32 slots, 256 steps in one CUDA graph",
+            "us_per_step": us, "algorithmic_bytes_per_step": nbytes, "achieved_gbs": gbs,
+            "frac_of_hbm": gbs / hbm_peak, "gpu_launches_per_step": 1}
+
+
+def cpu_baseline(x, cfg, ntok):
+    import oracle
+    n = min(ntok, cfg.T)
+    sl = {k: v[:, :, :n] for k, v in x.items()}
+    sl["lam"] = x["lam"][:, :, :n, :]
+    t0 = time.perf_counter()
+    oracle.fenwick(sl["q"], sl["k"], sl["v"], sl["g"], sl["lam"])
+    dt = time.perf_counter() - t0
+    return {"value": cfg.B * n / dt, "unit": "tokens/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"fp64 oracle, Fenwick recurrent form, all {cfg.H} heads, tokens [0,{n}) "
+                      f"of the T={cfg.T} workload ({dt:.1f} s)"}
+
+
+# ------------------------------------------------------- reference arm
+
+def run_reference(args):
+    import oracle
+    cfg = W.FWD_CONFIGS[WORKLOAD]
+    n = args.ref_tokens
+    x = W.make_fwd_inputs(cfg.with_(T=n))  # same recipe; first tokens of a shorter draw
+    sl = {k: v for k, v in x.items()}
+    # lambda width of the full workload (levels beyond the sample are unused)
+    lam = torch.zeros((cfg.B, cfg.H, n, cfg.L))
+    lam[..., :sl["lam"].shape[-1]] = sl["lam"]
+    sl["lam"] = lam
+    for _ in range(args.warmup):
+        oracle.fenwick(sl["q"], sl["k"], sl["v"], sl["g"], sl["lam"])
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.fenwick(sl["q"], sl["k"], sl["v"], sl["g"], sl["lam"])
+    dt = (time.perf_counter() - t0) / args.steps
+    value = cfg.B * n / dt
+    sample = (f"fp64 oracle (Fenwick recurrent form), all {cfg.H} heads x {n} tokens per step "
+              f"(bounded sample of the T={cfg.T} workload)")
+    return {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)", "impl": "reference",
+            "config": {"workload": f"{WORKLOAD}: B=1 H=16 T=32768 dk=dv=128 (sample: first {n} tokens)"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="lla", choices=["lla", "reference"])
+    ap.add_argument("--skip-decode", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--cpu-tokens", type=int, default=8192)
+    ap.add_argument("--ref-tokens", type=int, default=2048)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res = run_lla(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

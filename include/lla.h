@@ -1,0 +1,166 @@
+/*
+ * lla.h -- C ABI of liblla.so: log-linear attention (Log-Linear Mamba-2 form)
+ * on one NVIDIA GB300 GPU (sm_103a).
+ *
+ * The operator (page "Log-Linear Attention", gist.science 2506.04761,
+ * technical summary §2.2 output equation, with the scalar-gate Mamba-2
+ * instance of §3), for every batch b, head h and token t:
+ *
+ *     o_t = sum_{s <= t} lambda_t[l(t,s)] * exp(G_t - G_s) * (q_t . k_s) * v_s
+ *
+ *     G_t    = g_0 + ... + g_t          (inclusive running sum of the gates)
+ *     l(t,s) = bit_length(t XOR s)       (0 when s == t; otherwise the
+ *                                         Fenwick-tree bucket of [0,t) that
+ *                                         holds s, 2^(l-1) keys per bucket)
+ *     L      = 1 + bit_length(T - 1)     (lambda entries per token)
+ *
+ * Positions are 0-based.  Gates are log-decays, g <= 0 in the intended use
+ * (the library does not require it).  Lambda entries at levels with no
+ * bucket for a given t multiply an empty sum and are ignored.
+ *
+ * Conventions for every entry point:
+ *   - Tensor pointers are DEVICE pointers to caller-owned memory, densely
+ *     packed (C-contiguous) in the layout given, 16-byte aligned.  The
+ *     library keeps no pointer after a call returns and allocates no device
+ *     memory.  Scratch memory is a caller-provided workspace, sized by the
+ *     matching *_workspace_bytes query.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every call is asynchronous and stream-ordered: it enqueues
+ *     kernels and returns without synchronising the host.
+ *   - Arguments are validated before anything is enqueued.  A validation
+ *     failure returns an error and enqueues nothing.  LLA_ERR_CUDA means a
+ *     launch was rejected by the CUDA runtime (the runtime's last error is
+ *     left for the caller to inspect with cudaGetLastError).
+ *   - The current CUDA device must be the device that owns the pointers.
+ */
+#ifndef LLA_H
+#define LLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LLA_F32 = 0,  /* IEEE binary32                              */
+    LLA_BF16 = 1  /* bfloat16 (8-bit exponent, 7-bit mantissa)  */
+} lla_dtype;
+
+typedef enum {
+    LLA_OK = 0,
+    LLA_ERR_INVALID_ARGUMENT = 1,    /* null pointer, negative size, bad enum     */
+    LLA_ERR_UNSUPPORTED_SHAPE = 2,   /* a size outside the supported set          */
+    LLA_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < the query's answer       */
+    LLA_ERR_CUDA = 4,                /* a kernel launch failed                     */
+    LLA_ERR_DEVICE_REPORTED = 5      /* reserved for errors read back from device */
+} lla_status;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *lla_status_string(lla_status s);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int lla_version(void);
+
+/* L = 1 + bit_length(T-1): lambda entries per token for a length-T forward
+ * (level 0 plus the Fenwick levels of the longest prefix).  0 for T <= 0. */
+int lla_num_levels(int T);
+
+/*
+ * Chunked O(T log T) forward ("Log-Linear Attention" §2.3: the hierarchical
+ * mask trained in parallel, matmul-rich).  The sequence is cut into chunks of
+ * `chunk` tokens; within a chunk the masked product (Q K^T . M) V is formed
+ * directly, and every earlier chunk is reached through the chunk-level
+ * Fenwick-tree states of §2.2, each weighted per token by its lambda.  The
+ * result does not depend on `chunk` beyond rounding.
+ *
+ *   q      [B,H,T,dk]  in_dt       k [B,H,T,dk] in_dt      v [B,H,T,dv] in_dt
+ *   g      [B,H,T]     fp32        per-token log-gate
+ *   lambda [B,H,T,L]   fp32        L = lla_num_levels(T)
+ *   out    [B,H,T,dv]  out_dt      fully overwritten
+ *
+ * Supported: B,H >= 0; T >= 0 with T % chunk == 0 and T <= 2^24;
+ * chunk in {16,32,64,128}; dk, dv in {16,32,64,128};
+ * (in_dt, out_dt) in {(F32,F32), (BF16,F32), (BF16,BF16)}.
+ * B*H*T == 0 is a valid no-op.  Other shapes: LLA_ERR_UNSUPPORTED_SHAPE.
+ * workspace: device memory of at least lla_fwd_workspace_bytes(...) bytes,
+ * 256-byte aligned; its contents on entry do not matter and are undefined on
+ * return.  Calls that share a workspace must not overlap on the GPU.
+ * q, k, v, g, lambda are read only; out must not alias an input.
+ */
+size_t lla_fwd_workspace_bytes(int B, int H, int T, int dk, int dv, int chunk,
+                               lla_dtype in_dt);
+
+/* Number of kernel launches (memsets included) one lla_fwd call with these
+ * arguments enqueues on its stream; 0 for an empty or unsupported call. */
+int lla_fwd_launches(int B, int H, int T, int dk, int dv, int chunk, lla_dtype in_dt,
+                     lla_dtype out_dt);
+
+lla_status lla_fwd(const void *q, const void *k, const void *v,
+                   const float *g, const float *lambda, void *out,
+                   int B, int H, int T, int dk, int dv, int chunk,
+                   lla_dtype in_dt, lla_dtype out_dt,
+                   void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Decode state (the recurrent form of "Log-Linear Attention" §2.3: O(log T)
+ * states, each step reads and updates O(log T) of them).  For one (b,h) at
+ * token index t the state holds the Fenwick buckets of the prefix [0,t):
+ *   state_levels   [B,H,Ls,dk,dv] fp32: slot i holds level i+1;
+ *   state_logdecay [B,H,Ls]       fp32: the level's true state is
+ *                                 exp(state_logdecay) * state_levels.
+ * Slot i is live iff bit i of t is set; dead slots are never read.  A zeroed
+ * state is the state of the empty prefix (t = 0).
+ * lla_decode_state_bytes returns the size of state_levels in bytes.
+ */
+size_t lla_decode_state_bytes(int B, int H, int dk, int dv, int Ls);
+
+/*
+ * One decode step for B sequences x H heads; sequence b is at token index
+ * t = pos[b] (the state holds [0,t) and this call consumes token t):
+ *   1. logdecay += g for the live slots;
+ *   2. out = lambda[0] (q.k) v + sum_{live l} lambda[l] exp(logdecay_l) q^T S_l;
+ *   3. with m = trailing zeros of t+1, slot m (level m+1) becomes
+ *      k v^T + sum_{l=1..m} exp(logdecay_l) S_l with logdecay 0; slots
+ *      0..m-1 become dead (they are not cleared).
+ *   q, k [B,H,dk] in_dt; v [B,H,dv] in_dt; g [B,H] fp32;
+ *   lambda [B,H,Ls+1] fp32 (levels 0..Ls); out [B,H,dv] fp32;
+ *   pos [B] int64 on the device, read by the kernel (the caller advances it).
+ * Supported: dk, dv in {16,32,64,128}; 1 <= Ls <= 40; in_dt F32 or BF16.
+ * A sequence with pos < 0 or bit_length(pos+1) > Ls is skipped (its out and
+ * state are left untouched) and, if device_error is non-NULL, the kernel
+ * stores 1 + b into *device_error (one of the offending b when several).
+ * The kernel never traps.  device_error is device memory owned by the caller;
+ * the library only ever writes a nonzero value into it.
+ */
+lla_status lla_decode_step(float *state_levels, float *state_logdecay,
+                           const void *q, const void *k, const void *v,
+                           const float *g, const float *lambda, float *out,
+                           const int64_t *pos, int B, int H, int dk, int dv,
+                           int Ls, lla_dtype in_dt, int32_t *device_error,
+                           void *stream);
+
+/*
+ * Prefill -> decode hand-off: the decode state after the prefix [0,T), i.e.
+ * for the next token index t = T, computed from the bucket definition of
+ * "Log-Linear Attention" §2.2:
+ *   S_l = sum_{s<T, l(T,s)=l} exp(G_{T-1} - G_s) k_s v_s^T,   logdecay_l = 0,
+ * and dead slots zeroed.  k [B,H,T,dk], v [B,H,T,dv] in_dt; g [B,H,T] fp32;
+ * state_levels [B,H,Ls,dk,dv] fp32 and state_logdecay [B,H,Ls] fp32 are
+ * fully overwritten.  Requires bit_length(T) <= Ls <= 40, T <= 2^30.
+ * workspace: at least lla_prefill_workspace_bytes(B,H,T) bytes.
+ */
+size_t lla_prefill_workspace_bytes(int B, int H, int T);
+
+lla_status lla_prefill_state(const void *k, const void *v, const float *g,
+                             float *state_levels, float *state_logdecay,
+                             int B, int H, int T, int dk, int dv, int Ls,
+                             lla_dtype in_dt, void *workspace,
+                             size_t workspace_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LLA_H */

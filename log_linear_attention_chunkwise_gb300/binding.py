@@ -1,0 +1,180 @@
+"""Thin ctypes binding of liblla.so: the same entry points, torch tensors in.
+
+Argument marshalling only (shape/dtype/device checks, pointers, the current
+stream, workspace allocation through torch's allocator).  Every step of the
+operator runs in the library's CUDA kernels; there is no other code path.
+If ``liblla.so`` is missing the first call raises, it never falls back.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "liblla.so")
+
+LLA_F32, LLA_BF16 = 0, 1
+STATUS = {0: "LLA_OK", 1: "LLA_ERR_INVALID_ARGUMENT", 2: "LLA_ERR_UNSUPPORTED_SHAPE",
+          3: "LLA_ERR_WORKSPACE_TOO_SMALL", 4: "LLA_ERR_CUDA", 5: "LLA_ERR_DEVICE_REPORTED"}
+
+# name -> (restype, argtypes); mirrors include/lla.h
+_P, _I, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+SIGNATURES = {
+    "lla_status_string": (ctypes.c_char_p, [_I]),
+    "lla_version": (_I, []),
+    "lla_num_levels": (_I, [_I]),
+    "lla_fwd_workspace_bytes": (_Z, [_I] * 6 + [_I]),
+    "lla_fwd_launches": (_I, [_I] * 8),
+    "lla_fwd": (_I, [_P] * 6 + [_I] * 6 + [_I, _I] + [_P, _Z, _P]),
+    "lla_decode_state_bytes": (_Z, [_I] * 5),
+    "lla_decode_step": (_I, [_P] * 9 + [_I] * 5 + [_I, _P, _P]),
+    "lla_prefill_workspace_bytes": (_Z, [_I] * 3),
+    "lla_prefill_state": (_I, [_P] * 5 + [_I] * 6 + [_I, _P, _Z, _P]),
+}
+
+_lib = None
+
+
+class LLAError(RuntimeError):
+    def __init__(self, name, code):
+        super().__init__(f"{name} returned {STATUS.get(code, code)}")
+        self.code = code
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load liblla.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise ImportError(f"liblla.so not built at {path}: run __graft_entry__.build()")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return LLA_F32
+    if t.dtype == torch.bfloat16:
+        return LLA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(name, code):
+    if code != 0:
+        raise LLAError(name, code)
+
+
+def _need(t, name, dtype=None, ndim=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims")
+
+
+def num_levels(T: int) -> int:
+    return load().lla_num_levels(T)
+
+
+def fwd_workspace_bytes(B, H, T, dk, dv, chunk, in_dtype) -> int:
+    return load().lla_fwd_workspace_bytes(B, H, T, dk, dv, chunk, _dt(torch.empty(0, dtype=in_dtype)))
+
+
+def fwd(q, k, v, g, lam, chunk: int = 64, out_dtype=torch.float32, out=None, workspace=None,
+        stream=None):
+    """lla_fwd on torch tensors: q,k [B,H,T,dk], v [B,H,T,dv] (fp32 or bf16),
+    g [B,H,T] fp32, lam [B,H,T,L] fp32.  Returns out [B,H,T,dv]."""
+    lib = load()
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, n, q.dtype, 4)
+    _need(g, "g", torch.float32, 3)
+    _need(lam, "lam", torch.float32, 4)
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape[:3] != (B, H, T) or g.shape != (B, H, T) or \
+            lam.shape[:3] != (B, H, T) or lam.shape[3] != max(lib.lla_num_levels(T), 1):
+        raise ValueError("inconsistent shapes")
+    if out is None:
+        out = torch.empty((B, H, T, dv), dtype=out_dtype, device=q.device)
+    _need(out, "out", None, 4)
+    in_dt = _dt(q)
+    need = lib.lla_fwd_workspace_bytes(B, H, T, dk, dv, chunk, in_dt)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    rc = lib.lla_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(lam), _ptr(out), B, H, T, dk, dv,
+                     chunk, in_dt, _dt(out), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("lla_fwd", rc)
+    return out
+
+
+def decode_state_bytes(B, H, dk, dv, Ls) -> int:
+    return load().lla_decode_state_bytes(B, H, dk, dv, Ls)
+
+
+def decode_step(state, logdecay, q, k, v, g, lam, pos, out=None, device_error=None, stream=None):
+    """lla_decode_step: state [B,H,Ls,dk,dv] fp32 and logdecay [B,H,Ls] fp32
+    updated in place; q,k [B,H,dk], v [B,H,dv]; g [B,H]; lam [B,H,Ls+1];
+    pos [B] int64 (device).  Returns out [B,H,dv] fp32."""
+    lib = load()
+    _need(state, "state", torch.float32, 5)
+    _need(logdecay, "logdecay", torch.float32, 3)
+    _need(q, "q", None, 3)
+    _need(k, "k", q.dtype, 3)
+    _need(v, "v", q.dtype, 3)
+    _need(g, "g", torch.float32, 2)
+    _need(lam, "lam", torch.float32, 3)
+    _need(pos, "pos", torch.int64, 1)
+    B, H, Ls, dk, dv = state.shape
+    if q.shape != (B, H, dk) or k.shape != (B, H, dk) or v.shape != (B, H, dv) or \
+            g.shape != (B, H) or lam.shape != (B, H, Ls + 1) or pos.shape != (B,) or \
+            logdecay.shape != (B, H, Ls):
+        raise ValueError("inconsistent shapes")
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=torch.float32, device=q.device)
+    rc = lib.lla_decode_step(_ptr(state), _ptr(logdecay), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                             _ptr(lam), _ptr(out), _ptr(pos), B, H, dk, dv, Ls, _dt(q),
+                             _ptr(device_error), _stream(stream))
+    _check("lla_decode_step", rc)
+    return out
+
+
+def prefill_state(k, v, g, Ls: int, state=None, logdecay=None, workspace=None, stream=None):
+    """lla_prefill_state: decode state after the prefix k,v [B,H,T,d], g [B,H,T]."""
+    lib = load()
+    _need(k, "k", None, 4)
+    _need(v, "v", k.dtype, 4)
+    _need(g, "g", torch.float32, 3)
+    B, H, T, dk = k.shape
+    dv = v.shape[-1]
+    if state is None:
+        state = torch.empty((B, H, Ls, dk, dv), dtype=torch.float32, device=k.device)
+    if logdecay is None:
+        logdecay = torch.empty((B, H, Ls), dtype=torch.float32, device=k.device)
+    need = lib.lla_prefill_workspace_bytes(B, H, T)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=k.device)
+    rc = lib.lla_prefill_state(_ptr(k), _ptr(v), _ptr(g), _ptr(state), _ptr(logdecay), B, H, T,
+                               dk, dv, Ls, _dt(k), _ptr(workspace), workspace.numel(),
+                               _stream(stream))
+    _check("lla_prefill_state", rc)
+    return state, logdecay

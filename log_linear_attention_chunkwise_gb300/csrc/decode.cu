@@ -1,0 +1,307 @@
+// Recurrent decode step and prefill -> decode state hand-off.
+// Page "Log-Linear Attention" (gist.science 2506.04761), technical summary
+// §2.3: decoding is recurrent, each step touching O(log T) level states;
+// §2.2: one state per Fenwick bucket of the prefix [0, t).
+//
+// State of one (batch, head): S[Ls][dk][dv] fp32 (slot i = level i+1) and a
+// log-decay D[Ls]; the true level state is exp(D_i) * S_i.  Slot i is live at
+// token index t iff bit i of t is set.  Keeping the decay as a scalar per slot
+// means a step reads the popcount(t) live slots once and writes one slot,
+// instead of rescaling every live slot in memory.
+#include "decode.cuh"
+
+namespace lla {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kMaxLs = 40;
+
+// One CTA per (head, sequence) owns all dv columns, so the slot log-decays are
+// read and rewritten by a single CTA.  Thread layout: cg = column group of 4
+// (float4), rg = row group; a thread owns rows rg, rg+R, ... of its 4 columns
+// in every live slot.
+template <typename Tin, int DV, int NT>
+__global__ void __launch_bounds__(NT)
+decode_step_kernel(float *__restrict__ S, float *__restrict__ D, const Tin *__restrict__ q,
+                   const Tin *__restrict__ k, const Tin *__restrict__ v,
+                   const float *__restrict__ g, const float *__restrict__ lam,
+                   float *__restrict__ out, const int64_t *__restrict__ pos, int H, int dk,
+                   int Ls, int32_t *__restrict__ err)
+{
+    constexpr int dv = DV;
+    constexpr int NC4 = DV / 4;            // column groups
+    constexpr int R = NT / NC4;            // row groups
+    constexpr int RPT = (128 + R - 1) / R; // rows per thread (dk <= 128)
+    __shared__ float qs[128], kss[128], vs[DV];
+    __shared__ float wl[kMaxLs], el[kMaxLs], dnew[kMaxLs];
+    __shared__ float red[R][DV];
+    __shared__ float qk_sh;
+
+    const int h = blockIdx.x, b = blockIdx.y;
+    const long long bh = (long long)b * H + h;
+    const int64_t t = pos[b];
+    if (t < 0 || bit_length_u64((uint64_t)t + 1) > Ls) {
+        if (threadIdx.x == 0 && err != nullptr) *err = 1 + b;
+        return;
+    }
+    const int tid = threadIdx.x;
+    for (int r = tid; r < dk; r += NT) {
+        qs[r] = to_f32(q[bh * dk + r]);
+        kss[r] = to_f32(k[bh * dk + r]);
+    }
+    for (int c = tid; c < dv; c += NT) vs[c] = to_f32(v[bh * dv + c]);
+    const float gg = g[bh];
+    if (tid < Ls) {
+        const bool live = (t >> tid) & 1;
+        const float dn = D[bh * Ls + tid] + (live ? gg : 0.f);
+        dnew[tid] = dn;
+        const float e = live ? expf(dn) : 0.f;
+        el[tid] = e;
+        wl[tid] = live ? lam[bh * (Ls + 1) + tid + 1] * e : 0.f;
+    }
+    __syncthreads();
+    if (tid < 32) {
+        float p = 0.f;
+        for (int r = tid; r < dk; r += 32) p = fmaf(qs[r], kss[r], p);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
+        if (tid == 0) qk_sh = p;
+    }
+
+    const int m = ctz_u64((uint64_t)t + 1);
+    const int cg = tid % NC4, rg = tid / NC4;
+    const int col = cg * 4;
+    constexpr int ncol4 = DV / 4;
+    float4 mrg[RPT];
+#pragma unroll
+    for (int i = 0; i < RPT; i++) mrg[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+
+    for (int l = 0; l < Ls; l++) {
+        if (!((t >> l) & 1)) continue;
+        const float w = wl[l], e = el[l];
+        const bool merge = l < m;
+        const float4 *Sl = reinterpret_cast<const float4 *>(S + ((bh * Ls + l) * (long long)dk) * dv);
+        float4 sv[RPT];
+#pragma unroll
+        for (int i = 0; i < RPT; i++) {
+            const int r = rg + R * i;
+            sv[i] = (r < dk) ? __ldcs(Sl + (long long)r * ncol4 + col / 4)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < RPT; i++) {
+            const int r = rg + R * i;
+            const float qw = (r < dk) ? qs[r] * w : 0.f;
+            acc.x = fmaf(qw, sv[i].x, acc.x);
+            acc.y = fmaf(qw, sv[i].y, acc.y);
+            acc.z = fmaf(qw, sv[i].z, acc.z);
+            acc.w = fmaf(qw, sv[i].w, acc.w);
+            if (merge) {
+                mrg[i].x = fmaf(e, sv[i].x, mrg[i].x);
+                mrg[i].y = fmaf(e, sv[i].y, mrg[i].y);
+                mrg[i].z = fmaf(e, sv[i].z, mrg[i].z);
+                mrg[i].w = fmaf(e, sv[i].w, mrg[i].w);
+            }
+        }
+    }
+    red[rg][col + 0] = acc.x;
+    red[rg][col + 1] = acc.y;
+    red[rg][col + 2] = acc.z;
+    red[rg][col + 3] = acc.w;
+    // the new slot m (level m+1) is dead at t, so no thread of this step reads it
+    {
+        float4 *Sm = reinterpret_cast<float4 *>(S + ((bh * Ls + m) * (long long)dk) * dv);
+        const float4 vv = make_float4(vs[col], vs[col + 1], vs[col + 2], vs[col + 3]);
+#pragma unroll
+        for (int i = 0; i < RPT; i++) {
+            const int r = rg + R * i;
+            if (r < dk) {
+                const float kr = kss[r];
+                float4 o;
+                o.x = fmaf(kr, vv.x, mrg[i].x);
+                o.y = fmaf(kr, vv.y, mrg[i].y);
+                o.z = fmaf(kr, vv.z, mrg[i].z);
+                o.w = fmaf(kr, vv.w, mrg[i].w);
+                __stcs(Sm + (long long)r * ncol4 + col / 4, o);
+            }
+        }
+    }
+    __syncthreads();
+    for (int c = tid; c < DV; c += NT) {
+        float o = 0.f;
+#pragma unroll 4
+        for (int r = 0; r < R; r++) o += red[r][c];
+        out[bh * dv + c] = o + lam[bh * (Ls + 1)] * qk_sh * vs[c];
+    }
+    if (tid < Ls) D[bh * Ls + tid] = (tid == m) ? 0.f : dnew[tid];
+}
+
+// tail[bh][s] = sum_{r=s+1}^{T-1} g[bh][r] (accumulated in fp64, stored fp32).
+__global__ void __launch_bounds__(kThreads)
+prefill_tail_kernel(const float *__restrict__ g, float *__restrict__ tail, int T)
+{
+    __shared__ double part[kThreads];
+    const long long bh = blockIdx.x;
+    const float *gb = g + bh * (long long)T;
+    float *tb = tail + bh * (long long)T;
+    const int per = (T + kThreads - 1) / kThreads;
+    const int lo = min(T, (int)threadIdx.x * per), hi = min(T, lo + per);
+    double s = 0.0;
+    for (int r = lo; r < hi; r++) s += (double)gb[r];
+    part[threadIdx.x] = s;
+    __syncthreads();
+    if (threadIdx.x == 0) {  // exclusive suffix sums of the partials
+        double run = 0.0;
+        for (int u = kThreads - 1; u >= 0; u--) {
+            double x = part[u];
+            part[u] = run;
+            run += x;
+        }
+    }
+    __syncthreads();
+    double run = part[threadIdx.x];  // sum of g over [hi, T)
+    for (int r = hi - 1; r >= lo; r--) {
+        tb[r] = (float)run;
+        run += (double)gb[r];
+    }
+}
+
+constexpr int kSeg = 2048;  // tokens per CTA of the bucket kernel
+constexpr int kSub = 32;
+
+struct BucketTable {
+    long long start[kMaxLs];
+    long long len[kMaxLs];
+    int seg_begin[kMaxLs + 1];
+    int slot[kMaxLs];
+    int n;
+};
+
+template <typename Tin>
+__global__ void __launch_bounds__(kThreads)
+prefill_bucket_kernel(const Tin *__restrict__ k, const Tin *__restrict__ v,
+                      const float *__restrict__ tail, float *__restrict__ S, BucketTable tab,
+                      int T, int dk, int dv, int Ls)
+{
+    __shared__ float ks[kSub * 128];
+    __shared__ float vs[kSub * 128];
+    const long long bh = blockIdx.y;
+    const int sid = blockIdx.x;
+    int li = 0;
+    while (li + 1 < tab.n && tab.seg_begin[li + 1] <= sid) li++;
+    const long long s_lo = tab.start[li] + (long long)(sid - tab.seg_begin[li]) * kSeg;
+    const long long s_hi = min(s_lo + kSeg, tab.start[li] + tab.len[li]);
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const int RB = dk / 16, CB = dv / 16;
+    float acc[8][8];
+#pragma unroll
+    for (int a = 0; a < 8; a++)
+#pragma unroll
+        for (int b = 0; b < 8; b++) acc[a][b] = 0.f;
+    const Tin *kb = k + bh * (long long)T * dk;
+    const Tin *vb = v + bh * (long long)T * dv;
+    const float *tb = tail + bh * (long long)T;
+    for (long long s0 = s_lo; s0 < s_hi; s0 += kSub) {
+        const int ns = (int)min((long long)kSub, s_hi - s0);
+        __syncthreads();
+        for (int e = threadIdx.x; e < kSub * dk; e += kThreads) {
+            int s = e / dk, r = e % dk;
+            ks[e] = (s < ns) ? to_f32(kb[(s0 + s) * dk + r]) : 0.f;
+        }
+        for (int e = threadIdx.x; e < kSub * dv; e += kThreads) {
+            int s = e / dv, c = e % dv;
+            vs[e] = (s < ns) ? expf(tb[s0 + s]) * to_f32(vb[(s0 + s) * dv + c]) : 0.f;
+        }
+        __syncthreads();
+        for (int s = 0; s < ns; s++) {
+            float kr[8], vc[8];
+#pragma unroll
+            for (int a = 0; a < 8; a++) kr[a] = (a < RB) ? ks[s * dk + ty + 16 * a] : 0.f;
+#pragma unroll
+            for (int b = 0; b < 8; b++) vc[b] = (b < CB) ? vs[s * dv + tx + 16 * b] : 0.f;
+#pragma unroll
+            for (int a = 0; a < 8; a++)
+#pragma unroll
+                for (int b = 0; b < 8; b++) acc[a][b] = fmaf(kr[a], vc[b], acc[a][b]);
+        }
+    }
+    float *Sl = S + (bh * Ls + tab.slot[li]) * (long long)dk * dv;
+#pragma unroll
+    for (int a = 0; a < 8; a++)
+#pragma unroll
+        for (int b = 0; b < 8; b++)
+            if (a < RB && b < CB) atomicAdd(Sl + (ty + 16 * a) * dv + tx + 16 * b, acc[a][b]);
+}
+
+template <typename Tin, int DV, int NT>
+void launch_decode_dv(const DecodeArgs &A)
+{
+    decode_step_kernel<Tin, DV, NT><<<dim3(A.H, A.B), NT, 0, (cudaStream_t)A.stream>>>(
+        A.S, A.D, (const Tin *)A.q, (const Tin *)A.k, (const Tin *)A.v, A.g, A.lam, A.out,
+        A.pos, A.H, A.dk, A.Ls, A.err);
+}
+
+template <typename Tin>
+cudaError_t launch_decode(const DecodeArgs &A)
+{
+    switch (A.dv) {
+    case 16: launch_decode_dv<Tin, 16, 256>(A); break;
+    case 32: launch_decode_dv<Tin, 32, 256>(A); break;
+    case 64: launch_decode_dv<Tin, 64, 256>(A); break;
+    default: launch_decode_dv<Tin, 128, 512>(A); break;
+    }
+    return cudaPeekAtLastError();
+}
+
+template <typename Tin>
+cudaError_t launch_prefill(const PrefillArgs &A)
+{
+    cudaStream_t st = (cudaStream_t)A.stream;
+    const long long BH = (long long)A.B * A.H;
+    cudaError_t err = cudaMemsetAsync(A.S, 0, sizeof(float) * BH * A.Ls * A.dk * A.dv, st);
+    if (err != cudaSuccess) return err;
+    err = cudaMemsetAsync(A.D, 0, sizeof(float) * BH * A.Ls, st);
+    if (err != cudaSuccess) return err;
+    if (A.T == 0) return cudaSuccess;
+    BucketTable tab{};
+    int nseg = 0;
+    for (int l = 1; l <= A.Ls && l <= 40; l++) {
+        if (!(((long long)A.T >> (l - 1)) & 1)) continue;
+        const long long start = ((long long)A.T >> l) << l;
+        const long long len = 1LL << (l - 1);
+        tab.start[tab.n] = start;
+        tab.len[tab.n] = len;
+        tab.slot[tab.n] = l - 1;
+        tab.seg_begin[tab.n] = nseg;
+        nseg += (int)((len + kSeg - 1) / kSeg);
+        tab.n++;
+    }
+    tab.seg_begin[tab.n] = nseg;
+    float *tail = (float *)A.workspace;
+    prefill_tail_kernel<<<(unsigned)BH, kThreads, 0, st>>>(A.g, tail, A.T);
+    prefill_bucket_kernel<Tin><<<dim3(nseg, (unsigned)BH), kThreads, 0, st>>>(
+        (const Tin *)A.k, (const Tin *)A.v, tail, A.S, tab, A.T, A.dk, A.dv, A.Ls);
+    return cudaPeekAtLastError();
+}
+
+}  // namespace
+
+cudaError_t decode_step(const DecodeArgs &A)
+{
+    if (A.in_dt == LLA_F32) return launch_decode<float>(A);
+    return launch_decode<__nv_bfloat16>(A);
+}
+
+size_t prefill_workspace_bytes(int B, int H, int T)
+{
+    return align_up((size_t)B * H * (size_t)(T > 0 ? T : 1) * sizeof(float), 256);
+}
+
+cudaError_t prefill_state(const PrefillArgs &A)
+{
+    if (A.in_dt == LLA_F32) return launch_prefill<float>(A);
+    return launch_prefill<__nv_bfloat16>(A);
+}
+
+}  // namespace lla

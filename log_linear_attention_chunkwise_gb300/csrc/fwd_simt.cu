@@ -1,0 +1,355 @@
+// Chunked forward on CUDA cores (fp32 arithmetic): every supported shape and
+// the fp32-input path.  Four launches per call:
+//   1. chunk states  H_i = K_i^T diag(exp(Gam_i - gamma)) V_i, gate totals Gam_i
+//   2. chunk-gate prefix P_j = Gam_0 + ... + Gam_{j-1} (fp64)
+//   3. chunk-level Fenwick scan of the states into tree nodes
+//   4. per chunk: masked intra-chunk product + lambda-weighted node read-out
+// Page "Log-Linear Attention" (gist.science 2506.04761), technical summary:
+// §2.2 (Fenwick buckets, per-level states, output equation) and §2.3 (the
+// chunked, matmul-rich parallel form).
+//
+// Notation: chunk i holds tokens [iC, iC+C), C = 2^c.  gamma_a is the
+// inclusive gate sum inside the chunk, Gam_i its value at the chunk's last
+// token, P_i = G_{iC-1} the gate sum of all earlier chunks.  A key s in chunk
+// j < i has level c + bit_length(i XOR j) for every query of chunk i, so the
+// earlier chunks split into the chunk-level Fenwick buckets of [0, i): for
+// each set bit m of i, the bucket [i' - 2^m, i') with i' = i with bits below
+// m cleared.  Node_j (j >= 1) holds the chunks [j - lowbit(j), j) decayed to
+// the last token of chunk j-1:
+//   Node_j = H_{j-1} + sum_{k < ctz(j)} exp(P_j - P_{j-2^k}) Node_{j-2^k}.
+// Query row a of chunk i adds, for the bucket ending at j (m = ctz(j)),
+//   lambda_a[c+1+m] * exp(gamma_a + P_i - P_j) * q_a^T Node_j.
+#include "fwd_simt.cuh"
+
+namespace lla {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kSub = 32;  // tokens staged per step of the state kernel
+
+// Inclusive running sum of C <= 128 gates, by warp 0; src may be global.
+__device__ __forceinline__ void chunk_cumsum_warp0(const float *src, float *dst, int C)
+{
+    if (threadIdx.x >= 32) return;
+    const int lane = threadIdx.x;
+    const int per = (C + 31) / 32;
+    float loc[4];
+    float run = 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+        int idx = lane * per + u;
+        float x = (u < per && idx < C) ? src[idx] : 0.f;
+        run += x;
+        loc[u] = run;
+    }
+    float incl = run;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        float y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    float excl = incl - run;
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+        int idx = lane * per + u;
+        if (u < per && idx < C) dst[idx] = excl + loc[u];
+    }
+}
+
+template <typename Tin>
+__global__ void __launch_bounds__(kThreads)
+simt_chunk_state_kernel(const Tin *__restrict__ k, const Tin *__restrict__ v,
+                        const float *__restrict__ g, float *__restrict__ gam,
+                        float *__restrict__ nodes, int T, int dk, int dv, int C, int N)
+{
+    extern __shared__ float sm[];
+    float *gl = sm;                // [128] gamma
+    float *ks = gl + 128;          // [kSub][dk]
+    float *vs = ks + kSub * dk;    // [kSub][dv], rows scaled by exp(Gam - gamma)
+    const int i = blockIdx.x;
+    const long long bh = blockIdx.y;
+    const long long tok0 = bh * (long long)T + (long long)i * C;
+
+    chunk_cumsum_warp0(g + tok0, gl, C);
+    __syncthreads();
+    const float Gam = gl[C - 1];
+    if (threadIdx.x == 0) gam[bh * N + i] = Gam;
+    if (i == N - 1) return;  // the last chunk's state starts no node
+
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const int RB = dk / 16, CB = dv / 16;
+    float acc[8][8];
+#pragma unroll
+    for (int a = 0; a < 8; a++)
+#pragma unroll
+        for (int b = 0; b < 8; b++) acc[a][b] = 0.f;
+
+    for (int s0 = 0; s0 < C; s0 += kSub) {
+        const int ns = min(kSub, C - s0);
+        for (int e = threadIdx.x; e < kSub * dk; e += kThreads) {
+            int s = e / dk, r = e % dk;
+            ks[e] = (s < ns) ? to_f32(k[(tok0 + s0 + s) * dk + r]) : 0.f;
+        }
+        for (int e = threadIdx.x; e < kSub * dv; e += kThreads) {
+            int s = e / dv, cc = e % dv;
+            vs[e] = (s < ns) ? expf(Gam - gl[s0 + s]) * to_f32(v[(tok0 + s0 + s) * dv + cc]) : 0.f;
+        }
+        __syncthreads();
+        for (int s = 0; s < ns; s++) {
+            float kr[8], vc[8];
+#pragma unroll
+            for (int a = 0; a < 8; a++) kr[a] = (a < RB) ? ks[s * dk + ty + 16 * a] : 0.f;
+#pragma unroll
+            for (int b = 0; b < 8; b++) vc[b] = (b < CB) ? vs[s * dv + tx + 16 * b] : 0.f;
+#pragma unroll
+            for (int a = 0; a < 8; a++)
+#pragma unroll
+                for (int b = 0; b < 8; b++) acc[a][b] = fmaf(kr[a], vc[b], acc[a][b]);
+        }
+        __syncthreads();
+    }
+    float *H = nodes + (bh * N + (i + 1)) * (long long)dk * dv;
+#pragma unroll
+    for (int a = 0; a < 8; a++)
+#pragma unroll
+        for (int b = 0; b < 8; b++)
+            if (a < RB && b < CB) H[(ty + 16 * a) * dv + tx + 16 * b] = acc[a][b];
+}
+
+// P[bh][j] = sum_{i<j} gam[bh][i] in fp64, j = 0..N.
+__global__ void __launch_bounds__(kThreads)
+simt_gate_prefix_kernel(const float *__restrict__ gam, double *__restrict__ P, int N)
+{
+    __shared__ double part[kThreads];
+    const long long bh = blockIdx.x;
+    const int per = (N + kThreads - 1) / kThreads;
+    const int lo = min(N, (int)threadIdx.x * per), hi = min(N, lo + per);
+    double s = 0.0;
+    for (int j = lo; j < hi; j++) s += (double)gam[bh * N + j];
+    part[threadIdx.x] = s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double run = 0.0;
+        for (int u = 0; u < kThreads; u++) {
+            double x = part[u];
+            part[u] = run;
+            run += x;
+        }
+    }
+    __syncthreads();
+    double run = part[threadIdx.x];
+    double *Pb = P + bh * (long long)(N + 1);
+    for (int j = lo; j < hi; j++) {
+        Pb[j] = run;
+        run += (double)gam[bh * N + j];
+    }
+    if (threadIdx.x == kThreads - 1) Pb[N] = run;
+}
+
+// In place: slot j (1..N-1) holds H_{j-1} on entry and Node_j on exit.
+// One thread per state element; the open node of each level is kept in
+// registers (stack[z] = the latest node with ctz == z).
+constexpr int kMaxZ = 24;
+__global__ void __launch_bounds__(kThreads)
+simt_fenwick_scan_kernel(const double *__restrict__ P, float *__restrict__ nodes, int N, int E)
+{
+    const long long bh = blockIdx.y;
+    const int e = blockIdx.x * kThreads + threadIdx.x;
+    if (e >= E) return;
+    const double *Pb = P + bh * (long long)(N + 1);
+    float *base = nodes + bh * (long long)N * E + e;
+    float stack[kMaxZ];
+#pragma unroll
+    for (int z = 0; z < kMaxZ; z++) stack[z] = 0.f;
+    for (int j = 1; j < N; j++) {
+        const int z = ctz_u32((uint32_t)j);
+        float val = base[(long long)j * E];
+        const double Pj = Pb[j];
+#pragma unroll
+        for (int kk = 0; kk < kMaxZ; kk++)
+            if (kk < z) val = fmaf(expf((float)(Pj - Pb[j - (1 << kk)])), stack[kk], val);
+#pragma unroll
+        for (int kk = 0; kk < kMaxZ; kk++)
+            if (kk == z) stack[kk] = val;
+        base[(long long)j * E] = val;
+    }
+}
+
+template <typename Tin, typename Tout>
+__global__ void __launch_bounds__(kThreads)
+simt_chunk_output_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
+                         const Tin *__restrict__ v, const float *__restrict__ g,
+                         const float *__restrict__ lam, const double *__restrict__ P,
+                         const float *__restrict__ nodes, Tout *__restrict__ out,
+                         int T, int dk, int dv, int C, int cbits, int N, int L)
+{
+    extern __shared__ float sm[];
+    const int ldkv = (dk > dv ? dk : dv) + 1;
+    float *gl = sm;                    // [128]
+    float *Qs = gl + 128;              // [C][dk]
+    float *KVs = Qs + C * dk;          // [C][ldkv]: K rows, then V rows
+    float *Ps = KVs + C * ldkv;        // [C][C] masked scores
+    float *Nt = Ps + C * C;            // [16][dv] node rows
+    float *Ls = Nt + 16 * dv;          // [C][L] lambda rows
+    const int i = blockIdx.x;
+    const long long bh = blockIdx.y;
+    const long long tok0 = bh * (long long)T + (long long)i * C;
+
+    chunk_cumsum_warp0(g + tok0, gl, C);
+    for (int e = threadIdx.x; e < C * dk; e += kThreads) {
+        Qs[e] = to_f32(q[tok0 * dk + e]);
+        int s = e / dk, r = e % dk;
+        KVs[s * ldkv + r] = to_f32(k[tok0 * dk + e]);
+    }
+    for (int e = threadIdx.x; e < C * L; e += kThreads) Ls[e] = lam[tok0 * L + e];
+    __syncthreads();
+
+    // masked scores: M[a][b] = lambda_a[bit_length(a^b)] exp(gamma_a - gamma_b), b <= a
+    for (int e = threadIdx.x; e < C * C; e += kThreads) {
+        int a = e / C, b = e % C;
+        float s = 0.f;
+        if (b <= a) {
+            float d = 0.f;
+            for (int r = 0; r < dk; r++) d = fmaf(Qs[a * dk + r], KVs[b * ldkv + r], d);
+            s = d * Ls[a * L + bit_length_u32((uint32_t)(a ^ b))] * expf(gl[a] - gl[b]);
+        }
+        Ps[e] = s;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < C * dv; e += kThreads) {
+        int s = e / dv, cc = e % dv;
+        KVs[s * ldkv + cc] = to_f32(v[tok0 * dv + e]);
+    }
+    __syncthreads();
+
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const int RB = C / 16, CB = dv / 16;
+    float acc[8][8];
+#pragma unroll
+    for (int a = 0; a < 8; a++)
+#pragma unroll
+        for (int b = 0; b < 8; b++) acc[a][b] = 0.f;
+    for (int b = 0; b < C; b++) {
+        float vc[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; jj++) vc[jj] = (jj < CB) ? KVs[b * ldkv + tx + 16 * jj] : 0.f;
+#pragma unroll
+        for (int a = 0; a < 8; a++) {
+            float p = (a < RB) ? Ps[(ty + 16 * a) * C + b] : 0.f;
+#pragma unroll
+            for (int jj = 0; jj < 8; jj++) acc[a][jj] = fmaf(p, vc[jj], acc[a][jj]);
+        }
+    }
+
+    // read-out over the chunk-level Fenwick path of [0, i)
+    const double *Pb = P + bh * (long long)(N + 1);
+    for (int j = i; j > 0; j -= (j & -j)) {
+        const int m = ctz_u32((uint32_t)j);
+        const int lev = cbits + 1 + m;
+        const float dP = (float)(Pb[i] - Pb[j]);
+        const float *Nd = nodes + (bh * N + j) * (long long)dk * dv;
+        float u[8][8];
+#pragma unroll
+        for (int a = 0; a < 8; a++)
+#pragma unroll
+            for (int b = 0; b < 8; b++) u[a][b] = 0.f;
+        for (int r0 = 0; r0 < dk; r0 += 16) {
+            __syncthreads();
+            for (int e = threadIdx.x; e < 16 * dv; e += kThreads) Nt[e] = Nd[r0 * dv + e];
+            __syncthreads();
+            for (int rr = 0; rr < 16; rr++) {
+                float nc[8];
+#pragma unroll
+                for (int jj = 0; jj < 8; jj++) nc[jj] = (jj < CB) ? Nt[rr * dv + tx + 16 * jj] : 0.f;
+#pragma unroll
+                for (int a = 0; a < 8; a++) {
+                    float qv = (a < RB) ? Qs[(ty + 16 * a) * dk + r0 + rr] : 0.f;
+#pragma unroll
+                    for (int jj = 0; jj < 8; jj++) u[a][jj] = fmaf(qv, nc[jj], u[a][jj]);
+                }
+            }
+        }
+#pragma unroll
+        for (int a = 0; a < 8; a++) {
+            if (a < RB) {
+                int row = ty + 16 * a;
+                float w = Ls[row * L + lev] * expf(gl[row] + dP);
+#pragma unroll
+                for (int jj = 0; jj < 8; jj++) acc[a][jj] = fmaf(w, u[a][jj], acc[a][jj]);
+            }
+        }
+    }
+#pragma unroll
+    for (int a = 0; a < 8; a++)
+#pragma unroll
+        for (int jj = 0; jj < 8; jj++)
+            if (a < RB && jj < CB)
+                out[(tok0 + ty + 16 * a) * dv + tx + 16 * jj] = from_f32<Tout>(acc[a][jj]);
+}
+
+template <typename Tin, typename Tout>
+cudaError_t launch_all(const SimtFwdArgs &A)
+{
+    const int BH = A.B * A.H;
+    const int N = A.T / A.C;
+    cudaStream_t st = (cudaStream_t)A.stream;
+    char *ws = (char *)A.workspace;
+    float *gam = (float *)ws;
+    double *P = (double *)(ws + simt_ws_offset_P(A));
+    float *nodes = (float *)(ws + simt_ws_offset_nodes(A));
+
+    size_t sm1 = sizeof(float) * (128 + kSub * A.dk + kSub * A.dv);
+    simt_chunk_state_kernel<Tin><<<dim3(N, BH), kThreads, sm1, st>>>(
+        (const Tin *)A.k, (const Tin *)A.v, A.g, gam, nodes, A.T, A.dk, A.dv, A.C, N);
+    simt_gate_prefix_kernel<<<BH, kThreads, 0, st>>>(gam, P, N);
+    const int E = A.dk * A.dv;
+    if (N > 1)
+        simt_fenwick_scan_kernel<<<dim3((E + kThreads - 1) / kThreads, BH), kThreads, 0, st>>>(
+            P, nodes, N, E);
+    const int ldkv = (A.dk > A.dv ? A.dk : A.dv) + 1;
+    size_t sm4 = sizeof(float) * (128 + A.C * A.dk + A.C * ldkv + A.C * A.C + 16 * A.dv + A.C * A.L);
+    auto kern = simt_chunk_output_kernel<Tin, Tout>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm4);
+    if (err != cudaSuccess) return err;
+    int cbits = ctz_u32((uint32_t)A.C);
+    kern<<<dim3(N, BH), kThreads, sm4, st>>>(
+        (const Tin *)A.q, (const Tin *)A.k, (const Tin *)A.v, A.g, A.lam, P, nodes,
+        (Tout *)A.out, A.T, A.dk, A.dv, A.C, cbits, N, A.L);
+    return cudaPeekAtLastError();
+}
+
+}  // namespace
+
+size_t simt_ws_offset_P(const SimtFwdArgs &A)
+{
+    const size_t BH = (size_t)A.B * A.H, N = (size_t)(A.T / A.C);
+    return align_up(BH * N * sizeof(float), 256);
+}
+
+size_t simt_ws_offset_nodes(const SimtFwdArgs &A)
+{
+    const size_t BH = (size_t)A.B * A.H, N = (size_t)(A.T / A.C);
+    return simt_ws_offset_P(A) + align_up(BH * (N + 1) * sizeof(double), 256);
+}
+
+size_t simt_workspace_bytes(const SimtFwdArgs &A)
+{
+    const size_t BH = (size_t)A.B * A.H, N = (size_t)(A.T / A.C);
+    return simt_ws_offset_nodes(A) + align_up(BH * N * (size_t)A.dk * A.dv * sizeof(float), 256);
+}
+
+size_t simt_max_smem_bytes(const SimtFwdArgs &A)
+{
+    const int ldkv = (A.dk > A.dv ? A.dk : A.dv) + 1;
+    return sizeof(float) * (128 + (size_t)A.C * A.dk + (size_t)A.C * ldkv + (size_t)A.C * A.C +
+                            16 * (size_t)A.dv + (size_t)A.C * A.L);
+}
+
+cudaError_t simt_fwd(const SimtFwdArgs &A)
+{
+    if (A.in_dt == LLA_F32 && A.out_dt == LLA_F32) return launch_all<float, float>(A);
+    if (A.in_dt == LLA_BF16 && A.out_dt == LLA_F32) return launch_all<__nv_bfloat16, float>(A);
+    return launch_all<__nv_bfloat16, __nv_bfloat16>(A);
+}
+
+}  // namespace lla

@@ -1,0 +1,26 @@
+// Internal interface of the CUDA-core forward (fp32 arithmetic).
+#pragma once
+
+#include <stddef.h>
+
+#include "lla_common.cuh"
+
+namespace lla {
+
+struct SimtFwdArgs {
+    const void *q, *k, *v;
+    const float *g, *lam;
+    void *out;
+    int B, H, T, dk, dv, C, L;
+    lla_dtype in_dt, out_dt;
+    void *workspace;
+    void *stream;
+};
+
+size_t simt_ws_offset_P(const SimtFwdArgs &A);
+size_t simt_ws_offset_nodes(const SimtFwdArgs &A);
+size_t simt_workspace_bytes(const SimtFwdArgs &A);
+size_t simt_max_smem_bytes(const SimtFwdArgs &A);
+cudaError_t simt_fwd(const SimtFwdArgs &A);
+
+}  // namespace lla

@@ -1,0 +1,166 @@
+// C ABI of liblla.so: argument validation and dispatch to the kernels.
+// Declarations, layouts and error behaviour: include/lla.h.
+#include <stdint.h>
+
+#include "decode.cuh"
+#include "fwd_simt.cuh"
+#include "lla_common.cuh"
+
+using namespace lla;
+
+namespace {
+
+constexpr long long kMaxGridY = 65535;
+
+bool is_dim(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+bool is_chunk(int c) { return c == 16 || c == 32 || c == 64 || c == 128; }
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+lla_status fwd_shape_status(int B, int H, int T, int dk, int dv, int chunk, lla_dtype in_dt)
+{
+    if (B < 0 || H < 0 || T < 0) return LLA_ERR_INVALID_ARGUMENT;
+    if (in_dt != LLA_F32 && in_dt != LLA_BF16) return LLA_ERR_INVALID_ARGUMENT;
+    if (!is_chunk(chunk) || !is_dim(dk) || !is_dim(dv)) return LLA_ERR_UNSUPPORTED_SHAPE;
+    if (T % chunk != 0 || T > (1 << 24)) return LLA_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)B * H > kMaxGridY) return LLA_ERR_UNSUPPORTED_SHAPE;
+    return LLA_OK;
+}
+
+SimtFwdArgs simt_args(const void *q, const void *k, const void *v, const float *g,
+                      const float *lambda, void *out, int B, int H, int T, int dk, int dv,
+                      int chunk, lla_dtype in_dt, lla_dtype out_dt, void *ws, void *stream)
+{
+    SimtFwdArgs A;
+    A.q = q; A.k = k; A.v = v; A.g = g; A.lam = lambda; A.out = out;
+    A.B = B; A.H = H; A.T = T; A.dk = dk; A.dv = dv; A.C = chunk;
+    A.L = lla_num_levels(T);
+    A.in_dt = in_dt; A.out_dt = out_dt; A.workspace = ws; A.stream = stream;
+    return A;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *lla_status_string(lla_status s)
+{
+    switch (s) {
+    case LLA_OK: return "LLA_OK";
+    case LLA_ERR_INVALID_ARGUMENT: return "LLA_ERR_INVALID_ARGUMENT";
+    case LLA_ERR_UNSUPPORTED_SHAPE: return "LLA_ERR_UNSUPPORTED_SHAPE";
+    case LLA_ERR_WORKSPACE_TOO_SMALL: return "LLA_ERR_WORKSPACE_TOO_SMALL";
+    case LLA_ERR_CUDA: return "LLA_ERR_CUDA";
+    case LLA_ERR_DEVICE_REPORTED: return "LLA_ERR_DEVICE_REPORTED";
+    }
+    return "LLA_UNKNOWN_STATUS";
+}
+
+int lla_version(void) { return 100; }
+
+int lla_num_levels(int T)
+{
+    if (T <= 0) return 0;
+    return 1 + bit_length_u32((uint32_t)(T - 1));
+}
+
+size_t lla_fwd_workspace_bytes(int B, int H, int T, int dk, int dv, int chunk, lla_dtype in_dt)
+{
+    if (fwd_shape_status(B, H, T, dk, dv, chunk, in_dt) != LLA_OK) return 0;
+    if ((long long)B * H * T == 0) return 0;
+    SimtFwdArgs A = simt_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, B, H, T,
+                              dk, dv, chunk, in_dt, LLA_F32, nullptr, nullptr);
+    return simt_workspace_bytes(A);
+}
+
+int lla_fwd_launches(int B, int H, int T, int dk, int dv, int chunk, lla_dtype in_dt,
+                     lla_dtype out_dt)
+{
+    if (fwd_shape_status(B, H, T, dk, dv, chunk, in_dt) != LLA_OK) return 0;
+    if (out_dt != LLA_F32 && out_dt != LLA_BF16) return 0;
+    if (in_dt == LLA_F32 && out_dt != LLA_F32) return 0;
+    if ((long long)B * H * T == 0) return 0;
+    return T / chunk > 1 ? 4 : 3;
+}
+
+lla_status lla_fwd(const void *q, const void *k, const void *v, const float *g,
+                   const float *lambda, void *out, int B, int H, int T, int dk, int dv,
+                   int chunk, lla_dtype in_dt, lla_dtype out_dt, void *workspace,
+                   size_t workspace_bytes, void *stream)
+{
+    lla_status st = fwd_shape_status(B, H, T, dk, dv, chunk, in_dt);
+    if (st != LLA_OK) return st;
+    if (out_dt != LLA_F32 && out_dt != LLA_BF16) return LLA_ERR_INVALID_ARGUMENT;
+    if (in_dt == LLA_F32 && out_dt != LLA_F32) return LLA_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)B * H * T == 0) return LLA_OK;
+    if (!q || !k || !v || !g || !lambda || !out) return LLA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(lambda) ||
+        !aligned16(out))
+        return LLA_ERR_INVALID_ARGUMENT;
+    const size_t need = lla_fwd_workspace_bytes(B, H, T, dk, dv, chunk, in_dt);
+    if (workspace_bytes < need) return LLA_ERR_WORKSPACE_TOO_SMALL;
+    if (need > 0 && (workspace == nullptr || ((uintptr_t)workspace & 255u) != 0))
+        return LLA_ERR_INVALID_ARGUMENT;
+    SimtFwdArgs A = simt_args(q, k, v, g, lambda, out, B, H, T, dk, dv, chunk, in_dt, out_dt,
+                              workspace, stream);
+    if (simt_max_smem_bytes(A) > 227 * 1024) return LLA_ERR_UNSUPPORTED_SHAPE;
+    return simt_fwd(A) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+}
+
+size_t lla_decode_state_bytes(int B, int H, int dk, int dv, int Ls)
+{
+    if (B < 0 || H < 0 || dk < 0 || dv < 0 || Ls < 0) return 0;
+    return (size_t)B * H * Ls * dk * dv * sizeof(float);
+}
+
+lla_status lla_decode_step(float *state_levels, float *state_logdecay, const void *q,
+                           const void *k, const void *v, const float *g, const float *lambda,
+                           float *out, const int64_t *pos, int B, int H, int dk, int dv, int Ls,
+                           lla_dtype in_dt, int32_t *device_error, void *stream)
+{
+    if (B < 0 || H < 0) return LLA_ERR_INVALID_ARGUMENT;
+    if (in_dt != LLA_F32 && in_dt != LLA_BF16) return LLA_ERR_INVALID_ARGUMENT;
+    if (!is_dim(dk) || !is_dim(dv) || Ls < 1 || Ls > 40) return LLA_ERR_UNSUPPORTED_SHAPE;
+    if (B > kMaxGridY || H > (1 << 30)) return LLA_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)B * H == 0) return LLA_OK;
+    if (!state_levels || !state_logdecay || !q || !k || !v || !g || !lambda || !out || !pos)
+        return LLA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(state_levels) || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
+        !aligned16(out))
+        return LLA_ERR_INVALID_ARGUMENT;
+    DecodeArgs A;
+    A.S = state_levels; A.D = state_logdecay; A.q = q; A.k = k; A.v = v; A.g = g;
+    A.lam = lambda; A.out = out; A.pos = pos; A.B = B; A.H = H; A.dk = dk; A.dv = dv;
+    A.Ls = Ls; A.in_dt = in_dt; A.err = device_error; A.stream = stream;
+    return decode_step(A) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+}
+
+size_t lla_prefill_workspace_bytes(int B, int H, int T)
+{
+    if (B < 0 || H < 0 || T < 0) return 0;
+    return prefill_workspace_bytes(B, H, T);
+}
+
+lla_status lla_prefill_state(const void *k, const void *v, const float *g, float *state_levels,
+                             float *state_logdecay, int B, int H, int T, int dk, int dv, int Ls,
+                             lla_dtype in_dt, void *workspace, size_t workspace_bytes,
+                             void *stream)
+{
+    if (B < 0 || H < 0 || T < 0) return LLA_ERR_INVALID_ARGUMENT;
+    if (in_dt != LLA_F32 && in_dt != LLA_BF16) return LLA_ERR_INVALID_ARGUMENT;
+    if (!is_dim(dk) || !is_dim(dv) || Ls < 1 || Ls > 40) return LLA_ERR_UNSUPPORTED_SHAPE;
+    if (T > (1 << 30) || bit_length_u32((uint32_t)T) > Ls) return LLA_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)B * H > kMaxGridY) return LLA_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)B * H == 0) return LLA_OK;
+    if (!state_levels || !state_logdecay) return LLA_ERR_INVALID_ARGUMENT;
+    if (T > 0 && (!k || !v || !g)) return LLA_ERR_INVALID_ARGUMENT;
+    const size_t need = lla_prefill_workspace_bytes(B, H, T);
+    if (workspace_bytes < need) return LLA_ERR_WORKSPACE_TOO_SMALL;
+    if (workspace == nullptr || ((uintptr_t)workspace & 255u) != 0) return LLA_ERR_INVALID_ARGUMENT;
+    PrefillArgs A;
+    A.k = k; A.v = v; A.g = g; A.S = state_levels; A.D = state_logdecay;
+    A.B = B; A.H = H; A.T = T; A.dk = dk; A.dv = dv; A.Ls = Ls; A.in_dt = in_dt;
+    A.workspace = workspace; A.stream = stream;
+    return prefill_state(A) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -10,7 +10,7 @@ and marshals numpy arrays.
 What each function follows (page "Log-Linear Attention", gist.science
 2506.04761, technical summary):
   naive              §2.2 output equation, written as the double sum over keys
-                     with the Mamba-2 gate of §3;
+                     with the Mamba-2 gate of §3 (naive_rows: selected rows);
   fenwick            §2.2 Fenwick buckets + §2.3 recurrent form, per token;
   decode_step        §2.3 recurrent form on a lazily decayed level state;
   state_closed_form  §2.2 bucket states straight from the level definition;
@@ -53,12 +53,13 @@ def _load():
         P = ctypes.c_void_p
         I = ctypes.c_int64
         lib.oracle_naive.argtypes = [P] * 6 + [I] * 6
+        lib.oracle_naive_rows.argtypes = [P] * 7 + [I] * 5
         lib.oracle_fenwick.argtypes = [P] * 6 + [I] * 6 + [P]
         lib.oracle_decode_step.argtypes = [P] * 9 + [I] * 5
         lib.oracle_state_closed_form.argtypes = [P] * 6 + [I] * 6
         lib.oracle_ssd.argtypes = [P] * 5 + [I] * 5
         lib.oracle_level.argtypes = [I, I]
-        for name in ("oracle_naive", "oracle_fenwick", "oracle_decode_step",
+        for name in ("oracle_naive", "oracle_naive_rows", "oracle_fenwick", "oracle_decode_step",
                      "oracle_state_closed_form", "oracle_ssd", "oracle_level",
                      "oracle_num_threads"):
             getattr(lib, name).restype = ctypes.c_int
@@ -103,6 +104,20 @@ def naive(q, k, v, g, lam) -> np.ndarray:
     out = np.zeros((B, H, T, dv), np.float64)
     _check(_load().oracle_naive(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(lam),
                                 _ptr(out), B, H, T, dk, dv, L), "oracle_naive")
+    return out
+
+
+def naive_rows(q, k, v, g, lam, rows) -> np.ndarray:
+    """Rows ``rows`` of the double sum for ONE (batch, head) slice:
+    q,k [T,dk], v [T,dv], g [T], lam [T,L].  Returns [len(rows), dv]."""
+    q, k, v, g, lam = map(_f64, (q, k, v, g, lam))
+    rows = np.ascontiguousarray(np.asarray(rows), dtype=np.int64)
+    T, dk = q.shape
+    dv = v.shape[-1]
+    L = lam.shape[-1]
+    out = np.zeros((len(rows), dv), np.float64)
+    _check(_load().oracle_naive_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(lam), _ptr(rows),
+                                     _ptr(out), len(rows), T, dk, dv, L), "oracle_naive_rows")
     return out
 
 

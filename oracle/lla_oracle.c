@@ -142,6 +142,45 @@ int oracle_naive(const double *q, const double *k, const double *v,
 }
 
 /*
+ * The same double sum for selected rows only: one (batch, head) slice
+ * q [T,dk], k [T,dk], v [T,dv], g [T], lam [T,L]; rows[n] lists token
+ * indices t, out [n,dv] receives o_t.  O(n T (dk+dv)); lets a test check
+ * single outputs of long sequences.
+ */
+int oracle_naive_rows(const double *q, const double *k, const double *v,
+                      const double *g, const double *lam, const int64_t *rows,
+                      double *out, int64_t n, int64_t T, int64_t dk, int64_t dv,
+                      int64_t L)
+{
+    if (T < 0 || dk <= 0 || dv <= 0 || L <= 0 || n < 0)
+        return -1;
+    if (T > 0 && bit_length((uint64_t)(T - 1)) > L - 1)
+        return -2;
+    for (int64_t i = 0; i < n; i++)
+        if (rows[i] < 0 || rows[i] >= T)
+            return -5;
+    double *G = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+    if (!G)
+        return -3;
+    cumsum(g, T, G);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < n; i++) {
+        int64_t t = rows[i];
+        double *o = out + i * dv;
+        for (int64_t j = 0; j < dv; j++)
+            o[j] = 0.0;
+        for (int64_t s = 0; s <= t; s++) {
+            int lev = oracle_level(t, s);
+            double w = lam[t * L + lev] * exp(G[t] - G[s]) * dot(q + t * dk, k + s * dk, dk);
+            for (int64_t j = 0; j < dv; j++)
+                o[j] += w * v[s * dv + j];
+        }
+    }
+    free(G);
+    return 0;
+}
+
+/*
  * Per-token Fenwick recurrence ("Log-Linear Attention" §2.2 buckets, §2.3
  * recurrent decode), with the decay applied eagerly to every live state.
  *

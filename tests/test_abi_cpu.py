@@ -1,0 +1,98 @@
+"""The C-ABI library on a machine without a GPU: it loads, exports every
+symbol include/lla.h declares, answers its host-side queries, and rejects bad
+arguments before enqueueing anything."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from log_linear_attention_chunkwise_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(binding.LIB_PATH):
+        from log_linear_attention_chunkwise_gb300 import build
+        build.build()
+    return binding.load()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "lla.h")).read()
+    return sorted(set(re.findall(r"\b(lla_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_symbols()
+    assert len(names) >= 9
+    for name in names:
+        assert hasattr(lib, name), name
+    assert set(names) == set(binding.SIGNATURES), "binding and header disagree"
+
+
+def test_status_strings_and_version(lib):
+    for code, name in binding.STATUS.items():
+        assert lib.lla_status_string(code).decode() == name
+    assert lib.lla_version() >= 100
+
+
+def test_num_levels(lib):
+    assert [lib.lla_num_levels(T) for T in (1, 2, 3, 256, 2048, 8192, 32768, 65536)] == \
+        [1, 2, 3, 9, 12, 14, 16, 17]
+    assert lib.lla_num_levels(0) == 0
+
+
+def test_workspace_queries(lib):
+    n = lib.lla_fwd_workspace_bytes(1, 16, 32768, 128, 128, 64, binding.LLA_BF16)
+    assert n > 0 and n % 256 == 0
+    assert lib.lla_fwd_workspace_bytes(1, 16, 32768, 128, 128, 48, binding.LLA_BF16) == 0
+    assert lib.lla_fwd_workspace_bytes(0, 16, 32768, 128, 128, 64, binding.LLA_BF16) == 0
+    assert lib.lla_decode_state_bytes(64, 16, 128, 128, 17) == 64 * 16 * 17 * 128 * 128 * 4
+    assert lib.lla_prefill_workspace_bytes(1, 16, 1000) >= 16 * 1000 * 4
+
+
+NULL = None
+
+
+def fwd(lib, B=1, H=1, T=64, dk=64, dv=64, chunk=64, in_dt=1, out_dt=0, ws_bytes=1 << 30,
+        ptr=ctypes.c_void_p(256)):
+    p = ptr
+    return lib.lla_fwd(p, p, p, p, p, p, B, H, T, dk, dv, chunk, in_dt, out_dt, p, ws_bytes, NULL)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(chunk=48), 2), (dict(T=100), 2), (dict(dk=96), 2), (dict(dv=8), 2),
+    (dict(B=-1), 1), (dict(in_dt=7), 1), (dict(out_dt=9), 1), (dict(in_dt=0, out_dt=1), 2),
+    (dict(ws_bytes=0), 3), (dict(ptr=ctypes.c_void_p(0)), 1), (dict(ptr=ctypes.c_void_p(8)), 1),
+    (dict(T=1 << 25), 2), (dict(B=70000), 2),
+])
+def test_fwd_validation_rejects_before_launch(lib, kw, code):
+    assert fwd(lib, **kw) == code
+
+
+def test_fwd_empty_is_a_noop(lib):
+    assert fwd(lib, T=0, ptr=ctypes.c_void_p(0), ws_bytes=0) == 0
+    assert fwd(lib, B=0, ptr=ctypes.c_void_p(0), ws_bytes=0) == 0
+
+
+def test_decode_validation(lib):
+    p = ctypes.c_void_p(256)
+    args = lambda **kw: [kw.get("S", p), p, p, p, p, p, p, p, p, kw.get("B", 2), 2,
+                         kw.get("dk", 64), 64, kw.get("Ls", 17), kw.get("dt", 1), NULL, NULL]
+    assert lib.lla_decode_step(*args(dk=48)) == 2
+    assert lib.lla_decode_step(*args(Ls=0)) == 2
+    assert lib.lla_decode_step(*args(Ls=41)) == 2
+    assert lib.lla_decode_step(*args(dt=3)) == 1
+    assert lib.lla_decode_step(*args(S=ctypes.c_void_p(0))) == 1
+    assert lib.lla_decode_step(*args(B=0, S=ctypes.c_void_p(0))) == 0
+
+
+def test_prefill_validation(lib):
+    p = ctypes.c_void_p(256)
+    # bit_length(T) must fit in Ls slots
+    assert lib.lla_prefill_state(p, p, p, p, p, 1, 1, 8, 64, 64, 3, 1, p, 1 << 20, NULL) == 2
+    assert lib.lla_prefill_state(p, p, p, p, p, 1, 1, 8, 64, 64, 4, 1, p, 0, NULL) == 3

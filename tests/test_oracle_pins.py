@@ -262,3 +262,11 @@ def test_softplus_centre_is_one():
     """Page "Adaptive memory decay for Log-Linear Attention": the bias 0.54
     makes softplus start near 1.0."""
     assert abs(math.log1p(math.exp(0.54)) - 0.99916) < 5e-6
+
+
+def test_naive_rows_equal_full_double_sum():
+    q, k, v, g, lam = rand_inputs(1, 1, 130, 6, 5, seed=21)
+    full = oracle.naive(q, k, v, g, lam)[0, 0]
+    rows = [0, 1, 63, 64, 65, 127, 129]
+    part = oracle.naive_rows(q[0, 0], k[0, 0], v[0, 0], g[0, 0], lam[0, 0], rows)
+    np.testing.assert_array_equal(part, full[rows])
