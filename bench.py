@@ -311,17 +311,21 @@ def run_decode(dev, args):
                                     stream=torch.cuda.current_stream())
     reps = 5
     times = []
+    out.fill_(float("nan"))
     for r in range(reps + 1):
-        S.copy_(S0)
-        D.copy_(D0)
-        torch.cuda.synchronize(dev)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        graph.replay()
-        b.record(stream)
+        with torch.cuda.stream(stream):
+            S.copy_(S0)
+            D.copy_(D0)
+            torch.cuda.synchronize(dev)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
         torch.cuda.synchronize(dev)
         if r > 0:
             times.append(a.elapsed_time(b) / cfg.steps)
+    if not bool(torch.isfinite(out).all()):
+        raise RuntimeError("decode graph replay left outputs unwritten")
     us = statistics.median(times) * 1e3
     nbytes = statistics.mean(decode_bytes(cfg, pos0 + s) for s in range(cfg.steps))
     gbs = nbytes / (us / 1e6) / 1e9
@@ -385,7 +389,7 @@ def main():
     ap.add_argument("--impl", default="lla", choices=["lla", "reference"])
     ap.add_argument("--skip-decode", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
-    ap.add_argument("--cpu-tokens", type=int, default=8192)
+    ap.add_argument("--cpu-tokens", type=int, default=32768)
     ap.add_argument("--ref-tokens", type=int, default=2048)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

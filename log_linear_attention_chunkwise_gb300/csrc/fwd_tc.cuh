@@ -1,0 +1,25 @@
+// Internal interface of the tensor-core (tcgen05) forward.
+#pragma once
+
+#include <stddef.h>
+
+#include "lla_common.cuh"
+
+namespace lla {
+
+struct TcFwdArgs {
+    const void *q, *k, *v;
+    const float *g, *lam;
+    void *out;
+    int B, H, T, L;
+    lla_dtype out_dt;
+    void *workspace;
+    void *stream;
+};
+
+bool tc_supported(int dk, int dv, lla_dtype in_dt);
+size_t tc_workspace_bytes(int B, int H, int T);
+size_t tc_smem_bytes();
+cudaError_t tc_fwd(const TcFwdArgs &A);
+
+}  // namespace lla

@@ -4,6 +4,7 @@
 
 #include "decode.cuh"
 #include "fwd_simt.cuh"
+#include "fwd_tc.cuh"
 #include "lla_common.cuh"
 
 using namespace lla;
@@ -67,6 +68,7 @@ size_t lla_fwd_workspace_bytes(int B, int H, int T, int dk, int dv, int chunk, l
 {
     if (fwd_shape_status(B, H, T, dk, dv, chunk, in_dt) != LLA_OK) return 0;
     if ((long long)B * H * T == 0) return 0;
+    if (tc_supported(dk, dv, in_dt)) return tc_workspace_bytes(B, H, T);
     SimtFwdArgs A = simt_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, B, H, T,
                               dk, dv, chunk, in_dt, LLA_F32, nullptr, nullptr);
     return simt_workspace_bytes(A);
@@ -79,6 +81,7 @@ int lla_fwd_launches(int B, int H, int T, int dk, int dv, int chunk, lla_dtype i
     if (out_dt != LLA_F32 && out_dt != LLA_BF16) return 0;
     if (in_dt == LLA_F32 && out_dt != LLA_F32) return 0;
     if ((long long)B * H * T == 0) return 0;
+    if (tc_supported(dk, dv, in_dt)) return 2;
     return T / chunk > 1 ? 4 : 3;
 }
 
@@ -100,6 +103,13 @@ lla_status lla_fwd(const void *q, const void *k, const void *v, const float *g,
     if (workspace_bytes < need) return LLA_ERR_WORKSPACE_TOO_SMALL;
     if (need > 0 && (workspace == nullptr || ((uintptr_t)workspace & 255u) != 0))
         return LLA_ERR_INVALID_ARGUMENT;
+    if (tc_supported(dk, dv, in_dt)) {
+        TcFwdArgs A;
+        A.q = q; A.k = k; A.v = v; A.g = g; A.lam = lambda; A.out = out;
+        A.B = B; A.H = H; A.T = T; A.L = lla_num_levels(T); A.out_dt = out_dt;
+        A.workspace = workspace; A.stream = stream;
+        return tc_fwd(A) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+    }
     SimtFwdArgs A = simt_args(q, k, v, g, lambda, out, B, H, T, dk, dv, chunk, in_dt, out_dt,
                               workspace, stream);
     if (simt_max_smem_bytes(A) > 227 * 1024) return LLA_ERR_UNSUPPORTED_SHAPE;

@@ -6,6 +6,13 @@ fp32 inputs: ||gpu - oracle||_F / ||oracle||_F <= 1e-4 and
 max |gpu - oracle| <= 1e-4 * max |oracle|.
 The oracle reads the same rounded inputs the GPU reads, promoted exactly to
 fp64, so the comparison measures the kernels' arithmetic only.
+
+Stress variants (gates forced to 0 on some heads, so nothing decays and the
+outputs grow with the sequence length) keep the relative Frobenius bound and
+take the max-abs bound relative to the output's magnitude:
+max |gpu - oracle| <= max(2e-2, 5e-3 * max |oracle|).  The bf16 operands of
+the tensor-core products carry a relative rounding of 2^-9, so an absolute
+bound cannot hold for outputs of arbitrary magnitude.
 """
 
 import numpy as np
@@ -29,11 +36,12 @@ def errors(gpu, ref):
     return max_abs, rel_fro, ref_max
 
 
-def assert_parity(gpu, ref, in_dtype, what=""):
+def assert_parity(gpu, ref, in_dtype, what="", stress=False):
     max_abs, rel_fro, ref_max = errors(gpu, ref)
     if in_dtype == torch.bfloat16:
-        ok = max_abs <= BF16_MAX_ABS and rel_fro <= BF16_REL_FRO
-        bound = f"max_abs<={BF16_MAX_ABS}, rel_fro<={BF16_REL_FRO}"
+        amax = max(BF16_MAX_ABS, BF16_REL_FRO * ref_max) if stress else BF16_MAX_ABS
+        ok = max_abs <= amax and rel_fro <= BF16_REL_FRO
+        bound = f"max_abs<={amax:.3g}, rel_fro<={BF16_REL_FRO}"
     else:
         ok = rel_fro <= F32_REL_FRO and max_abs <= F32_REL_MAX * max(ref_max, 1e-30)
         bound = f"rel_fro<={F32_REL_FRO}, max_abs<={F32_REL_MAX}*{ref_max:.3g}"
