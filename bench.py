@@ -160,6 +160,8 @@ def run_lla(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     cfg = W.FWD_CONFIGS[WORKLOAD]
+    if args.heads or args.seq_len:  # a smaller case of the same recipe (profiling)
+        cfg = cfg.with_(H=args.heads or cfg.H, T=args.seq_len or cfg.T)
     x = W.make_fwd_inputs(cfg)
     xd = {n: t.to(dev) for n, t in x.items()}
     out = torch.empty((cfg.B, cfg.H, cfg.T, cfg.dv), dtype=torch.float32, device=dev)
@@ -242,7 +244,8 @@ def run_lla(args, rank, world, local_rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; q,k,v bf16, g,lambda fp32)",
-        "config": {"workload": f"{WORKLOAD}: B=1 H=16 T=32768 dk=dv=128 chunk=64 bf16 in, fp32 out",
+        "config": {"workload": f"{WORKLOAD}: B={cfg.B} H={cfg.H} T={cfg.T} dk=dv=128 chunk=64 "
+                               "bf16 in, fp32 out",
                    "global_batch": cfg.B * world, "seq_len": cfg.T,
                    "parallelism": f"replicas over (batch, head) units x{world}",
                    "l2": "inputs (436 MB) larger than L2, no flush"},
@@ -391,6 +394,8 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=32768)
     ap.add_argument("--ref-tokens", type=int, default=2048)
+    ap.add_argument("--heads", type=int, default=0, help="override H (smaller profiling case)")
+    ap.add_argument("--seq-len", type=int, default=0, help="override T (smaller profiling case)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -5,9 +5,12 @@
 // §2.2 (Fenwick buckets of [0,t), one state per bucket, lambda-weighted
 // read-out) and §2.3 (the hierarchical mask computed chunkwise with matmuls).
 //
-// One CTA handles one tile of 128 tokens of one (batch, head); tiles are
-// taken from a global ticket counter in (batch*head, tile) order, so a tile
-// only ever waits on tiles that started before it.  With Gam_i the gate sum
+// Four launches.  Two small kernels form the fp64 tile-gate prefix sums.  The node
+// producer (one CTA per tile, tickets in (tile, batch*head) order so a tile
+// only waits on tiles that started before it) computes each tile's state and
+// publishes the tile-level Fenwick node it closes.  The read-out consumer (one
+// CTA per tile, no waits: every node exists when it starts) forms the masked
+// intra-tile product and the lambda-weighted read-out of the nodes.  With Gam_i the gate sum
 // of tile i and P_i = Gam_0 + ... + Gam_{i-1} (fp64, from the prefix kernel),
 // the earlier tiles of tile i form the tile-level Fenwick buckets ending at
 // j = i, i - lowbit(i), ...; bucket j (level m = ctz(j)) holds the tiles
@@ -20,9 +23,11 @@
 //        Node_{i+1} = H + sum_{m < ctz(i+1)} exp(P_{i+1} - P_{j_m}) Node_{j_m},
 //        j_m = i + 1 - 2^m, published to global memory (fp32 + bf16 copy)
 //   P  = S . M,  M[a][b] = lambda_a[bit_length(a^b)] exp(gamma_a - gamma_b), b <= a
-//   O  = P V + sum_{path j} diag(lambda_.[8+m] exp(gamma_. + P_i - P_j)) Q Node_j
+//   O  = P V + sum_{path j} diag(lambda_.[8+m] exp(gamma_. + P_i - P_j)) (Q Node_j)
 // Every product above is a tcgen05 MMA of M = N = 128, bf16 operands in
-// 128-byte-swizzled shared memory, fp32 accumulators in tensor memory.
+// 128-byte-swizzled shared memory, fp32 accumulators in tensor memory.  The
+// read-out forms U_j = Q Node_j per path node in tensor memory and applies
+// the per-row weights in fp32 while draining it.
 #include "fwd_tc.cuh"
 #include "sm100.cuh"
 #include "tma_host.cuh"
@@ -35,30 +40,17 @@ using namespace sm100;
 constexpr int kTile = 128;       // tokens per tile (MMA M)
 constexpr int kD = 128;          // dk = dv
 constexpr int kTileLevels = 7;   // levels inside a tile: bit_length(a ^ b) <= 7
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;  // two warpgroups; warps w and w+4 share TMEM lanes
 constexpr uint32_t kBuf = kTile * kD * 2;  // one bf16 128x128 operand: 32 KB
 constexpr uint32_t kHalf = kBuf / 2;       // one 64-column swizzled block
 constexpr uint32_t kWaitIters = 1u << 22;  // bounded waits (~0.5 s with back-off)
 constexpr int kLamLd = 9;                  // padded row of the in-tile lambdas
+constexpr int kMaxPath = 17;               // levels of a tile index (T <= 2^24, so NT <= 2^17)
 
 // Error codes written to the workspace error word.
 constexpr int kErrLoadTimeout = 1;
 constexpr int kErrMmaTimeout = 2;
 constexpr int kErrNodeTimeout = 3;
-
-struct __align__(1024) TcSmem {
-    uint8_t q[kBuf];
-    uint8_t k[kBuf];
-    uint8_t v[kBuf];
-    uint8_t vs[kBuf];
-    uint8_t p[kBuf];
-    float gam[kTile];
-    float lam[kTile * kLamLd];
-    float wsum[4];
-    uint64_t bar_load, bar_mma, bar_node[2], bar_stage[2], bar_done;
-    uint32_t tmem;
-    int ticket;
-};
 
 struct TcParams {
     const float *g, *lam;
@@ -91,50 +83,45 @@ __device__ __forceinline__ void release_flag(int *flag)
     asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(flag), "r"(1) : "memory");
 }
 
-// Row `row` of a 128x128 bf16 operand stored as two 64-column 128B-swizzled
-// blocks: scale every element by w and write to the same place in dst.
-__device__ __forceinline__ void scale_row(const uint8_t *src, uint8_t *dst, int row, float w)
+// Block `blk` (64 columns) of row `row` of a 128x128 bf16 operand stored as
+// two 64-column 128B-swizzled blocks: scale by w into the same place in dst.
+__device__ __forceinline__ void scale_row_half(const uint8_t *src, uint8_t *dst, int row, int blk,
+                                               float w)
 {
 #pragma unroll
-    for (int blk = 0; blk < 2; blk++) {
+    for (int c = 0; c < 8; c++) {
+        const uint32_t off = blk * kHalf + row * 128 + c * 16;
+        uint4 raw = *reinterpret_cast<const uint4 *>(src + off);
+        __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&raw);
 #pragma unroll
-        for (int c = 0; c < 8; c++) {
-            const uint32_t off = blk * kHalf + row * 128 + c * 16;
-            uint4 raw = *reinterpret_cast<const uint4 *>(src + off);
-            __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&raw);
-#pragma unroll
-            for (int u = 0; u < 4; u++) {
-                float2 f = __bfloat1622float2(h[u]);
-                h[u] = __floats2bfloat162_rn(f.x * w, f.y * w);
-            }
-            *reinterpret_cast<uint4 *>(dst + off) = raw;
+        for (int u = 0; u < 4; u++) {
+            float2 f = __bfloat1622float2(h[u]);
+            h[u] = __floats2bfloat162_rn(f.x * w, f.y * w);
         }
+        *reinterpret_cast<uint4 *>(dst + off) = raw;
     }
 }
 
 // 8 MMAs over K = 128: A and B K-major (rows of 128 B, K split in two blocks).
-__device__ __forceinline__ void mma_kk(uint32_t d, const uint8_t *a, const uint8_t *b, uint32_t idesc,
-                                       bool accumulate)
+__device__ __forceinline__ void mma_kk(uint32_t d, const uint8_t *a, const uint8_t *b, uint32_t idesc)
 {
 #pragma unroll
     for (int kk = 0; kk < 8; kk++) {
         const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
         umma_bf16(d, desc_sw128(smem_u32(a) + off, 16, 1024), desc_sw128(smem_u32(b) + off, 16, 1024),
-                  idesc, (accumulate || kk > 0) ? 1u : 0u);
+                  idesc, kk > 0 ? 1u : 0u);
     }
 }
 
 // 8 MMAs over K = 128 with A K-major and B MN-major (rows = K index).
-__device__ __forceinline__ void mma_kmn(uint32_t d, const uint8_t *a, const uint8_t *b, uint32_t idesc,
-                                        bool accumulate)
+__device__ __forceinline__ void mma_kmn(uint32_t d, const uint8_t *a, const uint8_t *b, uint32_t idesc)
 {
 #pragma unroll
     for (int kk = 0; kk < 8; kk++) {
         const uint32_t offa = (kk >> 2) * kHalf + (kk & 3) * 32;
         const uint32_t offb = kk * 2048;
         umma_bf16(d, desc_sw128(smem_u32(a) + offa, 16, 1024),
-                  desc_sw128(smem_u32(b) + offb, kHalf, 1024), idesc,
-                  (accumulate || kk > 0) ? 1u : 0u);
+                  desc_sw128(smem_u32(b) + offb, kHalf, 1024), idesc, kk > 0 ? 1u : 0u);
     }
 }
 
@@ -150,82 +137,237 @@ __device__ __forceinline__ void mma_mnmn(uint32_t d, const uint8_t *a, const uin
     }
 }
 
-template <typename OutT>
-__device__ __forceinline__ void store_out16(OutT *dst, const float (&r)[16]);
-
-template <>
-__device__ __forceinline__ void store_out16<float>(float *dst, const float (&r)[16])
+// Inclusive running sum of the tile's gates: thread (row, half) gets
+// gamma_row; also returns the tile total Gam.  `wsum` is 4 floats of smem.
+__device__ __forceinline__ float tile_cumsum(float gv, float *wsum, float &Gam)
 {
-    float4 *d4 = reinterpret_cast<float4 *>(dst);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    float incl = gv;
 #pragma unroll
-    for (int u = 0; u < 4; u++) d4[u] = make_float4(r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3]);
+    for (int off = 1; off < 32; off <<= 1) {
+        float y = __shfl_up_sync(0xffffffffu, incl, off);
+        if ((tid & 31) >= off) incl += y;
+    }
+    if (tid < kTile && (tid & 31) == 31) wsum[warp] = incl;
+    __syncthreads();
+    float base = 0.f;
+    for (int w = 0; w < (warp & 3); w++) base += wsum[w];
+    Gam = wsum[0] + wsum[1] + wsum[2] + wsum[3];
+    return base + incl;
 }
 
-template <>
-__device__ __forceinline__ void store_out16<__nv_bfloat16>(__nv_bfloat16 *dst, const float (&r)[16])
+// ======================================================= node producer
+// CTA per tile i < NT-1 (tickets in tile-major order): Node_{i+1}.
+// Nodes move through shared memory by TMA: the fp32 node (the chain's
+// operand) as four 32-column boxes, the bf16 copy (the read-out's MMA
+// operand) as two 64-column boxes, all 128-byte swizzled.
+
+struct __align__(1024) ProdSmem {
+    uint8_t k[kBuf];   // K; then, with v, the fp32 staging of a node (64 KB)
+    uint8_t v[kBuf];
+    uint8_t vs[kBuf];  // V scaled by the decay; then the bf16 staging of the node
+    float wsum[4];
+    uint64_t bar_load, bar_mma, bar_dep;
+    uint32_t tmem;
+    int ticket;
+};
+
+// fp32 128x128 tile staged as four 32-column boxes of 128 rows x 128 B:
+// byte offset of the 4-float chunk holding columns [4c, 4c+4) of row r.
+__device__ __forceinline__ uint32_t f32_stage_off(int r, int c)
 {
-    uint4 w[2];
-    __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(w);
-#pragma unroll
-    for (int u = 0; u < 8; u++) h[u] = __floats2bfloat162_rn(r[2 * u], r[2 * u + 1]);
-    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-    d4[0] = w[0];
-    d4[1] = w[1];
+    return (uint32_t)(c >> 3) * (kTile * 128) + sw128_offset(r, c & 7);
 }
 
-template <typename OutT>
-__global__ void __launch_bounds__(kThreads, 1)
-lla_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-                  const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_node,
-                  const TcParams prm)
+__global__ void __launch_bounds__(kThreads, 2)
+lla_node_producer_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                         const __grid_constant__ CUtensorMap map_n32, const __grid_constant__ CUtensorMap map_n16,
+                         const TcParams prm)
 {
     extern __shared__ uint8_t smem_raw[];
-    TcSmem &s = *reinterpret_cast<TcSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                            ~uintptr_t(1023));
+    ProdSmem &s = *reinterpret_cast<ProdSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
+    const int row = tid & (kTile - 1);
+    const int half = tid >> 7;
 
     if (tid == 0) {
         mbar_init(&s.bar_load, 1);
         mbar_init(&s.bar_mma, 1);
-        mbar_init(&s.bar_node[0], 1);
-        mbar_init(&s.bar_node[1], 1);
-        mbar_init(&s.bar_stage[0], 1);
-        mbar_init(&s.bar_stage[1], 1);
-        mbar_init(&s.bar_done, 1);
+        mbar_init(&s.bar_dep, 1);
         fence_mbar_init();
-        tma_prefetch_map(&map_q);
         tma_prefetch_map(&map_k);
         tma_prefetch_map(&map_v);
-        tma_prefetch_map(&map_node);
+        tma_prefetch_map(&map_n32);
+        tma_prefetch_map(&map_n16);
     }
     if (warp == 0) {
-        tmem_alloc(&s.tmem, 512);
+        tmem_alloc(&s.tmem, 128);
         tmem_relinquish();
     }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
-    // The ticket is taken only once this CTA holds its tensor memory, so a
-    // tile with a ticket never waits on a CTA that cannot make progress.
+    // the ticket is taken once this CTA holds its tensor memory, so a tile
+    // with a ticket never waits on a CTA that cannot make progress
     if (tid == 0) s.ticket = atomicAdd(prm.ticket, 1);
     __syncthreads();
     const uint32_t tm = s.tmem;
-    const uint32_t tm_S = tm, tm_H = tm + 128, tm_O = tm + 256;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-
-    const int NT = prm.NT;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const int NT = prm.NT, BH = prm.BH;
     const int ticket = s.ticket;
-    const int bh = ticket / NT;
-    const int i = ticket - bh * NT;
-    const int tile_rows = min(kTile, prm.T - i * kTile);
-    const bool has_node = i < NT - 1;  // the last tile starts no node
-    const long long tok = (long long)bh * prm.T + (long long)i * kTile + tid;
+    if (ticket >= (NT - 1) * BH) {
+        tc_fence_before_sync();
+        __syncthreads();
+        if (warp == 0) tmem_dealloc(tm, 128);
+        return;
+    }
+    const int i = ticket / BH;
+    const int bh = ticket - i * BH;
     const double *Pb = prm.P + (long long)bh * (NT + 1);
     int *flags = prm.flags + (long long)bh * (NT + 1);
 
-    // ---- loads: Q, K, V by TMA; gates and in-tile lambdas by the threads
     if (tid == 0) {
+        mbar_arrive_expect_tx(&s.bar_load, 2 * kBuf);
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+            tma_load_3d(s.k + h * kHalf, &map_k, &s.bar_load, h * 64, i * kTile, bh);
+            tma_load_3d(s.v + h * kHalf, &map_v, &s.bar_load, h * 64, i * kTile, bh);
+        }
+    }
+    // tiles i < NT-1 are full: no ragged rows here
+    const long long tok = (long long)bh * prm.T + (long long)i * kTile + row;
+    float Gam;
+    const float gam_a = tile_cumsum(prm.g[tok], s.wsum, Gam);
+    if (!mbar_wait(&s.bar_load, 0, kWaitIters)) set_err(prm.err, kErrLoadTimeout);
+    scale_row_half(s.v, s.vs, row, half, __expf(Gam - gam_a));
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+        tc_fence_after_sync();
+        mma_mnmn(tm, s.k, s.vs, idesc_bf16_f32(128, 128, true, true));
+        umma_commit(&s.bar_mma);
+    }
+    const int z = __ffs(i + 1) - 1;  // ctz(i+1): the lower-level nodes folded in
+    if (!mbar_wait(&s.bar_mma, 0, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
+    tc_fence_after_sync();
+    // H row (dk index `row`), columns [64*half, 64*half + 64)
+    float r[64];
+#pragma unroll
+    for (int c0 = 0; c0 < 64; c0 += 16)
+        tmem_ld16(tm + lane_off + half * 64 + c0, *reinterpret_cast<float(*)[16]>(r + c0));
+    tmem_ld_wait();
+    tc_fence_before_sync();
+    __syncthreads();  // K, V and Vs are free from here on
+
+    // Node_{i+1} = H + sum_{m<z} exp(P_{i+1} - P_{j_m}) Node_{j_m},  j_m = i + 1 - 2^m
+    const double Pn = Pb[i + 1];
+    uint8_t *stage32 = s.k;  // 64 KB across k and v
+    for (int m = 0; m < z; m++) {
+        const int j = i + 1 - (1 << m);
+        if (tid == 0) {
+            if (!wait_flag(flags + j, kWaitIters)) set_err(prm.err, kErrNodeTimeout);
+            fence_proxy_async_global();
+            mbar_arrive_expect_tx(&s.bar_dep, 2 * kBuf);
+#pragma unroll
+            for (int b = 0; b < 4; b++)
+                tma_load_3d(stage32 + b * (kTile * 128), &map_n32, &s.bar_dep, b * 32, 0, bh * NT + j);
+        }
+        const float f = __expf((float)(Pn - Pb[j]));
+        if (!mbar_wait(&s.bar_dep, m & 1, kWaitIters)) set_err(prm.err, kErrLoadTimeout);
+#pragma unroll
+        for (int c = 0; c < 16; c++) {
+            const float4 x = *reinterpret_cast<const float4 *>(stage32 + f32_stage_off(row, half * 16 + c));
+            r[4 * c] = fmaf(f, x.x, r[4 * c]);
+            r[4 * c + 1] = fmaf(f, x.y, r[4 * c + 1]);
+            r[4 * c + 2] = fmaf(f, x.z, r[4 * c + 2]);
+            r[4 * c + 3] = fmaf(f, x.w, r[4 * c + 3]);
+        }
+        __syncthreads();  // the staging buffer is reused by the next load
+    }
+    // stage the node: fp32 in k/v, bf16 in vs (block `half`, 8 chunks of 8 columns)
+#pragma unroll
+    for (int c = 0; c < 16; c++)
+        *reinterpret_cast<float4 *>(stage32 + f32_stage_off(row, half * 16 + c)) =
+            make_float4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
+#pragma unroll
+    for (int c = 0; c < 8; c++) {
+        uint4 w;
+        __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&w);
+#pragma unroll
+        for (int u = 0; u < 4; u++) h[u] = __floats2bfloat162_rn(r[8 * c + 2 * u], r[8 * c + 2 * u + 1]);
+        *reinterpret_cast<uint4 *>(s.vs + half * kHalf + sw128_offset(row, c)) = w;
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+#pragma unroll
+        for (int b = 0; b < 4; b++) tma_store_3d(&map_n32, stage32 + b * (kTile * 128), b * 32, 0, bh * NT + i + 1);
+#pragma unroll
+        for (int h = 0; h < 2; h++) tma_store_3d(&map_n16, s.vs + h * kHalf, h * 64, 0, bh * NT + i + 1);
+        tma_store_commit();
+        tma_store_wait_all();
+        fence_proxy_async_global();
+        __threadfence();
+        release_flag(flags + i + 1);
+    }
+    if (warp == 0) tmem_dealloc(tm, 128);
+}
+
+// ======================================================= read-out consumer
+// CTA per tile; every node is published before this kernel starts.
+
+
+struct __align__(1024) ConsSmem {
+    uint8_t q[kBuf];
+    uint8_t k[kBuf];   // K, then P (masked scores), then node stage 0
+    uint8_t v[kBuf];   // V, then node stage 1
+    float gam[kTile];
+    float kf[kTile];              // exp(gamma_e - gamma_b), e = last key of b's 16-key chunk
+    float lam[kTile * kLamLd];
+    float wgt[kMaxPath * kTile];  // read-out weight of each path level per row
+    float wsum[4];
+    uint64_t bar_load, bar_s, bar_pv, bar_node[2], bar_u[2];
+    uint32_t tmem;
+};
+
+template <typename OutT>
+__global__ void __launch_bounds__(kThreads, 2)
+lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                            const __grid_constant__ CUtensorMap map_v,
+                            const __grid_constant__ CUtensorMap map_node,
+                            const __grid_constant__ CUtensorMap map_out, const TcParams prm)
+{
+    extern __shared__ uint8_t smem_raw[];
+    ConsSmem &s = *reinterpret_cast<ConsSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int row = tid & (kTile - 1);
+    const int half = tid >> 7;
+    const int NT = prm.NT, BH = prm.BH;
+    // tile-major, last tiles first: co-resident tiles share their deep nodes,
+    // and the nodes the producer wrote last are still in L2
+    const int rev = NT * BH - 1 - (int)blockIdx.x;
+    const int i = rev / BH;
+    const int bh = rev - i * BH;
+
+    if (tid == 0) {
+        mbar_init(&s.bar_load, 1);
+        mbar_init(&s.bar_s, 1);
+        mbar_init(&s.bar_pv, 1);
+        mbar_init(&s.bar_node[0], 1);
+        mbar_init(&s.bar_node[1], 1);
+        mbar_init(&s.bar_u[0], 1);
+        mbar_init(&s.bar_u[1], 1);
+        fence_mbar_init();
+        tma_prefetch_map(&map_q);
+        tma_prefetch_map(&map_k);
+        tma_prefetch_map(&map_v);
+        tma_prefetch_map(&map_node);
+        tma_prefetch_map(&map_out);
         mbar_arrive_expect_tx(&s.bar_load, 3 * kBuf);
 #pragma unroll
         for (int h = 0; h < 2; h++) {
@@ -234,239 +376,292 @@ lla_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             tma_load_3d(s.v + h * kHalf, &map_v, &s.bar_load, h * 64, i * kTile, bh);
         }
     }
-    const bool row_ok = tid < tile_rows;
-    const float gv = row_ok ? prm.g[tok] : 0.f;
-    const float *lam_row = prm.lam + tok * prm.L;
-#pragma unroll
-    for (int l = 0; l <= kTileLevels; l++)
-        s.lam[tid * kLamLd + l] = (row_ok && l < prm.L) ? lam_row[l] : 0.f;
-    // inclusive running sum of the gates over the tile
-    float incl = gv;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        float y = __shfl_up_sync(0xffffffffu, incl, off);
-        if ((tid & 31) >= off) incl += y;
+    if (warp == 0) {
+        tmem_alloc(&s.tmem, 256);
+        tmem_relinquish();
     }
-    if ((tid & 31) == 31) s.wsum[warp] = incl;
+    const int tile_rows = min(kTile, prm.T - i * kTile);
+    const bool row_ok = row < tile_rows;
+    const long long tok = (long long)bh * prm.T + (long long)i * kTile + row;
+    const float *lam_row = prm.lam + tok * prm.L;
+    const double *Pb = prm.P + (long long)bh * (NT + 1);
+    if (half == 0) {
+#pragma unroll
+        for (int l = 0; l <= kTileLevels; l++)
+            s.lam[row * kLamLd + l] = (row_ok && l < prm.L) ? lam_row[l] : 0.f;
+    }
+    float Gam;
+    const float gam_a = tile_cumsum(row_ok ? prm.g[tok] : 0.f, s.wsum, Gam);
+    if (half == 0) s.gam[row] = gam_a;
     __syncthreads();
-    float base = 0.f;
-    for (int w = 0; w < warp; w++) base += s.wsum[w];
-    const float gam_a = base + incl;
-    s.gam[tid] = gam_a;
-    const float Gam = s.wsum[0] + s.wsum[1] + s.wsum[2] + s.wsum[3];
-
-    if (!mbar_wait(&s.bar_load, 0, kWaitIters)) set_err(prm.err, kErrLoadTimeout);
-    // V scaled by exp(Gam - gamma_s), row s = this thread's token
-    if (has_node) scale_row(s.v, s.vs, tid, __expf(Gam - gam_a));
-    fence_proxy_async_smem();
+    if (half == 0) s.kf[row] = __expf(s.gam[row | 15] - gam_a);
+    // read-out weights: path level n (node j_n, level m_n = ctz(j_n)) of row a:
+    //   lambda_a[8 + m_n] * exp(gamma_a + P_i - P_{j_n}); the halves split the levels
+    int npath = 0;
+    {
+        const double Pi = Pb[i];
+        int n = 0;
+        for (int j = i; j > 0; j -= (j & -j), n++) {
+            if ((n & 1) == half) {
+                const int lev = kTileLevels + 1 + (__ffs(j) - 1);
+                s.wgt[n * kTile + row] =
+                    row_ok ? lam_row[lev] * __expf(gam_a + (float)(Pi - Pb[j])) : 0.f;
+            }
+        }
+        npath = n;
+    }
     tc_fence_before_sync();
     __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tm = s.tmem;
+    const uint32_t slot[2] = {tm, tm + 128};
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
 
-    // ---- S = Q K^T and H = K^T Vs
+    // ---- S = Q K^T
     if (tid == 0) {
+        if (!mbar_wait(&s.bar_load, 0, kWaitIters)) set_err(prm.err, kErrLoadTimeout);
         tc_fence_after_sync();
-        mma_kk(tm_S, s.q, s.k, idesc_bf16_f32(128, 128, false, false), false);
-        if (has_node) mma_mnmn(tm_H, s.k, s.vs, idesc_bf16_f32(128, 128, true, true));
-        umma_commit(&s.bar_mma);
+        mma_kk(slot[0], s.q, s.k, idesc_bf16_f32(128, 128, false, false));
+        umma_commit(&s.bar_s);
     }
-    if (!mbar_wait(&s.bar_mma, 0, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
+    if (!mbar_wait(&s.bar_s, 0, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
     tc_fence_after_sync();
 
-    // ---- Node_{i+1} = H + decayed lower-level path nodes; thread = dk row
-    if (has_node) {
-        const int z = __ffs(i + 1) - 1;  // ctz(i+1)
-        const double Pn = Pb[i + 1];
-        float fac[24];
-#pragma unroll
-        for (int m = 0; m < 24; m++) fac[m] = 0.f;
-        for (int m = 0; m < z; m++) {
-            const int j = i + 1 - (1 << m);
-            if (tid == 0 && !wait_flag(flags + j, kWaitIters)) set_err(prm.err, kErrNodeTimeout);
-        }
-        __syncthreads();
-#pragma unroll
-        for (int m = 0; m < 24; m++)
-            if (m < z) fac[m] = __expf((float)(Pn - Pb[i + 1 - (1 << m)]));
-        const long long nbase = ((long long)bh * NT) * (kD * kD);
-        float *dst32 = prm.node32 + nbase + (long long)(i + 1) * kD * kD + tid * kD;
-        __nv_bfloat16 *dst16 = prm.node16 + nbase + (long long)(i + 1) * kD * kD + tid * kD;
-#pragma unroll 1
-        for (int c0 = 0; c0 < kD; c0 += 16) {
-            float r[16];
-            tmem_ld16(tm_H + lane_off + c0, r);
-            tmem_ld_wait();
-            for (int m = 0; m < z; m++) {
-                const float4 *src = reinterpret_cast<const float4 *>(
-                    prm.node32 + nbase + (long long)(i + 1 - (1 << m)) * kD * kD + tid * kD + c0);
-                const float f = fac[m];
-#pragma unroll
-                for (int u = 0; u < 4; u++) {
-                    float4 x = __ldcg(src + u);
-                    r[4 * u] = fmaf(f, x.x, r[4 * u]);
-                    r[4 * u + 1] = fmaf(f, x.y, r[4 * u + 1]);
-                    r[4 * u + 2] = fmaf(f, x.z, r[4 * u + 2]);
-                    r[4 * u + 3] = fmaf(f, x.w, r[4 * u + 3]);
-                }
-            }
-            float4 *d4 = reinterpret_cast<float4 *>(dst32 + c0);
-#pragma unroll
-            for (int u = 0; u < 4; u++) __stcg(d4 + u, make_float4(r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3]));
-            uint4 w[2];
-            __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(w);
-#pragma unroll
-            for (int u = 0; u < 8; u++) h[u] = __floats2bfloat162_rn(r[2 * u], r[2 * u + 1]);
-            __stcg(reinterpret_cast<uint4 *>(dst16 + c0), w[0]);
-            __stcg(reinterpret_cast<uint4 *>(dst16 + c0) + 1, w[1]);
-        }
-        fence_proxy_async_global();  // the bf16 copy is read by other CTAs' TMA
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) release_flag(flags + i + 1);
-    }
-
-    // ---- P = S . M  (thread = query row a), bf16 into the K-major buffer
+    // ---- P = S . M  (thread = query row, 64 keys), bf16 into the K buffer
     {
-        const int a = tid;
+        const int a = row;
         const float *lam_a = s.lam + a * kLamLd;
 #pragma unroll 1
-        for (int c0 = 0; c0 < kTile; c0 += 16) {
+        for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
+            // the load is warp-collective: every lane issues it, whatever its row
             float r[16];
-            tmem_ld16(tm_S + lane_off + c0, r);
+            tmem_ld16(slot[0] + lane_off + c0, r);
             tmem_ld_wait();
             uint4 w[2];
             __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(w);
+            if (c0 > a || !row_ok) {  // strictly above the diagonal, or a row past T
+                w[0] = make_uint4(0u, 0u, 0u, 0u);
+                w[1] = w[0];
+            } else if (c0 + 16 <= a) {
+                // a whole 16-key chunk below the row: one level, and the decay
+                // exp(gamma_a - gamma_b) = exp(gamma_a - gamma_e) exp(gamma_e - gamma_b)
+                // with e = c0 + 15, both factors <= 1
+                const int lev = 32 - __clz(a ^ c0);
+                const float ra = lam_a[lev] * __expf(gam_a - s.gam[c0 + 15]);
 #pragma unroll
-            for (int u = 0; u < 8; u++) {
-                float x[2];
+                for (int u = 0; u < 8; u++)
+                    h[u] = __floats2bfloat162_rn(r[2 * u] * ra * s.kf[c0 + 2 * u],
+                                                 r[2 * u + 1] * ra * s.kf[c0 + 2 * u + 1]);
+            } else {
 #pragma unroll
-                for (int e = 0; e < 2; e++) {
-                    const int b = c0 + 2 * u + e;
-                    x[e] = 0.f;
-                    if (b <= a && row_ok) {
-                        const int lev = 32 - __clz(a ^ b);
-                        x[e] = r[2 * u + e] * lam_a[lev] * __expf(gam_a - s.gam[b]);
+                for (int u = 0; u < 8; u++) {
+                    float x[2];
+#pragma unroll
+                    for (int e = 0; e < 2; e++) {
+                        const int b = c0 + 2 * u + e;
+                        x[e] = 0.f;
+                        if (b <= a) {
+                            const int lev = 32 - __clz(a ^ b);
+                            x[e] = r[2 * u + e] * lam_a[lev] * __expf(gam_a - s.gam[b]);
+                        }
                     }
+                    h[u] = __floats2bfloat162_rn(x[0], x[1]);
                 }
-                h[u] = __floats2bfloat162_rn(x[0], x[1]);
             }
-            const int blk = c0 >> 6;
             const int ch = (c0 & 63) >> 3;
-            *reinterpret_cast<uint4 *>(s.p + blk * kHalf + sw128_offset(a, ch)) = w[0];
-            *reinterpret_cast<uint4 *>(s.p + blk * kHalf + sw128_offset(a, ch + 1)) = w[1];
+            *reinterpret_cast<uint4 *>(s.k + half * kHalf + sw128_offset(a, ch)) = w[0];
+            *reinterpret_cast<uint4 *>(s.k + half * kHalf + sw128_offset(a, ch + 1)) = w[1];
         }
     }
     fence_proxy_async_smem();
     tc_fence_before_sync();
     __syncthreads();
+    // ---- O = P V into slot 1; then the first two path nodes into the freed buffers
+    uint8_t *const nd[2] = {s.k, s.v};
     if (tid == 0) {
         tc_fence_after_sync();
-        mma_kmn(tm_O, s.p, s.v, idesc_bf16_f32(128, 128, false, true), false);
-        umma_commit(&s.bar_mma);
-    }
-
-    // ---- read-out: O += (w_m . Q) Node_j over the tile-level Fenwick path
-    // stage 0 uses the K / Vs buffers (free once S and H are done), stage 1
-    // the P / V buffers (free once P V is done).
-    uint8_t *wq_buf[2] = {s.k, s.p};
-    uint8_t *nd_buf[2] = {s.vs, s.v};
-    int n = 0;
-    for (int j = i; j > 0; j -= (j & -j), n++) {
-        const int st = n & 1;
-        const int m = __ffs(j) - 1;
-        const int lev = kTileLevels + 1 + m;
-        if (n == 1) {
-            if (!mbar_wait(&s.bar_mma, 1, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
-        } else if (n >= 2) {
-            if (!mbar_wait(&s.bar_stage[st], ((n - 2) >> 1) & 1, kWaitIters))
-                set_err(prm.err, kErrMmaTimeout);
-        }
-        tc_fence_after_sync();
-        if (tid == 0) {
-            if (!wait_flag(flags + j, kWaitIters)) set_err(prm.err, kErrNodeTimeout);
-            fence_proxy_async_global();
-            mbar_arrive_expect_tx(&s.bar_node[st], kBuf);
-            tma_load_3d(nd_buf[st], &map_node, &s.bar_node[st], 0, 0, bh * NT + j);
-            tma_load_3d(nd_buf[st] + kHalf, &map_node, &s.bar_node[st], 64, 0, bh * NT + j);
-        }
-        const float wl = row_ok ? lam_row[lev] * __expf(gam_a + (float)(Pb[i] - Pb[j])) : 0.f;
-        scale_row(s.q, wq_buf[st], tid, wl);
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        __syncthreads();
-        if (tid == 0) {
-            if (!mbar_wait(&s.bar_node[st], (n >> 1) & 1, kWaitIters)) set_err(prm.err, kErrLoadTimeout);
-            tc_fence_after_sync();
-            mma_kmn(tm_O, wq_buf[st], nd_buf[st], idesc_bf16_f32(128, 128, false, true), true);
-            umma_commit(&s.bar_stage[st]);
+        mma_kmn(slot[1], s.k, s.v, idesc_bf16_f32(128, 128, false, true));
+        umma_commit(&s.bar_pv);
+        if (npath > 0) {
+            if (!mbar_wait(&s.bar_pv, 0, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
+            int n = 0;
+            for (int j = i; j > 0 && n < 2; j -= (j & -j), n++) {
+                mbar_arrive_expect_tx(&s.bar_node[n], kBuf);
+                tma_load_3d(nd[n], &map_node, &s.bar_node[n], 0, 0, bh * NT + j);
+                tma_load_3d(nd[n] + kHalf, &map_node, &s.bar_node[n], 64, 0, bh * NT + j);
+            }
         }
     }
-    if (tid == 0) umma_commit(&s.bar_done);
-    if (!mbar_wait(&s.bar_done, 0, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
+    if (!mbar_wait(&s.bar_pv, 0, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
+    tc_fence_after_sync();
+    float o[64];
+#pragma unroll
+    for (int c0 = 0; c0 < 64; c0 += 16) {
+        float r[16];
+        tmem_ld16(slot[1] + lane_off + half * 64 + c0, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int u = 0; u < 16; u++) o[c0 + u] = r[u];
+    }
+    tc_fence_before_sync();
+    __syncthreads();  // slot 1 drained
     tc_fence_after_sync();
 
-    // ---- O epilogue: thread = output row
-    if (row_ok) {
-        OutT *dst = reinterpret_cast<OutT *>(prm.out) + tok * kD;
-#pragma unroll 1
-        for (int c0 = 0; c0 < kD; c0 += 16) {
-            float r[16];
-            tmem_ld16(tm_O + lane_off + c0, r);
-            tmem_ld_wait();
-            store_out16<OutT>(dst + c0, r);
+    // ---- read-out: U_n = Q Node_{j_n} into slot n&1, drained with fp32 weights
+    if (tid == 0 && npath > 0) {
+        if (!mbar_wait(&s.bar_node[0], 0, kWaitIters)) set_err(prm.err, kErrLoadTimeout);
+        tc_fence_after_sync();
+        mma_kmn(slot[0], s.q, nd[0], idesc_bf16_f32(128, 128, false, true));
+        umma_commit(&s.bar_u[0]);
+    }
+    int jn2 = i;  // node index of level n+2, advanced as levels are consumed
+    if (jn2 > 0) jn2 -= (jn2 & -jn2);
+    if (jn2 > 0) jn2 -= (jn2 & -jn2);
+    for (int n = 0; n < npath; n++) {
+        const int st = n & 1;
+        if (tid == 0 && n + 1 < npath) {
+            const int st1 = (n + 1) & 1;
+            if (!mbar_wait(&s.bar_node[st1], ((n + 1) >> 1) & 1, kWaitIters)) set_err(prm.err, kErrLoadTimeout);
+            tc_fence_after_sync();
+            mma_kmn(slot[st1], s.q, nd[st1], idesc_bf16_f32(128, 128, false, true));
+            umma_commit(&s.bar_u[st1]);
         }
+        if (!mbar_wait(&s.bar_u[st], (n >> 1) & 1, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
+        tc_fence_after_sync();
+        const float w = s.wgt[n * kTile + row];
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 16) {
+            float r[16];
+            tmem_ld16(slot[st] + lane_off + half * 64 + c0, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int u = 0; u < 16; u++) o[c0 + u] = fmaf(w, r[u], o[c0 + u]);
+        }
+        tc_fence_before_sync();
+        __syncthreads();  // slot st drained; MMA n done, so node buffer st is free
+        tc_fence_after_sync();
+        if (tid == 0 && n + 2 < npath) {
+            mbar_arrive_expect_tx(&s.bar_node[st], kBuf);
+            tma_load_3d(nd[st], &map_node, &s.bar_node[st], 0, 0, bh * NT + jn2);
+            tma_load_3d(nd[st] + kHalf, &map_node, &s.bar_node[st], 64, 0, bh * NT + jn2);
+        }
+        if (jn2 > 0) jn2 -= (jn2 & -jn2);
+    }
+
+    // ---- store: stage the tile in the (now idle) Q/K buffers, then TMA
+    // (rows past T are clipped by the tensor map)
+    if (sizeof(OutT) == 4) {
+        uint8_t *stage = s.q;  // four 32-column fp32 boxes, 64 KB across q and k
+#pragma unroll
+        for (int c = 0; c < 16; c++)
+            *reinterpret_cast<float4 *>(stage + f32_stage_off(row, half * 16 + c)) =
+                make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
     } else {
-        // keep every warp's tcgen05.ld collective: rows past T load and drop
-#pragma unroll 1
-        for (int c0 = 0; c0 < kD; c0 += 16) {
-            float r[16];
-            tmem_ld16(tm_O + lane_off + c0, r);
-            tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 8; c++) {
+            uint4 w;
+            __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&w);
+#pragma unroll
+            for (int u = 0; u < 4; u++) h[u] = __floats2bfloat162_rn(o[8 * c + 2 * u], o[8 * c + 2 * u + 1]);
+            *reinterpret_cast<uint4 *>(s.q + half * kHalf + sw128_offset(row, c)) = w;
         }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+        if (sizeof(OutT) == 4) {
+#pragma unroll
+            for (int b = 0; b < 4; b++) tma_store_3d(&map_out, s.q + b * (kTile * 128), b * 32, i * kTile, bh);
+        } else {
+#pragma unroll
+            for (int h = 0; h < 2; h++) tma_store_3d(&map_out, s.q + h * kHalf, h * 64, i * kTile, bh);
+        }
+        tma_store_commit();
+        tma_store_wait_all();
     }
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tm, 512);
+    if (warp == 0) tmem_dealloc(tm, 256);
 }
 
-// Per (batch*head): Gam_i of every tile in fp64, P_i = prefix sums, and the
-// publication flags and ticket reset for the main kernel.
-__global__ void __launch_bounds__(256)
-lla_tile_gate_prefix_kernel(const float *__restrict__ g, double *__restrict__ P, int *__restrict__ flags,
-                            int *__restrict__ ticket, int *__restrict__ err, int T, int NT)
+// Gate sums, in two small launches.  First, a warp per tile: Gam_i in fp64
+// from one coalesced float4 load per lane, stored in the P array shifted by
+// one (P[i+1] = Gam_i); the producer's flags and ticket are reset here too.
+// Then one CTA per (batch*head) turns the tile sums into the prefix
+// P_i = Gam_0 + ... + Gam_{i-1} in place.
+constexpr int kScanThreads = 1024;
+__global__ void __launch_bounds__(1024)
+lla_tile_gate_sum_kernel(const float *__restrict__ g, double *__restrict__ P, int *__restrict__ flags,
+                         int *__restrict__ ticket, int *__restrict__ err, int T, int NT)
 {
-    __shared__ double part[256];
-    const long long bh = blockIdx.x;
-    const float *gb = g + bh * (long long)T;
+    const long long bh = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tile = blockIdx.x * 32 + warp;
     double *Pb = P + bh * (long long)(NT + 1);
     int *fb = flags + bh * (long long)(NT + 1);
-    double carry = 0.0;
-    for (int t0 = 0; t0 < NT; t0 += 256) {
-        const int tile = t0 + threadIdx.x;
-        double s = 0.0;
-        if (tile < NT) {
-            const int lo = tile * kTile, hi = min(T, lo + kTile);
-            for (int t = lo; t < hi; t++) s += (double)gb[t];
+    if (tile < NT) {
+        const float *gb = g + bh * (long long)T + (long long)tile * kTile;
+        const int n = min(kTile, T - tile * kTile);
+        double acc = 0.0;
+        if (n == kTile) {
+            const float4 x = reinterpret_cast<const float4 *>(gb)[lane];
+            acc = (double)x.x + (double)x.y + (double)x.z + (double)x.w;
+        } else {
+            for (int t = lane; t < n; t += 32) acc += (double)gb[t];
         }
-        part[threadIdx.x] = s;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            double run = carry;
-            for (int u = 0; u < 256; u++) {
-                double x = part[u];
-                part[u] = run;
-                run += x;
-            }
-            carry = run;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) {
+            Pb[tile + 1] = acc;
+            fb[tile + 1] = 0;
         }
-        __syncthreads();
-        if (tile < NT) Pb[tile] = part[threadIdx.x];
-        __syncthreads();
     }
-    if (threadIdx.x == 0) Pb[NT] = carry;
-    for (int j = threadIdx.x; j <= NT; j += 256) fb[j] = 0;
-    if (bh == 0 && threadIdx.x == 0) {
-        *ticket = 0;
-        *err = 0;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        Pb[0] = 0.0;
+        fb[0] = 0;
+        if (bh == 0) {
+            *ticket = 0;
+            *err = 0;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kScanThreads)
+lla_tile_gate_scan_kernel(double *__restrict__ P, int NT)
+{
+    __shared__ double wsum[32];
+    __shared__ double carry_sh;
+    const long long bh = blockIdx.x;
+    double *Pb = P + bh * (long long)(NT + 1);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) carry_sh = 0.0;
+    __syncthreads();
+    for (int base = 1; base <= NT; base += kScanThreads) {
+        const int idx = base + threadIdx.x;
+        const double x = idx <= NT ? Pb[idx] : 0.0;
+        double incl = x;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            double y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        if (lane == 31) wsum[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            double w = wsum[lane], wi = w;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                double y = __shfl_up_sync(0xffffffffu, wi, off);
+                if (lane >= off) wi += y;
+            }
+            wsum[lane] = wi - w;  // exclusive prefix of the warp sums
+        }
+        __syncthreads();
+        const double c = carry_sh;
+        if (idx <= NT) Pb[idx] = c + wsum[warp] + incl;
+        __syncthreads();
+        if (threadIdx.x == kScanThreads - 1) carry_sh = c + wsum[warp] + incl;
+        __syncthreads();
     }
 }
 
@@ -492,7 +687,23 @@ bool tc_supported(int dk, int dv, lla_dtype in_dt)
     return in_dt == LLA_BF16 && dk == kD && dv == kD;
 }
 
-size_t tc_smem_bytes() { return sizeof(TcSmem) + 1024; }
+size_t tc_smem_bytes() { return sizeof(ConsSmem) + 1024; }
+
+static_assert(sizeof(ProdSmem) + 1024 <= 113 * 1024, "producer must fit two CTAs per SM");
+static_assert(sizeof(ConsSmem) + 1024 <= 113 * 1024, "consumer must fit two CTAs per SM");
+
+template <typename OutT>
+static cudaError_t launch_consumer(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                                   const CUtensorMap &mn, const CUtensorMap &mo, const TcParams &prm,
+                                   int grid, cudaStream_t st)
+{
+    const size_t smem = sizeof(ConsSmem) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(lla_readout_consumer_kernel<OutT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    lla_readout_consumer_kernel<OutT><<<grid, kThreads, smem, st>>>(mq, mk, mv, mn, mo, prm);
+    return cudaSuccess;
+}
 
 cudaError_t tc_fwd(const TcFwdArgs &A)
 {
@@ -512,28 +723,31 @@ cudaError_t tc_fwd(const TcFwdArgs &A)
     prm.NT = NT;
     prm.BH = BH;
     prm.L = A.L;
-    CUtensorMap mq, mk, mv, mn;
+    CUtensorMap mq, mk, mv, mn, mn32, mo;
+    const bool out32 = A.out_dt == LLA_F32;
     if (!make_map_bf16_3d(&mq, A.q, kD, A.T, BH, 64, kTile) ||
         !make_map_bf16_3d(&mk, A.k, kD, A.T, BH, 64, kTile) ||
         !make_map_bf16_3d(&mv, A.v, kD, A.T, BH, 64, kTile) ||
-        !make_map_bf16_3d(&mn, prm.node16, kD, kD, (uint64_t)BH * NT, 64, kTile))
+        !make_map_bf16_3d(&mn, prm.node16, kD, kD, (uint64_t)BH * NT, 64, kTile) ||
+        !make_map_f32_3d(&mn32, prm.node32, kD, kD, (uint64_t)BH * NT, 32, kTile) ||
+        !(out32 ? make_map_f32_3d(&mo, A.out, kD, A.T, BH, 32, kTile)
+                : make_map_bf16_3d(&mo, A.out, kD, A.T, BH, 64, kTile)))
         return cudaErrorInvalidValue;
     cudaStream_t st = (cudaStream_t)A.stream;
-    lla_tile_gate_prefix_kernel<<<BH, 256, 0, st>>>(A.g, (double *)prm.P, prm.flags, prm.ticket, prm.err,
-                                                   A.T, NT);
-    const size_t smem = tc_smem_bytes();
+    lla_tile_gate_sum_kernel<<<dim3((NT + 31) / 32, BH), 1024, 0, st>>>(A.g, (double *)prm.P, prm.flags,
+                                                                          prm.ticket, prm.err, A.T, NT);
+    lla_tile_gate_scan_kernel<<<BH, kScanThreads, 0, st>>>((double *)prm.P, NT);
     cudaError_t e;
-    if (A.out_dt == LLA_F32) {
-        e = cudaFuncSetAttribute(lla_fwd_tc_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
+    if (NT > 1) {
+        const size_t psmem = sizeof(ProdSmem) + 1024;
+        e = cudaFuncSetAttribute(lla_node_producer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)psmem);
         if (e != cudaSuccess) return e;
-        lla_fwd_tc_kernel<float><<<BH * NT, kThreads, smem, st>>>(mq, mk, mv, mn, prm);
-    } else {
-        e = cudaFuncSetAttribute(lla_fwd_tc_kernel<__nv_bfloat16>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        lla_fwd_tc_kernel<__nv_bfloat16><<<BH * NT, kThreads, smem, st>>>(mq, mk, mv, mn, prm);
+        lla_node_producer_kernel<<<(NT - 1) * BH, kThreads, psmem, st>>>(mk, mv, mn32, mn, prm);
     }
+    e = out32 ? launch_consumer<float>(mq, mk, mv, mn, mo, prm, NT * BH, st)
+              : launch_consumer<__nv_bfloat16>(mq, mk, mv, mn, mo, prm, NT * BH, st);
+    if (e != cudaSuccess) return e;
     return cudaPeekAtLastError();
 }
 

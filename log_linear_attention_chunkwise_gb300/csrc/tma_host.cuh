@@ -42,4 +42,21 @@ inline bool make_map_bf16_3d(CUtensorMap *map, const void *base, uint64_t n0, ui
     return r == CUDA_SUCCESS;
 }
 
+// The same for fp32 (box0 <= 32 so a box row is at most 128 bytes).
+inline bool make_map_f32_3d(CUtensorMap *map, const void *base, uint64_t n0, uint64_t n1, uint64_t n2,
+                            uint32_t box0, uint32_t box1)
+{
+    auto enc = tensor_map_encoder();
+    if (enc == nullptr) return false;
+    cuuint64_t dims[3] = {n0, n1, n2};
+    cuuint64_t strides[2] = {n0 * 4, n0 * n1 * 4};
+    cuuint32_t box[3] = {box0, box1, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace lla
