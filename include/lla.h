@@ -104,6 +104,30 @@ lla_status lla_fwd(const void *q, const void *k, const void *v,
                    void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * lla_fwd for callers that cannot allocate device memory.  The pages have
+ * no counterpart to this entry point; it exists for code that must not call
+ * cudaMalloc where it runs the forward (inside an allocator or memory-pool
+ * callback, a plugin handed only its input and output buffers, a runtime
+ * that forbids allocation while it records or replays work).
+ * Same arguments, layouts and results as lla_fwd, without the workspace:
+ * the scratch is one fixed array of lla_fwd_noalloc_max_scratch_bytes()
+ * bytes (64 MiB) compiled into the library, present on every GPU that loads
+ * it until the process exits.  A call that needs more scratch than that
+ * (lla_fwd_workspace_bytes(...) > the maximum) returns
+ * LLA_ERR_WORKSPACE_TOO_SMALL and enqueues nothing.  The first call on a
+ * device looks up the array's address with that device current; make it
+ * before any stream capture.  All calls share the array: calls that may
+ * overlap on the GPU race and must be ordered by the caller.  The library
+ * allocates nothing and nothing needs clearing between calls.
+ */
+size_t lla_fwd_noalloc_max_scratch_bytes(void);
+
+lla_status lla_fwd_noalloc(const void *q, const void *k, const void *v,
+                           const float *g, const float *lambda, void *out,
+                           int B, int H, int T, int dk, int dv, int chunk,
+                           lla_dtype in_dt, lla_dtype out_dt, void *stream);
+
+/*
  * Decode state (the recurrent form of "Log-Linear Attention" §2.3: O(log T)
  * states, each step reads and updates O(log T) of them).  For one (b,h) at
  * token index t the state holds the Fenwick buckets of the prefix [0,t):

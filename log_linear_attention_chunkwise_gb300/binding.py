@@ -29,6 +29,8 @@ SIGNATURES = {
     "lla_fwd_workspace_bytes": (_Z, [_I] * 6 + [_I]),
     "lla_fwd_launches": (_I, [_I] * 8),
     "lla_fwd": (_I, [_P] * 6 + [_I] * 6 + [_I, _I] + [_P, _Z, _P]),
+    "lla_fwd_noalloc_max_scratch_bytes": (_Z, []),
+    "lla_fwd_noalloc": (_I, [_P] * 6 + [_I] * 6 + [_I, _I] + [_P]),
     "lla_decode_state_bytes": (_Z, [_I] * 5),
     "lla_decode_step": (_I, [_P] * 9 + [_I] * 5 + [_I, _P, _P]),
     "lla_prefill_workspace_bytes": (_Z, [_I] * 3),
