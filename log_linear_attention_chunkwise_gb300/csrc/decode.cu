@@ -8,6 +8,8 @@
 // token index t iff bit i of t is set.  Keeping the decay as a scalar per slot
 // means a step reads the popcount(t) live slots once and writes one slot,
 // instead of rescaling every live slot in memory.
+#include <cooperative_groups.h>
+
 #include "decode.cuh"
 
 namespace lla {
@@ -16,40 +18,50 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kMaxLs = 40;
 
-// One CTA per (head, sequence) owns all dv columns, so the slot log-decays are
-// read and rewritten by a single CTA.  Thread layout: cg = column group of 4
-// (float4), rg = row group; a thread owns rows rg, rg+R, ... of its 4 columns
-// in every live slot.
-template <typename Tin, int DV, int NT>
-__global__ void __launch_bounds__(NT)
+// One cluster of kParts CTAs per (head, sequence); CTA `part` owns rows
+// [part*dk/kParts, (part+1)*dk/kParts) of every slot, all dv columns.  Thread
+// layout inside a CTA: cg = column group of 4 (float4), rg = row group; a
+// thread owns rows rg, rg+R, ... of its 4 columns.  The partial read-outs
+// are summed through distributed shared memory by CTA 0, which also writes
+// the slot log-decays once every CTA of the cluster has read them.
+constexpr int kParts = 4;
+
+template <typename Tin, int DV>
+__global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kThreads, 4)
 decode_step_kernel(float *__restrict__ S, float *__restrict__ D, const Tin *__restrict__ q,
                    const Tin *__restrict__ k, const Tin *__restrict__ v,
                    const float *__restrict__ g, const float *__restrict__ lam,
                    float *__restrict__ out, const int64_t *__restrict__ pos, int H, int dk,
                    int Ls, int32_t *__restrict__ err)
 {
+    namespace cg = cooperative_groups;
     constexpr int dv = DV;
-    constexpr int NC4 = DV / 4;            // column groups
-    constexpr int R = NT / NC4;            // row groups
-    constexpr int RPT = (128 + R - 1) / R; // rows per thread (dk <= 128)
+    constexpr int NC4 = DV / 4;                 // column groups
+    constexpr int R = kThreads / NC4;           // row groups
+    constexpr int RPT = (128 / kParts + R - 1) / R;  // rows per thread (dk <= 128)
     __shared__ float qs[128], kss[128], vs[DV];
     __shared__ float wl[kMaxLs], el[kMaxLs], dnew[kMaxLs];
     __shared__ float red[R][DV];
+    __shared__ float part_out[DV];
     __shared__ float qk_sh;
 
-    const int h = blockIdx.x, b = blockIdx.y;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int part = (int)cluster.block_rank();
+    const int h = blockIdx.x / kParts, b = blockIdx.y;
     const long long bh = (long long)b * H + h;
     const int64_t t = pos[b];
+    // every CTA of the cluster takes the same branch (same sequence)
     if (t < 0 || bit_length_u64((uint64_t)t + 1) > Ls) {
-        if (threadIdx.x == 0 && err != nullptr) *err = 1 + b;
+        if (part == 0 && threadIdx.x == 0 && err != nullptr) *err = 1 + b;
         return;
     }
     const int tid = threadIdx.x;
-    for (int r = tid; r < dk; r += NT) {
+    const int rows = dk / kParts, row0 = part * rows;
+    for (int r = tid; r < dk; r += kThreads) {
         qs[r] = to_f32(q[bh * dk + r]);
         kss[r] = to_f32(k[bh * dk + r]);
     }
-    for (int c = tid; c < dv; c += NT) vs[c] = to_f32(v[bh * dv + c]);
+    for (int c = tid; c < dv; c += kThreads) vs[c] = to_f32(v[bh * dv + c]);
     const float gg = g[bh];
     if (tid < Ls) {
         const bool live = (t >> tid) & 1;
@@ -60,7 +72,7 @@ decode_step_kernel(float *__restrict__ S, float *__restrict__ D, const Tin *__re
         wl[tid] = live ? lam[bh * (Ls + 1) + tid + 1] * e : 0.f;
     }
     __syncthreads();
-    if (tid < 32) {
+    if (part == 0 && tid < 32) {
         float p = 0.f;
         for (int r = tid; r < dk; r += 32) p = fmaf(qs[r], kss[r], p);
 #pragma unroll
@@ -69,72 +81,89 @@ decode_step_kernel(float *__restrict__ S, float *__restrict__ D, const Tin *__re
     }
 
     const int m = ctz_u64((uint64_t)t + 1);
-    const int cg = tid % NC4, rg = tid / NC4;
-    const int col = cg * 4;
+    const int cg4 = tid % NC4, rg = tid / NC4;
+    const int col = cg4 * 4;
     constexpr int ncol4 = DV / 4;
     float4 mrg[RPT];
 #pragma unroll
     for (int i = 0; i < RPT; i++) mrg[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 
-    for (int l = 0; l < Ls; l++) {
-        if (!((t >> l) & 1)) continue;
-        const float w = wl[l], e = el[l];
-        const bool merge = l < m;
-        const float4 *Sl = reinterpret_cast<const float4 *>(S + ((bh * Ls + l) * (long long)dk) * dv);
-        float4 sv[RPT];
+    // live slots, two per iteration so that two slots' loads are in flight
+    uint64_t live = (uint64_t)t & ((Ls >= 64) ? ~0ull : ((1ull << Ls) - 1));
+    while (live) {
+        const int l0 = ctz_u64(live);
+        live &= live - 1;
+        const int l1 = live ? ctz_u64(live) : -1;
+        if (live) live &= live - 1;
+        const float4 *S0 = reinterpret_cast<const float4 *>(S + ((bh * Ls + l0) * (long long)dk) * dv);
+        const float4 *S1 = reinterpret_cast<const float4 *>(S + ((bh * Ls + (l1 < 0 ? l0 : l1)) * (long long)dk) * dv);
+        float4 sv0[RPT], sv1[RPT];
 #pragma unroll
         for (int i = 0; i < RPT; i++) {
             const int r = rg + R * i;
-            sv[i] = (r < dk) ? __ldcs(Sl + (long long)r * ncol4 + col / 4)
-                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+            const long long idx = (long long)(row0 + r) * ncol4 + cg4;
+            sv0[i] = (r < rows) ? __ldcs(S0 + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
+            sv1[i] = (r < rows && l1 >= 0) ? __ldcs(S1 + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+        const float w0 = wl[l0], e0 = (l0 < m) ? el[l0] : 0.f;
+        const float w1 = l1 >= 0 ? wl[l1] : 0.f, e1 = (l1 >= 0 && l1 < m) ? el[l1] : 0.f;
 #pragma unroll
         for (int i = 0; i < RPT; i++) {
             const int r = rg + R * i;
-            const float qw = (r < dk) ? qs[r] * w : 0.f;
-            acc.x = fmaf(qw, sv[i].x, acc.x);
-            acc.y = fmaf(qw, sv[i].y, acc.y);
-            acc.z = fmaf(qw, sv[i].z, acc.z);
-            acc.w = fmaf(qw, sv[i].w, acc.w);
-            if (merge) {
-                mrg[i].x = fmaf(e, sv[i].x, mrg[i].x);
-                mrg[i].y = fmaf(e, sv[i].y, mrg[i].y);
-                mrg[i].z = fmaf(e, sv[i].z, mrg[i].z);
-                mrg[i].w = fmaf(e, sv[i].w, mrg[i].w);
-            }
+            const float qr = (r < rows) ? qs[row0 + r] : 0.f;
+            const float a0 = qr * w0, a1 = qr * w1;
+            acc.x = fmaf(a1, sv1[i].x, fmaf(a0, sv0[i].x, acc.x));
+            acc.y = fmaf(a1, sv1[i].y, fmaf(a0, sv0[i].y, acc.y));
+            acc.z = fmaf(a1, sv1[i].z, fmaf(a0, sv0[i].z, acc.z));
+            acc.w = fmaf(a1, sv1[i].w, fmaf(a0, sv0[i].w, acc.w));
+            // slots below m are carried into the new slot (e = 0 for the others)
+            mrg[i].x = fmaf(e1, sv1[i].x, fmaf(e0, sv0[i].x, mrg[i].x));
+            mrg[i].y = fmaf(e1, sv1[i].y, fmaf(e0, sv0[i].y, mrg[i].y));
+            mrg[i].z = fmaf(e1, sv1[i].z, fmaf(e0, sv0[i].z, mrg[i].z));
+            mrg[i].w = fmaf(e1, sv1[i].w, fmaf(e0, sv0[i].w, mrg[i].w));
         }
     }
     red[rg][col + 0] = acc.x;
     red[rg][col + 1] = acc.y;
     red[rg][col + 2] = acc.z;
     red[rg][col + 3] = acc.w;
-    // the new slot m (level m+1) is dead at t, so no thread of this step reads it
+    // the new slot m (level m+1) is dead at t, so no CTA of this step reads it
     {
         float4 *Sm = reinterpret_cast<float4 *>(S + ((bh * Ls + m) * (long long)dk) * dv);
         const float4 vv = make_float4(vs[col], vs[col + 1], vs[col + 2], vs[col + 3]);
 #pragma unroll
         for (int i = 0; i < RPT; i++) {
             const int r = rg + R * i;
-            if (r < dk) {
-                const float kr = kss[r];
+            if (r < rows) {
+                const float kr = kss[row0 + r];
                 float4 o;
                 o.x = fmaf(kr, vv.x, mrg[i].x);
                 o.y = fmaf(kr, vv.y, mrg[i].y);
                 o.z = fmaf(kr, vv.z, mrg[i].z);
                 o.w = fmaf(kr, vv.w, mrg[i].w);
-                __stcs(Sm + (long long)r * ncol4 + col / 4, o);
+                __stcs(Sm + (long long)(row0 + r) * ncol4 + cg4, o);
             }
         }
     }
     __syncthreads();
-    for (int c = tid; c < DV; c += NT) {
+    for (int c = tid; c < DV; c += kThreads) {
         float o = 0.f;
 #pragma unroll 4
         for (int r = 0; r < R; r++) o += red[r][c];
-        out[bh * dv + c] = o + lam[bh * (Ls + 1)] * qk_sh * vs[c];
+        part_out[c] = o;
     }
-    if (tid < Ls) D[bh * Ls + tid] = (tid == m) ? 0.f : dnew[tid];
+    cluster.sync();  // partials ready; every CTA has read the old log-decays
+    if (part == 0) {
+        for (int c = tid; c < DV; c += kThreads) {
+            float o = lam[bh * (Ls + 1)] * qk_sh * vs[c];
+#pragma unroll
+            for (int p2 = 0; p2 < kParts; p2++) o += cluster.map_shared_rank(part_out, p2)[c];
+            out[bh * dv + c] = o;
+        }
+        if (tid < Ls) D[bh * Ls + tid] = (tid == m) ? 0.f : dnew[tid];
+    }
+    cluster.sync();  // keep every CTA's partials alive until CTA 0 has read them
 }
 
 // tail[bh][s] = sum_{r=s+1}^{T-1} g[bh][r] (accumulated in fp64, stored fp32).
@@ -234,22 +263,22 @@ prefill_bucket_kernel(const Tin *__restrict__ k, const Tin *__restrict__ v,
             if (a < RB && b < CB) atomicAdd(Sl + (ty + 16 * a) * dv + tx + 16 * b, acc[a][b]);
 }
 
-template <typename Tin, int DV, int NT>
+template <typename Tin, int DV>
 void launch_decode_dv(const DecodeArgs &A)
 {
-    decode_step_kernel<Tin, DV, NT><<<dim3(A.H, A.B), NT, 0, (cudaStream_t)A.stream>>>(
-        A.S, A.D, (const Tin *)A.q, (const Tin *)A.k, (const Tin *)A.v, A.g, A.lam, A.out,
-        A.pos, A.H, A.dk, A.Ls, A.err);
+    decode_step_kernel<Tin, DV><<<dim3(A.H * kParts, A.B), kThreads, 0, (cudaStream_t)A.stream>>>(
+        A.S, A.D, (const Tin *)A.q, (const Tin *)A.k, (const Tin *)A.v, A.g, A.lam, A.out, A.pos,
+        A.H, A.dk, A.Ls, A.err);
 }
 
 template <typename Tin>
 cudaError_t launch_decode(const DecodeArgs &A)
 {
     switch (A.dv) {
-    case 16: launch_decode_dv<Tin, 16, 256>(A); break;
-    case 32: launch_decode_dv<Tin, 32, 256>(A); break;
-    case 64: launch_decode_dv<Tin, 64, 256>(A); break;
-    default: launch_decode_dv<Tin, 128, 512>(A); break;
+    case 16: launch_decode_dv<Tin, 16>(A); break;
+    case 32: launch_decode_dv<Tin, 32>(A); break;
+    case 64: launch_decode_dv<Tin, 64>(A); break;
+    default: launch_decode_dv<Tin, 128>(A); break;
     }
     return cudaPeekAtLastError();
 }
