@@ -50,57 +50,18 @@ constexpr int kMaxPath = 17;               // levels of a tile index (T <= 2^24,
 // Error codes written to the workspace error word.
 constexpr int kErrLoadTimeout = 1;
 constexpr int kErrMmaTimeout = 2;
-constexpr int kErrNodeTimeout = 3;
 
 struct TcParams {
     const float *g, *lam;
     void *out;
-    const double *P;   // [BH][NT+1]
-    int *flags;        // [BH][NT+1]
-    int *ticket;
-    int *err;
-    float *node32;     // [BH][NT][128][128]
-    __nv_bfloat16 *node16;
-    int T, NT, BH, L;
+    const double *P;        // [BH][NT+1] tile-gate prefix sums
+    int *err;               // first bounded wait that gave up (0: none)
+    float *segtot;          // [BH][nseg_full][128][128] decayed segment totals
+    __nv_bfloat16 *node16;  // [BH][NT][128][128] Fenwick nodes (index 0 unused)
+    int T, NT, BH, L, nseg_full;
 };
 
 __device__ __forceinline__ void set_err(int *err, int code) { atomicCAS(err, 0, code); }
-
-// Acquire-load of a publication flag, bounded.
-__device__ __forceinline__ bool wait_flag(const int *flag, uint32_t max_iter)
-{
-    for (uint32_t it = 0; it < max_iter; it++) {
-        int v;
-        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
-        if (v != 0) return true;
-        __nanosleep(it < 32 ? 32 : 256);
-    }
-    return false;
-}
-
-__device__ __forceinline__ void release_flag(int *flag)
-{
-    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(flag), "r"(1) : "memory");
-}
-
-// Block `blk` (64 columns) of row `row` of a 128x128 bf16 operand stored as
-// two 64-column 128B-swizzled blocks: scale by w into the same place in dst.
-__device__ __forceinline__ void scale_row_half(const uint8_t *src, uint8_t *dst, int row, int blk,
-                                               float w)
-{
-#pragma unroll
-    for (int c = 0; c < 8; c++) {
-        const uint32_t off = blk * kHalf + row * 128 + c * 16;
-        uint4 raw = *reinterpret_cast<const uint4 *>(src + off);
-        __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&raw);
-#pragma unroll
-        for (int u = 0; u < 4; u++) {
-            float2 f = __bfloat1622float2(h[u]);
-            h[u] = __floats2bfloat162_rn(f.x * w, f.y * w);
-        }
-        *reinterpret_cast<uint4 *>(dst + off) = raw;
-    }
-}
 
 // 8 MMAs over K = 128: A and B K-major (rows of 128 B, K split in two blocks).
 __device__ __forceinline__ void mma_kk(uint32_t d, const uint8_t *a, const uint8_t *b, uint32_t idesc)
@@ -125,18 +86,6 @@ __device__ __forceinline__ void mma_kmn(uint32_t d, const uint8_t *a, const uint
     }
 }
 
-// 8 MMAs over K = 128 with A and B MN-major (rows = K index).
-__device__ __forceinline__ void mma_mnmn(uint32_t d, const uint8_t *a, const uint8_t *b,
-                                         uint32_t idesc)
-{
-#pragma unroll
-    for (int kk = 0; kk < 8; kk++) {
-        const uint32_t off = kk * 2048;
-        umma_bf16(d, desc_sw128(smem_u32(a) + off, kHalf, 1024),
-                  desc_sw128(smem_u32(b) + off, kHalf, 1024), idesc, kk > 0 ? 1u : 0u);
-    }
-}
-
 // Inclusive running sum of the tile's gates: thread (row, half) gets
 // gamma_row; also returns the tile total Gam.  `wsum` is 4 floats of smem.
 __device__ __forceinline__ float tile_cumsum(float gv, float *wsum, float &Gam)
@@ -156,21 +105,18 @@ __device__ __forceinline__ float tile_cumsum(float gv, float *wsum, float &Gam)
     return base + incl;
 }
 
-// ======================================================= node producer
-// CTA per tile i < NT-1 (tickets in tile-major order): Node_{i+1}.
-// Nodes move through shared memory by TMA: the fp32 node (the chain's
-// operand) as four 32-column boxes, the bf16 copy (the read-out's MMA
-// operand) as two 64-column boxes, all 128-byte swizzled.
-
-struct __align__(1024) ProdSmem {
-    uint8_t k[kBuf];   // K; then, with v, the fp32 staging of a node (64 KB)
-    uint8_t v[kBuf];
-    uint8_t vs[kBuf];  // V scaled by the decay; then the bf16 staging of the node
-    float wsum[4];
-    uint64_t bar_load, bar_mma, bar_dep;
-    uint32_t tmem;
-    int ticket;
-};
+// ======================================================= node walkers
+// The tile-level Fenwick nodes Node_j (j = 1 .. NT-1) are built by walkers:
+// one CTA per (batch*head, 32-column slice of dv, segment of 64 tiles) goes
+// through its segment in order.  For tile i it forms H_i's slice on the
+// tensor cores and closes Node_{i+1}:
+//     Node_{i+1} = H_i + sum_{m < ctz(i+1)} exp(P_{i+1} - P_{i+1-2^m}) Node_{i+1-2^m},
+// keeping the latest node of each level (the Fenwick stack) in fp32 in
+// tensor memory, so nothing crosses CTAs and nothing waits.  Only the node
+// that closes a full segment reaches back before the segment; the walker
+// writes that segment's decayed total instead, and the fix-up kernel chains
+// the totals at segment granularity.  Nodes are published in bf16, the
+// read-out's MMA operand.
 
 // fp32 128x128 tile staged as four 32-column boxes of 128 rows x 128 B:
 // byte offset of the 4-float chunk holding columns [4c, 4c+4) of row r.
@@ -179,141 +125,185 @@ __device__ __forceinline__ uint32_t f32_stage_off(int r, int c)
     return (uint32_t)(c >> 3) * (kTile * 128) + sw128_offset(r, c & 7);
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
-lla_node_producer_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
-                         const __grid_constant__ CUtensorMap map_n32, const __grid_constant__ CUtensorMap map_n16,
-                         const TcParams prm)
+constexpr int kSliceW = 32;              // dv columns per walker
+constexpr int kSlices = kD / kSliceW;
+constexpr int kSegLog = 6;
+constexpr int kSeg = 1 << kSegLog;       // tiles per segment
+constexpr int kWalkThreads = 128;        // thread = token row (scaling) / dk row (epilogue)
+
+struct __align__(1024) WalkSmem {
+    uint8_t k[2][kBuf];   // K tiles, double-buffered
+    uint8_t v[2][kHalf];  // the 64-column V block holding the slice, double-buffered
+    float wsum[4];
+    uint64_t bar_load[2], bar_h[2];
+    uint32_t tmem;
+};
+
+__global__ void __launch_bounds__(kWalkThreads, 2)
+lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                       const TcParams prm)
 {
     extern __shared__ uint8_t smem_raw[];
-    ProdSmem &s = *reinterpret_cast<ProdSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+    WalkSmem &s = *reinterpret_cast<WalkSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
-    const int row = tid & (kTile - 1);
-    const int half = tid >> 7;
+    const int seg = blockIdx.x, slice = blockIdx.y, bh = blockIdx.z;
+    const int NT = prm.NT;
+    const int i0 = seg * kSeg, i1 = min(i0 + kSeg, NT - 1);  // tiles i0..i1-1 close Node_{i+1}
+    const double *Pb = prm.P + (long long)bh * (NT + 1);
+    const int vblk = slice >> 1;                 // 64-column V block holding the slice
+    const uint32_t voff = (uint32_t)(slice & 1) * 64;  // the slice's byte offset in a block row
 
     if (tid == 0) {
-        mbar_init(&s.bar_load, 1);
-        mbar_init(&s.bar_mma, 1);
-        mbar_init(&s.bar_dep, 1);
+        for (int b = 0; b < 2; b++) {
+            mbar_init(&s.bar_load[b], 1);
+            mbar_init(&s.bar_h[b], 1);
+        }
         fence_mbar_init();
         tma_prefetch_map(&map_k);
         tma_prefetch_map(&map_v);
-        tma_prefetch_map(&map_n32);
-        tma_prefetch_map(&map_n16);
     }
     if (warp == 0) {
-        tmem_alloc(&s.tmem, 128);
+        tmem_alloc(&s.tmem, 256);
         tmem_relinquish();
     }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
-    // the ticket is taken once this CTA holds its tensor memory, so a tile
-    // with a ticket never waits on a CTA that cannot make progress
-    if (tid == 0) s.ticket = atomicAdd(prm.ticket, 1);
-    __syncthreads();
     const uint32_t tm = s.tmem;
-    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const int NT = prm.NT, BH = prm.BH;
-    const int ticket = s.ticket;
-    if (ticket >= (NT - 1) * BH) {
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    // columns: stack level m at [32m, 32m+32) for m < kSegLog; H buffers after it
+    const uint32_t tm_h0 = tm + kSegLog * kSliceW;
+
+    auto issue_load = [&](int i, int st) {
+        mbar_arrive_expect_tx(&s.bar_load[st], kBuf + kHalf);
+        tma_load_3d(s.k[st], &map_k, &s.bar_load[st], 0, i * kTile, bh);
+        tma_load_3d(s.k[st] + kHalf, &map_k, &s.bar_load[st], 64, i * kTile, bh);
+        tma_load_3d(s.v[st], &map_v, &s.bar_load[st], vblk * 64, i * kTile, bh);
+    };
+    if (tid == 0 && i0 < i1) issue_load(i0, 0);
+
+    for (int i = i0; i < i1; i++) {
+        const int n = i - i0, st = n & 1;
+        // the other stage was last used by tile i-1, whose product is complete
+        if (tid == 0 && i + 1 < i1) issue_load(i + 1, st ^ 1);
+        // tiles before NT-1 are full: no ragged rows here
+        const long long tok = (long long)bh * prm.T + (long long)i * kTile + tid;
+        float Gam;
+        const float gam_a = tile_cumsum(prm.g[tok], s.wsum, Gam);
+        if (!mbar_wait(&s.bar_load[st], (n >> 1) & 1, kWaitIters)) set_err(prm.err, kErrLoadTimeout);
+        {   // V row `tid` of the slice, scaled in place by exp(Gam - gamma)
+            const float w = __expf(Gam - gam_a);
+            uint8_t *vrow = s.v[st];
+#pragma unroll
+            for (int c = 0; c < 4; c++) {
+                uint4 *p = reinterpret_cast<uint4 *>(vrow + sw128_offset(tid, (voff >> 4) + c));
+                uint4 raw = *p;
+                __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&raw);
+#pragma unroll
+                for (int u = 0; u < 4; u++) {
+                    float2 f = __bfloat1622float2(h[u]);
+                    h[u] = __floats2bfloat162_rn(f.x * w, f.y * w);
+                }
+                *p = raw;
+            }
+        }
+        fence_proxy_async_smem();
         tc_fence_before_sync();
         __syncthreads();
-        if (warp == 0) tmem_dealloc(tm, 128);
-        return;
-    }
-    const int i = ticket / BH;
-    const int bh = ticket - i * BH;
-    const double *Pb = prm.P + (long long)bh * (NT + 1);
-    int *flags = prm.flags + (long long)bh * (NT + 1);
-
-    if (tid == 0) {
-        mbar_arrive_expect_tx(&s.bar_load, 2 * kBuf);
-#pragma unroll
-        for (int h = 0; h < 2; h++) {
-            tma_load_3d(s.k + h * kHalf, &map_k, &s.bar_load, h * 64, i * kTile, bh);
-            tma_load_3d(s.v + h * kHalf, &map_v, &s.bar_load, h * 64, i * kTile, bh);
-        }
-    }
-    // tiles i < NT-1 are full: no ragged rows here
-    const long long tok = (long long)bh * prm.T + (long long)i * kTile + row;
-    float Gam;
-    const float gam_a = tile_cumsum(prm.g[tok], s.wsum, Gam);
-    if (!mbar_wait(&s.bar_load, 0, kWaitIters)) set_err(prm.err, kErrLoadTimeout);
-    scale_row_half(s.v, s.vs, row, half, __expf(Gam - gam_a));
-    fence_proxy_async_smem();
-    tc_fence_before_sync();
-    __syncthreads();
-    if (tid == 0) {
-        tc_fence_after_sync();
-        mma_mnmn(tm, s.k, s.vs, idesc_bf16_f32(128, 128, true, true));
-        umma_commit(&s.bar_mma);
-    }
-    const int z = __ffs(i + 1) - 1;  // ctz(i+1): the lower-level nodes folded in
-    if (!mbar_wait(&s.bar_mma, 0, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
-    tc_fence_after_sync();
-    // H row (dk index `row`), columns [64*half, 64*half + 64)
-    float r[64];
-#pragma unroll
-    for (int c0 = 0; c0 < 64; c0 += 16)
-        tmem_ld16(tm + lane_off + half * 64 + c0, *reinterpret_cast<float(*)[16]>(r + c0));
-    tmem_ld_wait();
-    tc_fence_before_sync();
-    __syncthreads();  // K, V and Vs are free from here on
-
-    // Node_{i+1} = H + sum_{m<z} exp(P_{i+1} - P_{j_m}) Node_{j_m},  j_m = i + 1 - 2^m
-    const double Pn = Pb[i + 1];
-    uint8_t *stage32 = s.k;  // 64 KB across k and v
-    for (int m = 0; m < z; m++) {
-        const int j = i + 1 - (1 << m);
         if (tid == 0) {
-            if (!wait_flag(flags + j, kWaitIters)) set_err(prm.err, kErrNodeTimeout);
-            fence_proxy_async_global();
-            mbar_arrive_expect_tx(&s.bar_dep, 2 * kBuf);
+            tc_fence_after_sync();
+            // H slice = K^T Vs: A = K^T (M = dk, MN-major), B = Vs slice (N = 32, MN-major)
+            const uint32_t idesc = idesc_bf16_f32(128, kSliceW, true, true);
 #pragma unroll
-            for (int b = 0; b < 4; b++)
-                tma_load_3d(stage32 + b * (kTile * 128), &map_n32, &s.bar_dep, b * 32, 0, bh * NT + j);
+            for (int kk = 0; kk < 8; kk++) {
+                const uint32_t off = kk * 2048;
+                umma_bf16(tm_h0 + st * kSliceW, desc_sw128(smem_u32(s.k[st]) + off, kHalf, 1024),
+                          desc_sw128(smem_u32(s.v[st]) + voff + off, kHalf, 1024), idesc,
+                          kk > 0 ? 1u : 0u);
+            }
+            umma_commit(&s.bar_h[st]);
         }
-        const float f = __expf((float)(Pn - Pb[j]));
-        if (!mbar_wait(&s.bar_dep, m & 1, kWaitIters)) set_err(prm.err, kErrLoadTimeout);
+        if (!mbar_wait(&s.bar_h[st], (n >> 1) & 1, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
+        tc_fence_after_sync();
+
+        // epilogue: thread = dk row `tid`, the slice's 32 columns
+        const int J = i + 1;
+        const int z = __ffs(J) - 1;
+        const bool cross = (J == i0 + kSeg);  // closes a full segment
+        const int mlim = cross ? kSegLog : z;
+        float acc[32];
+        tmem_ld16(tm_h0 + st * kSliceW + lane_off, *reinterpret_cast<float(*)[16]>(acc));
+        tmem_ld16(tm_h0 + st * kSliceW + lane_off + 16, *reinterpret_cast<float(*)[16]>(acc + 16));
+        tmem_ld_wait();
+        const double PJ = Pb[J];
+        for (int m = 0; m < mlim; m++) {
+            const float f = __expf((float)(PJ - Pb[J - (1 << m)]));
+            float x[32];
+            tmem_ld16(tm + m * kSliceW + lane_off, *reinterpret_cast<float(*)[16]>(x));
+            tmem_ld16(tm + m * kSliceW + lane_off + 16, *reinterpret_cast<float(*)[16]>(x + 16));
+            tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 16; c++) {
-            const float4 x = *reinterpret_cast<const float4 *>(stage32 + f32_stage_off(row, half * 16 + c));
-            r[4 * c] = fmaf(f, x.x, r[4 * c]);
-            r[4 * c + 1] = fmaf(f, x.y, r[4 * c + 1]);
-            r[4 * c + 2] = fmaf(f, x.z, r[4 * c + 2]);
-            r[4 * c + 3] = fmaf(f, x.w, r[4 * c + 3]);
+            for (int u = 0; u < 32; u++) acc[u] = fmaf(f, x[u], acc[u]);
         }
-        __syncthreads();  // the staging buffer is reused by the next load
+        if (!cross) {
+            if (z < kSegLog) {
+                tmem_st16(tm + z * kSliceW + lane_off, *reinterpret_cast<float(*)[16]>(acc));
+                tmem_st16(tm + z * kSliceW + lane_off + 16, *reinterpret_cast<float(*)[16]>(acc + 16));
+                tmem_st_wait();
+            }
+            uint4 w[4];
+            __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(w);
+#pragma unroll
+            for (int u = 0; u < 16; u++) h[u] = __floats2bfloat162_rn(acc[2 * u], acc[2 * u + 1]);
+            uint4 *dst = reinterpret_cast<uint4 *>(prm.node16 + (((long long)bh * NT + J) * kD + tid) * kD +
+                                                   slice * kSliceW);
+#pragma unroll
+            for (int u = 0; u < 4; u++) dst[u] = w[u];
+        } else {
+            float4 *dst = reinterpret_cast<float4 *>(
+                prm.segtot + ((((long long)bh * prm.nseg_full + seg) * kD + tid) * kD + slice * kSliceW));
+#pragma unroll
+            for (int u = 0; u < 8; u++) dst[u] = make_float4(acc[4 * u], acc[4 * u + 1], acc[4 * u + 2], acc[4 * u + 3]);
+        }
+        tc_fence_before_sync();
+        __syncthreads();  // stack and H buffer settled before the next tile
+        tc_fence_after_sync();
     }
-    // stage the node: fp32 in k/v, bf16 in vs (block `half`, 8 chunks of 8 columns)
-#pragma unroll
-    for (int c = 0; c < 16; c++)
-        *reinterpret_cast<float4 *>(stage32 + f32_stage_off(row, half * 16 + c)) =
-            make_float4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
-#pragma unroll
-    for (int c = 0; c < 8; c++) {
-        uint4 w;
-        __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&w);
-#pragma unroll
-        for (int u = 0; u < 4; u++) h[u] = __floats2bfloat162_rn(r[8 * c + 2 * u], r[8 * c + 2 * u + 1]);
-        *reinterpret_cast<uint4 *>(s.vs + half * kHalf + sw128_offset(row, c)) = w;
-    }
-    fence_proxy_async_smem();
+    tc_fence_before_sync();
     __syncthreads();
-    if (tid == 0) {
+    if (warp == 0) tmem_dealloc(tm, 256);
+}
+
+// Nodes that close full segments: Fenwick chain over the segment totals,
+//   Node_{(u)SEG} = Tot_{u-1} + sum_{k < ctz(u)} exp(P_{uSEG} - P_{(u-2^k)SEG}) Node_{(u-2^k)SEG},
+// one thread per state element, the open node of each level in registers.
+constexpr int kFixThreads = 256;
+constexpr int kFixMaxZ = 20;
+__global__ void __launch_bounds__(kFixThreads)
+lla_node_fixup_kernel(const TcParams prm)
+{
+    const int e = blockIdx.x * kFixThreads + threadIdx.x;  // element of the 128x128 state
+    const long long bh = blockIdx.y;
+    if (e >= kD * kD) return;
+    const int NT = prm.NT;
+    const double *Pb = prm.P + bh * (NT + 1);
+    float stack[kFixMaxZ];
 #pragma unroll
-        for (int b = 0; b < 4; b++) tma_store_3d(&map_n32, stage32 + b * (kTile * 128), b * 32, 0, bh * NT + i + 1);
+    for (int k = 0; k < kFixMaxZ; k++) stack[k] = 0.f;
+    for (int u = 1; u <= prm.nseg_full; u++) {
+        const int J = u * kSeg;
+        const int z = __ffs(u) - 1;
+        float val = prm.segtot[((bh * prm.nseg_full) + (u - 1)) * (kD * kD) + e];
 #pragma unroll
-        for (int h = 0; h < 2; h++) tma_store_3d(&map_n16, s.vs + h * kHalf, h * 64, 0, bh * NT + i + 1);
-        tma_store_commit();
-        tma_store_wait_all();
-        fence_proxy_async_global();
-        __threadfence();
-        release_flag(flags + i + 1);
+        for (int k = 0; k < kFixMaxZ; k++)
+            if (k < z) val = fmaf(__expf((float)(Pb[J] - Pb[J - (1 << k) * kSeg])), stack[k], val);
+#pragma unroll
+        for (int k = 0; k < kFixMaxZ; k++)
+            if (k == z) stack[k] = val;
+        prm.node16[(bh * NT + J) * (kD * kD) + e] = __float2bfloat16_rn(val);
     }
-    if (warp == 0) tmem_dealloc(tm, 128);
 }
 
 // ======================================================= read-out consumer
@@ -586,19 +576,18 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
 
 // Gate sums, in two small launches.  First, a warp per tile: Gam_i in fp64
 // from one coalesced float4 load per lane, stored in the P array shifted by
-// one (P[i+1] = Gam_i); the producer's flags and ticket are reset here too.
+// one (P[i+1] = Gam_i); the workspace error word is reset here too.
 // Then one CTA per (batch*head) turns the tile sums into the prefix
 // P_i = Gam_0 + ... + Gam_{i-1} in place.
 constexpr int kScanThreads = 1024;
 __global__ void __launch_bounds__(1024)
-lla_tile_gate_sum_kernel(const float *__restrict__ g, double *__restrict__ P, int *__restrict__ flags,
-                         int *__restrict__ ticket, int *__restrict__ err, int T, int NT)
+lla_tile_gate_sum_kernel(const float *__restrict__ g, double *__restrict__ P, int *__restrict__ err, int T,
+                         int NT)
 {
     const long long bh = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = blockIdx.x * 32 + warp;
     double *Pb = P + bh * (long long)(NT + 1);
-    int *fb = flags + bh * (long long)(NT + 1);
     if (tile < NT) {
         const float *gb = g + bh * (long long)T + (long long)tile * kTile;
         const int n = min(kTile, T - tile * kTile);
@@ -611,18 +600,11 @@ lla_tile_gate_sum_kernel(const float *__restrict__ g, double *__restrict__ P, in
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (lane == 0) {
-            Pb[tile + 1] = acc;
-            fb[tile + 1] = 0;
-        }
+        if (lane == 0) Pb[tile + 1] = acc;
     }
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         Pb[0] = 0.0;
-        fb[0] = 0;
-        if (bh == 0) {
-            *ticket = 0;
-            *err = 0;
-        }
+        if (bh == 0) *err = 0;
     }
 }
 
@@ -667,13 +649,13 @@ lla_tile_gate_scan_kernel(double *__restrict__ P, int NT)
 
 }  // namespace
 
-// Workspace: [P fp64 BH*(NT+1)] [flags int BH*(NT+1)] [ticket, err] [node32] [node16]
-static size_t off_flags(int BH, int NT) { return align_up((size_t)BH * (NT + 1) * 8, 256); }
-static size_t off_ticket(int BH, int NT) { return off_flags(BH, NT) + align_up((size_t)BH * (NT + 1) * 4, 256); }
-static size_t off_node32(int BH, int NT) { return off_ticket(BH, NT) + 256; }
+// Workspace: [P fp64 BH*(NT+1)] [err word] [segment totals fp32] [nodes bf16]
+static int nseg_full_of(int NT) { return NT > 1 ? (NT - 1) / kSeg : 0; }
+static size_t off_err(int BH, int NT) { return align_up((size_t)BH * (NT + 1) * 8, 256); }
+static size_t off_segtot(int BH, int NT) { return off_err(BH, NT) + 256; }
 static size_t off_node16(int BH, int NT)
 {
-    return off_node32(BH, NT) + align_up((size_t)BH * NT * kD * kD * 4, 1024);
+    return off_segtot(BH, NT) + align_up((size_t)BH * nseg_full_of(NT) * kD * kD * 4, 1024);
 }
 
 size_t tc_workspace_bytes(int B, int H, int T)
@@ -689,7 +671,14 @@ bool tc_supported(int dk, int dv, lla_dtype in_dt)
 
 size_t tc_smem_bytes() { return sizeof(ConsSmem) + 1024; }
 
-static_assert(sizeof(ProdSmem) + 1024 <= 113 * 1024, "producer must fit two CTAs per SM");
+int tc_launches(int T)
+{
+    const int NT = (T + kTile - 1) / kTile;
+    if (NT <= 1) return 3;                          // gate sum, gate scan, read-out
+    return 4 + (nseg_full_of(NT) > 0 ? 1 : 0);      // + walkers (+ segment fix-up)
+}
+
+static_assert(sizeof(WalkSmem) + 1024 <= 113 * 1024, "walker must fit two CTAs per SM");
 static_assert(sizeof(ConsSmem) + 1024 <= 113 * 1024, "consumer must fit two CTAs per SM");
 
 template <typename OutT>
@@ -714,36 +703,37 @@ cudaError_t tc_fwd(const TcFwdArgs &A)
     prm.lam = A.lam;
     prm.out = A.out;
     prm.P = (const double *)ws;
-    prm.flags = (int *)(ws + off_flags(BH, NT));
-    prm.ticket = (int *)(ws + off_ticket(BH, NT));
-    prm.err = prm.ticket + 1;
-    prm.node32 = (float *)(ws + off_node32(BH, NT));
+    prm.err = (int *)(ws + off_err(BH, NT));
+    prm.segtot = (float *)(ws + off_segtot(BH, NT));
     prm.node16 = (__nv_bfloat16 *)(ws + off_node16(BH, NT));
     prm.T = A.T;
     prm.NT = NT;
     prm.BH = BH;
     prm.L = A.L;
-    CUtensorMap mq, mk, mv, mn, mn32, mo;
+    prm.nseg_full = nseg_full_of(NT);
+    CUtensorMap mq, mk, mv, mn, mo;
     const bool out32 = A.out_dt == LLA_F32;
     if (!make_map_bf16_3d(&mq, A.q, kD, A.T, BH, 64, kTile) ||
         !make_map_bf16_3d(&mk, A.k, kD, A.T, BH, 64, kTile) ||
         !make_map_bf16_3d(&mv, A.v, kD, A.T, BH, 64, kTile) ||
         !make_map_bf16_3d(&mn, prm.node16, kD, kD, (uint64_t)BH * NT, 64, kTile) ||
-        !make_map_f32_3d(&mn32, prm.node32, kD, kD, (uint64_t)BH * NT, 32, kTile) ||
         !(out32 ? make_map_f32_3d(&mo, A.out, kD, A.T, BH, 32, kTile)
                 : make_map_bf16_3d(&mo, A.out, kD, A.T, BH, 64, kTile)))
         return cudaErrorInvalidValue;
     cudaStream_t st = (cudaStream_t)A.stream;
-    lla_tile_gate_sum_kernel<<<dim3((NT + 31) / 32, BH), 1024, 0, st>>>(A.g, (double *)prm.P, prm.flags,
-                                                                          prm.ticket, prm.err, A.T, NT);
+    lla_tile_gate_sum_kernel<<<dim3((NT + 31) / 32, BH), 1024, 0, st>>>(A.g, (double *)prm.P, prm.err,
+                                                                          A.T, NT);
     lla_tile_gate_scan_kernel<<<BH, kScanThreads, 0, st>>>((double *)prm.P, NT);
     cudaError_t e;
     if (NT > 1) {
-        const size_t psmem = sizeof(ProdSmem) + 1024;
-        e = cudaFuncSetAttribute(lla_node_producer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)psmem);
+        const size_t wsmem = sizeof(WalkSmem) + 1024;
+        e = cudaFuncSetAttribute(lla_node_walker_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)wsmem);
         if (e != cudaSuccess) return e;
-        lla_node_producer_kernel<<<(NT - 1) * BH, kThreads, psmem, st>>>(mk, mv, mn32, mn, prm);
+        const int nseg = (NT - 1 + kSeg - 1) / kSeg;
+        lla_node_walker_kernel<<<dim3(nseg, kSlices, BH), kWalkThreads, wsmem, st>>>(mk, mv, prm);
+        if (prm.nseg_full > 0)
+            lla_node_fixup_kernel<<<dim3(kD * kD / kFixThreads, BH), kFixThreads, 0, st>>>(prm);
     }
     e = out32 ? launch_consumer<float>(mq, mk, mv, mn, mo, prm, NT * BH, st)
               : launch_consumer<__nv_bfloat16>(mq, mk, mv, mn, mo, prm, NT * BH, st);

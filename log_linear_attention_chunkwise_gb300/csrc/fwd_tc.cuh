@@ -20,6 +20,7 @@ struct TcFwdArgs {
 bool tc_supported(int dk, int dv, lla_dtype in_dt);
 size_t tc_workspace_bytes(int B, int H, int T);
 size_t tc_smem_bytes();
+int tc_launches(int T);
 cudaError_t tc_fwd(const TcFwdArgs &A);
 
 }  // namespace lla

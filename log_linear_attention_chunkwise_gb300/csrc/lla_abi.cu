@@ -81,7 +81,7 @@ int lla_fwd_launches(int B, int H, int T, int dk, int dv, int chunk, lla_dtype i
     if (out_dt != LLA_F32 && out_dt != LLA_BF16) return 0;
     if (in_dt == LLA_F32 && out_dt != LLA_F32) return 0;
     if ((long long)B * H * T == 0) return 0;
-    if (tc_supported(dk, dv, in_dt)) return T > 128 ? 4 : 3;
+    if (tc_supported(dk, dv, in_dt)) return tc_launches(T);
     return T / chunk > 1 ? 4 : 3;
 }
 
