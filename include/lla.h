@@ -183,6 +183,21 @@ lla_status lla_prefill_state(const void *k, const void *v, const float *g,
                              lla_dtype in_dt, void *workspace,
                              size_t workspace_bytes, void *stream);
 
+/*
+ * Level weights from a two-layer MLP ("Adaptive memory decay for Log-Linear
+ * Attention", §Method "LambdaMLPSoftplus"): for every (token, head),
+ *     h = d W1 (width 2L, no activation),   lambda = softplus(h W2 + b),
+ * so lambda >= 0 with every level scaled independently.  W2 = 0, b = 0.54
+ * gives softplus(0.54), about 1.0, everywhere (the page's initialisation).
+ *   d      [B,H,T,Dd] in_dt   the per-(token, head) input representation
+ *   W1     [Dd, 2L]  fp32     W2 [2L, L] fp32     b [L] fp32 (shared by heads)
+ *   lambda [B,H,T,L] fp32     output, the layout lla_fwd reads
+ * Supported: 1 <= Dd <= 256, 1 <= L <= 32 (shared memory holds the weights).
+ */
+lla_status lla_lambda_mlp(const void *d, const float *W1, const float *W2,
+                          const float *b, float *lambda, int B, int H, int T,
+                          int Dd, int L, lla_dtype in_dt, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

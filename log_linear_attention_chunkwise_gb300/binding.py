@@ -35,6 +35,7 @@ SIGNATURES = {
     "lla_decode_step": (_I, [_P] * 9 + [_I] * 5 + [_I, _P, _P]),
     "lla_prefill_workspace_bytes": (_Z, [_I] * 3),
     "lla_prefill_state": (_I, [_P] * 5 + [_I] * 6 + [_I, _P, _Z, _P]),
+    "lla_lambda_mlp": (_I, [_P] * 5 + [_I] * 5 + [_I, _P]),
 }
 
 _lib = None
@@ -180,3 +181,22 @@ def prefill_state(k, v, g, Ls: int, state=None, logdecay=None, workspace=None, s
                                _stream(stream))
     _check("lla_prefill_state", rc)
     return state, logdecay
+
+
+def lambda_mlp(d, W1, W2, b, out=None, stream=None):
+    """lla_lambda_mlp: lambda [B,H,T,L] = softplus((d W1) W2 + b) for
+    d [B,H,T,Dd] (fp32 or bf16), W1 [Dd,2L], W2 [2L,L], b [L] fp32."""
+    lib = load()
+    _need(d, "d", None, 4)
+    for n, t in (("W1", W1), ("W2", W2), ("b", b)):
+        _need(t, n, torch.float32, None)
+    B, H, T, Dd = d.shape
+    L = b.shape[0]
+    if W1.shape != (Dd, 2 * L) or W2.shape != (2 * L, L):
+        raise ValueError("inconsistent shapes")
+    if out is None:
+        out = torch.empty((B, H, T, L), dtype=torch.float32, device=d.device)
+    rc = lib.lla_lambda_mlp(_ptr(d), _ptr(W1), _ptr(W2), _ptr(b), _ptr(out), B, H, T, Dd, L,
+                            _dt(d), _stream(stream))
+    _check("lla_lambda_mlp", rc)
+    return out

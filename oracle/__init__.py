@@ -15,7 +15,9 @@ What each function follows (page "Log-Linear Attention", gist.science
   decode_step        §2.3 recurrent form on a lazily decayed level state;
   state_closed_form  §2.2 bucket states straight from the level definition;
   ssd                the plain gated linear-attention scan (§1 / §3 Mamba-2),
-                     which the operator reduces to when every lambda is 1.
+                     which the operator reduces to when every lambda is 1;
+  lambda_mlp         page "Adaptive memory decay for Log-Linear Attention",
+                     §LambdaMLPSoftplus: lambda = softplus((d W1) W2 + b).
 Every function is pinned by tests in ``tests/test_oracle_pins.py``.
 """
 
@@ -59,8 +61,9 @@ def _load():
         lib.oracle_state_closed_form.argtypes = [P] * 6 + [I] * 6
         lib.oracle_ssd.argtypes = [P] * 5 + [I] * 5
         lib.oracle_level.argtypes = [I, I]
+        lib.oracle_lambda_mlp.argtypes = [P] * 5 + [I] * 3
         for name in ("oracle_naive", "oracle_naive_rows", "oracle_fenwick", "oracle_decode_step",
-                     "oracle_state_closed_form", "oracle_ssd", "oracle_level",
+                     "oracle_state_closed_form", "oracle_ssd", "oracle_level", "oracle_lambda_mlp",
                      "oracle_num_threads"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -172,3 +175,18 @@ def ssd(q, k, v, g) -> np.ndarray:
     _check(_load().oracle_ssd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(out),
                               B, H, T, dk, dv), "oracle_ssd")
     return out
+
+
+def lambda_mlp(d, W1, W2, b) -> np.ndarray:
+    """lambda [..., L] = softplus((d W1) W2 + b) for d [..., Dd], W1 [Dd, 2L],
+    W2 [2L, L], b [L]."""
+    d, W1, W2, b = map(_f64, (d, W1, W2, b))
+    lead = d.shape[:-1]
+    Dd = d.shape[-1]
+    L = b.shape[0]
+    assert W1.shape == (Dd, 2 * L) and W2.shape == (2 * L, L)
+    dd = np.ascontiguousarray(d.reshape(-1, Dd))
+    out = np.zeros((dd.shape[0], L), np.float64)
+    _check(_load().oracle_lambda_mlp(_ptr(dd), _ptr(W1), _ptr(W2), _ptr(b), _ptr(out),
+                                     dd.shape[0], Dd, L), "oracle_lambda_mlp")
+    return out.reshape(*lead, L)

@@ -457,3 +457,40 @@ int oracle_ssd(const double *q, const double *k, const double *v,
     }
     return 0;
 }
+
+/*
+ * Per-(token, head) level weights from a two-layer MLP ("Adaptive memory
+ * decay for Log-Linear Attention", §Method "LambdaMLPSoftplus"):
+ *     h = d W1,   lambda = softplus(h W2 + b),
+ * hidden width 2L, no activation between the layers.  Reading: d is one
+ * vector of width Dd per (token, head) and the weights are shared by heads.
+ * d [N,Dd], W1 [Dd,2L], W2 [2L,L], b [L] -> out [N,L]; softplus(z) =
+ * log(1 + exp(z)), evaluated as max(z,0) + log1p(exp(-|z|)).
+ */
+int oracle_lambda_mlp(const double *d, const double *W1, const double *W2,
+                      const double *b, double *out, int64_t N, int64_t Dd,
+                      int64_t L)
+{
+    if (N < 0 || Dd <= 0 || L <= 0)
+        return -1;
+    const int64_t Hd = 2 * L;
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; n++) {
+        double h[2 * 64];
+        if (Hd > 2 * 64)
+            continue;
+        for (int64_t j = 0; j < Hd; j++) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < Dd; k++)
+                acc += d[n * Dd + k] * W1[k * Hd + j];
+            h[j] = acc;
+        }
+        for (int64_t l = 0; l < L; l++) {
+            double z = b[l];
+            for (int64_t j = 0; j < Hd; j++)
+                z += h[j] * W2[j * L + l];
+            out[n * L + l] = (z > 0.0 ? z : 0.0) + log1p(exp(-fabs(z)));
+        }
+    }
+    return L > 64 ? -2 : 0;
+}

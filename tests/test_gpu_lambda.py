@@ -1,0 +1,76 @@
+"""GPU parity of lla_lambda_mlp (the level-weight producer of "Adaptive memory
+decay for Log-Linear Attention") against the fp64 oracle, and its use as the
+forward's lambda."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from log_linear_attention_chunkwise_gb300 import binding
+from log_linear_attention_chunkwise_gb300 import workloads as W
+from parity import assert_parity
+
+pytestmark = pytest.mark.gpu
+
+
+def weights(Dd, L, seed):
+    g = torch.Generator().manual_seed(seed)
+    W1 = torch.randn((Dd, 2 * L), generator=g) / math.sqrt(Dd)
+    W2 = torch.randn((2 * L, L), generator=g) / math.sqrt(2 * L)
+    b = 0.54 + 0.3 * torch.randn((L,), generator=g)
+    return W1, W2, b
+
+
+@pytest.mark.parametrize("B,H,T,Dd,L,dtype", [(2, 3, 100, 64, 7, torch.float32),
+                                              (1, 4, 333, 128, 12, torch.bfloat16),
+                                              (1, 2, 64, 256, 25, torch.bfloat16),
+                                              (3, 1, 7, 1, 1, torch.float32)])
+def test_lambda_mlp_matches_oracle(B, H, T, Dd, L, dtype):
+    g = torch.Generator().manual_seed(Dd + L)
+    d = torch.randn((B, H, T, Dd), generator=g).to(dtype)
+    W1, W2, b = weights(Dd, L, seed=L)
+    lam = binding.lambda_mlp(d.cuda(), W1.cuda(), W2.cuda(), b.cuda())
+    torch.cuda.synchronize()
+    ref = oracle.lambda_mlp(d, W1, W2, b)
+    np.testing.assert_allclose(lam.double().cpu().numpy(), ref, rtol=2e-5, atol=2e-6)
+
+
+def test_lambda_mlp_initialisation_gives_one():
+    d = torch.randn((1, 2, 300, 64), device="cuda")
+    W1 = torch.randn((64, 18), device="cuda")
+    lam = binding.lambda_mlp(d, W1, torch.zeros((18, 9), device="cuda"),
+                             torch.full((9,), 0.54, device="cuda"))
+    torch.cuda.synchronize()
+    assert torch.allclose(lam, torch.full_like(lam, 0.99916), atol=1e-5)
+
+
+def test_lambda_mlp_feeds_the_forward():
+    """lambda from the MLP on the keys, then the tensor-core forward: the
+    result matches the oracle run on the oracle's own lambda."""
+    cfg = W.small_fwd_config(1, 4, 2048, 128, 128, 64, torch.bfloat16, seed=21)
+    x = W.make_fwd_inputs(cfg)
+    W1, W2, b = weights(128, cfg.L, seed=5)
+    xd = {n: t.cuda() for n, t in x.items()}
+    lam = binding.lambda_mlp(xd["k"], W1.cuda(), W2.cuda(), b.cuda())
+    out = binding.fwd(xd["q"], xd["k"], xd["v"], xd["g"], lam, chunk=64)
+    torch.cuda.synchronize()
+    lam_ref = oracle.lambda_mlp(x["k"], W1, W2, b)
+    np.testing.assert_allclose(lam.double().cpu().numpy(), lam_ref, rtol=2e-5, atol=2e-6)
+    ref = oracle.naive(x["q"], x["k"], x["v"], x["g"], lam_ref)
+    assert_parity(out, ref, torch.bfloat16, "forward on MLP lambda")
+
+
+def test_lambda_mlp_full_size_sampled_rows():
+    B, H, T, Dd, L = 1, 16, 32768, 128, 16
+    g = torch.Generator(device="cuda").manual_seed(7)
+    d = torch.randn((B, H, T, Dd), generator=g, device="cuda").bfloat16()
+    W1, W2, b = weights(Dd, L, seed=8)
+    lam = binding.lambda_mlp(d, W1.cuda(), W2.cuda(), b.cuda())
+    torch.cuda.synchronize()
+    rows = torch.tensor([0, 1, 127, 128, 4095, 16384, 32766, 32767])
+    for h in (0, 7, 15):
+        ref = oracle.lambda_mlp(d[0, h, rows].cpu(), W1, W2, b)
+        np.testing.assert_allclose(lam[0, h, rows].double().cpu().numpy(), ref, rtol=2e-5, atol=2e-6)

@@ -270,3 +270,46 @@ def test_naive_rows_equal_full_double_sum():
     rows = [0, 1, 63, 64, 65, 127, 129]
     part = oracle.naive_rows(q[0, 0], k[0, 0], v[0, 0], g[0, 0], lam[0, 0], rows)
     np.testing.assert_array_equal(part, full[rows])
+
+
+# ------------------------------------------------------ lambda producer
+
+def mlp_inputs(N, Dd, L, seed):
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal((N, Dd)), rng.standard_normal((Dd, 2 * L)) / math.sqrt(Dd),
+            rng.standard_normal((2 * L, L)) / math.sqrt(2 * L), rng.standard_normal(L))
+
+
+def inv_softplus(y):
+    return y + np.log(-np.expm1(-y))
+
+
+def test_lambda_mlp_initialisation_is_one():
+    """Page "Adaptive memory decay for Log-Linear Attention": W2 = 0 and
+    b = 0.54 make every weight softplus(0.54), about 1.0."""
+    d, W1, _, _ = mlp_inputs(50, 16, 9, seed=1)
+    lam = oracle.lambda_mlp(d, W1, np.zeros((18, 9)), np.full(9, 0.54))
+    np.testing.assert_allclose(lam, 0.99916, atol=5e-6)
+
+
+def test_lambda_mlp_layers_are_linear_in_d():
+    """No activation between the two layers: the pre-activation is linear in d."""
+    d1, W1, W2, b = mlp_inputs(40, 12, 7, seed=2)
+    d2 = mlp_inputs(40, 12, 7, seed=3)[0]
+    pre = lambda d: inv_softplus(oracle.lambda_mlp(d, W1, W2, b)) - b
+    np.testing.assert_allclose(pre(d1 + d2), pre(d1) + pre(d2), rtol=1e-9, atol=1e-9)
+    np.testing.assert_allclose(pre(3.0 * d1), 3.0 * pre(d1), rtol=1e-9, atol=1e-9)
+
+
+def test_lambda_mlp_softplus_identities():
+    """softplus(z) - softplus(-z) = z, positivity, and the tails z and e^z."""
+    d, W1, W2, b = mlp_inputs(30, 8, 5, seed=4)
+    plus = oracle.lambda_mlp(d, W1, W2, b)
+    minus = oracle.lambda_mlp(d, W1, -W2, -b)
+    z = (d @ W1) @ W2 + b
+    np.testing.assert_allclose(plus - minus, z, rtol=1e-10, atol=1e-12)
+    assert (plus > 0).all()
+    big = oracle.lambda_mlp(d, W1, W2, b + 60.0)
+    np.testing.assert_allclose(big, z + 60.0, rtol=1e-12)
+    small = oracle.lambda_mlp(d, W1, W2, b - 60.0)
+    np.testing.assert_allclose(small, np.exp(z - 60.0), rtol=1e-9)
