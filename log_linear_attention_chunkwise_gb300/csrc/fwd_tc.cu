@@ -5,13 +5,14 @@
 // §2.2 (Fenwick buckets of [0,t), one state per bucket, lambda-weighted
 // read-out) and §2.3 (the hierarchical mask computed chunkwise with matmuls).
 //
-// Four launches.  Two small kernels form the fp64 tile-gate prefix sums.  The node
-// producer (one CTA per tile, tickets in (tile, batch*head) order so a tile
-// only waits on tiles that started before it) computes each tile's state and
-// publishes the tile-level Fenwick node it closes.  The read-out consumer (one
-// CTA per tile, no waits: every node exists when it starts) forms the masked
-// intra-tile product and the lambda-weighted read-out of the nodes.  With Gam_i the gate sum
-// of tile i and P_i = Gam_0 + ... + Gam_{i-1} (fp64, from the prefix kernel),
+// Five launches.  Two small kernels form the fp64 tile-gate prefix sums.  Node
+// walkers (one CTA per head, dv slice and segment of tiles, walking in order
+// with the Fenwick stack in tensor memory) compute each tile's state and
+// publish the tile-level Fenwick nodes; a fix-up kernel chains the nodes that
+// span segments.  The read-out consumer (one CTA per tile, no waits: every
+// node exists when it starts) forms the masked intra-tile product and the
+// lambda-weighted read-out of the nodes.  With Gam_i the gate sum
+// of tile i and P_i = Gam_0 + ... + Gam_{i-1} (fp64, from the prefix kernels),
 // the earlier tiles of tile i form the tile-level Fenwick buckets ending at
 // j = i, i - lowbit(i), ...; bucket j (level m = ctz(j)) holds the tiles
 // [j - 2^m, j) decayed to the end of tile j-1:
@@ -21,7 +22,7 @@
 //   S  = Q K^T                              (tcgen05, TMEM)
 //   H  = K^T diag(exp(Gam - gamma)) V        (tcgen05, TMEM) -> Node_{i+1}
 //        Node_{i+1} = H + sum_{m < ctz(i+1)} exp(P_{i+1} - P_{j_m}) Node_{j_m},
-//        j_m = i + 1 - 2^m, published to global memory (fp32 + bf16 copy)
+//        j_m = i + 1 - 2^m, published to global memory in bf16
 //   P  = S . M,  M[a][b] = lambda_a[bit_length(a^b)] exp(gamma_a - gamma_b), b <= a
 //   O  = P V + sum_{path j} diag(lambda_.[8+m] exp(gamma_. + P_i - P_j)) (Q Node_j)
 // Every product above is a tcgen05 MMA of M = N = 128, bf16 operands in
@@ -55,6 +56,7 @@ struct TcParams {
     const float *g, *lam;
     void *out;
     const double *P;        // [BH][NT+1] tile-gate prefix sums
+    float *gamma;           // [BH][T] inclusive gate sum inside each tile (fp32)
     int *err;               // first bounded wait that gave up (0: none)
     float *segtot;          // [BH][nseg_full][128][128] decayed segment totals
     __nv_bfloat16 *node16;  // [BH][NT][128][128] Fenwick nodes (index 0 unused)
@@ -86,25 +88,6 @@ __device__ __forceinline__ void mma_kmn(uint32_t d, const uint8_t *a, const uint
     }
 }
 
-// Inclusive running sum of the tile's gates: thread (row, half) gets
-// gamma_row; also returns the tile total Gam.  `wsum` is 4 floats of smem.
-__device__ __forceinline__ float tile_cumsum(float gv, float *wsum, float &Gam)
-{
-    const int tid = threadIdx.x, warp = tid >> 5;
-    float incl = gv;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        float y = __shfl_up_sync(0xffffffffu, incl, off);
-        if ((tid & 31) >= off) incl += y;
-    }
-    if (tid < kTile && (tid & 31) == 31) wsum[warp] = incl;
-    __syncthreads();
-    float base = 0.f;
-    for (int w = 0; w < (warp & 3); w++) base += wsum[w];
-    Gam = wsum[0] + wsum[1] + wsum[2] + wsum[3];
-    return base + incl;
-}
-
 // ======================================================= node walkers
 // The tile-level Fenwick nodes Node_j (j = 1 .. NT-1) are built by walkers:
 // one CTA per (batch*head, 32-column slice of dv, segment of 64 tiles) goes
@@ -127,18 +110,26 @@ __device__ __forceinline__ uint32_t f32_stage_off(int r, int c)
 
 constexpr int kSliceW = 32;              // dv columns per walker
 constexpr int kSlices = kD / kSliceW;
-constexpr int kSegLog = 6;
+constexpr int kSegLog = 5;
 constexpr int kSeg = 1 << kSegLog;       // tiles per segment
-constexpr int kWalkThreads = 128;        // thread = token row (scaling) / dk row (epilogue)
+constexpr int kWalkStages = 2;           // K/V tiles in flight per walker (2 walkers per SM)
+constexpr int kWalkThreads = 256;        // warps 0-3: node epilogue; warps 4-7: tile preparation
 
 struct __align__(1024) WalkSmem {
-    uint8_t k[2][kBuf];   // K tiles, double-buffered
-    uint8_t v[2][kHalf];  // the 64-column V block holding the slice, double-buffered
-    float wsum[4];
-    uint64_t bar_load[2], bar_h[2];
+    uint8_t k[kWalkStages][kBuf];   // K tiles
+    uint8_t v[kWalkStages][kHalf];  // the 64-column V block holding the slice
+    float gm[kWalkStages][kTile];   // the tile's inclusive gate sums gamma
+    double P[kSeg + 1];             // P_{i0} .. P_{i0+kSeg}
+    uint64_t bar_load[kWalkStages], bar_h[2], bar_hfree[2];
     uint32_t tmem;
 };
 
+__device__ __forceinline__ void prep_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Warp-specialised: the preparation warps (thread = token row) load gates,
+// scale the V slice by exp(Gam - gamma) and issue the state product of tile
+// n while the epilogue warps (thread = dk row) fold tile n-1's state into
+// the Fenwick stack; TMA keeps kWalkStages tiles in flight.
 __global__ void __launch_bounds__(kWalkThreads, 2)
 lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                        const TcParams prm)
@@ -151,14 +142,16 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
     const int seg = blockIdx.x, slice = blockIdx.y, bh = blockIdx.z;
     const int NT = prm.NT;
     const int i0 = seg * kSeg, i1 = min(i0 + kSeg, NT - 1);  // tiles i0..i1-1 close Node_{i+1}
+    const int ntiles = i1 - i0;
     const double *Pb = prm.P + (long long)bh * (NT + 1);
-    const int vblk = slice >> 1;                 // 64-column V block holding the slice
+    const int vblk = slice >> 1;                       // 64-column V block holding the slice
     const uint32_t voff = (uint32_t)(slice & 1) * 64;  // the slice's byte offset in a block row
 
     if (tid == 0) {
+        for (int b = 0; b < kWalkStages; b++) mbar_init(&s.bar_load[b], 1);
         for (int b = 0; b < 2; b++) {
-            mbar_init(&s.bar_load[b], 1);
             mbar_init(&s.bar_h[b], 1);
+            mbar_init(&s.bar_hfree[b], 128);
         }
         fence_mbar_init();
         tma_prefetch_map(&map_k);
@@ -168,108 +161,121 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
         tmem_alloc(&s.tmem, 256);
         tmem_relinquish();
     }
+    for (int j = tid; j <= kSeg; j += kWalkThreads) s.P[j] = (i0 + j <= NT) ? Pb[i0 + j] : 0.0;
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tm = s.tmem;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    // columns: stack level m at [32m, 32m+32) for m < kSegLog; H buffers after it
+    // columns: stack level m at [32m, 32m+32) for m < kSegLog; two H buffers after it
     const uint32_t tm_h0 = tm + kSegLog * kSliceW;
 
-    auto issue_load = [&](int i, int st) {
-        mbar_arrive_expect_tx(&s.bar_load[st], kBuf + kHalf);
-        tma_load_3d(s.k[st], &map_k, &s.bar_load[st], 0, i * kTile, bh);
-        tma_load_3d(s.k[st] + kHalf, &map_k, &s.bar_load[st], 64, i * kTile, bh);
-        tma_load_3d(s.v[st], &map_v, &s.bar_load[st], vblk * 64, i * kTile, bh);
+    // a tile's 128 gamma values are one aligned 512-byte run
+    auto issue_load = [&](int n) {
+        const int ls = n % kWalkStages, i = i0 + n;
+        mbar_arrive_expect_tx(&s.bar_load[ls], kBuf + kHalf + kTile * 4);
+        tma_load_3d(s.k[ls], &map_k, &s.bar_load[ls], 0, i * kTile, bh);
+        tma_load_3d(s.k[ls] + kHalf, &map_k, &s.bar_load[ls], 64, i * kTile, bh);
+        tma_load_3d(s.v[ls], &map_v, &s.bar_load[ls], vblk * 64, i * kTile, bh);
+        bulk_load(s.gm[ls], prm.gamma + ((long long)bh * NT + i) * kTile, kTile * 4, &s.bar_load[ls]);
     };
-    if (tid == 0 && i0 < i1) issue_load(i0, 0);
 
-    for (int i = i0; i < i1; i++) {
-        const int n = i - i0, st = n & 1;
-        // the other stage was last used by tile i-1, whose product is complete
-        if (tid == 0 && i + 1 < i1) issue_load(i + 1, st ^ 1);
-        // tiles before NT-1 are full: no ragged rows here
-        const long long tok = (long long)bh * prm.T + (long long)i * kTile + tid;
-        float Gam;
-        const float gam_a = tile_cumsum(prm.g[tok], s.wsum, Gam);
-        if (!mbar_wait(&s.bar_load[st], (n >> 1) & 1, kWaitIters)) set_err(prm.err, kErrLoadTimeout);
-        {   // V row `tid` of the slice, scaled in place by exp(Gam - gamma)
-            const float w = __expf(Gam - gam_a);
-            uint8_t *vrow = s.v[st];
+    if (warp >= 4) {
+        // ---------------- preparation warps
+        const int p = tid - 128;
+        if (p == 0)
+            for (int n = 0; n < min(kWalkStages, ntiles); n++) issue_load(n);
+        for (int n = 0; n < ntiles; n++) {
+            const int ls = n % kWalkStages, hb = n & 1;
+            if (p == 0 && n >= 1 && n - 1 + kWalkStages < ntiles) {
+                // stage of tile n-1 is free once its product is done
+                if (!mbar_wait(&s.bar_h[(n - 1) & 1], ((n - 1) >> 1) & 1, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
+                issue_load(n - 1 + kWalkStages);
+            }
+            if (!mbar_wait(&s.bar_load[ls], (n / kWalkStages) & 1, kWaitIters)) set_err(prm.err, kErrLoadTimeout);
+            const float Gam = s.gm[ls][kTile - 1];
+            const float gam_a = s.gm[ls][p];
+            {   // V row p of the slice, scaled in place by exp(Gam - gamma)
+                const float w = __expf(Gam - gam_a);
 #pragma unroll
-            for (int c = 0; c < 4; c++) {
-                uint4 *p = reinterpret_cast<uint4 *>(vrow + sw128_offset(tid, (voff >> 4) + c));
-                uint4 raw = *p;
-                __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&raw);
+                for (int c = 0; c < 4; c++) {
+                    uint4 *q4 = reinterpret_cast<uint4 *>(s.v[ls] + sw128_offset(p, (voff >> 4) + c));
+                    uint4 raw = *q4;
+                    __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&raw);
 #pragma unroll
-                for (int u = 0; u < 4; u++) {
-                    float2 f = __bfloat1622float2(h[u]);
-                    h[u] = __floats2bfloat162_rn(f.x * w, f.y * w);
+                    for (int u = 0; u < 4; u++) {
+                        float2 f = __bfloat1622float2(h[u]);
+                        h[u] = __floats2bfloat162_rn(f.x * w, f.y * w);
+                    }
+                    *q4 = raw;
                 }
-                *p = raw;
+            }
+            fence_proxy_async_smem();
+            prep_sync();
+            if (p == 0) {
+                if (n >= 2 && !mbar_wait(&s.bar_hfree[hb], ((n - 2) >> 1) & 1, kWaitIters))
+                    set_err(prm.err, kErrMmaTimeout);
+                tc_fence_after_sync();
+                // H slice = K^T Vs: A = K^T (M = dk, MN-major), B = Vs slice (N = 32, MN-major)
+                const uint32_t idesc = idesc_bf16_f32(128, kSliceW, true, true);
+#pragma unroll
+                for (int kk = 0; kk < 8; kk++) {
+                    const uint32_t off = kk * 2048;
+                    umma_bf16(tm_h0 + hb * kSliceW, desc_sw128(smem_u32(s.k[ls]) + off, kHalf, 1024),
+                              desc_sw128(smem_u32(s.v[ls]) + voff + off, kHalf, 1024), idesc,
+                              kk > 0 ? 1u : 0u);
+                }
+                umma_commit(&s.bar_h[hb]);
             }
         }
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        __syncthreads();
-        if (tid == 0) {
+    } else {
+        // ---------------- epilogue warps: thread = dk row `tid`, the slice's 32 columns
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        for (int n = 0; n < ntiles; n++) {
+            const int hb = n & 1;
+            const int J = i0 + n + 1;
+            const int z = __ffs(J) - 1;
+            const bool cross = (J == i0 + kSeg);  // closes a full segment
+            const int mlim = cross ? kSegLog : z;
+            if (!mbar_wait(&s.bar_h[hb], (n >> 1) & 1, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
             tc_fence_after_sync();
-            // H slice = K^T Vs: A = K^T (M = dk, MN-major), B = Vs slice (N = 32, MN-major)
-            const uint32_t idesc = idesc_bf16_f32(128, kSliceW, true, true);
-#pragma unroll
-            for (int kk = 0; kk < 8; kk++) {
-                const uint32_t off = kk * 2048;
-                umma_bf16(tm_h0 + st * kSliceW, desc_sw128(smem_u32(s.k[st]) + off, kHalf, 1024),
-                          desc_sw128(smem_u32(s.v[st]) + voff + off, kHalf, 1024), idesc,
-                          kk > 0 ? 1u : 0u);
-            }
-            umma_commit(&s.bar_h[st]);
-        }
-        if (!mbar_wait(&s.bar_h[st], (n >> 1) & 1, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
-        tc_fence_after_sync();
-
-        // epilogue: thread = dk row `tid`, the slice's 32 columns
-        const int J = i + 1;
-        const int z = __ffs(J) - 1;
-        const bool cross = (J == i0 + kSeg);  // closes a full segment
-        const int mlim = cross ? kSegLog : z;
-        float acc[32];
-        tmem_ld16(tm_h0 + st * kSliceW + lane_off, *reinterpret_cast<float(*)[16]>(acc));
-        tmem_ld16(tm_h0 + st * kSliceW + lane_off + 16, *reinterpret_cast<float(*)[16]>(acc + 16));
-        tmem_ld_wait();
-        const double PJ = Pb[J];
-        for (int m = 0; m < mlim; m++) {
-            const float f = __expf((float)(PJ - Pb[J - (1 << m)]));
-            float x[32];
-            tmem_ld16(tm + m * kSliceW + lane_off, *reinterpret_cast<float(*)[16]>(x));
-            tmem_ld16(tm + m * kSliceW + lane_off + 16, *reinterpret_cast<float(*)[16]>(x + 16));
+            float acc[32];
+            tmem_ld16(tm_h0 + hb * kSliceW + lane_off, *reinterpret_cast<float(*)[16]>(acc));
+            tmem_ld16(tm_h0 + hb * kSliceW + lane_off + 16, *reinterpret_cast<float(*)[16]>(acc + 16));
             tmem_ld_wait();
+            tc_fence_before_sync();
+            mbar_arrive(&s.bar_hfree[hb]);
+            const double PJ = s.P[J - i0];
+            for (int m = 0; m < mlim; m++) {
+                const float f = __expf((float)(PJ - s.P[J - (1 << m) - i0]));
+                float x[32];
+                tmem_ld16(tm + m * kSliceW + lane_off, *reinterpret_cast<float(*)[16]>(x));
+                tmem_ld16(tm + m * kSliceW + lane_off + 16, *reinterpret_cast<float(*)[16]>(x + 16));
+                tmem_ld_wait();
 #pragma unroll
-            for (int u = 0; u < 32; u++) acc[u] = fmaf(f, x[u], acc[u]);
-        }
-        if (!cross) {
-            if (z < kSegLog) {
-                tmem_st16(tm + z * kSliceW + lane_off, *reinterpret_cast<float(*)[16]>(acc));
-                tmem_st16(tm + z * kSliceW + lane_off + 16, *reinterpret_cast<float(*)[16]>(acc + 16));
-                tmem_st_wait();
+                for (int u = 0; u < 32; u++) acc[u] = fmaf(f, x[u], acc[u]);
             }
-            uint4 w[4];
-            __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(w);
+            if (!cross) {
+                if (z < kSegLog) {
+                    tmem_st16(tm + z * kSliceW + lane_off, *reinterpret_cast<float(*)[16]>(acc));
+                    tmem_st16(tm + z * kSliceW + lane_off + 16, *reinterpret_cast<float(*)[16]>(acc + 16));
+                    tmem_st_wait();
+                }
+                uint4 w[4];
+                __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(w);
 #pragma unroll
-            for (int u = 0; u < 16; u++) h[u] = __floats2bfloat162_rn(acc[2 * u], acc[2 * u + 1]);
-            uint4 *dst = reinterpret_cast<uint4 *>(prm.node16 + (((long long)bh * NT + J) * kD + tid) * kD +
-                                                   slice * kSliceW);
+                for (int u = 0; u < 16; u++) h[u] = __floats2bfloat162_rn(acc[2 * u], acc[2 * u + 1]);
+                uint4 *dst = reinterpret_cast<uint4 *>(prm.node16 + (((long long)bh * NT + J) * kD + tid) * kD +
+                                                       slice * kSliceW);
 #pragma unroll
-            for (int u = 0; u < 4; u++) dst[u] = w[u];
-        } else {
-            float4 *dst = reinterpret_cast<float4 *>(
-                prm.segtot + ((((long long)bh * prm.nseg_full + seg) * kD + tid) * kD + slice * kSliceW));
+                for (int u = 0; u < 4; u++) dst[u] = w[u];
+            } else {
+                float4 *dst = reinterpret_cast<float4 *>(
+                    prm.segtot + ((((long long)bh * prm.nseg_full + seg) * kD + tid) * kD + slice * kSliceW));
 #pragma unroll
-            for (int u = 0; u < 8; u++) dst[u] = make_float4(acc[4 * u], acc[4 * u + 1], acc[4 * u + 2], acc[4 * u + 3]);
+                for (int u = 0; u < 8; u++)
+                    dst[u] = make_float4(acc[4 * u], acc[4 * u + 1], acc[4 * u + 2], acc[4 * u + 3]);
+            }
         }
-        tc_fence_before_sync();
-        __syncthreads();  // stack and H buffer settled before the next tile
-        tc_fence_after_sync();
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -278,31 +284,51 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
 
 // Nodes that close full segments: Fenwick chain over the segment totals,
 //   Node_{(u)SEG} = Tot_{u-1} + sum_{k < ctz(u)} exp(P_{uSEG} - P_{(u-2^k)SEG}) Node_{(u-2^k)SEG},
-// one thread per state element, the open node of each level in registers.
+// eight state elements per thread, the open node of each level in
+// registers, the decay factors in shared memory.
 constexpr int kFixThreads = 256;
-constexpr int kFixMaxZ = 20;
+constexpr int kFixMaxZ = 12;    // levels of a segment index: (2^24/128)/64 segments < 2^12
+constexpr int kFixMaxSeg = 2048;
 __global__ void __launch_bounds__(kFixThreads)
 lla_node_fixup_kernel(const TcParams prm)
 {
-    const int e = blockIdx.x * kFixThreads + threadIdx.x;  // element of the 128x128 state
+    __shared__ double pseg[kFixMaxSeg + 1];  // P at segment boundaries
     const long long bh = blockIdx.y;
-    if (e >= kD * kD) return;
-    const int NT = prm.NT;
+    const int NT = prm.NT, nseg = prm.nseg_full;
     const double *Pb = prm.P + bh * (NT + 1);
-    float stack[kFixMaxZ];
+    for (int u = threadIdx.x; u <= nseg; u += kFixThreads) pseg[u] = Pb[u * kSeg];
+    __syncthreads();
+    const int e0 = (blockIdx.x * kFixThreads + threadIdx.x) * 8;  // 8 consecutive elements
+    if (e0 >= kD * kD) return;
+    float stack[kFixMaxZ][8];
 #pragma unroll
-    for (int k = 0; k < kFixMaxZ; k++) stack[k] = 0.f;
-    for (int u = 1; u <= prm.nseg_full; u++) {
-        const int J = u * kSeg;
+    for (int k = 0; k < kFixMaxZ; k++)
+#pragma unroll
+        for (int c = 0; c < 8; c++) stack[k][c] = 0.f;
+    for (int u = 1; u <= nseg; u++) {
         const int z = __ffs(u) - 1;
-        float val = prm.segtot[((bh * prm.nseg_full) + (u - 1)) * (kD * kD) + e];
+        const float4 *src = reinterpret_cast<const float4 *>(prm.segtot + ((bh * nseg) + (u - 1)) * (kD * kD) + e0);
+        const float4 a = src[0], b = src[1];
+        float val[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int k = 0; k < kFixMaxZ; k++) {
+            if (k < z) {
+                const float f = __expf((float)(pseg[u] - pseg[u - (1 << k)]));
+#pragma unroll
+                for (int c = 0; c < 8; c++) val[c] = fmaf(f, stack[k][c], val[c]);
+            }
+        }
 #pragma unroll
         for (int k = 0; k < kFixMaxZ; k++)
-            if (k < z) val = fmaf(__expf((float)(Pb[J] - Pb[J - (1 << k) * kSeg])), stack[k], val);
+            if (k == z) {
 #pragma unroll
-        for (int k = 0; k < kFixMaxZ; k++)
-            if (k == z) stack[k] = val;
-        prm.node16[(bh * NT + J) * (kD * kD) + e] = __float2bfloat16_rn(val);
+                for (int c = 0; c < 8; c++) stack[k][c] = val[c];
+            }
+        uint4 w;
+        __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&w);
+#pragma unroll
+        for (int c = 0; c < 4; c++) h[c] = __floats2bfloat162_rn(val[2 * c], val[2 * c + 1]);
+        *reinterpret_cast<uint4 *>(prm.node16 + (bh * NT + (long long)u * kSeg) * (kD * kD) + e0) = w;
     }
 }
 
@@ -318,7 +344,6 @@ struct __align__(1024) ConsSmem {
     float kf[kTile];              // exp(gamma_e - gamma_b), e = last key of b's 16-key chunk
     float lam[kTile * kLamLd];
     float wgt[kMaxPath * kTile];  // read-out weight of each path level per row
-    float wsum[4];
     uint64_t bar_load, bar_s, bar_pv, bar_node[2], bar_u[2];
     uint32_t tmem;
 };
@@ -380,8 +405,7 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
         for (int l = 0; l <= kTileLevels; l++)
             s.lam[row * kLamLd + l] = (row_ok && l < prm.L) ? lam_row[l] : 0.f;
     }
-    float Gam;
-    const float gam_a = tile_cumsum(row_ok ? prm.g[tok] : 0.f, s.wsum, Gam);
+    const float gam_a = prm.gamma[((long long)bh * NT + i) * kTile + row];
     if (half == 0) s.gam[row] = gam_a;
     __syncthreads();
     if (half == 0) s.kf[row] = __expf(s.gam[row | 15] - gam_a);
@@ -567,7 +591,7 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
             for (int h = 0; h < 2; h++) tma_store_3d(&map_out, s.q + h * kHalf, h * 64, i * kTile, bh);
         }
         tma_store_commit();
-        tma_store_wait_all();
+        tma_store_wait_read();  // shared memory may be released; the writes finish with the kernel
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -581,8 +605,8 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
 // P_i = Gam_0 + ... + Gam_{i-1} in place.
 constexpr int kScanThreads = 1024;
 __global__ void __launch_bounds__(1024)
-lla_tile_gate_sum_kernel(const float *__restrict__ g, double *__restrict__ P, int *__restrict__ err, int T,
-                         int NT)
+lla_tile_gate_sum_kernel(const float *__restrict__ g, double *__restrict__ P, float *__restrict__ gamma,
+                         int *__restrict__ err, int T, int NT)
 {
     const long long bh = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -592,12 +616,29 @@ lla_tile_gate_sum_kernel(const float *__restrict__ g, double *__restrict__ P, in
         const float *gb = g + bh * (long long)T + (long long)tile * kTile;
         const int n = min(kTile, T - tile * kTile);
         double acc = 0.0;
+        // 4 consecutive gates per lane; rows past T count as 0
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
         if (n == kTile) {
-            const float4 x = reinterpret_cast<const float4 *>(gb)[lane];
-            acc = (double)x.x + (double)x.y + (double)x.z + (double)x.w;
+            x = reinterpret_cast<const float4 *>(gb)[lane];
         } else {
-            for (int t = lane; t < n; t += 32) acc += (double)gb[t];
+            const int t = 4 * lane;
+            if (t < n) x.x = gb[t];
+            if (t + 1 < n) x.y = gb[t + 1];
+            if (t + 2 < n) x.z = gb[t + 2];
+            if (t + 3 < n) x.w = gb[t + 3];
         }
+        acc = (double)x.x + (double)x.y + (double)x.z + (double)x.w;
+        // inclusive running sum inside the tile (fp32), the form the kernels use
+        const float s1 = x.x, s2 = s1 + x.y, s3 = s2 + x.z, s4 = s3 + x.w;
+        float incl = s4;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            float y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        const float ex = incl - s4;
+        float *gm = gamma + bh * (long long)NT * kTile + (long long)tile * kTile;
+        reinterpret_cast<float4 *>(gm)[lane] = make_float4(ex + s1, ex + s2, ex + s3, ex + s4);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
         if (lane == 0) Pb[tile + 1] = acc;
@@ -649,9 +690,10 @@ lla_tile_gate_scan_kernel(double *__restrict__ P, int NT)
 
 }  // namespace
 
-// Workspace: [P fp64 BH*(NT+1)] [err word] [segment totals fp32] [nodes bf16]
+// Workspace: [P fp64 BH*(NT+1)] [gamma fp32 BH*NT*128] [err word] [segment totals fp32] [nodes bf16]
 static int nseg_full_of(int NT) { return NT > 1 ? (NT - 1) / kSeg : 0; }
-static size_t off_err(int BH, int NT) { return align_up((size_t)BH * (NT + 1) * 8, 256); }
+static size_t off_gamma(int BH, int NT) { return align_up((size_t)BH * (NT + 1) * 8, 256); }
+static size_t off_err(int BH, int NT) { return off_gamma(BH, NT) + align_up((size_t)BH * NT * kTile * 4, 256); }
 static size_t off_segtot(int BH, int NT) { return off_err(BH, NT) + 256; }
 static size_t off_node16(int BH, int NT)
 {
@@ -704,6 +746,7 @@ cudaError_t tc_fwd(const TcFwdArgs &A)
     prm.out = A.out;
     prm.P = (const double *)ws;
     prm.err = (int *)(ws + off_err(BH, NT));
+    prm.gamma = (float *)(ws + off_gamma(BH, NT));
     prm.segtot = (float *)(ws + off_segtot(BH, NT));
     prm.node16 = (__nv_bfloat16 *)(ws + off_node16(BH, NT));
     prm.T = A.T;
@@ -721,8 +764,8 @@ cudaError_t tc_fwd(const TcFwdArgs &A)
                 : make_map_bf16_3d(&mo, A.out, kD, A.T, BH, 64, kTile)))
         return cudaErrorInvalidValue;
     cudaStream_t st = (cudaStream_t)A.stream;
-    lla_tile_gate_sum_kernel<<<dim3((NT + 31) / 32, BH), 1024, 0, st>>>(A.g, (double *)prm.P, prm.err,
-                                                                          A.T, NT);
+    lla_tile_gate_sum_kernel<<<dim3((NT + 31) / 32, BH), 1024, 0, st>>>(A.g, (double *)prm.P, prm.gamma,
+                                                                          prm.err, A.T, NT);
     lla_tile_gate_scan_kernel<<<BH, kScanThreads, 0, st>>>((double *)prm.P, NT);
     cudaError_t e;
     if (NT > 1) {
@@ -733,7 +776,7 @@ cudaError_t tc_fwd(const TcFwdArgs &A)
         const int nseg = (NT - 1 + kSeg - 1) / kSeg;
         lla_node_walker_kernel<<<dim3(nseg, kSlices, BH), kWalkThreads, wsmem, st>>>(mk, mv, prm);
         if (prm.nseg_full > 0)
-            lla_node_fixup_kernel<<<dim3(kD * kD / kFixThreads, BH), kFixThreads, 0, st>>>(prm);
+            lla_node_fixup_kernel<<<dim3(kD * kD / 8 / kFixThreads, BH), kFixThreads, 0, st>>>(prm);
     }
     e = out32 ? launch_consumer<float>(mq, mk, mv, mn, mo, prm, NT * BH, st)
               : launch_consumer<__nv_bfloat16>(mq, mk, mv, mn, mo, prm, NT * BH, st);

@@ -5,6 +5,7 @@
 #include "decode.cuh"
 #include "fwd_simt.cuh"
 #include "fwd_tc.cuh"
+#include "lambda_mlp.cuh"
 #include "lla_common.cuh"
 
 using namespace lla;
@@ -171,6 +172,22 @@ lla_status lla_prefill_state(const void *k, const void *v, const float *g, float
     A.B = B; A.H = H; A.T = T; A.dk = dk; A.dv = dv; A.Ls = Ls; A.in_dt = in_dt;
     A.workspace = workspace; A.stream = stream;
     return prefill_state(A) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+}
+
+lla_status lla_lambda_mlp(const void *d, const float *W1, const float *W2, const float *b,
+                          float *lambda, int B, int H, int T, int Dd, int L, lla_dtype in_dt,
+                          void *stream)
+{
+    if (B < 0 || H < 0 || T < 0) return LLA_ERR_INVALID_ARGUMENT;
+    if (in_dt != LLA_F32 && in_dt != LLA_BF16) return LLA_ERR_INVALID_ARGUMENT;
+    if (Dd < 1 || Dd > 256 || L < 1 || L > 32) return LLA_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)B * H * T == 0) return LLA_OK;
+    if ((long long)B * H * T > (1LL << 38)) return LLA_ERR_UNSUPPORTED_SHAPE;
+    if (!d || !W1 || !W2 || !b || !lambda) return LLA_ERR_INVALID_ARGUMENT;
+    LambdaMlpArgs A;
+    A.d = d; A.W1 = W1; A.W2 = W2; A.bias = b; A.lam = lambda;
+    A.B = B; A.H = H; A.T = T; A.Dd = Dd; A.L = L; A.in_dt = in_dt; A.stream = stream;
+    return lambda_mlp(A) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
 }
 
 }  // extern "C"
