@@ -41,7 +41,6 @@ using namespace sm100;
 constexpr int kTile = 128;       // tokens per tile (MMA M)
 constexpr int kD = 128;          // dk = dv
 constexpr int kTileLevels = 7;   // levels inside a tile: bit_length(a ^ b) <= 7
-constexpr int kThreads = 256;  // two warpgroups; warps w and w+4 share TMEM lanes
 constexpr uint32_t kBuf = kTile * kD * 2;  // one bf16 128x128 operand: 32 KB
 constexpr uint32_t kHalf = kBuf / 2;       // one 64-column swizzled block
 constexpr uint32_t kWaitIters = 1u << 22;  // bounded waits (~0.5 s with back-off)
@@ -333,23 +332,31 @@ lla_node_fixup_kernel(const TcParams prm)
 }
 
 // ======================================================= read-out consumer
-// CTA per tile; every node is published before this kernel starts.
+// CTA per tile; every node is published before this kernel starts.  Warps
+// 0-7 (thread = (row, 64 columns)) drain tensor memory; warp 8 issues the
+// TMA loads and the MMAs.  The two hand off through mbarriers only, so a node
+// buffer is refilled as soon as the MMA reading it completes.
 
+constexpr int kConsThreads = 288;  // 8 epilogue warps + 1 control warp
+constexpr int kEpiThreads = 256;
 
 struct __align__(1024) ConsSmem {
     uint8_t q[kBuf];
-    uint8_t k[kBuf];   // K, then P (masked scores), then node stage 0
+    uint8_t k[kBuf];   // K, then node stage 0, then (with q) the output staging
     uint8_t v[kBuf];   // V, then node stage 1
     float gam[kTile];
     float kf[kTile];              // exp(gamma_e - gamma_b), e = last key of b's 16-key chunk
     float lam[kTile * kLamLd];
     float wgt[kMaxPath * kTile];  // read-out weight of each path level per row
-    uint64_t bar_load, bar_s, bar_pv, bar_node[2], bar_u[2];
+    double pj[kMaxPath + 1];      // P at the path nodes, then P_i
+    uint64_t bar_load, bar_s, bar_pready, bar_pv, bar_pvfree, bar_node[2], bar_u[2], bar_ufree[2];
     uint32_t tmem;
 };
 
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
 template <typename OutT>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kConsThreads, 2)
 lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                             const __grid_constant__ CUtensorMap map_v,
                             const __grid_constant__ CUtensorMap map_node,
@@ -360,23 +367,27 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
                                                 ~uintptr_t(1023));
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
-    const int row = tid & (kTile - 1);
-    const int half = tid >> 7;
     const int NT = prm.NT, BH = prm.BH;
     // tile-major, last tiles first: co-resident tiles share their deep nodes,
-    // and the nodes the producer wrote last are still in L2
+    // and the nodes written last are still in L2
     const int rev = NT * BH - 1 - (int)blockIdx.x;
     const int i = rev / BH;
     const int bh = rev - i * BH;
+    const double *Pb = prm.P + (long long)bh * (NT + 1);
+    int npath = 0;
+    for (int j = i; j > 0; j -= (j & -j)) npath++;
 
-    if (tid == 0) {
+    if (tid == kEpiThreads) {
         mbar_init(&s.bar_load, 1);
         mbar_init(&s.bar_s, 1);
+        mbar_init(&s.bar_pready, kEpiThreads);
         mbar_init(&s.bar_pv, 1);
-        mbar_init(&s.bar_node[0], 1);
-        mbar_init(&s.bar_node[1], 1);
-        mbar_init(&s.bar_u[0], 1);
-        mbar_init(&s.bar_u[1], 1);
+        mbar_init(&s.bar_pvfree, kEpiThreads);
+        for (int b = 0; b < 2; b++) {
+            mbar_init(&s.bar_node[b], 1);
+            mbar_init(&s.bar_u[b], 1);
+            mbar_init(&s.bar_ufree[b], kEpiThreads);
+        }
         fence_mbar_init();
         tma_prefetch_map(&map_q);
         tma_prefetch_map(&map_k);
@@ -395,203 +406,267 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
         tmem_alloc(&s.tmem, 256);
         tmem_relinquish();
     }
+    const int row = tid & (kTile - 1);
+    const int half = (tid >> 7) & 1;
     const int tile_rows = min(kTile, prm.T - i * kTile);
     const bool row_ok = row < tile_rows;
     const long long tok = (long long)bh * prm.T + (long long)i * kTile + row;
     const float *lam_row = prm.lam + tok * prm.L;
-    const double *Pb = prm.P + (long long)bh * (NT + 1);
-    if (half == 0) {
+    float gam_a = 0.f;
+    if (tid < kEpiThreads) {
+        // every global load first, then the stores that depend on them
+        gam_a = prm.gamma[((long long)bh * NT + i) * kTile + row];
+        float lv[kTileLevels + 1];
+        if (half == 0) {
 #pragma unroll
-        for (int l = 0; l <= kTileLevels; l++)
-            s.lam[row * kLamLd + l] = (row_ok && l < prm.L) ? lam_row[l] : 0.f;
-    }
-    const float gam_a = prm.gamma[((long long)bh * NT + i) * kTile + row];
-    if (half == 0) s.gam[row] = gam_a;
-    __syncthreads();
-    if (half == 0) s.kf[row] = __expf(s.gam[row | 15] - gam_a);
-    // read-out weights: path level n (node j_n, level m_n = ctz(j_n)) of row a:
-    //   lambda_a[8 + m_n] * exp(gamma_a + P_i - P_{j_n}); the halves split the levels
-    int npath = 0;
-    {
-        const double Pi = Pb[i];
-        int n = 0;
-        for (int j = i; j > 0; j -= (j & -j), n++) {
-            if ((n & 1) == half) {
-                const int lev = kTileLevels + 1 + (__ffs(j) - 1);
-                s.wgt[n * kTile + row] =
-                    row_ok ? lam_row[lev] * __expf(gam_a + (float)(Pi - Pb[j])) : 0.f;
+            for (int l = 0; l <= kTileLevels; l++) lv[l] = (row_ok && l < prm.L) ? lam_row[l] : 0.f;
+        }
+        // read-out weights: path level n (node j_n, level m_n = ctz(j_n)):
+        //   lambda_a[8 + m_n] * exp(gamma_a + P_i - P_{j_n}); the halves split the levels
+        float lw[kMaxPath];
+        {
+            int j = i;
+#pragma unroll
+            for (int n = 0; n < kMaxPath; n++) {
+                lw[n] = 0.f;
+                if (j > 0) {
+                    if ((n & 1) == half && row_ok) lw[n] = lam_row[kTileLevels + 1 + (__ffs(j) - 1)];
+                    j -= (j & -j);
+                }
             }
         }
-        npath = n;
+        if (tid < npath) {  // P at the path nodes: thread n clears the n lowest set bits of i
+            int j = i;
+            for (int c = 0; c < tid; c++) j -= (j & -j);
+            s.pj[tid] = Pb[j];
+        }
+        if (tid == 0) s.pj[kMaxPath] = Pb[i];
+        if (half == 0) {
+            s.gam[row] = gam_a;
+#pragma unroll
+            for (int l = 0; l <= kTileLevels; l++) s.lam[row * kLamLd + l] = lv[l];
+        }
+        epi_sync();
+        {
+            const double Pi = s.pj[kMaxPath];
+#pragma unroll
+            for (int n = 0; n < kMaxPath; n++)
+                if (n < npath && (n & 1) == half)
+                    s.wgt[n * kTile + row] = lw[n] * __expf(gam_a + (float)(Pi - s.pj[n]));
+        }
+        epi_sync();
+        if (half == 0) s.kf[row] = __expf(s.gam[row | 15] - gam_a);
     }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tm = s.tmem;
     const uint32_t slot[2] = {tm, tm + 128};
-    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    uint8_t *const nd[2] = {s.k, s.v};
 
-    // ---- S = Q K^T
-    if (tid == 0) {
-        if (!mbar_wait(&s.bar_load, 0, kWaitIters)) set_err(prm.err, kErrLoadTimeout);
-        tc_fence_after_sync();
-        mma_kk(slot[0], s.q, s.k, idesc_bf16_f32(128, 128, false, false));
-        umma_commit(&s.bar_s);
-    }
-    if (!mbar_wait(&s.bar_s, 0, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
-    tc_fence_after_sync();
-
-    // ---- P = S . M  (thread = query row, 64 keys), bf16 into the K buffer
-    {
-        const int a = row;
-        const float *lam_a = s.lam + a * kLamLd;
-#pragma unroll 1
-        for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
-            // the load is warp-collective: every lane issues it, whatever its row
-            float r[16];
-            tmem_ld16(slot[0] + lane_off + c0, r);
-            tmem_ld_wait();
-            uint4 w[2];
-            __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(w);
-            if (c0 > a || !row_ok) {  // strictly above the diagonal, or a row past T
-                w[0] = make_uint4(0u, 0u, 0u, 0u);
-                w[1] = w[0];
-            } else if (c0 + 16 <= a) {
-                // a whole 16-key chunk below the row: one level, and the decay
-                // exp(gamma_a - gamma_b) = exp(gamma_a - gamma_e) exp(gamma_e - gamma_b)
-                // with e = c0 + 15, both factors <= 1
-                const int lev = 32 - __clz(a ^ c0);
-                const float ra = lam_a[lev] * __expf(gam_a - s.gam[c0 + 15]);
+    if (warp == 8) {
+        // ---------------- control warp (one lane issues)
+        if ((tid & 31) == 0) {
+            auto load_node = [&](int st, int j) {
+                mbar_arrive_expect_tx(&s.bar_node[st], kBuf);
+                tma_load_3d(nd[st], &map_node, &s.bar_node[st], 0, 0, bh * NT + j);
+                tma_load_3d(nd[st] + kHalf, &map_node, &s.bar_node[st], 64, 0, bh * NT + j);
+            };
+            const uint32_t id_kmn = idesc_bf16_f32(128, 128, false, true);
+            if (!mbar_wait(&s.bar_load, 0, kWaitIters)) set_err(prm.err, kErrLoadTimeout);
+            tc_fence_after_sync();
+            mma_kk(slot[0], s.q, s.k, idesc_bf16_f32(128, 128, false, false));
+            umma_commit(&s.bar_s);
+            // path nodes in order: jn[n] computed on the fly
+            int jnext = i;
+            if (npath > 0) {
+                if (!mbar_wait(&s.bar_s, 0, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
+                load_node(0, jnext);  // the K buffer is free once S is done
+                jnext -= (jnext & -jnext);
+            }
+            // O = P V: P from tensor memory once the epilogue has stored it
+            if (!mbar_wait(&s.bar_pready, 0, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
+            tc_fence_after_sync();
 #pragma unroll
-                for (int u = 0; u < 8; u++)
-                    h[u] = __floats2bfloat162_rn(r[2 * u] * ra * s.kf[c0 + 2 * u],
-                                                 r[2 * u + 1] * ra * s.kf[c0 + 2 * u + 1]);
-            } else {
-#pragma unroll
-                for (int u = 0; u < 8; u++) {
-                    float x[2];
-#pragma unroll
-                    for (int e = 0; e < 2; e++) {
-                        const int b = c0 + 2 * u + e;
-                        x[e] = 0.f;
-                        if (b <= a) {
-                            const int lev = 32 - __clz(a ^ b);
-                            x[e] = r[2 * u + e] * lam_a[lev] * __expf(gam_a - s.gam[b]);
-                        }
+            for (int kk = 0; kk < 8; kk++)
+                umma_bf16_tmem_a(slot[1], slot[0] + kk * 8,
+                                 desc_sw128(smem_u32(s.v) + kk * 2048, kHalf, 1024), id_kmn, kk > 0 ? 1u : 0u);
+            umma_commit(&s.bar_pv);
+            if (npath > 0) {
+                if (!mbar_wait(&s.bar_pv, 0, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
+                if (npath > 1) {
+                    load_node(1, jnext);  // the V buffer is free once P V is done
+                    jnext -= (jnext & -jnext);
+                }
+                // level 0 into slot 0 (P has been consumed)
+                if (!mbar_wait(&s.bar_node[0], 0, kWaitIters)) set_err(prm.err, kErrLoadTimeout);
+                tc_fence_after_sync();
+                mma_kmn(slot[0], s.q, nd[0], id_kmn);
+                umma_commit(&s.bar_u[0]);
+            }
+            for (int n = 0; n < npath; n++) {
+                const int st = n & 1, st1 = st ^ 1;
+                if (n + 1 < npath) {
+                    // slot st1 is free once level n-1 (or, for level 1, P V) is drained
+                    if (n == 0) {
+                        if (!mbar_wait(&s.bar_pvfree, 0, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
+                    } else {
+                        if (!mbar_wait(&s.bar_ufree[st1], ((n - 1) >> 1) & 1, kWaitIters))
+                            set_err(prm.err, kErrMmaTimeout);
                     }
-                    h[u] = __floats2bfloat162_rn(x[0], x[1]);
+                    if (!mbar_wait(&s.bar_node[st1], ((n + 1) >> 1) & 1, kWaitIters)) set_err(prm.err, kErrLoadTimeout);
+                    tc_fence_after_sync();
+                    mma_kmn(slot[st1], s.q, nd[st1], id_kmn);
+                    umma_commit(&s.bar_u[st1]);
+                }
+                if (n + 2 < npath) {
+                    // node buffer st is free once level n's product is done
+                    if (!mbar_wait(&s.bar_u[st], (n >> 1) & 1, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
+                    load_node(st, jnext);
+                    jnext -= (jnext & -jnext);
                 }
             }
-            const int ch = (c0 & 63) >> 3;
-            *reinterpret_cast<uint4 *>(s.k + half * kHalf + sw128_offset(a, ch)) = w[0];
-            *reinterpret_cast<uint4 *>(s.k + half * kHalf + sw128_offset(a, ch + 1)) = w[1];
         }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before_sync();
-    __syncthreads();
-    // ---- O = P V into slot 1; then the first two path nodes into the freed buffers
-    uint8_t *const nd[2] = {s.k, s.v};
-    if (tid == 0) {
+    } else {
+        // ---------------- epilogue warps
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        if (!mbar_wait(&s.bar_s, 0, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
         tc_fence_after_sync();
-        mma_kmn(slot[1], s.k, s.v, idesc_bf16_f32(128, 128, false, true));
-        umma_commit(&s.bar_pv);
-        if (npath > 0) {
-            if (!mbar_wait(&s.bar_pv, 0, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
-            int n = 0;
-            for (int j = i; j > 0 && n < 2; j -= (j & -j), n++) {
-                mbar_arrive_expect_tx(&s.bar_node[n], kBuf);
-                tma_load_3d(nd[n], &map_node, &s.bar_node[n], 0, 0, bh * NT + j);
-                tma_load_3d(nd[n] + kHalf, &map_node, &s.bar_node[n], 64, 0, bh * NT + j);
+        // P = S . M  (thread = query row, 64 keys), packed bf16 pairs in registers
+        uint32_t pk[32];
+        {
+            const int a = row;
+            const float *lam_a = s.lam + a * kLamLd;
+#pragma unroll
+            for (int cc = 0; cc < 4; cc += 2) {
+                const int c0 = half * 64 + cc * 16;
+                // the loads are warp-collective: every lane issues them, whatever its row
+                float r2[2][16];
+                tmem_ld16(slot[0] + lane_off + c0, r2[0]);
+                tmem_ld16(slot[0] + lane_off + c0 + 16, r2[1]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int q2 = 0; q2 < 2; q2++) {
+                    const int cb = c0 + q2 * 16;
+                    const float *r = r2[q2];
+                    __nv_bfloat162 h[8];
+                    if (cb > a || !row_ok) {  // strictly above the diagonal, or a row past T
+#pragma unroll
+                        for (int u = 0; u < 8; u++) h[u] = __floats2bfloat162_rn(0.f, 0.f);
+                    } else if (cb + 16 <= a) {
+                        // a whole 16-key chunk below the row: one level, and the decay
+                        // exp(gamma_a - gamma_b) = exp(gamma_a - gamma_e) exp(gamma_e - gamma_b)
+                        // with e = cb + 15, both factors <= 1
+                        const int lev = 32 - __clz(a ^ cb);
+                        const float ra = lam_a[lev] * __expf(gam_a - s.gam[cb + 15]);
+#pragma unroll
+                        for (int u = 0; u < 8; u++)
+                            h[u] = __floats2bfloat162_rn(r[2 * u] * ra * s.kf[cb + 2 * u],
+                                                         r[2 * u + 1] * ra * s.kf[cb + 2 * u + 1]);
+                    } else {
+#pragma unroll
+                        for (int u = 0; u < 8; u++) {
+                            float x[2];
+#pragma unroll
+                            for (int e = 0; e < 2; e++) {
+                                const int b = cb + 2 * u + e;
+                                x[e] = 0.f;
+                                if (b <= a) {
+                                    const int lev = 32 - __clz(a ^ b);
+                                    x[e] = r[2 * u + e] * lam_a[lev] * __expf(gam_a - s.gam[b]);
+                                }
+                            }
+                            h[u] = __floats2bfloat162_rn(x[0], x[1]);
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; u++) pk[(cc + q2) * 8 + u] = *reinterpret_cast<uint32_t *>(&h[u]);
+                }
             }
         }
-    }
-    if (!mbar_wait(&s.bar_pv, 0, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
-    tc_fence_after_sync();
-    float o[64];
-#pragma unroll
-    for (int c0 = 0; c0 < 64; c0 += 16) {
-        float r[16];
-        tmem_ld16(slot[1] + lane_off + half * 64 + c0, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int u = 0; u < 16; u++) o[c0 + u] = r[u];
-    }
-    tc_fence_before_sync();
-    __syncthreads();  // slot 1 drained
-    tc_fence_after_sync();
+        // P replaces S in tensor memory (keys 2c, 2c+1 in column c) once every
+        // epilogue thread has read its S columns
+        tc_fence_before_sync();
+        epi_sync();
+        tc_fence_after_sync();
+        tmem_st16(slot[0] + lane_off + half * 32, *reinterpret_cast<const float(*)[16]>(pk));
+        tmem_st16(slot[0] + lane_off + half * 32 + 16, *reinterpret_cast<const float(*)[16]>(pk + 16));
+        tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(&s.bar_pready);
 
-    // ---- read-out: U_n = Q Node_{j_n} into slot n&1, drained with fp32 weights
-    if (tid == 0 && npath > 0) {
-        if (!mbar_wait(&s.bar_node[0], 0, kWaitIters)) set_err(prm.err, kErrLoadTimeout);
+        if (!mbar_wait(&s.bar_pv, 0, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
         tc_fence_after_sync();
-        mma_kmn(slot[0], s.q, nd[0], idesc_bf16_f32(128, 128, false, true));
-        umma_commit(&s.bar_u[0]);
-    }
-    int jn2 = i;  // node index of level n+2, advanced as levels are consumed
-    if (jn2 > 0) jn2 -= (jn2 & -jn2);
-    if (jn2 > 0) jn2 -= (jn2 & -jn2);
-    for (int n = 0; n < npath; n++) {
-        const int st = n & 1;
-        if (tid == 0 && n + 1 < npath) {
-            const int st1 = (n + 1) & 1;
-            if (!mbar_wait(&s.bar_node[st1], ((n + 1) >> 1) & 1, kWaitIters)) set_err(prm.err, kErrLoadTimeout);
-            tc_fence_after_sync();
-            mma_kmn(slot[st1], s.q, nd[st1], idesc_bf16_f32(128, 128, false, true));
-            umma_commit(&s.bar_u[st1]);
-        }
-        if (!mbar_wait(&s.bar_u[st], (n >> 1) & 1, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
-        tc_fence_after_sync();
-        const float w = s.wgt[n * kTile + row];
+        float o[64];
+        {
+            float r2[2][16];
 #pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 16) {
-            float r[16];
-            tmem_ld16(slot[st] + lane_off + half * 64 + c0, r);
-            tmem_ld_wait();
+            for (int c0 = 0; c0 < 64; c0 += 32) {
+                tmem_ld16(slot[1] + lane_off + half * 64 + c0, r2[0]);
+                tmem_ld16(slot[1] + lane_off + half * 64 + c0 + 16, r2[1]);
+                tmem_ld_wait();
 #pragma unroll
-            for (int u = 0; u < 16; u++) o[c0 + u] = fmaf(w, r[u], o[c0 + u]);
+                for (int u = 0; u < 16; u++) {
+                    o[c0 + u] = r2[0][u];
+                    o[c0 + 16 + u] = r2[1][u];
+                }
+            }
         }
         tc_fence_before_sync();
-        __syncthreads();  // slot st drained; MMA n done, so node buffer st is free
-        tc_fence_after_sync();
-        if (tid == 0 && n + 2 < npath) {
-            mbar_arrive_expect_tx(&s.bar_node[st], kBuf);
-            tma_load_3d(nd[st], &map_node, &s.bar_node[st], 0, 0, bh * NT + jn2);
-            tma_load_3d(nd[st] + kHalf, &map_node, &s.bar_node[st], 64, 0, bh * NT + jn2);
-        }
-        if (jn2 > 0) jn2 -= (jn2 & -jn2);
-    }
+        mbar_arrive(&s.bar_pvfree);
 
-    // ---- store: stage the tile in the (now idle) Q/K buffers, then TMA
-    // (rows past T are clipped by the tensor map)
-    if (sizeof(OutT) == 4) {
-        uint8_t *stage = s.q;  // four 32-column fp32 boxes, 64 KB across q and k
+        // read-out: U_n = Q Node_{j_n} in slot n&1, drained with the fp32 weights
+        for (int n = 0; n < npath; n++) {
+            const int st = n & 1;
+            const float w = s.wgt[n * kTile + row];
+            if (!mbar_wait(&s.bar_u[st], (n >> 1) & 1, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
+            tc_fence_after_sync();
+            float r2[2][16];
 #pragma unroll
-        for (int c = 0; c < 16; c++)
-            *reinterpret_cast<float4 *>(stage + f32_stage_off(row, half * 16 + c)) =
-                make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
-    } else {
+            for (int c0 = 0; c0 < 64; c0 += 32) {
+                tmem_ld16(slot[st] + lane_off + half * 64 + c0, r2[0]);
+                tmem_ld16(slot[st] + lane_off + half * 64 + c0 + 16, r2[1]);
+                tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 8; c++) {
-            uint4 w;
-            __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&w);
-#pragma unroll
-            for (int u = 0; u < 4; u++) h[u] = __floats2bfloat162_rn(o[8 * c + 2 * u], o[8 * c + 2 * u + 1]);
-            *reinterpret_cast<uint4 *>(s.q + half * kHalf + sw128_offset(row, c)) = w;
+                for (int u = 0; u < 16; u++) {
+                    o[c0 + u] = fmaf(w, r2[0][u], o[c0 + u]);
+                    o[c0 + 16 + u] = fmaf(w, r2[1][u], o[c0 + 16 + u]);
+                }
+            }
+            tc_fence_before_sync();
+            mbar_arrive(&s.bar_ufree[st]);
         }
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (tid == 0) {
+
+        // ---- store: stage the tile in the Q/K buffers (every product that read
+        // them is complete), then TMA; rows past T are clipped by the tensor map
         if (sizeof(OutT) == 4) {
 #pragma unroll
-            for (int b = 0; b < 4; b++) tma_store_3d(&map_out, s.q + b * (kTile * 128), b * 32, i * kTile, bh);
+            for (int c = 0; c < 16; c++)
+                *reinterpret_cast<float4 *>(s.q + f32_stage_off(row, half * 16 + c)) =
+                    make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
         } else {
 #pragma unroll
-            for (int h = 0; h < 2; h++) tma_store_3d(&map_out, s.q + h * kHalf, h * 64, i * kTile, bh);
+            for (int c = 0; c < 8; c++) {
+                uint4 w4;
+                __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&w4);
+#pragma unroll
+                for (int u = 0; u < 4; u++) h[u] = __floats2bfloat162_rn(o[8 * c + 2 * u], o[8 * c + 2 * u + 1]);
+                *reinterpret_cast<uint4 *>(s.q + half * kHalf + sw128_offset(row, c)) = w4;
+            }
         }
-        tma_store_commit();
-        tma_store_wait_read();  // shared memory may be released; the writes finish with the kernel
+        fence_proxy_async_smem();
+        epi_sync();
+        if (tid == 0) {
+            if (sizeof(OutT) == 4) {
+#pragma unroll
+                for (int b = 0; b < 4; b++) tma_store_3d(&map_out, s.q + b * (kTile * 128), b * 32, i * kTile, bh);
+            } else {
+#pragma unroll
+                for (int h = 0; h < 2; h++) tma_store_3d(&map_out, s.q + h * kHalf, h * 64, i * kTile, bh);
+            }
+            tma_store_commit();
+            tma_store_wait_read();  // shared memory may be released; the writes finish with the kernel
+        }
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -732,7 +807,7 @@ static cudaError_t launch_consumer(const CUtensorMap &mq, const CUtensorMap &mk,
     cudaError_t e = cudaFuncSetAttribute(lla_readout_consumer_kernel<OutT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    lla_readout_consumer_kernel<OutT><<<grid, kThreads, smem, st>>>(mq, mk, mv, mn, mo, prm);
+    lla_readout_consumer_kernel<OutT><<<grid, kConsThreads, smem, st>>>(mq, mk, mv, mn, mo, prm);
     return cudaSuccess;
 }
 
