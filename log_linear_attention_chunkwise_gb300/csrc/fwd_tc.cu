@@ -146,6 +146,7 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
     const int vblk = slice >> 1;                       // 64-column V block holding the slice
     const uint32_t voff = (uint32_t)(slice & 1) * 64;  // the slice's byte offset in a block row
 
+    grid_launch_dependents();  // the fix-up and read-out may start in this grid's tail
     if (tid == 0) {
         for (int b = 0; b < kWalkStages; b++) mbar_init(&s.bar_load[b], 1);
         for (int b = 0; b < 2; b++) {
@@ -292,6 +293,8 @@ __global__ void __launch_bounds__(kFixThreads)
 lla_node_fixup_kernel(const TcParams prm)
 {
     __shared__ double pseg[kFixMaxSeg + 1];  // P at segment boundaries
+    grid_launch_dependents();
+    grid_dependency_wait();  // the walkers' segment totals
     const long long bh = blockIdx.y;
     const int NT = prm.NT, nseg = prm.nseg_full;
     const double *Pb = prm.P + bh * (NT + 1);
@@ -481,6 +484,9 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
             int jnext = i;
             if (npath > 0) {
                 if (!mbar_wait(&s.bar_s, 0, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
+                // the nodes come from the previous launches; everything before this
+                // point reads only inputs and the gate sums
+                grid_dependency_wait();
                 load_node(0, jnext);  // the K buffer is free once S is done
                 jnext -= (jnext & -jnext);
             }
@@ -798,17 +804,36 @@ int tc_launches(int T)
 static_assert(sizeof(WalkSmem) + 1024 <= 113 * 1024, "walker must fit two CTAs per SM");
 static_assert(sizeof(ConsSmem) + 1024 <= 113 * 1024, "consumer must fit two CTAs per SM");
 
+// Launch configuration, optionally as a programmatic dependent of the
+// previous kernel in the stream (it may start before that one finishes and
+// synchronises with griddepcontrol.wait).
+static cudaLaunchConfig_t launch_cfg(dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool dependent,
+                                     cudaLaunchAttribute *attr)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    attr->id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr->val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = dependent ? 1 : 0;
+    return cfg;
+}
+
 template <typename OutT>
 static cudaError_t launch_consumer(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                                    const CUtensorMap &mn, const CUtensorMap &mo, const TcParams &prm,
-                                   int grid, cudaStream_t st)
+                                   int grid, cudaStream_t st, bool dependent)
 {
     const size_t smem = sizeof(ConsSmem) + 1024;
     cudaError_t e = cudaFuncSetAttribute(lla_readout_consumer_kernel<OutT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    lla_readout_consumer_kernel<OutT><<<grid, kConsThreads, smem, st>>>(mq, mk, mv, mn, mo, prm);
-    return cudaSuccess;
+    cudaLaunchAttribute attr;
+    cudaLaunchConfig_t cfg = launch_cfg(dim3(grid), dim3(kConsThreads), smem, st, dependent, &attr);
+    return cudaLaunchKernelEx(&cfg, lla_readout_consumer_kernel<OutT>, mq, mk, mv, mn, mo, prm);
 }
 
 cudaError_t tc_fwd(const TcFwdArgs &A)
@@ -850,11 +875,17 @@ cudaError_t tc_fwd(const TcFwdArgs &A)
         if (e != cudaSuccess) return e;
         const int nseg = (NT - 1 + kSeg - 1) / kSeg;
         lla_node_walker_kernel<<<dim3(nseg, kSlices, BH), kWalkThreads, wsmem, st>>>(mk, mv, prm);
-        if (prm.nseg_full > 0)
-            lla_node_fixup_kernel<<<dim3(kD * kD / 8 / kFixThreads, BH), kFixThreads, 0, st>>>(prm);
+        if (prm.nseg_full > 0) {
+            cudaLaunchAttribute attr;
+            cudaLaunchConfig_t cfg =
+                launch_cfg(dim3(kD * kD / 8 / kFixThreads, BH), dim3(kFixThreads), 0, st, true, &attr);
+            e = cudaLaunchKernelEx(&cfg, lla_node_fixup_kernel, prm);
+            if (e != cudaSuccess) return e;
+        }
     }
-    e = out32 ? launch_consumer<float>(mq, mk, mv, mn, mo, prm, NT * BH, st)
-              : launch_consumer<__nv_bfloat16>(mq, mk, mv, mn, mo, prm, NT * BH, st);
+    // with nodes to read, the read-out starts in the tail of the node launches
+    e = out32 ? launch_consumer<float>(mq, mk, mv, mn, mo, prm, NT * BH, st, NT > 1)
+              : launch_consumer<__nv_bfloat16>(mq, mk, mv, mn, mo, prm, NT * BH, st, NT > 1);
     if (e != cudaSuccess) return e;
     return cudaPeekAtLastError();
 }

@@ -132,6 +132,22 @@ __device__ __forceinline__ void fence_proxy_async_global()
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// ------------------------------------------- programmatic dependent launch
+
+// Let the next kernel in the stream (launched with programmatic stream
+// serialisation) start its CTAs once every CTA of this grid has run this.
+__device__ __forceinline__ void grid_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until the grid this one depends on has completed and its memory
+// operations are visible.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------------ tensor memory
 
 // Whole warp: allocate ncols (power of two >= 32) TMEM columns; the base
