@@ -17,7 +17,9 @@ What each function follows (page "Log-Linear Attention", gist.science
   ssd                the plain gated linear-attention scan (§1 / §3 Mamba-2),
                      which the operator reduces to when every lambda is 1;
   lambda_mlp         page "Adaptive memory decay for Log-Linear Attention",
-                     §LambdaMLPSoftplus: lambda = softplus((d W1) W2 + b).
+                     §LambdaMLPSoftplus: lambda = softplus((d W1) W2 + b);
+  backward           the derivatives of the §2.2 double sum, term by term
+                     (the pages give no backward; see the C source).
 Every function is pinned by tests in ``tests/test_oracle_pins.py``.
 """
 
@@ -62,9 +64,10 @@ def _load():
         lib.oracle_ssd.argtypes = [P] * 5 + [I] * 5
         lib.oracle_level.argtypes = [I, I]
         lib.oracle_lambda_mlp.argtypes = [P] * 5 + [I] * 3
+        lib.oracle_backward.argtypes = [P] * 11 + [I] * 6
         for name in ("oracle_naive", "oracle_naive_rows", "oracle_fenwick", "oracle_decode_step",
                      "oracle_state_closed_form", "oracle_ssd", "oracle_level", "oracle_lambda_mlp",
-                     "oracle_num_threads"):
+                     "oracle_num_threads", "oracle_backward"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -190,3 +193,20 @@ def lambda_mlp(d, W1, W2, b) -> np.ndarray:
     _check(_load().oracle_lambda_mlp(_ptr(dd), _ptr(W1), _ptr(W2), _ptr(b), _ptr(out),
                                      dd.shape[0], Dd, L), "oracle_lambda_mlp")
     return out.reshape(*lead, L)
+
+
+def backward(q, k, v, g, lam, dout):
+    """Gradients (dq, dk, dv, dg, dlam) of sum(dout * naive(q, k, v, g, lam))."""
+    q, k, v, g, lam, dout = map(_f64, (q, k, v, g, lam, dout))
+    B, H, T, Dk = q.shape
+    Dv = v.shape[-1]
+    L = lam.shape[-1]
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    dg = np.zeros_like(g)
+    dlam = np.zeros_like(lam)
+    _check(_load().oracle_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(lam), _ptr(dout),
+                                   _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dlam),
+                                   B, H, T, Dk, Dv, L), "oracle_backward")
+    return dq, dk, dv, dg, dlam

@@ -494,3 +494,81 @@ int oracle_lambda_mlp(const double *d, const double *W1, const double *W2,
     }
     return L > 64 ? -2 : 0;
 }
+
+/*
+ * Gradients of L = sum_t dout_t . o_t with o_t the defining double sum of
+ * "Log-Linear Attention" §2.2 (Mamba-2 gate of §3).  The pages print no
+ * backward; each term below is the derivative of one summand
+ *     a_ts = lam_t[l] * E_ts * (q_t . k_s) * (dout_t . v_s),
+ *     E_ts = exp(G_t - G_s),  l = level(t,s),  s <= t,
+ * accumulated pair by pair:
+ *     dq_t      += lam_t[l] E_ts (dout_t . v_s) k_s
+ *     dk_s      += lam_t[l] E_ts (dout_t . v_s) q_t
+ *     dv_s      += lam_t[l] E_ts (q_t . k_s) dout_t
+ *     dlam_t[l] += E_ts (q_t . k_s)(dout_t . v_s)
+ *     dG_t += a_ts,  dG_s -= a_ts
+ * and, since G_u = g_0 + ... + g_u, dg_r = sum_{u >= r} dG_u.
+ * Arrays as for oracle_naive; dout [B,H,T,dv]; outputs dq [B,H,T,dk],
+ * dk [B,H,T,dk], dv [B,H,T,dv], dg [B,H,T], dlam [B,H,T,L] (overwritten).
+ */
+int oracle_backward(const double *q, const double *k, const double *v,
+                    const double *g, const double *lam, const double *dout,
+                    double *dq, double *dk, double *dv, double *dg,
+                    double *dlam, int64_t B, int64_t H, int64_t T, int64_t Dk,
+                    int64_t Dv, int64_t L)
+{
+    if (B < 0 || H < 0 || T < 0 || Dk <= 0 || Dv <= 0 || L <= 0)
+        return -1;
+    if (T > 0 && bit_length((uint64_t)(T - 1)) > L - 1)
+        return -2;
+    int64_t BH = B * H;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t bh = 0; bh < BH; bh++) {
+        const double *qh = q + bh * T * Dk, *kh = k + bh * T * Dk;
+        const double *vh = v + bh * T * Dv, *dh = dout + bh * T * Dv;
+        const double *lh = lam + bh * T * L;
+        double *dqh = dq + bh * T * Dk, *dkh = dk + bh * T * Dk;
+        double *dvh = dv + bh * T * Dv, *dgh = dg + bh * T;
+        double *dlh = dlam + bh * T * L;
+        memset(dqh, 0, sizeof(double) * (size_t)(T * Dk));
+        memset(dkh, 0, sizeof(double) * (size_t)(T * Dk));
+        memset(dvh, 0, sizeof(double) * (size_t)(T * Dv));
+        memset(dlh, 0, sizeof(double) * (size_t)(T * L));
+        double *G = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+        double *dG = (double *)calloc((size_t)(T > 0 ? T : 1), sizeof(double));
+        if (!G || !dG) {
+            free(G);
+            free(dG);
+            bad |= 1;
+            continue;
+        }
+        cumsum(g + bh * T, T, G);
+        for (int64_t t = 0; t < T; t++) {
+            for (int64_t s = 0; s <= t; s++) {
+                int lev = oracle_level(t, s);
+                double E = exp(G[t] - G[s]);
+                double qk = dot(qh + t * Dk, kh + s * Dk, Dk);
+                double ov = dot(dh + t * Dv, vh + s * Dv, Dv);
+                double A = lh[t * L + lev] * E;
+                for (int64_t r = 0; r < Dk; r++) {
+                    dqh[t * Dk + r] += A * ov * kh[s * Dk + r];
+                    dkh[s * Dk + r] += A * ov * qh[t * Dk + r];
+                }
+                for (int64_t c = 0; c < Dv; c++)
+                    dvh[s * Dv + c] += A * qk * dh[t * Dv + c];
+                dlh[t * L + lev] += E * qk * ov;
+                dG[t] += A * qk * ov;
+                dG[s] -= A * qk * ov;
+            }
+        }
+        double run = 0.0;
+        for (int64_t r = T - 1; r >= 0; r--) {
+            run += dG[r];
+            dgh[r] = run;
+        }
+        free(G);
+        free(dG);
+    }
+    return bad ? -3 : 0;
+}

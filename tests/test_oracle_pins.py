@@ -9,6 +9,12 @@ Page "Log-Linear Attention" (gist.science 2506.04761), technical summary:
 Page "Adaptive memory decay for Log-Linear Attention", §LambdaMLPSoftplus:
   softplus(0.54) is about 1.0 (the lambda initialisation the workloads centre on).
 
+The backward (no formula on the pages) is pinned to the forward double sum by
+central finite differences, and by identities of that sum: it is linear in each
+of q, k, v and lambda (so, by Euler's theorem, <x, dx> equals the loss for each),
+dq is the forward with (q, k, v) -> (dout, v, k), and the loss depends on G only
+through differences, so dg_0 = sum_u dG_u = 0.
+
 Each test below would fail on a plausible slip in the oracle: a wrong level
 index (bucket tests, hand table), an exclusive instead of inclusive gate sum or
 a sign error in the decay (hand-expanded T=3 case, SSD reduction), a dropped
@@ -313,3 +319,45 @@ def test_lambda_mlp_softplus_identities():
     np.testing.assert_allclose(big, z + 60.0, rtol=1e-12)
     small = oracle.lambda_mlp(d, W1, W2, b - 60.0)
     np.testing.assert_allclose(small, np.exp(z - 60.0), rtol=1e-9)
+
+
+def loss_of(q, k, v, g, lam, dout):
+    return float(np.sum(dout * oracle.naive(q, k, v, g, lam)))
+
+
+def test_backward_matches_finite_differences():
+    q, k, v, g, lam = rand_inputs(1, 2, 7, 3, 2, seed=41)
+    dout = np.random.default_rng(42).standard_normal(v.shape)
+    grads = oracle.backward(q, k, v, g, lam, dout)
+    args = [q, k, v, g, lam]
+    h = 1e-6
+    for which, grad in zip((0, 1, 2, 3, 4), (grads[0], grads[1], grads[2], grads[3], grads[4])):
+        x = args[which]
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            saved = x[idx]
+            x[idx] = saved + h
+            up = loss_of(*args, dout)
+            x[idx] = saved - h
+            dn = loss_of(*args, dout)
+            x[idx] = saved
+            num[idx] = (up - dn) / (2 * h)
+        assert np.max(np.abs(num - grad)) < 1e-7 * max(1.0, np.max(np.abs(grad))), which
+
+
+def test_backward_dq_is_the_forward_with_swapped_roles():
+    q, k, v, g, lam = rand_inputs(2, 1, 40, 5, 6, seed=43)
+    dout = np.random.default_rng(44).standard_normal(v.shape)
+    dq = oracle.backward(q, k, v, g, lam, dout)[0]
+    assert relerr(dq, oracle.naive(dout, v, k, g, lam)) < 1e-12
+
+
+def test_backward_euler_identities_and_gate_shift():
+    q, k, v, g, lam = rand_inputs(1, 3, 33, 4, 5, seed=45, g_scale=0.3)
+    dout = np.random.default_rng(46).standard_normal(v.shape)
+    dq, dk, dv, dg, dlam = oracle.backward(q, k, v, g, lam, dout)
+    loss = np.sum(dout * oracle.naive(q, k, v, g, lam), axis=(2, 3))
+    for x, dx in ((q, dq), (k, dk), (v, dv), (lam, dlam)):
+        assert np.allclose(np.sum(x * dx, axis=(2, 3)), loss, rtol=1e-11, atol=1e-11)
+    # the loss sees G only through differences: the total gate gradient vanishes
+    assert np.max(np.abs(dg[:, :, 0])) < 1e-11 * max(1.0, np.max(np.abs(dg)))
