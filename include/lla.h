@@ -184,6 +184,40 @@ lla_status lla_prefill_state(const void *k, const void *v, const float *g,
                              size_t workspace_bytes, void *stream);
 
 /*
+ * Backward of lla_fwd: given dout = dLoss/dout, the gradients of every input.
+ * "Log-Linear Attention" §2.2 defines the forward only; these are the
+ * derivatives of that double sum (A_ts = lambda_t[l(t,s)] exp(G_t - G_s),
+ * s <= t, G the inclusive running sum of g):
+ *   dq_t = sum_s A_ts (dout_t . v_s) k_s       dk_s = sum_t A_ts (dout_t . v_s) q_t
+ *   dv_s = sum_t A_ts (q_t . k_s) dout_t
+ *   dlambda_t[l] = sum_{s: l(t,s)=l} exp(G_t - G_s) (q_t . k_s)(dout_t . v_s)
+ *   dg_r = sum_{u >= r} (sum_l lambda_u[l] dlambda_u[l] - k_u . dk_u).
+ * Computed chunkwise on CUDA cores in fp32: the forward's chunk-level Fenwick
+ * nodes serve dq and dlambda; one lambda-weighted state per (level, aligned
+ * block of later chunks) serves dk and dv.  Sums run in a fixed order, so
+ * repeated calls give bitwise-identical results.
+ *   q, k [B,H,T,dk], v [B,H,T,dv] in in_dt; g [B,H,T], lambda [B,H,T,L]
+ *   (L = lla_num_levels(T)), dout [B,H,T,dv] fp32; outputs (caller-owned,
+ *   fully overwritten, fp32): dq, dk [B,H,T,dk], dv [B,H,T,dv], dg [B,H,T],
+ *   dlambda [B,H,T,L].  All row-major and contiguous.
+ * Supported: chunk in {16,32,64}, T % chunk == 0, T <= 2^24,
+ * dk, dv in {16,32,64,128}.  B*H*T == 0 is a no-op returning LLA_OK.
+ * workspace: >= lla_bwd_workspace_bytes(...) bytes, 256-byte aligned, owned
+ * by the caller; no allocation happens inside.  Errors: a bad shape returns
+ * LLA_ERR_UNSUPPORTED_SHAPE, a NULL pointer or misaligned workspace
+ * LLA_ERR_INVALID_ARGUMENT, a short workspace LLA_ERR_WORKSPACE_TOO_SMALL,
+ * all before any launch; a failed launch returns LLA_ERR_CUDA.
+ */
+size_t lla_bwd_workspace_bytes(int B, int H, int T, int dk, int dv, int chunk,
+                               lla_dtype in_dt);
+
+lla_status lla_bwd(const void *q, const void *k, const void *v, const float *g,
+                   const float *lambda, const float *dout, float *dq, float *dk,
+                   float *dv, float *dg, float *dlambda, int B, int H, int T,
+                   int dk_dim, int dv_dim, int chunk, lla_dtype in_dt,
+                   void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Level weights from a two-layer MLP ("Adaptive memory decay for Log-Linear
  * Attention", §Method "LambdaMLPSoftplus"): for every (token, head),
  *     h = d W1 (width 2L, no activation),   lambda = softplus(h W2 + b),

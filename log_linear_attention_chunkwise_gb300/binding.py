@@ -36,6 +36,8 @@ SIGNATURES = {
     "lla_prefill_workspace_bytes": (_Z, [_I] * 3),
     "lla_prefill_state": (_I, [_P] * 5 + [_I] * 6 + [_I, _P, _Z, _P]),
     "lla_lambda_mlp": (_I, [_P] * 5 + [_I] * 5 + [_I, _P]),
+    "lla_bwd_workspace_bytes": (_Z, [_I] * 7),
+    "lla_bwd": (_I, [_P] * 11 + [_I] * 7 + [_P, _Z, _P]),
 }
 
 _lib = None
@@ -200,3 +202,34 @@ def lambda_mlp(d, W1, W2, b, out=None, stream=None):
                             _dt(d), _stream(stream))
     _check("lla_lambda_mlp", rc)
     return out
+
+
+def bwd(q, k, v, g, lam, dout, chunk: int = 64, workspace=None, stream=None):
+    """lla_bwd: gradients (dq, dk, dv, dg, dlam) of sum(dout * lla_fwd(q, k, v, g, lam))."""
+    lib = load()
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, n, q.dtype, 4)
+    _need(g, "g", torch.float32, 3)
+    _need(lam, "lam", torch.float32, 4)
+    _need(dout, "dout", torch.float32, 4)
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape[:3] != (B, H, T) or g.shape != (B, H, T) or \
+            dout.shape != v.shape or lam.shape[:3] != (B, H, T) or \
+            lam.shape[3] != max(lib.lla_num_levels(T), 1):
+        raise ValueError("inconsistent shapes")
+    f32 = dict(dtype=torch.float32, device=q.device)
+    dq = torch.empty((B, H, T, dk), **f32)
+    dkk = torch.empty((B, H, T, dk), **f32)
+    dvv = torch.empty((B, H, T, dv), **f32)
+    dg = torch.empty((B, H, T), **f32)
+    dl = torch.empty(tuple(lam.shape), **f32)
+    in_dt = _dt(q)
+    need = lib.lla_bwd_workspace_bytes(B, H, T, dk, dv, chunk, in_dt)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    rc = lib.lla_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(lam), _ptr(dout), _ptr(dq), _ptr(dkk),
+                     _ptr(dvv), _ptr(dg), _ptr(dl), B, H, T, dk, dv, chunk, in_dt, _ptr(workspace),
+                     workspace.numel(), _stream(stream))
+    _check("lla_bwd", rc)
+    return dq, dkk, dvv, dg, dl

@@ -1,0 +1,24 @@
+// Internal interface of the backward (CUDA cores, fp32 arithmetic).
+#pragma once
+
+#include <stddef.h>
+
+#include "lla_common.cuh"
+
+namespace lla {
+
+struct BwdArgs {
+    const void *q, *k, *v;
+    const float *g, *lam, *dout;
+    float *dq, *dkey, *dval, *dg, *dlam;
+    int B, H, T, dk, dv, C, L;
+    lla_dtype in_dt;
+    void *workspace;
+    void *stream;
+};
+
+size_t bwd_workspace_bytes(const BwdArgs &A);
+size_t bwd_smem_bytes(const BwdArgs &A);
+cudaError_t bwd(const BwdArgs &A);
+
+}  // namespace lla

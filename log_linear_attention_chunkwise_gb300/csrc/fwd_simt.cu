@@ -287,8 +287,9 @@ simt_chunk_output_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                 out[(tok0 + ty + 16 * a) * dv + tx + 16 * jj] = from_f32<Tout>(acc[a][jj]);
 }
 
-template <typename Tin, typename Tout>
-cudaError_t launch_all(const SimtFwdArgs &A)
+// Steps 1-3 only (chunk states, fp64 prefix, Fenwick scan) into the workspace.
+template <typename Tin>
+cudaError_t launch_nodes(const SimtFwdArgs &A)
 {
     const int BH = A.B * A.H;
     const int N = A.T / A.C;
@@ -297,7 +298,6 @@ cudaError_t launch_all(const SimtFwdArgs &A)
     float *gam = (float *)ws;
     double *P = (double *)(ws + simt_ws_offset_P(A));
     float *nodes = (float *)(ws + simt_ws_offset_nodes(A));
-
     size_t sm1 = sizeof(float) * (128 + kSub * A.dk + kSub * A.dv);
     simt_chunk_state_kernel<Tin><<<dim3(N, BH), kThreads, sm1, st>>>(
         (const Tin *)A.k, (const Tin *)A.v, A.g, gam, nodes, A.T, A.dk, A.dv, A.C, N);
@@ -306,10 +306,24 @@ cudaError_t launch_all(const SimtFwdArgs &A)
     if (N > 1)
         simt_fenwick_scan_kernel<<<dim3((E + kThreads - 1) / kThreads, BH), kThreads, 0, st>>>(
             P, nodes, N, E);
+    return cudaPeekAtLastError();
+}
+
+template <typename Tin, typename Tout>
+cudaError_t launch_all(const SimtFwdArgs &A)
+{
+    const int BH = A.B * A.H;
+    const int N = A.T / A.C;
+    cudaStream_t st = (cudaStream_t)A.stream;
+    char *ws = (char *)A.workspace;
+    double *P = (double *)(ws + simt_ws_offset_P(A));
+    float *nodes = (float *)(ws + simt_ws_offset_nodes(A));
+    cudaError_t err = launch_nodes<Tin>(A);
+    if (err != cudaSuccess) return err;
     const int ldkv = (A.dk > A.dv ? A.dk : A.dv) + 1;
     size_t sm4 = sizeof(float) * (128 + A.C * A.dk + A.C * ldkv + A.C * A.C + 16 * A.dv + A.C * A.L);
     auto kern = simt_chunk_output_kernel<Tin, Tout>;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm4);
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm4);
     if (err != cudaSuccess) return err;
     int cbits = ctz_u32((uint32_t)A.C);
     kern<<<dim3(N, BH), kThreads, sm4, st>>>(
@@ -343,6 +357,11 @@ size_t simt_max_smem_bytes(const SimtFwdArgs &A)
     const int ldkv = (A.dk > A.dv ? A.dk : A.dv) + 1;
     return sizeof(float) * (128 + (size_t)A.C * A.dk + (size_t)A.C * ldkv + (size_t)A.C * A.C +
                             16 * (size_t)A.dv + (size_t)A.C * A.L);
+}
+
+cudaError_t simt_build_nodes(const SimtFwdArgs &A)
+{
+    return A.in_dt == LLA_F32 ? launch_nodes<float>(A) : launch_nodes<__nv_bfloat16>(A);
 }
 
 cudaError_t simt_fwd(const SimtFwdArgs &A)

@@ -22,5 +22,8 @@ size_t simt_ws_offset_nodes(const SimtFwdArgs &A);
 size_t simt_workspace_bytes(const SimtFwdArgs &A);
 size_t simt_max_smem_bytes(const SimtFwdArgs &A);
 cudaError_t simt_fwd(const SimtFwdArgs &A);
+// Chunk states, chunk-gate prefix and Fenwick nodes only (the backward reads
+// them): P at simt_ws_offset_P, Node_j at slot j of simt_ws_offset_nodes.
+cudaError_t simt_build_nodes(const SimtFwdArgs &A);
 
 }  // namespace lla

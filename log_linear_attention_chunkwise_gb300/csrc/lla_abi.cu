@@ -2,6 +2,7 @@
 // Declarations, layouts and error behaviour: include/lla.h.
 #include <stdint.h>
 
+#include "bwd_simt.cuh"
 #include "decode.cuh"
 #include "fwd_simt.cuh"
 #include "fwd_tc.cuh"
@@ -188,6 +189,39 @@ lla_status lla_lambda_mlp(const void *d, const float *W1, const float *W2, const
     A.d = d; A.W1 = W1; A.W2 = W2; A.bias = b; A.lam = lambda;
     A.B = B; A.H = H; A.T = T; A.Dd = Dd; A.L = L; A.in_dt = in_dt; A.stream = stream;
     return lambda_mlp(A) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+}
+
+size_t lla_bwd_workspace_bytes(int B, int H, int T, int dk, int dv, int chunk, lla_dtype in_dt)
+{
+    if (fwd_shape_status(B, H, T, dk, dv, chunk, in_dt) != LLA_OK || chunk > 64) return 0;
+    if ((long long)B * H * T == 0) return 0;
+    lla::BwdArgs A{};
+    A.B = B; A.H = H; A.T = T; A.dk = dk; A.dv = dv; A.C = chunk;
+    A.L = lla_num_levels(T); A.in_dt = in_dt;
+    return lla::bwd_workspace_bytes(A);
+}
+
+lla_status lla_bwd(const void *q, const void *k, const void *v, const float *g, const float *lambda,
+                   const float *dout, float *dq, float *dk, float *dv, float *dg, float *dlambda,
+                   int B, int H, int T, int dk_dim, int dv_dim, int chunk, lla_dtype in_dt,
+                   void *workspace, size_t workspace_bytes, void *stream)
+{
+    lla_status st = fwd_shape_status(B, H, T, dk_dim, dv_dim, chunk, in_dt);
+    if (st != LLA_OK) return st;
+    if (chunk > 64) return LLA_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)B * H * T == 0) return LLA_OK;
+    if (!q || !k || !v || !g || !lambda || !dout || !dq || !dk || !dv || !dg || !dlambda)
+        return LLA_ERR_INVALID_ARGUMENT;
+    lla::BwdArgs A{};
+    A.B = B; A.H = H; A.T = T; A.dk = dk_dim; A.dv = dv_dim; A.C = chunk;
+    A.L = lla_num_levels(T); A.in_dt = in_dt;
+    if (workspace_bytes < lla::bwd_workspace_bytes(A)) return LLA_ERR_WORKSPACE_TOO_SMALL;
+    if (workspace == nullptr || ((uintptr_t)workspace & 255u) != 0) return LLA_ERR_INVALID_ARGUMENT;
+    if (lla::bwd_smem_bytes(A) > 227 * 1024) return LLA_ERR_UNSUPPORTED_SHAPE;
+    A.q = q; A.k = k; A.v = v; A.g = g; A.lam = lambda; A.dout = dout;
+    A.dq = dq; A.dkey = dk; A.dval = dv; A.dg = dg; A.dlam = dlambda;
+    A.workspace = workspace; A.stream = stream;
+    return lla::bwd(A) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
 }
 
 }  // extern "C"

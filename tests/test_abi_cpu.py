@@ -96,3 +96,21 @@ def test_prefill_validation(lib):
     # bit_length(T) must fit in Ls slots
     assert lib.lla_prefill_state(p, p, p, p, p, 1, 1, 8, 64, 64, 3, 1, p, 1 << 20, NULL) == 2
     assert lib.lla_prefill_state(p, p, p, p, p, 1, 1, 8, 64, 64, 4, 1, p, 0, NULL) == 3
+
+
+def test_bwd_validation(lib):
+    p = ctypes.c_void_p(256)
+
+    def bwd(B=1, T=256, dk=64, chunk=64, dt=1, ws=1 << 30, ptr=p):
+        return lib.lla_bwd(ptr, p, p, p, p, p, p, p, p, p, p, B, 1, T, dk, 64, chunk, dt,
+                           p, ws, NULL)
+    assert bwd(chunk=128) == 2          # the backward takes chunks up to 64
+    assert bwd(dk=48) == 2
+    assert bwd(T=100) == 2
+    assert bwd(dt=5) == 1
+    assert bwd(ws=0) == 3
+    assert bwd(ptr=ctypes.c_void_p(0)) == 1
+    assert bwd(B=0, ptr=ctypes.c_void_p(0), ws=0) == 0
+    assert lib.lla_bwd_workspace_bytes(1, 1, 256, 64, 64, 128, 1) == 0
+    # Fenwick nodes [BH][N][dk][dv] plus block states, both fp32
+    assert lib.lla_bwd_workspace_bytes(1, 2, 256, 64, 64, 64, 1) >= 2 * (4 + 4) * 64 * 64 * 4
