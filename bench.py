@@ -60,6 +60,56 @@ def fwd_bytes(cfg: W.FwdConfig, out_bytes: int = 4) -> float:
     return cfg.B * cfg.H * cfg.T * per_tok
 
 
+def bwd_flops(cfg: W.FwdConfig) -> float:
+    """Algorithmic flops of one chunked backward: the forward's chunk states
+    and node scan (recomputed), per chunk the causal pairs' two dot products
+    and three masked products (dq, dk, dv), the query-side read-out of
+    popcount(i) nodes (dq and the level gradient), one state per (level,
+    block of later chunks) and its key-side read-out (dk, dv)."""
+    C, N, dk, dv = cfg.chunk, cfg.T // cfg.chunk, cfg.dk, cfg.dv
+    nodes = N * 2 * C * dk * dv + sum(1 + ((j & -j).bit_length() - 1) for j in range(1, N)) * 2 * dk * dv
+    pairs = N * C * (C + 1) / 2
+    intra = pairs * 2 * (dk + dv) + pairs * 2 * (2 * dk + dv)
+    query = sum(bin(i).count("1") for i in range(N)) * (2 * C * dk * dv + 2 * C * dk)
+    nlev = (N - 1).bit_length() if N > 1 else 0
+    blocks = 0
+    keyside = 0
+    for m in range(nlev):
+        for b in range(1, (N + (1 << m) - 1) >> m, 2):
+            blocks += min(N, (b + 1) << m) - (b << m)          # chunks summed into R_{m,b}
+        keyside += sum(1 for i in range(N) if not (i >> m) & 1 and ((i >> m) + 1) << m < N)
+    state = blocks * C * 2 * dk * dv
+    keyside *= 2 * (2 * C * dk * dv)
+    return cfg.B * cfg.H * (nodes + intra + query + state + keyside)
+
+
+def fp32_alu_peak_tflops(sm_mhz: float) -> float:
+    """CUDA-core fp32 peak: 152 SMs x 128 fp32 lanes x 2 flops (FMA) x clock."""
+    return 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
+
+
+def time_calls(fn, stream, warm=2, reps=5):
+    """Mean ms per call over reps back-to-back calls, CUDA events on stream."""
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def load_peaks_raw() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f)
+    return {}
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -69,10 +119,15 @@ def load_peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+FWD_SOURCES = ("fwd_tc.cu", "fwd_tc.cuh", "sm100.cuh", "tma_host.cuh", "lla_common.cuh")
+
+
 def source_digest() -> str:
+    """Digest of the tensor-core forward's sources (the kernels whose DRAM
+    traffic profiles/traffic.json records)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "log_linear_attention_chunkwise_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in FWD_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -264,10 +319,83 @@ def run_lla(args, rank, world, local_rank):
     del hx, hout
     if rank == 0 and not args.skip_decode:
         res["decode"] = run_decode(dev, args)
+    if rank == 0 and not args.skip_next:
+        res["next_rows"] = run_next_rows(dev, x, cfg, args)
     if rank == 0 and not args.skip_cpu:
         res["cpu_baseline"] = cpu_baseline(x, cfg, args.cpu_tokens)
     res["context"] = ("pages: a Triton kernel overtakes FlashAttention-2 from about 8K tokens "
                       "(hardware not named)")
+    return res
+
+
+def run_next_rows(dev, x, cfg, args):
+    """Timings of the entry points beyond the forward on the same T=32768
+    inputs: prefill (decode state from a prefix), backward, lambda MLP."""
+    from log_linear_attention_chunkwise_gb300 import binding
+    stream = torch.cuda.current_stream(dev)
+    hbm_peak = load_peaks()[0]
+    xd = {n: t.to(dev) for n, t in x.items()}
+    BHT = cfg.B * cfg.H * cfg.T
+    res = {}
+
+    # prefill: state after the whole sequence (Ls = bit_length(T) slots)
+    Ls = cfg.T.bit_length()
+    S = torch.empty((cfg.B, cfg.H, Ls, cfg.dk, cfg.dv), device=dev)
+    D = torch.empty((cfg.B, cfg.H, Ls), device=dev)
+    ws = torch.empty(max(binding.load().lla_prefill_workspace_bytes(cfg.B, cfg.H, cfg.T), 1),
+                     dtype=torch.uint8, device=dev)
+    ms = time_calls(lambda: binding.prefill_state(xd["k"], xd["v"], xd["g"], Ls, state=S,
+                                                  logdecay=D, workspace=ws, stream=stream), stream)
+    nbytes = BHT * ((cfg.dk + cfg.dv) * 2 + 4) + cfg.B * cfg.H * Ls * (cfg.dk * cfg.dv + 1) * 4
+    gbs = nbytes / (ms / 1e3) / 1e9
+    res["prefill_state"] = {
+        "workload": f"k,v of the forward workload -> {Ls}-slot decode state", "ms": ms,
+        "tokens_per_s": cfg.B * cfg.T / (ms / 1e3),
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": gbs / hbm_peak, "algorithmic_bytes": nbytes}}
+    del S, D, ws
+
+    # lambda MLP on the keys (d = k), L levels
+    L = cfg.L
+    g = torch.Generator().manual_seed(5)
+    W1 = (torch.randn((cfg.dk, 2 * L), generator=g) / math.sqrt(cfg.dk)).to(dev)
+    W2 = (torch.randn((2 * L, L), generator=g) / math.sqrt(2 * L)).to(dev)
+    bias = torch.full((L,), 0.54, device=dev)
+    lam = torch.empty((cfg.B, cfg.H, cfg.T, L), device=dev)
+    ms = time_calls(lambda: binding.lambda_mlp(xd["k"], W1, W2, bias, out=lam, stream=stream), stream)
+    nbytes = BHT * (cfg.dk * 2 + L * 4)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    res["lambda_mlp"] = {
+        "workload": f"d = k [B,H,T,{cfg.dk}] bf16 -> lambda [B,H,T,{L}] fp32, hidden {2 * L}",
+        "ms": ms, "tokens_per_s": cfg.B * cfg.T / (ms / 1e3),
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": gbs / hbm_peak, "algorithmic_bytes": nbytes}}
+    del lam
+
+    # backward (CUDA cores, fp32 arithmetic)
+    if not args.skip_bwd:
+        gen = torch.Generator().manual_seed(cfg.seed + 1000)
+        dout = torch.randn((cfg.B, cfg.H, cfg.T, cfg.dv), generator=gen).to(dev)
+        need = binding.load().lla_bwd_workspace_bytes(cfg.B, cfg.H, cfg.T, cfg.dk, cfg.dv,
+                                                      cfg.chunk, binding.LLA_BF16)
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
+        with ClockSampler(dev.index or 0) as clk:
+            ms = time_calls(lambda: binding.bwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["lam"], dout,
+                                                chunk=cfg.chunk, workspace=ws, stream=stream),
+                            stream, warm=1, reps=3)
+        clocks = clk.summary()
+        flops = bwd_flops(cfg)
+        tf = flops / (ms / 1e3) / 1e12
+        mhz = load_peaks_raw().get("sm_max_mhz", 2070.0)
+        peak = fp32_alu_peak_tflops(mhz)
+        res["backward"] = {
+            "workload": "gradients of the forward workload (dq, dk, dv, dg, dlambda), chunk 64",
+            "ms": ms, "tokens_per_s": cfg.B * cfg.T / (ms / 1e3),
+            "roofline": {"bound": "alu", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tf / peak, "algorithmic_flops": flops,
+                         "peak_source": f"fp32 CUDA-core FMA rate at {mhz:.0f} MHz (152 SMs x 128 lanes x 2)"},
+            "clocks": clocks}
+        del ws, dout
     return res
 
 
@@ -392,6 +520,9 @@ def main():
     ap.add_argument("--impl", default="lla", choices=["lla", "reference"])
     ap.add_argument("--skip-decode", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--skip-next", action="store_true",
+                    help="skip the prefill / lambda-MLP / backward timings")
+    ap.add_argument("--skip-bwd", action="store_true", help="skip the backward timing")
     ap.add_argument("--cpu-tokens", type=int, default=32768)
     ap.add_argument("--ref-tokens", type=int, default=2048)
     ap.add_argument("--heads", type=int, default=0, help="override H (smaller profiling case)")
