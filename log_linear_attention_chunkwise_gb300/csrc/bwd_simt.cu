@@ -59,10 +59,14 @@ bwd_gamma_kernel(const float *__restrict__ g, float *__restrict__ gamma, int T, 
     }
 }
 
+constexpr int kCk = 64;  // dv columns of a node staged at a time
+
 size_t query_smem_floats(int C, int Dk, int Dv, int L)
 {
     const size_t lk = Dk + 1, lv = Dv + 1;
-    const size_t scratch = 3 * (size_t)C * C > (size_t)C * lk ? 3 * (size_t)C * C : (size_t)C * lk;
+    const size_t intra = 3 * (size_t)C * C;
+    const size_t node = (size_t)kCk * Dk;
+    const size_t scratch = intra > node ? intra : node;
     return 128 + 2 * (size_t)C * lk + 2 * (size_t)C * lv + scratch + 2 * (size_t)C * L;
 }
 
@@ -89,7 +93,7 @@ bwd_query_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin
     float *W1 = dL + C * L;         // [C][C]   M . (dO.v)      (intra phase)
     float *W2 = W1 + C * C;         // [C][C]   M . (q.k)
     float *X = W2 + C * C;          // [C][C]   decay . (q.k)(dO.v)
-    float *U = W1;                  // [C][lk]  q_t[r] (Node dO_t)[r]  (path phase)
+    float *Nt = W1;                 // [kCk][Dk] node columns, transposed (path phase)
     const int i = blockIdx.x;
     const long long bh = blockIdx.y;
     const long long tok0 = bh * (long long)T + (long long)i * C;
@@ -156,54 +160,137 @@ bwd_query_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin
         dv[(tok0 + s) * Dv + c] = a;
     }
     __syncthreads();
-    // earlier chunks through the forward's path nodes
+    // Earlier chunks through the forward's path nodes.  Thread (ty, tx) owns
+    // rows t0..t0+3 (t0 = 4 ty) and columns r0..r0+7 (r0 = 8 tx) of
+    // U = dO Node_j^T; dq accumulates in registers over the path.
     const double *Pb = P + bh * (long long)(N + 1);
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const int t0 = 4 * ty, r0 = 8 * tx;
+    const bool own = t0 < C && r0 < Dk;
+    float dqa[4][8];
+#pragma unroll
+    for (int a = 0; a < 4; a++)
+#pragma unroll
+        for (int c = 0; c < 8; c++) dqa[a][c] = 0.f;
     for (int j = i; j > 0; j -= (j & -j)) {
         const int lev = cbits + 1 + ctz_u32((uint32_t)j);
         const float dP = (float)(Pb[i] - Pb[j]);
         const float *Nd = nodes + (bh * N + j) * (long long)Dk * Dv;
-        for (int e = threadIdx.x; e < C * Dk; e += kThreads) {
-            const int r = e / C, t = e % C;  // consecutive threads share a node row
-            float u = 0.f;
-            for (int c = 0; c < Dv; c++) u = fmaf(Nd[r * Dv + c], Ds[t * lv + c], u);
+        float u[4][8];
+#pragma unroll
+        for (int a = 0; a < 4; a++)
+#pragma unroll
+            for (int c = 0; c < 8; c++) u[a][c] = 0.f;
+        for (int c0 = 0; c0 < Dv; c0 += kCk) {
+            const int nc = min(kCk, Dv - c0);
+            __syncthreads();
+            for (int e = threadIdx.x; e < Dk * (nc / 4); e += kThreads) {
+                const int r = e % Dk, c4 = e / Dk;
+                const float4 x = *reinterpret_cast<const float4 *>(Nd + (long long)r * Dv + c0 + 4 * c4);
+                Nt[(4 * c4 + 0) * Dk + r] = x.x;
+                Nt[(4 * c4 + 1) * Dk + r] = x.y;
+                Nt[(4 * c4 + 2) * Dk + r] = x.z;
+                Nt[(4 * c4 + 3) * Dk + r] = x.w;
+            }
+            __syncthreads();
+            if (own) {
+                for (int cc = 0; cc < nc; cc++) {
+                    float dv4[4];
+#pragma unroll
+                    for (int a = 0; a < 4; a++) dv4[a] = Ds[(t0 + a) * lv + c0 + cc];
+                    const float4 n0 = *reinterpret_cast<const float4 *>(Nt + cc * Dk + r0);
+                    const float4 n1 = *reinterpret_cast<const float4 *>(Nt + cc * Dk + r0 + 4);
+                    const float nn[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
+#pragma unroll
+                    for (int a = 0; a < 4; a++)
+#pragma unroll
+                        for (int c = 0; c < 8; c++) u[a][c] = fmaf(dv4[a], nn[c], u[a][c]);
+                }
+            }
+        }
+        // dq_t += lambda_t[lev] w_t U_t ;  dlam_t[lev] += w_t q_t . U_t
+        float part[4];
+#pragma unroll
+        for (int a = 0; a < 4; a++) {
+            const int t = min(t0 + a, C - 1);
             const float w = expf(gl[t] + dP);
-            dq[(tok0 + t) * Dk + r] += Ls[t * L + lev] * w * u;
-            U[t * lk + r] = w * Qs[t * lk + r] * u;
+            const float lw = Ls[t * L + lev] * w;
+            float pr = 0.f;
+#pragma unroll
+            for (int c = 0; c < 8; c++) {
+                dqa[a][c] = fmaf(lw, u[a][c], dqa[a][c]);
+                pr = fmaf(own ? Qs[t * lk + r0 + c] : 0.f, u[a][c], pr);
+            }
+            part[a] = w * pr;
         }
-        __syncthreads();
-        for (int t = threadIdx.x; t < C; t += kThreads) {
-            float a = 0.f;
-            for (int r = 0; r < Dk; r++) a += U[t * lk + r];
-            dL[t * L + lev] += a;
+#pragma unroll
+        for (int a = 0; a < 4; a++)
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) part[a] += __shfl_xor_sync(0xffffffffu, part[a], off, 16);
+        if (tx == 0 && t0 < C) {
+#pragma unroll
+            for (int a = 0; a < 4; a++) dL[(t0 + a) * L + lev] += part[a];
         }
-        __syncthreads();
+    }
+    __syncthreads();
+    if (own && i > 0) {
+#pragma unroll
+        for (int a = 0; a < 4; a++) {
+            float *dst = dq + (tok0 + t0 + a) * Dk + r0;
+            float4 x0 = *reinterpret_cast<float4 *>(dst), x1 = *reinterpret_cast<float4 *>(dst + 4);
+            x0.x += dqa[a][0]; x0.y += dqa[a][1]; x0.z += dqa[a][2]; x0.w += dqa[a][3];
+            x1.x += dqa[a][4]; x1.y += dqa[a][5]; x1.z += dqa[a][6]; x1.w += dqa[a][7];
+            *reinterpret_cast<float4 *>(dst) = x0;
+            *reinterpret_cast<float4 *>(dst + 4) = x1;
+        }
     }
     for (int e = threadIdx.x; e < C * L; e += kThreads) dlam[tok0 * L + e] = dL[e];
 }
 
-// R_{m,b} for every level m and block b (odd b below N; other CTAs exit).
+// Work items of the block states: level m, odd block b (chunks
+// [b 2^m, min(N, (b+1) 2^m))) and a piece of at most Pc of those chunks.
+// Level m has nb/2 odd blocks (nb = ceil(N / 2^m)), each cut into
+// ceil(2^m / Pc) pieces (empty pieces of a short last block do nothing).
+struct Item {
+    int m, b, p, pp;
+};
+
+__device__ __forceinline__ bool decode_item(int idx, int N, int nlev, int Pc, Item *it)
+{
+    for (int m = 0; m < nlev; m++) {
+        const int nb = (N + (1 << m) - 1) >> m;
+        const int pp = ((1 << m) + Pc - 1) / Pc;
+        const int cnt = (nb / 2) * pp;
+        if (idx < cnt) {
+            it->m = m;
+            it->b = 2 * (idx / pp) + 1;
+            it->p = idx % pp;
+            it->pp = pp;
+            return true;
+        }
+        idx -= cnt;
+    }
+    return false;
+}
+
+// One piece of R_{m,b} = sum_t lambda_t[c+1+m] exp(G_t - G_ref) q_t dO_t^T.
 template <typename Tin>
 __global__ void __launch_bounds__(kThreads)
-bwd_block_state_kernel(const Tin *__restrict__ q, const float *__restrict__ dout,
+bwd_block_piece_kernel(const Tin *__restrict__ q, const float *__restrict__ dout,
                        const float *__restrict__ gamma, const float *__restrict__ lam,
-                       const double *__restrict__ P, float *__restrict__ R, int T, int Dk, int Dv,
-                       int C, int cbits, int N, int L, int nlev)
+                       const double *__restrict__ P, float *__restrict__ part, int T, int Dk, int Dv,
+                       int C, int cbits, int N, int L, int nlev, int Pc)
 {
     __shared__ float qs[kSub * 128];
     __shared__ float ds[kSub * 128];
     const long long bh = blockIdx.y;
-    // locate (m, b) from the flat index: level m has ceil(N / 2^m) blocks
-    int idx = blockIdx.x, m = 0, nb = N;
-    while (m < nlev && idx >= nb) {
-        idx -= nb;
-        m++;
-        nb = (N + (1 << m) - 1) >> m;
-    }
-    if (m >= nlev) return;
-    const int b = idx;
-    if ((b & 1) == 0 || ((long long)b << m) >= N) return;
-    const int c0 = b << m, c1 = min(N, (b + 1) << m);  // chunks of the block
-    const int lev = cbits + 1 + m;
+    Item it;
+    if (!decode_item(blockIdx.x, N, nlev, Pc, &it)) return;
+    const int c0 = it.b << it.m;
+    const int blk_end = min(N, (it.b + 1) << it.m);
+    const int p0 = c0 + it.p * Pc, p1 = min(blk_end, p0 + Pc);
+    if (p0 >= p1) return;
+    const int lev = cbits + 1 + it.m;
     const double *Pb = P + bh * (long long)(N + 1);
     const double Pref = Pb[c0];
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
@@ -213,7 +300,7 @@ bwd_block_state_kernel(const Tin *__restrict__ q, const float *__restrict__ dout
     for (int a = 0; a < 8; a++)
 #pragma unroll
         for (int cc = 0; cc < 8; cc++) acc[a][cc] = 0.f;
-    const long long t_lo = (long long)c0 * C, t_hi = (long long)c1 * C;
+    const long long t_lo = (long long)p0 * C, t_hi = (long long)p1 * C;
     for (long long t0 = t_lo; t0 < t_hi; t0 += kSub) {
         const int nt = (int)min((long long)kSub, t_hi - t0);
         __syncthreads();
@@ -246,7 +333,7 @@ bwd_block_state_kernel(const Tin *__restrict__ q, const float *__restrict__ dout
                 for (int cc = 0; cc < 8; cc++) acc[a][cc] = fmaf(qr[a], dc[cc], acc[a][cc]);
         }
     }
-    float *out = R + ((bh * gridDim.x) + blockIdx.x) * (long long)Dk * Dv;
+    float *out = part + ((bh * gridDim.x) + blockIdx.x) * (long long)Dk * Dv;
 #pragma unroll
     for (int a = 0; a < 8; a++)
 #pragma unroll
@@ -254,16 +341,57 @@ bwd_block_state_kernel(const Tin *__restrict__ q, const float *__restrict__ dout
             if (a < RB && cc < CB) out[(ty + 16 * a) * Dv + tx + 16 * cc] = acc[a][cc];
 }
 
-// Per chunk: the key side of the later chunks, dk_s += f_s R v_s, dv_s += f_s R^T k_s.
+// R_{m,b} = sum of its pieces in piece order (bitwise reproducible).  One
+// CTA per (level, block) slot; even or absent blocks exit.
+__global__ void __launch_bounds__(kThreads)
+bwd_block_reduce_kernel(const float *__restrict__ part, float *__restrict__ R, int Dk, int Dv, int N,
+                        int nlev, int Pc, int nitems, int nblocks)
+{
+    const long long bh = blockIdx.y;
+    int idx = blockIdx.x, m = 0, nb = N, first = 0;
+    while (m < nlev && idx >= nb) {
+        idx -= nb;
+        first += (nb / 2) * (((1 << m) + Pc - 1) / Pc);
+        m++;
+        nb = (N + (1 << m) - 1) >> m;
+    }
+    if (m >= nlev) return;
+    const int b = idx;
+    if ((b & 1) == 0 || ((long long)b << m) >= N) return;
+    const int pp = ((1 << m) + Pc - 1) / Pc;
+    const int blk_end = min(N, (b + 1) << m);
+    const int npieces = (blk_end - (b << m) + Pc - 1) / Pc;  // non-empty pieces
+    const float4 *src = reinterpret_cast<const float4 *>(part) +
+                        ((bh * nitems) + first + (b / 2) * pp) * (long long)(Dk * Dv / 4);
+    float4 *dst = reinterpret_cast<float4 *>(R) + ((bh * nblocks) + blockIdx.x) * (long long)(Dk * Dv / 4);
+    const int E4 = Dk * Dv / 4;
+    for (int e = threadIdx.x; e < E4; e += kThreads) {
+        float4 acc = src[e];
+        for (int p = 1; p < npieces; p++) {
+            const float4 x = src[(long long)p * E4 + e];
+            acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+        }
+        dst[e] = acc;
+    }
+}
+
+constexpr int kRowsPer = 4;  // rows of a thread tile
+constexpr int kColsPer = 8;  // columns of a thread tile
+
+// Per chunk: the key side of the later chunks, over every level m whose
+// right-hand block exists:  dk_s += f_s R v_s,  dv_s += f_s R^T k_s.
+// Thread (ty, tx) owns rows s0..s0+3 and columns 8 tx..8 tx+7 of dk and of
+// dv, accumulated in registers over the levels.
 template <typename Tin>
 __global__ void __launch_bounds__(kThreads)
 bwd_key_kernel(const Tin *__restrict__ k, const Tin *__restrict__ v, const float *__restrict__ gamma,
                const double *__restrict__ P, const float *__restrict__ R, float *__restrict__ dk,
                float *__restrict__ dv, int T, int Dk, int Dv, int C, int N, int nlev, int nblocks)
 {
-    extern __shared__ float sm[];
+    extern __shared__ __align__(16) float sm[];
     const int lk = Dk + 1, lv = Dv + 1;
-    float *Ks = sm;               // [C][lk]
+    float *Rb = sm;               // [Dk*Dv] R or R^T
+    float *Ks = Rb + Dk * Dv;     // [C][lk]
     float *Vs = Ks + C * lk;      // [C][lv]
     float *gl = Vs + C * lv;      // [C]
     const int i = blockIdx.x;
@@ -273,75 +401,190 @@ bwd_key_kernel(const Tin *__restrict__ k, const Tin *__restrict__ v, const float
     for (int e = threadIdx.x; e < C * Dv; e += kThreads) Vs[(e / Dv) * lv + e % Dv] = to_f32(v[tok0 * Dv + e]);
     for (int e = threadIdx.x; e < C; e += kThreads) gl[e] = gamma[tok0 + e];
     __syncthreads();
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const int s0 = kRowsPer * ty, x0 = kColsPer * tx;
+    const bool rows_ok = s0 < C;
+    const bool own_k = rows_ok && x0 < Dk, own_v = rows_ok && x0 < Dv;
+    float dka[kRowsPer][kColsPer], dva[kRowsPer][kColsPer];
+#pragma unroll
+    for (int a = 0; a < kRowsPer; a++)
+#pragma unroll
+        for (int c = 0; c < kColsPer; c++) dka[a][c] = dva[a][c] = 0.f;
     const double *Pb = P + bh * (long long)(N + 1);
+    bool any = false;
     int off = 0;
     for (int m = 0; m < nlev; m++) {
         const int nb = (N + (1 << m) - 1) >> m;
         const int b = (i >> m) + 1;
         if (((i >> m) & 1) == 0 && ((long long)b << m) < N) {
+            any = true;
             const float *Rm = R + ((bh * nblocks) + off + b) * (long long)Dk * Dv;
             const float dP = (float)(Pb[b << m] - Pb[i]);
-            for (int e = threadIdx.x; e < C * Dk; e += kThreads) {
-                const int r = e / C, s = e % C;
-                float a = 0.f;
-                for (int c = 0; c < Dv; c++) a = fmaf(Rm[r * Dv + c], Vs[s * lv + c], a);
-                dk[(tok0 + s) * Dk + r] += expf(dP - gl[s]) * a;
+            float f[kRowsPer];
+#pragma unroll
+            for (int a = 0; a < kRowsPer; a++) f[a] = expf(dP - gl[min(s0 + a, C - 1)]);
+            // dk: reduce over c with R^T staged ([c][r])
+            __syncthreads();
+            for (int e = threadIdx.x; e < Dk * (Dv / 4); e += kThreads) {
+                const int r = e % Dk, c4 = e / Dk;
+                const float4 x = *reinterpret_cast<const float4 *>(Rm + (long long)r * Dv + 4 * c4);
+                Rb[(4 * c4 + 0) * Dk + r] = x.x;
+                Rb[(4 * c4 + 1) * Dk + r] = x.y;
+                Rb[(4 * c4 + 2) * Dk + r] = x.z;
+                Rb[(4 * c4 + 3) * Dk + r] = x.w;
             }
-            for (int e = threadIdx.x; e < C * Dv; e += kThreads) {
-                const int c = e / C, s = e % C;
-                float a = 0.f;
-                for (int r = 0; r < Dk; r++) a = fmaf(Rm[r * Dv + c], Ks[s * lk + r], a);
-                dv[(tok0 + s) * Dv + c] += expf(dP - gl[s]) * a;
+            __syncthreads();
+            if (own_k) {
+                float t[kRowsPer][kColsPer];
+#pragma unroll
+                for (int a = 0; a < kRowsPer; a++)
+#pragma unroll
+                    for (int c = 0; c < kColsPer; c++) t[a][c] = 0.f;
+                for (int c = 0; c < Dv; c++) {
+                    float va[kRowsPer];
+#pragma unroll
+                    for (int a = 0; a < kRowsPer; a++) va[a] = Vs[(s0 + a) * lv + c];
+                    const float4 r0 = *reinterpret_cast<const float4 *>(Rb + c * Dk + x0);
+                    const float4 r1 = *reinterpret_cast<const float4 *>(Rb + c * Dk + x0 + 4);
+                    const float rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+                    for (int a = 0; a < kRowsPer; a++)
+#pragma unroll
+                        for (int cc = 0; cc < kColsPer; cc++) t[a][cc] = fmaf(va[a], rr[cc], t[a][cc]);
+                }
+#pragma unroll
+                for (int a = 0; a < kRowsPer; a++)
+#pragma unroll
+                    for (int cc = 0; cc < kColsPer; cc++) dka[a][cc] = fmaf(f[a], t[a][cc], dka[a][cc]);
+            }
+            // dv: reduce over r with R staged as is ([r][c])
+            __syncthreads();
+            for (int e = threadIdx.x; e < Dk * Dv / 4; e += kThreads)
+                reinterpret_cast<float4 *>(Rb)[e] = reinterpret_cast<const float4 *>(Rm)[e];
+            __syncthreads();
+            if (own_v) {
+                float t[kRowsPer][kColsPer];
+#pragma unroll
+                for (int a = 0; a < kRowsPer; a++)
+#pragma unroll
+                    for (int c = 0; c < kColsPer; c++) t[a][c] = 0.f;
+                for (int r = 0; r < Dk; r++) {
+                    float ka[kRowsPer];
+#pragma unroll
+                    for (int a = 0; a < kRowsPer; a++) ka[a] = Ks[(s0 + a) * lk + r];
+                    const float4 r0 = *reinterpret_cast<const float4 *>(Rb + r * Dv + x0);
+                    const float4 r1 = *reinterpret_cast<const float4 *>(Rb + r * Dv + x0 + 4);
+                    const float rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+                    for (int a = 0; a < kRowsPer; a++)
+#pragma unroll
+                        for (int cc = 0; cc < kColsPer; cc++) t[a][cc] = fmaf(ka[a], rr[cc], t[a][cc]);
+                }
+#pragma unroll
+                for (int a = 0; a < kRowsPer; a++)
+#pragma unroll
+                    for (int cc = 0; cc < kColsPer; cc++) dva[a][cc] = fmaf(f[a], t[a][cc], dva[a][cc]);
             }
         }
         off += nb;
     }
+    if (!any) return;
+    auto add8 = [](float *dst, const float *x) {
+        float4 a = *reinterpret_cast<float4 *>(dst), b = *reinterpret_cast<float4 *>(dst + 4);
+        a.x += x[0]; a.y += x[1]; a.z += x[2]; a.w += x[3];
+        b.x += x[4]; b.y += x[5]; b.z += x[6]; b.w += x[7];
+        *reinterpret_cast<float4 *>(dst) = a;
+        *reinterpret_cast<float4 *>(dst + 4) = b;
+    };
+#pragma unroll
+    for (int a = 0; a < kRowsPer; a++) {
+        if (own_k) add8(dk + (tok0 + s0 + a) * Dk + x0, dka[a]);
+        if (own_v) add8(dv + (tok0 + s0 + a) * Dv + x0, dva[a]);
+    }
 }
 
-// dG_u = sum_l lam_u[l] dlam_u[l] - k_u . dk_u, then dg = reverse running sum (fp64).
+// dG_u = sum_l lam_u[l] dlam_u[l] - k_u . dk_u, one warp per token, fp64 sums.
 template <typename Tin>
 __global__ void __launch_bounds__(kThreads)
-bwd_gate_kernel(const Tin *__restrict__ k, const float *__restrict__ lam, const float *__restrict__ dlam,
-                const float *__restrict__ dk, float *__restrict__ dg, int T, int Dk, int L)
+bwd_gate_grad_kernel(const Tin *__restrict__ k, const float *__restrict__ lam,
+                     const float *__restrict__ dlam, const float *__restrict__ dk,
+                     double *__restrict__ dG, int T, int Dk, int L)
 {
-    __shared__ double part[kThreads];
+    const int lane = threadIdx.x & 31;
+    const int u = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+    if (u >= T) return;
+    const long long gi = (long long)blockIdx.y * T + u;
+    double a = 0.0;
+    for (int l = lane; l < L; l += 32) a += (double)lam[gi * L + l] * (double)dlam[gi * L + l];
+    for (int r = lane; r < Dk; r += 32) a -= (double)to_f32(k[gi * Dk + r]) * (double)dk[gi * Dk + r];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+    if (lane == 0) dG[gi] = a;
+}
+
+// dg_r = sum_{u >= r} dG_u per (batch, head), fp64, one CTA of 1024 threads.
+__global__ void __launch_bounds__(1024)
+bwd_gate_scan_kernel(const double *__restrict__ dG, float *__restrict__ dg, int T)
+{
+    __shared__ double part[1024];
+    __shared__ double wsum[32];
     const long long bh = blockIdx.x;
-    const int per = (T + kThreads - 1) / kThreads;
+    const double *src = dG + bh * T;
+    const int per = (T + 1023) / 1024;
     const int lo = min(T, (int)threadIdx.x * per), hi = min(T, lo + per);
-    auto dG = [&](int u) -> double {
-        const long long gi = bh * T + u;
-        double a = 0.0;
-        for (int l = 0; l < L; l++) a += (double)lam[gi * L + l] * (double)dlam[gi * L + l];
-        for (int r = 0; r < Dk; r++) a -= (double)to_f32(k[gi * Dk + r]) * (double)dk[gi * Dk + r];
-        return a;
-    };
     double s = 0.0;
-    for (int u = lo; u < hi; u++) s += dG(u);
-    part[threadIdx.x] = s;
+    for (int u = lo; u < hi; u++) s += src[u];
+    // exclusive suffix sum of the per-thread totals
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    double incl = s;  // inclusive suffix within the warp (lanes >= this one)
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const double y = __shfl_down_sync(0xffffffffu, incl, off);
+        if (lane + off < 32) incl += y;
+    }
+    if (lane == 0) wsum[w] = incl;
     __syncthreads();
-    if (threadIdx.x == 0) {  // exclusive suffix sums of the partials
-        double run = 0.0;
-        for (int w = kThreads - 1; w >= 0; w--) {
-            const double x = part[w];
-            part[w] = run;
-            run += x;
+    if (w == 0) {
+        double x = wsum[lane], wi = x;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const double y = __shfl_down_sync(0xffffffffu, wi, off);
+            if (lane + off < 32) wi += y;
         }
+        wsum[lane] = wi - x;  // sum over later warps
     }
     __syncthreads();
+    part[threadIdx.x] = incl - s + wsum[w];  // sum over later threads
     double run = part[threadIdx.x];
     for (int u = hi - 1; u >= lo; u--) {
-        run += dG(u);
+        run += src[u];
         dg[bh * T + u] = (float)run;
     }
 }
 
 int block_levels(int N) { return N > 1 ? bit_length_u32((uint32_t)(N - 1)) : 0; }
 
+// R slots: every block of every level (odd ones used), flat by level.
 int total_blocks(int N)
 {
     int tot = 0;
     for (int m = 0; m < block_levels(N); m++) tot += (N + (1 << m) - 1) >> m;
     return tot;
+}
+
+int piece_chunks(int C) { return 1024 / C > 1 ? 1024 / C : 1; }
+
+int total_items(int N, int Pc)
+{
+    int tot = 0;
+    for (int m = 0; m < block_levels(N); m++)
+        tot += (((N + (1 << m) - 1) >> m) / 2) * (((1 << m) + Pc - 1) / Pc);
+    return tot;
+}
+
+size_t key_smem_floats(int C, int Dk, int Dv)
+{
+    return (size_t)Dk * Dv + (size_t)C * (Dk + 1) + (size_t)C * (Dv + 1) + C;
 }
 
 SimtFwdArgs node_args(const BwdArgs &A)
@@ -351,6 +594,27 @@ SimtFwdArgs node_args(const BwdArgs &A)
     F.B = A.B; F.H = A.H; F.T = A.T; F.dk = A.dk; F.dv = A.dv; F.C = A.C; F.L = A.L;
     F.in_dt = A.in_dt; F.out_dt = LLA_F32; F.workspace = A.workspace; F.stream = A.stream;
     return F;
+}
+
+// Workspace: the CUDA-core forward's (chunk gate sums, P, nodes), then
+// gamma [BH][T] fp32, R [BH][total_blocks][Dk][Dv] fp32,
+// pieces [BH][total_items][Dk][Dv] fp32, dG [BH][T] fp64.
+struct BwdLayout {
+    size_t gamma, R, parts, dG, end;
+};
+
+BwdLayout layout(const BwdArgs &A)
+{
+    SimtFwdArgs F = node_args(A);
+    const size_t BH = (size_t)A.B * A.H, st = (size_t)A.dk * A.dv * 4;
+    const int N = A.T / A.C;
+    BwdLayout l;
+    l.gamma = simt_workspace_bytes(F);
+    l.R = l.gamma + align_up(BH * A.T * 4, 256);
+    l.parts = l.R + align_up(BH * (size_t)total_blocks(N) * st, 256);
+    l.dG = l.parts + align_up(BH * (size_t)total_items(N, piece_chunks(A.C)) * st, 256);
+    l.end = l.dG + align_up(BH * A.T * 8, 256);
+    return l;
 }
 
 template <typename Tin>
@@ -363,10 +627,13 @@ cudaError_t launch_bwd(const BwdArgs &A)
     cudaError_t e = simt_build_nodes(F);
     if (e != cudaSuccess) return e;
     char *ws = (char *)A.workspace;
+    const BwdLayout lay = layout(A);
     const double *P = (const double *)(ws + simt_ws_offset_P(F));
     const float *nodes = (const float *)(ws + simt_ws_offset_nodes(F));
-    float *gamma = (float *)(ws + simt_workspace_bytes(F));
-    float *R = (float *)(ws + simt_workspace_bytes(F) + align_up((size_t)BH * A.T * 4, 256));
+    float *gamma = (float *)(ws + lay.gamma);
+    float *R = (float *)(ws + lay.R);
+    float *parts = (float *)(ws + lay.parts);
+    double *dG = (double *)(ws + lay.dG);
     bwd_gamma_kernel<<<dim3(N, BH), 32, 0, st>>>(A.g, gamma, A.T, A.C);
     const size_t smq = sizeof(float) * query_smem_floats(A.C, A.dk, A.dv, A.L);
     e = cudaFuncSetAttribute(bwd_query_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smq);
@@ -375,33 +642,35 @@ cudaError_t launch_bwd(const BwdArgs &A)
         (const Tin *)A.q, (const Tin *)A.k, (const Tin *)A.v, A.dout, gamma, A.lam, P, nodes, A.dq,
         A.dkey, A.dval, A.dlam, A.T, A.dk, A.dv, A.C, cbits, N, A.L);
     const int nlev = block_levels(N), nblocks = total_blocks(N);
-    if (nblocks > 0) {
-        bwd_block_state_kernel<Tin><<<dim3(nblocks, BH), kThreads, 0, st>>>(
-            (const Tin *)A.q, A.dout, gamma, A.lam, P, R, A.T, A.dk, A.dv, A.C, cbits, N, A.L, nlev);
-        const size_t smk = sizeof(float) * ((size_t)A.C * (A.dk + 1) + (size_t)A.C * (A.dv + 1) + A.C);
+    const int Pc = piece_chunks(A.C), nitems = total_items(N, Pc);
+    if (nitems > 0) {
+        bwd_block_piece_kernel<Tin><<<dim3(nitems, BH), kThreads, 0, st>>>(
+            (const Tin *)A.q, A.dout, gamma, A.lam, P, parts, A.T, A.dk, A.dv, A.C, cbits, N, A.L, nlev,
+            Pc);
+        bwd_block_reduce_kernel<<<dim3(nblocks, BH), kThreads, 0, st>>>(parts, R, A.dk, A.dv, N, nlev, Pc,
+                                                                        nitems, nblocks);
+        const size_t smk = sizeof(float) * key_smem_floats(A.C, A.dk, A.dv);
         e = cudaFuncSetAttribute(bwd_key_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smk);
         if (e != cudaSuccess) return e;
         bwd_key_kernel<Tin><<<dim3(N, BH), kThreads, smk, st>>>(
             (const Tin *)A.k, (const Tin *)A.v, gamma, P, R, A.dkey, A.dval, A.T, A.dk, A.dv, A.C, N, nlev,
             nblocks);
     }
-    bwd_gate_kernel<Tin><<<BH, kThreads, 0, st>>>((const Tin *)A.k, A.lam, A.dlam, A.dkey, A.dg, A.T,
-                                                   A.dk, A.L);
+    bwd_gate_grad_kernel<Tin><<<dim3((A.T + kThreads / 32 - 1) / (kThreads / 32), BH), kThreads, 0, st>>>(
+        (const Tin *)A.k, A.lam, A.dlam, A.dkey, dG, A.T, A.dk, A.L);
+    bwd_gate_scan_kernel<<<BH, 1024, 0, st>>>(dG, A.dg, A.T);
     return cudaPeekAtLastError();
 }
 
 }  // namespace
 
-size_t bwd_workspace_bytes(const BwdArgs &A)
-{
-    SimtFwdArgs F = node_args(A);
-    const size_t BH = (size_t)A.B * A.H;
-    const int N = A.T / A.C;
-    return simt_workspace_bytes(F) + align_up(BH * A.T * 4, 256) +
-           align_up(BH * (size_t)total_blocks(N) * A.dk * A.dv * 4, 256);
-}
+size_t bwd_workspace_bytes(const BwdArgs &A) { return layout(A).end; }
 
-size_t bwd_smem_bytes(const BwdArgs &A) { return sizeof(float) * query_smem_floats(A.C, A.dk, A.dv, A.L); }
+size_t bwd_smem_bytes(const BwdArgs &A)
+{
+    const size_t q = query_smem_floats(A.C, A.dk, A.dv, A.L), k = key_smem_floats(A.C, A.dk, A.dv);
+    return sizeof(float) * (q > k ? q : k);
+}
 
 cudaError_t bwd(const BwdArgs &A)
 {

@@ -166,8 +166,10 @@ simt_fenwick_scan_kernel(const double *__restrict__ P, float *__restrict__ nodes
         float val = base[(long long)j * E];
         const double Pj = Pb[j];
 #pragma unroll
-        for (int kk = 0; kk < kMaxZ; kk++)
-            if (kk < z) val = fmaf(expf((float)(Pj - Pb[j - (1 << kk)])), stack[kk], val);
+        for (int kk = 0; kk < kMaxZ; kk++) {  // only the z lower levels fold in
+            if (kk >= z) break;
+            val = fmaf(expf((float)(Pj - Pb[j - (1 << kk)])), stack[kk], val);
+        }
 #pragma unroll
         for (int kk = 0; kk < kMaxZ; kk++)
             if (kk == z) stack[kk] = val;
