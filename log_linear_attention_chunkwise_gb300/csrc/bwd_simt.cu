@@ -23,12 +23,12 @@
 // reproducible from call to call.
 #include "bwd_simt.cuh"
 #include "fwd_simt.cuh"
+#include "outer_simt.cuh"
 
 namespace lla {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kSub = 32;
 
 // gamma [BH][T]: inclusive gate sum inside each chunk (C <= 128), by one warp.
 __global__ void __launch_bounds__(32)
@@ -281,8 +281,9 @@ bwd_block_piece_kernel(const Tin *__restrict__ q, const float *__restrict__ dout
                        const double *__restrict__ P, float *__restrict__ part, int T, int Dk, int Dv,
                        int C, int cbits, int N, int L, int nlev, int Pc)
 {
-    __shared__ float qs[kSub * 128];
-    __shared__ float ds[kSub * 128];
+    __shared__ __align__(16) float qs[kOuterSub * 128];
+    __shared__ __align__(16) float ds[kOuterSub * 128];
+    __shared__ float sc[kOuterSub];
     const long long bh = blockIdx.y;
     Item it;
     if (!decode_item(blockIdx.x, N, nlev, Pc, &it)) return;
@@ -293,52 +294,27 @@ bwd_block_piece_kernel(const Tin *__restrict__ q, const float *__restrict__ dout
     const int lev = cbits + 1 + it.m;
     const double *Pb = P + bh * (long long)(N + 1);
     const double Pref = Pb[c0];
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-    const int RB = Dk / 16, CB = Dv / 16;
     float acc[8][8];
-#pragma unroll
-    for (int a = 0; a < 8; a++)
-#pragma unroll
-        for (int cc = 0; cc < 8; cc++) acc[a][cc] = 0.f;
+    outer_zero(acc);
     const long long t_lo = (long long)p0 * C, t_hi = (long long)p1 * C;
-    for (long long t0 = t_lo; t0 < t_hi; t0 += kSub) {
-        const int nt = (int)min((long long)kSub, t_hi - t0);
-        __syncthreads();
-        for (int e = threadIdx.x; e < kSub * Dk; e += kThreads) {
-            const int tt = e / Dk, r = e % Dk;
-            float x = 0.f;
-            if (tt < nt) {
-                const long long t = t0 + tt;
-                const int j = (int)(t / C);
+    for (long long t0 = t_lo; t0 < t_hi; t0 += kOuterSub) {
+        const int nt = (int)min((long long)kOuterSub, t_hi - t0);
+        if (threadIdx.x < kOuterSub) {
+            float w = 0.f;
+            if ((int)threadIdx.x < nt) {
+                const long long t = t0 + threadIdx.x;
                 const long long gi = bh * T + t;
-                const float w = lam[gi * L + lev] * expf((float)(Pb[j] - Pref) + gamma[gi]);
-                x = w * to_f32(q[gi * Dk + r]);
+                w = lam[gi * L + lev] * expf((float)(Pb[t / C] - Pref) + gamma[gi]);
             }
-            qs[e] = x;
-        }
-        for (int e = threadIdx.x; e < kSub * Dv; e += kThreads) {
-            const int tt = e / Dv, c = e % Dv;
-            ds[e] = (tt < nt) ? dout[(bh * T + t0 + tt) * Dv + c] : 0.f;
+            sc[threadIdx.x] = w;
         }
         __syncthreads();
-        for (int tt = 0; tt < nt; tt++) {
-            float qr[8], dc[8];
-#pragma unroll
-            for (int a = 0; a < 8; a++) qr[a] = (a < RB) ? qs[tt * Dk + ty + 16 * a] : 0.f;
-#pragma unroll
-            for (int cc = 0; cc < 8; cc++) dc[cc] = (cc < CB) ? ds[tt * Dv + tx + 16 * cc] : 0.f;
-#pragma unroll
-            for (int a = 0; a < 8; a++)
-#pragma unroll
-                for (int cc = 0; cc < 8; cc++) acc[a][cc] = fmaf(qr[a], dc[cc], acc[a][cc]);
-        }
+        outer_stage<Tin>(qs, q + (bh * T + t0) * Dk, sc, nt, Dk);
+        outer_stage<float>(ds, dout + (bh * T + t0) * Dv, nullptr, nt, Dv);
+        __syncthreads();
+        outer_accumulate(acc, qs, ds, nt, Dk, Dv);
     }
-    float *out = part + ((bh * gridDim.x) + blockIdx.x) * (long long)Dk * Dv;
-#pragma unroll
-    for (int a = 0; a < 8; a++)
-#pragma unroll
-        for (int cc = 0; cc < 8; cc++)
-            if (a < RB && cc < CB) out[(ty + 16 * a) * Dv + tx + 16 * cc] = acc[a][cc];
+    outer_store(part + ((bh * gridDim.x) + blockIdx.x) * (long long)Dk * Dv, acc, Dk, Dv, false);
 }
 
 // R_{m,b} = sum of its pieces in piece order (bitwise reproducible).  One

@@ -11,6 +11,7 @@
 #include <cooperative_groups.h>
 
 #include "decode.cuh"
+#include "outer_simt.cuh"
 
 namespace lla {
 namespace {
@@ -196,8 +197,7 @@ prefill_tail_kernel(const float *__restrict__ g, float *__restrict__ tail, int T
     }
 }
 
-constexpr int kSeg = 2048;  // tokens per CTA of the bucket kernel
-constexpr int kSub = 32;
+constexpr int kSeg = 1024;  // tokens per CTA of the bucket kernel
 
 struct BucketTable {
     long long start[kMaxLs];
@@ -213,54 +213,36 @@ prefill_bucket_kernel(const Tin *__restrict__ k, const Tin *__restrict__ v,
                       const float *__restrict__ tail, float *__restrict__ S, BucketTable tab,
                       int T, int dk, int dv, int Ls)
 {
-    __shared__ float ks[kSub * 128];
-    __shared__ float vs[kSub * 128];
+    __shared__ __align__(16) float ks[kOuterSub * 128];
+    __shared__ __align__(16) float vs[kOuterSub * 128];
+    __shared__ float sc[kOuterSub];
     const long long bh = blockIdx.y;
     const int sid = blockIdx.x;
     int li = 0;
     while (li + 1 < tab.n && tab.seg_begin[li + 1] <= sid) li++;
     const long long s_lo = tab.start[li] + (long long)(sid - tab.seg_begin[li]) * kSeg;
     const long long s_hi = min(s_lo + kSeg, tab.start[li] + tab.len[li]);
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-    const int RB = dk / 16, CB = dv / 16;
     float acc[8][8];
-#pragma unroll
-    for (int a = 0; a < 8; a++)
-#pragma unroll
-        for (int b = 0; b < 8; b++) acc[a][b] = 0.f;
+    outer_zero(acc);
     const Tin *kb = k + bh * (long long)T * dk;
     const Tin *vb = v + bh * (long long)T * dv;
     const float *tb = tail + bh * (long long)T;
-    for (long long s0 = s_lo; s0 < s_hi; s0 += kSub) {
-        const int ns = (int)min((long long)kSub, s_hi - s0);
+    for (long long s0 = s_lo; s0 < s_hi; s0 += kOuterSub) {
+        const int ns = (int)min((long long)kOuterSub, s_hi - s0);
+        if (threadIdx.x < kOuterSub) sc[threadIdx.x] = (int)threadIdx.x < ns ? expf(tb[s0 + threadIdx.x]) : 0.f;
         __syncthreads();
-        for (int e = threadIdx.x; e < kSub * dk; e += kThreads) {
-            int s = e / dk, r = e % dk;
-            ks[e] = (s < ns) ? to_f32(kb[(s0 + s) * dk + r]) : 0.f;
-        }
-        for (int e = threadIdx.x; e < kSub * dv; e += kThreads) {
-            int s = e / dv, c = e % dv;
-            vs[e] = (s < ns) ? expf(tb[s0 + s]) * to_f32(vb[(s0 + s) * dv + c]) : 0.f;
-        }
+        outer_stage<Tin>(ks, kb + s0 * dk, nullptr, ns, dk);
+        outer_stage<Tin>(vs, vb + s0 * dv, sc, ns, dv);
         __syncthreads();
-        for (int s = 0; s < ns; s++) {
-            float kr[8], vc[8];
-#pragma unroll
-            for (int a = 0; a < 8; a++) kr[a] = (a < RB) ? ks[s * dk + ty + 16 * a] : 0.f;
-#pragma unroll
-            for (int b = 0; b < 8; b++) vc[b] = (b < CB) ? vs[s * dv + tx + 16 * b] : 0.f;
-#pragma unroll
-            for (int a = 0; a < 8; a++)
-#pragma unroll
-                for (int b = 0; b < 8; b++) acc[a][b] = fmaf(kr[a], vc[b], acc[a][b]);
-        }
+        outer_accumulate(acc, ks, vs, ns, dk, dv);
     }
+    const int r0 = 8 * (threadIdx.x >> 4), c0 = 8 * (threadIdx.x & 15);
+    if (r0 >= dk || c0 >= dv) return;
     float *Sl = S + (bh * Ls + tab.slot[li]) * (long long)dk * dv;
 #pragma unroll
     for (int a = 0; a < 8; a++)
 #pragma unroll
-        for (int b = 0; b < 8; b++)
-            if (a < RB && b < CB) atomicAdd(Sl + (ty + 16 * a) * dv + tx + 16 * b, acc[a][b]);
+        for (int b = 0; b < 8; b++) atomicAdd(Sl + (r0 + a) * dv + c0 + b, acc[a][b]);
 }
 
 template <typename Tin, int DV>

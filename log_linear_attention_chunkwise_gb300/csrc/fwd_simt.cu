@@ -20,6 +20,7 @@
 // Query row a of chunk i adds, for the bucket ending at j (m = ctz(j)),
 //   lambda_a[c+1+m] * exp(gamma_a + P_i - P_j) * q_a^T Node_j.
 #include "fwd_simt.cuh"
+#include "outer_simt.cuh"
 
 namespace lla {
 namespace {
@@ -62,10 +63,12 @@ simt_chunk_state_kernel(const Tin *__restrict__ k, const Tin *__restrict__ v,
                         const float *__restrict__ g, float *__restrict__ gam,
                         float *__restrict__ nodes, int T, int dk, int dv, int C, int N)
 {
-    extern __shared__ float sm[];
+    static_assert(kThreads == kOuterThreads && kSub == kOuterSub, "outer-product tiling");
+    extern __shared__ __align__(16) float sm[];
     float *gl = sm;                // [128] gamma
-    float *ks = gl + 128;          // [kSub][dk]
-    float *vs = ks + kSub * dk;    // [kSub][dv], rows scaled by exp(Gam - gamma)
+    float *sc = gl + 128;          // [kSub] row scales exp(Gam - gamma)
+    float *ks = sc + kSub;         // [kSub][dk]
+    float *vs = ks + kSub * dk;    // [kSub][dv], rows scaled
     const int i = blockIdx.x;
     const long long bh = blockIdx.y;
     const long long tok0 = bh * (long long)T + (long long)i * C;
@@ -76,44 +79,18 @@ simt_chunk_state_kernel(const Tin *__restrict__ k, const Tin *__restrict__ v,
     if (threadIdx.x == 0) gam[bh * N + i] = Gam;
     if (i == N - 1) return;  // the last chunk's state starts no node
 
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-    const int RB = dk / 16, CB = dv / 16;
     float acc[8][8];
-#pragma unroll
-    for (int a = 0; a < 8; a++)
-#pragma unroll
-        for (int b = 0; b < 8; b++) acc[a][b] = 0.f;
-
+    outer_zero(acc);
     for (int s0 = 0; s0 < C; s0 += kSub) {
         const int ns = min(kSub, C - s0);
-        for (int e = threadIdx.x; e < kSub * dk; e += kThreads) {
-            int s = e / dk, r = e % dk;
-            ks[e] = (s < ns) ? to_f32(k[(tok0 + s0 + s) * dk + r]) : 0.f;
-        }
-        for (int e = threadIdx.x; e < kSub * dv; e += kThreads) {
-            int s = e / dv, cc = e % dv;
-            vs[e] = (s < ns) ? expf(Gam - gl[s0 + s]) * to_f32(v[(tok0 + s0 + s) * dv + cc]) : 0.f;
-        }
+        if (threadIdx.x < kSub) sc[threadIdx.x] = threadIdx.x < ns ? expf(Gam - gl[s0 + threadIdx.x]) : 0.f;
         __syncthreads();
-        for (int s = 0; s < ns; s++) {
-            float kr[8], vc[8];
-#pragma unroll
-            for (int a = 0; a < 8; a++) kr[a] = (a < RB) ? ks[s * dk + ty + 16 * a] : 0.f;
-#pragma unroll
-            for (int b = 0; b < 8; b++) vc[b] = (b < CB) ? vs[s * dv + tx + 16 * b] : 0.f;
-#pragma unroll
-            for (int a = 0; a < 8; a++)
-#pragma unroll
-                for (int b = 0; b < 8; b++) acc[a][b] = fmaf(kr[a], vc[b], acc[a][b]);
-        }
+        outer_stage<Tin>(ks, k + (tok0 + s0) * dk, nullptr, ns, dk);
+        outer_stage<Tin>(vs, v + (tok0 + s0) * dv, sc, ns, dv);
         __syncthreads();
+        outer_accumulate(acc, ks, vs, ns, dk, dv);
     }
-    float *H = nodes + (bh * N + (i + 1)) * (long long)dk * dv;
-#pragma unroll
-    for (int a = 0; a < 8; a++)
-#pragma unroll
-        for (int b = 0; b < 8; b++)
-            if (a < RB && b < CB) H[(ty + 16 * a) * dv + tx + 16 * b] = acc[a][b];
+    outer_store(nodes + (bh * N + (i + 1)) * (long long)dk * dv, acc, dk, dv, false);
 }
 
 // P[bh][j] = sum_{i<j} gam[bh][i] in fp64, j = 0..N.
@@ -300,7 +277,7 @@ cudaError_t launch_nodes(const SimtFwdArgs &A)
     float *gam = (float *)ws;
     double *P = (double *)(ws + simt_ws_offset_P(A));
     float *nodes = (float *)(ws + simt_ws_offset_nodes(A));
-    size_t sm1 = sizeof(float) * (128 + kSub * A.dk + kSub * A.dv);
+    size_t sm1 = sizeof(float) * (128 + kSub + kSub * A.dk + kSub * A.dv);
     simt_chunk_state_kernel<Tin><<<dim3(N, BH), kThreads, sm1, st>>>(
         (const Tin *)A.k, (const Tin *)A.v, A.g, gam, nodes, A.T, A.dk, A.dv, A.C, N);
     simt_gate_prefix_kernel<<<BH, kThreads, 0, st>>>(gam, P, N);
