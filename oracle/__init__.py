@@ -19,7 +19,12 @@ What each function follows (page "Log-Linear Attention", gist.science
   lambda_mlp         page "Adaptive memory decay for Log-Linear Attention",
                      §LambdaMLPSoftplus: lambda = softplus((d W1) W2 + b);
   backward           the derivatives of the §2.2 double sum, term by term
-                     (the pages give no backward; see the C source).
+                     (the pages give no backward; see the C source);
+  gdn_*              Log-Linear Gated DeltaNet (§3 names it, gives no formula):
+                     per-bucket Gated DeltaNet states read out with lambda,
+                     in a pair form (gdn_naive), a recurrent form
+                     (gdn_fenwick, gdn_decode_step) and the base model
+                     (gdn_base).
 Every function is pinned by tests in ``tests/test_oracle_pins.py``.
 """
 
@@ -65,9 +70,14 @@ def _load():
         lib.oracle_level.argtypes = [I, I]
         lib.oracle_lambda_mlp.argtypes = [P] * 5 + [I] * 3
         lib.oracle_backward.argtypes = [P] * 11 + [I] * 6
+        lib.oracle_gdn_naive.argtypes = [P] * 7 + [I] * 6
+        lib.oracle_gdn_fenwick.argtypes = [P] * 7 + [I] * 6
+        lib.oracle_gdn_base.argtypes = [P] * 6 + [I] * 5
+        lib.oracle_gdn_decode_step.argtypes = [P] * 9 + [I] * 5
         for name in ("oracle_naive", "oracle_naive_rows", "oracle_fenwick", "oracle_decode_step",
                      "oracle_state_closed_form", "oracle_ssd", "oracle_level", "oracle_lambda_mlp",
-                     "oracle_num_threads", "oracle_backward"):
+                     "oracle_num_threads", "oracle_backward", "oracle_gdn_naive",
+                     "oracle_gdn_fenwick", "oracle_gdn_base", "oracle_gdn_decode_step"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -210,3 +220,47 @@ def backward(q, k, v, g, lam, dout):
                                    _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dlam),
                                    B, H, T, Dk, Dv, L), "oracle_backward")
     return dq, dk, dv, dg, dlam
+
+
+def gdn_naive(q, k, v, g, beta, lam) -> np.ndarray:
+    q, k, v, g, beta, lam = map(_f64, (q, k, v, g, beta, lam))
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    out = np.zeros((B, H, T, dv), np.float64)
+    _check(_load().oracle_gdn_naive(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(lam),
+                                    _ptr(out), B, H, T, dk, dv, lam.shape[-1]), "oracle_gdn_naive")
+    return out
+
+
+def gdn_fenwick(q, k, v, g, beta, lam) -> np.ndarray:
+    q, k, v, g, beta, lam = map(_f64, (q, k, v, g, beta, lam))
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    out = np.zeros((B, H, T, dv), np.float64)
+    _check(_load().oracle_gdn_fenwick(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(lam),
+                                      _ptr(out), B, H, T, dk, dv, lam.shape[-1]), "oracle_gdn_fenwick")
+    return out
+
+
+def gdn_base(q, k, v, g, beta) -> np.ndarray:
+    q, k, v, g, beta = map(_f64, (q, k, v, g, beta))
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    out = np.zeros((B, H, T, dv), np.float64)
+    _check(_load().oracle_gdn_base(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(out),
+                                   B, H, T, dk, dv), "oracle_gdn_base")
+    return out
+
+
+def gdn_decode_step(S, q, k, v, g, beta, lam, pos) -> np.ndarray:
+    """One step on the eager level state S [B,H,Ls,dk,dv] (updated in place);
+    returns out [B,H,dv]."""
+    assert S.dtype == np.float64 and S.flags.c_contiguous
+    q, k, v, g, beta, lam = map(_f64, (q, k, v, g, beta, lam))
+    pos = np.ascontiguousarray(np.asarray(pos), dtype=np.int64)
+    B, H, Ls, dk, dv = S.shape
+    out = np.zeros((B, H, dv), np.float64)
+    _check(_load().oracle_gdn_decode_step(_ptr(S), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                          _ptr(lam), _ptr(out), _ptr(pos), B, H, dk, dv, Ls),
+           "oracle_gdn_decode_step")
+    return out

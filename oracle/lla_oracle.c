@@ -572,3 +572,258 @@ int oracle_backward(const double *q, const double *k, const double *v,
     }
     return bad ? -3 : 0;
 }
+
+/*
+ * Log-Linear Gated DeltaNet.  "Log-Linear Attention" §3 names the variant
+ * and says it keeps the base model's structure and adds the hierarchical
+ * (Fenwick) mask; it prints no formula.  Reading taken: every Fenwick
+ * bucket keeps its own state, all states follow the Gated DeltaNet
+ * transition of each new token, and the read-out weights them by lambda:
+ *     A_r = alpha_r (I - beta_r k_r k_r^T),  alpha_r = exp(g_r),
+ *     o_t = sum_{s<=t} lam_t[level(t,s)] beta_s v_s (k_s^T A_{s+1} ... A_t q_t).
+ * With lambda = 1 this is Gated DeltaNet (sum of the bucket states = its
+ * single state); with mutually orthogonal keys the transitions reduce to
+ * the scalar decay and it is Log-Linear Mamba-2 with values beta_s v_s.
+ * Arrays as for oracle_naive plus beta [B,H,T].
+ */
+
+/* x <- A_r x for one token r. */
+static void gdn_apply(double *x, const double *kr, double alpha, double beta,
+                      int64_t dk)
+{
+    double c = beta * dot(kr, x, dk);
+    for (int64_t i = 0; i < dk; i++)
+        x[i] = alpha * (x[i] - c * kr[i]);
+}
+
+/* Pair form: for each query t walk s = t, t-1, ..., 0 carrying
+   x = A_{s+1} ... A_t q_t.  O(T^2 (dk+dv)) per (batch, head). */
+int oracle_gdn_naive(const double *q, const double *k, const double *v,
+                     const double *g, const double *beta, const double *lam,
+                     double *out, int64_t B, int64_t H, int64_t T, int64_t dk,
+                     int64_t dv, int64_t L)
+{
+    if (B < 0 || H < 0 || T < 0 || dk <= 0 || dv <= 0 || L <= 0)
+        return -1;
+    if (T > 0 && bit_length((uint64_t)(T - 1)) > L - 1)
+        return -2;
+    int64_t BH = B * H;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t bh = 0; bh < BH; bh++) {
+        const double *qh = q + bh * T * dk, *kh = k + bh * T * dk;
+        const double *vh = v + bh * T * dv, *gh = g + bh * T, *bt = beta + bh * T;
+        const double *lh = lam + bh * T * L;
+        double *oh = out + bh * T * dv;
+        double *x = (double *)malloc(sizeof(double) * (size_t)dk);
+        if (!x) {
+            bad |= 1;
+            continue;
+        }
+        for (int64_t t = 0; t < T; t++) {
+            double *o = oh + t * dv;
+            for (int64_t j = 0; j < dv; j++)
+                o[j] = 0.0;
+            memcpy(x, qh + t * dk, sizeof(double) * (size_t)dk);
+            for (int64_t s = t; s >= 0; s--) {
+                double w = lh[t * L + oracle_level(t, s)] * bt[s] * dot(kh + s * dk, x, dk);
+                for (int64_t j = 0; j < dv; j++)
+                    o[j] += w * vh[s * dv + j];
+                gdn_apply(x, kh + s * dk, exp(gh[s]), bt[s], dk);
+            }
+        }
+        free(x);
+    }
+    return bad ? -3 : 0;
+}
+
+/* S <- A S for a state S [dk][dv] (S = sum k v^T form), column by column. */
+static void gdn_transition(double *S, const double *kt, double alpha,
+                           double beta, int64_t dk, int64_t dv)
+{
+    for (int64_t j = 0; j < dv; j++) {
+        double c = 0.0;
+        for (int64_t i = 0; i < dk; i++)
+            c += kt[i] * S[i * dv + j];
+        c *= beta;
+        for (int64_t i = 0; i < dk; i++)
+            S[i * dv + j] = alpha * (S[i * dv + j] - c * kt[i]);
+    }
+}
+
+/*
+ * Recurrent form, per token t (states as in oracle_fenwick, S = sum k v^T):
+ *   1. every live level state: S_l <- A_t S_l;
+ *   2. o_t = lam_t[0] beta_t (q_t.k_t) v_t + sum_{live l} lam_t[l] S_l^T q_t;
+ *   3. Fenwick insert: S_{m+1} = beta_t k_t v_t^T + sum_{l=1..m} S_l,
+ *      m = trailing zeros of t+1.
+ */
+int oracle_gdn_fenwick(const double *q, const double *k, const double *v,
+                       const double *g, const double *beta, const double *lam,
+                       double *out, int64_t B, int64_t H, int64_t T, int64_t dk,
+                       int64_t dv, int64_t L)
+{
+    if (B < 0 || H < 0 || T < 0 || dk <= 0 || dv <= 0 || L <= 0)
+        return -1;
+    if (T > 0 && bit_length((uint64_t)(T - 1)) > L - 1)
+        return -2;
+    const int64_t nslot = L + 1;
+    int64_t BH = B * H;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t bh = 0; bh < BH; bh++) {
+        const double *qh = q + bh * T * dk, *kh = k + bh * T * dk;
+        const double *vh = v + bh * T * dv, *gh = g + bh * T, *bt = beta + bh * T;
+        const double *lh = lam + bh * T * L;
+        double *oh = out + bh * T * dv;
+        double *S = (double *)calloc((size_t)(nslot * dk * dv), sizeof(double));
+        int *live = (int *)calloc((size_t)nslot, sizeof(int));
+        if (!S || !live) {
+            free(S);
+            free(live);
+            bad |= 1;
+            continue;
+        }
+        for (int64_t t = 0; t < T; t++) {
+            const double *qt = qh + t * dk, *kt = kh + t * dk, *vt = vh + t * dv;
+            const double *lt = lh + t * L;
+            double *o = oh + t * dv;
+            for (int64_t l = 1; l < nslot; l++)
+                if (live[l])
+                    gdn_transition(S + l * dk * dv, kt, exp(gh[t]), bt[t], dk, dv);
+            double diag = lt[0] * bt[t] * dot(qt, kt, dk);
+            for (int64_t j = 0; j < dv; j++)
+                o[j] = diag * vt[j];
+            for (int64_t l = 1; l < nslot; l++) {
+                if (!live[l])
+                    continue;
+                if (l >= L) {
+                    bad |= 2;
+                    continue;
+                }
+                const double *Sl = S + l * dk * dv;
+                for (int64_t j = 0; j < dv; j++) {
+                    double acc = 0.0;
+                    for (int64_t i = 0; i < dk; i++)
+                        acc += qt[i] * Sl[i * dv + j];
+                    o[j] += lt[l] * acc;
+                }
+            }
+            int m = trailing_zeros((uint64_t)(t + 1));
+            if (m + 1 >= nslot) {
+                bad |= 4;
+                continue;
+            }
+            double *dst = S + (m + 1) * dk * dv;
+            for (int64_t i = 0; i < dk; i++)
+                for (int64_t j = 0; j < dv; j++)
+                    dst[i * dv + j] = bt[t] * kt[i] * vt[j];
+            for (int64_t l = 1; l <= m; l++) {
+                const double *Sl = S + l * dk * dv;
+                for (int64_t e = 0; e < dk * dv; e++)
+                    dst[e] += Sl[e];
+                live[l] = 0;
+            }
+            live[m + 1] = 1;
+        }
+        free(S);
+        free(live);
+    }
+    return bad ? -(8 + bad) : 0;
+}
+
+/* The base model, Gated DeltaNet, with one state: S <- A_t S + beta_t k_t v_t^T,
+   o_t = S^T q_t. */
+int oracle_gdn_base(const double *q, const double *k, const double *v,
+                    const double *g, const double *beta, double *out, int64_t B,
+                    int64_t H, int64_t T, int64_t dk, int64_t dv)
+{
+    if (B < 0 || H < 0 || T < 0 || dk <= 0 || dv <= 0)
+        return -1;
+    int64_t BH = B * H;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t bh = 0; bh < BH; bh++) {
+        double *S = (double *)calloc((size_t)(dk * dv), sizeof(double));
+        if (!S) {
+            bad |= 1;
+            continue;
+        }
+        for (int64_t t = 0; t < T; t++) {
+            const double *qt = q + (bh * T + t) * dk, *kt = k + (bh * T + t) * dk;
+            const double *vt = v + (bh * T + t) * dv;
+            double bt = beta[bh * T + t];
+            gdn_transition(S, kt, exp(g[bh * T + t]), bt, dk, dv);
+            for (int64_t i = 0; i < dk; i++)
+                for (int64_t j = 0; j < dv; j++)
+                    S[i * dv + j] += bt * kt[i] * vt[j];
+            double *o = out + (bh * T + t) * dv;
+            for (int64_t j = 0; j < dv; j++) {
+                double acc = 0.0;
+                for (int64_t i = 0; i < dk; i++)
+                    acc += qt[i] * S[i * dv + j];
+                o[j] = acc;
+            }
+        }
+        free(S);
+    }
+    return bad ? -3 : 0;
+}
+
+/*
+ * One decode step of the recurrent form on an eager level state
+ * S [B,H,Ls,dk,dv] (slot i = level i+1; slot i is live for token t iff
+ * bit i of t is set): steps 1-3 of oracle_gdn_fenwick for the token index
+ * t = pos[b].  q,k [B,H,dk], v [B,H,dv], g, beta [B,H], lam [B,H,Ls+1],
+ * out [B,H,dv].  Returns -4 if some t has bit_length(t+1) > Ls.
+ */
+int oracle_gdn_decode_step(double *S, const double *q, const double *k,
+                           const double *v, const double *g, const double *beta,
+                           const double *lam, double *out, const int64_t *pos,
+                           int64_t B, int64_t H, int64_t dk, int64_t dv, int64_t Ls)
+{
+    if (B < 0 || H < 0 || dk <= 0 || dv <= 0 || Ls <= 0)
+        return -1;
+    for (int64_t b = 0; b < B; b++)
+        if (pos[b] < 0 || bit_length((uint64_t)(pos[b] + 1)) > Ls)
+            return -4;
+    for (int64_t bh = 0; bh < B * H; bh++) {
+        const int64_t t = pos[bh / H];
+        double *Sb = S + bh * Ls * dk * dv;
+        const double *qt = q + bh * dk, *kt = k + bh * dk, *vt = v + bh * dv;
+        const double *lt = lam + bh * (Ls + 1);
+        const double bt = beta[bh];
+        double *o = out + bh * dv;
+        for (int64_t i = 0; i < Ls; i++)
+            if ((t >> i) & 1)
+                gdn_transition(Sb + i * dk * dv, kt, exp(g[bh]), bt, dk, dv);
+        double diag = lt[0] * bt * dot(qt, kt, dk);
+        for (int64_t j = 0; j < dv; j++)
+            o[j] = diag * vt[j];
+        for (int64_t i = 0; i < Ls; i++) {
+            if (!((t >> i) & 1))
+                continue;
+            const double *Sl = Sb + i * dk * dv;
+            for (int64_t j = 0; j < dv; j++) {
+                double acc = 0.0;
+                for (int64_t r = 0; r < dk; r++)
+                    acc += qt[r] * Sl[r * dv + j];
+                o[j] += lt[i + 1] * acc;
+            }
+        }
+        int m = trailing_zeros((uint64_t)(t + 1));
+        double *dst = Sb + m * dk * dv;
+        double *tmp = (double *)malloc(sizeof(double) * (size_t)(dk * dv));
+        if (!tmp)
+            return -3;
+        for (int64_t r = 0; r < dk; r++)
+            for (int64_t j = 0; j < dv; j++)
+                tmp[r * dv + j] = bt * kt[r] * vt[j];
+        for (int64_t i = 0; i < m; i++)
+            for (int64_t e = 0; e < dk * dv; e++)
+                tmp[e] += Sb[i * dk * dv + e];
+        memcpy(dst, tmp, sizeof(double) * (size_t)(dk * dv));
+        free(tmp);
+    }
+    return 0;
+}
