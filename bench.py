@@ -83,6 +83,18 @@ def bwd_flops(cfg: W.FwdConfig) -> float:
     return cfg.B * cfg.H * (nodes + intra + query + state + keyside)
 
 
+def gdn_flops(cfg: W.FwdConfig) -> float:
+    """Algorithmic flops of the recurrent Log-Linear Gated DeltaNet forward:
+    per token, every live bucket state (popcount(t) of them) takes two
+    column dot products (q.S, k.S) and the rank-one transition (3 x 2 dk dv),
+    the states folded into the new bucket are added (ctz(t+1) x dk dv) and
+    the new state is written (2 dk dv)."""
+    dk, dv = cfg.dk, cfg.dv
+    per = sum(bin(t).count("1") * 6 * dk * dv + ((t + 1) & -(t + 1)).bit_length() * dk * dv
+              + 2 * dk * dv for t in range(cfg.T))
+    return cfg.B * cfg.H * per
+
+
 def fp32_alu_peak_tflops(sm_mhz: float) -> float:
     """CUDA-core fp32 peak: 152 SMs x 128 fp32 lanes x 2 flops (FMA) x clock."""
     return 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
@@ -371,6 +383,46 @@ def run_next_rows(dev, x, cfg, args):
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
                      "frac": gbs / hbm_peak, "algorithmic_bytes": nbytes}}
     del lam
+
+    # Log-Linear Gated DeltaNet: recurrent forward at its 2K workload and a
+    # decode step at the decode workload's shape on a random state
+    gcfg = W.GDN_CONFIG
+    gx = {n: t.to(dev) for n, t in W.make_gdn_inputs(gcfg).items()}
+    gout = torch.empty((gcfg.B, gcfg.H, gcfg.T, gcfg.dv), device=dev)
+    ms = time_calls(lambda: binding.gdn_fwd(gx["q"], gx["k"], gx["v"], gx["g"], gx["beta"], gx["lam"],
+                                            out=gout, stream=stream), stream)
+    flops = gdn_flops(gcfg)
+    tf = flops / (ms / 1e3) / 1e12
+    peak = fp32_alu_peak_tflops(load_peaks_raw().get("sm_max_mhz", 2070.0))
+    res["gdn_fwd"] = {
+        "workload": f"{gcfg.name}: B={gcfg.B} H={gcfg.H} T={gcfg.T} dk=dv={gcfg.dk} bf16, recurrent form",
+        "ms": ms, "tokens_per_s": gcfg.B * gcfg.T / (ms / 1e3),
+        "roofline": {"bound": "alu", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
+                     "algorithmic_flops": flops,
+                     "note": "T dependent steps per (batch, head, column block): latency-bound"}}
+    del gx, gout
+    dc = W.DECODE_CONFIG
+    pos = W.make_decode_positions(dc).to(dev)
+    gS = (0.01 * torch.randn((dc.batch, dc.H, dc.Ls, dc.dk, dc.dv), device=dev)).contiguous()
+    gq = torch.randn((dc.batch, dc.H, dc.dk), device=dev).to(torch.bfloat16)
+    gk = torch.nn.functional.normalize(torch.randn((dc.batch, dc.H, dc.dk), device=dev), dim=-1).to(torch.bfloat16)
+    gv = torch.randn((dc.batch, dc.H, dc.dv), device=dev).to(torch.bfloat16)
+    gg = -torch.nn.functional.softplus(torch.randn((dc.batch, dc.H), device=dev))
+    gb = torch.sigmoid(torch.randn((dc.batch, dc.H), device=dev))
+    gl = torch.ones((dc.batch, dc.H, dc.Ls + 1), device=dev)
+    go = torch.empty((dc.batch, dc.H, dc.dv), device=dev)
+    ms = time_calls(lambda: binding.gdn_decode_step(gS, gq, gk, gv, gg, gb, gl, pos, out=go, stream=stream),
+                    stream, warm=3, reps=20)
+    slot = dc.dk * dc.dv * 4
+    nbytes = dc.H * sum((2 * bin(int(p)).count("1") + 1) * slot for p in pos.tolist())
+    gbs = nbytes / (ms / 1e3) / 1e9
+    res["gdn_decode"] = {
+        "workload": "decode shape: 64 seqs, H=16, dk=dv=128, 17 fp32 slots, one token per step",
+        "us_per_step": ms * 1e3,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": gbs / hbm_peak, "algorithmic_bytes": nbytes,
+                     "note": "live slots read and written once, the new slot written"}}
+    del gS
 
     # backward (CUDA cores, fp32 arithmetic)
     if not args.skip_bwd:

@@ -184,6 +184,51 @@ lla_status lla_prefill_state(const void *k, const void *v, const float *g,
                              size_t workspace_bytes, void *stream);
 
 /*
+ * Log-Linear Gated DeltaNet ("Log-Linear Attention" §3 names it: the Gated
+ * DeltaNet state update under the hierarchical Fenwick mask; the pages give
+ * no formula).  Reading implemented: every Fenwick bucket keeps its own
+ * state, all bucket states take each token's transition
+ *   A_t = exp(g_t) (I - beta_t k_t k_t^T),
+ * and the read-out weights them by lambda:
+ *   o_t = sum_{s<=t} lambda_t[l(t,s)] beta_s v_s (k_s^T A_{s+1} ... A_t q_t).
+ * With lambda = 1 it is Gated DeltaNet.  Keys should be L2-normalised and
+ * beta in [0,1] for the transitions to be contractions (not checked).
+ *
+ * lla_gdn_fwd runs the recurrent form (§2.3) over a whole sequence from the
+ * empty state on CUDA cores (fp32): one CTA per (batch, head, 8 or 16 value
+ * columns) steps through the tokens with the bucket states in shared memory.
+ *   q, k [B,H,T,dk], v [B,H,T,dv] in in_dt; g, beta [B,H,T] fp32;
+ *   lambda [B,H,T,L] fp32 with L = lla_num_levels(T); out [B,H,T,dv] fp32.
+ *   state_out (nullable) [B,H,Ls_out,dk,dv] fp32 receives the state after the
+ *   sequence in the layout of lla_gdn_decode_step (slot i = level i+1, dead
+ *   slots zeroed); Ls_out >= bit_length(T) when state_out is given.
+ * Supported: dk, dv in {16,32,64,128}, T <= 2^16 (the bucket states must fit
+ * in shared memory), B, H <= 65535.  No workspace.  Errors as lla_fwd.
+ */
+lla_status lla_gdn_fwd(const void *q, const void *k, const void *v, const float *g,
+                       const float *beta, const float *lambda, float *out,
+                       float *state_out, int B, int H, int T, int dk, int dv,
+                       int Ls_out, lla_dtype in_dt, void *stream);
+
+/*
+ * One decode step of Log-Linear Gated DeltaNet on an eager level state:
+ *   state [B,H,Ls,dk,dv] fp32, slot i = level i+1, live for token t = pos[b]
+ *   iff bit i of t is set (the state holds the prefix [0, t));
+ *   q, k [B,H,dk], v [B,H,dv] in_dt; g, beta [B,H] fp32; lambda [B,H,Ls+1];
+ *   out [B,H,dv] fp32; pos [B] int64 on the device.
+ * The step transitions every live slot in place, reads out, and writes slot
+ * ctz(t+1) = beta k v^T + the slots below it (which become dead; their
+ * contents are left as they were).  A position without room
+ * (bit_length(t+1) > Ls) sets *device_error = 1 + b (if non-NULL) and that
+ * batch row is skipped.  Ls <= 40.
+ */
+lla_status lla_gdn_decode_step(float *state, const void *q, const void *k,
+                               const void *v, const float *g, const float *beta,
+                               const float *lambda, float *out, const int64_t *pos,
+                               int B, int H, int dk, int dv, int Ls, lla_dtype in_dt,
+                               int32_t *device_error, void *stream);
+
+/*
  * Backward of lla_fwd: given dout = dLoss/dout, the gradients of every input.
  * "Log-Linear Attention" §2.2 defines the forward only; these are the
  * derivatives of that double sum (A_ts = lambda_t[l(t,s)] exp(G_t - G_s),

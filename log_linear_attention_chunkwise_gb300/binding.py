@@ -38,6 +38,8 @@ SIGNATURES = {
     "lla_lambda_mlp": (_I, [_P] * 5 + [_I] * 5 + [_I, _P]),
     "lla_bwd_workspace_bytes": (_Z, [_I] * 7),
     "lla_bwd": (_I, [_P] * 11 + [_I] * 7 + [_P, _Z, _P]),
+    "lla_gdn_fwd": (_I, [_P] * 8 + [_I] * 6 + [_I, _P]),
+    "lla_gdn_decode_step": (_I, [_P] * 9 + [_I] * 5 + [_I, _P, _P]),
 }
 
 _lib = None
@@ -233,3 +235,56 @@ def bwd(q, k, v, g, lam, dout, chunk: int = 64, workspace=None, stream=None):
                      workspace.numel(), _stream(stream))
     _check("lla_bwd", rc)
     return dq, dkk, dvv, dg, dl
+
+
+def gdn_fwd(q, k, v, g, beta, lam, out=None, state_Ls: int = 0, stream=None):
+    """lla_gdn_fwd: Log-Linear Gated DeltaNet over whole sequences.  Returns
+    out [B,H,T,dv], or (out, state [B,H,state_Ls,dk,dv]) when state_Ls > 0."""
+    lib = load()
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, n, q.dtype, 4)
+    _need(g, "g", torch.float32, 3)
+    _need(beta, "beta", torch.float32, 3)
+    _need(lam, "lam", torch.float32, 4)
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape[:3] != (B, H, T) or g.shape != (B, H, T) or \
+            beta.shape != (B, H, T) or lam.shape[:3] != (B, H, T) or \
+            lam.shape[3] != max(lib.lla_num_levels(T), 1):
+        raise ValueError("inconsistent shapes")
+    if out is None:
+        out = torch.empty((B, H, T, dv), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.float32, 4)
+    state = None
+    if state_Ls > 0:
+        state = torch.empty((B, H, state_Ls, dk, dv), dtype=torch.float32, device=q.device)
+    rc = lib.lla_gdn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(lam), _ptr(out),
+                         _ptr(state) if state is not None else None, B, H, T, dk, dv, state_Ls,
+                         _dt(q), _stream(stream))
+    _check("lla_gdn_fwd", rc)
+    return (out, state) if state is not None else out
+
+
+def gdn_decode_step(state, q, k, v, g, beta, lam, pos, out=None, device_error=None, stream=None):
+    """lla_gdn_decode_step: one token per (batch, head) on state [B,H,Ls,dk,dv]
+    (updated in place).  Returns out [B,H,dv]."""
+    lib = load()
+    _need(state, "state", torch.float32, 5)
+    B, H, Ls, dk, dv = state.shape
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, n, q.dtype, 3)
+    _need(g, "g", torch.float32, 2)
+    _need(beta, "beta", torch.float32, 2)
+    _need(lam, "lam", torch.float32, 3)
+    _need(pos, "pos", torch.int64, 1)
+    if q.shape != (B, H, dk) or k.shape != (B, H, dk) or v.shape != (B, H, dv) or \
+            lam.shape != (B, H, Ls + 1) or pos.shape != (B,):
+        raise ValueError("inconsistent shapes")
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=torch.float32, device=q.device)
+    rc = lib.lla_gdn_decode_step(_ptr(state), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                 _ptr(lam), _ptr(out), _ptr(pos), B, H, dk, dv, Ls, _dt(q),
+                                 _ptr(device_error) if device_error is not None else None,
+                                 _stream(stream))
+    _check("lla_gdn_decode_step", rc)
+    return out

@@ -1,0 +1,290 @@
+// Log-Linear Gated DeltaNet, recurrent form.
+//
+// "Log-Linear Attention" §3 builds Log-Linear Gated DeltaNet by keeping the
+// Gated DeltaNet state update and adding the hierarchical (Fenwick) mask; the
+// pages give no formula.  Here every Fenwick bucket of the prefix keeps its
+// own state S_l (dk x dv, the sum-of-k-v^T orientation) and all of them take
+// each token's transition A_t = alpha_t (I - beta_t k_t k_t^T),
+// alpha_t = exp(g_t).  Per token t (§2.3's recurrent form, slot i = level
+// i+1, live iff bit i of t is set):
+//   1. S_l <- A_t S_l for every live slot;
+//   2. o_t = lam_t[0] beta_t (q_t.k_t) v_t + sum_live lam_t[l] S_l^T q_t;
+//   3. slot m = ctz(t+1) receives beta_t k_t v_t^T + sum of slots below it.
+// Column c of every state only ever mixes with itself: with
+// P = q.S[:,c] and U = k.S[:,c] of the old state, the new column is
+// alpha (S[:,c] - beta U k) and its read-out alpha (P - beta U (q.k)).
+// A CTA owns kW columns of one (batch, head) and a thread (c, rg) owns R
+// rows of its column, so the only cross-thread step is summing P and U over
+// the row groups.
+#include "gdn.cuh"
+
+namespace lla {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kTokBlk = 32;  // tokens staged per refill of the forward
+
+template <int KW>
+__host__ __device__ constexpr int row_groups() { return kThreads / KW; }
+
+size_t fwd_smem_floats(int T, int dk, int L, int kw)
+{
+    const int Lsi = T > 0 ? bit_length_u32((uint32_t)T) : 1;
+    const int rg = kThreads / kw;
+    return (size_t)Lsi * dk * kw          // states
+           + 2 * (size_t)Lsi * 2 * rg * kw  // partial sums, two buffers
+           + 2 * (size_t)kTokBlk * dk       // q, k
+           + (size_t)kTokBlk * kw           // v columns
+           + 3 * (size_t)kTokBlk            // alpha, beta, q.k
+           + (size_t)kTokBlk * L;           // lambda rows
+}
+
+int fwd_columns(int dk) { return dk >= 128 ? 8 : 16; }
+
+template <typename Tin, int KW>
+__global__ void __launch_bounds__(kThreads)
+gdn_fwd_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
+               const float *__restrict__ g, const float *__restrict__ beta, const float *__restrict__ lam,
+               float *__restrict__ out, float *__restrict__ state_out, int T, int H, int dk, int dv, int L,
+               int Ls_out)
+{
+    constexpr int RG = row_groups<KW>();
+    extern __shared__ __align__(16) float sm[];
+    const int Lsi = T > 0 ? bit_length_u32((uint32_t)T) : 1;
+    float *S = sm;                              // [Lsi][dk][KW]
+    float *red = S + Lsi * dk * KW;             // [2][Lsi][2][RG][KW]
+    float *qs = red + 2 * Lsi * 2 * RG * KW;    // [kTokBlk][dk]
+    float *ks = qs + kTokBlk * dk;              // [kTokBlk][dk]
+    float *vs = ks + kTokBlk * dk;              // [kTokBlk][KW]
+    float *as = vs + kTokBlk * KW;              // [kTokBlk] alpha
+    float *bs = as + kTokBlk;                   // [kTokBlk] beta
+    float *qk = bs + kTokBlk;                   // [kTokBlk] q.k
+    float *ls = qk + kTokBlk;                   // [kTokBlk][L]
+    const int c = threadIdx.x % KW, rg = threadIdx.x / KW;
+    const int R = dk / RG;  // rows per thread (1..8)
+    const int col = blockIdx.x * KW + c;
+    const long long bh = (long long)blockIdx.z * H + blockIdx.y;
+    const long long tok0 = bh * (long long)T;
+    for (int t0 = 0; t0 < T; t0 += kTokBlk) {
+        const int nt = min(kTokBlk, T - t0);
+        __syncthreads();  // the previous block is consumed
+        for (int e = threadIdx.x; e < nt * dk; e += kThreads) {
+            qs[e] = to_f32(q[(tok0 + t0) * dk + e]);
+            ks[e] = to_f32(k[(tok0 + t0) * dk + e]);
+        }
+        for (int e = threadIdx.x; e < nt * KW; e += kThreads)
+            vs[e] = to_f32(v[(tok0 + t0 + e / KW) * dv + blockIdx.x * KW + e % KW]);
+        for (int e = threadIdx.x; e < nt; e += kThreads) {
+            as[e] = expf(g[tok0 + t0 + e]);
+            bs[e] = beta[tok0 + t0 + e];
+        }
+        for (int e = threadIdx.x; e < nt * L; e += kThreads) ls[e] = lam[(tok0 + t0) * L + e];
+        __syncthreads();
+        if (threadIdx.x < nt) {
+            float a = 0.f;
+            for (int r = 0; r < dk; r++) a = fmaf(qs[threadIdx.x * dk + r], ks[threadIdx.x * dk + r], a);
+            qk[threadIdx.x] = a;
+        }
+        __syncthreads();
+        for (int tt = 0; tt < nt; tt++) {
+            const uint32_t t = (uint32_t)(t0 + tt);
+            float *rd = red + (tt & 1) * (Lsi * 2 * RG * KW);
+            const float *qt = qs + tt * dk, *kt = ks + tt * dk;
+            // partial P, U of every live slot over this thread's rows
+            for (int i = 0; i < Lsi; i++) {
+                if (!((t >> i) & 1u)) continue;
+                float p = 0.f, u = 0.f;
+                for (int j = 0; j < R; j++) {
+                    const int r = rg * R + j;
+                    const float s = S[(i * dk + r) * KW + c];
+                    p = fmaf(qt[r], s, p);
+                    u = fmaf(kt[r], s, u);
+                }
+                rd[((i * 2 + 0) * RG + rg) * KW + c] = p;
+                rd[((i * 2 + 1) * RG + rg) * KW + c] = u;
+            }
+            __syncthreads();
+            const int m = ctz_u32(t + 1u);
+            const float al = as[tt], be = bs[tt], qkt = qk[tt], vc = vs[tt * KW + c];
+            const float *lt = ls + tt * L;
+            float o = lt[0] * be * qkt * vc;
+            float macc[8];
+#pragma unroll
+            for (int j = 0; j < 8; j++) macc[j] = 0.f;
+            for (int i = 0; i < Lsi; i++) {
+                if (!((t >> i) & 1u)) continue;
+                float P = 0.f, U = 0.f;
+                for (int x = 0; x < RG; x++) {
+                    P += rd[((i * 2 + 0) * RG + x) * KW + c];
+                    U += rd[((i * 2 + 1) * RG + x) * KW + c];
+                }
+                const float bu = be * U;
+#pragma unroll
+                for (int j = 0; j < 8; j++) {
+                    if (j >= R) break;
+                    const int r = rg * R + j;
+                    float *sp = S + (i * dk + r) * KW + c;
+                    const float sn = al * (*sp - bu * kt[r]);
+                    *sp = sn;
+                    if (i < m) macc[j] += sn;
+                }
+                o = fmaf(lt[i + 1], al * (P - bu * qkt), o);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                if (j >= R) break;
+                const int r = rg * R + j;
+                S[(m * dk + r) * KW + c] = fmaf(be * kt[r], vc, macc[j]);
+            }
+            if (rg == 0) out[(tok0 + t) * dv + col] = o;
+        }
+    }
+    if (state_out) {  // the state after [0, T): slot i live iff bit i of T
+        for (int i = 0; i < Ls_out; i++) {
+            const bool live = i < Lsi && (((uint32_t)T >> i) & 1u);
+            for (int j = 0; j < R; j++) {
+                const int r = rg * R + j;
+                state_out[((bh * Ls_out + i) * dk + r) * dv + col] = live ? S[(i * dk + r) * KW + c] : 0.f;
+            }
+        }
+    }
+}
+
+constexpr int kDecW = 16;  // columns per CTA of the decode step
+
+// One decode step on the level state in global memory [B,H,Ls,dk,dv].
+template <typename Tin>
+__global__ void __launch_bounds__(kThreads)
+gdn_decode_kernel(float *__restrict__ S, const Tin *__restrict__ q, const Tin *__restrict__ k,
+                  const Tin *__restrict__ v, const float *__restrict__ g, const float *__restrict__ beta,
+                  const float *__restrict__ lam, float *__restrict__ out, const int64_t *__restrict__ pos,
+                  int H, int dk, int dv, int Ls, int32_t *__restrict__ err)
+{
+    constexpr int RG = kThreads / kDecW;
+    extern __shared__ __align__(16) float sm[];
+    float *red = sm;                 // [Ls][2][RG][kDecW]
+    float *qs = red + Ls * 2 * RG * kDecW;  // [dk]
+    float *ks = qs + dk;             // [dk]
+    __shared__ float qk_s;
+    const int c = threadIdx.x % kDecW, rg = threadIdx.x / kDecW;
+    const int R = dk / RG;
+    const int col = blockIdx.x * kDecW + c;
+    const int b = blockIdx.z;
+    const long long bh = (long long)b * H + blockIdx.y;
+    const long long t64 = pos[b];
+    if (t64 < 0 || bit_length_u64((uint64_t)(t64 + 1)) > Ls) {  // no room in the state
+        if (err && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicCAS(err, 0, 1 + b);
+        return;
+    }
+    const uint64_t t = (uint64_t)t64;
+    for (int e = threadIdx.x; e < dk; e += kThreads) {
+        qs[e] = to_f32(q[bh * dk + e]);
+        ks[e] = to_f32(k[bh * dk + e]);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        float a = 0.f;
+        for (int r = threadIdx.x; r < dk; r += 32) a = fmaf(qs[r], ks[r], a);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+        if (threadIdx.x == 0) qk_s = a;
+    }
+    float *Sb = S + bh * (long long)Ls * dk * dv;
+    for (int i = 0; i < Ls; i++) {
+        if (!((t >> i) & 1u)) continue;
+        float p = 0.f, u = 0.f;
+        for (int j = 0; j < R; j++) {
+            const int r = rg * R + j;
+            const float s = Sb[((long long)i * dk + r) * dv + col];
+            p = fmaf(qs[r], s, p);
+            u = fmaf(ks[r], s, u);
+        }
+        red[((i * 2 + 0) * RG + rg) * kDecW + c] = p;
+        red[((i * 2 + 1) * RG + rg) * kDecW + c] = u;
+    }
+    __syncthreads();
+    const int m = ctz_u64(t + 1u);
+    const float al = expf(g[bh]), be = beta[bh], qkt = qk_s, vc = to_f32(v[bh * dv + col]);
+    const float *lt = lam + bh * (Ls + 1);
+    float o = lt[0] * be * qkt * vc;
+    float macc[8];
+#pragma unroll
+    for (int j = 0; j < 8; j++) macc[j] = 0.f;
+    for (int i = 0; i < Ls; i++) {
+        if (!((t >> i) & 1u)) continue;
+        float P = 0.f, U = 0.f;
+        for (int x = 0; x < RG; x++) {
+            P += red[((i * 2 + 0) * RG + x) * kDecW + c];
+            U += red[((i * 2 + 1) * RG + x) * kDecW + c];
+        }
+        const float bu = be * U;
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            if (j >= R) break;
+            const int r = rg * R + j;
+            float *sp = Sb + ((long long)i * dk + r) * dv + col;
+            const float sn = al * (*sp - bu * ks[r]);
+            if (i < m) macc[j] += sn;
+            else *sp = sn;  // slots below m are folded into slot m and die
+        }
+        o = fmaf(lt[i + 1], al * (P - bu * qkt), o);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        if (j >= R) break;
+        const int r = rg * R + j;
+        Sb[((long long)m * dk + r) * dv + col] = fmaf(be * ks[r], vc, macc[j]);
+    }
+    if (rg == 0) out[bh * dv + col] = o;
+}
+
+template <typename Tin, int KW>
+cudaError_t launch_fwd_w(const GdnFwdArgs &A)
+{
+    const size_t smem = sizeof(float) * fwd_smem_floats(A.T, A.dk, A.L, KW);
+    auto kern = gdn_fwd_kernel<Tin, KW>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(A.dv / KW, A.H, A.B), kThreads, smem, (cudaStream_t)A.stream>>>(
+        (const Tin *)A.q, (const Tin *)A.k, (const Tin *)A.v, A.g, A.beta, A.lam, A.out, A.state_out, A.T,
+        A.H, A.dk, A.dv, A.L, A.Ls_out);
+    return cudaPeekAtLastError();
+}
+
+template <typename Tin>
+cudaError_t launch_fwd(const GdnFwdArgs &A)
+{
+    return fwd_columns(A.dk) == 8 ? launch_fwd_w<Tin, 8>(A) : launch_fwd_w<Tin, 16>(A);
+}
+
+template <typename Tin>
+cudaError_t launch_decode(const GdnDecodeArgs &A)
+{
+    const size_t smem = sizeof(float) * ((size_t)A.Ls * 2 * (kThreads / kDecW) * kDecW + 2 * (size_t)A.dk);
+    auto kern = gdn_decode_kernel<Tin>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(A.dv / kDecW, A.H, A.B), kThreads, smem, (cudaStream_t)A.stream>>>(
+        A.S, (const Tin *)A.q, (const Tin *)A.k, (const Tin *)A.v, A.g, A.beta, A.lam, A.out, A.pos, A.H,
+        A.dk, A.dv, A.Ls, A.err);
+    return cudaPeekAtLastError();
+}
+
+}  // namespace
+
+size_t gdn_fwd_smem_bytes(int T, int dk, int L)
+{
+    return sizeof(float) * fwd_smem_floats(T, dk, L, fwd_columns(dk));
+}
+
+cudaError_t gdn_fwd(const GdnFwdArgs &A)
+{
+    return A.in_dt == LLA_F32 ? launch_fwd<float>(A) : launch_fwd<__nv_bfloat16>(A);
+}
+
+cudaError_t gdn_decode_step(const GdnDecodeArgs &A)
+{
+    return A.in_dt == LLA_F32 ? launch_decode<float>(A) : launch_decode<__nv_bfloat16>(A);
+}
+
+}  // namespace lla

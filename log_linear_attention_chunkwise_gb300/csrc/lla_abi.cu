@@ -4,6 +4,7 @@
 
 #include "bwd_simt.cuh"
 #include "decode.cuh"
+#include "gdn.cuh"
 #include "fwd_simt.cuh"
 #include "fwd_tc.cuh"
 #include "lambda_mlp.cuh"
@@ -222,6 +223,46 @@ lla_status lla_bwd(const void *q, const void *k, const void *v, const float *g, 
     A.dq = dq; A.dkey = dk; A.dval = dv; A.dg = dg; A.dlam = dlambda;
     A.workspace = workspace; A.stream = stream;
     return lla::bwd(A) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+}
+
+lla_status lla_gdn_fwd(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                       const float *lambda, float *out, float *state_out, int B, int H, int T, int dk,
+                       int dv, int Ls_out, lla_dtype in_dt, void *stream)
+{
+    if (B < 0 || H < 0 || T < 0) return LLA_ERR_INVALID_ARGUMENT;
+    if (in_dt != LLA_F32 && in_dt != LLA_BF16) return LLA_ERR_INVALID_ARGUMENT;
+    if (!is_dim(dk) || !is_dim(dv) || T > (1 << 16) || B > 65535 || H > 65535)
+        return LLA_ERR_UNSUPPORTED_SHAPE;
+    const int need_slots = T > 0 ? bit_length_u32((uint32_t)T) : 0;
+    if (state_out && (Ls_out < need_slots || Ls_out > 40)) return LLA_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)B * H * T == 0) return LLA_OK;
+    if (!q || !k || !v || !g || !beta || !lambda || !out) return LLA_ERR_INVALID_ARGUMENT;
+    const int L = lla_num_levels(T);
+    if (lla::gdn_fwd_smem_bytes(T, dk, L) > 227 * 1024) return LLA_ERR_UNSUPPORTED_SHAPE;
+    lla::GdnFwdArgs A;
+    A.q = q; A.k = k; A.v = v; A.g = g; A.beta = beta; A.lam = lambda; A.out = out;
+    A.state_out = state_out; A.B = B; A.H = H; A.T = T; A.dk = dk; A.dv = dv; A.L = L;
+    A.Ls_out = state_out ? Ls_out : 0; A.in_dt = in_dt; A.stream = stream;
+    return lla::gdn_fwd(A) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+}
+
+lla_status lla_gdn_decode_step(float *state, const void *q, const void *k, const void *v, const float *g,
+                               const float *beta, const float *lambda, float *out, const int64_t *pos,
+                               int B, int H, int dk, int dv, int Ls, lla_dtype in_dt,
+                               int32_t *device_error, void *stream)
+{
+    if (B < 0 || H < 0) return LLA_ERR_INVALID_ARGUMENT;
+    if (in_dt != LLA_F32 && in_dt != LLA_BF16) return LLA_ERR_INVALID_ARGUMENT;
+    if (!is_dim(dk) || !is_dim(dv) || Ls < 1 || Ls > 40) return LLA_ERR_UNSUPPORTED_SHAPE;
+    if (B > 65535 || H > 65535) return LLA_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)B * H == 0) return LLA_OK;
+    if (!state || !q || !k || !v || !g || !beta || !lambda || !out || !pos)
+        return LLA_ERR_INVALID_ARGUMENT;
+    lla::GdnDecodeArgs A;
+    A.S = state; A.q = q; A.k = k; A.v = v; A.g = g; A.beta = beta; A.lam = lambda; A.out = out;
+    A.pos = pos; A.B = B; A.H = H; A.dk = dk; A.dv = dv; A.Ls = Ls; A.in_dt = in_dt;
+    A.err = device_error; A.stream = stream;
+    return lla::gdn_decode_step(A) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
 }
 
 }  // extern "C"

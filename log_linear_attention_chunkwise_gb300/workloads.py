@@ -123,6 +123,21 @@ def small_fwd_config(B=1, H=2, T=256, dk=32, dv=32, chunk=16, dtype=torch.float3
                      g_zero_head_frac)
 
 
+# Log-Linear Gated DeltaNet: no workload on the pages; the 2K shape of the
+# chunked forward with a per-token beta = sigmoid(N(0,1)).
+GDN_CONFIG = FwdConfig("gdn_bf16_T2048", 4, 8, 2048, 64, 64, 64, torch.bfloat16, 5)
+
+
+def make_gdn_inputs(cfg: FwdConfig, device="cpu") -> dict:
+    """The forward inputs of cfg plus beta [B,H,T] fp32 in (0,1), drawn from a
+    generator of its own (seed + 7919) so q, k, v, g, lambda match make_fwd_inputs."""
+    x = make_fwd_inputs(cfg, device)
+    gen = torch.Generator(device="cpu").manual_seed(cfg.seed + 7919)
+    beta = torch.sigmoid(torch.randn((cfg.B, cfg.H, cfg.T), generator=gen, dtype=torch.float32))
+    x["beta"] = beta.to(device) if device != "cpu" else beta
+    return x
+
+
 def make_decode_positions(cfg: DecodeConfig) -> torch.Tensor:
     """Start positions pos0 [batch] ~ U[pos_lo, pos_hi] (int64)."""
     gen = torch.Generator(device="cpu").manual_seed(cfg.seed)

@@ -114,3 +114,17 @@ def test_bwd_validation(lib):
     assert lib.lla_bwd_workspace_bytes(1, 1, 256, 64, 64, 128, 1) == 0
     # Fenwick nodes [BH][N][dk][dv] plus block states, both fp32
     assert lib.lla_bwd_workspace_bytes(1, 2, 256, 64, 64, 64, 1) >= 2 * (4 + 4) * 64 * 64 * 4
+
+
+def test_gdn_validation(lib):
+    p = ctypes.c_void_p(256)
+
+    def fwd(B=1, T=64, dk=64, Ls=0, st=NULL, dt=1):
+        return lib.lla_gdn_fwd(p, p, p, p, p, p, p, st, B, 1, T, dk, 64, Ls, dt, NULL)
+    assert fwd(dk=48) == 2
+    assert fwd(T=(1 << 16) + 1) == 2
+    assert fwd(st=p, Ls=6) == 2          # 64 tokens need bit_length(64) = 7 slots
+    assert fwd(dt=4) == 1
+    assert fwd(B=0) == 0
+    assert lib.lla_gdn_decode_step(p, p, p, p, p, p, p, p, p, 1, 1, 64, 64, 41, 1, NULL, NULL) == 2
+    assert lib.lla_gdn_decode_step(NULL, p, p, p, p, p, p, p, p, 1, 1, 64, 64, 17, 1, NULL, NULL) == 1
