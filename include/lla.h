@@ -184,6 +184,29 @@ lla_status lla_prefill_state(const void *k, const void *v, const float *g,
                              size_t workspace_bytes, void *stream);
 
 /*
+ * lla_fwd on inputs and outputs in host memory (same layouts and dtypes as
+ * lla_fwd, host pointers; pin them for asynchronous copies).  The pages have
+ * no counterpart: this is the host-facing call of the library.  The
+ * (batch, head) pairs are processed in groups of `group` pairs (0: about an
+ * eighth of them), pipelined over two device slots so that copying group
+ * j+1 in, computing group j and copying group j-1 out overlap (two internal
+ * streams, created on the first call on a device and kept until exit).
+ * Ordered on `stream`: earlier work on it completes before the first copy,
+ * and the stream waits for the last copy out, so synchronising the stream
+ * makes the host output valid.  Results are identical to lla_fwd.
+ * workspace: device memory of at least lla_fwd_host_workspace_bytes(...)
+ * bytes (two slots of group-sized copies plus the forward's workspace),
+ * 256-byte aligned.  Errors as lla_fwd, all before the first copy.
+ */
+size_t lla_fwd_host_workspace_bytes(int B, int H, int T, int dk, int dv, int chunk,
+                                    lla_dtype in_dt, lla_dtype out_dt, int group);
+
+lla_status lla_fwd_host(const void *q, const void *k, const void *v, const float *g,
+                        const float *lambda, void *out, int B, int H, int T, int dk,
+                        int dv, int chunk, lla_dtype in_dt, lla_dtype out_dt, int group,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Log-Linear Gated DeltaNet ("Log-Linear Attention" §3 names it: the Gated
  * DeltaNet state update under the hierarchical Fenwick mask; the pages give
  * no formula).  Reading implemented: every Fenwick bucket keeps its own

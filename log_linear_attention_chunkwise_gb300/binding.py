@@ -39,6 +39,8 @@ SIGNATURES = {
     "lla_bwd_workspace_bytes": (_Z, [_I] * 7),
     "lla_bwd": (_I, [_P] * 11 + [_I] * 7 + [_P, _Z, _P]),
     "lla_gdn_fwd": (_I, [_P] * 8 + [_I] * 6 + [_I, _P]),
+    "lla_fwd_host_workspace_bytes": (_Z, [_I] * 9),
+    "lla_fwd_host": (_I, [_P] * 6 + [_I] * 6 + [_I, _I, _I, _P, _Z, _P]),
     "lla_gdn_decode_step": (_I, [_P] * 9 + [_I] * 5 + [_I, _P, _P]),
 }
 
@@ -287,4 +289,28 @@ def gdn_decode_step(state, q, k, v, g, beta, lam, pos, out=None, device_error=No
                                  _ptr(device_error) if device_error is not None else None,
                                  _stream(stream))
     _check("lla_gdn_decode_step", rc)
+    return out
+
+
+def fwd_host(q, k, v, g, lam, out=None, chunk: int = 64, out_dtype=torch.float32, group: int = 0,
+             workspace=None, stream=None, device=None):
+    """lla_fwd_host: the forward on CPU tensors (pin them for overlap), run on
+    `device`; returns the CPU output (valid once `stream` is synchronised)."""
+    lib = load()
+    for n, t in (("q", q), ("k", k), ("v", v), ("g", g), ("lam", lam)):
+        if t.device.type != "cpu" or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous CPU tensor")
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((B, H, T, dv), dtype=out_dtype, pin_memory=True)
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    need = lib.lla_fwd_host_workspace_bytes(B, H, T, dk, dv, chunk, _dt(q), _dt(out), group)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
+    with torch.cuda.device(device):
+        rc = lib.lla_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(lam), _ptr(out), B, H, T, dk, dv,
+                              chunk, _dt(q), _dt(out), group, _ptr(workspace), workspace.numel(),
+                              _stream(stream))
+    _check("lla_fwd_host", rc)
     return out
