@@ -167,34 +167,76 @@ decode_step_kernel(float *__restrict__ S, float *__restrict__ D, const Tin *__re
     cluster.sync();  // keep every CTA's partials alive until CTA 0 has read them
 }
 
-// tail[bh][s] = sum_{r=s+1}^{T-1} g[bh][r] (accumulated in fp64, stored fp32).
-__global__ void __launch_bounds__(kThreads)
-prefill_tail_kernel(const float *__restrict__ g, float *__restrict__ tail, int T)
+// tail[bh][s] = sum_{r=s+1}^{T-1} g[bh][r], accumulated in fp64 and stored
+// fp32, in three launches over chunks of kTailChunk tokens: chunk sums, the
+// chunks' exclusive suffix sums, then each chunk's suffix scan plus its carry.
+constexpr int kTailChunk = 1024;
+
+__global__ void __launch_bounds__(256)
+prefill_chunk_sum_kernel(const float *__restrict__ g, double *__restrict__ csum, int T, int nchunk)
 {
-    __shared__ double part[kThreads];
+    __shared__ double wsum[8];
+    const long long bh = blockIdx.y;
+    const int c = blockIdx.x;
+    double a = 0.0;
+    for (int i = threadIdx.x; i < kTailChunk; i += 256) {
+        const long long r = (long long)c * kTailChunk + i;
+        if (r < T) a += (double)g[bh * T + r];
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+    if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = a;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double t = 0.0;
+        for (int w = 0; w < 8; w++) t += wsum[w];
+        csum[bh * nchunk + c] = t;
+    }
+}
+
+// carry[c] = sum of the chunk sums after c, per (batch, head); one thread walks them.
+__global__ void __launch_bounds__(32)
+prefill_chunk_carry_kernel(const double *__restrict__ csum, double *__restrict__ carry, int nchunk)
+{
+    if (threadIdx.x != 0) return;
     const long long bh = blockIdx.x;
-    const float *gb = g + bh * (long long)T;
-    float *tb = tail + bh * (long long)T;
-    const int per = (T + kThreads - 1) / kThreads;
-    const int lo = min(T, (int)threadIdx.x * per), hi = min(T, lo + per);
-    double s = 0.0;
-    for (int r = lo; r < hi; r++) s += (double)gb[r];
-    part[threadIdx.x] = s;
+    double run = 0.0;
+    for (int c = nchunk - 1; c >= 0; c--) {
+        carry[bh * nchunk + c] = run;
+        run += csum[bh * nchunk + c];
+    }
+}
+
+__global__ void __launch_bounds__(kTailChunk)
+prefill_tail_kernel(const float *__restrict__ g, const double *__restrict__ carry, float *__restrict__ tail,
+                    int T, int nchunk)
+{
+    __shared__ double wsum[kTailChunk / 32];
+    const long long bh = blockIdx.y;
+    const int c = blockIdx.x;
+    const int i = threadIdx.x, lane = i & 31, w = i >> 5;
+    const long long r = (long long)c * kTailChunk + i;
+    const double x = r < T ? (double)g[bh * T + r] : 0.0;
+    double incl = x;  // sum over this lane and the later lanes of the warp
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const double y = __shfl_down_sync(0xffffffffu, incl, off);
+        if (lane + off < 32) incl += y;
+    }
+    if (lane == 0) wsum[w] = incl;
     __syncthreads();
-    if (threadIdx.x == 0) {  // exclusive suffix sums of the partials
-        double run = 0.0;
-        for (int u = kThreads - 1; u >= 0; u--) {
-            double x = part[u];
-            part[u] = run;
-            run += x;
+    if (w == 0) {
+        const double own = wsum[lane];
+        double s = own;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const double y = __shfl_down_sync(0xffffffffu, s, off);
+            if (lane + off < 32) s += y;
         }
+        wsum[lane] = s - own;  // later warps of the chunk
     }
     __syncthreads();
-    double run = part[threadIdx.x];  // sum of g over [hi, T)
-    for (int r = hi - 1; r >= lo; r--) {
-        tb[r] = (float)run;
-        run += (double)gb[r];
-    }
+    if (r < T) tail[bh * T + r] = (float)(carry[bh * nchunk + c] + wsum[w] + (incl - x));
 }
 
 constexpr int kSeg = 1024;  // tokens per CTA of the bucket kernel
@@ -290,7 +332,19 @@ cudaError_t launch_prefill(const PrefillArgs &A)
     }
     tab.seg_begin[tab.n] = nseg;
     float *tail = (float *)A.workspace;
-    prefill_tail_kernel<<<(unsigned)BH, kThreads, 0, st>>>(A.g, tail, A.T);
+    const int nchunk = (A.T + kTailChunk - 1) / kTailChunk;
+    const size_t tail_bytes = align_up((size_t)BH * A.T * sizeof(float), 256);
+    double *csum = (double *)((char *)A.workspace + tail_bytes);
+    double *carry = csum + align_up((size_t)BH * nchunk, 32);
+    prefill_chunk_sum_kernel<<<dim3(nchunk, (unsigned)BH), 256, 0, st>>>(A.g, csum, A.T, nchunk);
+    prefill_chunk_carry_kernel<<<(unsigned)BH, 32, 0, st>>>(csum, carry, nchunk);
+    prefill_tail_kernel<<<dim3(nchunk, (unsigned)BH), kTailChunk, 0, st>>>(A.g, carry, tail, A.T, nchunk);
+    if (prefill_tc_supported(A)) {
+        int *dev_err = (int *)((char *)(carry + align_up((size_t)BH * nchunk, 32)));
+        err = cudaMemsetAsync(dev_err, 0, sizeof(int), st);
+        if (err != cudaSuccess) return err;
+        return prefill_tc(A, tail, dev_err);
+    }
     prefill_bucket_kernel<Tin><<<dim3(nseg, (unsigned)BH), kThreads, 0, st>>>(
         (const Tin *)A.k, (const Tin *)A.v, tail, A.S, tab, A.T, A.dk, A.dv, A.Ls);
     return cudaPeekAtLastError();
@@ -306,7 +360,11 @@ cudaError_t decode_step(const DecodeArgs &A)
 
 size_t prefill_workspace_bytes(int B, int H, int T)
 {
-    return align_up((size_t)B * H * (size_t)(T > 0 ? T : 1) * sizeof(float), 256);
+    // per-token tails, chunk sums and carries (fp64), the tensor-core path's error word
+    const size_t BH = (size_t)B * H;
+    const size_t nchunk = (size_t)((T > 0 ? T : 1) + kTailChunk - 1) / kTailChunk;
+    return align_up(BH * (size_t)(T > 0 ? T : 1) * sizeof(float), 256) +
+           2 * align_up(BH * nchunk, 32) * sizeof(double) + 256;
 }
 
 cudaError_t prefill_state(const PrefillArgs &A)

@@ -32,5 +32,9 @@ struct PrefillArgs {
 cudaError_t decode_step(const DecodeArgs &A);
 size_t prefill_workspace_bytes(int B, int H, int T);
 cudaError_t prefill_state(const PrefillArgs &A);
+// Tensor-core bucket states (bf16, dk = dv = 128): after the tail kernel and
+// the zeroing of the state; err is a zeroed device word.
+bool prefill_tc_supported(const PrefillArgs &A);
+cudaError_t prefill_tc(const PrefillArgs &A, const float *tail, int *err);
 
 }  // namespace lla

@@ -162,3 +162,24 @@ def test_decode_workload_sampled_pairs():
         _, rel_fro, _ = errors(true_state(S_end[b, h], D_end[b, h])[live],
                                true_state(So[0, 0], Do[0, 0])[live])
         assert rel_fro <= 5e-3, rel_fro
+
+
+@pytest.mark.parametrize("T", [100, 300, 2944, 16384])
+def test_prefill_state_tensor_core_buckets(T):
+    """bf16, dk = dv = 128: the tensor-core bucket path, with buckets shorter
+    than a 128-token tile, buckets that start off a tile boundary and a
+    multi-CTA bucket."""
+    B, H, d = 1, 2, 128
+    Ls = T.bit_length()
+    cfg = W.small_fwd_config(B, H, T, d, d, 1, torch.bfloat16, seed=T + 1)
+    x = W.make_fwd_inputs(cfg)
+    S, D = binding.prefill_state(x["k"].cuda(), x["v"].cuda(), x["g"].cuda(), Ls)
+    torch.cuda.synchronize()
+    pos = np.full(B, T)
+    S_cf, _ = oracle.state_closed_form(x["k"], x["v"], x["g"], pos, Ls)
+    live = live_mask(pos, Ls)[0]
+    Sn = S.cpu().double().numpy()
+    max_abs, rel_fro, _ = errors(Sn[:, :, live], S_cf[:, :, live])
+    assert rel_fro <= 1e-3, rel_fro
+    if (~live).any():
+        assert np.abs(Sn[:, :, ~live]).max() == 0.0
