@@ -5,9 +5,10 @@
 
 One step = one lla_fwd over the T=32768 workload (B=1, H=16, dk=dv=128,
 chunk 64, bf16 q/k/v, fp32 g/lambda/out), inputs resident in HBM.  Rank 0
-prints one JSON line.  With N > 1 (torchrun) every rank runs its own copy of
-the workload on its GPU (independent (batch, head) units: weak scaling, no
-collective on the data path); time is the max over ranks.
+prints one JSON line.  With N > 1 (torchrun) every rank runs its own shard of
+a global batch of N x B sequences on its GPU (independent (batch, head)
+units drawn from a seed of its own: weak scaling, no collective on the data
+path); time is the max over ranks.
 
 --impl reference times the fp64 CPU oracle (its Fenwick recurrent form, the
 O(T log T) one) on a bounded sample of the same workload, on this host's
@@ -158,6 +159,28 @@ def load_traffic(kernel_digest: str):
     return d.get("bytes_per_launch"), d.get("kernel")
 
 
+# ------------------------------------------------------- multi-rank logic
+
+def rank_shard(cfg: W.FwdConfig, rank: int, world: int) -> W.FwdConfig:
+    """The workload of one rank under weak scaling: its own B sequences
+    (global batch indices [rank B, (rank+1) B)), drawn from a seed of its own,
+    so the ranks process disjoint (batch, head) units with no exchange."""
+    if world <= 1:
+        return cfg
+    return cfg.with_(seed=cfg.seed + 1_000_003 * rank, name=f"{cfg.name}/rank{rank}of{world}")
+
+
+def max_over_ranks(x: float, device) -> float:
+    """The job's time is the slowest rank's: all-reduce MAX (no-op for one rank)."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return x
+    if torch.distributed.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 class ClockSampler:
     """nvidia-smi clock/throttle samples while the timed region runs."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
@@ -229,7 +252,7 @@ def run_lla(args, rank, world, local_rank):
     cfg = W.FWD_CONFIGS[WORKLOAD]
     if args.heads or args.seq_len:  # a smaller case of the same recipe (profiling)
         cfg = cfg.with_(H=args.heads or cfg.H, T=args.seq_len or cfg.T)
-    x = W.make_fwd_inputs(cfg)
+    x = W.make_fwd_inputs(rank_shard(cfg, rank, world))
     xd = {n: t.to(dev) for n, t in x.items()}
     out = torch.empty((cfg.B, cfg.H, cfg.T, cfg.dv), dtype=torch.float32, device=dev)
     need = binding.fwd_workspace_bytes(cfg.B, cfg.H, cfg.T, cfg.dk, cfg.dv, cfg.chunk, cfg.dtype)
@@ -264,10 +287,7 @@ def run_lla(args, rank, world, local_rank):
         torch.distributed.barrier()
     total_ms = t_start.elapsed_time(t_end)
     per_launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dev)
     ms_per_step = total_ms / args.steps
     tokens = cfg.tokens * world
     value = tokens / (ms_per_step / 1e3)
@@ -297,10 +317,7 @@ def run_lla(args, rank, world, local_rank):
     b.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = a.elapsed_time(b) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dev)
     del hws
 
     hbm_peak, bf16_peak, bf16_sus, peak_src = load_peaks()
@@ -317,7 +334,7 @@ def run_lla(args, rank, world, local_rank):
         "config": {"workload": f"{WORKLOAD}: B={cfg.B} H={cfg.H} T={cfg.T} dk=dv=128 chunk=64 "
                                "bf16 in, fp32 out",
                    "global_batch": cfg.B * world, "seq_len": cfg.T,
-                   "parallelism": f"replicas over (batch, head) units x{world}",
+                   "parallelism": f"(batch, head) units sharded over {world} rank(s), no collective",
                    "l2": "inputs (436 MB) larger than L2, no flush"},
         "tflops": tflops, "tflops_frac_of_bf16_peak": tflops / bf16_peak,
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
