@@ -110,23 +110,66 @@ bwd_query_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin
     }
     for (int e = threadIdx.x; e < C * L; e += kThreads) Ls[e] = lam[tok0 * L + e];
     __syncthreads();
-    // masked pair weights
-    for (int e = threadIdx.x; e < C * C; e += kThreads) {
-        const int t = e / C, s = e % C;
-        float w1 = 0.f, w2 = 0.f, x = 0.f;
-        if (s <= t) {
-            float qk = 0.f, ov = 0.f;
-            for (int r = 0; r < Dk; r++) qk = fmaf(Qs[t * lk + r], Ks[s * lk + r], qk);
-            for (int c = 0; c < Dv; c++) ov = fmaf(Ds[t * lv + c], Vs[s * lv + c], ov);
-            const float dec = expf(gl[t] - gl[s]);
-            const float m = Ls[t * L + bit_length_u32((uint32_t)(t ^ s))] * dec;
-            w1 = m * ov;
-            w2 = m * qk;
-            x = dec * qk * ov;
+    // Masked pair weights.  Thread (ty, tx) computes the 4 x 4 block of
+    // pairs t = 4 ty + i, s = 4 tx + j of S = Q K^T and dP = dO V^T.
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    {
+        const int t0 = 4 * ty, s0 = 4 * tx;
+        if (t0 < C && s0 < C && s0 <= t0 + 3) {
+            float qk[4][4], ov[4][4];
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+#pragma unroll
+                for (int j = 0; j < 4; j++) qk[i][j] = ov[i][j] = 0.f;
+            for (int r = 0; r < Dk; r++) {
+                float a[4], b[4];
+#pragma unroll
+                for (int i = 0; i < 4; i++) a[i] = Qs[(t0 + i) * lk + r];
+#pragma unroll
+                for (int j = 0; j < 4; j++) b[j] = Ks[(s0 + j) * lk + r];
+#pragma unroll
+                for (int i = 0; i < 4; i++)
+#pragma unroll
+                    for (int j = 0; j < 4; j++) qk[i][j] = fmaf(a[i], b[j], qk[i][j]);
+            }
+            for (int c = 0; c < Dv; c++) {
+                float a[4], b[4];
+#pragma unroll
+                for (int i = 0; i < 4; i++) a[i] = Ds[(t0 + i) * lv + c];
+#pragma unroll
+                for (int j = 0; j < 4; j++) b[j] = Vs[(s0 + j) * lv + c];
+#pragma unroll
+                for (int i = 0; i < 4; i++)
+#pragma unroll
+                    for (int j = 0; j < 4; j++) ov[i][j] = fmaf(a[i], b[j], ov[i][j]);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+#pragma unroll
+                for (int j = 0; j < 4; j++) {
+                    const int t = t0 + i, s2 = s0 + j;
+                    float w1 = 0.f, w2 = 0.f, x = 0.f;
+                    if (s2 <= t) {
+                        const float dec = expf(gl[t] - gl[s2]);
+                        const float m = Ls[t * L + bit_length_u32((uint32_t)(t ^ s2))] * dec;
+                        w1 = m * ov[i][j];
+                        w2 = m * qk[i][j];
+                        x = dec * qk[i][j] * ov[i][j];
+                    }
+                    W1[t * C + s2] = w1;
+                    W2[t * C + s2] = w2;
+                    X[t * C + s2] = x;
+                }
+        } else if (t0 < C && s0 < C) {  // blocks above the diagonal
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+#pragma unroll
+                for (int j = 0; j < 4; j++) {
+                    W1[(t0 + i) * C + s0 + j] = 0.f;
+                    W2[(t0 + i) * C + s0 + j] = 0.f;
+                    X[(t0 + i) * C + s0 + j] = 0.f;
+                }
         }
-        W1[e] = w1;
-        W2[e] = w2;
-        X[e] = x;
     }
     __syncthreads();
     // intra-chunk level gradients: level 0 is s = t, level l >= 1 the keys
@@ -138,33 +181,79 @@ bwd_query_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin
             a = X[t * C + t];
         } else if (l <= cbits && ((t >> (l - 1)) & 1)) {
             const int lo = (t >> l) << l, hi = lo + (1 << (l - 1));
-            for (int s = lo; s < hi; s++) a += X[t * C + s];
+            for (int s2 = lo; s2 < hi; s2++) a += X[t * C + s2];
         }
         dL[e] = a;
     }
-    // intra parts: dq_t = sum_s W1[t][s] k_s ; dk_s = sum_t W1[t][s] q_t ; dv_s = sum_t W2[t][s] dO_t
-    for (int e = threadIdx.x; e < C * Dk; e += kThreads) {
-        const int t = e / Dk, r = e % Dk;
-        float a = 0.f, b = 0.f;
-        for (int s = 0; s < C; s++) {
-            a = fmaf(W1[t * C + s], Ks[s * lk + r], a);   // t as query
-            b = fmaf(W1[s * C + t], Qs[s * lk + r], b);   // t as key
+    // Intra parts: dq_t = sum_s W1[t][s] k_s and, with t as a key,
+    // dk_t = sum_u W1[u][t] q_u; dv_t = sum_u W2[u][t] dO_u.  Thread (ty, tx)
+    // owns rows 4 ty .. 4 ty + 3 and columns tx, tx + 16, ... (conflict-free
+    // row reads of K, Q, dO).
+    {
+        const int t0 = 4 * ty;
+        const int RK = Dk / 16, RV = Dv / 16;
+        if (t0 < C) {
+            float aq[4][8], ak[4][8];
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+#pragma unroll
+                for (int c = 0; c < 8; c++) aq[i][c] = ak[i][c] = 0.f;
+            for (int u = 0; u < C; u++) {
+                float wq[4], wk[4], kv[8], qv[8];
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    wq[i] = W1[(t0 + i) * C + u];  // t0+i as query, u as key
+                    wk[i] = W1[u * C + t0 + i];    // u as query, t0+i as key
+                }
+#pragma unroll
+                for (int c = 0; c < 8; c++) {
+                    kv[c] = c < RK ? Ks[u * lk + tx + 16 * c] : 0.f;
+                    qv[c] = c < RK ? Qs[u * lk + tx + 16 * c] : 0.f;
+                }
+#pragma unroll
+                for (int i = 0; i < 4; i++)
+#pragma unroll
+                    for (int c = 0; c < 8; c++) {
+                        aq[i][c] = fmaf(wq[i], kv[c], aq[i][c]);
+                        ak[i][c] = fmaf(wk[i], qv[c], ak[i][c]);
+                    }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+#pragma unroll
+                for (int c = 0; c < 8; c++)
+                    if (c < RK) {
+                        dq[(tok0 + t0 + i) * Dk + tx + 16 * c] = aq[i][c];
+                        dk[(tok0 + t0 + i) * Dk + tx + 16 * c] = ak[i][c];
+                    }
+            float av[4][8];
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+#pragma unroll
+                for (int c = 0; c < 8; c++) av[i][c] = 0.f;
+            for (int u = 0; u < C; u++) {
+                float wv[4], dvv[8];
+#pragma unroll
+                for (int i = 0; i < 4; i++) wv[i] = W2[u * C + t0 + i];
+#pragma unroll
+                for (int c = 0; c < 8; c++) dvv[c] = c < RV ? Ds[u * lv + tx + 16 * c] : 0.f;
+#pragma unroll
+                for (int i = 0; i < 4; i++)
+#pragma unroll
+                    for (int c = 0; c < 8; c++) av[i][c] = fmaf(wv[i], dvv[c], av[i][c]);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+#pragma unroll
+                for (int c = 0; c < 8; c++)
+                    if (c < RV) dv[(tok0 + t0 + i) * Dv + tx + 16 * c] = av[i][c];
         }
-        dq[(tok0 + t) * Dk + r] = a;
-        dk[(tok0 + t) * Dk + r] = b;
-    }
-    for (int e = threadIdx.x; e < C * Dv; e += kThreads) {
-        const int s = e / Dv, c = e % Dv;
-        float a = 0.f;
-        for (int t = 0; t < C; t++) a = fmaf(W2[t * C + s], Ds[t * lv + c], a);
-        dv[(tok0 + s) * Dv + c] = a;
     }
     __syncthreads();
     // Earlier chunks through the forward's path nodes.  Thread (ty, tx) owns
     // rows t0..t0+3 (t0 = 4 ty) and columns r0..r0+7 (r0 = 8 tx) of
     // U = dO Node_j^T; dq accumulates in registers over the path.
     const double *Pb = P + bh * (long long)(N + 1);
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
     const int t0 = 4 * ty, r0 = 8 * tx;
     const bool own = t0 < C && r0 < Dk;
     float dqa[4][8];
@@ -479,7 +568,8 @@ bwd_key_kernel(const Tin *__restrict__ k, const Tin *__restrict__ v, const float
     }
 }
 
-// dG_u = sum_l lam_u[l] dlam_u[l] - k_u . dk_u, one warp per token, fp64 sums.
+// dG_u = sum_l lam_u[l] dlam_u[l] - k_u . dk_u, one warp per token (fp32 sums;
+// the long running sum over tokens below is fp64).
 template <typename Tin>
 __global__ void __launch_bounds__(kThreads)
 bwd_gate_grad_kernel(const Tin *__restrict__ k, const float *__restrict__ lam,
@@ -490,12 +580,12 @@ bwd_gate_grad_kernel(const Tin *__restrict__ k, const float *__restrict__ lam,
     const int u = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
     if (u >= T) return;
     const long long gi = (long long)blockIdx.y * T + u;
-    double a = 0.0;
-    for (int l = lane; l < L; l += 32) a += (double)lam[gi * L + l] * (double)dlam[gi * L + l];
-    for (int r = lane; r < Dk; r += 32) a -= (double)to_f32(k[gi * Dk + r]) * (double)dk[gi * Dk + r];
+    float a = 0.f;  // at most 4 + 1 terms per lane; the token's dG is summed in fp32
+    for (int l = lane; l < L; l += 32) a = fmaf(lam[gi * L + l], dlam[gi * L + l], a);
+    for (int r = lane; r < Dk; r += 32) a = fmaf(-to_f32(k[gi * Dk + r]), dk[gi * Dk + r], a);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
-    if (lane == 0) dG[gi] = a;
+    if (lane == 0) dG[gi] = (double)a;
 }
 
 // dg_r = sum_{u >= r} dG_u per (batch, head), fp64, one CTA of 1024 threads.
