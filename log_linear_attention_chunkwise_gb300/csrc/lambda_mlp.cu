@@ -8,6 +8,8 @@
 // its row against weights held in shared memory (zero-padded to HP hidden
 // columns so every weight row is read as float4 broadcasts).
 #include "lambda_mlp.cuh"
+#include "sm100.cuh"
+#include "tma_host.cuh"
 
 namespace lla {
 namespace {
@@ -144,10 +146,220 @@ cudaError_t launch_t(const LambdaMlpArgs &A)
     return launch_l<Tin, 64>(A);
 }
 
+
+// ------------------------------------------------ tensor-core path
+// bf16 d with Dd a multiple of 64 (<= 256): the first layer h = d W1 runs on
+// the tensor cores.  d is exact in bf16; W1 is split into three bf16 parts
+// (hi + mid + lo reproduce each fp32 weight to about 24 bits), so
+// h = d W1_hi + d W1_mid + d W1_lo accumulates in fp32 tensor memory with
+// the error of an fp32 dot product.  Per 128-row tile: TMA brings the d rows
+// (two-stage ring), one thread issues the products into one of two
+// tensor-memory accumulators, and four epilogue warps (thread = row) read
+// h, apply the second layer and softplus in fp32 and store the row's L
+// weights.  CTAs are persistent over the tiles.
+constexpr int kTcRows = 128;
+constexpr int kTcEpi = 128;             // epilogue threads (one per row)
+constexpr int kTcThreads = kTcEpi + 32;  // plus one issuing warp
+constexpr uint32_t kTcWait = 1u << 22;
+
+using namespace sm100;
+
+// Sticky record of a bounded wait that gave up (1: load, 2: product); the
+// kernel carries on, so the results of that call are not to be trusted.
+__device__ int lla_lambda_tc_wait_err;
+
+__host__ __device__ constexpr int tc_tmem_cols(int NP) { return NP <= 16 ? 32 : NP <= 32 ? 64 : 128; }
+
+struct TcLayout {  // byte offsets in dynamic shared memory (1024-aligned base)
+    uint32_t w1, w2, d0, d1, bars, total;
+};
+
+__host__ __device__ inline TcLayout tc_layout(int Dd, int NP, int L)
+{
+    TcLayout t;
+    const uint32_t wblk = (uint32_t)NP * 128;              // one 64-wide K block of W1^T part
+    const uint32_t wpart = wblk * (uint32_t)(Dd / 64);     // one part
+    const uint32_t dtile = (uint32_t)kTcRows * 128 * (uint32_t)(Dd / 64);
+    t.w1 = 0;
+    t.d0 = (3 * wpart + 1023) & ~1023u;
+    t.d1 = t.d0 + dtile;
+    t.w2 = t.d1 + dtile;
+    const int Lp = (L + 3) & ~3;
+    t.bars = (t.w2 + (uint32_t)(NP * Lp + Lp) * 4 + 15) & ~15u;
+    t.total = t.bars + 8 * 8 + 16;
+    return t;
+}
+
+template <int NP>
+__global__ void __launch_bounds__(kTcThreads, 1)
+lambda_tc_kernel(const __grid_constant__ CUtensorMap map_d, const float *__restrict__ W1,
+                 const float *__restrict__ W2, const float *__restrict__ bias, float *__restrict__ lam,
+                 long long N, int Dd, int L)
+{
+    int *err = &lla_lambda_tc_wait_err;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const TcLayout lay = tc_layout(Dd, NP, L);
+    const int Hd = 2 * L;
+    const int nb = Dd / 64;
+    const uint32_t wblk = (uint32_t)NP * 128, wpart = wblk * nb;
+    const uint32_t dblk = (uint32_t)kTcRows * 128;
+    uint8_t *dbuf[2] = {sm + lay.d0, sm + lay.d1};
+    const int Lp = (L + 3) & ~3;
+    float *w2 = reinterpret_cast<float *>(sm + lay.w2);  // [NP][Lp] zero-padded, then bias [Lp]
+    float *bs = w2 + NP * Lp;
+    uint64_t *bar_load = reinterpret_cast<uint64_t *>(sm + lay.bars);  // [2]
+    uint64_t *bar_mma = bar_load + 2;                                  // [2]
+    uint64_t *bar_free = bar_load + 4;                                 // [2]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_load + 6);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    // W1^T split into three bf16 parts in the K-major 128-byte-swizzled layout
+    for (int e = tid; e < NP * Dd; e += kTcThreads) {
+        const int n = e / Dd, k = e % Dd;
+        float w = n < Hd ? W1[k * Hd + n] : 0.f;
+        const uint32_t off = (uint32_t)(k / 64) * wblk + sw128_offset(n, (k % 64) / 8) + (k % 8) * 2;
+#pragma unroll
+        for (int part = 0; part < 3; part++) {
+            const __nv_bfloat16 b = __float2bfloat16_rn(w);
+            *reinterpret_cast<__nv_bfloat16 *>(sm + lay.w1 + part * wpart + off) = b;
+            w -= __bfloat162float(b);
+        }
+    }
+    for (int e = tid; e < NP * Lp; e += kTcThreads) {
+        const int j = e / Lp, l = e % Lp;
+        w2[e] = (j < Hd && l < L) ? W2[j * L + l] : 0.f;
+    }
+    for (int e = tid; e < Lp; e += kTcThreads) bs[e] = e < L ? bias[e] : 0.f;
+    if (tid == kTcEpi) {
+        for (int b = 0; b < 2; b++) {
+            mbar_init(&bar_load[b], 1);
+            mbar_init(&bar_mma[b], 1);
+            mbar_init(&bar_free[b], kTcEpi);
+        }
+        fence_mbar_init();
+        tma_prefetch_map(&map_d);
+    }
+    if (warp == 4) {
+        tmem_alloc(tmem_slot, tc_tmem_cols(NP));
+        tmem_relinquish();
+    }
+    fence_proxy_async_smem();  // W1 parts written by threads, read by the tensor cores
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tm = *tmem_slot;
+    const long long ntiles = (N + kTcRows - 1) / kTcRows;
+    const int my = (int)((ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x);  // tiles of this CTA
+    if (warp == 4) {
+        if (tid == kTcEpi) {
+            auto load = [&](int i) {
+                const int st = i & 1;
+                const long long tile = blockIdx.x + (long long)i * gridDim.x;
+                mbar_arrive_expect_tx(&bar_load[st], dblk * nb);
+                for (int b = 0; b < nb; b++)
+                    tma_load_3d(dbuf[st] + b * dblk, &map_d, &bar_load[st], 64 * b, (int)(tile * kTcRows), 0);
+            };
+            for (int i = 0; i < min(2, my); i++) load(i);
+            const uint32_t idesc = idesc_bf16_f32(128, NP, false, false);
+            for (int i = 0; i < my; i++) {
+                const int st = i & 1;
+                if (!mbar_wait(&bar_load[st], (i >> 1) & 1, kTcWait)) atomicCAS(err, 0, 1);
+                if (i >= 2 && !mbar_wait(&bar_free[st], ((i - 2) >> 1) & 1, kTcWait)) atomicCAS(err, 0, 2);
+                tc_fence_after_sync();
+                const uint32_t acc = tm + (uint32_t)(st * NP);
+                int first = 1;
+                for (int part = 0; part < 3; part++)
+                    for (int kk = 0; kk < 4 * nb; kk++) {
+                        const uint32_t offa = (kk >> 2) * dblk + (kk & 3) * 32;
+                        const uint32_t offb = part * wpart + (kk >> 2) * wblk + (kk & 3) * 32;
+                        umma_bf16(acc, desc_sw128(smem_u32(dbuf[st]) + offa, 16, 1024),
+                                  desc_sw128(smem_u32(sm + lay.w1) + offb, 16, 1024), idesc, first ? 0u : 1u);
+                        first = 0;
+                    }
+                umma_commit(&bar_mma[st]);
+                if (i + 2 < my) {  // the stage is free once this tile's products are done
+                    if (!mbar_wait(&bar_mma[st], (i >> 1) & 1, kTcWait)) atomicCAS(err, 0, 2);
+                    load(i + 2);
+                }
+            }
+        }
+    } else {
+        // epilogue: thread = row of the tile = tensor-memory lane
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        for (int i = 0; i < my; i++) {
+            const int st = i & 1;
+            const long long row = (blockIdx.x + (long long)i * gridDim.x) * kTcRows + tid;
+            if (!mbar_wait(&bar_mma[st], (i >> 1) & 1, kTcWait)) atomicCAS(err, 0, 2);
+            tc_fence_after_sync();
+            float h[NP];
+#pragma unroll
+            for (int c = 0; c < NP; c += 16)
+                tmem_ld16(tm + (uint32_t)(st * NP + c) + lane_off, *reinterpret_cast<float(*)[16]>(h + c));
+            tmem_ld_wait();
+            tc_fence_before_sync();
+            mbar_arrive(&bar_free[st]);
+            if (row < N) {
+                float *out = lam + row * L;
+                for (int l0 = 0; l0 < L; l0 += 4) {
+                    float4 z = *reinterpret_cast<const float4 *>(bs + l0);
+#pragma unroll
+                    for (int j = 0; j < NP; j++) {
+                        const float4 w = *reinterpret_cast<const float4 *>(w2 + j * Lp + l0);
+                        z.x = fmaf(h[j], w.x, z.x);
+                        z.y = fmaf(h[j], w.y, z.y);
+                        z.z = fmaf(h[j], w.z, z.z);
+                        z.w = fmaf(h[j], w.w, z.w);
+                    }
+                    const float zz[4] = {z.x, z.y, z.z, z.w};
+#pragma unroll
+                    for (int q = 0; q < 4; q++)
+                        if (l0 + q < L) out[l0 + q] = softplus_f(zz[q]);
+                }
+            }
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 4) tmem_dealloc(tm, tc_tmem_cols(NP));
+}
+
+template <int NP>
+cudaError_t launch_tc_np(const LambdaMlpArgs &A)
+{
+    const long long N = (long long)A.B * A.H * A.T;
+    CUtensorMap md;
+    if (!make_map_bf16_3d(&md, A.d, (uint64_t)A.Dd, (uint64_t)N, 1, 64, kTcRows)) return cudaErrorInvalidValue;
+    const size_t smem = tc_layout(A.Dd, NP, A.L).total + 1024;
+    auto kern = lambda_tc_kernel<NP>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int dev = 0, nsm = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    const long long ntiles = (N + kTcRows - 1) / kTcRows;
+    const int grid = (int)(ntiles < nsm ? ntiles : nsm);
+    kern<<<grid, kTcThreads, smem, (cudaStream_t)A.stream>>>(md, A.W1, A.W2, A.bias, A.lam, N, A.Dd, A.L);
+    return cudaPeekAtLastError();
+}
+
 }  // namespace
+
+bool lambda_tc_supported(const LambdaMlpArgs &A)
+{
+    return A.in_dt == LLA_BF16 && A.Dd % 64 == 0 && A.Dd <= 256 && 2 * A.L <= 64 &&
+           ((uintptr_t)A.d & 15) == 0 && tc_layout(A.Dd, 64, A.L).total + 1024 <= 227 * 1024;
+}
 
 cudaError_t lambda_mlp(const LambdaMlpArgs &A)
 {
+    if (lambda_tc_supported(A)) {
+        const int np = 2 * A.L <= 16 ? 16 : 2 * A.L <= 32 ? 32 : 2 * A.L <= 48 ? 48 : 64;
+        switch (np) {
+        case 16: return launch_tc_np<16>(A);
+        case 32: return launch_tc_np<32>(A);
+        case 48: return launch_tc_np<48>(A);
+        default: return launch_tc_np<64>(A);
+        }
+    }
     return A.in_dt == LLA_F32 ? launch_t<float>(A) : launch_t<__nv_bfloat16>(A);
 }
 

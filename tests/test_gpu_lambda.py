@@ -27,7 +27,14 @@ def weights(Dd, L, seed):
 @pytest.mark.parametrize("B,H,T,Dd,L,dtype", [(2, 3, 100, 64, 7, torch.float32),
                                               (1, 4, 333, 128, 12, torch.bfloat16),
                                               (1, 2, 64, 256, 25, torch.bfloat16),
-                                              (3, 1, 7, 1, 1, torch.float32)])
+                                              (3, 1, 7, 1, 1, torch.float32),
+                                              # tensor-core first layer: K blocks of 64, padded
+                                              # hidden widths, ragged last tile, several tiles per CTA
+                                              (1, 2, 777, 192, 16, torch.bfloat16),
+                                              (2, 1, 300, 64, 8, torch.bfloat16),
+                                              (1, 4, 8192, 128, 14, torch.bfloat16),
+                                              (1, 1, 5000, 128, 24, torch.bfloat16),
+                                              (1, 1, 513, 64, 32, torch.bfloat16)])
 def test_lambda_mlp_matches_oracle(B, H, T, Dd, L, dtype):
     g = torch.Generator().manual_seed(Dd + L)
     d = torch.randn((B, H, T, Dd), generator=g).to(dtype)
