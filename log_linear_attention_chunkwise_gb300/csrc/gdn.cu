@@ -13,9 +13,9 @@
 // Column c of every state only ever mixes with itself: with
 // P = q.S[:,c] and U = k.S[:,c] of the old state, the new column is
 // alpha (S[:,c] - beta U k) and its read-out alpha (P - beta U (q.k)).
-// A CTA owns kW columns of one (batch, head) and a thread (c, rg) owns R
-// rows of its column, so the only cross-thread step is summing P and U over
-// the row groups.
+// A CTA owns KW columns of one (batch, head) and RG lanes of one warp share a
+// column, each holding R of its rows, so the only cross-thread step is summing
+// P and U over those lanes (warp shuffles).
 #include "gdn.cuh"
 
 namespace lla {
@@ -27,20 +27,26 @@ constexpr int kTokBlk = 32;  // tokens staged per refill of the forward
 template <int KW>
 __host__ __device__ constexpr int row_groups() { return kThreads / KW; }
 
+// Column stride of the states in shared memory: 16 banks apart, so the two
+// columns that share a warp never meet in a bank.
+__host__ __device__ inline int col_stride(int dk) { return dk % 32 == 16 ? dk : dk + 16; }
+
 size_t fwd_smem_floats(int T, int dk, int L, int kw)
 {
     const int Lsi = T > 0 ? bit_length_u32((uint32_t)T) : 1;
-    const int rg = kThreads / kw;
-    return (size_t)Lsi * dk * kw          // states
-           + 2 * (size_t)Lsi * 2 * rg * kw  // partial sums, two buffers
+    return (size_t)Lsi * kw * col_stride(dk)  // states, one padded column after another
            + 2 * (size_t)kTokBlk * dk       // q, k
            + (size_t)kTokBlk * kw           // v columns
            + 3 * (size_t)kTokBlk            // alpha, beta, q.k
            + (size_t)kTokBlk * L;           // lambda rows
 }
 
-int fwd_columns(int dk) { return dk >= 128 ? 8 : 16; }
-
+// A CTA owns KW value columns; the RG = 256/KW lanes of one column are
+// consecutive lanes of one warp and hold rows rg, rg + RG, ... of it, so the
+// sums over rows are warp shuffles and no barrier is needed between tokens.
+// A column's states sit contiguously in shared memory (padded to dk + 1) so
+// the lanes of a column read consecutive banks.
+constexpr int kFwdColumns = 16;
 template <typename Tin, int KW>
 __global__ void __launch_bounds__(kThreads)
 gdn_fwd_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
@@ -49,22 +55,28 @@ gdn_fwd_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *
                int Ls_out)
 {
     constexpr int RG = row_groups<KW>();
+    static_assert(RG <= 32 && (32 % RG) == 0, "a column's lanes lie inside one warp");
     extern __shared__ __align__(16) float sm[];
     const int Lsi = T > 0 ? bit_length_u32((uint32_t)T) : 1;
-    float *S = sm;                              // [Lsi][dk][KW]
-    float *red = S + Lsi * dk * KW;             // [2][Lsi][2][RG][KW]
-    float *qs = red + 2 * Lsi * 2 * RG * KW;    // [kTokBlk][dk]
+    const int ldc = col_stride(dk);
+    float *S = sm;                              // [Lsi][KW][ldc]
+    float *qs = S + Lsi * KW * ldc;             // [kTokBlk][dk]
     float *ks = qs + kTokBlk * dk;              // [kTokBlk][dk]
     float *vs = ks + kTokBlk * dk;              // [kTokBlk][KW]
     float *as = vs + kTokBlk * KW;              // [kTokBlk] alpha
     float *bs = as + kTokBlk;                   // [kTokBlk] beta
     float *qk = bs + kTokBlk;                   // [kTokBlk] q.k
     float *ls = qk + kTokBlk;                   // [kTokBlk][L]
-    const int c = threadIdx.x % KW, rg = threadIdx.x / KW;
+    const int c = threadIdx.x / RG, rg = threadIdx.x % RG;
     const int R = dk / RG;  // rows per thread (1..8)
     const int col = blockIdx.x * KW + c;
     const long long bh = (long long)blockIdx.z * H + blockIdx.y;
     const long long tok0 = bh * (long long)T;
+    auto colsum = [](float x) {
+#pragma unroll
+        for (int off = RG / 2; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off, RG);
+        return x;
+    };
     for (int t0 = 0; t0 < T; t0 += kTokBlk) {
         const int nt = min(kTokBlk, T - t0);
         __syncthreads();  // the previous block is consumed
@@ -88,22 +100,7 @@ gdn_fwd_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *
         __syncthreads();
         for (int tt = 0; tt < nt; tt++) {
             const uint32_t t = (uint32_t)(t0 + tt);
-            float *rd = red + (tt & 1) * (Lsi * 2 * RG * KW);
             const float *qt = qs + tt * dk, *kt = ks + tt * dk;
-            // partial P, U of every live slot over this thread's rows
-            for (int i = 0; i < Lsi; i++) {
-                if (!((t >> i) & 1u)) continue;
-                float p = 0.f, u = 0.f;
-                for (int j = 0; j < R; j++) {
-                    const int r = rg * R + j;
-                    const float s = S[(i * dk + r) * KW + c];
-                    p = fmaf(qt[r], s, p);
-                    u = fmaf(kt[r], s, u);
-                }
-                rd[((i * 2 + 0) * RG + rg) * KW + c] = p;
-                rd[((i * 2 + 1) * RG + rg) * KW + c] = u;
-            }
-            __syncthreads();
             const int m = ctz_u32(t + 1u);
             const float al = as[tt], be = bs[tt], qkt = qk[tt], vc = vs[tt * KW + c];
             const float *lt = ls + tt * L;
@@ -113,38 +110,45 @@ gdn_fwd_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *
             for (int j = 0; j < 8; j++) macc[j] = 0.f;
             for (int i = 0; i < Lsi; i++) {
                 if (!((t >> i) & 1u)) continue;
-                float P = 0.f, U = 0.f;
-                for (int x = 0; x < RG; x++) {
-                    P += rd[((i * 2 + 0) * RG + x) * KW + c];
-                    U += rd[((i * 2 + 1) * RG + x) * KW + c];
+                float *Sc = S + (i * KW + c) * ldc;
+                float x[8], p = 0.f, u = 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; j++) {
+                    if (j >= R) break;
+                    const int r = rg + RG * j;
+                    x[j] = Sc[r];
+                    p = fmaf(qt[r], x[j], p);
+                    u = fmaf(kt[r], x[j], u);
                 }
+                const float P = colsum(p), U = colsum(u);
                 const float bu = be * U;
 #pragma unroll
                 for (int j = 0; j < 8; j++) {
                     if (j >= R) break;
-                    const int r = rg * R + j;
-                    float *sp = S + (i * dk + r) * KW + c;
-                    const float sn = al * (*sp - bu * kt[r]);
-                    *sp = sn;
+                    const int r = rg + RG * j;
+                    const float sn = al * (x[j] - bu * kt[r]);
+                    Sc[r] = sn;
                     if (i < m) macc[j] += sn;
                 }
                 o = fmaf(lt[i + 1], al * (P - bu * qkt), o);
             }
+            float *Sm = S + (m * KW + c) * ldc;
 #pragma unroll
             for (int j = 0; j < 8; j++) {
                 if (j >= R) break;
-                const int r = rg * R + j;
-                S[(m * dk + r) * KW + c] = fmaf(be * kt[r], vc, macc[j]);
+                const int r = rg + RG * j;
+                Sm[r] = fmaf(be * kt[r], vc, macc[j]);
             }
             if (rg == 0) out[(tok0 + t) * dv + col] = o;
         }
     }
     if (state_out) {  // the state after [0, T): slot i live iff bit i of T
+        __syncthreads();
         for (int i = 0; i < Ls_out; i++) {
             const bool live = i < Lsi && (((uint32_t)T >> i) & 1u);
             for (int j = 0; j < R; j++) {
-                const int r = rg * R + j;
-                state_out[((bh * Ls_out + i) * dk + r) * dv + col] = live ? S[(i * dk + r) * KW + c] : 0.f;
+                const int r = rg + RG * j;
+                state_out[((bh * Ls_out + i) * dk + r) * dv + col] = live ? S[(i * KW + c) * ldc + r] : 0.f;
             }
         }
     }
@@ -269,7 +273,7 @@ cudaError_t launch_fwd_w(const GdnFwdArgs &A)
 template <typename Tin>
 cudaError_t launch_fwd(const GdnFwdArgs &A)
 {
-    return fwd_columns(A.dk) == 8 ? launch_fwd_w<Tin, 8>(A) : launch_fwd_w<Tin, 16>(A);
+    return launch_fwd_w<Tin, kFwdColumns>(A);
 }
 
 template <typename Tin, int DK, int DV>
@@ -309,7 +313,7 @@ cudaError_t launch_decode(const GdnDecodeArgs &A)
 
 size_t gdn_fwd_smem_bytes(int T, int dk, int L)
 {
-    return sizeof(float) * fwd_smem_floats(T, dk, L, fwd_columns(dk));
+    return sizeof(float) * fwd_smem_floats(T, dk, L, kFwdColumns);
 }
 
 cudaError_t gdn_fwd(const GdnFwdArgs &A)
