@@ -46,7 +46,7 @@ size_t fwd_smem_floats(int T, int dk, int L, int kw)
 // sums over rows are warp shuffles and no barrier is needed between tokens.
 // A column's states sit contiguously in shared memory (padded to dk + 1) so
 // the lanes of a column read consecutive banks.
-constexpr int kFwdColumns = 16;
+inline int fwd_columns(int dk) { return dk >= 32 ? 8 : 16; }  // 8: a whole warp per column
 template <typename Tin, int KW>
 __global__ void __launch_bounds__(kThreads)
 gdn_fwd_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
@@ -273,7 +273,7 @@ cudaError_t launch_fwd_w(const GdnFwdArgs &A)
 template <typename Tin>
 cudaError_t launch_fwd(const GdnFwdArgs &A)
 {
-    return launch_fwd_w<Tin, kFwdColumns>(A);
+    return fwd_columns(A.dk) == 8 ? launch_fwd_w<Tin, 8>(A) : launch_fwd_w<Tin, 16>(A);
 }
 
 template <typename Tin, int DK, int DV>
@@ -313,7 +313,7 @@ cudaError_t launch_decode(const GdnDecodeArgs &A)
 
 size_t gdn_fwd_smem_bytes(int T, int dk, int L)
 {
-    return sizeof(float) * fwd_smem_floats(T, dk, L, kFwdColumns);
+    return sizeof(float) * fwd_smem_floats(T, dk, L, fwd_columns(dk));
 }
 
 cudaError_t gdn_fwd(const GdnFwdArgs &A)
