@@ -70,13 +70,14 @@ def _load():
         lib.oracle_level.argtypes = [I, I]
         lib.oracle_lambda_mlp.argtypes = [P] * 5 + [I] * 3
         lib.oracle_backward.argtypes = [P] * 11 + [I] * 6
+        lib.oracle_backward_rows.argtypes = [P] * 7 + [I, P, I] + [P] * 4 + [I] * 4
         lib.oracle_gdn_naive.argtypes = [P] * 7 + [I] * 6
         lib.oracle_gdn_fenwick.argtypes = [P] * 7 + [I] * 6
         lib.oracle_gdn_base.argtypes = [P] * 6 + [I] * 5
         lib.oracle_gdn_decode_step.argtypes = [P] * 9 + [I] * 5
         for name in ("oracle_naive", "oracle_naive_rows", "oracle_fenwick", "oracle_decode_step",
                      "oracle_state_closed_form", "oracle_ssd", "oracle_level", "oracle_lambda_mlp",
-                     "oracle_num_threads", "oracle_backward", "oracle_gdn_naive",
+                     "oracle_num_threads", "oracle_backward", "oracle_backward_rows", "oracle_gdn_naive",
                      "oracle_gdn_fenwick", "oracle_gdn_base", "oracle_gdn_decode_step"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -264,3 +265,22 @@ def gdn_decode_step(S, q, k, v, g, beta, lam, pos) -> np.ndarray:
                                           _ptr(lam), _ptr(out), _ptr(pos), B, H, dk, dv, Ls),
            "oracle_gdn_decode_step")
     return out
+
+
+def backward_rows(q, k, v, g, lam, dout, query_rows, key_rows):
+    """The backward of one (batch, head) slice at selected rows:
+    (dq [nq,dk], dlam [nq,L]) at query_rows, (dk [ns,dk], dv [ns,dv]) at key_rows."""
+    q, k, v, g, lam, dout = map(_f64, (q, k, v, g, lam, dout))
+    T, Dk = q.shape
+    Dv = v.shape[-1]
+    L = lam.shape[-1]
+    tq = np.ascontiguousarray(np.asarray(query_rows), dtype=np.int64)
+    ts = np.ascontiguousarray(np.asarray(key_rows), dtype=np.int64)
+    dq = np.zeros((len(tq), Dk))
+    dl = np.zeros((len(tq), L))
+    dk = np.zeros((len(ts), Dk))
+    dv = np.zeros((len(ts), Dv))
+    _check(_load().oracle_backward_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(lam), _ptr(dout),
+                                        _ptr(tq), len(tq), _ptr(ts), len(ts), _ptr(dq), _ptr(dl),
+                                        _ptr(dk), _ptr(dv), T, Dk, Dv, L), "oracle_backward_rows")
+    return dq, dl, dk, dv

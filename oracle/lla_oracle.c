@@ -827,3 +827,68 @@ int oracle_gdn_decode_step(double *S, const double *q, const double *k,
     }
     return 0;
 }
+
+/*
+ * The backward of oracle_backward at selected rows only, for one (batch,
+ * head) slice q,k [T,dk], v,dout [T,dv], g [T], lam [T,L]:
+ *   query rows tq[nq]: dq [nq,dk], dlam [nq,L]  (sums over s <= t)
+ *   key rows   ts[ns]: dk [ns,dk], dv [ns,dv]   (sums over t >= s)
+ * O((nq + ns) T (dk+dv)); lets a test check single rows of long sequences.
+ */
+int oracle_backward_rows(const double *q, const double *k, const double *v,
+                         const double *g, const double *lam, const double *dout,
+                         const int64_t *tq, int64_t nq, const int64_t *ts, int64_t ns,
+                         double *dq, double *dlam, double *dk, double *dv,
+                         int64_t T, int64_t Dk, int64_t Dv, int64_t L)
+{
+    if (T < 0 || Dk <= 0 || Dv <= 0 || L <= 0 || nq < 0 || ns < 0)
+        return -1;
+    if (T > 0 && bit_length((uint64_t)(T - 1)) > L - 1)
+        return -2;
+    for (int64_t i = 0; i < nq; i++)
+        if (tq[i] < 0 || tq[i] >= T)
+            return -5;
+    for (int64_t i = 0; i < ns; i++)
+        if (ts[i] < 0 || ts[i] >= T)
+            return -5;
+    double *G = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+    if (!G)
+        return -3;
+    cumsum(g, T, G);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < nq; i++) {
+        const int64_t t = tq[i];
+        double *dqi = dq + i * Dk, *dli = dlam + i * L;
+        memset(dqi, 0, sizeof(double) * (size_t)Dk);
+        memset(dli, 0, sizeof(double) * (size_t)L);
+        for (int64_t s = 0; s <= t; s++) {
+            int lev = oracle_level(t, s);
+            double E = exp(G[t] - G[s]);
+            double qk = dot(q + t * Dk, k + s * Dk, Dk);
+            double ov = dot(dout + t * Dv, v + s * Dv, Dv);
+            double A = lam[t * L + lev] * E;
+            for (int64_t r = 0; r < Dk; r++)
+                dqi[r] += A * ov * k[s * Dk + r];
+            dli[lev] += E * qk * ov;
+        }
+    }
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < ns; i++) {
+        const int64_t s = ts[i];
+        double *dki = dk + i * Dk, *dvi = dv + i * Dv;
+        memset(dki, 0, sizeof(double) * (size_t)Dk);
+        memset(dvi, 0, sizeof(double) * (size_t)Dv);
+        for (int64_t t = s; t < T; t++) {
+            int lev = oracle_level(t, s);
+            double A = lam[t * L + lev] * exp(G[t] - G[s]);
+            double qk = dot(q + t * Dk, k + s * Dk, Dk);
+            double ov = dot(dout + t * Dv, v + s * Dv, Dv);
+            for (int64_t r = 0; r < Dk; r++)
+                dki[r] += A * ov * q[t * Dk + r];
+            for (int64_t c = 0; c < Dv; c++)
+                dvi[c] += A * qk * dout[t * Dv + c];
+        }
+    }
+    free(G);
+    return 0;
+}

@@ -103,3 +103,34 @@ def test_bwd_rejects_chunk_128():
     x = {n: t.cuda() for n, t in inputs(cfg).items()}
     with pytest.raises(RuntimeError):
         binding.bwd(x["q"], x["k"], x["v"], x["g"], x["lam"], x["dout"], chunk=128)
+
+
+def test_bwd_at_the_32k_workload_sampled_rows_and_identities():
+    """The T=32768 workload (B=1, H=16, d=128, bf16, chunk 64) as bench.py times
+    it.  Sampled rows of every gradient but dg against the oracle's row-wise
+    backward (fp32 bound over the sampled rows); then properties that hold at
+    any size, per head: the loss sum_t dO_t . o_t is linear in each of q, k, v
+    and lambda, so <q,dq> = <k,dk> = <v,dv> = <lambda,dlambda> (Euler), and it
+    sees the gates only through differences of G, so dg_0 = 0."""
+    cfg = W.FWD_CONFIGS["bf16_T32768_slowdecay"]
+    x = inputs(cfg)
+    got = gpu_bwd(x, cfg.chunk)
+    dq, dk, dv, dg, dl = (t.cpu().double() for t in got)
+    T = cfg.T
+    rows = [0, 1, 127, 128, 4095, 20000, T - 1]
+    sel = {n: t[0] for n, t in x.items()}
+    for h in (0, 11):
+        rq, rl, rk, rv = oracle.backward_rows(sel["q"][h], sel["k"][h], sel["v"][h], sel["g"][h],
+                                              sel["lam"][h], sel["dout"][h], rows, rows)
+        for name, a, r in (("dq", dq[0, h, rows], rq), ("dlam", dl[0, h, rows], rl),
+                           ("dk", dk[0, h, rows], rk), ("dv", dv[0, h, rows], rv)):
+            max_abs, rel_fro, ref_max = errors(a, r)
+            assert rel_fro <= REL_FRO and max_abs <= REL_MAX * max(ref_max, 1e-30), (
+                f"head {h} {name}: max_abs={max_abs:.3e} rel_fro={rel_fro:.3e}")
+    q, k, v, lam = (x[n].double() for n in ("q", "k", "v", "lam"))
+    for h in range(cfg.H):
+        sums = [float((q[0, h] * dq[0, h]).sum()), float((k[0, h] * dk[0, h]).sum()),
+                float((v[0, h] * dv[0, h]).sum()), float((lam[0, h] * dl[0, h]).sum())]
+        scale = max(abs(s) for s in sums)
+        assert max(sums) - min(sums) <= 1e-4 * scale, (h, sums)
+        assert abs(float(dg[0, h, 0])) <= 1e-4 * scale + 1e-6 * float(dg[0, h].abs().max()), (h, float(dg[0, h, 0]))

@@ -361,3 +361,14 @@ def test_backward_euler_identities_and_gate_shift():
         assert np.allclose(np.sum(x * dx, axis=(2, 3)), loss, rtol=1e-11, atol=1e-11)
     # the loss sees G only through differences: the total gate gradient vanishes
     assert np.max(np.abs(dg[:, :, 0])) < 1e-11 * max(1.0, np.max(np.abs(dg)))
+
+
+def test_backward_rows_equal_the_full_backward():
+    q, k, v, g, lam = rand_inputs(1, 1, 45, 4, 3, seed=47)
+    dout = np.random.default_rng(48).standard_normal(v.shape)
+    dq, dk, dv, dg, dlam = oracle.backward(q, k, v, g, lam, dout)
+    rows = [0, 7, 31, 44]
+    rq, rl, rk, rv = oracle.backward_rows(q[0, 0], k[0, 0], v[0, 0], g[0, 0], lam[0, 0], dout[0, 0],
+                                          rows, rows)
+    for got, full in ((rq, dq), (rl, dlam), (rk, dk), (rv, dv)):
+        assert relerr(got, full[0, 0, rows]) < 1e-13
