@@ -183,3 +183,21 @@ def test_prefill_state_tensor_core_buckets(T):
     assert rel_fro <= 1e-3, rel_fro
     if (~live).any():
         assert np.abs(Sn[:, :, ~live]).max() == 0.0
+
+
+def test_prefill_state_at_the_32k_workload():
+    """k, v, g of the T=32768 workload (B=1, H=16, d=128, bf16) as bench.py times
+    it: the state of two heads against the closed form."""
+    cfg = W.FWD_CONFIGS["bf16_T32768_slowdecay"]
+    x = W.make_fwd_inputs(cfg)
+    Ls = cfg.T.bit_length()
+    S, D = binding.prefill_state(x["k"].cuda(), x["v"].cuda(), x["g"].cuda(), Ls)
+    torch.cuda.synchronize()
+    assert float(D.abs().max()) == 0.0
+    for h in (3, 15):
+        sl = {n: t[:, h:h + 1] for n, t in x.items()}
+        S_cf, _ = oracle.state_closed_form(sl["k"], sl["v"], sl["g"], np.array([cfg.T]), Ls)
+        live = live_mask(np.array([cfg.T]), Ls)[0]
+        Sn = S[:, h:h + 1].cpu().double().numpy()
+        max_abs, rel_fro, _ = errors(Sn[:, :, live], S_cf[:, :, live])
+        assert rel_fro <= 1e-3, (h, rel_fro)

@@ -81,3 +81,17 @@ def test_lambda_mlp_full_size_sampled_rows():
     for h in (0, 7, 15):
         ref = oracle.lambda_mlp(d[0, h, rows].cpu(), W1, W2, b)
         np.testing.assert_allclose(lam[0, h, rows].double().cpu().numpy(), ref, rtol=2e-5, atol=2e-6)
+
+
+def test_lambda_mlp_at_the_32k_workload_sampled_rows():
+    """d = k of the T=32768 workload (B=1, H=16, Dd=128, bf16, L=16) as bench.py
+    times it; 2048 sampled rows against the oracle."""
+    cfg = W.FWD_CONFIGS["bf16_T32768_slowdecay"]
+    k = W.make_fwd_inputs(cfg)["k"]
+    W1, W2, b = weights(128, cfg.L, seed=9)
+    lam = binding.lambda_mlp(k.cuda(), W1.cuda(), W2.cuda(), b.cuda())
+    torch.cuda.synchronize()
+    rows = torch.randint(0, cfg.H * cfg.T, (2048,), generator=torch.Generator().manual_seed(3))
+    flat = lam.reshape(-1, cfg.L).cpu()[rows]
+    ref = oracle.lambda_mlp(k.reshape(-1, 128)[rows], W1, W2, b)
+    np.testing.assert_allclose(flat.double().numpy(), ref, rtol=2e-5, atol=2e-6)
