@@ -1,0 +1,233 @@
+// Key side of the backward on the tensor cores (bf16 k, v; dk = dv = 128;
+// chunk 64).
+//
+// For chunk i and level m with bit m of i clear, the later chunks of block
+// b = (i >> m) + 1 contribute  dk_s += f_s R_{m,b} v_s,  dv_s += f_s R_{m,b}^T k_s
+// with f_s = exp(G_ref - G_s), ref = the last token before the block (see the
+// CUDA-core backward).  A CTA takes the pair of chunks (2p, 2p+1) as one
+// 128-row tile.  For m >= 1 both chunks see the same block, and
+// f_s = c_m rho_s with c_m = exp(P_{b 2^m} - P_{2p+2}) (block start to pair
+// end) and rho_s = exp(P_{2p+2} - G_s) (token to pair end), both <= 1, so
+// c_m R_m is staged per level and every level accumulates into one pair of
+// tensor-memory accumulators:  dK = rho . sum_m V (c_m R_m)^T,
+// dV = rho . sum_m K (c_m R_m).  Level 0 concerns chunk 2p alone (its block
+// is chunk 2p+1) and goes to a second pair of accumulators, weighted by f_s
+// for the first 64 rows and 0 for the others.  R is fp32: each staged
+// c_m R_m is split into a bf16 high part and a bf16 remainder, and both are
+// multiplied (k and v are exact in bf16), so the products keep about 16
+// bits.  The staged R serves as the K-major B operand of the dk product and
+// the MN-major B operand of the dv product.  Results are added to dk, dv.
+#include "bwd_simt.cuh"
+#include "sm100.cuh"
+#include "tma_host.cuh"
+
+namespace lla {
+namespace {
+
+using namespace sm100;
+
+constexpr int kKT = 128;                      // tile rows (two chunks of 64)
+constexpr int kKD = 128;                      // dk = dv
+constexpr uint32_t kKBuf = kKT * kKD * 2;     // bf16 128 x 128: 32 KB
+constexpr uint32_t kKHalf = kKBuf / 2;
+constexpr int kKThreads = 128;
+constexpr uint32_t kKWait = 1u << 22;
+
+struct __align__(1024) KeySmem {
+    uint8_t k[kKBuf];
+    uint8_t v[kKBuf];
+    uint8_t rhi[2][kKBuf];
+    uint8_t rlo[2][kKBuf];
+    uint64_t bar_load, bar_mma[2], bar_done;
+    uint32_t tmem;
+};
+
+__device__ __forceinline__ void key_err(int *err, int code) { atomicCAS(err, 0, code); }
+
+// 8 MMAs over K = 128, A K-major; B K-major (kmaj) or MN-major.
+__device__ __forceinline__ void mma8(uint32_t d, const uint8_t *a, const uint8_t *b, uint32_t idesc, bool b_kmaj,
+                                     bool acc)
+{
+#pragma unroll
+    for (int kk = 0; kk < 8; kk++) {
+        const uint32_t offa = (kk >> 2) * kKHalf + (kk & 3) * 32;
+        const uint64_t bd = b_kmaj ? desc_sw128(smem_u32(b) + offa, 16, 1024)
+                                   : desc_sw128(smem_u32(b) + kk * 2048, kKHalf, 1024);
+        umma_bf16(d, desc_sw128(smem_u32(a) + offa, 16, 1024), bd, idesc, (acc || kk > 0) ? 1u : 0u);
+    }
+}
+
+__global__ void __launch_bounds__(kKThreads, 1)
+bwd_key_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                  const float *__restrict__ gamma, const double *__restrict__ P, const float *__restrict__ R,
+                  float *__restrict__ dk, float *__restrict__ dv, int T, int N, int nlev, int nblocks,
+                  int *__restrict__ err)
+{
+    extern __shared__ uint8_t smem_raw[];
+    KeySmem &s = *reinterpret_cast<KeySmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int p = threadIdx.x;  // tile row
+    const int pair = blockIdx.x;
+    const int bh = blockIdx.y;
+    const int c0 = 2 * pair;                 // first chunk of the pair
+    const int pend = min(N, c0 + 2);         // chunk index after the pair
+    const double *Pb = P + (long long)bh * (N + 1);
+    // levels of the pair: m >= 1 shared, m = 0 only for chunk c0
+    bool lev0 = (c0 + 1) < N;
+    int levs[24];
+    int nl = 0;
+    for (int m = 1; m < nlev; m++)
+        if (((c0 >> m) & 1) == 0 && (((long long)(c0 >> m) + 1) << m) < N) levs[nl++] = m;
+    if (!lev0 && nl == 0) return;
+    if (p == 0) {
+        mbar_init(&s.bar_load, 1);
+        mbar_init(&s.bar_mma[0], 1);
+        mbar_init(&s.bar_mma[1], 1);
+        mbar_init(&s.bar_done, 1);
+        fence_mbar_init();
+        tma_prefetch_map(&map_k);
+        tma_prefetch_map(&map_v);
+        mbar_arrive_expect_tx(&s.bar_load, 2 * kKBuf);
+        for (int h = 0; h < 2; h++) {
+            tma_load_3d(s.k + h * kKHalf, &map_k, &s.bar_load, h * 64, pair * kKT, bh);
+            tma_load_3d(s.v + h * kKHalf, &map_v, &s.bar_load, h * 64, pair * kKT, bh);
+        }
+    }
+    if (p < 32) {
+        tmem_alloc(&s.tmem, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tm = s.tmem;
+    const uint32_t acc_k = tm, acc_v = tm + 128, acc_k0 = tm + 256, acc_v0 = tm + 384;
+    const uint32_t id_kk = idesc_bf16_f32(128, 128, false, false);
+    const uint32_t id_kmn = idesc_bf16_f32(128, 128, false, true);
+    const double Pend = Pb[pend];
+    // stage c * R (fp32 [128][128]) as bf16 high and remainder parts, 128-byte swizzled
+    auto stage = [&](int buf, const float *Rm, float c) {
+        // thread p converts row p: 128 values, 16 chunks of 8
+        const float4 *src = reinterpret_cast<const float4 *>(Rm + (long long)p * kKD);
+#pragma unroll 4
+        for (int ch = 0; ch < 16; ch++) {
+            const float4 a = src[2 * ch], b = src[2 * ch + 1];
+            const float x[8] = {a.x * c, a.y * c, a.z * c, a.w * c, b.x * c, b.y * c, b.z * c, b.w * c};
+            uint4 hi, lo;
+            __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&hi);
+            __nv_bfloat162 *l2 = reinterpret_cast<__nv_bfloat162 *>(&lo);
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                const __nv_bfloat162 hv = __floats2bfloat162_rn(x[2 * u], x[2 * u + 1]);
+                const float2 hf = __bfloat1622float2(hv);
+                h2[u] = hv;
+                l2[u] = __floats2bfloat162_rn(x[2 * u] - hf.x, x[2 * u + 1] - hf.y);
+            }
+            const uint32_t off = (ch >> 3) * kKHalf + sw128_offset(p, ch & 7);
+            *reinterpret_cast<uint4 *>(s.rhi[buf] + off) = hi;
+            *reinterpret_cast<uint4 *>(s.rlo[buf] + off) = lo;
+        }
+    };
+    // the level sequence: level 0 first (if any), then the shared levels
+    const int total = (lev0 ? 1 : 0) + nl;
+    int off_tab[24];
+    {
+        int off = 0;
+        for (int m = 0; m < nlev; m++) {
+            off_tab[m] = off;
+            off += (N + (1 << m) - 1) >> m;
+        }
+    }
+    bool acc_started = false;
+    if (!mbar_wait(&s.bar_load, 0, kKWait)) key_err(err, 1);
+    for (int n = 0; n < total; n++) {
+        const int buf = n & 1;
+        const bool is0 = lev0 && n == 0;
+        const int m = is0 ? 0 : levs[n - (lev0 ? 1 : 0)];
+        const int b = (c0 >> m) + 1;
+        const float *Rm = R + (((long long)bh * nblocks) + off_tab[m] + b) * kKD * kKD;
+        const float c = is0 ? 1.f : (float)exp(Pb[b << m] - Pend);
+        if (n >= 2 && !mbar_wait(&s.bar_mma[buf], ((n - 2) >> 1) & 1, kKWait)) key_err(err, 2);
+        stage(buf, Rm, c);
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (p == 0) {
+            tc_fence_after_sync();
+            const uint32_t dk_acc = is0 ? acc_k0 : acc_k, dv_acc = is0 ? acc_v0 : acc_v;
+            const bool acc = is0 ? false : acc_started;
+            mma8(dk_acc, s.v, s.rhi[buf], id_kk, true, acc);
+            mma8(dk_acc, s.v, s.rlo[buf], id_kk, true, true);
+            mma8(dv_acc, s.k, s.rhi[buf], id_kmn, false, acc);
+            mma8(dv_acc, s.k, s.rlo[buf], id_kmn, false, true);
+            umma_commit(&s.bar_mma[buf]);
+        }
+        if (!is0) acc_started = true;
+    }
+    if (p == 0) umma_commit(&s.bar_done);
+    if (!mbar_wait(&s.bar_done, 0, kKWait)) key_err(err, 2);
+    tc_fence_after_sync();
+    // drain: row p; weights rho (shared levels) and f0 (level 0, first chunk)
+    const long long row = (long long)pair * kKT + p;
+    const int chunk = c0 + (p >> 6);
+    const float gam = (row < T) ? gamma[(long long)bh * T + row] : 0.f;
+    const double Gs = Pb[min(chunk, N)] + (double)gam;
+    const float rho = (row < T) ? (float)exp(Pend - Gs) : 0.f;
+    const float f0 = (lev0 && p < 64) ? (float)exp(Pb[c0 + 1] - Gs) : 0.f;
+    const uint32_t lane_off = (uint32_t)((p >> 5) * 32) << 16;
+    const bool have_shared = nl > 0;
+    for (int which = 0; which < 2; which++) {
+        const uint32_t a_sh = which == 0 ? acc_k : acc_v, a_0 = which == 0 ? acc_k0 : acc_v0;
+        float *dst = (which == 0 ? dk : dv) + ((long long)bh * T + row) * kKD;
+#pragma unroll 1
+        for (int cb = 0; cb < kKD; cb += 16) {
+            float x[16], y[16];
+            tmem_ld16(a_sh + lane_off + cb, x);
+            tmem_ld16(a_0 + lane_off + cb, y);
+            tmem_ld_wait();
+            if (row < T) {
+                float4 *d4 = reinterpret_cast<float4 *>(dst + cb);
+#pragma unroll
+                for (int u = 0; u < 4; u++) {
+                    // an accumulator no level wrote holds no data: select, do not scale
+                    float a[4];
+#pragma unroll
+                    for (int e = 0; e < 4; e++)
+                        a[e] = (have_shared ? rho * x[4 * u + e] : 0.f) + (lev0 ? f0 * y[4 * u + e] : 0.f);
+                    float4 o = d4[u];
+                    o.x += a[0];
+                    o.y += a[1];
+                    o.z += a[2];
+                    o.w += a[3];
+                    d4[u] = o;
+                }
+            }
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (p < 32) tmem_dealloc(tm, 512);
+}
+
+}  // namespace
+
+bool bwd_key_tc_supported(const BwdArgs &A)
+{
+    return A.in_dt == LLA_BF16 && A.dk == kKD && A.dv == kKD && A.C == 64 && ((uintptr_t)A.k & 15) == 0 &&
+           ((uintptr_t)A.v & 15) == 0 && ((uintptr_t)A.dkey & 15) == 0 && ((uintptr_t)A.dval & 15) == 0;
+}
+
+cudaError_t bwd_key_tc(const BwdArgs &A, const float *gamma, const double *P, const float *R, int nlev,
+                       int nblocks, int *err)
+{
+    const int BH = A.B * A.H, N = A.T / A.C;
+    CUtensorMap mk, mv;
+    if (!make_map_bf16_3d(&mk, A.k, kKD, A.T, BH, 64, kKT) || !make_map_bf16_3d(&mv, A.v, kKD, A.T, BH, 64, kKT))
+        return cudaErrorInvalidValue;
+    const size_t smem = sizeof(KeySmem) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(bwd_key_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    bwd_key_tc_kernel<<<dim3((N + 1) / 2, BH), kKThreads, smem, (cudaStream_t)A.stream>>>(
+        mk, mv, gamma, P, R, A.dkey, A.dval, A.T, N, nlev, nblocks, err);
+    return cudaPeekAtLastError();
+}
+
+}  // namespace lla

@@ -666,7 +666,7 @@ SimtFwdArgs node_args(const BwdArgs &A)
 // gamma [BH][T] fp32, R [BH][total_blocks][Dk][Dv] fp32,
 // pieces [BH][total_items][Dk][Dv] fp32, dG [BH][T] fp64.
 struct BwdLayout {
-    size_t gamma, R, parts, dG, end;
+    size_t gamma, R, parts, dG, err, end;
 };
 
 BwdLayout layout(const BwdArgs &A)
@@ -679,7 +679,8 @@ BwdLayout layout(const BwdArgs &A)
     l.R = l.gamma + align_up(BH * A.T * 4, 256);
     l.parts = l.R + align_up(BH * (size_t)total_blocks(N) * st, 256);
     l.dG = l.parts + align_up(BH * (size_t)total_items(N, piece_chunks(A.C)) * st, 256);
-    l.end = l.dG + align_up(BH * A.T * 8, 256);
+    l.err = l.dG + align_up(BH * A.T * 8, 256);
+    l.end = l.err + 256;
     return l;
 }
 
@@ -715,12 +716,20 @@ cudaError_t launch_bwd(const BwdArgs &A)
             Pc);
         bwd_block_reduce_kernel<<<dim3(nblocks, BH), kThreads, 0, st>>>(parts, R, A.dk, A.dv, N, nlev, Pc,
                                                                         nitems, nblocks);
-        const size_t smk = sizeof(float) * key_smem_floats(A.C, A.dk, A.dv);
-        e = cudaFuncSetAttribute(bwd_key_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smk);
-        if (e != cudaSuccess) return e;
-        bwd_key_kernel<Tin><<<dim3(N, BH), kThreads, smk, st>>>(
-            (const Tin *)A.k, (const Tin *)A.v, gamma, P, R, A.dkey, A.dval, A.T, A.dk, A.dv, A.C, N, nlev,
-            nblocks);
+        if (bwd_key_tc_supported(A)) {
+            int *err = (int *)(ws + lay.err);
+            e = cudaMemsetAsync(err, 0, sizeof(int), st);
+            if (e != cudaSuccess) return e;
+            e = bwd_key_tc(A, gamma, P, R, nlev, nblocks, err);
+            if (e != cudaSuccess) return e;
+        } else {
+            const size_t smk = sizeof(float) * key_smem_floats(A.C, A.dk, A.dv);
+            e = cudaFuncSetAttribute(bwd_key_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smk);
+            if (e != cudaSuccess) return e;
+            bwd_key_kernel<Tin><<<dim3(N, BH), kThreads, smk, st>>>(
+                (const Tin *)A.k, (const Tin *)A.v, gamma, P, R, A.dkey, A.dval, A.T, A.dk, A.dv, A.C, N,
+                nlev, nblocks);
+        }
     }
     bwd_gate_grad_kernel<Tin><<<dim3((A.T + kThreads / 32 - 1) / (kThreads / 32), BH), kThreads, 0, st>>>(
         (const Tin *)A.k, A.lam, A.dlam, A.dkey, dG, A.T, A.dk, A.L);

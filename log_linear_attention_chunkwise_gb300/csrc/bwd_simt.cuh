@@ -20,5 +20,9 @@ struct BwdArgs {
 size_t bwd_workspace_bytes(const BwdArgs &A);
 size_t bwd_smem_bytes(const BwdArgs &A);
 cudaError_t bwd(const BwdArgs &A);
+// Key side on the tensor cores (bf16, dk = dv = 128, chunk 64): adds to dk, dv.
+bool bwd_key_tc_supported(const BwdArgs &A);
+cudaError_t bwd_key_tc(const BwdArgs &A, const float *gamma, const double *P, const float *R, int nlev,
+                       int nblocks, int *err);
 
 }  // namespace lla

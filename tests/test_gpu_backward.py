@@ -54,6 +54,8 @@ def check(cfg):
     (2, 1, 224, 32, 64, 32, torch.float32, 0.0),     # 7 chunks: ragged Fenwick tree
     (1, 1, 64, 64, 32, 64, torch.bfloat16, 0.0),     # one chunk: no inter-chunk term
     (1, 2, 512, 128, 128, 64, torch.bfloat16, 0.0),
+    (2, 1, 448, 128, 128, 64, torch.bfloat16, -2.0),   # 7 chunks: a lone last chunk (tensor-core key side)
+    (1, 1, 64, 128, 128, 64, torch.bfloat16, 0.0),     # one chunk: no key-side level at all
     (1, 3, 384, 64, 64, 32, torch.bfloat16, -2.0),   # 12 chunks, slow decay
     (1, 1, 1008, 16, 128, 16, torch.float32, -2.0),  # 63 chunks, six block levels
 ])
