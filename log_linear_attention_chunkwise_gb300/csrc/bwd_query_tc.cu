@@ -1,0 +1,229 @@
+// Query side of the backward on the tensor cores (bf16 q, k; dk = dv = 128;
+// chunk 64): the read-out of the forward's chunk-level Fenwick nodes.
+//
+// For a row t of chunk i and each node j on the Fenwick path of i (level
+// l = c + 1 + ctz(j)), with U_t = Node_j dO_t and w_t = exp(G_t - P_j) <= 1:
+//     dq_t += lambda_t[l] w_t U_t,   dlambda_t[l] += w_t q_t . U_t.
+// A CTA takes the pair of chunks (2p, 2p+1) as one 128-row tile: the path
+// of 2p+1 is node 2p+1 followed by the path of 2p, so every node of the pair
+// is one product over all 128 rows, with weight 0 on the rows it does not
+// concern.  U = dO Node^T runs on the tensor cores with dO and the node (both
+// fp32) split into bf16 high and remainder parts (three products: hi.hi,
+// hi.lo, lo.hi); a two-deep ring of node stages and of accumulators lets the
+// staging of node n+1 and the product of node n overlap the drain of node
+// n-1.  Eight warps drain: thread = (row, half of the 128 columns); the two
+// halves' q.U partial sums meet in shared memory.  Results are added to dq
+// and dlambda.
+#include "bwd_simt.cuh"
+#include "sm100.cuh"
+
+namespace lla {
+namespace {
+
+using namespace sm100;
+
+constexpr int kQT = 128;
+constexpr int kQD = 128;
+constexpr uint32_t kQBuf = kQT * kQD * 2;  // bf16 128 x 128: 32 KB
+constexpr uint32_t kQHalf = kQBuf / 2;
+constexpr int kQThreads = 256;
+constexpr uint32_t kQWait = 1u << 22;
+constexpr int kQMaxPath = 20;
+
+struct __align__(1024) QuerySmem {
+    uint8_t ohi[kQBuf], olo[kQBuf];     // dO tile, high and remainder parts
+    uint8_t nhi[2][kQBuf], nlo[2][kQBuf];  // node stages
+    float part[2][kQT];                 // q.U partial sums of the second half
+    uint64_t bar_mma[2];
+    uint32_t tmem;
+};
+
+__device__ __forceinline__ void q_err(int *err, int code) { atomicCAS(err, 0, code); }
+
+__device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+
+// Rows [r0, r0 + nrows) of an fp32 [.][128] matrix (row stride 128) as bf16
+// high and remainder parts in the 128-byte-swizzled K-major layout; each of
+// the calling threads converts half a row (64 values).
+__device__ __forceinline__ void stage_split(uint8_t *hi, uint8_t *lo, const float *src, int row, int half, float scale,
+                                            bool valid)
+{
+    const float4 *s4 = reinterpret_cast<const float4 *>(src + (long long)row * kQD + half * 64);
+#pragma unroll 2
+    for (int ch = 0; ch < 8; ch++) {
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+        if (valid) {
+            a = s4[2 * ch];
+            b = s4[2 * ch + 1];
+        }
+        const float x[8] = {a.x * scale, a.y * scale, a.z * scale, a.w * scale,
+                            b.x * scale, b.y * scale, b.z * scale, b.w * scale};
+        uint4 h, l;
+        __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&h);
+        __nv_bfloat162 *l2 = reinterpret_cast<__nv_bfloat162 *>(&l);
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+            const __nv_bfloat162 hv = __floats2bfloat162_rn(x[2 * u], x[2 * u + 1]);
+            const float2 hf = __bfloat1622float2(hv);
+            h2[u] = hv;
+            l2[u] = __floats2bfloat162_rn(x[2 * u] - hf.x, x[2 * u + 1] - hf.y);
+        }
+        const uint32_t off = half * kQHalf + sw128_offset(row, ch);
+        *reinterpret_cast<uint4 *>(hi + off) = h;
+        *reinterpret_cast<uint4 *>(lo + off) = l;
+    }
+}
+
+// 8 MMAs over K = 128, A and B K-major.
+__device__ __forceinline__ void mma8k(uint32_t d, const uint8_t *a, const uint8_t *b, uint32_t idesc, bool acc)
+{
+#pragma unroll
+    for (int kk = 0; kk < 8; kk++) {
+        const uint32_t off = (kk >> 2) * kQHalf + (kk & 3) * 32;
+        umma_bf16(d, desc_sw128(smem_u32(a) + off, 16, 1024), desc_sw128(smem_u32(b) + off, 16, 1024), idesc,
+                  (acc || kk > 0) ? 1u : 0u);
+    }
+}
+
+template <typename Tin>
+__global__ void __launch_bounds__(kQThreads, 1)
+bwd_query_tc_kernel(const Tin *__restrict__ q, const float *__restrict__ dout, const float *__restrict__ gamma,
+                    const float *__restrict__ lam, const double *__restrict__ P, const float *__restrict__ nodes,
+                    float *__restrict__ dq, float *__restrict__ dlam, int T, int N, int L, int cbits,
+                    int *__restrict__ err)
+{
+    extern __shared__ uint8_t smem_raw[];
+    QuerySmem &s = *reinterpret_cast<QuerySmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x;
+    const int row = tid & (kQT - 1), half = tid >> 7;
+    const int pair = blockIdx.x, bh = blockIdx.y;
+    const int c0 = 2 * pair;
+    // the pair's nodes: 2p+1 (second chunk only, if it exists), then the path of 2p
+    int js[kQMaxPath];
+    int np = 0;
+    if (c0 + 1 < N) js[np++] = c0 + 1;
+    for (int j = c0; j > 0; j -= (j & -j)) js[np++] = j;
+    if (np == 0) return;
+    const double *Pb = P + (long long)bh * (N + 1);
+    const long long trow = (long long)pair * kQT + row;
+    const bool row_ok = trow < T;
+    const int chunk = c0 + (row >> 6);
+    const long long tok = (long long)bh * T + trow;
+    if (tid == 0) {
+        mbar_init(&s.bar_mma[0], 1);
+        mbar_init(&s.bar_mma[1], 1);
+        fence_mbar_init();
+    }
+    if (tid < 32) {
+        tmem_alloc(&s.tmem, 256);
+        tmem_relinquish();
+    }
+    // dO tile and the first node
+    stage_split(s.ohi, s.olo, dout + (long long)bh * T * kQD + (long long)pair * kQT * kQD, row, half, 1.f, row_ok);
+    const float *node_base = nodes + (long long)bh * N * kQD * kQD;
+    stage_split(s.nhi[0], s.nlo[0], node_base + (long long)js[0] * kQD * kQD, row, half, 1.f, true);
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tm = s.tmem;
+    const uint32_t idesc = idesc_bf16_f32(128, 128, false, false);
+    // this thread's q half row, and G_t
+    float qv[64];
+    {
+        const Tin *qr = q + tok * kQD + half * 64;
+#pragma unroll
+        for (int c = 0; c < 64; c++) qv[c] = row_ok ? to_f32(qr[c]) : 0.f;
+    }
+    const double Gt = Pb[min(chunk, N)] + (double)(row_ok ? gamma[tok] : 0.f);
+    const float *lam_row = lam + tok * L;
+    float dqa[64];
+#pragma unroll
+    for (int c = 0; c < 64; c++) dqa[c] = 0.f;
+    const uint32_t lane_off = (uint32_t)((tid >> 5) & 3) * 32 << 16;
+    auto issue = [&](int n) {
+        const int b = n & 1;
+        tc_fence_after_sync();
+        mma8k(tm + b * 128, s.ohi, s.nhi[b], idesc, false);
+        mma8k(tm + b * 128, s.ohi, s.nlo[b], idesc, true);
+        mma8k(tm + b * 128, s.olo, s.nhi[b], idesc, true);
+        umma_commit(&s.bar_mma[b]);
+    };
+    auto drain = [&](int n) {
+        const int b = n & 1;
+        const int j = js[n];
+        const int lev = cbits + 1 + (__ffs(j) - 1);
+        // node 2p+1 concerns the second chunk only; the path of 2p both
+        const bool mine = row_ok && (j <= chunk);
+        const float w = mine ? (float)exp(Gt - Pb[j]) : 0.f;
+        const float lw = mine ? lam_row[lev] * w : 0.f;
+        if (!mbar_wait(&s.bar_mma[b], (n >> 1) & 1, kQWait)) q_err(err, 2);
+        tc_fence_after_sync();
+        float dot = 0.f;
+#pragma unroll
+        for (int c0c = 0; c0c < 64; c0c += 16) {
+            float u[16];
+            tmem_ld16(tm + b * 128 + lane_off + half * 64 + c0c, u);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; e++) {
+                dqa[c0c + e] = fmaf(lw, u[e], dqa[c0c + e]);
+                dot = fmaf(qv[c0c + e], u[e], dot);
+            }
+        }
+        tc_fence_before_sync();
+        if (half == 1) s.part[b][row] = dot;
+        named_sync(1, kQThreads);
+        if (half == 0 && mine) dlam[tok * L + lev] += w * (dot + s.part[b][row]);
+    };
+    if (tid == 0) issue(0);
+    for (int n = 0; n < np; n++) {
+        if (n + 1 < np) {
+            // stage node n+1 into the other buffer once node n-1's product is done
+            const int b1 = (n + 1) & 1;
+            if (n >= 1 && !mbar_wait(&s.bar_mma[b1], ((n - 1) >> 1) & 1, kQWait)) q_err(err, 2);
+            stage_split(s.nhi[b1], s.nlo[b1], node_base + (long long)js[n + 1] * kQD * kQD, row, half, 1.f, true);
+            fence_proxy_async_smem();
+        }
+        drain(n);  // contains a barrier of all threads: node n+1 is staged and U_{n-1} drained
+        if (n + 1 < np && tid == 0) issue(n + 1);
+    }
+    if (row_ok) {
+        float4 *d4 = reinterpret_cast<float4 *>(dq + tok * kQD + half * 64);
+#pragma unroll
+        for (int u = 0; u < 16; u++) {
+            float4 o = d4[u];
+            o.x += dqa[4 * u];
+            o.y += dqa[4 * u + 1];
+            o.z += dqa[4 * u + 2];
+            o.w += dqa[4 * u + 3];
+            d4[u] = o;
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (tid < 32) tmem_dealloc(tm, 256);
+}
+
+}  // namespace
+
+bool bwd_query_tc_supported(const BwdArgs &A)
+{
+    return A.in_dt == LLA_BF16 && A.dk == kQD && A.dv == kQD && A.C == 64 && ((uintptr_t)A.dout & 15) == 0 &&
+           ((uintptr_t)A.dq & 15) == 0;
+}
+
+cudaError_t bwd_query_tc(const BwdArgs &A, const float *gamma, const double *P, const float *nodes, int *err)
+{
+    const int BH = A.B * A.H, N = A.T / A.C;
+    const int cbits = 6;
+    const size_t smem = sizeof(QuerySmem) + 1024;
+    auto kern = bwd_query_tc_kernel<__nv_bfloat16>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3((N + 1) / 2, BH), kQThreads, smem, (cudaStream_t)A.stream>>>(
+        (const __nv_bfloat16 *)A.q, A.dout, gamma, A.lam, P, nodes, A.dq, A.dlam, A.T, N, A.L, cbits, err);
+    return cudaPeekAtLastError();
+}
+
+}  // namespace lla

@@ -79,7 +79,7 @@ bwd_query_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin
                  const float *__restrict__ lam, const double *__restrict__ P,
                  const float *__restrict__ nodes, float *__restrict__ dq, float *__restrict__ dk,
                  float *__restrict__ dv, float *__restrict__ dlam, int T, int Dk, int Dv, int C,
-                 int cbits, int N, int L)
+                 int cbits, int N, int L, int do_path)
 {
     extern __shared__ float sm[];
     const int lk = Dk + 1, lv = Dv + 1;
@@ -261,7 +261,7 @@ bwd_query_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin
     for (int a = 0; a < 4; a++)
 #pragma unroll
         for (int c = 0; c < 8; c++) dqa[a][c] = 0.f;
-    for (int j = i; j > 0; j -= (j & -j)) {
+    for (int j = do_path ? i : 0; j > 0; j -= (j & -j)) {
         const int lev = cbits + 1 + ctz_u32((uint32_t)j);
         const float dP = (float)(Pb[i] - Pb[j]);
         const float *Nd = nodes + (bh * N + j) * (long long)Dk * Dv;
@@ -322,7 +322,7 @@ bwd_query_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin
         }
     }
     __syncthreads();
-    if (own && i > 0) {
+    if (own && i > 0 && do_path) {
 #pragma unroll
         for (int a = 0; a < 4; a++) {
             float *dst = dq + (tok0 + t0 + a) * Dk + r0;
@@ -707,7 +707,14 @@ cudaError_t launch_bwd(const BwdArgs &A)
     if (e != cudaSuccess) return e;
     bwd_query_kernel<Tin><<<dim3(N, BH), kThreads, smq, st>>>(
         (const Tin *)A.q, (const Tin *)A.k, (const Tin *)A.v, A.dout, gamma, A.lam, P, nodes, A.dq,
-        A.dkey, A.dval, A.dlam, A.T, A.dk, A.dv, A.C, cbits, N, A.L);
+        A.dkey, A.dval, A.dlam, A.T, A.dk, A.dv, A.C, cbits, N, A.L, bwd_query_tc_supported(A) ? 0 : 1);
+    if (bwd_query_tc_supported(A) && N > 1) {
+        int *err = (int *)(ws + lay.err);
+        e = cudaMemsetAsync(err, 0, sizeof(int), st);
+        if (e != cudaSuccess) return e;
+        e = bwd_query_tc(A, gamma, P, nodes, err);
+        if (e != cudaSuccess) return e;
+    }
     const int nlev = block_levels(N), nblocks = total_blocks(N);
     const int Pc = piece_chunks(A.C), nitems = total_items(N, Pc);
     if (nitems > 0) {

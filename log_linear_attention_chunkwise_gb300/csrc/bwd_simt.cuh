@@ -24,5 +24,8 @@ cudaError_t bwd(const BwdArgs &A);
 bool bwd_key_tc_supported(const BwdArgs &A);
 cudaError_t bwd_key_tc(const BwdArgs &A, const float *gamma, const double *P, const float *R, int nlev,
                        int nblocks, int *err);
+// Query side (node read-out) on the tensor cores, same conditions: adds to dq, dlambda.
+bool bwd_query_tc_supported(const BwdArgs &A);
+cudaError_t bwd_query_tc(const BwdArgs &A, const float *gamma, const double *P, const float *nodes, int *err);
 
 }  // namespace lla
