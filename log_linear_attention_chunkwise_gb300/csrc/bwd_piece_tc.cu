@@ -1,0 +1,187 @@
+// Block-state pieces of the backward on the tensor cores (bf16 q; dk = dv =
+// 128; chunk 64):  piece = sum_t w_t q_t dO_t^T over a run of tokens of one
+// (level m, block b), w_t = lambda_t[c+1+m] exp(G_t - G_ref) (see the
+// CUDA-core backward).  A CTA takes one piece (up to 16 chunks) in 128-token
+// tiles: TMA brings the q tile; the threads scale their dO row by w (0 for
+// tokens outside the piece) and split it into bf16 high and remainder parts;
+// one thread issues piece += Q^T (w dO)_hi + Q^T (w dO)_lo (M = dk, N = dv,
+// K = 128 tokens) into a tensor-memory accumulator.  The finished piece is
+// written to its own slot; the reduction that follows sums a block's pieces
+// in order.
+#include "bwd_simt.cuh"
+#include "sm100.cuh"
+#include "tma_host.cuh"
+
+namespace lla {
+namespace {
+
+using namespace sm100;
+
+constexpr int kPT = 128;
+constexpr int kPDm = 128;
+constexpr uint32_t kPB = kPT * kPDm * 2;  // 32 KB
+constexpr uint32_t kPH = kPB / 2;
+constexpr int kPThreads = 128;
+constexpr uint32_t kPWait = 1u << 22;
+
+struct __align__(1024) PieceSmem {
+    uint8_t q[2][kPB];
+    uint8_t bhi[2][kPB], blo[2][kPB];
+    uint64_t bar_load[2], bar_mma[2], bar_done;
+    uint32_t tmem;
+};
+
+__global__ void __launch_bounds__(kPThreads, 1)
+bwd_piece_tc_kernel(const __grid_constant__ CUtensorMap map_q, const float *__restrict__ dout,
+                    const float *__restrict__ gamma, const float *__restrict__ lam, const double *__restrict__ P,
+                    float *__restrict__ part, int T, int N, int L, int cbits, int nlev, int Pc,
+                    int *__restrict__ err)
+{
+    extern __shared__ uint8_t smem_raw[];
+    PieceSmem &s = *reinterpret_cast<PieceSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int p = threadIdx.x;
+    const int bh = blockIdx.y;
+    // locate (m, b, piece) as the CUDA-core kernel does
+    int idx = blockIdx.x, m = -1, b = 0, pc = 0;
+    for (int mm = 0; mm < nlev; mm++) {
+        const int nb = (N + (1 << mm) - 1) >> mm;
+        const int pp = ((1 << mm) + Pc - 1) / Pc;
+        const int cnt = (nb / 2) * pp;
+        if (idx < cnt) {
+            m = mm;
+            b = 2 * (idx / pp) + 1;
+            pc = idx % pp;
+            break;
+        }
+        idx -= cnt;
+    }
+    if (m < 0) return;
+    const int c0 = b << m;
+    const int blk_end = min(N, (b + 1) << m);
+    const int p0 = c0 + pc * Pc, p1 = min(blk_end, p0 + Pc);
+    if (p0 >= p1) return;
+    const int lev = cbits + 1 + m;
+    const double *Pb = P + (long long)bh * (N + 1);
+    const double Pref = Pb[c0];
+    const long long t_lo = (long long)p0 * 64, t_hi = (long long)p1 * 64;
+    const int ntiles = (int)((t_hi - t_lo + kPT - 1) / kPT);
+    if (p == 0) {
+        for (int i = 0; i < 2; i++) {
+            mbar_init(&s.bar_load[i], 1);
+            mbar_init(&s.bar_mma[i], 1);
+        }
+        mbar_init(&s.bar_done, 1);
+        fence_mbar_init();
+        tma_prefetch_map(&map_q);
+    }
+    if (p < 32) {
+        tmem_alloc(&s.tmem, 128);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tm = s.tmem;
+    auto load_q = [&](int n) {
+        const int st = n & 1;
+        mbar_arrive_expect_tx(&s.bar_load[st], kPB);
+        tma_load_3d(s.q[st], &map_q, &s.bar_load[st], 0, (int)(t_lo + (long long)n * kPT), bh);
+        tma_load_3d(s.q[st] + kPH, &map_q, &s.bar_load[st], 64, (int)(t_lo + (long long)n * kPT), bh);
+    };
+    if (p == 0)
+        for (int n = 0; n < min(2, ntiles); n++) load_q(n);
+    const uint32_t idesc = idesc_bf16_f32(128, 128, true, true);
+    for (int n = 0; n < ntiles; n++) {
+        const int st = n & 1;
+        if (p == 0 && n >= 1 && n + 1 < ntiles) {  // q stage of tile n-1 is free once its product is done
+            if (!mbar_wait(&s.bar_mma[(n - 1) & 1], ((n - 1) >> 1) & 1, kPWait)) atomicCAS(err, 0, 2);
+            load_q(n + 1);
+        }
+        if (n >= 2 && !mbar_wait(&s.bar_mma[st], ((n - 2) >> 1) & 1, kPWait)) atomicCAS(err, 0, 2);
+        // token row p of the tile: w dO, split
+        const long long t = t_lo + (long long)n * kPT + p;
+        float w = 0.f;
+        if (t < t_hi) {
+            const long long gi = (long long)bh * T + t;
+            w = lam[gi * L + lev] * __expf((float)(Pb[t >> 6] - Pref) + gamma[gi]);
+        }
+        const float4 *src = reinterpret_cast<const float4 *>(dout + ((long long)bh * T + (t < t_hi ? t : t_lo)) * kPDm);
+#pragma unroll 4
+        for (int ch = 0; ch < 16; ch++) {
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f), c = a;
+            if (t < t_hi) {
+                a = src[2 * ch];
+                c = src[2 * ch + 1];
+            }
+            const float x[8] = {a.x * w, a.y * w, a.z * w, a.w * w, c.x * w, c.y * w, c.z * w, c.w * w};
+            uint4 h, l;
+            __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&h);
+            __nv_bfloat162 *l2 = reinterpret_cast<__nv_bfloat162 *>(&l);
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                const __nv_bfloat162 hv = __floats2bfloat162_rn(x[2 * u], x[2 * u + 1]);
+                const float2 hf = __bfloat1622float2(hv);
+                h2[u] = hv;
+                l2[u] = __floats2bfloat162_rn(x[2 * u] - hf.x, x[2 * u + 1] - hf.y);
+            }
+            const uint32_t off = (ch >> 3) * kPH + sw128_offset(p, ch & 7);
+            *reinterpret_cast<uint4 *>(s.bhi[st] + off) = h;
+            *reinterpret_cast<uint4 *>(s.blo[st] + off) = l;
+        }
+        fence_proxy_async_smem();
+        if (!mbar_wait(&s.bar_load[st], (n >> 1) & 1, kPWait)) atomicCAS(err, 0, 1);
+        __syncthreads();
+        if (p == 0) {
+            tc_fence_after_sync();
+#pragma unroll
+            for (int kk = 0; kk < 8; kk++) {
+                const uint64_t a = desc_sw128(smem_u32(s.q[st]) + kk * 2048, kPH, 1024);
+                umma_bf16(tm, a, desc_sw128(smem_u32(s.bhi[st]) + kk * 2048, kPH, 1024), idesc,
+                          (n > 0 || kk > 0) ? 1u : 0u);
+                umma_bf16(tm, a, desc_sw128(smem_u32(s.blo[st]) + kk * 2048, kPH, 1024), idesc, 1u);
+            }
+            umma_commit(&s.bar_mma[st]);
+        }
+    }
+    if (p == 0) umma_commit(&s.bar_done);
+    if (!mbar_wait(&s.bar_done, 0, kPWait)) atomicCAS(err, 0, 2);
+    tc_fence_after_sync();
+    float4 *dst = reinterpret_cast<float4 *>(part + (((long long)bh * gridDim.x) + blockIdx.x) * kPDm * kPDm +
+                                             (long long)p * kPDm);
+    const uint32_t lane_off = (uint32_t)((p >> 5) * 32) << 16;
+#pragma unroll 1
+    for (int cb = 0; cb < kPDm; cb += 16) {
+        float x[16];
+        tmem_ld16(tm + lane_off + cb, x);
+        tmem_ld_wait();
+#pragma unroll
+        for (int u = 0; u < 4; u++) dst[cb / 4 + u] = make_float4(x[4 * u], x[4 * u + 1], x[4 * u + 2], x[4 * u + 3]);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (p < 32) tmem_dealloc(tm, 128);
+}
+
+}  // namespace
+
+bool bwd_piece_tc_supported(const BwdArgs &A)
+{
+    return A.in_dt == LLA_BF16 && A.dk == kPDm && A.dv == kPDm && A.C == 64 && ((uintptr_t)A.q & 15) == 0 &&
+           ((uintptr_t)A.dout & 15) == 0;
+}
+
+cudaError_t bwd_piece_tc(const BwdArgs &A, const float *gamma, const double *P, float *part, int nlev, int Pc,
+                         int nitems, int *err)
+{
+    const int BH = A.B * A.H, N = A.T / A.C;
+    CUtensorMap mq;
+    if (!make_map_bf16_3d(&mq, A.q, kPDm, A.T, BH, 64, kPT)) return cudaErrorInvalidValue;
+    const size_t smem = sizeof(PieceSmem) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(bwd_piece_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    bwd_piece_tc_kernel<<<dim3(nitems, BH), kPThreads, smem, (cudaStream_t)A.stream>>>(
+        mq, A.dout, gamma, A.lam, P, part, A.T, N, A.L, 6, nlev, Pc, err);
+    return cudaPeekAtLastError();
+}
+
+}  // namespace lla

@@ -718,9 +718,14 @@ cudaError_t launch_bwd(const BwdArgs &A)
     const int nlev = block_levels(N), nblocks = total_blocks(N);
     const int Pc = piece_chunks(A.C), nitems = total_items(N, Pc);
     if (nitems > 0) {
-        bwd_block_piece_kernel<Tin><<<dim3(nitems, BH), kThreads, 0, st>>>(
-            (const Tin *)A.q, A.dout, gamma, A.lam, P, parts, A.T, A.dk, A.dv, A.C, cbits, N, A.L, nlev,
-            Pc);
+        if (bwd_piece_tc_supported(A)) {
+            e = bwd_piece_tc(A, gamma, P, parts, nlev, Pc, nitems, (int *)(ws + lay.err));
+            if (e != cudaSuccess) return e;
+        } else {
+            bwd_block_piece_kernel<Tin><<<dim3(nitems, BH), kThreads, 0, st>>>(
+                (const Tin *)A.q, A.dout, gamma, A.lam, P, parts, A.T, A.dk, A.dv, A.C, cbits, N, A.L, nlev,
+                Pc);
+        }
         bwd_block_reduce_kernel<<<dim3(nblocks, BH), kThreads, 0, st>>>(parts, R, A.dk, A.dv, N, nlev, Pc,
                                                                         nitems, nblocks);
         if (bwd_key_tc_supported(A)) {
