@@ -445,7 +445,7 @@ def run_next_rows(dev, x, cfg, args):
                      "note": "live slots read and written once, the new slot written"}}
     del gS
 
-    # backward (CUDA cores, fp32 arithmetic)
+    # backward (fp32-accurate; tensor cores for the bf16 d=128 workload)
     if not args.skip_bwd:
         gen = torch.Generator().manual_seed(cfg.seed + 1000)
         dout = torch.randn((cfg.B, cfg.H, cfg.T, cfg.dv), generator=gen).to(dev)
@@ -459,14 +459,20 @@ def run_next_rows(dev, x, cfg, args):
         clocks = clk.summary()
         flops = bwd_flops(cfg)
         tf = flops / (ms / 1e3) / 1e12
-        mhz = load_peaks_raw().get("sm_max_mhz", 2070.0)
-        peak = fp32_alu_peak_tflops(mhz)
+        # compulsory bytes: q, k, v (bf16), g, lambda, dO (fp32) in; dq, dk, dv, dg, dlambda (fp32) out
+        e = 2
+        per_tok = (2 * cfg.dk + cfg.dv) * e + 4 + 4 * cfg.L + 4 * cfg.dv + \
+            (2 * cfg.dk + cfg.dv) * 4 + 4 + 4 * cfg.L
+        nbytes = BHT * per_tok
+        gbs = nbytes / (ms / 1e3) / 1e9
         res["backward"] = {
             "workload": "gradients of the forward workload (dq, dk, dv, dg, dlambda), chunk 64",
-            "ms": ms, "tokens_per_s": cfg.B * cfg.T / (ms / 1e3),
-            "roofline": {"bound": "alu", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
-                         "frac": tf / peak, "algorithmic_flops": flops,
-                         "peak_source": f"fp32 CUDA-core FMA rate at {mhz:.0f} MHz (152 SMs x 128 lanes x 2)"},
+            "ms": ms, "tokens_per_s": cfg.B * cfg.T / (ms / 1e3), "tflops": tf,
+            "algorithmic_flops": flops,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": gbs / hbm_peak, "algorithmic_bytes": nbytes,
+                         "note": "compulsory bytes only; arithmetic intensity (flops / bytes) is below the "
+                                 "bf16 ridge, so HBM bounds the ideal backward"},
             "clocks": clocks}
         del ws, dout
     return res
