@@ -126,7 +126,11 @@ simt_gate_prefix_kernel(const float *__restrict__ gam, double *__restrict__ P, i
 // In place: slot j (1..N-1) holds H_{j-1} on entry and Node_j on exit.
 // One thread per state element; the open node of each level is kept in
 // registers (stack[z] = the latest node with ctz == z).
-constexpr int kMaxZ = 24;
+// In-place Fenwick scan of one state element per thread, level by level:
+// slot j holds H_{j-1} and becomes
+//     Node_j = H_{j-1} + sum_{m < ctz(j)} exp(P_j - P_{j-2^m}) Node_{j-2^m}.
+// Every node of level z reads only nodes of lower levels, so the nodes of
+// one level are independent and their loads overlap.
 __global__ void __launch_bounds__(kThreads)
 simt_fenwick_scan_kernel(const double *__restrict__ P, float *__restrict__ nodes, int N, int E)
 {
@@ -135,22 +139,17 @@ simt_fenwick_scan_kernel(const double *__restrict__ P, float *__restrict__ nodes
     if (e >= E) return;
     const double *Pb = P + bh * (long long)(N + 1);
     float *base = nodes + bh * (long long)N * E + e;
-    float stack[kMaxZ];
-#pragma unroll
-    for (int z = 0; z < kMaxZ; z++) stack[z] = 0.f;
-    for (int j = 1; j < N; j++) {
-        const int z = ctz_u32((uint32_t)j);
-        float val = base[(long long)j * E];
-        const double Pj = Pb[j];
-#pragma unroll
-        for (int kk = 0; kk < kMaxZ; kk++) {  // only the z lower levels fold in
-            if (kk >= z) break;
-            val = fmaf(expf((float)(Pj - Pb[j - (1 << kk)])), stack[kk], val);
+    for (int z = 1; (1 << z) < N; z++) {
+        // j = odd multiples of 2^z below N
+        for (int j = 1 << z; j < N; j += 2 << z) {
+            const double Pj = Pb[j];
+            float val = base[(long long)j * E];
+            for (int m = 0; m < z; m++) {
+                const int jm = j - (1 << m);
+                val = fmaf(expf((float)(Pj - Pb[jm])), base[(long long)jm * E], val);
+            }
+            base[(long long)j * E] = val;
         }
-#pragma unroll
-        for (int kk = 0; kk < kMaxZ; kk++)
-            if (kk == z) stack[kk] = val;
-        base[(long long)j * E] = val;
     }
 }
 
