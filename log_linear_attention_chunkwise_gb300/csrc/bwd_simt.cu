@@ -702,12 +702,20 @@ cudaError_t launch_bwd(const BwdArgs &A)
     float *parts = (float *)(ws + lay.parts);
     double *dG = (double *)(ws + lay.dG);
     bwd_gamma_kernel<<<dim3(N, BH), 32, 0, st>>>(A.g, gamma, A.T, A.C);
-    const size_t smq = sizeof(float) * query_smem_floats(A.C, A.dk, A.dv, A.L);
-    e = cudaFuncSetAttribute(bwd_query_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smq);
-    if (e != cudaSuccess) return e;
-    bwd_query_kernel<Tin><<<dim3(N, BH), kThreads, smq, st>>>(
-        (const Tin *)A.q, (const Tin *)A.k, (const Tin *)A.v, A.dout, gamma, A.lam, P, nodes, A.dq,
-        A.dkey, A.dval, A.dlam, A.T, A.dk, A.dv, A.C, cbits, N, A.L, bwd_query_tc_supported(A) ? 0 : 1);
+    if (bwd_intra_tc_supported(A)) {
+        int *err = (int *)(ws + lay.err);
+        e = cudaMemsetAsync(err, 0, sizeof(int), st);
+        if (e != cudaSuccess) return e;
+        e = bwd_intra_tc(A, gamma, err);
+        if (e != cudaSuccess) return e;
+    } else {
+        const size_t smq = sizeof(float) * query_smem_floats(A.C, A.dk, A.dv, A.L);
+        e = cudaFuncSetAttribute(bwd_query_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smq);
+        if (e != cudaSuccess) return e;
+        bwd_query_kernel<Tin><<<dim3(N, BH), kThreads, smq, st>>>(
+            (const Tin *)A.q, (const Tin *)A.k, (const Tin *)A.v, A.dout, gamma, A.lam, P, nodes, A.dq,
+            A.dkey, A.dval, A.dlam, A.T, A.dk, A.dv, A.C, cbits, N, A.L, bwd_query_tc_supported(A) ? 0 : 1);
+    }
     if (bwd_query_tc_supported(A) && N > 1) {
         int *err = (int *)(ws + lay.err);
         e = cudaMemsetAsync(err, 0, sizeof(int), st);

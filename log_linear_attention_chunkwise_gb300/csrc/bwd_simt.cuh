@@ -27,6 +27,9 @@ cudaError_t bwd_key_tc(const BwdArgs &A, const float *gamma, const double *P, co
 // Query side (node read-out) on the tensor cores, same conditions: adds to dq, dlambda.
 bool bwd_query_tc_supported(const BwdArgs &A);
 cudaError_t bwd_query_tc(const BwdArgs &A, const float *gamma, const double *P, const float *nodes, int *err);
+// Intra-chunk part on the tensor cores, same conditions: writes dq, dk, dv, dlambda.
+bool bwd_intra_tc_supported(const BwdArgs &A);
+cudaError_t bwd_intra_tc(const BwdArgs &A, const float *gamma, int *err);
 // Block-state pieces on the tensor cores, same conditions: writes every piece slot it owns.
 bool bwd_piece_tc_supported(const BwdArgs &A);
 cudaError_t bwd_piece_tc(const BwdArgs &A, const float *gamma, const double *P, float *part, int nlev, int Pc,
