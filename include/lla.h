@@ -260,10 +260,13 @@ lla_status lla_gdn_decode_step(float *state, const void *q, const void *k,
  *   dv_s = sum_t A_ts (q_t . k_s) dout_t
  *   dlambda_t[l] = sum_{s: l(t,s)=l} exp(G_t - G_s) (q_t . k_s)(dout_t . v_s)
  *   dg_r = sum_{u >= r} (sum_l lambda_u[l] dlambda_u[l] - k_u . dk_u).
- * Computed chunkwise on CUDA cores in fp32: the forward's chunk-level Fenwick
- * nodes serve dq and dlambda; one lambda-weighted state per (level, aligned
- * block of later chunks) serves dk and dv.  Sums run in a fixed order, so
- * repeated calls give bitwise-identical results.
+ * Computed chunkwise: the forward's chunk-level Fenwick nodes serve dq and
+ * dlambda; one lambda-weighted state per (level, aligned block of later
+ * chunks) serves dk and dv.  For bf16 inputs with dk = dv = 128 and chunk 64
+ * the products run on the tensor cores with every fp32 operand split into
+ * two or three bf16 parts (fp32-level accuracy); otherwise on CUDA cores in
+ * fp32.  Sums run in a fixed order, so repeated calls give bitwise-identical
+ * results.
  *   q, k [B,H,T,dk], v [B,H,T,dv] in in_dt; g [B,H,T], lambda [B,H,T,L]
  *   (L = lla_num_levels(T)), dout [B,H,T,dv] fp32; outputs (caller-owned,
  *   fully overwritten, fp32): dq, dk [B,H,T,dk], dv [B,H,T,dv], dg [B,H,T],
