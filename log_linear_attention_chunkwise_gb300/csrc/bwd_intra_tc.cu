@@ -14,6 +14,7 @@
 // written here (the node and block-state parts add to them afterwards).
 #include "bwd_simt.cuh"
 #include "sm100.cuh"
+#include "split_stage.cuh"
 #include "tma_host.cuh"
 
 namespace lla {
@@ -52,30 +53,8 @@ __device__ __forceinline__ void mma8x(uint32_t d, const uint8_t *a, bool a_mn, c
     }
 }
 
-// 64 fp32 values of row `row` at columns [c0, c0 + 64) of a 128-wide tile, split
-// into bf16 high and remainder parts (128-byte swizzle, 64-column blocks).
-__device__ __forceinline__ void put_split64(uint8_t *hi, uint8_t *lo, int row, int c0, const float *x)
-{
-#pragma unroll
-    for (int ch = 0; ch < 8; ch++) {
-        uint4 h, l;
-        __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&h);
-        __nv_bfloat162 *l2 = reinterpret_cast<__nv_bfloat162 *>(&l);
-#pragma unroll
-        for (int u = 0; u < 4; u++) {
-            const float a = x[8 * ch + 2 * u], b = x[8 * ch + 2 * u + 1];
-            const __nv_bfloat162 hv = __floats2bfloat162_rn(a, b);
-            const float2 hf = __bfloat1622float2(hv);
-            h2[u] = hv;
-            l2[u] = __floats2bfloat162_rn(a - hf.x, b - hf.y);
-        }
-        const uint32_t off = (c0 >> 6) * kIH + sw128_offset(row, ch);
-        *reinterpret_cast<uint4 *>(hi + off) = h;
-        *reinterpret_cast<uint4 *>(lo + off) = l;
-    }
-}
-
-// The same in three bf16 parts (high, middle, low: about 24 bits together).
+// 64 fp32 values of row `row` at columns [c0, c0 + 64) of a 128-wide tile in
+// three bf16 parts (high, middle, low: about 24 bits together), 128-byte swizzle.
 __device__ __forceinline__ void put_split64x3(uint8_t *hi, uint8_t *mid, uint8_t *lo, int row, int c0, const float *x)
 {
 #pragma unroll
@@ -148,18 +127,11 @@ bwd_intra_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
         tmem_alloc(&s.tmem, 512);
         tmem_relinquish();
     }
-    // dO row t, split
+    // dO tile, split
     {
-        const float *src = dout + tok * kID;
-        for (int h = 0; h < 2; h++) {
-            float x[64];
-#pragma unroll
-            for (int c = 0; c < 64; c += 4) {
-                float4 a = row_ok ? *reinterpret_cast<const float4 *>(src + h * 64 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-                x[c] = a.x; x[c + 1] = a.y; x[c + 2] = a.z; x[c + 3] = a.w;
-            }
-            put_split64(s.ohi, s.olo, t, h * 64, x);
-        }
+        uint8_t *d[2] = {s.ohi, s.olo};
+        stage_split_tile<2, kIThreads>(d, dout + ((long long)bh * T + (long long)pair * kIT) * kID, kID, nullptr, 1.f,
+                            (int)min((long long)kIT, (long long)T - (long long)pair * kIT));
     }
     const float gam_t = row_ok ? gamma[tok] : 0.f;
     fence_proxy_async_smem();

@@ -19,6 +19,7 @@
 // the MN-major B operand of the dv product.  Results are added to dk, dv.
 #include "bwd_simt.cuh"
 #include "sm100.cuh"
+#include "split_stage.cuh"
 #include "tma_host.cuh"
 
 namespace lla {
@@ -106,26 +107,8 @@ bwd_key_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_consta
     const double Pend = Pb[pend];
     // stage c * R (fp32 [128][128]) as bf16 high and remainder parts, 128-byte swizzled
     auto stage = [&](int buf, const float *Rm, float c) {
-        // thread p converts row p: 128 values, 16 chunks of 8
-        const float4 *src = reinterpret_cast<const float4 *>(Rm + (long long)p * kKD);
-#pragma unroll 4
-        for (int ch = 0; ch < 16; ch++) {
-            const float4 a = src[2 * ch], b = src[2 * ch + 1];
-            const float x[8] = {a.x * c, a.y * c, a.z * c, a.w * c, b.x * c, b.y * c, b.z * c, b.w * c};
-            uint4 hi, lo;
-            __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&hi);
-            __nv_bfloat162 *l2 = reinterpret_cast<__nv_bfloat162 *>(&lo);
-#pragma unroll
-            for (int u = 0; u < 4; u++) {
-                const __nv_bfloat162 hv = __floats2bfloat162_rn(x[2 * u], x[2 * u + 1]);
-                const float2 hf = __bfloat1622float2(hv);
-                h2[u] = hv;
-                l2[u] = __floats2bfloat162_rn(x[2 * u] - hf.x, x[2 * u + 1] - hf.y);
-            }
-            const uint32_t off = (ch >> 3) * kKHalf + sw128_offset(p, ch & 7);
-            *reinterpret_cast<uint4 *>(s.rhi[buf] + off) = hi;
-            *reinterpret_cast<uint4 *>(s.rlo[buf] + off) = lo;
-        }
+        uint8_t *dst[2] = {s.rhi[buf], s.rlo[buf]};
+        stage_split_tile<2, kKThreads>(dst, Rm, kKD, nullptr, c, kKD);
     };
     // the level sequence: level 0 first (if any), then the shared levels
     const int total = (lev0 ? 1 : 0) + nl;

@@ -16,6 +16,7 @@
 // and dlambda.
 #include "bwd_simt.cuh"
 #include "sm100.cuh"
+#include "split_stage.cuh"
 
 namespace lla {
 namespace {
@@ -41,38 +42,6 @@ struct __align__(1024) QuerySmem {
 __device__ __forceinline__ void q_err(int *err, int code) { atomicCAS(err, 0, code); }
 
 __device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
-
-// Rows [r0, r0 + nrows) of an fp32 [.][128] matrix (row stride 128) as bf16
-// high and remainder parts in the 128-byte-swizzled K-major layout; each of
-// the calling threads converts half a row (64 values).
-__device__ __forceinline__ void stage_split(uint8_t *hi, uint8_t *lo, const float *src, int row, int half, float scale,
-                                            bool valid)
-{
-    const float4 *s4 = reinterpret_cast<const float4 *>(src + (long long)row * kQD + half * 64);
-#pragma unroll 2
-    for (int ch = 0; ch < 8; ch++) {
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-        if (valid) {
-            a = s4[2 * ch];
-            b = s4[2 * ch + 1];
-        }
-        const float x[8] = {a.x * scale, a.y * scale, a.z * scale, a.w * scale,
-                            b.x * scale, b.y * scale, b.z * scale, b.w * scale};
-        uint4 h, l;
-        __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&h);
-        __nv_bfloat162 *l2 = reinterpret_cast<__nv_bfloat162 *>(&l);
-#pragma unroll
-        for (int u = 0; u < 4; u++) {
-            const __nv_bfloat162 hv = __floats2bfloat162_rn(x[2 * u], x[2 * u + 1]);
-            const float2 hf = __bfloat1622float2(hv);
-            h2[u] = hv;
-            l2[u] = __floats2bfloat162_rn(x[2 * u] - hf.x, x[2 * u + 1] - hf.y);
-        }
-        const uint32_t off = half * kQHalf + sw128_offset(row, ch);
-        *reinterpret_cast<uint4 *>(hi + off) = h;
-        *reinterpret_cast<uint4 *>(lo + off) = l;
-    }
-}
 
 // 8 MMAs over K = 128, A and B K-major.
 __device__ __forceinline__ void mma8k(uint32_t d, const uint8_t *a, const uint8_t *b, uint32_t idesc, bool acc)
@@ -119,9 +88,17 @@ bwd_query_tc_kernel(const Tin *__restrict__ q, const float *__restrict__ dout, c
         tmem_relinquish();
     }
     // dO tile and the first node
-    stage_split(s.ohi, s.olo, dout + (long long)bh * T * kQD + (long long)pair * kQT * kQD, row, half, 1.f, row_ok);
+    const int nrows = (int)min((long long)kQT, (long long)T - (long long)pair * kQT);
+    {
+        uint8_t *d0[2] = {s.ohi, s.olo};
+        stage_split_tile<2, kQThreads>(d0, dout + ((long long)bh * T + (long long)pair * kQT) * kQD, kQD, nullptr,
+                                       1.f, nrows);
+    }
     const float *node_base = nodes + (long long)bh * N * kQD * kQD;
-    stage_split(s.nhi[0], s.nlo[0], node_base + (long long)js[0] * kQD * kQD, row, half, 1.f, true);
+    {
+        uint8_t *d1[2] = {s.nhi[0], s.nlo[0]};
+        stage_split_tile<2, kQThreads>(d1, node_base + (long long)js[0] * kQD * kQD, kQD, nullptr, 1.f, kQD);
+    }
     fence_proxy_async_smem();
     tc_fence_before_sync();
     __syncthreads();
@@ -182,7 +159,8 @@ bwd_query_tc_kernel(const Tin *__restrict__ q, const float *__restrict__ dout, c
             // stage node n+1 into the other buffer once node n-1's product is done
             const int b1 = (n + 1) & 1;
             if (n >= 1 && !mbar_wait(&s.bar_mma[b1], ((n - 1) >> 1) & 1, kQWait)) q_err(err, 2);
-            stage_split(s.nhi[b1], s.nlo[b1], node_base + (long long)js[n + 1] * kQD * kQD, row, half, 1.f, true);
+            uint8_t *d1[2] = {s.nhi[b1], s.nlo[b1]};
+            stage_split_tile<2, kQThreads>(d1, node_base + (long long)js[n + 1] * kQD * kQD, kQD, nullptr, 1.f, kQD);
             fence_proxy_async_smem();
         }
         drain(n);  // contains a barrier of all threads: node n+1 is staged and U_{n-1} drained
