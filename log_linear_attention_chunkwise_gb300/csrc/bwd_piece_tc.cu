@@ -10,7 +10,6 @@
 // in order.
 #include "bwd_simt.cuh"
 #include "sm100.cuh"
-#include "split_stage.cuh"
 #include "tma_host.cuh"
 
 namespace lla {
@@ -28,7 +27,6 @@ constexpr uint32_t kPWait = 1u << 22;
 struct __align__(1024) PieceSmem {
     uint8_t q[2][kPB];
     uint8_t bhi[2][kPB], blo[2][kPB];
-    float w[kPT];  // per-token weights of the tile being staged
     uint64_t bar_load[2], bar_mma[2], bar_done;
     uint32_t tmem;
 };
@@ -100,22 +98,35 @@ bwd_piece_tc_kernel(const __grid_constant__ CUtensorMap map_q, const float *__re
             load_q(n + 1);
         }
         if (n >= 2 && !mbar_wait(&s.bar_mma[st], ((n - 2) >> 1) & 1, kPWait)) atomicCAS(err, 0, 2);
-        // token row p of the tile: its weight, then the tile w dO, split (rows past the piece: 0)
-        {
-            const long long t = t_lo + (long long)n * kPT + p;
-            float w = 0.f;
-            if (t < t_hi) {
-                const long long gi = (long long)bh * T + t;
-                w = lam[gi * L + lev] * __expf((float)(Pb[t >> 6] - Pref) + gamma[gi]);
-            }
-            s.w[p] = w;
+        // token row p of the tile: w dO, split
+        const long long t = t_lo + (long long)n * kPT + p;
+        float w = 0.f;
+        if (t < t_hi) {
+            const long long gi = (long long)bh * T + t;
+            w = lam[gi * L + lev] * __expf((float)(Pb[t >> 6] - Pref) + gamma[gi]);
         }
-        __syncthreads();
-        {
-            const long long r0 = t_lo + (long long)n * kPT;
-            uint8_t *d[2] = {s.bhi[st], s.blo[st]};
-            stage_split_tile<2, kPThreads>(d, dout + ((long long)bh * T + r0) * kPDm, kPDm, s.w, 1.f,
-                                (int)min((long long)kPT, t_hi - r0));
+        const float4 *src = reinterpret_cast<const float4 *>(dout + ((long long)bh * T + (t < t_hi ? t : t_lo)) * kPDm);
+#pragma unroll 4
+        for (int ch = 0; ch < 16; ch++) {
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f), c = a;
+            if (t < t_hi) {
+                a = src[2 * ch];
+                c = src[2 * ch + 1];
+            }
+            const float x[8] = {a.x * w, a.y * w, a.z * w, a.w * w, c.x * w, c.y * w, c.z * w, c.w * w};
+            uint4 h, l;
+            __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&h);
+            __nv_bfloat162 *l2 = reinterpret_cast<__nv_bfloat162 *>(&l);
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                const __nv_bfloat162 hv = __floats2bfloat162_rn(x[2 * u], x[2 * u + 1]);
+                const float2 hf = __bfloat1622float2(hv);
+                h2[u] = hv;
+                l2[u] = __floats2bfloat162_rn(x[2 * u] - hf.x, x[2 * u + 1] - hf.y);
+            }
+            const uint32_t off = (ch >> 3) * kPH + sw128_offset(p, ch & 7);
+            *reinterpret_cast<uint4 *>(s.bhi[st] + off) = h;
+            *reinterpret_cast<uint4 *>(s.blo[st] + off) = l;
         }
         fence_proxy_async_smem();
         if (!mbar_wait(&s.bar_load[st], (n >> 1) & 1, kPWait)) atomicCAS(err, 0, 1);
