@@ -21,11 +21,12 @@
 namespace lla {
 namespace {
 
-constexpr int kThreads = 256;
 constexpr int kTokBlk = 32;  // tokens staged per refill of the forward
 
-template <int KW>
-__host__ __device__ constexpr int row_groups() { return kThreads / KW; }
+// The forward's CTA: KW columns, 32 lanes per column when dk >= 32 (16 when
+// dk = 16), so 32 KW (or 16 KW) threads.
+template <int KW, int RG>
+__host__ __device__ constexpr int fwd_threads() { return KW * RG; }
 
 // Column stride of the states in shared memory: 16 banks apart, so the two
 // columns that share a warp never meet in a bank.
@@ -33,6 +34,7 @@ __host__ __device__ inline int col_stride(int dk) { return dk % 32 == 16 ? dk : 
 
 size_t fwd_smem_floats(int T, int dk, int L, int kw)
 {
+    // (the staging sizes do not depend on the thread count)
     const int Lsi = T > 0 ? bit_length_u32((uint32_t)T) : 1;
     return (size_t)Lsi * kw * col_stride(dk)  // states, one padded column after another
            + 2 * (size_t)kTokBlk * dk       // q, k
@@ -41,20 +43,20 @@ size_t fwd_smem_floats(int T, int dk, int L, int kw)
            + (size_t)kTokBlk * L;           // lambda rows
 }
 
-// A CTA owns KW value columns; the RG = 256/KW lanes of one column are
+// A CTA owns KW value columns; the RG lanes of one column are
 // consecutive lanes of one warp and hold rows rg, rg + RG, ... of it, so the
 // sums over rows are warp shuffles and no barrier is needed between tokens.
 // A column's states sit contiguously in shared memory (padded to dk + 1) so
 // the lanes of a column read consecutive banks.
 inline int fwd_columns(int dk) { return dk >= 32 ? 8 : 16; }  // 8: a whole warp per column
-template <typename Tin, int KW>
-__global__ void __launch_bounds__(kThreads)
+template <typename Tin, int KW, int RG>
+__global__ void __launch_bounds__(KW * RG)
 gdn_fwd_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
                const float *__restrict__ g, const float *__restrict__ beta, const float *__restrict__ lam,
                float *__restrict__ out, float *__restrict__ state_out, int T, int H, int dk, int dv, int L,
                int Ls_out)
 {
-    constexpr int RG = row_groups<KW>();
+    constexpr int NT = fwd_threads<KW, RG>();
     static_assert(RG <= 32 && (32 % RG) == 0, "a column's lanes lie inside one warp");
     extern __shared__ __align__(16) float sm[];
     const int Lsi = T > 0 ? bit_length_u32((uint32_t)T) : 1;
@@ -80,17 +82,17 @@ gdn_fwd_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *
     for (int t0 = 0; t0 < T; t0 += kTokBlk) {
         const int nt = min(kTokBlk, T - t0);
         __syncthreads();  // the previous block is consumed
-        for (int e = threadIdx.x; e < nt * dk; e += kThreads) {
+        for (int e = threadIdx.x; e < nt * dk; e += NT) {
             qs[e] = to_f32(q[(tok0 + t0) * dk + e]);
             ks[e] = to_f32(k[(tok0 + t0) * dk + e]);
         }
-        for (int e = threadIdx.x; e < nt * KW; e += kThreads)
+        for (int e = threadIdx.x; e < nt * KW; e += NT)
             vs[e] = to_f32(v[(tok0 + t0 + e / KW) * dv + blockIdx.x * KW + e % KW]);
-        for (int e = threadIdx.x; e < nt; e += kThreads) {
+        for (int e = threadIdx.x; e < nt; e += NT) {
             as[e] = expf(g[tok0 + t0 + e]);
             bs[e] = beta[tok0 + t0 + e];
         }
-        for (int e = threadIdx.x; e < nt * L; e += kThreads) ls[e] = lam[(tok0 + t0) * L + e];
+        for (int e = threadIdx.x; e < nt * L; e += NT) ls[e] = lam[(tok0 + t0) * L + e];
         __syncthreads();
         if (threadIdx.x < nt) {
             float a = 0.f;
@@ -257,14 +259,14 @@ gdn_decode_kernel(float *__restrict__ S, const Tin *__restrict__ q, const Tin *_
     if (active && part == 0) out[bh * dv + col] = o;
 }
 
-template <typename Tin, int KW>
+template <typename Tin, int KW, int RG>
 cudaError_t launch_fwd_w(const GdnFwdArgs &A)
 {
     const size_t smem = sizeof(float) * fwd_smem_floats(A.T, A.dk, A.L, KW);
-    auto kern = gdn_fwd_kernel<Tin, KW>;
+    auto kern = gdn_fwd_kernel<Tin, KW, RG>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<dim3(A.dv / KW, A.H, A.B), kThreads, smem, (cudaStream_t)A.stream>>>(
+    kern<<<dim3(A.dv / KW, A.H, A.B), KW * RG, smem, (cudaStream_t)A.stream>>>(
         (const Tin *)A.q, (const Tin *)A.k, (const Tin *)A.v, A.g, A.beta, A.lam, A.out, A.state_out, A.T,
         A.H, A.dk, A.dv, A.L, A.Ls_out);
     return cudaPeekAtLastError();
@@ -273,7 +275,7 @@ cudaError_t launch_fwd_w(const GdnFwdArgs &A)
 template <typename Tin>
 cudaError_t launch_fwd(const GdnFwdArgs &A)
 {
-    return fwd_columns(A.dk) == 8 ? launch_fwd_w<Tin, 8>(A) : launch_fwd_w<Tin, 16>(A);
+    return fwd_columns(A.dk) == 8 ? launch_fwd_w<Tin, 8, 32>(A) : launch_fwd_w<Tin, 16, 16>(A);
 }
 
 template <typename Tin, int DK, int DV>
