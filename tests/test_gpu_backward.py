@@ -69,6 +69,13 @@ def test_bwd_stress_no_decay_and_unit_lambda():
                              lam_one_frac=0.5, g_zero_head_frac=0.5, name="stress"))
 
 
+def test_bwd_stress_tensor_core_path():
+    """dk = dv = 128, bf16, chunk 64 (the tensor-core kernels) with gates forced to
+    0 on half of the heads, so every level state carries undecayed mass."""
+    check(W.small_fwd_config(1, 4, 640, 128, 128, 64, torch.bfloat16, seed=5, g_mu=-2.0,
+                             lam_one_frac=0.5, g_zero_head_frac=0.5, name="stress_tc"))
+
+
 def test_bwd_at_the_2k_context_shape():
     """T = 2048, d = 128, bf16 inputs (the shape of the 2K workload), two heads."""
     check(W.small_fwd_config(1, 2, 2048, 128, 128, 64, torch.bfloat16, seed=77, name="T2048"))
