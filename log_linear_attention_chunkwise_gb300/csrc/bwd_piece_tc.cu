@@ -63,7 +63,7 @@ bwd_piece_tc_kernel(const __grid_constant__ CUtensorMap map_q, const float *__re
     const int lev = cbits + 1 + m;
     const double *Pb = P + (long long)bh * (N + 1);
     const double Pref = Pb[c0];
-    const long long t_lo = (long long)p0 * 64, t_hi = (long long)p1 * 64;
+    const long long t_lo = (long long)p0 << cbits, t_hi = (long long)p1 << cbits;
     const int ntiles = (int)((t_hi - t_lo + kPT - 1) / kPT);
     if (p == 0) {
         for (int i = 0; i < 2; i++) {
@@ -103,7 +103,7 @@ bwd_piece_tc_kernel(const __grid_constant__ CUtensorMap map_q, const float *__re
         float w = 0.f;
         if (t < t_hi) {
             const long long gi = (long long)bh * T + t;
-            w = lam[gi * L + lev] * __expf((float)(Pb[t >> 6] - Pref) + gamma[gi]);
+            w = lam[gi * L + lev] * __expf((float)(Pb[t >> cbits] - Pref) + gamma[gi]);
         }
         const float4 *src = reinterpret_cast<const float4 *>(dout + ((long long)bh * T + (t < t_hi ? t : t_lo)) * kPDm);
 #pragma unroll 4
@@ -180,7 +180,7 @@ cudaError_t bwd_piece_tc(const BwdArgs &A, const float *gamma, const double *P, 
     cudaError_t e = cudaFuncSetAttribute(bwd_piece_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     bwd_piece_tc_kernel<<<dim3(nitems, BH), kPThreads, smem, (cudaStream_t)A.stream>>>(
-        mq, A.dout, gamma, A.lam, P, part, A.T, N, A.L, 6, nlev, Pc, err);
+        mq, A.dout, gamma, A.lam, P, part, A.T, N, A.L, ctz_u32((uint32_t)A.C), nlev, Pc, err);
     return cudaPeekAtLastError();
 }
 

@@ -194,7 +194,7 @@ bool bwd_query_tc_supported(const BwdArgs &A)
 cudaError_t bwd_query_tc(const BwdArgs &A, const float *gamma, const double *P, const float *nodes, int *err)
 {
     const int BH = A.B * A.H, N = A.T / A.C;
-    const int cbits = 6;
+    const int cbits = ctz_u32((uint32_t)A.C);  // 6: the supported chunk is 64
     const size_t smem = sizeof(QuerySmem) + 1024;
     auto kern = bwd_query_tc_kernel<__nv_bfloat16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
