@@ -217,21 +217,34 @@ lla_status lla_fwd_host(const void *q, const void *k, const void *v, const float
  * With lambda = 1 it is Gated DeltaNet.  Keys should be L2-normalised and
  * beta in [0,1] for the transitions to be contractions (not checked).
  *
- * lla_gdn_fwd runs the recurrent form (§2.3) over a whole sequence from the
- * empty state on CUDA cores (fp32): one CTA per (batch, head, 8 or 16 value
- * columns) steps through the tokens with the bucket states in shared memory.
+ * lla_gdn_fwd runs the chunkwise form (§2.3's chunked evaluation with the
+ * delta rule's compact product): per chunk of 64 tokens the product of the
+ * undecayed factors is I - K^T T K with
+ * T = (I + strict_lower(diag(beta) K K^T))^{-1} diag(beta), so the
+ * intra-chunk output, the read-out of earlier states and the chunk's
+ * transition are small matrix products; the chunk-level Fenwick states are
+ * then carried across chunks in order.  fp32 on CUDA cores, two launches.
  *   q, k [B,H,T,dk], v [B,H,T,dv] in in_dt; g, beta [B,H,T] fp32;
  *   lambda [B,H,T,L] fp32 with L = lla_num_levels(T); out [B,H,T,dv] fp32.
+ *   k must be 16-byte aligned (its rows are copied in 16-byte pieces).
  *   state_out (nullable) [B,H,Ls_out,dk,dv] fp32 receives the state after the
  *   sequence in the layout of lla_gdn_decode_step (slot i = level i+1, dead
  *   slots zeroed); Ls_out >= bit_length(T) when state_out is given.
- * Supported: dk, dv in {16,32,64,128}, T <= 2^16 (the bucket states must fit
- * in shared memory), B, H <= 65535.  No workspace.  Errors as lla_fwd.
+ * Supported: dk, dv in {16,32,64,128}, T <= 2^24 (and the per-CTA state of
+ * the chunk scan, bit_length(ceil(T/64)) x dk x 8 floats plus staging, must
+ * fit in shared memory), B, H <= 65535.
+ * workspace: >= lla_gdn_fwd_workspace_bytes(B,H,T,dk,dv) bytes, 256-byte
+ * aligned, owned by the caller (per chunk: q~ and w transposed, the chunk
+ * state H, its total decay; fp32).  Errors as lla_fwd: a bad shape returns
+ * LLA_ERR_UNSUPPORTED_SHAPE, a NULL or misaligned pointer or a short
+ * workspace LLA_ERR_INVALID_ARGUMENT.  B*H*T == 0 is a no-op returning LLA_OK.
  */
+size_t lla_gdn_fwd_workspace_bytes(int B, int H, int T, int dk, int dv);
 lla_status lla_gdn_fwd(const void *q, const void *k, const void *v, const float *g,
                        const float *beta, const float *lambda, float *out,
                        float *state_out, int B, int H, int T, int dk, int dv,
-                       int Ls_out, lla_dtype in_dt, void *stream);
+                       int Ls_out, lla_dtype in_dt, void *workspace,
+                       size_t workspace_bytes, void *stream);
 
 /*
  * One decode step of Log-Linear Gated DeltaNet on an eager level state:

@@ -38,7 +38,8 @@ SIGNATURES = {
     "lla_lambda_mlp": (_I, [_P] * 5 + [_I] * 5 + [_I, _P]),
     "lla_bwd_workspace_bytes": (_Z, [_I] * 7),
     "lla_bwd": (_I, [_P] * 11 + [_I] * 7 + [_P, _Z, _P]),
-    "lla_gdn_fwd": (_I, [_P] * 8 + [_I] * 6 + [_I, _P]),
+    "lla_gdn_fwd_workspace_bytes": (_Z, [_I] * 5),
+    "lla_gdn_fwd": (_I, [_P] * 8 + [_I] * 6 + [_I, _P, _Z, _P]),
     "lla_fwd_host_workspace_bytes": (_Z, [_I] * 9),
     "lla_fwd_host": (_I, [_P] * 6 + [_I] * 6 + [_I, _I, _I, _P, _Z, _P]),
     "lla_gdn_decode_step": (_I, [_P] * 9 + [_I] * 5 + [_I, _P, _P]),
@@ -239,7 +240,7 @@ def bwd(q, k, v, g, lam, dout, chunk: int = 64, workspace=None, stream=None):
     return dq, dkk, dvv, dg, dl
 
 
-def gdn_fwd(q, k, v, g, beta, lam, out=None, state_Ls: int = 0, stream=None):
+def gdn_fwd(q, k, v, g, beta, lam, out=None, state_Ls: int = 0, workspace=None, stream=None):
     """lla_gdn_fwd: Log-Linear Gated DeltaNet over whole sequences.  Returns
     out [B,H,T,dv], or (out, state [B,H,state_Ls,dk,dv]) when state_Ls > 0."""
     lib = load()
@@ -260,9 +261,12 @@ def gdn_fwd(q, k, v, g, beta, lam, out=None, state_Ls: int = 0, stream=None):
     state = None
     if state_Ls > 0:
         state = torch.empty((B, H, state_Ls, dk, dv), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        need = lib.lla_gdn_fwd_workspace_bytes(B, H, T, dk, dv)
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     rc = lib.lla_gdn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(lam), _ptr(out),
                          _ptr(state) if state is not None else None, B, H, T, dk, dv, state_Ls,
-                         _dt(q), _stream(stream))
+                         _dt(q), _ptr(workspace), workspace.numel(), _stream(stream))
     _check("lla_gdn_fwd", rc)
     return (out, state) if state is not None else out
 

@@ -1,4 +1,4 @@
-// Log-Linear Gated DeltaNet, recurrent form.
+// Log-Linear Gated DeltaNet, one decode step (the recurrent form).
 //
 // "Log-Linear Attention" §3 builds Log-Linear Gated DeltaNet by keeping the
 // Gated DeltaNet state update and adding the hierarchical (Fenwick) mask; the
@@ -13,148 +13,11 @@
 // Column c of every state only ever mixes with itself: with
 // P = q.S[:,c] and U = k.S[:,c] of the old state, the new column is
 // alpha (S[:,c] - beta U k) and its read-out alpha (P - beta U (q.k)).
-// A CTA owns KW columns of one (batch, head) and RG lanes of one warp share a
-// column, each holding R of its rows, so the only cross-thread step is summing
-// P and U over those lanes (warp shuffles).
+// The forward over whole sequences is the chunkwise form (gdn_chunk.cu).
 #include "gdn.cuh"
 
 namespace lla {
 namespace {
-
-constexpr int kTokBlk = 32;  // tokens staged per refill of the forward
-
-// The forward's CTA: KW columns, 32 lanes per column when dk >= 32 (16 when
-// dk = 16), so 32 KW (or 16 KW) threads.
-template <int KW, int RG>
-__host__ __device__ constexpr int fwd_threads() { return KW * RG; }
-
-// Column stride of the states in shared memory: 16 banks apart, so the two
-// columns that share a warp never meet in a bank.
-__host__ __device__ inline int col_stride(int dk) { return dk % 32 == 16 ? dk : dk + 16; }
-
-size_t fwd_smem_floats(int T, int dk, int L, int kw)
-{
-    // (the staging sizes do not depend on the thread count)
-    const int Lsi = T > 0 ? bit_length_u32((uint32_t)T) : 1;
-    return (size_t)Lsi * kw * col_stride(dk)  // states, one padded column after another
-           + 2 * (size_t)kTokBlk * dk       // q, k
-           + (size_t)kTokBlk * kw           // v columns
-           + 3 * (size_t)kTokBlk            // alpha, beta, q.k
-           + (size_t)kTokBlk * L;           // lambda rows
-}
-
-// A CTA owns KW value columns; the RG lanes of one column are
-// consecutive lanes of one warp and hold rows rg, rg + RG, ... of it, so the
-// sums over rows are warp shuffles and no barrier is needed between tokens.
-// A column's states sit contiguously in shared memory (padded to dk + 1) so
-// the lanes of a column read consecutive banks.
-inline int fwd_columns(int dk) { return dk >= 32 ? 8 : 16; }  // 8: a whole warp per column
-template <typename Tin, int KW, int RG>
-__global__ void __launch_bounds__(KW * RG)
-gdn_fwd_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
-               const float *__restrict__ g, const float *__restrict__ beta, const float *__restrict__ lam,
-               float *__restrict__ out, float *__restrict__ state_out, int T, int H, int dk, int dv, int L,
-               int Ls_out)
-{
-    constexpr int NT = fwd_threads<KW, RG>();
-    static_assert(RG <= 32 && (32 % RG) == 0, "a column's lanes lie inside one warp");
-    extern __shared__ __align__(16) float sm[];
-    const int Lsi = T > 0 ? bit_length_u32((uint32_t)T) : 1;
-    const int ldc = col_stride(dk);
-    float *S = sm;                              // [Lsi][KW][ldc]
-    float *qs = S + Lsi * KW * ldc;             // [kTokBlk][dk]
-    float *ks = qs + kTokBlk * dk;              // [kTokBlk][dk]
-    float *vs = ks + kTokBlk * dk;              // [kTokBlk][KW]
-    float *as = vs + kTokBlk * KW;              // [kTokBlk] alpha
-    float *bs = as + kTokBlk;                   // [kTokBlk] beta
-    float *qk = bs + kTokBlk;                   // [kTokBlk] q.k
-    float *ls = qk + kTokBlk;                   // [kTokBlk][L]
-    const int c = threadIdx.x / RG, rg = threadIdx.x % RG;
-    const int R = dk / RG;  // rows per thread (1..8)
-    const int col = blockIdx.x * KW + c;
-    const long long bh = (long long)blockIdx.z * H + blockIdx.y;
-    const long long tok0 = bh * (long long)T;
-    auto colsum = [](float x) {
-#pragma unroll
-        for (int off = RG / 2; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off, RG);
-        return x;
-    };
-    for (int t0 = 0; t0 < T; t0 += kTokBlk) {
-        const int nt = min(kTokBlk, T - t0);
-        __syncthreads();  // the previous block is consumed
-        for (int e = threadIdx.x; e < nt * dk; e += NT) {
-            qs[e] = to_f32(q[(tok0 + t0) * dk + e]);
-            ks[e] = to_f32(k[(tok0 + t0) * dk + e]);
-        }
-        for (int e = threadIdx.x; e < nt * KW; e += NT)
-            vs[e] = to_f32(v[(tok0 + t0 + e / KW) * dv + blockIdx.x * KW + e % KW]);
-        for (int e = threadIdx.x; e < nt; e += NT) {
-            as[e] = expf(g[tok0 + t0 + e]);
-            bs[e] = beta[tok0 + t0 + e];
-        }
-        for (int e = threadIdx.x; e < nt * L; e += NT) ls[e] = lam[(tok0 + t0) * L + e];
-        __syncthreads();
-        if (threadIdx.x < nt) {
-            float a = 0.f;
-            for (int r = 0; r < dk; r++) a = fmaf(qs[threadIdx.x * dk + r], ks[threadIdx.x * dk + r], a);
-            qk[threadIdx.x] = a;
-        }
-        __syncthreads();
-        for (int tt = 0; tt < nt; tt++) {
-            const uint32_t t = (uint32_t)(t0 + tt);
-            const float *qt = qs + tt * dk, *kt = ks + tt * dk;
-            const int m = ctz_u32(t + 1u);
-            const float al = as[tt], be = bs[tt], qkt = qk[tt], vc = vs[tt * KW + c];
-            const float *lt = ls + tt * L;
-            float o = lt[0] * be * qkt * vc;
-            float macc[8];
-#pragma unroll
-            for (int j = 0; j < 8; j++) macc[j] = 0.f;
-            for (int i = 0; i < Lsi; i++) {
-                if (!((t >> i) & 1u)) continue;
-                float *Sc = S + (i * KW + c) * ldc;
-                float x[8], p = 0.f, u = 0.f;
-#pragma unroll
-                for (int j = 0; j < 8; j++) {
-                    if (j >= R) break;
-                    const int r = rg + RG * j;
-                    x[j] = Sc[r];
-                    p = fmaf(qt[r], x[j], p);
-                    u = fmaf(kt[r], x[j], u);
-                }
-                const float P = colsum(p), U = colsum(u);
-                const float bu = be * U;
-#pragma unroll
-                for (int j = 0; j < 8; j++) {
-                    if (j >= R) break;
-                    const int r = rg + RG * j;
-                    const float sn = al * (x[j] - bu * kt[r]);
-                    Sc[r] = sn;
-                    if (i < m) macc[j] += sn;
-                }
-                o = fmaf(lt[i + 1], al * (P - bu * qkt), o);
-            }
-            float *Sm = S + (m * KW + c) * ldc;
-#pragma unroll
-            for (int j = 0; j < 8; j++) {
-                if (j >= R) break;
-                const int r = rg + RG * j;
-                Sm[r] = fmaf(be * kt[r], vc, macc[j]);
-            }
-            if (rg == 0) out[(tok0 + t) * dv + col] = o;
-        }
-    }
-    if (state_out) {  // the state after [0, T): slot i live iff bit i of T
-        __syncthreads();
-        for (int i = 0; i < Ls_out; i++) {
-            const bool live = i < Lsi && (((uint32_t)T >> i) & 1u);
-            for (int j = 0; j < R; j++) {
-                const int r = rg + RG * j;
-                state_out[((bh * Ls_out + i) * dk + r) * dv + col] = live ? S[(i * KW + c) * ldc + r] : 0.f;
-            }
-        }
-    }
-}
 
 // One decode step on the level state in global memory [B,H,Ls,dk,dv].
 // A warp owns 32/SPLIT value columns of one (batch, head); SPLIT lanes share
@@ -259,25 +122,6 @@ gdn_decode_kernel(float *__restrict__ S, const Tin *__restrict__ q, const Tin *_
     if (active && part == 0) out[bh * dv + col] = o;
 }
 
-template <typename Tin, int KW, int RG>
-cudaError_t launch_fwd_w(const GdnFwdArgs &A)
-{
-    const size_t smem = sizeof(float) * fwd_smem_floats(A.T, A.dk, A.L, KW);
-    auto kern = gdn_fwd_kernel<Tin, KW, RG>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    kern<<<dim3(A.dv / KW, A.H, A.B), KW * RG, smem, (cudaStream_t)A.stream>>>(
-        (const Tin *)A.q, (const Tin *)A.k, (const Tin *)A.v, A.g, A.beta, A.lam, A.out, A.state_out, A.T,
-        A.H, A.dk, A.dv, A.L, A.Ls_out);
-    return cudaPeekAtLastError();
-}
-
-template <typename Tin>
-cudaError_t launch_fwd(const GdnFwdArgs &A)
-{
-    return fwd_columns(A.dk) == 8 ? launch_fwd_w<Tin, 8, 32>(A) : launch_fwd_w<Tin, 16, 16>(A);
-}
-
 template <typename Tin, int DK, int DV>
 void launch_decode_dkv(const GdnDecodeArgs &A)
 {
@@ -312,16 +156,6 @@ cudaError_t launch_decode(const GdnDecodeArgs &A)
 }
 
 }  // namespace
-
-size_t gdn_fwd_smem_bytes(int T, int dk, int L)
-{
-    return sizeof(float) * fwd_smem_floats(T, dk, L, fwd_columns(dk));
-}
-
-cudaError_t gdn_fwd(const GdnFwdArgs &A)
-{
-    return A.in_dt == LLA_F32 ? launch_fwd<float>(A) : launch_fwd<__nv_bfloat16>(A);
-}
 
 cudaError_t gdn_decode_step(const GdnDecodeArgs &A)
 {

@@ -1,4 +1,4 @@
-// Internal interface of Log-Linear Gated DeltaNet (recurrent form).
+// Internal interface of Log-Linear Gated DeltaNet (chunkwise forward, decode step).
 #pragma once
 
 #include <stddef.h>
@@ -13,6 +13,7 @@ struct GdnFwdArgs {
     float *out, *state_out;
     int B, H, T, dk, dv, L, Ls_out;
     lla_dtype in_dt;
+    void *workspace;  // gdn_fwd_workspace_bytes(...) bytes, 256-byte aligned
     void *stream;
 };
 
@@ -28,7 +29,9 @@ struct GdnDecodeArgs {
     void *stream;
 };
 
-size_t gdn_fwd_smem_bytes(int T, int dk, int L);
+size_t gdn_fwd_workspace_bytes(int B, int H, int T, int dk, int dv);
+// Whether both forward kernels' shared memory fits one CTA at this shape.
+bool gdn_fwd_fits(int T, int dk, int dv, int L, int tin_bytes);
 cudaError_t gdn_fwd(const GdnFwdArgs &A);
 cudaError_t gdn_decode_step(const GdnDecodeArgs &A);
 

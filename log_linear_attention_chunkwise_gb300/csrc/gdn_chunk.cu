@@ -1,0 +1,613 @@
+// Log-Linear Gated DeltaNet forward, chunkwise form.
+//
+// The per-token model is the one of the decode step (each Fenwick bucket
+// keeps its own state S_l, dk x dv; every state takes each token's
+// transition A_t = alpha_t (I - beta_t k_t k_t^T), alpha_t = exp(g_t); the
+// read-out is sum_l lambda_t[l] S_l^T q_t; see "Log-Linear Attention" §3 for
+// the hierarchical-mask construction and §2.3 for the chunked evaluation).
+// Over a chunk of C = 64 tokens the product of the undecayed factors has the
+// compact (UT / WY) form
+//     (I - beta_{C-1} k k^T) ... (I - beta_0 k k^T) = I - K^T T K,
+//     T = (I + strict_lower(diag(beta) K K^T))^{-1} diag(beta),
+// and the decay is a scalar, so with gam_a = g_0 + ... + g_a (inclusive):
+//   * state read-out at local row a: exp(gam_a) S^T qt_a,
+//     qt_a = q_a - sum_{b <= a} (q_a . k_b) w_b,  W = T K;
+//   * chunk transition: S <- exp(gam_{C-1}) (S - K^T (W S));
+//   * the chunk's own contribution at its end: H = K^T T diag(exp(gam_{C-1} - gam)) V;
+//   * intra-chunk output: o_a = sum_{s <= a} lambda_a[l(a,s)] exp(gam_a - gam_s) Cm[a,s] v_s,
+//     Cm = inclusive_lower(Q K^T) T  (Cm[a,a] = beta_a q_a.k_a: level 0).
+// Two launches: gdn_chunk_prep_kernel does everything that is local to a
+// chunk for all chunks at once (one CTA per chunk; fp32 CUDA cores; the
+// inverse by 16 x 16 diagonal blocks and block substitution), writing the
+// intra-chunk output, qt and w (transposed, for the scan's row-per-lane
+// reads), H and exp(gam_{C-1}); gdn_chunk_scan_kernel walks the chunks of one
+// (batch, head) in order for 8 value columns (a state column only mixes with
+// itself), keeping the chunk-level Fenwick states in shared memory: read-out
+// added to the output, transition, and the fold of H into the new level.
+// The next chunk's operands are prefetched with cp.async while one is worked.
+#include "gdn.cuh"
+
+namespace lla {
+namespace {
+
+constexpr int kGC = 64;        // chunk length
+constexpr int kGCBits = 6;     // log2(kGC)
+constexpr int kGT = 256;       // threads of both kernels
+constexpr int kLdm = kGC + 1;  // row stride of the 64 x 64 matrices in shared memory
+constexpr int kGW = 8;         // value columns of a scan CTA
+constexpr int kLdws = kGW + 1; // row stride of the scan's W S rows
+constexpr size_t kMaxSmem = 227 * 1024;  // dynamic shared memory of one CTA
+
+// acc[i][j] += sum_{k < K} A(ty + 16 i, k) B(k, tx + 16 j), A(r, k) = A[r ar + k ak],
+// B(k, c) = B[k bk + c bc]; columns j >= cj are skipped.
+template <int RI, int CJ>
+__device__ __forceinline__ void mm16(float (&acc)[RI][CJ], const float *A, int ar, int ak, const float *B, int bk,
+                                     int bc, int K, int ty, int tx, int cj = CJ)
+{
+    const float *pa = A + ty * ar;
+    const float *pb = B + tx * bc;
+#pragma unroll 4
+    for (int k = 0; k < K; k++) {
+        float a[RI], b[CJ];
+#pragma unroll
+        for (int i = 0; i < RI; i++) a[i] = pa[16 * i * ar + k * ak];
+#pragma unroll
+        for (int j = 0; j < CJ; j++) b[j] = j < cj ? pb[k * bk + 16 * j * bc] : 0.f;
+#pragma unroll
+        for (int i = 0; i < RI; i++)
+#pragma unroll
+            for (int j = 0; j < CJ; j++) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+}
+
+template <int RI, int CJ>
+__device__ __forceinline__ void zero(float (&acc)[RI][CJ])
+{
+#pragma unroll
+    for (int i = 0; i < RI; i++)
+#pragma unroll
+        for (int j = 0; j < CJ; j++) acc[i][j] = 0.f;
+}
+
+// Shared memory of the prep kernel, in floats after the 64 fp64 running sums.
+struct PrepLayout {
+    int ldk, ldq;
+    size_t k, q, v, m1, m2, x, y, lam, beta, floats;
+};
+
+__host__ __device__ inline PrepLayout prep_layout(int dk, int dv, int L)
+{
+    PrepLayout P;
+    P.ldk = dk + 1;                        // odd strides: rows read across lanes never share a bank
+    P.ldq = (dk > dv ? dk : dv) + 1;       // Q, later U = T' V
+    P.k = 2 * kGC;                         // after double gam[64]
+    P.q = P.k + (size_t)kGC * P.ldk;
+    P.v = P.q + (size_t)kGC * P.ldq;
+    P.m1 = P.v + (size_t)kGC * dv;
+    P.m2 = P.m1 + (size_t)kGC * kLdm;
+    P.x = P.m2 + (size_t)kGC * kLdm;
+    P.y = P.x + (size_t)kGC * kLdm;        // [3][16][17] block products of the inverse
+    P.lam = P.y + 3 * 16 * 17;
+    P.beta = P.lam + (size_t)kGC * L;
+    P.floats = P.beta + kGC;
+    return P;
+}
+
+// Workspace: [BH][N][2][dk][64] (qt^T then w^T), [BH][N][dk][dv] (H), [BH][N] exp(gam_{C-1}).
+struct WsLayout {
+    size_t qw, h, gend, bytes;
+};
+
+inline WsLayout ws_layout(long long BH, int N, int dk, int dv)
+{
+    WsLayout W;
+    W.qw = 0;
+    W.h = W.qw + align_up((size_t)BH * N * 2 * dk * kGC * sizeof(float), 256);
+    W.gend = W.h + align_up((size_t)BH * N * dk * dv * sizeof(float), 256);
+    W.bytes = W.gend + align_up((size_t)BH * N * sizeof(float), 256);
+    return W;
+}
+
+template <typename Tin, int DK>
+__global__ void __launch_bounds__(kGT, DK <= 64 ? 2 : 1)
+gdn_chunk_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
+                      const float *__restrict__ g, const float *__restrict__ beta, const float *__restrict__ lam,
+                      float *__restrict__ out, float *__restrict__ ws_qw, float *__restrict__ ws_h,
+                      float *__restrict__ ws_gend, float *__restrict__ state_out, int T, int N, int H, int dv,
+                      int L, int Ls_out)
+{
+    extern __shared__ __align__(16) float sm[];
+    const PrepLayout P = prep_layout(DK, dv, L);
+    const int ldk = P.ldk, ldq = P.ldq;
+    double *gam = reinterpret_cast<double *>(sm);
+    float *Ks = sm + P.k, *Qs = sm + P.q, *Vs = sm + P.v;
+    float *M1 = sm + P.m1, *M2 = sm + P.m2, *Xs = sm + P.x, *Ys = sm + P.y;
+    float *ls = sm + P.lam, *bs = sm + P.beta;
+    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+    const int ci = blockIdx.x;
+    const long long bh = (long long)blockIdx.z * H + blockIdx.y;
+    const long long tok0 = bh * T + (long long)ci * kGC;
+    const int nv = min(kGC, T - ci * kGC);
+    const int cj = dv / 16;
+
+    // 1. the chunk's inputs, zero past T (a padded token has k = v = 0, beta = 0,
+    //    g = 0: its factor is the identity and it adds nothing)
+    for (int e = tid; e < kGC * DK; e += kGT) {
+        const int a = e / DK, r = e % DK;
+        const bool ok = a < nv;
+        Ks[a * ldk + r] = ok ? to_f32(k[tok0 * DK + e]) : 0.f;
+        Qs[a * ldq + r] = ok ? to_f32(q[tok0 * DK + e]) : 0.f;
+    }
+    for (int e = tid; e < kGC * dv; e += kGT) Vs[e] = e / dv < nv ? to_f32(v[tok0 * dv + e]) : 0.f;
+    for (int e = tid; e < kGC * L; e += kGT) ls[e] = e / L < nv ? lam[tok0 * L + e] : 0.f;
+    for (int e = tid; e < kGC * kLdm; e += kGT) Xs[e] = 0.f;
+    if (tid < kGC) bs[tid] = tid < nv ? beta[tok0 + tid] : 0.f;
+    if (tid < 32) {  // inclusive fp64 running sum of the gates, two tokens per lane
+        const int a0 = 2 * tid;
+        const double g0 = a0 < nv ? (double)g[tok0 + a0] : 0.0;
+        const double g1 = a0 + 1 < nv ? (double)g[tok0 + a0 + 1] : 0.0;
+        double s = g0 + g1;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const double y = __shfl_up_sync(0xffffffffu, s, off);
+            if (tid >= off) s += y;
+        }
+        gam[a0 + 1] = s;
+        gam[a0] = s - g1;
+    }
+    __syncthreads();
+
+    // 2. M1 = strict_lower(diag(beta) K K^T), M2 = inclusive_lower(Q K^T)
+    {
+        float ak[4][4], aq[4][4];
+        zero(ak);
+        zero(aq);
+        mm16<4, 4>(ak, Ks, ldk, 1, Ks, 1, ldk, DK, ty, tx);
+        mm16<4, 4>(aq, Qs, ldq, 1, Ks, 1, ldk, DK, ty, tx);
+#pragma unroll
+        for (int i = 0; i < 4; i++)
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                const int a = ty + 16 * i, b = tx + 16 * j;
+                M1[a * kLdm + b] = b < a ? bs[a] * ak[i][j] : 0.f;
+                M2[a * kLdm + b] = b <= a ? aq[i][j] : 0.f;
+            }
+    }
+    __syncthreads();
+
+    // 3. X = (I + M1)^{-1}: the four 16 x 16 diagonal blocks by forward
+    //    substitution (a lane per column, the column in registers), then the
+    //    blocks below the diagonal, one block diagonal at a time:
+    //    X_ij = -X_ii sum_{j <= m < i} M1_im X_mj
+    if (tid < 128 && (tid & 31) < 16) {
+        const int w = tid >> 5, l = tid & 31;
+        const float *Lw = M1 + 16 * w * kLdm + 16 * w;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; r++) {
+            float s = r == l ? 1.f : 0.f;
+#pragma unroll
+            for (int j = 0; j < r; j++) s = fmaf(-Lw[r * kLdm + j], x[j], s);
+            x[r] = s;
+        }
+#pragma unroll
+        for (int r = 0; r < 16; r++) Xs[(16 * w + r) * kLdm + 16 * w + l] = x[r];
+    }
+    __syncthreads();
+    {
+        const int r = tid >> 4, c = tid & 15;
+        for (int d = 1; d < 4; d++) {
+            for (int blk = 0; blk + d < 4; blk++) {
+                const int bi = blk + d, bj = blk;
+                float y = 0.f;
+                for (int m = bj; m < bi; m++)
+#pragma unroll
+                    for (int e = 0; e < 16; e++)
+                        y = fmaf(M1[(16 * bi + r) * kLdm + 16 * m + e], Xs[(16 * m + e) * kLdm + 16 * bj + c], y);
+                Ys[(blk * 16 + r) * 17 + c] = y;
+            }
+            __syncthreads();
+            for (int blk = 0; blk + d < 4; blk++) {
+                const int bi = blk + d, bj = blk;
+                float x = 0.f;
+#pragma unroll
+                for (int e = 0; e < 16; e++)
+                    x = fmaf(Xs[(16 * bi + r) * kLdm + 16 * bi + e], Ys[(blk * 16 + e) * 17 + c], x);
+                Xs[(16 * bi + r) * kLdm + 16 * bj + c] = -x;
+            }
+            __syncthreads();
+        }
+    }
+    // 4. T = X diag(beta), in place
+    for (int e = tid; e < kGC * kGC; e += kGT) {
+        const int a = e >> kGCBits, b = e & (kGC - 1);
+        Xs[a * kLdm + b] *= bs[b];
+    }
+    __syncthreads();
+
+    // 5. Cm = M2 T (lower triangular) into M1; the intra-chunk weights
+    //    lambda_a[l(a,s)] exp(gam_a - gam_s) Cm[a,s] into M2
+    {
+        float acc[4][4];
+        zero(acc);
+        mm16<4, 4>(acc, M2, kLdm, 1, Xs, kLdm, 1, kGC, ty, tx);
+        __syncthreads();  // every read of M1 (done) and M2 precedes the writes
+#pragma unroll
+        for (int i = 0; i < 4; i++)
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                const int a = ty + 16 * i, s = tx + 16 * j;
+                M1[a * kLdm + s] = acc[i][j];
+                float m = 0.f;
+                if (s <= a && a < nv) {
+                    const int lev = 32 - __clz(a ^ s);
+                    m = ls[a * L + lev] * expf((float)(gam[a] - gam[s])) * acc[i][j];
+                }
+                M2[a * kLdm + s] = m;
+            }
+    }
+    __syncthreads();
+
+    // 6. w^T = (T K)^T and qt^T = (diag(exp(gam)) (Q - Cm K))^T into the workspace
+    {
+        float *qt_ws = ws_qw + (bh * N + ci) * (2LL * DK * kGC);
+        float *w_ws = qt_ws + DK * kGC;
+        constexpr int RI = DK / 16;
+        float aw[RI][4], ac[RI][4];
+        zero(aw);
+        zero(ac);
+        mm16<RI, 4>(aw, Ks, 1, ldk, Xs, 1, kLdm, kGC, ty, tx);  // A(r, b) = K[b][r], B(b, a) = T[a][b]
+        mm16<RI, 4>(ac, Ks, 1, ldk, M1, 1, kLdm, kGC, ty, tx);  // B(b, a) = Cm[a][b]
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const int a = tx + 16 * j;
+            const float ea = expf((float)gam[a]);
+#pragma unroll
+            for (int i = 0; i < RI; i++) {
+                const int r = ty + 16 * i;
+                w_ws[r * kGC + a] = aw[i][j];
+                qt_ws[r * kGC + a] = ea * (Qs[a * ldq + r] - ac[i][j]);
+            }
+        }
+    }
+    // 7. intra-chunk output
+    {
+        float acc[4][8];
+        zero(acc);
+        mm16<4, 8>(acc, M2, kLdm, 1, Vs, dv, 1, kGC, ty, tx, cj);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const int a = ty + 16 * i;
+            if (a < nv) {
+#pragma unroll
+                for (int j = 0; j < 8; j++)
+                    if (j < cj) out[(tok0 + a) * dv + tx + 16 * j] = acc[i][j];
+            }
+        }
+    }
+    __syncthreads();  // M1 (Cm) and Qs are free
+
+    // 8. T' = T diag(exp(gam_{C-1} - gam)) into M1, U = T' V into Qs, H = K^T U
+    const double Gam = gam[kGC - 1];
+    for (int e = tid; e < kGC * kGC; e += kGT) {
+        const int a = e >> kGCBits, b = e & (kGC - 1);
+        M1[a * kLdm + b] = Xs[a * kLdm + b] * expf((float)(Gam - gam[b]));
+    }
+    __syncthreads();
+    auto kt_u = [&](int lo, int hi, float *dst) {
+        // U = T'[:, lo:hi] V[lo:hi, :] into Qs, then dst = K^T U (dk x dv)
+        {
+            float acc[4][8];
+            zero(acc);
+            mm16<4, 8>(acc, M1 + lo, kLdm, 1, Vs + lo * dv, dv, 1, hi - lo, ty, tx, cj);
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+#pragma unroll
+                for (int j = 0; j < 8; j++)
+                    if (j < cj) Qs[(ty + 16 * i) * ldq + tx + 16 * j] = acc[i][j];
+        }
+        __syncthreads();
+        constexpr int RI = DK / 16;
+        float acc[RI][8];
+        zero(acc);
+        mm16<RI, 8>(acc, Ks, 1, ldk, Qs, ldq, 1, kGC, ty, tx, cj);  // A(r, a) = K[a][r], B(a, c) = U[a][c]
+#pragma unroll
+        for (int i = 0; i < RI; i++)
+#pragma unroll
+            for (int j = 0; j < 8; j++)
+                if (j < cj) dst[(ty + 16 * i) * dv + tx + 16 * j] = acc[i][j];
+    };
+    kt_u(0, kGC, ws_h + (bh * N + ci) * (long long)DK * dv);
+    if (tid == 0) ws_gend[bh * N + ci] = expf((float)Gam);
+
+    // 9. after a ragged last chunk the sequence's low bits are buckets inside
+    //    it: slot j (bit j of T) holds K^T T'[:, B_j] V[B_j, :] over its tokens
+    if (state_out && ci == N - 1 && nv < kGC) {
+        for (int j = 0; j < kGCBits; j++) {
+            if (!((nv >> j) & 1)) continue;
+            const int hi = nv - (nv & ((1 << j) - 1)), lo = hi - (1 << j);
+            __syncthreads();  // Qs is reused
+            kt_u(lo, hi, state_out + ((bh * Ls_out + j) * DK) * (long long)dv);
+        }
+    }
+}
+
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async4(void *dst, const void *src, int src_bytes)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Shared memory of the scan kernel: states, W S rows, then one or two stages.
+struct ScanLayout {
+    size_t S, WS, stage, qw, kr, h, lam, gend, stage_bytes, bytes;
+};
+
+__host__ __device__ inline ScanLayout scan_layout(int dk, int NS, int nlv, int nst, int tin_bytes)
+{
+    ScanLayout Y;
+    Y.S = 0;                                                        // [NS][kGW][dk] fp32
+    Y.WS = Y.S + (size_t)NS * kGW * dk * 4;                         // [NS][64][kGW + 1] fp32
+    Y.stage = align_up(Y.WS + (size_t)NS * kGC * kLdws * 4, 16);
+    Y.qw = 0;                                                       // qt^T, w^T [2][dk][64] fp32
+    Y.kr = Y.qw + (size_t)2 * dk * kGC * 4;                         // K [64][dk] in the input type
+    Y.h = Y.kr + (size_t)kGC * dk * tin_bytes;                      // H slice [dk][kGW]
+    Y.lam = Y.h + (size_t)dk * kGW * 4;                             // chunk-level lambda [64][nlv]
+    Y.gend = Y.lam + (size_t)kGC * nlv * 4;
+    Y.stage_bytes = align_up(Y.gend + 16, 16);
+    Y.bytes = Y.stage + (size_t)nst * Y.stage_bytes;
+    return Y;
+}
+
+template <typename Tin, int DK>
+__global__ void __launch_bounds__(kGT)
+gdn_chunk_scan_kernel(const Tin *__restrict__ k, const float *__restrict__ lam, float *__restrict__ out,
+                      const float *__restrict__ ws_qw, const float *__restrict__ ws_h,
+                      const float *__restrict__ ws_gend, float *__restrict__ state_out, int T, int N, int H, int dv,
+                      int L, int Ls_out, int nst)
+{
+    extern __shared__ __align__(16) uint8_t smb[];
+    const int NS = bit_length_u32((uint32_t)N);  // chunk-level slots: slot m = level kGCBits + 1 + m
+    const int nlv = max(L - (kGCBits + 1), 0);
+    const ScanLayout Y = scan_layout(DK, NS, nlv, nst, (int)sizeof(Tin));
+    float *S = reinterpret_cast<float *>(smb + Y.S);
+    float *WS = reinterpret_cast<float *>(smb + Y.WS);
+    const int tid = threadIdx.x;
+    const int col0 = blockIdx.x * kGW;
+    const long long bh = (long long)blockIdx.z * H + blockIdx.y;
+    const bool ragged = (T % kGC) != 0;
+
+    auto stage_ptr = [&](int st) { return smb + Y.stage + (size_t)st * Y.stage_bytes; };
+    auto load = [&](int st, int ci) {
+        uint8_t *b = stage_ptr(st);
+        const int nvc = min(kGC, T - ci * kGC);
+        const float *qw = ws_qw + (bh * N + ci) * (2LL * DK * kGC);
+        for (int e = tid; e < 2 * DK * kGC / 4; e += kGT) cp_async16(b + Y.qw + 16 * e, qw + 4 * e, 16);
+        constexpr int cpr = DK * (int)sizeof(Tin) / 16;  // 16-byte pieces per key row
+        for (int e = tid; e < kGC * cpr; e += kGT) {
+            const int a = e / cpr, p = e % cpr;
+            const Tin *src = k + (bh * T + (long long)ci * kGC + min(a, nvc - 1)) * DK + p * (16 / (int)sizeof(Tin));
+            cp_async16(b + Y.kr + 16 * e, src, a < nvc ? 16 : 0);
+        }
+        const float *h = ws_h + (bh * N + ci) * (long long)DK * dv + col0;
+        for (int e = tid; e < DK * kGW / 4; e += kGT) {
+            const int r = e / (kGW / 4), p = e % (kGW / 4);
+            cp_async16(b + Y.h + 16 * e, h + (long long)r * dv + 4 * p, 16);
+        }
+        for (int e = tid; e < kGC * nlv; e += kGT) {
+            const int a = e / nlv, m = e % nlv;
+            const float *src = lam + (bh * T + (long long)ci * kGC + min(a, nvc - 1)) * L + kGCBits + 1 + m;
+            cp_async4(b + Y.lam + 4 * e, src, a < nvc ? 4 : 0);
+        }
+        if (tid == 0) cp_async4(b + Y.gend, ws_gend + bh * N + ci, 4);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+
+    if (nst == 2) load(0, 0);
+    for (int ci = 0; ci < N; ci++) {
+        const int st = nst == 2 ? (ci & 1) : 0;
+        if (nst == 1) load(0, ci);
+        cp_async_wait_all();
+        __syncthreads();  // stage ci is visible; chunk ci-1 is finished with the other stage
+        if (nst == 2 && ci + 1 < N) load((ci + 1) & 1, ci + 1);
+        const uint8_t *b = stage_ptr(st);
+        const float *QtT = reinterpret_cast<const float *>(b + Y.qw);
+        const float *WT = QtT + DK * kGC;
+        const Tin *Kr = reinterpret_cast<const Tin *>(b + Y.kr);
+        const float *Hs = reinterpret_cast<const float *>(b + Y.h);
+        const float *lamc = reinterpret_cast<const float *>(b + Y.lam);
+        const float ge = *reinterpret_cast<const float *>(b + Y.gend);
+        const uint32_t live = (uint32_t)ci;  // slot m is live at chunk ci iff bit m of ci is set
+
+        // A. read-out of the live states into the output, and W S of each
+        if (live) {
+            const int a = tid & (kGC - 1), cg = tid >> kGCBits;  // columns cg and cg + 4
+            float o0 = 0.f, o1 = 0.f;
+            uint32_t rem = live;
+            while (rem) {
+                int mm[4];
+                int nu = 0;
+#pragma unroll
+                for (int u = 0; u < 4; u++) {
+                    mm[u] = rem ? __ffs((int)rem) - 1 : 0;
+                    if (rem) { nu++; rem &= rem - 1; }
+                }
+                float po[4][2], pw[4][2];
+#pragma unroll
+                for (int u = 0; u < 4; u++) po[u][0] = po[u][1] = pw[u][0] = pw[u][1] = 0.f;
+#pragma unroll 4
+                for (int r = 0; r < DK; r++) {
+                    const float qv = QtT[r * kGC + a], wv = WT[r * kGC + a];
+#pragma unroll
+                    for (int u = 0; u < 4; u++) {
+                        if (u < nu) {
+                            const float s0 = S[(mm[u] * kGW + cg) * DK + r];
+                            const float s1 = S[(mm[u] * kGW + cg + 4) * DK + r];
+                            po[u][0] = fmaf(qv, s0, po[u][0]);
+                            po[u][1] = fmaf(qv, s1, po[u][1]);
+                            pw[u][0] = fmaf(wv, s0, pw[u][0]);
+                            pw[u][1] = fmaf(wv, s1, pw[u][1]);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; u++) {
+                    if (u < nu) {
+                        const float lw = lamc[a * nlv + mm[u]];
+                        o0 = fmaf(lw, po[u][0], o0);
+                        o1 = fmaf(lw, po[u][1], o1);
+                        WS[(mm[u] * kGC + a) * kLdws + cg] = pw[u][0];
+                        WS[(mm[u] * kGC + a) * kLdws + cg + 4] = pw[u][1];
+                    }
+                }
+            }
+            if (a < T - ci * kGC) {
+                float *po = out + (bh * T + (long long)ci * kGC + a) * dv + col0 + cg;
+                po[0] += o0;
+                po[4] += o1;
+            }
+        }
+        __syncthreads();
+
+        // B. transition of the live states, then the fold into slot ctz(ci+1)
+        {
+            constexpr int ncg = kGT / DK;
+            const int r = tid % DK, cg = tid / DK;
+            const bool fold = ci + 1 < N || !ragged;  // a ragged last chunk stays out of the chunk levels
+            const int m0 = ctz_u32((uint32_t)ci + 1u);
+            for (int c = cg; c < kGW; c += ncg) {
+                uint32_t rem = live;
+                while (rem) {
+                    int mm[4];
+                    int nu = 0;
+#pragma unroll
+                    for (int u = 0; u < 4; u++) {
+                        mm[u] = rem ? __ffs((int)rem) - 1 : 0;
+                        if (rem) { nu++; rem &= rem - 1; }
+                    }
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+                    for (int a = 0; a < kGC; a++) {
+                        const float kv = to_f32(Kr[a * DK + r]);
+#pragma unroll
+                        for (int u = 0; u < 4; u++)
+                            if (u < nu) acc[u] = fmaf(kv, WS[(mm[u] * kGC + a) * kLdws + c], acc[u]);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; u++) {
+                        if (u < nu) {
+                            float *s = S + (mm[u] * kGW + c) * DK + r;
+                            *s = ge * (*s - acc[u]);
+                        }
+                    }
+                }
+                if (fold) {
+                    float s = Hs[r * kGW + c];
+                    for (int m = 0; m < m0; m++) s += S[(m * kGW + c) * DK + r];
+                    S[(m0 * kGW + c) * DK + r] = s;
+                }
+            }
+        }
+        if (nst == 1) __syncthreads();  // the single stage is reloaded next
+    }
+
+    // the state after the sequence in the decode layout (slot j = level j + 1,
+    // live iff bit j of T); the slots below kGCBits that are live come from the
+    // prep kernel's last chunk
+    if (state_out) {
+        __syncthreads();
+        const long long nfull = T >> kGCBits;
+        for (int j = 0; j < Ls_out; j++) {
+            if (j < kGCBits && ((T >> j) & 1)) continue;
+            const int m = j - kGCBits;
+            const bool on = m >= 0 && m < NS && ((nfull >> m) & 1);
+            for (int e = tid; e < DK * kGW; e += kGT) {
+                const int r = e % DK, c = e / DK;
+                state_out[((bh * Ls_out + j) * DK + r) * (long long)dv + col0 + c] =
+                    on ? S[(m * kGW + c) * DK + r] : 0.f;
+            }
+        }
+    }
+}
+
+int scan_stages(int dk, int NS, int nlv, int tin_bytes)
+{
+    return scan_layout(dk, NS, nlv, 2, tin_bytes).bytes <= kMaxSmem ? 2 : 1;
+}
+
+template <typename Tin, int DK>
+cudaError_t launch_chunk_dk(const GdnFwdArgs &A)
+{
+    const int N = (A.T + kGC - 1) / kGC;
+    const long long BH = (long long)A.B * A.H;
+    const WsLayout W = ws_layout(BH, N, DK, A.dv);
+    uint8_t *ws = (uint8_t *)A.workspace;
+    float *ws_qw = (float *)(ws + W.qw), *ws_h = (float *)(ws + W.h), *ws_gend = (float *)(ws + W.gend);
+    cudaStream_t s = (cudaStream_t)A.stream;
+
+    const size_t psmem = prep_layout(DK, A.dv, A.L).floats * sizeof(float);
+    auto prep = gdn_chunk_prep_kernel<Tin, DK>;
+    cudaError_t e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
+    if (e != cudaSuccess) return e;
+    prep<<<dim3(N, A.H, A.B), kGT, psmem, s>>>((const Tin *)A.q, (const Tin *)A.k, (const Tin *)A.v, A.g, A.beta,
+                                                A.lam, A.out, ws_qw, ws_h, ws_gend, A.state_out, A.T, N, A.H, A.dv,
+                                                A.L, A.Ls_out);
+    e = cudaPeekAtLastError();
+    if (e != cudaSuccess) return e;
+
+    const int NS = bit_length_u32((uint32_t)N);
+    const int nlv = A.L - (kGCBits + 1) > 0 ? A.L - (kGCBits + 1) : 0;
+    const int nst = scan_stages(DK, NS, nlv, (int)sizeof(Tin));
+    const size_t ssmem = scan_layout(DK, NS, nlv, nst, (int)sizeof(Tin)).bytes;
+    auto scan = gdn_chunk_scan_kernel<Tin, DK>;
+    e = cudaFuncSetAttribute(scan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssmem);
+    if (e != cudaSuccess) return e;
+    scan<<<dim3(A.dv / kGW, A.H, A.B), kGT, ssmem, s>>>((const Tin *)A.k, A.lam, A.out, ws_qw, ws_h, ws_gend,
+                                                         A.state_out, A.T, N, A.H, A.dv, A.L, A.Ls_out, nst);
+    return cudaPeekAtLastError();
+}
+
+template <typename Tin>
+cudaError_t launch_chunk(const GdnFwdArgs &A)
+{
+    switch (A.dk) {
+    case 16: return launch_chunk_dk<Tin, 16>(A);
+    case 32: return launch_chunk_dk<Tin, 32>(A);
+    case 64: return launch_chunk_dk<Tin, 64>(A);
+    default: return launch_chunk_dk<Tin, 128>(A);
+    }
+}
+
+}  // namespace
+
+size_t gdn_fwd_workspace_bytes(int B, int H, int T, int dk, int dv)
+{
+    if ((long long)B * H * T <= 0) return 0;
+    return ws_layout((long long)B * H, (T + kGC - 1) / kGC, dk, dv).bytes;
+}
+
+bool gdn_fwd_fits(int T, int dk, int dv, int L, int tin_bytes)
+{
+    const int N = (T + kGC - 1) / kGC;
+    const int NS = bit_length_u32((uint32_t)N);
+    const int nlv = L - (kGCBits + 1) > 0 ? L - (kGCBits + 1) : 0;
+    return prep_layout(dk, dv, L).floats * sizeof(float) <= kMaxSmem &&
+           scan_layout(dk, NS, nlv, 1, tin_bytes).bytes <= kMaxSmem;
+}
+
+cudaError_t gdn_fwd(const GdnFwdArgs &A)
+{
+    return A.in_dt == LLA_F32 ? launch_chunk<float>(A) : launch_chunk<__nv_bfloat16>(A);
+}
+
+}  // namespace lla

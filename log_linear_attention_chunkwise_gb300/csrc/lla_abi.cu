@@ -225,24 +225,35 @@ lla_status lla_bwd(const void *q, const void *k, const void *v, const float *g, 
     return lla::bwd(A) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
 }
 
+size_t lla_gdn_fwd_workspace_bytes(int B, int H, int T, int dk, int dv)
+{
+    if (B <= 0 || H <= 0 || T <= 0 || !is_dim(dk) || !is_dim(dv) || T > (1 << 24)) return 0;
+    return lla::gdn_fwd_workspace_bytes(B, H, T, dk, dv);
+}
+
 lla_status lla_gdn_fwd(const void *q, const void *k, const void *v, const float *g, const float *beta,
                        const float *lambda, float *out, float *state_out, int B, int H, int T, int dk,
-                       int dv, int Ls_out, lla_dtype in_dt, void *stream)
+                       int dv, int Ls_out, lla_dtype in_dt, void *workspace, size_t workspace_bytes,
+                       void *stream)
 {
     if (B < 0 || H < 0 || T < 0) return LLA_ERR_INVALID_ARGUMENT;
     if (in_dt != LLA_F32 && in_dt != LLA_BF16) return LLA_ERR_INVALID_ARGUMENT;
-    if (!is_dim(dk) || !is_dim(dv) || T > (1 << 16) || B > 65535 || H > 65535)
+    if (!is_dim(dk) || !is_dim(dv) || T > (1 << 24) || B > 65535 || H > 65535)
         return LLA_ERR_UNSUPPORTED_SHAPE;
     const int need_slots = T > 0 ? bit_length_u32((uint32_t)T) : 0;
     if (state_out && (Ls_out < need_slots || Ls_out > 40)) return LLA_ERR_UNSUPPORTED_SHAPE;
     if ((long long)B * H * T == 0) return LLA_OK;
-    if (!q || !k || !v || !g || !beta || !lambda || !out) return LLA_ERR_INVALID_ARGUMENT;
     const int L = lla_num_levels(T);
-    if (lla::gdn_fwd_smem_bytes(T, dk, L) > 227 * 1024) return LLA_ERR_UNSUPPORTED_SHAPE;
+    const int tin_bytes = in_dt == LLA_F32 ? 4 : 2;
+    if (!lla::gdn_fwd_fits(T, dk, dv, L, tin_bytes)) return LLA_ERR_UNSUPPORTED_SHAPE;
+    if (!q || !k || !v || !g || !beta || !lambda || !out || !workspace) return LLA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(k) || ((uintptr_t)workspace & 255u) != 0 ||
+        workspace_bytes < lla::gdn_fwd_workspace_bytes(B, H, T, dk, dv))
+        return LLA_ERR_INVALID_ARGUMENT;
     lla::GdnFwdArgs A;
     A.q = q; A.k = k; A.v = v; A.g = g; A.beta = beta; A.lam = lambda; A.out = out;
     A.state_out = state_out; A.B = B; A.H = H; A.T = T; A.dk = dk; A.dv = dv; A.L = L;
-    A.Ls_out = state_out ? Ls_out : 0; A.in_dt = in_dt; A.stream = stream;
+    A.Ls_out = state_out ? Ls_out : 0; A.in_dt = in_dt; A.workspace = workspace; A.stream = stream;
     return lla::gdn_fwd(A) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
 }
 

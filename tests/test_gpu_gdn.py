@@ -35,12 +35,15 @@ def run_fwd(cfg, state_Ls=0):
 
 
 @pytest.mark.parametrize("B,H,T,dk,dv,dtype", [
-    (1, 2, 64, 16, 16, torch.float32),
-    (2, 1, 100, 32, 64, torch.float32),     # T not a power of two
+    (1, 2, 64, 16, 16, torch.float32),      # one full chunk
+    (2, 1, 100, 32, 64, torch.float32),     # a ragged second chunk
     (1, 1, 1, 64, 32, torch.float32),       # one token: only the diagonal
+    (1, 1, 65, 64, 16, torch.float32),      # one token past the first chunk
     (1, 2, 333, 64, 64, torch.bfloat16),
-    (1, 1, 256, 128, 128, torch.bfloat16),  # 8-column CTAs
+    (1, 1, 256, 128, 128, torch.bfloat16),
     (1, 1, 512, 128, 16, torch.float32),
+    (1, 1, 1024, 16, 128, torch.bfloat16),  # 16 chunks: four chunk levels live at once
+    (2, 1, 1000, 32, 32, torch.float32),
 ])
 def test_gdn_fwd_matches_oracle(B, H, T, dk, dv, dtype):
     cfg = W.small_fwd_config(B, H, T, dk, dv, 16, dtype, seed=T + dv)
@@ -57,6 +60,37 @@ def test_gdn_fwd_lambda_one_is_gated_deltanet():
     out = binding.gdn_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["lam"])
     torch.cuda.synchronize()
     check(out, oracle.gdn_base(x["q"], x["k"], x["v"], x["g"], x["beta"]), "lambda=1")
+
+
+@pytest.mark.parametrize("T,dk,dv", [(45, 32, 32), (128, 32, 32), (200, 64, 32), (448, 16, 64), (513, 32, 16)])
+def test_gdn_final_state_matches_the_oracle(T, dk, dv):
+    """The state after the sequence (decode layout, every slot compared, the
+    dead ones zero) against the oracle's decode steps from the empty state:
+    chunk-level slots from the scan, the low-bit slots of a ragged end from
+    the last chunk's buckets."""
+    B, H = 1, 2
+    cfg = W.small_fwd_config(B, H, T, dk, dv, 16, torch.float32, seed=T + 5)
+    x = W.make_gdn_inputs(cfg)
+    Ls = T.bit_length() + 1
+    d = {n: t.cuda() for n, t in x.items()}
+    out, S = binding.gdn_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["lam"], state_Ls=Ls)
+    torch.cuda.synchronize()
+    check(out, oracle.gdn_naive(x["q"], x["k"], x["v"], x["g"], x["beta"], x["lam"]), f"T{T} out")
+    S_ref = np.zeros((B, H, Ls, dk, dv))
+    q, k, v, g, beta, lam = (x[n].double().numpy() for n in ("q", "k", "v", "g", "beta", "lam"))
+    for t in range(T):
+        lam_t = np.zeros((B, H, Ls + 1))
+        lam_t[..., :lam.shape[-1]] = lam[:, :, t]
+        oracle.gdn_decode_step(S_ref, q[:, :, t], k[:, :, t], v[:, :, t], g[:, :, t], beta[:, :, t], lam_t,
+                               np.full((B,), t))
+    S = S.cpu().double().numpy()
+    live = [i for i in range(Ls) if (T >> i) & 1]
+    # the live slots as one state: a deep slot can decay below fp32's range
+    # (1e-70 in fp64 at T = 448), so its error is measured against the state
+    check(S[:, :, live], S_ref[:, :, live], f"T{T} live slots {live}")
+    for i in range(Ls):
+        if i not in live:
+            assert not S[:, :, i].any(), f"T{T} dead slot {i} not zero"
 
 
 def test_gdn_workload_sampled_heads():
