@@ -35,28 +35,64 @@ constexpr int kGCBits = 6;     // log2(kGC)
 constexpr int kGT = 256;       // threads of both kernels
 constexpr int kLdm = kGC + 1;  // row stride of the 64 x 64 matrices in shared memory
 constexpr int kGW = 8;         // value columns of a scan CTA
-constexpr int kLdws = kGW + 1; // row stride of the scan's W S rows
 constexpr size_t kMaxSmem = 227 * 1024;  // dynamic shared memory of one CTA
 
 // acc[i][j] += sum_{k < K} A(ty + 16 i, k) B(k, tx + 16 j), A(r, k) = A[r ar + k ak],
-// B(k, c) = B[k bk + c bc]; columns j >= cj are skipped.
-template <int RI, int CJ>
+// B(k, c) = B[k bk + c bc]; columns j >= cj are skipped.  The thread's rows
+// and columns fall one in each 16-wide block, so a triangular operand zeroes
+// whole (block, block) pairs, which MODE skips at compile time:
+//   kFull      every product;
+//   kOutLower  the result is kept below the block diagonal only: j > i skipped;
+//   kALower    A(r, k) = 0 for k > r (K = 64 in blocks of 16: block kb skips rows i < kb);
+//   kBUpper    B(k, c) = 0 for k > c (block kb skips columns j < kb).
+enum { kFull = 0, kOutLower = 1, kALower = 2, kBUpper = 3 };
+
+template <int RI, int CJ, int MODE = kFull>
 __device__ __forceinline__ void mm16(float (&acc)[RI][CJ], const float *A, int ar, int ak, const float *B, int bk,
                                      int bc, int K, int ty, int tx, int cj = CJ)
 {
     const float *pa = A + ty * ar;
     const float *pb = B + tx * bc;
+    if constexpr (MODE == kALower || MODE == kBUpper) {
+#pragma unroll
+        for (int kb = 0; kb < 4; kb++) {
 #pragma unroll 4
-    for (int k = 0; k < K; k++) {
-        float a[RI], b[CJ];
+            for (int kk = 0; kk < 16; kk++) {
+                const int k = 16 * kb + kk;
+                float a[RI], b[CJ];
 #pragma unroll
-        for (int i = 0; i < RI; i++) a[i] = pa[16 * i * ar + k * ak];
+                for (int i = 0; i < RI; i++)
+                    a[i] = (MODE == kALower && i < kb) ? 0.f : pa[16 * i * ar + k * ak];
 #pragma unroll
-        for (int j = 0; j < CJ; j++) b[j] = j < cj ? pb[k * bk + 16 * j * bc] : 0.f;
+                for (int j = 0; j < CJ; j++)
+                    b[j] = ((MODE == kBUpper && j < kb) || j >= cj) ? 0.f : pb[k * bk + 16 * j * bc];
 #pragma unroll
-        for (int i = 0; i < RI; i++)
+                for (int i = 0; i < RI; i++) {
+                    if (MODE == kALower && i < kb) continue;
 #pragma unroll
-            for (int j = 0; j < CJ; j++) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+                    for (int j = 0; j < CJ; j++) {
+                        if (MODE == kBUpper && j < kb) continue;
+                        acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+                    }
+                }
+            }
+        }
+    } else {
+#pragma unroll 4
+        for (int k = 0; k < K; k++) {
+            float a[RI], b[CJ];
+#pragma unroll
+            for (int i = 0; i < RI; i++) a[i] = pa[16 * i * ar + k * ak];
+#pragma unroll
+            for (int j = 0; j < CJ; j++) b[j] = j < cj ? pb[k * bk + 16 * j * bc] : 0.f;
+#pragma unroll
+            for (int i = 0; i < RI; i++)
+#pragma unroll
+                for (int j = 0; j < CJ; j++) {
+                    if (MODE == kOutLower && j > i) continue;
+                    acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+                }
+        }
     }
 }
 
@@ -93,7 +129,8 @@ __host__ __device__ inline PrepLayout prep_layout(int dk, int dv, int L)
     return P;
 }
 
-// Workspace: [BH][N][2][dk][64] (qt^T then w^T), [BH][N][dk][dv] (H), [BH][N] exp(gam_{C-1}).
+// Workspace: [BH][N][dk][64][2] ((qt, w) pairs by row of q~^T and w^T), [BH][N][dk][dv] (H),
+// [BH][N] exp(gam_{C-1}).
 struct WsLayout {
     size_t qw, h, gend, bytes;
 };
@@ -162,8 +199,8 @@ gdn_chunk_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, cons
         float ak[4][4], aq[4][4];
         zero(ak);
         zero(aq);
-        mm16<4, 4>(ak, Ks, ldk, 1, Ks, 1, ldk, DK, ty, tx);
-        mm16<4, 4>(aq, Qs, ldq, 1, Ks, 1, ldk, DK, ty, tx);
+        mm16<4, 4, kOutLower>(ak, Ks, ldk, 1, Ks, 1, ldk, DK, ty, tx);
+        mm16<4, 4, kOutLower>(aq, Qs, ldq, 1, Ks, 1, ldk, DK, ty, tx);
 #pragma unroll
         for (int i = 0; i < 4; i++)
 #pragma unroll
@@ -230,7 +267,7 @@ gdn_chunk_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, cons
     {
         float acc[4][4];
         zero(acc);
-        mm16<4, 4>(acc, M2, kLdm, 1, Xs, kLdm, 1, kGC, ty, tx);
+        mm16<4, 4, kALower>(acc, M2, kLdm, 1, Xs, kLdm, 1, kGC, ty, tx);
         __syncthreads();  // every read of M1 (done) and M2 precedes the writes
 #pragma unroll
         for (int i = 0; i < 4; i++)
@@ -248,16 +285,15 @@ gdn_chunk_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, cons
     }
     __syncthreads();
 
-    // 6. w^T = (T K)^T and qt^T = (diag(exp(gam)) (Q - Cm K))^T into the workspace
+    // 6. (qt, w) pairs, [r][a][2]: qt^T = (diag(exp(gam)) (Q - Cm K))^T and w^T = (T K)^T
     {
-        float *qt_ws = ws_qw + (bh * N + ci) * (2LL * DK * kGC);
-        float *w_ws = qt_ws + DK * kGC;
+        float2 *qw_ws = reinterpret_cast<float2 *>(ws_qw + (bh * N + ci) * (2LL * DK * kGC));
         constexpr int RI = DK / 16;
         float aw[RI][4], ac[RI][4];
         zero(aw);
         zero(ac);
-        mm16<RI, 4>(aw, Ks, 1, ldk, Xs, 1, kLdm, kGC, ty, tx);  // A(r, b) = K[b][r], B(b, a) = T[a][b]
-        mm16<RI, 4>(ac, Ks, 1, ldk, M1, 1, kLdm, kGC, ty, tx);  // B(b, a) = Cm[a][b]
+        mm16<RI, 4, kBUpper>(aw, Ks, 1, ldk, Xs, 1, kLdm, kGC, ty, tx);  // A(r, b) = K[b][r], B(b, a) = T[a][b]
+        mm16<RI, 4, kBUpper>(ac, Ks, 1, ldk, M1, 1, kLdm, kGC, ty, tx);  // B(b, a) = Cm[a][b]
 #pragma unroll
         for (int j = 0; j < 4; j++) {
             const int a = tx + 16 * j;
@@ -265,8 +301,7 @@ gdn_chunk_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, cons
 #pragma unroll
             for (int i = 0; i < RI; i++) {
                 const int r = ty + 16 * i;
-                w_ws[r * kGC + a] = aw[i][j];
-                qt_ws[r * kGC + a] = ea * (Qs[a * ldq + r] - ac[i][j]);
+                qw_ws[r * kGC + a] = make_float2(ea * (Qs[a * ldq + r] - ac[i][j]), aw[i][j]);
             }
         }
     }
@@ -274,7 +309,7 @@ gdn_chunk_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, cons
     {
         float acc[4][8];
         zero(acc);
-        mm16<4, 8>(acc, M2, kLdm, 1, Vs, dv, 1, kGC, ty, tx, cj);
+        mm16<4, 8, kALower>(acc, M2, kLdm, 1, Vs, dv, 1, kGC, ty, tx, cj);
 #pragma unroll
         for (int i = 0; i < 4; i++) {
             const int a = ty + 16 * i;
@@ -299,7 +334,10 @@ gdn_chunk_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, cons
         {
             float acc[4][8];
             zero(acc);
-            mm16<4, 8>(acc, M1 + lo, kLdm, 1, Vs + lo * dv, dv, 1, hi - lo, ty, tx, cj);
+            if (lo == 0 && hi == kGC)
+                mm16<4, 8, kALower>(acc, M1, kLdm, 1, Vs, dv, 1, kGC, ty, tx, cj);
+            else
+                mm16<4, 8>(acc, M1 + lo, kLdm, 1, Vs + lo * dv, dv, 1, hi - lo, ty, tx, cj);
 #pragma unroll
             for (int i = 0; i < 4; i++)
 #pragma unroll
@@ -349,24 +387,102 @@ __device__ __forceinline__ void cp_async4(void *dst, const void *src, int src_by
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Shared memory of the scan kernel: states, W S rows, then one or two stages.
+// State and W S rows hold the CTA's 8 columns at a stride of 10 floats, so a
+// float2 per lane over consecutive rows touches distinct banks.
+constexpr int kSld = 10;
+
 struct ScanLayout {
-    size_t S, WS, stage, qw, kr, h, lam, gend, stage_bytes, bytes;
+    size_t S, WS, stage, qw, kr, h, o, lam, gend, stage_bytes, bytes;
 };
 
 __host__ __device__ inline ScanLayout scan_layout(int dk, int NS, int nlv, int nst, int tin_bytes)
 {
     ScanLayout Y;
-    Y.S = 0;                                                        // [NS][kGW][dk] fp32
-    Y.WS = Y.S + (size_t)NS * kGW * dk * 4;                         // [NS][64][kGW + 1] fp32
-    Y.stage = align_up(Y.WS + (size_t)NS * kGC * kLdws * 4, 16);
-    Y.qw = 0;                                                       // qt^T, w^T [2][dk][64] fp32
+    Y.S = 0;                                                        // [NS][dk][kSld] fp32
+    Y.WS = Y.S + (size_t)NS * dk * kSld * 4;                        // [NS][64][kSld] fp32
+    Y.stage = align_up(Y.WS + (size_t)NS * kGC * kSld * 4, 16);
+    Y.qw = 0;                                                       // (qt, w) pairs [dk][64][2] fp32
     Y.kr = Y.qw + (size_t)2 * dk * kGC * 4;                         // K [64][dk] in the input type
     Y.h = Y.kr + (size_t)kGC * dk * tin_bytes;                      // H slice [dk][kGW]
-    Y.lam = Y.h + (size_t)dk * kGW * 4;                             // chunk-level lambda [64][nlv]
+    Y.o = Y.h + (size_t)dk * kGW * 4;                               // output slice [64][kGW]
+    Y.lam = Y.o + (size_t)kGC * kGW * 4;                            // chunk-level lambda [64][nlv]
     Y.gend = Y.lam + (size_t)kGC * nlv * 4;
     Y.stage_bytes = align_up(Y.gend + 16, 16);
     Y.bytes = Y.stage + (size_t)nst * Y.stage_bytes;
     return Y;
+}
+
+// Up to four live slots mm[0..NU): with a = the thread's row and cp its column
+// pair, po[u] = (qt_a . S_u[:, cp]) and pw[u] = (w_a . S_u[:, cp]).
+template <int NU, int DK>
+__device__ __forceinline__ void scan_readout(const float2 *__restrict__ QW, const float *__restrict__ S,
+                                             const int (&mm)[4], int a, int cp, float2 (&po)[4], float2 (&pw)[4])
+{
+    const float *sp[NU];
+#pragma unroll
+    for (int u = 0; u < NU; u++) {
+        sp[u] = S + mm[u] * DK * kSld + 2 * cp;
+        po[u] = pw[u] = make_float2(0.f, 0.f);
+    }
+#pragma unroll 8
+    for (int r = 0; r < DK; r++) {
+        const float2 qw = QW[r * kGC + a];
+#pragma unroll
+        for (int u = 0; u < NU; u++) {
+            const float2 sv = *reinterpret_cast<const float2 *>(sp[u] + r * kSld);
+            po[u].x = fmaf(qw.x, sv.x, po[u].x);
+            po[u].y = fmaf(qw.x, sv.y, po[u].y);
+            pw[u].x = fmaf(qw.y, sv.x, pw[u].x);
+            pw[u].y = fmaf(qw.y, sv.y, pw[u].y);
+        }
+    }
+}
+
+// S_u[r, cp] <- ge (S_u[r, cp] - sum_a K[a][r] (W S_u)[a, cp]) for the live slots mm[0..NU).
+template <int NU, int DK, typename Tin>
+__device__ __forceinline__ void scan_transition(const Tin *__restrict__ Kr, const float *__restrict__ WS, float *S,
+                                                const int (&mm)[4], int r, int cp, float ge)
+{
+    const float *wp[NU];
+    float2 acc[NU];
+#pragma unroll
+    for (int u = 0; u < NU; u++) {
+        wp[u] = WS + mm[u] * kGC * kSld + 2 * cp;
+        acc[u] = make_float2(0.f, 0.f);
+    }
+#pragma unroll 8
+    for (int a = 0; a < kGC; a++) {
+        const float kv = to_f32(Kr[a * DK + r]);
+#pragma unroll
+        for (int u = 0; u < NU; u++) {
+            const float2 w = *reinterpret_cast<const float2 *>(wp[u] + a * kSld);
+            acc[u].x = fmaf(kv, w.x, acc[u].x);
+            acc[u].y = fmaf(kv, w.y, acc[u].y);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < NU; u++) {
+        float2 *sp = reinterpret_cast<float2 *>(S + (mm[u] * DK + r) * kSld + 2 * cp);
+        float2 x = *sp;
+        x.x = ge * (x.x - acc[u].x);
+        x.y = ge * (x.y - acc[u].y);
+        *sp = x;
+    }
+}
+
+// The next (up to) four live slots of rem, lowest first; returns how many.
+__device__ __forceinline__ int take_slots(uint32_t &rem, int (&mm)[4])
+{
+    int nu = 0;
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+        mm[u] = rem ? __ffs((int)rem) - 1 : mm[0];
+        if (rem) {
+            nu = u + 1;
+            rem &= rem - 1;
+        }
+    }
+    return nu;
 }
 
 template <typename Tin, int DK>
@@ -391,12 +507,13 @@ gdn_chunk_scan_kernel(const Tin *__restrict__ k, const float *__restrict__ lam, 
     auto load = [&](int st, int ci) {
         uint8_t *b = stage_ptr(st);
         const int nvc = min(kGC, T - ci * kGC);
+        const long long row0 = bh * T + (long long)ci * kGC;
         const float *qw = ws_qw + (bh * N + ci) * (2LL * DK * kGC);
         for (int e = tid; e < 2 * DK * kGC / 4; e += kGT) cp_async16(b + Y.qw + 16 * e, qw + 4 * e, 16);
         constexpr int cpr = DK * (int)sizeof(Tin) / 16;  // 16-byte pieces per key row
         for (int e = tid; e < kGC * cpr; e += kGT) {
             const int a = e / cpr, p = e % cpr;
-            const Tin *src = k + (bh * T + (long long)ci * kGC + min(a, nvc - 1)) * DK + p * (16 / (int)sizeof(Tin));
+            const Tin *src = k + (row0 + min(a, nvc - 1)) * DK + p * (16 / (int)sizeof(Tin));
             cp_async16(b + Y.kr + 16 * e, src, a < nvc ? 16 : 0);
         }
         const float *h = ws_h + (bh * N + ci) * (long long)DK * dv + col0;
@@ -404,10 +521,15 @@ gdn_chunk_scan_kernel(const Tin *__restrict__ k, const float *__restrict__ lam, 
             const int r = e / (kGW / 4), p = e % (kGW / 4);
             cp_async16(b + Y.h + 16 * e, h + (long long)r * dv + 4 * p, 16);
         }
+        if (ci > 0) {  // the output slice the read-out adds to (chunk 0 has nothing to read out)
+            for (int e = tid; e < kGC * kGW / 4; e += kGT) {
+                const int a = e / (kGW / 4), p = e % (kGW / 4);
+                cp_async16(b + Y.o + 16 * e, out + (row0 + min(a, nvc - 1)) * dv + col0 + 4 * p, a < nvc ? 16 : 0);
+            }
+        }
         for (int e = tid; e < kGC * nlv; e += kGT) {
             const int a = e / nlv, m = e % nlv;
-            const float *src = lam + (bh * T + (long long)ci * kGC + min(a, nvc - 1)) * L + kGCBits + 1 + m;
-            cp_async4(b + Y.lam + 4 * e, src, a < nvc ? 4 : 0);
+            cp_async4(b + Y.lam + 4 * e, lam + (row0 + min(a, nvc - 1)) * L + kGCBits + 1 + m, a < nvc ? 4 : 0);
         }
         if (tid == 0) cp_async4(b + Y.gend, ws_gend + bh * N + ci, 4);
         asm volatile("cp.async.commit_group;" ::: "memory");
@@ -421,100 +543,69 @@ gdn_chunk_scan_kernel(const Tin *__restrict__ k, const float *__restrict__ lam, 
         __syncthreads();  // stage ci is visible; chunk ci-1 is finished with the other stage
         if (nst == 2 && ci + 1 < N) load((ci + 1) & 1, ci + 1);
         const uint8_t *b = stage_ptr(st);
-        const float *QtT = reinterpret_cast<const float *>(b + Y.qw);
-        const float *WT = QtT + DK * kGC;
+        const float2 *QW = reinterpret_cast<const float2 *>(b + Y.qw);
         const Tin *Kr = reinterpret_cast<const Tin *>(b + Y.kr);
         const float *Hs = reinterpret_cast<const float *>(b + Y.h);
+        const float *Os = reinterpret_cast<const float *>(b + Y.o);
         const float *lamc = reinterpret_cast<const float *>(b + Y.lam);
         const float ge = *reinterpret_cast<const float *>(b + Y.gend);
         const uint32_t live = (uint32_t)ci;  // slot m is live at chunk ci iff bit m of ci is set
 
         // A. read-out of the live states into the output, and W S of each
         if (live) {
-            const int a = tid & (kGC - 1), cg = tid >> kGCBits;  // columns cg and cg + 4
-            float o0 = 0.f, o1 = 0.f;
+            const int a = tid & (kGC - 1), cp = tid >> kGCBits;  // row, column pair
+            float2 o = *reinterpret_cast<const float2 *>(Os + a * kGW + 2 * cp);
             uint32_t rem = live;
             while (rem) {
                 int mm[4];
-                int nu = 0;
-#pragma unroll
-                for (int u = 0; u < 4; u++) {
-                    mm[u] = rem ? __ffs((int)rem) - 1 : 0;
-                    if (rem) { nu++; rem &= rem - 1; }
-                }
-                float po[4][2], pw[4][2];
-#pragma unroll
-                for (int u = 0; u < 4; u++) po[u][0] = po[u][1] = pw[u][0] = pw[u][1] = 0.f;
-#pragma unroll 4
-                for (int r = 0; r < DK; r++) {
-                    const float qv = QtT[r * kGC + a], wv = WT[r * kGC + a];
-#pragma unroll
-                    for (int u = 0; u < 4; u++) {
-                        if (u < nu) {
-                            const float s0 = S[(mm[u] * kGW + cg) * DK + r];
-                            const float s1 = S[(mm[u] * kGW + cg + 4) * DK + r];
-                            po[u][0] = fmaf(qv, s0, po[u][0]);
-                            po[u][1] = fmaf(qv, s1, po[u][1]);
-                            pw[u][0] = fmaf(wv, s0, pw[u][0]);
-                            pw[u][1] = fmaf(wv, s1, pw[u][1]);
-                        }
-                    }
+                const int nu = take_slots(rem, mm);
+                float2 po[4], pw[4];
+                switch (nu) {
+                case 1: scan_readout<1, DK>(QW, S, mm, a, cp, po, pw); break;
+                case 2: scan_readout<2, DK>(QW, S, mm, a, cp, po, pw); break;
+                case 3: scan_readout<3, DK>(QW, S, mm, a, cp, po, pw); break;
+                default: scan_readout<4, DK>(QW, S, mm, a, cp, po, pw); break;
                 }
 #pragma unroll
                 for (int u = 0; u < 4; u++) {
                     if (u < nu) {
                         const float lw = lamc[a * nlv + mm[u]];
-                        o0 = fmaf(lw, po[u][0], o0);
-                        o1 = fmaf(lw, po[u][1], o1);
-                        WS[(mm[u] * kGC + a) * kLdws + cg] = pw[u][0];
-                        WS[(mm[u] * kGC + a) * kLdws + cg + 4] = pw[u][1];
+                        o.x = fmaf(lw, po[u].x, o.x);
+                        o.y = fmaf(lw, po[u].y, o.y);
+                        *reinterpret_cast<float2 *>(WS + (mm[u] * kGC + a) * kSld + 2 * cp) = pw[u];
                     }
                 }
             }
-            if (a < T - ci * kGC) {
-                float *po = out + (bh * T + (long long)ci * kGC + a) * dv + col0 + cg;
-                po[0] += o0;
-                po[4] += o1;
-            }
+            if (a < T - ci * kGC)
+                *reinterpret_cast<float2 *>(out + (bh * T + (long long)ci * kGC + a) * dv + col0 + 2 * cp) = o;
         }
         __syncthreads();
 
         // B. transition of the live states, then the fold into slot ctz(ci+1)
         {
-            constexpr int ncg = kGT / DK;
-            const int r = tid % DK, cg = tid / DK;
             const bool fold = ci + 1 < N || !ragged;  // a ragged last chunk stays out of the chunk levels
             const int m0 = ctz_u32((uint32_t)ci + 1u);
-            for (int c = cg; c < kGW; c += ncg) {
+            for (int e = tid; e < DK * (kGW / 2); e += kGT) {
+                const int r = e % DK, cp = e / DK;
                 uint32_t rem = live;
                 while (rem) {
                     int mm[4];
-                    int nu = 0;
-#pragma unroll
-                    for (int u = 0; u < 4; u++) {
-                        mm[u] = rem ? __ffs((int)rem) - 1 : 0;
-                        if (rem) { nu++; rem &= rem - 1; }
-                    }
-                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-                    for (int a = 0; a < kGC; a++) {
-                        const float kv = to_f32(Kr[a * DK + r]);
-#pragma unroll
-                        for (int u = 0; u < 4; u++)
-                            if (u < nu) acc[u] = fmaf(kv, WS[(mm[u] * kGC + a) * kLdws + c], acc[u]);
-                    }
-#pragma unroll
-                    for (int u = 0; u < 4; u++) {
-                        if (u < nu) {
-                            float *s = S + (mm[u] * kGW + c) * DK + r;
-                            *s = ge * (*s - acc[u]);
-                        }
+                    const int nu = take_slots(rem, mm);
+                    switch (nu) {
+                    case 1: scan_transition<1, DK>(Kr, WS, S, mm, r, cp, ge); break;
+                    case 2: scan_transition<2, DK>(Kr, WS, S, mm, r, cp, ge); break;
+                    case 3: scan_transition<3, DK>(Kr, WS, S, mm, r, cp, ge); break;
+                    default: scan_transition<4, DK>(Kr, WS, S, mm, r, cp, ge); break;
                     }
                 }
                 if (fold) {
-                    float s = Hs[r * kGW + c];
-                    for (int m = 0; m < m0; m++) s += S[(m * kGW + c) * DK + r];
-                    S[(m0 * kGW + c) * DK + r] = s;
+                    float2 sv = *reinterpret_cast<const float2 *>(Hs + r * kGW + 2 * cp);
+                    for (int m = 0; m < m0; m++) {
+                        const float2 x = *reinterpret_cast<const float2 *>(S + (m * DK + r) * kSld + 2 * cp);
+                        sv.x += x.x;
+                        sv.y += x.y;
+                    }
+                    *reinterpret_cast<float2 *>(S + (m0 * DK + r) * kSld + 2 * cp) = sv;
                 }
             }
         }
@@ -534,7 +625,7 @@ gdn_chunk_scan_kernel(const Tin *__restrict__ k, const float *__restrict__ lam, 
             for (int e = tid; e < DK * kGW; e += kGT) {
                 const int r = e % DK, c = e / DK;
                 state_out[((bh * Ls_out + j) * DK + r) * (long long)dv + col0 + c] =
-                    on ? S[(m * kGW + c) * DK + r] : 0.f;
+                    on ? S[(m * DK + r) * kSld + c] : 0.f;
             }
         }
     }
