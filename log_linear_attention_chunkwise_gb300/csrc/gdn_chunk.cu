@@ -96,6 +96,15 @@ __device__ __forceinline__ void mm16(float (&acc)[RI][CJ], const float *A, int a
     }
 }
 
+// Dynamic shared memory of this launch, in bytes: a kernel whose layout does
+// not fit returns before touching shared memory.
+__device__ __forceinline__ uint32_t dynamic_smem_bytes()
+{
+    uint32_t x;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(x));
+    return x;
+}
+
 template <int RI, int CJ>
 __device__ __forceinline__ void zero(float (&acc)[RI][CJ])
 {
@@ -105,7 +114,7 @@ __device__ __forceinline__ void zero(float (&acc)[RI][CJ])
         for (int j = 0; j < CJ; j++) acc[i][j] = 0.f;
 }
 
-// Shared memory of the prep kernel, in floats after the 64 fp64 running sums.
+// Shared memory of the prep kernel, in floats after the 64 running gate sums.
 struct PrepLayout {
     int ldk, ldq;
     size_t k, q, v, m1, m2, x, y, lam, beta, floats;
@@ -116,7 +125,7 @@ __host__ __device__ inline PrepLayout prep_layout(int dk, int dv, int L)
     PrepLayout P;
     P.ldk = dk + 1;                        // odd strides: rows read across lanes never share a bank
     P.ldq = (dk > dv ? dk : dv) + 1;       // Q, later U = T' V
-    P.k = 2 * kGC;                         // after double gam[64]
+    P.k = kGC;                             // after gam[64]
     P.q = P.k + (size_t)kGC * P.ldk;
     P.v = P.q + (size_t)kGC * P.ldq;
     P.m1 = P.v + (size_t)kGC * dv;
@@ -129,8 +138,7 @@ __host__ __device__ inline PrepLayout prep_layout(int dk, int dv, int L)
     return P;
 }
 
-// Workspace: [BH][N][dk][64][2] ((qt, w) pairs by row of q~^T and w^T), [BH][N][dk][dv] (H),
-// [BH][N] exp(gam_{C-1}).
+// Workspace: [BH][N][128][dk] (rows of q~, then of W), [BH][N][dk][dv] (H), [BH][N] exp(gam_{C-1}).
 struct WsLayout {
     size_t qw, h, gend, bytes;
 };
@@ -145,6 +153,78 @@ inline WsLayout ws_layout(long long BH, int N, int dk, int dv)
     return W;
 }
 
+// Steps 7 to 9 of the prep kernel for dv = 16 CJ: the intra-chunk output,
+// the chunk state H, and the low-bit states of a ragged last chunk.
+template <int DK, int CJ>
+__device__ __forceinline__ void prep_tail(float *M1, const float *M2, const float *Xs, const float *Ks, float *Qs,
+                                          const float *Vs, const float *gam, float *__restrict__ out,
+                                          float *__restrict__ ws_h, float *__restrict__ ws_gend,
+                                          float *__restrict__ state_out, long long tok0, long long bh, int ci, int N,
+                                          int nv, int dv, int ldq, int Ls_out)
+{
+    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+    // 7. intra-chunk output
+    {
+        float acc[4][CJ];
+        zero(acc);
+        mm16<4, CJ, kALower>(acc, M2, kLdm, 1, Vs, dv, 1, kGC, ty, tx);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const int a = ty + 16 * i;
+            if (a < nv) {
+#pragma unroll
+                for (int j = 0; j < CJ; j++) out[(tok0 + a) * dv + tx + 16 * j] = acc[i][j];
+            }
+        }
+    }
+    __syncthreads();  // M1 (Cm) and Qs are free
+
+    // 8. T' = T diag(exp(gam_{C-1} - gam)) into M1, U = T' V into Qs, H = K^T U
+    const float Gam = gam[kGC - 1];
+    for (int e = tid; e < kGC * kGC; e += kGT) {
+        const int a = e >> kGCBits, b = e & (kGC - 1);
+        M1[a * kLdm + b] = Xs[a * kLdm + b] * expf(Gam - gam[b]);
+    }
+    __syncthreads();
+    auto kt_u = [&](int lo, int hi, float *dst) {
+        // U = T'[:, lo:hi] V[lo:hi, :] into Qs, then dst = K^T U (dk x dv)
+        {
+            float acc[4][CJ];
+            zero(acc);
+            if (lo == 0 && hi == kGC)
+                mm16<4, CJ, kALower>(acc, M1, kLdm, 1, Vs, dv, 1, kGC, ty, tx);
+            else
+                mm16<4, CJ>(acc, M1 + lo, kLdm, 1, Vs + lo * dv, dv, 1, hi - lo, ty, tx);
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+#pragma unroll
+                for (int j = 0; j < CJ; j++) Qs[(ty + 16 * i) * ldq + tx + 16 * j] = acc[i][j];
+        }
+        __syncthreads();
+        constexpr int RI = DK / 16;
+        float acc[RI][CJ];
+        zero(acc);
+        mm16<RI, CJ>(acc, Ks, 1, DK + 1, Qs, ldq, 1, kGC, ty, tx);  // A(r, a) = K[a][r], B(a, c) = U[a][c]
+#pragma unroll
+        for (int i = 0; i < RI; i++)
+#pragma unroll
+            for (int j = 0; j < CJ; j++) dst[(ty + 16 * i) * dv + tx + 16 * j] = acc[i][j];
+    };
+    kt_u(0, kGC, ws_h + (bh * N + ci) * (long long)DK * dv);
+    if (tid == 0) ws_gend[bh * N + ci] = expf(Gam);
+
+    // 9. after a ragged last chunk the sequence's low bits are buckets inside
+    //    it: slot j (bit j of T) holds K^T T'[:, B_j] V[B_j, :] over its tokens
+    if (state_out && ci == N - 1 && nv < kGC) {
+        for (int j = 0; j < kGCBits; j++) {
+            if (!((nv >> j) & 1)) continue;
+            const int hi = nv - (nv & ((1 << j) - 1)), lo = hi - (1 << j);
+            __syncthreads();  // Qs is reused
+            kt_u(lo, hi, state_out + ((bh * Ls_out + j) * DK) * (long long)dv);
+        }
+    }
+}
+
 template <typename Tin, int DK>
 __global__ void __launch_bounds__(kGT, DK <= 64 ? 2 : 1)
 gdn_chunk_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
@@ -155,8 +235,9 @@ gdn_chunk_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, cons
 {
     extern __shared__ __align__(16) float sm[];
     const PrepLayout P = prep_layout(DK, dv, L);
+    if (P.floats * sizeof(float) > dynamic_smem_bytes()) return;
     const int ldk = P.ldk, ldq = P.ldq;
-    double *gam = reinterpret_cast<double *>(sm);
+    float *gam = sm;
     float *Ks = sm + P.k, *Qs = sm + P.q, *Vs = sm + P.v;
     float *M1 = sm + P.m1, *M2 = sm + P.m2, *Xs = sm + P.x, *Ys = sm + P.y;
     float *ls = sm + P.lam, *bs = sm + P.beta;
@@ -179,7 +260,7 @@ gdn_chunk_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, cons
     for (int e = tid; e < kGC * L; e += kGT) ls[e] = e / L < nv ? lam[tok0 * L + e] : 0.f;
     for (int e = tid; e < kGC * kLdm; e += kGT) Xs[e] = 0.f;
     if (tid < kGC) bs[tid] = tid < nv ? beta[tok0 + tid] : 0.f;
-    if (tid < 32) {  // inclusive fp64 running sum of the gates, two tokens per lane
+    if (tid < 32) {  // inclusive running sum of the gates (fp64, stored fp32), two tokens per lane
         const int a0 = 2 * tid;
         const double g0 = a0 < nv ? (double)g[tok0 + a0] : 0.0;
         const double g1 = a0 + 1 < nv ? (double)g[tok0 + a0 + 1] : 0.0;
@@ -189,8 +270,8 @@ gdn_chunk_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, cons
             const double y = __shfl_up_sync(0xffffffffu, s, off);
             if (tid >= off) s += y;
         }
-        gam[a0 + 1] = s;
-        gam[a0] = s - g1;
+        gam[a0 + 1] = (float)s;
+        gam[a0] = (float)(s - g1);
     }
     __syncthreads();
 
@@ -278,95 +359,39 @@ gdn_chunk_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, cons
                 float m = 0.f;
                 if (s <= a && a < nv) {
                     const int lev = 32 - __clz(a ^ s);
-                    m = ls[a * L + lev] * expf((float)(gam[a] - gam[s])) * acc[i][j];
+                    m = ls[a * L + lev] * expf(gam[a] - gam[s]) * acc[i][j];
                 }
                 M2[a * kLdm + s] = m;
             }
     }
     __syncthreads();
 
-    // 6. (qt, w) pairs, [r][a][2]: qt^T = (diag(exp(gam)) (Q - Cm K))^T and w^T = (T K)^T
+    // 6. q~ = diag(exp(gam)) (Q - Cm K) and W = T K, rows [a][r]: q~ in rows 0..63, W in 64..127
     {
-        float2 *qw_ws = reinterpret_cast<float2 *>(ws_qw + (bh * N + ci) * (2LL * DK * kGC));
-        constexpr int RI = DK / 16;
-        float aw[RI][4], ac[RI][4];
+        float *qw_ws = ws_qw + (bh * N + ci) * (2LL * DK * kGC);
+        constexpr int CJ = DK / 16;
+        float aw[4][CJ], ac[4][CJ];
         zero(aw);
         zero(ac);
-        mm16<RI, 4, kBUpper>(aw, Ks, 1, ldk, Xs, 1, kLdm, kGC, ty, tx);  // A(r, b) = K[b][r], B(b, a) = T[a][b]
-        mm16<RI, 4, kBUpper>(ac, Ks, 1, ldk, M1, 1, kLdm, kGC, ty, tx);  // B(b, a) = Cm[a][b]
-#pragma unroll
-        for (int j = 0; j < 4; j++) {
-            const int a = tx + 16 * j;
-            const float ea = expf((float)gam[a]);
-#pragma unroll
-            for (int i = 0; i < RI; i++) {
-                const int r = ty + 16 * i;
-                qw_ws[r * kGC + a] = make_float2(ea * (Qs[a * ldq + r] - ac[i][j]), aw[i][j]);
-            }
-        }
-    }
-    // 7. intra-chunk output
-    {
-        float acc[4][8];
-        zero(acc);
-        mm16<4, 8, kALower>(acc, M2, kLdm, 1, Vs, dv, 1, kGC, ty, tx, cj);
+        mm16<4, CJ, kALower>(aw, Xs, kLdm, 1, Ks, ldk, 1, kGC, ty, tx);  // A(a, b) = T[a][b], B(b, r) = K[b][r]
+        mm16<4, CJ, kALower>(ac, M1, kLdm, 1, Ks, ldk, 1, kGC, ty, tx);  // A(a, b) = Cm[a][b]
 #pragma unroll
         for (int i = 0; i < 4; i++) {
             const int a = ty + 16 * i;
-            if (a < nv) {
+            const float ea = expf(gam[a]);
 #pragma unroll
-                for (int j = 0; j < 8; j++)
-                    if (j < cj) out[(tok0 + a) * dv + tx + 16 * j] = acc[i][j];
+            for (int j = 0; j < CJ; j++) {
+                const int r = tx + 16 * j;
+                qw_ws[a * DK + r] = ea * (Qs[a * ldq + r] - ac[i][j]);
+                qw_ws[(kGC + a) * DK + r] = aw[i][j];
             }
         }
     }
-    __syncthreads();  // M1 (Cm) and Qs are free
-
-    // 8. T' = T diag(exp(gam_{C-1} - gam)) into M1, U = T' V into Qs, H = K^T U
-    const double Gam = gam[kGC - 1];
-    for (int e = tid; e < kGC * kGC; e += kGT) {
-        const int a = e >> kGCBits, b = e & (kGC - 1);
-        M1[a * kLdm + b] = Xs[a * kLdm + b] * expf((float)(Gam - gam[b]));
-    }
-    __syncthreads();
-    auto kt_u = [&](int lo, int hi, float *dst) {
-        // U = T'[:, lo:hi] V[lo:hi, :] into Qs, then dst = K^T U (dk x dv)
-        {
-            float acc[4][8];
-            zero(acc);
-            if (lo == 0 && hi == kGC)
-                mm16<4, 8, kALower>(acc, M1, kLdm, 1, Vs, dv, 1, kGC, ty, tx, cj);
-            else
-                mm16<4, 8>(acc, M1 + lo, kLdm, 1, Vs + lo * dv, dv, 1, hi - lo, ty, tx, cj);
-#pragma unroll
-            for (int i = 0; i < 4; i++)
-#pragma unroll
-                for (int j = 0; j < 8; j++)
-                    if (j < cj) Qs[(ty + 16 * i) * ldq + tx + 16 * j] = acc[i][j];
-        }
-        __syncthreads();
-        constexpr int RI = DK / 16;
-        float acc[RI][8];
-        zero(acc);
-        mm16<RI, 8>(acc, Ks, 1, ldk, Qs, ldq, 1, kGC, ty, tx, cj);  // A(r, a) = K[a][r], B(a, c) = U[a][c]
-#pragma unroll
-        for (int i = 0; i < RI; i++)
-#pragma unroll
-            for (int j = 0; j < 8; j++)
-                if (j < cj) dst[(ty + 16 * i) * dv + tx + 16 * j] = acc[i][j];
-    };
-    kt_u(0, kGC, ws_h + (bh * N + ci) * (long long)DK * dv);
-    if (tid == 0) ws_gend[bh * N + ci] = expf((float)Gam);
-
-    // 9. after a ragged last chunk the sequence's low bits are buckets inside
-    //    it: slot j (bit j of T) holds K^T T'[:, B_j] V[B_j, :] over its tokens
-    if (state_out && ci == N - 1 && nv < kGC) {
-        for (int j = 0; j < kGCBits; j++) {
-            if (!((nv >> j) & 1)) continue;
-            const int hi = nv - (nv & ((1 << j) - 1)), lo = hi - (1 << j);
-            __syncthreads();  // Qs is reused
-            kt_u(lo, hi, state_out + ((bh * Ls_out + j) * DK) * (long long)dv);
-        }
+    switch (cj) {
+    case 1: prep_tail<DK, 1>(M1, M2, Xs, Ks, Qs, Vs, gam, out, ws_h, ws_gend, state_out, tok0, bh, ci, N, nv, dv, ldq, Ls_out); break;
+    case 2: prep_tail<DK, 2>(M1, M2, Xs, Ks, Qs, Vs, gam, out, ws_h, ws_gend, state_out, tok0, bh, ci, N, nv, dv, ldq, Ls_out); break;
+    case 4: prep_tail<DK, 4>(M1, M2, Xs, Ks, Qs, Vs, gam, out, ws_h, ws_gend, state_out, tok0, bh, ci, N, nv, dv, ldq, Ls_out); break;
+    default: prep_tail<DK, 8>(M1, M2, Xs, Ks, Qs, Vs, gam, out, ws_h, ws_gend, state_out, tok0, bh, ci, N, nv, dv, ldq, Ls_out); break;
     }
 }
 
@@ -387,90 +412,86 @@ __device__ __forceinline__ void cp_async4(void *dst, const void *src, int src_by
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Shared memory of the scan kernel: states, W S rows, then one or two stages.
-// State and W S rows hold the CTA's 8 columns at a stride of 10 floats, so a
-// float2 per lane over consecutive rows touches distinct banks.
-constexpr int kSld = 10;
-
+// The scan's products have 8 columns (one CTA's value slice), so they run as
+// warp-level m16n8k8 TF32 tensor-core products; every fp32 operand is split
+// into a TF32 high part and a TF32 remainder and the three significant
+// partial products (hi.hi, hi.lo, lo.hi) are accumulated in fp32, which keeps
+// about 21 bits (bf16 keys are exact in TF32 and need no split).  The staged
+// q~ / W and key rows are stored with their 16-byte pieces XOR-permuted by
+// row, so the fragment loads (lane 4 g + t reads row g, column t, or row t,
+// columns g) fall in distinct banks without padding.
 struct ScanLayout {
-    size_t S, WS, stage, qw, kr, h, o, lam, gend, stage_bytes, bytes;
+    size_t S, WS, stage, qw, kr, h, lam, gend, stage_bytes, bytes;
 };
 
-__host__ __device__ inline ScanLayout scan_layout(int dk, int NS, int nlv, int nst, int tin_bytes)
+__host__ __device__ inline ScanLayout scan_layout(int dk, int N, int nlv, int nst, int tin_bytes)
 {
     ScanLayout Y;
-    Y.S = 0;                                                        // [NS][dk][kSld] fp32
-    Y.WS = Y.S + (size_t)NS * dk * kSld * 4;                        // [NS][64][kSld] fp32
-    Y.stage = align_up(Y.WS + (size_t)NS * kGC * kSld * 4, 16);
-    Y.qw = 0;                                                       // (qt, w) pairs [dk][64][2] fp32
-    Y.kr = Y.qw + (size_t)2 * dk * kGC * 4;                         // K [64][dk] in the input type
+    const int NS = bit_length_u32((uint32_t)N);                     // slots (the last fold included)
+    const int nl = bit_length_u32((uint32_t)(N - 1));               // slots live at some chunk < N
+    const int nws = nl > 1 ? nl : 1;
+    Y.S = 0;                                                        // [NS][dk][kGW] fp32
+    Y.WS = Y.S + (size_t)NS * dk * kGW * 4;                         // [nws][64][kGW] fp32
+    Y.stage = align_up(Y.WS + (size_t)nws * kGC * kGW * 4, 16);
+    Y.qw = 0;                                                       // [128][dk] fp32, permuted
+    Y.kr = Y.qw + (size_t)2 * kGC * dk * 4;                         // [64][dk] input type, permuted
     Y.h = Y.kr + (size_t)kGC * dk * tin_bytes;                      // H slice [dk][kGW]
-    Y.o = Y.h + (size_t)dk * kGW * 4;                               // output slice [64][kGW]
-    Y.lam = Y.o + (size_t)kGC * kGW * 4;                            // chunk-level lambda [64][nlv]
+    Y.lam = Y.h + (size_t)dk * kGW * 4;                             // chunk-level lambda [64][nlv]
     Y.gend = Y.lam + (size_t)kGC * nlv * 4;
     Y.stage_bytes = align_up(Y.gend + 16, 16);
     Y.bytes = Y.stage + (size_t)nst * Y.stage_bytes;
     return Y;
 }
 
-// Up to four live slots mm[0..NU): with a = the thread's row and cp its column
-// pair, po[u] = (qt_a . S_u[:, cp]) and pw[u] = (w_a . S_u[:, cp]).
-template <int NU, int DK>
-__device__ __forceinline__ void scan_readout(const float2 *__restrict__ QW, const float *__restrict__ S,
-                                             const int (&mm)[4], int a, int cp, float2 (&po)[4], float2 (&pw)[4])
+// Element offset of (row, c) in a staged q~ / W tile: piece c/4 of the row
+// is stored at piece (c/4) ^ (row & 7) (fewer pieces per row: fewer bits).
+template <int DK>
+__device__ __forceinline__ int qw_off(int row, int c)
 {
-    const float *sp[NU];
-#pragma unroll
-    for (int u = 0; u < NU; u++) {
-        sp[u] = S + mm[u] * DK * kSld + 2 * cp;
-        po[u] = pw[u] = make_float2(0.f, 0.f);
-    }
-#pragma unroll 8
-    for (int r = 0; r < DK; r++) {
-        const float2 qw = QW[r * kGC + a];
-#pragma unroll
-        for (int u = 0; u < NU; u++) {
-            const float2 sv = *reinterpret_cast<const float2 *>(sp[u] + r * kSld);
-            po[u].x = fmaf(qw.x, sv.x, po[u].x);
-            po[u].y = fmaf(qw.x, sv.y, po[u].y);
-            pw[u].x = fmaf(qw.y, sv.x, pw[u].x);
-            pw[u].y = fmaf(qw.y, sv.y, pw[u].y);
-        }
-    }
+    constexpr int msk = (DK / 4 < 8 ? DK / 4 : 8) - 1;
+    return row * DK + ((((c >> 2) ^ (row & msk)) << 2) | (c & 3));
 }
 
-// S_u[r, cp] <- ge (S_u[r, cp] - sum_a K[a][r] (W S_u)[a, cp]) for the live slots mm[0..NU).
-template <int NU, int DK, typename Tin>
-__device__ __forceinline__ void scan_transition(const Tin *__restrict__ Kr, const float *__restrict__ WS, float *S,
-                                                const int (&mm)[4], int r, int cp, float ge)
+// Element offset of (a, r) in a staged key tile: the 16-byte piece holding r
+// is moved by a & 3 pieces (bf16) or 2 (a & 3) pieces (fp32, whose 8
+// consecutive columns span two pieces).
+template <int DK, typename Tin>
+__device__ __forceinline__ int k_piece_xor(int a)
 {
-    const float *wp[NU];
-    float2 acc[NU];
-#pragma unroll
-    for (int u = 0; u < NU; u++) {
-        wp[u] = WS + mm[u] * kGC * kSld + 2 * cp;
-        acc[u] = make_float2(0.f, 0.f);
-    }
-#pragma unroll 8
-    for (int a = 0; a < kGC; a++) {
-        const float kv = to_f32(Kr[a * DK + r]);
-#pragma unroll
-        for (int u = 0; u < NU; u++) {
-            const float2 w = *reinterpret_cast<const float2 *>(wp[u] + a * kSld);
-            acc[u].x = fmaf(kv, w.x, acc[u].x);
-            acc[u].y = fmaf(kv, w.y, acc[u].y);
-        }
-    }
-#pragma unroll
-    for (int u = 0; u < NU; u++) {
-        float2 *sp = reinterpret_cast<float2 *>(S + (mm[u] * DK + r) * kSld + 2 * cp);
-        float2 x = *sp;
-        x.x = ge * (x.x - acc[u].x);
-        x.y = ge * (x.y - acc[u].y);
-        *sp = x;
-    }
+    constexpr int cpr = DK * (int)sizeof(Tin) / 16;
+    return (sizeof(Tin) == 2 ? (a & 3) : ((a & 3) << 1)) & (cpr - 1);
 }
 
-// The next (up to) four live slots of rem, lowest first; returns how many.
+template <int DK, typename Tin>
+__device__ __forceinline__ int k_off(int a, int r)
+{
+    constexpr int epc = 16 / (int)sizeof(Tin);
+    return a * DK + ((((r / epc) ^ k_piece_xor<DK, Tin>(a)) * epc) + (r % epc));
+}
+
+__device__ __forceinline__ uint32_t to_tf32(float x)
+{
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo)
+{
+    hi = to_tf32(x);
+    lo = to_tf32(x - __uint_as_float(hi));
+}
+
+// d += a b, m16n8k8, A row-major 16 x 8, B column-major 8 x 8, TF32 in, fp32 accumulate.
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+                 "{%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// The next (up to) four slots of rem, lowest first; returns how many.
 __device__ __forceinline__ int take_slots(uint32_t &rem, int (&mm)[4])
 {
     int nu = 0;
@@ -485,8 +506,84 @@ __device__ __forceinline__ int take_slots(uint32_t &rem, int (&mm)[4])
     return nu;
 }
 
+// Read-out and W S of a warp's 16 rows of [q~; W] (rows r0..r0+15 of the
+// 128) against live slots mm[0..NU): d[u] is the m16n8 result tile.
+template <int NU, int DK>
+__device__ __forceinline__ void scan_rows(const float *__restrict__ QWs, const float *__restrict__ S,
+                                          const int (&mm)[4], int r0, int g, int t, float (&d)[4][4])
+{
+#pragma unroll
+    for (int u = 0; u < NU; u++) d[u][0] = d[u][1] = d[u][2] = d[u][3] = 0.f;
+#pragma unroll 2
+    for (int kk = 0; kk < DK / 8; kk++) {
+        uint32_t ah[4], al[4];
+        split_tf32(QWs[qw_off<DK>(r0 + g, 8 * kk + t)], ah[0], al[0]);
+        split_tf32(QWs[qw_off<DK>(r0 + g + 8, 8 * kk + t)], ah[1], al[1]);
+        split_tf32(QWs[qw_off<DK>(r0 + g, 8 * kk + t + 4)], ah[2], al[2]);
+        split_tf32(QWs[qw_off<DK>(r0 + g + 8, 8 * kk + t + 4)], ah[3], al[3]);
+#pragma unroll
+        for (int u = 0; u < NU; u++) {
+            const float *Sm = S + (mm[u] * DK + 8 * kk + t) * kGW + g;
+            uint32_t bh0, bl0, bh1, bl1;
+            split_tf32(Sm[0], bh0, bl0);
+            split_tf32(Sm[4 * kGW], bh1, bl1);
+            mma_tf32(d[u], ah, bh0, bh1);
+            mma_tf32(d[u], ah, bl0, bl1);
+            mma_tf32(d[u], al, bh0, bh1);
+        }
+    }
+}
+
+// The transition of live slots mm[0..NU) on a warp's 16 state rows r0..r0+15:
+// S[r, :] <- ge (S[r, :] - sum_a K[a][r] (W S)[a, :]).
+template <int NU, int DK, typename Tin>
+__device__ __forceinline__ void scan_transition(const Tin *__restrict__ Kr, const float *__restrict__ WS, float *S,
+                                                const int (&mm)[4], int r0, int g, int t, float ge)
+{
+    float d[4][4];
+#pragma unroll
+    for (int u = 0; u < NU; u++) d[u][0] = d[u][1] = d[u][2] = d[u][3] = 0.f;
+#pragma unroll 2
+    for (int kk = 0; kk < kGC / 8; kk++) {  // A(row r, col a) = K[a][r]
+        const int a0 = 8 * kk + t, a1 = a0 + 4;
+        const float x[4] = {to_f32(Kr[k_off<DK, Tin>(a0, r0 + g)]), to_f32(Kr[k_off<DK, Tin>(a0, r0 + g + 8)]),
+                            to_f32(Kr[k_off<DK, Tin>(a1, r0 + g)]), to_f32(Kr[k_off<DK, Tin>(a1, r0 + g + 8)])};
+        uint32_t ah[4], al[4];
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            if (sizeof(Tin) == 2) {
+                ah[e] = __float_as_uint(x[e]);  // a bf16 value is exact in TF32
+                al[e] = 0u;
+            } else {
+                split_tf32(x[e], ah[e], al[e]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < NU; u++) {
+            const float *W0 = WS + (mm[u] * kGC + 8 * kk + t) * kGW + g;
+            uint32_t bh0, bl0, bh1, bl1;
+            split_tf32(W0[0], bh0, bl0);
+            split_tf32(W0[4 * kGW], bh1, bl1);
+            mma_tf32(d[u], ah, bh0, bh1);
+            mma_tf32(d[u], ah, bl0, bl1);
+            if (sizeof(Tin) == 4) mma_tf32(d[u], al, bh0, bh1);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < NU; u++) {
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+            float2 *sp = reinterpret_cast<float2 *>(S + (mm[u] * DK + r0 + g + 8 * h) * kGW + 2 * t);
+            float2 x = *sp;
+            x.x = ge * (x.x - d[u][2 * h]);
+            x.y = ge * (x.y - d[u][2 * h + 1]);
+            *sp = x;
+        }
+    }
+}
+
 template <typename Tin, int DK>
-__global__ void __launch_bounds__(kGT)
+__global__ void __launch_bounds__(kGT, 2)
 gdn_chunk_scan_kernel(const Tin *__restrict__ k, const float *__restrict__ lam, float *__restrict__ out,
                       const float *__restrict__ ws_qw, const float *__restrict__ ws_h,
                       const float *__restrict__ ws_gend, float *__restrict__ state_out, int T, int N, int H, int dv,
@@ -495,10 +592,12 @@ gdn_chunk_scan_kernel(const Tin *__restrict__ k, const float *__restrict__ lam, 
     extern __shared__ __align__(16) uint8_t smb[];
     const int NS = bit_length_u32((uint32_t)N);  // chunk-level slots: slot m = level kGCBits + 1 + m
     const int nlv = max(L - (kGCBits + 1), 0);
-    const ScanLayout Y = scan_layout(DK, NS, nlv, nst, (int)sizeof(Tin));
+    const ScanLayout Y = scan_layout(DK, N, nlv, nst, (int)sizeof(Tin));
+    if (Y.bytes > dynamic_smem_bytes()) return;
     float *S = reinterpret_cast<float *>(smb + Y.S);
     float *WS = reinterpret_cast<float *>(smb + Y.WS);
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, t = lane & 3;
     const int col0 = blockIdx.x * kGW;
     const long long bh = (long long)blockIdx.z * H + blockIdx.y;
     const bool ragged = (T % kGC) != 0;
@@ -509,23 +608,21 @@ gdn_chunk_scan_kernel(const Tin *__restrict__ k, const float *__restrict__ lam, 
         const int nvc = min(kGC, T - ci * kGC);
         const long long row0 = bh * T + (long long)ci * kGC;
         const float *qw = ws_qw + (bh * N + ci) * (2LL * DK * kGC);
-        for (int e = tid; e < 2 * DK * kGC / 4; e += kGT) cp_async16(b + Y.qw + 16 * e, qw + 4 * e, 16);
+        constexpr int qpr = DK / 4;  // 16-byte pieces per q~ / W row
+        for (int e = tid; e < 2 * kGC * qpr; e += kGT) {
+            const int r = e / qpr, p = e % qpr;
+            cp_async16(b + Y.qw + (size_t)qw_off<DK>(r, 4 * p) * 4, qw + r * DK + 4 * p, 16);
+        }
         constexpr int cpr = DK * (int)sizeof(Tin) / 16;  // 16-byte pieces per key row
         for (int e = tid; e < kGC * cpr; e += kGT) {
             const int a = e / cpr, p = e % cpr;
             const Tin *src = k + (row0 + min(a, nvc - 1)) * DK + p * (16 / (int)sizeof(Tin));
-            cp_async16(b + Y.kr + 16 * e, src, a < nvc ? 16 : 0);
+            cp_async16(b + Y.kr + ((size_t)a * cpr + (p ^ k_piece_xor<DK, Tin>(a))) * 16, src, a < nvc ? 16 : 0);
         }
         const float *h = ws_h + (bh * N + ci) * (long long)DK * dv + col0;
         for (int e = tid; e < DK * kGW / 4; e += kGT) {
             const int r = e / (kGW / 4), p = e % (kGW / 4);
             cp_async16(b + Y.h + 16 * e, h + (long long)r * dv + 4 * p, 16);
-        }
-        if (ci > 0) {  // the output slice the read-out adds to (chunk 0 has nothing to read out)
-            for (int e = tid; e < kGC * kGW / 4; e += kGT) {
-                const int a = e / (kGW / 4), p = e % (kGW / 4);
-                cp_async16(b + Y.o + 16 * e, out + (row0 + min(a, nvc - 1)) * dv + col0 + 4 * p, a < nvc ? 16 : 0);
-            }
         }
         for (int e = tid; e < kGC * nlv; e += kGT) {
             const int a = e / nlv, m = e % nlv;
@@ -535,6 +632,10 @@ gdn_chunk_scan_kernel(const Tin *__restrict__ k, const float *__restrict__ lam, 
         asm volatile("cp.async.commit_group;" ::: "memory");
     };
 
+    constexpr int MT = DK / 16;       // 16-row tiles of a state
+    constexpr int NSP = 8 / MT;       // warps sharing one state tile (they split the slots)
+    const int mt = warp % MT, sp = warp / MT;
+
     if (nst == 2) load(0, 0);
     for (int ci = 0; ci < N; ci++) {
         const int st = nst == 2 ? (ci & 1) : 0;
@@ -543,70 +644,98 @@ gdn_chunk_scan_kernel(const Tin *__restrict__ k, const float *__restrict__ lam, 
         __syncthreads();  // stage ci is visible; chunk ci-1 is finished with the other stage
         if (nst == 2 && ci + 1 < N) load((ci + 1) & 1, ci + 1);
         const uint8_t *b = stage_ptr(st);
-        const float2 *QW = reinterpret_cast<const float2 *>(b + Y.qw);
+        const float *QWs = reinterpret_cast<const float *>(b + Y.qw);
         const Tin *Kr = reinterpret_cast<const Tin *>(b + Y.kr);
         const float *Hs = reinterpret_cast<const float *>(b + Y.h);
-        const float *Os = reinterpret_cast<const float *>(b + Y.o);
         const float *lamc = reinterpret_cast<const float *>(b + Y.lam);
         const float ge = *reinterpret_cast<const float *>(b + Y.gend);
         const uint32_t live = (uint32_t)ci;  // slot m is live at chunk ci iff bit m of ci is set
 
-        // A. read-out of the live states into the output, and W S of each
         if (live) {
-            const int a = tid & (kGC - 1), cp = tid >> kGCBits;  // row, column pair
-            float2 o = *reinterpret_cast<const float2 *>(Os + a * kGW + 2 * cp);
+            // A. warp w takes rows 16w..16w+15 of [q~; W]: warps 0-3 read out into
+            //    the output, warps 4-7 leave W S of each live slot for the transition
+            const int r0 = 16 * warp;
+            const bool readout = warp < 4;
+            const int nvc = T - ci * kGC;
+            float o[4] = {0.f, 0.f, 0.f, 0.f};
+            float *orow[2];
+            if (readout) {  // the intra-chunk output this adds to, loaded while the products run
+#pragma unroll
+                for (int h = 0; h < 2; h++) {
+                    const int a = r0 + g + 8 * h;
+                    orow[h] = out + (bh * T + (long long)ci * kGC + a) * dv + col0 + 2 * t;
+                    if (a < nvc) {
+                        const float2 x = *reinterpret_cast<const float2 *>(orow[h]);
+                        o[2 * h] = x.x;
+                        o[2 * h + 1] = x.y;
+                    }
+                }
+            }
             uint32_t rem = live;
             while (rem) {
                 int mm[4];
                 const int nu = take_slots(rem, mm);
-                float2 po[4], pw[4];
+                float d[4][4];
                 switch (nu) {
-                case 1: scan_readout<1, DK>(QW, S, mm, a, cp, po, pw); break;
-                case 2: scan_readout<2, DK>(QW, S, mm, a, cp, po, pw); break;
-                case 3: scan_readout<3, DK>(QW, S, mm, a, cp, po, pw); break;
-                default: scan_readout<4, DK>(QW, S, mm, a, cp, po, pw); break;
+                case 1: scan_rows<1, DK>(QWs, S, mm, r0, g, t, d); break;
+                case 2: scan_rows<2, DK>(QWs, S, mm, r0, g, t, d); break;
+                case 3: scan_rows<3, DK>(QWs, S, mm, r0, g, t, d); break;
+                default: scan_rows<4, DK>(QWs, S, mm, r0, g, t, d); break;
                 }
 #pragma unroll
                 for (int u = 0; u < 4; u++) {
-                    if (u < nu) {
-                        const float lw = lamc[a * nlv + mm[u]];
-                        o.x = fmaf(lw, po[u].x, o.x);
-                        o.y = fmaf(lw, po[u].y, o.y);
-                        *reinterpret_cast<float2 *>(WS + (mm[u] * kGC + a) * kSld + 2 * cp) = pw[u];
+                    if (u >= nu) break;
+                    if (readout) {
+                        const float l0 = lamc[(r0 + g) * nlv + mm[u]], l1 = lamc[(r0 + g + 8) * nlv + mm[u]];
+                        o[0] = fmaf(l0, d[u][0], o[0]);
+                        o[1] = fmaf(l0, d[u][1], o[1]);
+                        o[2] = fmaf(l1, d[u][2], o[2]);
+                        o[3] = fmaf(l1, d[u][3], o[3]);
+                    } else {
+                        float *w = WS + (mm[u] * kGC + r0 - kGC + g) * kGW + 2 * t;
+                        *reinterpret_cast<float2 *>(w) = make_float2(d[u][0], d[u][1]);
+                        *reinterpret_cast<float2 *>(w + 8 * kGW) = make_float2(d[u][2], d[u][3]);
                     }
                 }
             }
-            if (a < T - ci * kGC)
-                *reinterpret_cast<float2 *>(out + (bh * T + (long long)ci * kGC + a) * dv + col0 + 2 * cp) = o;
-        }
-        __syncthreads();
+            if (readout) {
+#pragma unroll
+                for (int h = 0; h < 2; h++)
+                    if (r0 + g + 8 * h < nvc)
+                        *reinterpret_cast<float2 *>(orow[h]) = make_float2(o[2 * h], o[2 * h + 1]);
+            }
+            __syncthreads();
 
-        // B. transition of the live states, then the fold into slot ctz(ci+1)
-        {
-            const bool fold = ci + 1 < N || !ragged;  // a ragged last chunk stays out of the chunk levels
-            const int m0 = ctz_u32((uint32_t)ci + 1u);
-            for (int e = tid; e < DK * (kGW / 2); e += kGT) {
-                const int r = e % DK, cp = e / DK;
+            // B. transition: warp (tile mt, part sp) takes every NSP-th live slot
+            uint32_t mine = 0;
+            {
                 uint32_t rem = live;
-                while (rem) {
-                    int mm[4];
-                    const int nu = take_slots(rem, mm);
-                    switch (nu) {
-                    case 1: scan_transition<1, DK>(Kr, WS, S, mm, r, cp, ge); break;
-                    case 2: scan_transition<2, DK>(Kr, WS, S, mm, r, cp, ge); break;
-                    case 3: scan_transition<3, DK>(Kr, WS, S, mm, r, cp, ge); break;
-                    default: scan_transition<4, DK>(Kr, WS, S, mm, r, cp, ge); break;
-                    }
+                for (int n = 0; rem; n++) {
+                    const uint32_t low = rem & (0u - rem);
+                    if (n % NSP == sp) mine |= low;
+                    rem ^= low;
                 }
-                if (fold) {
-                    float2 sv = *reinterpret_cast<const float2 *>(Hs + r * kGW + 2 * cp);
-                    for (int m = 0; m < m0; m++) {
-                        const float2 x = *reinterpret_cast<const float2 *>(S + (m * DK + r) * kSld + 2 * cp);
-                        sv.x += x.x;
-                        sv.y += x.y;
-                    }
-                    *reinterpret_cast<float2 *>(S + (m0 * DK + r) * kSld + 2 * cp) = sv;
+            }
+            while (mine) {
+                int mm[4];
+                const int nu = take_slots(mine, mm);
+                switch (nu) {
+                case 1: scan_transition<1, DK>(Kr, WS, S, mm, 16 * mt, g, t, ge); break;
+                case 2: scan_transition<2, DK>(Kr, WS, S, mm, 16 * mt, g, t, ge); break;
+                case 3: scan_transition<3, DK>(Kr, WS, S, mm, 16 * mt, g, t, ge); break;
+                default: scan_transition<4, DK>(Kr, WS, S, mm, 16 * mt, g, t, ge); break;
                 }
+            }
+            __syncthreads();
+        }
+
+        // C. the fold into slot ctz(ci+1) of the chunk's state and the slots below it
+        if (ci + 1 < N || !ragged) {  // a ragged last chunk stays out of the chunk levels
+            const int m0 = ctz_u32((uint32_t)ci + 1u);
+            for (int e = tid; e < DK * kGW; e += kGT) {
+                float sv = Hs[e];
+                for (int m = 0; m < m0; m++) sv += S[m * DK * kGW + e];
+                S[m0 * DK * kGW + e] = sv;
             }
         }
         if (nst == 1) __syncthreads();  // the single stage is reloaded next
@@ -623,17 +752,17 @@ gdn_chunk_scan_kernel(const Tin *__restrict__ k, const float *__restrict__ lam, 
             const int m = j - kGCBits;
             const bool on = m >= 0 && m < NS && ((nfull >> m) & 1);
             for (int e = tid; e < DK * kGW; e += kGT) {
-                const int r = e % DK, c = e / DK;
+                const int r = e / kGW, c = e % kGW;
                 state_out[((bh * Ls_out + j) * DK + r) * (long long)dv + col0 + c] =
-                    on ? S[(m * DK + r) * kSld + c] : 0.f;
+                    on ? S[(m * DK + r) * kGW + c] : 0.f;
             }
         }
     }
 }
 
-int scan_stages(int dk, int NS, int nlv, int tin_bytes)
+int scan_stages(int dk, int N, int nlv, int tin_bytes)
 {
-    return scan_layout(dk, NS, nlv, 2, tin_bytes).bytes <= kMaxSmem ? 2 : 1;
+    return scan_layout(dk, N, nlv, 2, tin_bytes).bytes <= kMaxSmem ? 2 : 1;
 }
 
 template <typename Tin, int DK>
@@ -656,10 +785,9 @@ cudaError_t launch_chunk_dk(const GdnFwdArgs &A)
     e = cudaPeekAtLastError();
     if (e != cudaSuccess) return e;
 
-    const int NS = bit_length_u32((uint32_t)N);
     const int nlv = A.L - (kGCBits + 1) > 0 ? A.L - (kGCBits + 1) : 0;
-    const int nst = scan_stages(DK, NS, nlv, (int)sizeof(Tin));
-    const size_t ssmem = scan_layout(DK, NS, nlv, nst, (int)sizeof(Tin)).bytes;
+    const int nst = scan_stages(DK, N, nlv, (int)sizeof(Tin));
+    const size_t ssmem = scan_layout(DK, N, nlv, nst, (int)sizeof(Tin)).bytes;
     auto scan = gdn_chunk_scan_kernel<Tin, DK>;
     e = cudaFuncSetAttribute(scan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssmem);
     if (e != cudaSuccess) return e;
@@ -690,10 +818,9 @@ size_t gdn_fwd_workspace_bytes(int B, int H, int T, int dk, int dv)
 bool gdn_fwd_fits(int T, int dk, int dv, int L, int tin_bytes)
 {
     const int N = (T + kGC - 1) / kGC;
-    const int NS = bit_length_u32((uint32_t)N);
     const int nlv = L - (kGCBits + 1) > 0 ? L - (kGCBits + 1) : 0;
     return prep_layout(dk, dv, L).floats * sizeof(float) <= kMaxSmem &&
-           scan_layout(dk, NS, nlv, 1, tin_bytes).bytes <= kMaxSmem;
+           scan_layout(dk, N, nlv, 1, tin_bytes).bytes <= kMaxSmem;
 }
 
 cudaError_t gdn_fwd(const GdnFwdArgs &A)
