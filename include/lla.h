@@ -226,7 +226,7 @@ lla_status lla_fwd_host(const void *q, const void *k, const void *v, const float
  * then carried across chunks in order.  fp32 on CUDA cores, two launches.
  *   q, k [B,H,T,dk], v [B,H,T,dv] in in_dt; g, beta [B,H,T] fp32;
  *   lambda [B,H,T,L] fp32 with L = lla_num_levels(T); out [B,H,T,dv] fp32.
- *   k and out must be 16-byte aligned (copied to shared memory in 16-byte pieces).
+ *   q, k, v and out must be 16-byte aligned (read and written in 16-byte pieces).
  *   state_out (nullable) [B,H,Ls_out,dk,dv] fp32 receives the state after the
  *   sequence in the layout of lla_gdn_decode_step (slot i = level i+1, dead
  *   slots zeroed); Ls_out >= bit_length(T) when state_out is given.

@@ -105,6 +105,28 @@ __device__ __forceinline__ uint32_t dynamic_smem_bytes()
     return x;
 }
 
+// One 16-byte piece of the input (8 bf16 or 4 fp32) as fp32, or zeros.
+template <typename Tin>
+__device__ __forceinline__ void load16_f32(const Tin *p, bool ok, float (&x)[16 / sizeof(Tin)])
+{
+    constexpr int n = 16 / (int)sizeof(Tin);
+    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+    if (ok) w = *reinterpret_cast<const uint4 *>(p);
+    if constexpr (sizeof(Tin) == 4) {
+        x[0] = __uint_as_float(w.x);
+        x[1] = __uint_as_float(w.y);
+        x[2] = __uint_as_float(w.z);
+        x[3] = __uint_as_float(w.w);
+    } else {
+        const uint32_t h[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int u = 0; u < n / 2; u++) {
+            x[2 * u] = __uint_as_float(h[u] << 16);            // bf16 -> fp32: the high half of the word
+            x[2 * u + 1] = __uint_as_float(h[u] & 0xffff0000u);
+        }
+    }
+}
+
 template <int RI, int CJ>
 __device__ __forceinline__ void zero(float (&acc)[RI][CJ])
 {
@@ -250,13 +272,25 @@ gdn_chunk_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, cons
 
     // 1. the chunk's inputs, zero past T (a padded token has k = v = 0, beta = 0,
     //    g = 0: its factor is the identity and it adds nothing)
-    for (int e = tid; e < kGC * DK; e += kGT) {
-        const int a = e / DK, r = e % DK;
-        const bool ok = a < nv;
-        Ks[a * ldk + r] = ok ? to_f32(k[tok0 * DK + e]) : 0.f;
-        Qs[a * ldq + r] = ok ? to_f32(q[tok0 * DK + e]) : 0.f;
+    //    (16-byte vector loads: every row starts on a 16-byte boundary)
+    constexpr int EPV = 16 / (int)sizeof(Tin);  // elements per 16-byte piece
+    for (int e = tid; e < kGC * DK / EPV; e += kGT) {
+        const int a = e / (DK / EPV), r = (e % (DK / EPV)) * EPV;
+        float xk[EPV], xq[EPV];
+        load16_f32<Tin>(k + tok0 * DK + (long long)e * EPV, a < nv, xk);
+        load16_f32<Tin>(q + tok0 * DK + (long long)e * EPV, a < nv, xq);
+#pragma unroll
+        for (int u = 0; u < EPV; u++) {
+            Ks[a * ldk + r + u] = xk[u];
+            Qs[a * ldq + r + u] = xq[u];
+        }
     }
-    for (int e = tid; e < kGC * dv; e += kGT) Vs[e] = e / dv < nv ? to_f32(v[tok0 * dv + e]) : 0.f;
+    for (int e = tid; e < kGC * dv / EPV; e += kGT) {
+        float xv[EPV];
+        load16_f32<Tin>(v + tok0 * dv + (long long)e * EPV, e * EPV / dv < nv, xv);
+#pragma unroll
+        for (int u = 0; u < EPV; u++) Vs[e * EPV + u] = xv[u];
+    }
     for (int e = tid; e < kGC * L; e += kGT) ls[e] = e / L < nv ? lam[tok0 * L + e] : 0.f;
     for (int e = tid; e < kGC * kLdm; e += kGT) Xs[e] = 0.f;
     if (tid < kGC) bs[tid] = tid < nv ? beta[tok0 + tid] : 0.f;

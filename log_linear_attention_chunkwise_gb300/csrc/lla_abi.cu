@@ -247,7 +247,7 @@ lla_status lla_gdn_fwd(const void *q, const void *k, const void *v, const float 
     const int tin_bytes = in_dt == LLA_F32 ? 4 : 2;
     if (!lla::gdn_fwd_fits(T, dk, dv, L, tin_bytes)) return LLA_ERR_UNSUPPORTED_SHAPE;
     if (!q || !k || !v || !g || !beta || !lambda || !out || !workspace) return LLA_ERR_INVALID_ARGUMENT;
-    if (!aligned16(k) || !aligned16(out) || ((uintptr_t)workspace & 255u) != 0 ||
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || ((uintptr_t)workspace & 255u) != 0 ||
         workspace_bytes < lla::gdn_fwd_workspace_bytes(B, H, T, dk, dv))
         return LLA_ERR_INVALID_ARGUMENT;
     lla::GdnFwdArgs A;

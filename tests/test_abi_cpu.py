@@ -119,8 +119,8 @@ def test_bwd_validation(lib):
 def test_gdn_validation(lib):
     p = ctypes.c_void_p(256)
 
-    def fwd(B=1, T=64, dk=64, Ls=0, st=NULL, dt=1, k=p, out=p, ws=p, wsb=1 << 30):
-        return lib.lla_gdn_fwd(p, k, p, p, p, p, out, st, B, 1, T, dk, 64, Ls, dt, ws, wsb, NULL)
+    def fwd(B=1, T=64, dk=64, Ls=0, st=NULL, dt=1, q=p, k=p, v=p, out=p, ws=p, wsb=1 << 30):
+        return lib.lla_gdn_fwd(q, k, v, p, p, p, out, st, B, 1, T, dk, 64, Ls, dt, ws, wsb, NULL)
     assert fwd(dk=48) == 2
     assert fwd(T=(1 << 24) + 1) == 2
     assert fwd(st=p, Ls=6) == 2          # 64 tokens need bit_length(64) = 7 slots
@@ -130,6 +130,8 @@ def test_gdn_validation(lib):
     assert fwd(ws=ctypes.c_void_p(256 + 16)) == 1   # workspace not 256-byte aligned
     assert fwd(k=ctypes.c_void_p(256 + 4)) == 1     # k not 16-byte aligned
     assert fwd(out=ctypes.c_void_p(256 + 8)) == 1   # out not 16-byte aligned
+    assert fwd(q=ctypes.c_void_p(256 + 2)) == 1     # q, v read in 16-byte pieces
+    assert fwd(v=ctypes.c_void_p(256 + 2)) == 1
     assert fwd(wsb=lib.lla_gdn_fwd_workspace_bytes(1, 1, 64, 64, 64) - 1) == 1
     # per chunk of 64: q~^T and w^T [2][dk][64], H [dk][dv], the decay (fp32)
     assert lib.lla_gdn_fwd_workspace_bytes(1, 1, 64, 64, 64) >= (2 * 64 * 64 + 64 * 64 + 1) * 4
