@@ -123,32 +123,61 @@ simt_gate_prefix_kernel(const float *__restrict__ gam, double *__restrict__ P, i
     if (threadIdx.x == kThreads - 1) Pb[N] = run;
 }
 
-// In place: slot j (1..N-1) holds H_{j-1} on entry and Node_j on exit.
-// One thread per state element; the open node of each level is kept in
-// registers (stack[z] = the latest node with ctz == z).
-// In-place Fenwick scan of one state element per thread, level by level:
-// slot j holds H_{j-1} and becomes
+// In-place Fenwick scan, level by level: slot j (1..N-1) holds H_{j-1} and becomes
 //     Node_j = H_{j-1} + sum_{m < ctz(j)} exp(P_j - P_{j-2^m}) Node_{j-2^m}.
-// Every node of level z reads only nodes of lower levels, so the nodes of
-// one level are independent and their loads overlap.
+// Every node of level z reads only nodes of lower levels, so the nodes of one
+// level are independent.  The CTA forms the weights of a batch of up to
+// kScanBatch nodes of one level in shared memory (one fp64 difference each,
+// shared by every element), then each thread updates four adjacent elements
+// (float4) of four nodes at a time, all loads of the four before their stores.
+constexpr int kScanBatch = 256;
+constexpr int kScanMaxZ = 20;  // levels of a chunk index below 2^20
+
 __global__ void __launch_bounds__(kThreads)
 simt_fenwick_scan_kernel(const double *__restrict__ P, float *__restrict__ nodes, int N, int E)
 {
+    __shared__ float wt[kScanBatch * kScanMaxZ];
     const long long bh = blockIdx.y;
-    const int e = blockIdx.x * kThreads + threadIdx.x;
-    if (e >= E) return;
+    const int e4 = blockIdx.x * kThreads + threadIdx.x;  // float4 index within a node
+    const bool act = 4 * e4 < E;
     const double *Pb = P + bh * (long long)(N + 1);
-    float *base = nodes + bh * (long long)N * E + e;
+    float4 *base = reinterpret_cast<float4 *>(nodes + bh * (long long)N * E) + e4;
+    const long long E4 = E / 4;
     for (int z = 1; (1 << z) < N; z++) {
-        // j = odd multiples of 2^z below N
-        for (int j = 1 << z; j < N; j += 2 << z) {
-            const double Pj = Pb[j];
-            float val = base[(long long)j * E];
-            for (int m = 0; m < z; m++) {
-                const int jm = j - (1 << m);
-                val = fmaf(expf((float)(Pj - Pb[jm])), base[(long long)jm * E], val);
+        const int step = 2 << z;
+        const int nz = (N - (1 << z) + step - 1) / step;  // nodes of level z: j = 2^z + n step
+        for (int n0 = 0; n0 < nz; n0 += kScanBatch) {
+            const int nb = min(kScanBatch, nz - n0);
+            __syncthreads();  // the previous batch's weights are no longer read
+            for (int x = threadIdx.x; x < nb * z; x += kThreads) {
+                const int n = x / z, m = x % z;
+                const int j = (1 << z) + (n0 + n) * step;
+                wt[n * kScanMaxZ + m] = expf((float)(Pb[j] - Pb[j - (1 << m)]));
             }
-            base[(long long)j * E] = val;
+            __syncthreads();
+            if (!act) continue;
+            for (int n = 0; n < nb; n += 4) {
+                float4 val[4];
+#pragma unroll
+                for (int u = 0; u < 4; u++) {
+                    if (n + u >= nb) break;
+                    const int j = (1 << z) + (n0 + n + u) * step;
+                    val[u] = base[(long long)j * E4];
+                    const float *w = wt + (n + u) * kScanMaxZ;
+                    for (int m = 0; m < z; m++) {
+                        const float4 lo = base[(long long)(j - (1 << m)) * E4];
+                        val[u].x = fmaf(w[m], lo.x, val[u].x);
+                        val[u].y = fmaf(w[m], lo.y, val[u].y);
+                        val[u].z = fmaf(w[m], lo.z, val[u].z);
+                        val[u].w = fmaf(w[m], lo.w, val[u].w);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; u++) {
+                    if (n + u >= nb) break;
+                    base[(long long)((1 << z) + (n0 + n + u) * step) * E4] = val[u];
+                }
+            }
         }
     }
 }
@@ -280,9 +309,9 @@ cudaError_t launch_nodes(const SimtFwdArgs &A)
     simt_chunk_state_kernel<Tin><<<dim3(N, BH), kThreads, sm1, st>>>(
         (const Tin *)A.k, (const Tin *)A.v, A.g, gam, nodes, A.T, A.dk, A.dv, A.C, N);
     simt_gate_prefix_kernel<<<BH, kThreads, 0, st>>>(gam, P, N);
-    const int E = A.dk * A.dv;
+    const int E = A.dk * A.dv;  // a multiple of 256: every node row splits into float4s
     if (N > 1)
-        simt_fenwick_scan_kernel<<<dim3((E + kThreads - 1) / kThreads, BH), kThreads, 0, st>>>(
+        simt_fenwick_scan_kernel<<<dim3((E / 4 + kThreads - 1) / kThreads, BH), kThreads, 0, st>>>(
             P, nodes, N, E);
     return cudaPeekAtLastError();
 }
