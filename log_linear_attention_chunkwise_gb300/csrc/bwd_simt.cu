@@ -691,17 +691,28 @@ cudaError_t launch_bwd(const BwdArgs &A)
     const int cbits = ctz_u32((uint32_t)A.C);
     cudaStream_t st = (cudaStream_t)A.stream;
     SimtFwdArgs F = node_args(A);
-    cudaError_t e = simt_build_nodes(F);
-    if (e != cudaSuccess) return e;
     char *ws = (char *)A.workspace;
     const BwdLayout lay = layout(A);
     const double *P = (const double *)(ws + simt_ws_offset_P(F));
-    const float *nodes = (const float *)(ws + simt_ws_offset_nodes(F));
+    float *nodes = (float *)(ws + simt_ws_offset_nodes(F));
     float *gamma = (float *)(ws + lay.gamma);
     float *R = (float *)(ws + lay.R);
     float *parts = (float *)(ws + lay.parts);
     double *dG = (double *)(ws + lay.dG);
     bwd_gamma_kernel<<<dim3(N, BH), 32, 0, st>>>(A.g, gamma, A.T, A.C);
+    cudaError_t e;
+    if (bwd_state_tc_supported(A)) {
+        // the forward's chunk states on the tensor cores, then its prefix and scan
+        int *err = (int *)(ws + lay.err);
+        e = cudaMemsetAsync(err, 0, sizeof(int), st);
+        if (e != cudaSuccess) return e;
+        e = bwd_state_tc(A, gamma, (float *)ws, nodes, err);
+        if (e != cudaSuccess) return e;
+        e = simt_nodes_from_states(F);
+    } else {
+        e = simt_build_nodes(F);
+    }
+    if (e != cudaSuccess) return e;
     if (bwd_intra_tc_supported(A)) {
         int *err = (int *)(ws + lay.err);
         e = cudaMemsetAsync(err, 0, sizeof(int), st);

@@ -30,6 +30,10 @@ cudaError_t bwd_query_tc(const BwdArgs &A, const float *gamma, const double *P, 
 // Intra-chunk part on the tensor cores, same conditions: writes dq, dk, dv, dlambda.
 bool bwd_intra_tc_supported(const BwdArgs &A);
 cudaError_t bwd_intra_tc(const BwdArgs &A, const float *gamma, int *err);
+// Chunk states of the rebuilt forward nodes on the tensor cores, same conditions:
+// the chunk gate totals (every chunk) and H_i in node slot i+1 (i < N-1).
+bool bwd_state_tc_supported(const BwdArgs &A);
+cudaError_t bwd_state_tc(const BwdArgs &A, const float *gamma, float *gam_tot, float *nodes, int *err);
 // Block-state pieces on the tensor cores, same conditions: writes every piece slot it owns.
 bool bwd_piece_tc_supported(const BwdArgs &A);
 cudaError_t bwd_piece_tc(const BwdArgs &A, const float *gamma, const double *P, float *part, int nlev, int Pc,

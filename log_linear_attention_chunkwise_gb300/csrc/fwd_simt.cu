@@ -296,7 +296,7 @@ simt_chunk_output_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 
 // Steps 1-3 only (chunk states, fp64 prefix, Fenwick scan) into the workspace.
 template <typename Tin>
-cudaError_t launch_nodes(const SimtFwdArgs &A)
+cudaError_t launch_nodes(const SimtFwdArgs &A, bool states = true)
 {
     const int BH = A.B * A.H;
     const int N = A.T / A.C;
@@ -305,9 +305,11 @@ cudaError_t launch_nodes(const SimtFwdArgs &A)
     float *gam = (float *)ws;
     double *P = (double *)(ws + simt_ws_offset_P(A));
     float *nodes = (float *)(ws + simt_ws_offset_nodes(A));
-    size_t sm1 = sizeof(float) * (128 + kSub + kSub * A.dk + kSub * A.dv);
-    simt_chunk_state_kernel<Tin><<<dim3(N, BH), kThreads, sm1, st>>>(
-        (const Tin *)A.k, (const Tin *)A.v, A.g, gam, nodes, A.T, A.dk, A.dv, A.C, N);
+    if (states) {
+        size_t sm1 = sizeof(float) * (128 + kSub + kSub * A.dk + kSub * A.dv);
+        simt_chunk_state_kernel<Tin><<<dim3(N, BH), kThreads, sm1, st>>>(
+            (const Tin *)A.k, (const Tin *)A.v, A.g, gam, nodes, A.T, A.dk, A.dv, A.C, N);
+    }
     simt_gate_prefix_kernel<<<BH, kThreads, 0, st>>>(gam, P, N);
     const int E = A.dk * A.dv;  // a multiple of 256: every node row splits into float4s
     if (N > 1)
@@ -369,6 +371,11 @@ size_t simt_max_smem_bytes(const SimtFwdArgs &A)
 cudaError_t simt_build_nodes(const SimtFwdArgs &A)
 {
     return A.in_dt == LLA_F32 ? launch_nodes<float>(A) : launch_nodes<__nv_bfloat16>(A);
+}
+
+cudaError_t simt_nodes_from_states(const SimtFwdArgs &A)
+{
+    return launch_nodes<float>(A, false);  // the input type is not read
 }
 
 cudaError_t simt_fwd(const SimtFwdArgs &A)

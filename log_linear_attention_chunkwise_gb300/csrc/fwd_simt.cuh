@@ -25,5 +25,9 @@ cudaError_t simt_fwd(const SimtFwdArgs &A);
 // Chunk states, chunk-gate prefix and Fenwick nodes only (the backward reads
 // them): P at simt_ws_offset_P, Node_j at slot j of simt_ws_offset_nodes.
 cudaError_t simt_build_nodes(const SimtFwdArgs &A);
+// The same with the chunk states and chunk gate totals already in place
+// (totals [BH][N] fp32 at the workspace start, H_{j-1} in node slot j):
+// only the prefix and the Fenwick scan run.
+cudaError_t simt_nodes_from_states(const SimtFwdArgs &A);
 
 }  // namespace lla
