@@ -17,10 +17,10 @@
 //   * intra-chunk output: o_a = sum_{s <= a} lambda_a[l(a,s)] exp(gam_a - gam_s) Cm[a,s] v_s,
 //     Cm = inclusive_lower(Q K^T) T  (Cm[a,a] = beta_a q_a.k_a: level 0).
 // Two launches: gdn_chunk_prep_kernel does everything that is local to a
-// chunk for all chunks at once (one CTA per chunk; fp32 CUDA cores; the
-// inverse by 16 x 16 diagonal blocks and block substitution), writing the
-// intra-chunk output, qt and w (transposed, for the scan's row-per-lane
-// reads), H and exp(gam_{C-1}); gdn_chunk_scan_kernel walks the chunks of one
+// chunk for all chunks at once (one CTA per chunk; the products on TF32
+// tensor-core fragments with split operands, the inverse by 16 x 16 diagonal
+// blocks and block substitution on CUDA cores), writing the intra-chunk
+// output, the rows of q~ and W, H and exp(gam_{C-1}); gdn_chunk_scan_kernel walks the chunks of one
 // (batch, head) in order for 8 value columns (a state column only mixes with
 // itself), keeping the chunk-level Fenwick states in shared memory: read-out
 // added to the output, transition, and the fold of H into the new level.
@@ -33,66 +33,30 @@ namespace {
 constexpr int kGC = 64;        // chunk length
 constexpr int kGCBits = 6;     // log2(kGC)
 constexpr int kGT = 256;       // threads of both kernels
-constexpr int kLdm = kGC + 1;  // row stride of the 64 x 64 matrices in shared memory
+constexpr int kLdm = kGC + 4;  // row stride of the 64 x 64 matrices in shared memory (fragment rows: distinct banks)
 constexpr int kGW = 8;         // value columns of a scan CTA
 constexpr size_t kMaxSmem = 227 * 1024;  // dynamic shared memory of one CTA
 
 // acc[i][j] += sum_{k < K} A(ty + 16 i, k) B(k, tx + 16 j), A(r, k) = A[r ar + k ak],
-// B(k, c) = B[k bk + c bc]; columns j >= cj are skipped.  The thread's rows
-// and columns fall one in each 16-wide block, so a triangular operand zeroes
-// whole (block, block) pairs, which MODE skips at compile time:
-//   kFull      every product;
-//   kOutLower  the result is kept below the block diagonal only: j > i skipped;
-//   kALower    A(r, k) = 0 for k > r (K = 64 in blocks of 16: block kb skips rows i < kb);
-//   kBUpper    B(k, c) = 0 for k > c (block kb skips columns j < kb).
-enum { kFull = 0, kOutLower = 1, kALower = 2, kBUpper = 3 };
-
-template <int RI, int CJ, int MODE = kFull>
+// B(k, c) = B[k bk + c bc]: fp32 CUDA cores, for the few products of any K
+// (the buckets of a ragged end).
+template <int RI, int CJ>
 __device__ __forceinline__ void mm16(float (&acc)[RI][CJ], const float *A, int ar, int ak, const float *B, int bk,
-                                     int bc, int K, int ty, int tx, int cj = CJ)
+                                     int bc, int K, int ty, int tx)
 {
     const float *pa = A + ty * ar;
     const float *pb = B + tx * bc;
-    if constexpr (MODE == kALower || MODE == kBUpper) {
-#pragma unroll
-        for (int kb = 0; kb < 4; kb++) {
 #pragma unroll 4
-            for (int kk = 0; kk < 16; kk++) {
-                const int k = 16 * kb + kk;
-                float a[RI], b[CJ];
+    for (int k = 0; k < K; k++) {
+        float a[RI], b[CJ];
 #pragma unroll
-                for (int i = 0; i < RI; i++)
-                    a[i] = (MODE == kALower && i < kb) ? 0.f : pa[16 * i * ar + k * ak];
+        for (int i = 0; i < RI; i++) a[i] = pa[16 * i * ar + k * ak];
 #pragma unroll
-                for (int j = 0; j < CJ; j++)
-                    b[j] = ((MODE == kBUpper && j < kb) || j >= cj) ? 0.f : pb[k * bk + 16 * j * bc];
+        for (int j = 0; j < CJ; j++) b[j] = pb[k * bk + 16 * j * bc];
 #pragma unroll
-                for (int i = 0; i < RI; i++) {
-                    if (MODE == kALower && i < kb) continue;
+        for (int i = 0; i < RI; i++)
 #pragma unroll
-                    for (int j = 0; j < CJ; j++) {
-                        if (MODE == kBUpper && j < kb) continue;
-                        acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-                    }
-                }
-            }
-        }
-    } else {
-#pragma unroll 4
-        for (int k = 0; k < K; k++) {
-            float a[RI], b[CJ];
-#pragma unroll
-            for (int i = 0; i < RI; i++) a[i] = pa[16 * i * ar + k * ak];
-#pragma unroll
-            for (int j = 0; j < CJ; j++) b[j] = j < cj ? pb[k * bk + 16 * j * bc] : 0.f;
-#pragma unroll
-            for (int i = 0; i < RI; i++)
-#pragma unroll
-                for (int j = 0; j < CJ; j++) {
-                    if (MODE == kOutLower && j > i) continue;
-                    acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-                }
-        }
+            for (int j = 0; j < CJ; j++) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
     }
 }
 
@@ -136,21 +100,108 @@ __device__ __forceinline__ void zero(float (&acc)[RI][CJ])
         for (int j = 0; j < CJ; j++) acc[i][j] = 0.f;
 }
 
+__device__ __forceinline__ uint32_t to_tf32(float x)
+{
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo)
+{
+    hi = to_tf32(x);
+    lo = to_tf32(x - __uint_as_float(hi));
+}
+
+// d += a b, m16n8k8, A row-major 16 x 8, B column-major 8 x 8, TF32 in, fp32 accumulate.
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+                 "{%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+
+// Warp-level tensor-core product on m16n8k8 TF32 tiles: acc[i] is the tile
+// tt = warp + 8 i of an (16 MT) x (8 NT) result (row block tt % MT, column
+// block tt / MT; tiles past MT x NT are skipped), lane 4 g + t holding rows
+// g, g + 8 and columns 2 t, 2 t + 1:
+//   acc += sum_k A(r, k) B(k, c),  A(r, k) = A[r ar + k ak], B(k, c) = B[k bk + c bc].
+// SA / SB split that operand into TF32 high and remainder parts (an operand
+// exact in TF32, such as a bf16 input, is used whole); the partial products
+// hi.hi, hi.lo, lo.hi keep about 21 bits.  Triangular operands skip k-steps:
+// ALOW (A(r, k) = 0 for k > r), BLOW (B(k, c) = 0 for c > k); OUTLOW skips
+// tiles wholly above the diagonal (the caller keeps the lower part only).
+template <int NTW, int MT, int NT, bool SA, bool SB, bool ALOW, bool BLOW, bool OUTLOW>
+__device__ __forceinline__ void warp_mma(float (&acc)[NTW][4], const float *A, int ar, int ak, const float *B, int bk,
+                                         int bc, int K, int warp, int g, int t)
+{
+#pragma unroll
+    for (int i = 0; i < NTW; i++) {
+        acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+        const int tt = warp + 8 * i;
+        if (tt >= MT * NT) continue;
+        const int mt = tt % MT, nt = tt / MT;
+        const float *a0 = A + (16 * mt + g) * ar + t * ak;
+        const float *b0 = B + t * bk + (8 * nt + g) * bc;
+        const int k_lo = BLOW ? 8 * nt : 0;
+        int k_hi = ALOW ? min(K, 16 * mt + 16) : K;
+        if (OUTLOW && 8 * nt > 16 * mt + 15) k_hi = k_lo;
+#pragma unroll 2
+        for (int k0 = k_lo; k0 < k_hi; k0 += 8) {
+            const float ax[4] = {a0[k0 * ak], a0[8 * ar + k0 * ak], a0[(k0 + 4) * ak], a0[8 * ar + (k0 + 4) * ak]};
+            const float bx[2] = {b0[k0 * bk], b0[(k0 + 4) * bk]};
+            uint32_t ah[4], al[4], bh[2], bl[2];
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                if (SA) split_tf32(ax[e], ah[e], al[e]);
+                else ah[e] = __float_as_uint(ax[e]);
+            }
+#pragma unroll
+            for (int e = 0; e < 2; e++) {
+                if (SB) split_tf32(bx[e], bh[e], bl[e]);
+                else bh[e] = __float_as_uint(bx[e]);
+            }
+            mma_tf32(acc[i], ah, bh[0], bh[1]);
+            if (SB) mma_tf32(acc[i], ah, bl[0], bl[1]);
+            if (SA) mma_tf32(acc[i], al, bh[0], bh[1]);
+        }
+    }
+}
+
+// Calls f(row, col, value) for every element of the warp's tiles of warp_mma.
+template <int NTW, int MT, int NT, typename F>
+__device__ __forceinline__ void warp_tiles(const float (&acc)[NTW][4], int warp, int g, int t, F &&f)
+{
+#pragma unroll
+    for (int i = 0; i < NTW; i++) {
+        const int tt = warp + 8 * i;
+        if (tt >= MT * NT) continue;
+        const int r = 16 * (tt % MT) + g, c = 8 * (tt / MT) + 2 * t;
+        f(r, c, acc[i][0], acc[i][1]);
+        f(r + 8, c, acc[i][2], acc[i][3]);
+    }
+}
+
 // Shared memory of the prep kernel, in floats after the 64 running gate sums.
 struct PrepLayout {
-    int ldk, ldq;
+    int ldk, ldq, ldv;
     size_t k, q, v, m1, m2, x, y, lam, beta, floats;
 };
 
 __host__ __device__ inline PrepLayout prep_layout(int dk, int dv, int L)
 {
     PrepLayout P;
-    P.ldk = dk + 1;                        // odd strides: rows read across lanes never share a bank
-    P.ldq = (dk > dv ? dk : dv) + 1;       // Q, later U = T' V
+    // strides = 4 (mod 32) words: a fragment's rows g and columns t land in
+    // 4 g + t, 32 distinct banks; V (read as k-rows t, columns g) uses 8 (mod 32)
+    P.ldk = dk + 4;
+    P.ldq = (dk > dv ? dk : dv) + 4;       // Q, later U = T' V
+    P.ldv = dv + 8;
     P.k = kGC;                             // after gam[64]
     P.q = P.k + (size_t)kGC * P.ldk;
     P.v = P.q + (size_t)kGC * P.ldq;
-    P.m1 = P.v + (size_t)kGC * dv;
+    P.m1 = P.v + (size_t)kGC * P.ldv;
     P.m2 = P.m1 + (size_t)kGC * kLdm;
     P.x = P.m2 + (size_t)kGC * kLdm;
     P.y = P.x + (size_t)kGC * kLdm;        // [3][16][17] block products of the inverse
@@ -176,61 +227,61 @@ inline WsLayout ws_layout(long long BH, int N, int dk, int dv)
 }
 
 // Steps 7 to 9 of the prep kernel for dv = 16 CJ: the intra-chunk output,
-// the chunk state H, and the low-bit states of a ragged last chunk.
-template <int DK, int CJ>
+// the chunk state H, and the low-bit states of a ragged last chunk.  SIN:
+// the inputs (K, V) need splitting for TF32 (fp32 inputs; bf16 are exact).
+template <int DK, int CJ, bool SIN>
 __device__ __forceinline__ void prep_tail(float *M1, const float *M2, const float *Xs, const float *Ks, float *Qs,
                                           const float *Vs, const float *gam, float *__restrict__ out,
                                           float *__restrict__ ws_h, float *__restrict__ ws_gend,
                                           float *__restrict__ state_out, long long tok0, long long bh, int ci, int N,
-                                          int nv, int dv, int ldq, int Ls_out)
+                                          int nv, int dv, int ldq, int ldv, int Ls_out)
 {
+    constexpr int DV = 16 * CJ;
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-    // 7. intra-chunk output
+    const int warp = tid >> 5, g = (tid & 31) >> 2, t = tid & 3;
+    // 7. intra-chunk output M V
     {
-        float acc[4][CJ];
-        zero(acc);
-        mm16<4, CJ, kALower>(acc, M2, kLdm, 1, Vs, dv, 1, kGC, ty, tx);
-#pragma unroll
-        for (int i = 0; i < 4; i++) {
-            const int a = ty + 16 * i;
-            if (a < nv) {
-#pragma unroll
-                for (int j = 0; j < CJ; j++) out[(tok0 + a) * dv + tx + 16 * j] = acc[i][j];
-            }
-        }
+        float acc[CJ][4];
+        warp_mma<CJ, 4, DV / 8, true, SIN, true, false, false>(acc, M2, kLdm, 1, Vs, ldv, 1, kGC, warp, g, t);
+        warp_tiles<CJ, 4, DV / 8>(acc, warp, g, t, [&](int r, int c, float x, float y) {
+            if (r < nv) *reinterpret_cast<float2 *>(out + (tok0 + r) * dv + c) = make_float2(x, y);
+        });
     }
     __syncthreads();  // M1 (Cm) and Qs are free
 
     // 8. T' = T diag(exp(gam_{C-1} - gam)) into M1, U = T' V into Qs, H = K^T U
     const float Gam = gam[kGC - 1];
     for (int e = tid; e < kGC * kGC; e += kGT) {
-        const int a = e >> kGCBits, b = e & (kGC - 1);
-        M1[a * kLdm + b] = Xs[a * kLdm + b] * expf(Gam - gam[b]);
+        const int r = e >> kGCBits, b = e & (kGC - 1);
+        M1[r * kLdm + b] = Xs[r * kLdm + b] * expf(Gam - gam[b]);
     }
     __syncthreads();
+    constexpr int HT = (DK / 16) * (DV / 8);  // m16n8 tiles of H
     auto kt_u = [&](int lo, int hi, float *dst) {
         // U = T'[:, lo:hi] V[lo:hi, :] into Qs, then dst = K^T U (dk x dv)
-        {
+        if (lo == 0 && hi == kGC) {
+            float acc[CJ][4];
+            warp_mma<CJ, 4, DV / 8, true, SIN, true, false, false>(acc, M1, kLdm, 1, Vs, ldv, 1, kGC, warp, g, t);
+            warp_tiles<CJ, 4, DV / 8>(acc, warp, g, t, [&](int r, int c, float x, float y) {
+                *reinterpret_cast<float2 *>(Qs + r * ldq + c) = make_float2(x, y);
+            });
+        } else {
             float acc[4][CJ];
             zero(acc);
-            if (lo == 0 && hi == kGC)
-                mm16<4, CJ, kALower>(acc, M1, kLdm, 1, Vs, dv, 1, kGC, ty, tx);
-            else
-                mm16<4, CJ>(acc, M1 + lo, kLdm, 1, Vs + lo * dv, dv, 1, hi - lo, ty, tx);
+            mm16<4, CJ>(acc, M1 + lo, kLdm, 1, Vs + lo * ldv, ldv, 1, hi - lo, ty, tx);
 #pragma unroll
             for (int i = 0; i < 4; i++)
 #pragma unroll
                 for (int j = 0; j < CJ; j++) Qs[(ty + 16 * i) * ldq + tx + 16 * j] = acc[i][j];
         }
         __syncthreads();
-        constexpr int RI = DK / 16;
-        float acc[RI][CJ];
-        zero(acc);
-        mm16<RI, CJ>(acc, Ks, 1, DK + 1, Qs, ldq, 1, kGC, ty, tx);  // A(r, a) = K[a][r], B(a, c) = U[a][c]
-#pragma unroll
-        for (int i = 0; i < RI; i++)
-#pragma unroll
-            for (int j = 0; j < CJ; j++) dst[(ty + 16 * i) * dv + tx + 16 * j] = acc[i][j];
+        float acc[(HT + 7) / 8][4];
+        // A(r, a) = K[a][r], B(a, c) = U[a][c]
+        warp_mma<(HT + 7) / 8, DK / 16, DV / 8, SIN, true, false, false, false>(acc, Ks, 1, DK + 4, Qs, ldq, 1, kGC,
+                                                                                warp, g, t);
+        warp_tiles<(HT + 7) / 8, DK / 16, DV / 8>(acc, warp, g, t, [&](int r, int c, float x, float y) {
+            *reinterpret_cast<float2 *>(dst + r * dv + c) = make_float2(x, y);
+        });
     };
     kt_u(0, kGC, ws_h + (bh * N + ci) * (long long)DK * dv);
     if (tid == 0) ws_gend[bh * N + ci] = expf(Gam);
@@ -258,12 +309,14 @@ gdn_chunk_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, cons
     extern __shared__ __align__(16) float sm[];
     const PrepLayout P = prep_layout(DK, dv, L);
     if (P.floats * sizeof(float) > dynamic_smem_bytes()) return;
-    const int ldk = P.ldk, ldq = P.ldq;
+    const int ldk = P.ldk, ldq = P.ldq, ldv = P.ldv;
+    constexpr bool SIN = sizeof(Tin) == 4;  // fp32 inputs are split for TF32; bf16 are exact
     float *gam = sm;
     float *Ks = sm + P.k, *Qs = sm + P.q, *Vs = sm + P.v;
     float *M1 = sm + P.m1, *M2 = sm + P.m2, *Xs = sm + P.x, *Ys = sm + P.y;
     float *ls = sm + P.lam, *bs = sm + P.beta;
-    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, fg = (tid & 31) >> 2, ft = tid & 3;  // fragment lane: row group, column
     const int ci = blockIdx.x;
     const long long bh = (long long)blockIdx.z * H + blockIdx.y;
     const long long tok0 = bh * T + (long long)ci * kGC;
@@ -287,9 +340,10 @@ gdn_chunk_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, cons
     }
     for (int e = tid; e < kGC * dv / EPV; e += kGT) {
         float xv[EPV];
-        load16_f32<Tin>(v + tok0 * dv + (long long)e * EPV, e * EPV / dv < nv, xv);
+        const int a = e * EPV / dv, c = e * EPV % dv;
+        load16_f32<Tin>(v + tok0 * dv + (long long)e * EPV, a < nv, xv);
 #pragma unroll
-        for (int u = 0; u < EPV; u++) Vs[e * EPV + u] = xv[u];
+        for (int u = 0; u < EPV; u++) Vs[a * ldv + c + u] = xv[u];
     }
     for (int e = tid; e < kGC * L; e += kGT) ls[e] = e / L < nv ? lam[tok0 * L + e] : 0.f;
     for (int e = tid; e < kGC * kLdm; e += kGT) Xs[e] = 0.f;
@@ -312,18 +366,17 @@ gdn_chunk_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, cons
     // 2. M1 = strict_lower(diag(beta) K K^T), M2 = inclusive_lower(Q K^T)
     {
         float ak[4][4], aq[4][4];
-        zero(ak);
-        zero(aq);
-        mm16<4, 4, kOutLower>(ak, Ks, ldk, 1, Ks, 1, ldk, DK, ty, tx);
-        mm16<4, 4, kOutLower>(aq, Qs, ldq, 1, Ks, 1, ldk, DK, ty, tx);
-#pragma unroll
-        for (int i = 0; i < 4; i++)
-#pragma unroll
-            for (int j = 0; j < 4; j++) {
-                const int a = ty + 16 * i, b = tx + 16 * j;
-                M1[a * kLdm + b] = b < a ? bs[a] * ak[i][j] : 0.f;
-                M2[a * kLdm + b] = b <= a ? aq[i][j] : 0.f;
-            }
+        // A(a, r) = K[a][r] (or Q), B(r, b) = K[b][r]
+        warp_mma<4, 4, 8, SIN, SIN, false, false, true>(ak, Ks, ldk, 1, Ks, 1, ldk, DK, warp, fg, ft);
+        warp_mma<4, 4, 8, SIN, SIN, false, false, true>(aq, Qs, ldq, 1, Ks, 1, ldk, DK, warp, fg, ft);
+        warp_tiles<4, 4, 8>(ak, warp, fg, ft, [&](int r, int c, float x, float y) {
+            M1[r * kLdm + c] = c < r ? bs[r] * x : 0.f;
+            M1[r * kLdm + c + 1] = c + 1 < r ? bs[r] * y : 0.f;
+        });
+        warp_tiles<4, 4, 8>(aq, warp, fg, ft, [&](int r, int c, float x, float y) {
+            M2[r * kLdm + c] = c <= r ? x : 0.f;
+            M2[r * kLdm + c + 1] = c + 1 <= r ? y : 0.f;
+        });
     }
     __syncthreads();
 
@@ -381,51 +434,47 @@ gdn_chunk_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, cons
     //    lambda_a[l(a,s)] exp(gam_a - gam_s) Cm[a,s] into M2
     {
         float acc[4][4];
-        zero(acc);
-        mm16<4, 4, kALower>(acc, M2, kLdm, 1, Xs, kLdm, 1, kGC, ty, tx);
+        warp_mma<4, 4, 8, true, true, true, true, false>(acc, M2, kLdm, 1, Xs, kLdm, 1, kGC, warp, fg, ft);
         __syncthreads();  // every read of M1 (done) and M2 precedes the writes
+        warp_tiles<4, 4, 8>(acc, warp, fg, ft, [&](int r, int c, float x, float y) {
+            const float v2[2] = {x, y};
 #pragma unroll
-        for (int i = 0; i < 4; i++)
-#pragma unroll
-            for (int j = 0; j < 4; j++) {
-                const int a = ty + 16 * i, s = tx + 16 * j;
-                M1[a * kLdm + s] = acc[i][j];
+            for (int u = 0; u < 2; u++) {
+                const int s2 = c + u;
+                M1[r * kLdm + s2] = v2[u];
                 float m = 0.f;
-                if (s <= a && a < nv) {
-                    const int lev = 32 - __clz(a ^ s);
-                    m = ls[a * L + lev] * expf(gam[a] - gam[s]) * acc[i][j];
+                if (s2 <= r && r < nv) {
+                    const int lev = 32 - __clz(r ^ s2);
+                    m = ls[r * L + lev] * expf(gam[r] - gam[s2]) * v2[u];
                 }
-                M2[a * kLdm + s] = m;
+                M2[r * kLdm + s2] = m;
             }
+        });
     }
     __syncthreads();
 
     // 6. q~ = diag(exp(gam)) (Q - Cm K) and W = T K, rows [a][r]: q~ in rows 0..63, W in 64..127
     {
         float *qw_ws = ws_qw + (bh * N + ci) * (2LL * DK * kGC);
-        constexpr int CJ = DK / 16;
-        float aw[4][CJ], ac[4][CJ];
-        zero(aw);
-        zero(ac);
-        mm16<4, CJ, kALower>(aw, Xs, kLdm, 1, Ks, ldk, 1, kGC, ty, tx);  // A(a, b) = T[a][b], B(b, r) = K[b][r]
-        mm16<4, CJ, kALower>(ac, M1, kLdm, 1, Ks, ldk, 1, kGC, ty, tx);  // A(a, b) = Cm[a][b]
-#pragma unroll
-        for (int i = 0; i < 4; i++) {
-            const int a = ty + 16 * i;
-            const float ea = expf(gam[a]);
-#pragma unroll
-            for (int j = 0; j < CJ; j++) {
-                const int r = tx + 16 * j;
-                qw_ws[a * DK + r] = ea * (Qs[a * ldq + r] - ac[i][j]);
-                qw_ws[(kGC + a) * DK + r] = aw[i][j];
-            }
-        }
+        constexpr int NTW = DK / 16;
+        float aw[NTW][4], ac[NTW][4];
+        // A(a, b) = T[a][b] (or Cm), B(b, r) = K[b][r]
+        warp_mma<NTW, 4, DK / 8, true, SIN, true, false, false>(aw, Xs, kLdm, 1, Ks, ldk, 1, kGC, warp, fg, ft);
+        warp_mma<NTW, 4, DK / 8, true, SIN, true, false, false>(ac, M1, kLdm, 1, Ks, ldk, 1, kGC, warp, fg, ft);
+        warp_tiles<NTW, 4, DK / 8>(aw, warp, fg, ft, [&](int r, int c, float x, float y) {
+            *reinterpret_cast<float2 *>(qw_ws + (kGC + r) * DK + c) = make_float2(x, y);
+        });
+        warp_tiles<NTW, 4, DK / 8>(ac, warp, fg, ft, [&](int r, int c, float x, float y) {
+            const float ea = expf(gam[r]);
+            *reinterpret_cast<float2 *>(qw_ws + r * DK + c) =
+                make_float2(ea * (Qs[r * ldq + c] - x), ea * (Qs[r * ldq + c + 1] - y));
+        });
     }
     switch (cj) {
-    case 1: prep_tail<DK, 1>(M1, M2, Xs, Ks, Qs, Vs, gam, out, ws_h, ws_gend, state_out, tok0, bh, ci, N, nv, dv, ldq, Ls_out); break;
-    case 2: prep_tail<DK, 2>(M1, M2, Xs, Ks, Qs, Vs, gam, out, ws_h, ws_gend, state_out, tok0, bh, ci, N, nv, dv, ldq, Ls_out); break;
-    case 4: prep_tail<DK, 4>(M1, M2, Xs, Ks, Qs, Vs, gam, out, ws_h, ws_gend, state_out, tok0, bh, ci, N, nv, dv, ldq, Ls_out); break;
-    default: prep_tail<DK, 8>(M1, M2, Xs, Ks, Qs, Vs, gam, out, ws_h, ws_gend, state_out, tok0, bh, ci, N, nv, dv, ldq, Ls_out); break;
+    case 1: prep_tail<DK, 1, SIN>(M1, M2, Xs, Ks, Qs, Vs, gam, out, ws_h, ws_gend, state_out, tok0, bh, ci, N, nv, dv, ldq, ldv, Ls_out); break;
+    case 2: prep_tail<DK, 2, SIN>(M1, M2, Xs, Ks, Qs, Vs, gam, out, ws_h, ws_gend, state_out, tok0, bh, ci, N, nv, dv, ldq, ldv, Ls_out); break;
+    case 4: prep_tail<DK, 4, SIN>(M1, M2, Xs, Ks, Qs, Vs, gam, out, ws_h, ws_gend, state_out, tok0, bh, ci, N, nv, dv, ldq, ldv, Ls_out); break;
+    default: prep_tail<DK, 8, SIN>(M1, M2, Xs, Ks, Qs, Vs, gam, out, ws_h, ws_gend, state_out, tok0, bh, ci, N, nv, dv, ldq, ldv, Ls_out); break;
     }
 }
 
@@ -501,28 +550,6 @@ __device__ __forceinline__ int k_off(int a, int r)
 {
     constexpr int epc = 16 / (int)sizeof(Tin);
     return a * DK + ((((r / epc) ^ k_piece_xor<DK, Tin>(a)) * epc) + (r % epc));
-}
-
-__device__ __forceinline__ uint32_t to_tf32(float x)
-{
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
-
-__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo)
-{
-    hi = to_tf32(x);
-    lo = to_tf32(x - __uint_as_float(hi));
-}
-
-// d += a b, m16n8k8, A row-major 16 x 8, B column-major 8 x 8, TF32 in, fp32 accumulate.
-__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
-{
-    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-                 "{%8, %9}, {%0, %1, %2, %3};"
-                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 // The next (up to) four slots of rem, lowest first; returns how many.
