@@ -31,7 +31,7 @@ constexpr int kKT = 128;                      // tile rows (two chunks of 64)
 constexpr int kKD = 128;                      // dk = dv
 constexpr uint32_t kKBuf = kKT * kKD * 2;     // bf16 128 x 128: 32 KB
 constexpr uint32_t kKHalf = kKBuf / 2;
-constexpr int kKThreads = 128;
+constexpr int kKThreads = 256;  // staging: twice the loads in flight; drain: a row's two column halves
 constexpr uint32_t kKWait = 1u << 22;
 
 struct __align__(1024) KeySmem {
@@ -66,7 +66,8 @@ bwd_key_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_consta
 {
     extern __shared__ uint8_t smem_raw[];
     KeySmem &s = *reinterpret_cast<KeySmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int p = threadIdx.x;  // tile row
+    const int tid = threadIdx.x;
+    const int p = tid & 127, half = tid >> 7;  // tile row, column half of the drain
     const int pair = blockIdx.x;
     const int bh = blockIdx.y;
     const int c0 = 2 * pair;                 // first chunk of the pair
@@ -79,7 +80,7 @@ bwd_key_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_consta
     for (int m = 1; m < nlev; m++)
         if (((c0 >> m) & 1) == 0 && (((long long)(c0 >> m) + 1) << m) < N) levs[nl++] = m;
     if (!lev0 && nl == 0) return;
-    if (p == 0) {
+    if (tid == 0) {
         mbar_init(&s.bar_load, 1);
         mbar_init(&s.bar_mma[0], 1);
         mbar_init(&s.bar_mma[1], 1);
@@ -93,7 +94,7 @@ bwd_key_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_consta
             tma_load_3d(s.v + h * kKHalf, &map_v, &s.bar_load, h * 64, pair * kKT, bh);
         }
     }
-    if (p < 32) {
+    if (tid < 32) {
         tmem_alloc(&s.tmem, 512);
         tmem_relinquish();
     }
@@ -128,12 +129,12 @@ bwd_key_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_consta
         const int m = is0 ? 0 : levs[n - (lev0 ? 1 : 0)];
         const int b = (c0 >> m) + 1;
         const float *Rm = R + (((long long)bh * nblocks) + off_tab[m] + b) * kKD * kKD;
-        const float c = is0 ? 1.f : (float)exp(Pb[b << m] - Pend);
+        const float c = is0 ? 1.f : expf((float)(Pb[b << m] - Pend));
         if (n >= 2 && !mbar_wait(&s.bar_mma[buf], ((n - 2) >> 1) & 1, kKWait)) key_err(err, 2);
         stage(buf, Rm, c);
         fence_proxy_async_smem();
         __syncthreads();
-        if (p == 0) {
+        if (tid == 0) {
             tc_fence_after_sync();
             const uint32_t dk_acc = is0 ? acc_k0 : acc_k, dv_acc = is0 ? acc_v0 : acc_v;
             const bool acc = is0 ? false : acc_started;
@@ -145,7 +146,7 @@ bwd_key_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_consta
         }
         if (!is0) acc_started = true;
     }
-    if (p == 0) umma_commit(&s.bar_done);
+    if (tid == 0) umma_commit(&s.bar_done);
     if (!mbar_wait(&s.bar_done, 0, kKWait)) key_err(err, 2);
     tc_fence_after_sync();
     // drain: row p; weights rho (shared levels) and f0 (level 0, first chunk)
@@ -153,15 +154,15 @@ bwd_key_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_consta
     const int chunk = c0 + (p >> 6);
     const float gam = (row < T) ? gamma[(long long)bh * T + row] : 0.f;
     const double Gs = Pb[min(chunk, N)] + (double)gam;
-    const float rho = (row < T) ? (float)exp(Pend - Gs) : 0.f;
-    const float f0 = (lev0 && p < 64) ? (float)exp(Pb[c0 + 1] - Gs) : 0.f;
+    const float rho = (row < T) ? expf((float)(Pend - Gs)) : 0.f;
+    const float f0 = (lev0 && p < 64) ? expf((float)(Pb[c0 + 1] - Gs)) : 0.f;
     const uint32_t lane_off = (uint32_t)((p >> 5) * 32) << 16;
     const bool have_shared = nl > 0;
     for (int which = 0; which < 2; which++) {
         const uint32_t a_sh = which == 0 ? acc_k : acc_v, a_0 = which == 0 ? acc_k0 : acc_v0;
         float *dst = (which == 0 ? dk : dv) + ((long long)bh * T + row) * kKD;
 #pragma unroll 1
-        for (int cb = 0; cb < kKD; cb += 16) {
+        for (int cb = half * 64; cb < half * 64 + 64; cb += 16) {
             float x[16], y[16];
             tmem_ld16(a_sh + lane_off + cb, x);
             tmem_ld16(a_0 + lane_off + cb, y);
@@ -187,7 +188,7 @@ bwd_key_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_consta
     }
     tc_fence_before_sync();
     __syncthreads();
-    if (p < 32) tmem_dealloc(tm, 512);
+    if (tid < 32) tmem_dealloc(tm, 512);
 }
 
 }  // namespace

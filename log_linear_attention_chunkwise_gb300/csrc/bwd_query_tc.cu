@@ -35,6 +35,8 @@ struct __align__(1024) QuerySmem {
     uint8_t ohi[kQBuf], olo[kQBuf];     // dO tile, high and remainder parts
     uint8_t nhi[2][kQBuf], nlo[2][kQBuf];  // node stages
     float part[2][kQT];                 // q.U partial sums of the second half
+    float wt[kQMaxPath][kQT];           // per path node and row: exp(G_t - P_j) (0 where it does not apply)
+    float lwt[kQMaxPath][kQT];          // the same times lambda_t at the node's level
     uint64_t bar_mma[2];
     uint32_t tmem;
 };
@@ -87,6 +89,19 @@ bwd_query_tc_kernel(const Tin *__restrict__ q, const float *__restrict__ dout, c
         tmem_alloc(&s.tmem, 256);
         tmem_relinquish();
     }
+    // read-out weights of every path node for this row (the halves split the
+    // nodes): w = exp(G_t - P_j) from one fp64 difference, lw = lambda_t[l] w
+    {
+        const double Gt = Pb[min(chunk, N)] + (double)(row_ok ? gamma[tok] : 0.f);
+        const float *lam_row = lam + tok * L;
+        for (int n = half; n < np; n += 2) {
+            const int j = js[n];
+            const bool mine = row_ok && (j <= chunk);  // node 2p+1 concerns the second chunk only
+            const float w = mine ? expf((float)(Gt - Pb[j])) : 0.f;
+            s.wt[n][row] = w;
+            s.lwt[n][row] = mine ? lam_row[cbits + 1 + (__ffs(j) - 1)] * w : 0.f;
+        }
+    }
     // dO tile and the first node
     const int nrows = (int)min((long long)kQT, (long long)T - (long long)pair * kQT);
     {
@@ -105,15 +120,21 @@ bwd_query_tc_kernel(const Tin *__restrict__ q, const float *__restrict__ dout, c
     tc_fence_after_sync();
     const uint32_t tm = s.tmem;
     const uint32_t idesc = idesc_bf16_f32(128, 128, false, false);
-    // this thread's q half row, and G_t
+    // this thread's q half row (16-byte loads), and G_t
     float qv[64];
     {
-        const Tin *qr = q + tok * kQD + half * 64;
+        const uint4 *qr = reinterpret_cast<const uint4 *>(q + tok * kQD + half * 64);
 #pragma unroll
-        for (int c = 0; c < 64; c++) qv[c] = row_ok ? to_f32(qr[c]) : 0.f;
+        for (int u = 0; u < 8; u++) {
+            const uint4 w4 = row_ok ? qr[u] : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t h4[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                qv[8 * u + 2 * e] = __uint_as_float(h4[e] << 16);  // bf16 -> fp32: the high half of the word
+                qv[8 * u + 2 * e + 1] = __uint_as_float(h4[e] & 0xffff0000u);
+            }
+        }
     }
-    const double Gt = Pb[min(chunk, N)] + (double)(row_ok ? gamma[tok] : 0.f);
-    const float *lam_row = lam + tok * L;
     float dqa[64];
 #pragma unroll
     for (int c = 0; c < 64; c++) dqa[c] = 0.f;
@@ -130,10 +151,8 @@ bwd_query_tc_kernel(const Tin *__restrict__ q, const float *__restrict__ dout, c
         const int b = n & 1;
         const int j = js[n];
         const int lev = cbits + 1 + (__ffs(j) - 1);
-        // node 2p+1 concerns the second chunk only; the path of 2p both
         const bool mine = row_ok && (j <= chunk);
-        const float w = mine ? (float)exp(Gt - Pb[j]) : 0.f;
-        const float lw = mine ? lam_row[lev] * w : 0.f;
+        const float w = s.wt[n][row], lw = s.lwt[n][row];
         if (!mbar_wait(&s.bar_mma[b], (n >> 1) & 1, kQWait)) q_err(err, 2);
         tc_fence_after_sync();
         float dot = 0.f;
