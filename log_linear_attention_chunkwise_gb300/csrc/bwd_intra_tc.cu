@@ -34,6 +34,7 @@ struct __align__(1024) IntraSmem {
     uint8_t ohi[kIB], olo[kIB];  // dO split
     uint8_t v[kIB];              // V, then the high part of W1 / W2
     uint8_t wmid[kIB], wlo[kIB]; // the second and third parts of W1 / W2
+    float gam[kIT];              // in-chunk gate sums of the tile's rows
     uint64_t bar_load, bar_mma;
     uint32_t tmem;
 };
@@ -130,10 +131,11 @@ bwd_intra_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
     // dO tile, split
     {
         uint8_t *d[2] = {s.ohi, s.olo};
-        stage_split_tile<2, kIThreads>(d, dout + ((long long)bh * T + (long long)pair * kIT) * kID, kID, nullptr, 1.f,
+        stage_split_tile<2, kIThreads, 8>(d, dout + ((long long)bh * T + (long long)pair * kIT) * kID, kID, nullptr, 1.f,
                             (int)min((long long)kIT, (long long)T - (long long)pair * kIT));
     }
     const float gam_t = row_ok ? gamma[tok] : 0.f;
+    s.gam[t] = gam_t;
     fence_proxy_async_smem();
     tc_fence_before_sync();
     __syncthreads();
@@ -176,8 +178,7 @@ bwd_intra_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                 const int b = c0 + e;
                 float x1 = 0.f, x2 = 0.f;
                 if (b <= a && row_ok) {
-                    const long long sk = (long long)bh * T + (long long)pair * kIT + cb + b;
-                    const float dec = __expf(gam_t - gamma[sk]);
+                    const float dec = __expf(gam_t - s.gam[cb + b]);
                     const int lev = 32 - __clz(a ^ b);
                     const float m = lamv[lev] * dec;
                     x1 = m * pv[e];

@@ -2,8 +2,9 @@
 // 128; chunk 64):  piece = sum_t w_t q_t dO_t^T over a run of tokens of one
 // (level m, block b), w_t = lambda_t[c+1+m] exp(G_t - G_ref) (see the
 // CUDA-core backward).  A CTA takes one piece (up to 16 chunks) in 128-token
-// tiles: TMA brings the q tile; the threads scale their dO row by w (0 for
-// tokens outside the piece) and split it into bf16 high and remainder parts;
+// tiles: TMA brings the q tile; two threads per token row scale half the dO
+// row each by w (0 for tokens outside the piece) and split it into bf16 high
+// and remainder parts;
 // one thread issues piece += Q^T (w dO)_hi + Q^T (w dO)_lo (M = dk, N = dv,
 // K = 128 tokens) into a tensor-memory accumulator.  The finished piece is
 // written to its own slot; the reduction that follows sums a block's pieces
@@ -21,7 +22,7 @@ constexpr int kPT = 128;
 constexpr int kPDm = 128;
 constexpr uint32_t kPB = kPT * kPDm * 2;  // 32 KB
 constexpr uint32_t kPH = kPB / 2;
-constexpr int kPThreads = 128;
+constexpr int kPThreads = 256;  // (token row, column half)
 constexpr uint32_t kPWait = 1u << 22;
 
 struct __align__(1024) PieceSmem {
@@ -39,7 +40,8 @@ bwd_piece_tc_kernel(const __grid_constant__ CUtensorMap map_q, const float *__re
 {
     extern __shared__ uint8_t smem_raw[];
     PieceSmem &s = *reinterpret_cast<PieceSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int p = threadIdx.x;
+    const int tid = threadIdx.x;
+    const int p = tid & 127, half = tid >> 7;  // token row of a tile, half of its columns
     const int bh = blockIdx.y;
     // locate (m, b, piece) as the CUDA-core kernel does
     int idx = blockIdx.x, m = -1, b = 0, pc = 0;
@@ -65,7 +67,7 @@ bwd_piece_tc_kernel(const __grid_constant__ CUtensorMap map_q, const float *__re
     const double Pref = Pb[c0];
     const long long t_lo = (long long)p0 << cbits, t_hi = (long long)p1 << cbits;
     const int ntiles = (int)((t_hi - t_lo + kPT - 1) / kPT);
-    if (p == 0) {
+    if (tid == 0) {
         for (int i = 0; i < 2; i++) {
             mbar_init(&s.bar_load[i], 1);
             mbar_init(&s.bar_mma[i], 1);
@@ -74,7 +76,7 @@ bwd_piece_tc_kernel(const __grid_constant__ CUtensorMap map_q, const float *__re
         fence_mbar_init();
         tma_prefetch_map(&map_q);
     }
-    if (p < 32) {
+    if (tid < 32) {
         tmem_alloc(&s.tmem, 128);
         tmem_relinquish();
     }
@@ -88,12 +90,12 @@ bwd_piece_tc_kernel(const __grid_constant__ CUtensorMap map_q, const float *__re
         tma_load_3d(s.q[st], &map_q, &s.bar_load[st], 0, (int)(t_lo + (long long)n * kPT), bh);
         tma_load_3d(s.q[st] + kPH, &map_q, &s.bar_load[st], 64, (int)(t_lo + (long long)n * kPT), bh);
     };
-    if (p == 0)
+    if (tid == 0)
         for (int n = 0; n < min(2, ntiles); n++) load_q(n);
     const uint32_t idesc = idesc_bf16_f32(128, 128, true, true);
     for (int n = 0; n < ntiles; n++) {
         const int st = n & 1;
-        if (p == 0 && n >= 1 && n + 1 < ntiles) {  // q stage of tile n-1 is free once its product is done
+        if (tid == 0 && n >= 1 && n + 1 < ntiles) {  // q stage of tile n-1 is free once its product is done
             if (!mbar_wait(&s.bar_mma[(n - 1) & 1], ((n - 1) >> 1) & 1, kPWait)) atomicCAS(err, 0, 2);
             load_q(n + 1);
         }
@@ -107,7 +109,7 @@ bwd_piece_tc_kernel(const __grid_constant__ CUtensorMap map_q, const float *__re
         }
         const float4 *src = reinterpret_cast<const float4 *>(dout + ((long long)bh * T + (t < t_hi ? t : t_lo)) * kPDm);
 #pragma unroll 4
-        for (int ch = 0; ch < 16; ch++) {
+        for (int ch = 8 * half; ch < 8 * half + 8; ch++) {
             float4 a = make_float4(0.f, 0.f, 0.f, 0.f), c = a;
             if (t < t_hi) {
                 a = src[2 * ch];
@@ -131,7 +133,7 @@ bwd_piece_tc_kernel(const __grid_constant__ CUtensorMap map_q, const float *__re
         fence_proxy_async_smem();
         if (!mbar_wait(&s.bar_load[st], (n >> 1) & 1, kPWait)) atomicCAS(err, 0, 1);
         __syncthreads();
-        if (p == 0) {
+        if (tid == 0) {
             tc_fence_after_sync();
 #pragma unroll
             for (int kk = 0; kk < 8; kk++) {
@@ -143,14 +145,14 @@ bwd_piece_tc_kernel(const __grid_constant__ CUtensorMap map_q, const float *__re
             umma_commit(&s.bar_mma[st]);
         }
     }
-    if (p == 0) umma_commit(&s.bar_done);
+    if (tid == 0) umma_commit(&s.bar_done);
     if (!mbar_wait(&s.bar_done, 0, kPWait)) atomicCAS(err, 0, 2);
     tc_fence_after_sync();
     float4 *dst = reinterpret_cast<float4 *>(part + (((long long)bh * gridDim.x) + blockIdx.x) * kPDm * kPDm +
                                              (long long)p * kPDm);
     const uint32_t lane_off = (uint32_t)((p >> 5) * 32) << 16;
 #pragma unroll 1
-    for (int cb = 0; cb < kPDm; cb += 16) {
+    for (int cb = 64 * half; cb < 64 * half + 64; cb += 16) {
         float x[16];
         tmem_ld16(tm + lane_off + cb, x);
         tmem_ld_wait();
@@ -159,7 +161,7 @@ bwd_piece_tc_kernel(const __grid_constant__ CUtensorMap map_q, const float *__re
     }
     tc_fence_before_sync();
     __syncthreads();
-    if (p < 32) tmem_dealloc(tm, 128);
+    if (tid < 32) tmem_dealloc(tm, 128);
 }
 
 }  // namespace

@@ -17,13 +17,13 @@ namespace lla {
 // Rows [0, 128) of src (row stride ld floats); row r scaled by
 // all * scale[r] (scale nullptr: all) and rows >= nrows written as 0.  NPARTS = 2 or 3; part p goes
 // to dst[p].  NTHREADS threads (a multiple of 32) call it together; each
-// issues the loads of four rows before converting them.
-template <int NPARTS, int NTHREADS>
+// issues the loads of GROUP rows before converting them.
+template <int NPARTS, int NTHREADS, int GROUP = 4>
 __device__ __forceinline__ void stage_split_tile(uint8_t *const *dst, const float *src, long long ld,
                                                  const float *scale, float all, int nrows)
 {
     constexpr int kPass = (NTHREADS / 32) * 2;  // rows per pass
-    constexpr int kGroup = 4;                   // passes whose loads are issued together
+    constexpr int kGroup = GROUP;               // passes whose loads are issued together
     const int tid = threadIdx.x;
     const int sub = (tid & 31) >> 4;        // which of the warp's two rows
     const int c8 = (tid & 15) * 8;          // first column of this lane
