@@ -61,8 +61,8 @@ __device__ __forceinline__ void mma8(uint32_t d, const uint8_t *a, const uint8_t
 __global__ void __launch_bounds__(kKThreads, 1)
 bwd_key_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                   const float *__restrict__ gamma, const double *__restrict__ P, const float *__restrict__ R,
-                  float *__restrict__ dk, float *__restrict__ dv, int T, int N, int nlev, int nblocks,
-                  int *__restrict__ err)
+                  const float *__restrict__ part, float *__restrict__ dk, float *__restrict__ dv, int T, int N,
+                  int nlev, int nblocks, int Pc, int nitems, int *__restrict__ err)
 {
     extern __shared__ uint8_t smem_raw[];
     KeySmem &s = *reinterpret_cast<KeySmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -113,14 +113,6 @@ bwd_key_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_consta
     };
     // the level sequence: level 0 first (if any), then the shared levels
     const int total = (lev0 ? 1 : 0) + nl;
-    int off_tab[24];
-    {
-        int off = 0;
-        for (int m = 0; m < nlev; m++) {
-            off_tab[m] = off;
-            off += (N + (1 << m) - 1) >> m;
-        }
-    }
     bool acc_started = false;
     if (!mbar_wait(&s.bar_load, 0, kKWait)) key_err(err, 1);
     for (int n = 0; n < total; n++) {
@@ -128,7 +120,7 @@ bwd_key_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_consta
         const bool is0 = lev0 && n == 0;
         const int m = is0 ? 0 : levs[n - (lev0 ? 1 : 0)];
         const int b = (c0 >> m) + 1;
-        const float *Rm = R + (((long long)bh * nblocks) + off_tab[m] + b) * kKD * kKD;
+        const float *Rm = block_state(R, part, bh, m, b, N, Pc, nitems, nblocks, kKD * kKD);
         const float c = is0 ? 1.f : expf((float)(Pb[b << m] - Pend));
         if (n >= 2 && !mbar_wait(&s.bar_mma[buf], ((n - 2) >> 1) & 1, kKWait)) key_err(err, 2);
         stage(buf, Rm, c);
@@ -199,8 +191,8 @@ bool bwd_key_tc_supported(const BwdArgs &A)
            ((uintptr_t)A.v & 15) == 0 && ((uintptr_t)A.dkey & 15) == 0 && ((uintptr_t)A.dval & 15) == 0;
 }
 
-cudaError_t bwd_key_tc(const BwdArgs &A, const float *gamma, const double *P, const float *R, int nlev,
-                       int nblocks, int *err)
+cudaError_t bwd_key_tc(const BwdArgs &A, const float *gamma, const double *P, const float *R, const float *part,
+                       int nlev, int nblocks, int Pc, int nitems, int *err)
 {
     const int BH = A.B * A.H, N = A.T / A.C;
     CUtensorMap mk, mv;
@@ -210,7 +202,7 @@ cudaError_t bwd_key_tc(const BwdArgs &A, const float *gamma, const double *P, co
     cudaError_t e = cudaFuncSetAttribute(bwd_key_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     bwd_key_tc_kernel<<<dim3((N + 1) / 2, BH), kKThreads, smem, (cudaStream_t)A.stream>>>(
-        mk, mv, gamma, P, R, A.dkey, A.dval, A.T, N, nlev, nblocks, err);
+        mk, mv, gamma, P, R, part, A.dkey, A.dval, A.T, N, nlev, nblocks, Pc, nitems, err);
     return cudaPeekAtLastError();
 }
 

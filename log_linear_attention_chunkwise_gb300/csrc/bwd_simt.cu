@@ -407,7 +407,8 @@ bwd_block_piece_kernel(const Tin *__restrict__ q, const float *__restrict__ dout
 }
 
 // R_{m,b} = sum of its pieces in piece order (bitwise reproducible).  One
-// CTA per (level, block) slot; even or absent blocks exit.
+// CTA per (level, block) slot; even or absent blocks exit, and so do blocks
+// of a single piece (block_state reads the piece itself).
 __global__ void __launch_bounds__(kThreads)
 bwd_block_reduce_kernel(const float *__restrict__ part, float *__restrict__ R, int Dk, int Dv, int N,
                         int nlev, int Pc, int nitems, int nblocks)
@@ -426,6 +427,7 @@ bwd_block_reduce_kernel(const float *__restrict__ part, float *__restrict__ R, i
     const int pp = ((1 << m) + Pc - 1) / Pc;
     const int blk_end = min(N, (b + 1) << m);
     const int npieces = (blk_end - (b << m) + Pc - 1) / Pc;  // non-empty pieces
+    if (npieces <= 1) return;
     const float4 *src = reinterpret_cast<const float4 *>(part) +
                         ((bh * nitems) + first + (b / 2) * pp) * (long long)(Dk * Dv / 4);
     float4 *dst = reinterpret_cast<float4 *>(R) + ((bh * nblocks) + blockIdx.x) * (long long)(Dk * Dv / 4);
@@ -450,8 +452,9 @@ constexpr int kColsPer = 8;  // columns of a thread tile
 template <typename Tin>
 __global__ void __launch_bounds__(kThreads)
 bwd_key_kernel(const Tin *__restrict__ k, const Tin *__restrict__ v, const float *__restrict__ gamma,
-               const double *__restrict__ P, const float *__restrict__ R, float *__restrict__ dk,
-               float *__restrict__ dv, int T, int Dk, int Dv, int C, int N, int nlev, int nblocks)
+               const double *__restrict__ P, const float *__restrict__ R, const float *__restrict__ part,
+               float *__restrict__ dk, float *__restrict__ dv, int T, int Dk, int Dv, int C, int N, int nlev,
+               int nblocks, int Pc, int nitems)
 {
     extern __shared__ __align__(16) float sm[];
     const int lk = Dk + 1, lv = Dv + 1;
@@ -477,13 +480,11 @@ bwd_key_kernel(const Tin *__restrict__ k, const Tin *__restrict__ v, const float
         for (int c = 0; c < kColsPer; c++) dka[a][c] = dva[a][c] = 0.f;
     const double *Pb = P + bh * (long long)(N + 1);
     bool any = false;
-    int off = 0;
     for (int m = 0; m < nlev; m++) {
-        const int nb = (N + (1 << m) - 1) >> m;
         const int b = (i >> m) + 1;
         if (((i >> m) & 1) == 0 && ((long long)b << m) < N) {
             any = true;
-            const float *Rm = R + ((bh * nblocks) + off + b) * (long long)Dk * Dv;
+            const float *Rm = block_state(R, part, bh, m, b, N, Pc, nitems, nblocks, Dk * Dv);
             const float dP = (float)(Pb[b << m] - Pb[i]);
             float f[kRowsPer];
 #pragma unroll
@@ -551,7 +552,6 @@ bwd_key_kernel(const Tin *__restrict__ k, const Tin *__restrict__ v, const float
                     for (int cc = 0; cc < kColsPer; cc++) dva[a][cc] = fmaf(f[a], t[a][cc], dva[a][cc]);
             }
         }
-        off += nb;
     }
     if (!any) return;
     auto add8 = [](float *dst, const float *x) {
@@ -751,15 +751,15 @@ cudaError_t launch_bwd(const BwdArgs &A)
             int *err = (int *)(ws + lay.err);
             e = cudaMemsetAsync(err, 0, sizeof(int), st);
             if (e != cudaSuccess) return e;
-            e = bwd_key_tc(A, gamma, P, R, nlev, nblocks, err);
+            e = bwd_key_tc(A, gamma, P, R, parts, nlev, nblocks, Pc, nitems, err);
             if (e != cudaSuccess) return e;
         } else {
             const size_t smk = sizeof(float) * key_smem_floats(A.C, A.dk, A.dv);
             e = cudaFuncSetAttribute(bwd_key_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smk);
             if (e != cudaSuccess) return e;
             bwd_key_kernel<Tin><<<dim3(N, BH), kThreads, smk, st>>>(
-                (const Tin *)A.k, (const Tin *)A.v, gamma, P, R, A.dkey, A.dval, A.T, A.dk, A.dv, A.C, N,
-                nlev, nblocks);
+                (const Tin *)A.k, (const Tin *)A.v, gamma, P, R, parts, A.dkey, A.dval, A.T, A.dk, A.dv, A.C, N,
+                nlev, nblocks, Pc, nitems);
         }
     }
     bwd_gate_grad_kernel<Tin><<<dim3((A.T + kThreads / 32 - 1) / (kThreads / 32), BH), kThreads, 0, st>>>(

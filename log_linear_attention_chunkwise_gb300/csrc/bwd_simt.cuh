@@ -17,13 +17,34 @@ struct BwdArgs {
     void *stream;
 };
 
+// The state R_{m,b} of block b at level m ([Dk][Dv] fp32, E = Dk Dv): a block
+// of several pieces has the sum of its pieces in its R slot (block slots flat
+// by level); a block that is a single piece is read from that piece's slot
+// directly (the reduction skips it).  Piece slots are flat by level, (b / 2)
+// times pieces-per-block within a level.
+__device__ __forceinline__ const float *block_state(const float *R, const float *part, long long bh, int m, int b,
+                                                    int N, int Pc, int nitems, int nblocks, int E)
+{
+    int off = 0, first = 0;
+    for (int mm = 0; mm < m; mm++) {
+        const int nb = (N + (1 << mm) - 1) >> mm;
+        off += nb;
+        first += (nb / 2) * (((1 << mm) + Pc - 1) / Pc);
+    }
+    const int pp = ((1 << m) + Pc - 1) / Pc;
+    const int blk_end = min(N, (b + 1) << m);
+    if (blk_end - (b << m) <= Pc)
+        return part + ((bh * nitems) + first + (long long)(b / 2) * pp) * (long long)E;
+    return R + ((bh * nblocks) + off + b) * (long long)E;
+}
+
 size_t bwd_workspace_bytes(const BwdArgs &A);
 size_t bwd_smem_bytes(const BwdArgs &A);
 cudaError_t bwd(const BwdArgs &A);
 // Key side on the tensor cores (bf16, dk = dv = 128, chunk 64): adds to dk, dv.
 bool bwd_key_tc_supported(const BwdArgs &A);
-cudaError_t bwd_key_tc(const BwdArgs &A, const float *gamma, const double *P, const float *R, int nlev,
-                       int nblocks, int *err);
+cudaError_t bwd_key_tc(const BwdArgs &A, const float *gamma, const double *P, const float *R, const float *part,
+                       int nlev, int nblocks, int Pc, int nitems, int *err);
 // Query side (node read-out) on the tensor cores, same conditions: adds to dq, dlambda.
 bool bwd_query_tc_supported(const BwdArgs &A);
 cudaError_t bwd_query_tc(const BwdArgs &A, const float *gamma, const double *P, const float *nodes, int *err);
