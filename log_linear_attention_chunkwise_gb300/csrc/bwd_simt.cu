@@ -407,30 +407,34 @@ bwd_block_piece_kernel(const Tin *__restrict__ q, const float *__restrict__ dout
 }
 
 // R_{m,b} = sum of its pieces in piece order (bitwise reproducible).  One
-// CTA per (level, block) slot; even or absent blocks exit, and so do blocks
-// of a single piece (block_state reads the piece itself).
+// CTA per odd block of the levels whose blocks span several pieces
+// (2^m > Pc); a ragged last block of one piece exits (block_state reads the
+// piece itself, as for every block of the lower levels).
 __global__ void __launch_bounds__(kThreads)
 bwd_block_reduce_kernel(const float *__restrict__ part, float *__restrict__ R, int Dk, int Dv, int N,
                         int nlev, int Pc, int nitems, int nblocks)
 {
     const long long bh = blockIdx.y;
-    int idx = blockIdx.x, m = 0, nb = N, first = 0;
-    while (m < nlev && idx >= nb) {
-        idx -= nb;
-        first += (nb / 2) * (((1 << m) + Pc - 1) / Pc);
-        m++;
-        nb = (N + (1 << m) - 1) >> m;
+    int idx = blockIdx.x, m = 0, off = 0, first = 0;
+    for (; m < nlev; m++) {
+        const int nb = (N + (1 << m) - 1) >> m;
+        const int pp = ((1 << m) + Pc - 1) / Pc;
+        if (pp > 1) {
+            if (idx < nb / 2) break;
+            idx -= nb / 2;
+        }
+        off += nb;
+        first += (nb / 2) * pp;
     }
     if (m >= nlev) return;
-    const int b = idx;
-    if ((b & 1) == 0 || ((long long)b << m) >= N) return;
+    const int b = 2 * idx + 1;
     const int pp = ((1 << m) + Pc - 1) / Pc;
     const int blk_end = min(N, (b + 1) << m);
     const int npieces = (blk_end - (b << m) + Pc - 1) / Pc;  // non-empty pieces
     if (npieces <= 1) return;
     const float4 *src = reinterpret_cast<const float4 *>(part) +
                         ((bh * nitems) + first + (b / 2) * pp) * (long long)(Dk * Dv / 4);
-    float4 *dst = reinterpret_cast<float4 *>(R) + ((bh * nblocks) + blockIdx.x) * (long long)(Dk * Dv / 4);
+    float4 *dst = reinterpret_cast<float4 *>(R) + ((bh * nblocks) + off + b) * (long long)(Dk * Dv / 4);
     const int E4 = Dk * Dv / 4;
     for (int e = threadIdx.x; e < E4; e += kThreads) {
         float4 acc = src[e];
@@ -640,6 +644,15 @@ int total_blocks(int N)
 
 int piece_chunks(int C) { return 1024 / C > 1 ? 1024 / C : 1; }
 
+// Odd blocks of the levels whose blocks span several pieces (the reduction's CTAs).
+int multi_piece_blocks(int N, int Pc)
+{
+    int tot = 0;
+    for (int m = 0; m < block_levels(N); m++)
+        if (((1 << m) + Pc - 1) / Pc > 1) tot += ((N + (1 << m) - 1) >> m) / 2;
+    return tot;
+}
+
 int total_items(int N, int Pc)
 {
     int tot = 0;
@@ -745,8 +758,10 @@ cudaError_t launch_bwd(const BwdArgs &A)
                 (const Tin *)A.q, A.dout, gamma, A.lam, P, parts, A.T, A.dk, A.dv, A.C, cbits, N, A.L, nlev,
                 Pc);
         }
-        bwd_block_reduce_kernel<<<dim3(nblocks, BH), kThreads, 0, st>>>(parts, R, A.dk, A.dv, N, nlev, Pc,
-                                                                        nitems, nblocks);
+        const int nred = multi_piece_blocks(N, Pc);
+        if (nred > 0)
+            bwd_block_reduce_kernel<<<dim3(nred, BH), kThreads, 0, st>>>(parts, R, A.dk, A.dv, N, nlev, Pc, nitems,
+                                                                         nblocks);
         if (bwd_key_tc_supported(A)) {
             int *err = (int *)(ws + lay.err);
             e = cudaMemsetAsync(err, 0, sizeof(int), st);
