@@ -110,19 +110,30 @@ bwd_state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __nv_bfloat
     }
     if (!mbar_wait(&s.bar_mma, 0, kSWait)) atomicCAS(err, 0, 2);
     tc_fence_after_sync();
-    // row p of each state (tensor-memory lane p) to node slot c0 + h + 1
+    // each state through shared memory (the operand stages are free now), then
+    // to node slot c0 + h + 1 as whole rows: row p (tensor-memory lane p) is
+    // staged by thread p at a 132-float stride, and the warps write 512-byte rows
+    float *stg = reinterpret_cast<float *>(s.k);  // [128][132] fp32 = 66 KB of the 96 KB stages
+    constexpr int kLds = kSD + 4;
     const uint32_t lane_off = (uint32_t)((p >> 5) * 32) << 16;
     for (int h = 0; h < nst; h++) {
-        float4 *dst = reinterpret_cast<float4 *>(nodes + ((long long)bh * N + c0 + h + 1) * kSD * kSD +
-                                                 (long long)p * kSD);
 #pragma unroll 1
         for (int cb = 0; cb < kSD; cb += 16) {
             float x[16];
             tmem_ld16(tm + 128 * h + lane_off + cb, x);
             tmem_ld_wait();
 #pragma unroll
-            for (int u = 0; u < 4; u++) dst[cb / 4 + u] = make_float4(x[4 * u], x[4 * u + 1], x[4 * u + 2], x[4 * u + 3]);
+            for (int u = 0; u < 4; u++)
+                *reinterpret_cast<float4 *>(stg + p * kLds + cb + 4 * u) =
+                    make_float4(x[4 * u], x[4 * u + 1], x[4 * u + 2], x[4 * u + 3]);
         }
+        __syncthreads();
+        float4 *dst = reinterpret_cast<float4 *>(nodes + ((long long)bh * N + c0 + h + 1) * kSD * kSD);
+        for (int e = p; e < kSD * kSD / 4; e += kSThreads) {
+            const int r = e >> 5, c4 = e & 31;
+            dst[e] = *reinterpret_cast<const float4 *>(stg + r * kLds + 4 * c4);
+        }
+        __syncthreads();  // the staging is rewritten by the next state
     }
     tc_fence_before_sync();
     __syncthreads();
