@@ -225,22 +225,28 @@ bwd_intra_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
         mma8x(tV, s.wlo, true, s.ohi, true, id_mnmn, true);
         umma_commit(&s.bar_mma);
     }
-    // dq, dk rows while dv runs (the tensor-memory loads are warp-collective:
-    // every lane issues them; only rows inside the sequence are stored)
-    for (int o = 0; o < 2; o++) {
-        float *dst = (o == 0 ? dq : dk) + tok * kID;
-        const uint32_t src = o == 0 ? tQ : tK;
+    // dq, dk while dv runs, then dv: each through shared memory (the q and k
+    // stages, which no product reads any more) and out as whole rows.  The
+    // tensor-memory loads are warp-collective: every lane issues them.
+    float *tile = reinterpret_cast<float *>(s.q);
+    const int nrows = (int)min((long long)kIT, (long long)T - (long long)pair * kIT);
+    const long long row0 = (long long)bh * T + (long long)pair * kIT;
+    auto put = [&](uint32_t src) {
 #pragma unroll 1
         for (int c0 = 0; c0 < kID; c0 += 16) {
             float x[16];
             tmem_ld16(src + lane_off + c0, x);
             tmem_ld_wait();
-            if (row_ok) {
-                float4 *d4 = reinterpret_cast<float4 *>(dst + c0);
 #pragma unroll
-                for (int u = 0; u < 4; u++) d4[u] = make_float4(x[4 * u], x[4 * u + 1], x[4 * u + 2], x[4 * u + 3]);
-            }
+            for (int u = 0; u < 4; u++)
+                *out_tile_piece(tile, t, c0 / 4 + u) = make_float4(x[4 * u], x[4 * u + 1], x[4 * u + 2], x[4 * u + 3]);
         }
+    };
+    for (int o = 0; o < 2; o++) {
+        put(o == 0 ? tQ : tK);
+        __syncthreads();
+        out_tile_store<kIThreads, false>((o == 0 ? dq : dk) + row0 * kID, tile, nrows);
+        __syncthreads();
     }
     if (row_ok) {
         float *dlr = dlam + tok * L;
@@ -248,17 +254,9 @@ bwd_intra_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
     }
     if (!mbar_wait(&s.bar_mma, 0, kIWait)) atomicCAS(err, 0, 2);
     tc_fence_after_sync();
-#pragma unroll 1
-    for (int c0 = 0; c0 < kID; c0 += 16) {
-        float x[16];
-        tmem_ld16(tV + lane_off + c0, x);
-        tmem_ld_wait();
-        if (row_ok) {
-            float4 *d4 = reinterpret_cast<float4 *>(dv + tok * kID + c0);
-#pragma unroll
-            for (int u = 0; u < 4; u++) d4[u] = make_float4(x[4 * u], x[4 * u + 1], x[4 * u + 2], x[4 * u + 3]);
-        }
-    }
+    put(tV);
+    __syncthreads();
+    out_tile_store<kIThreads, false>(dv + row0 * kID, tile, nrows);
     tc_fence_before_sync();
     __syncthreads();
     if (t < 32) tmem_dealloc(tm, 512);

@@ -150,33 +150,32 @@ bwd_key_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_consta
     const float f0 = (lev0 && p < 64) ? expf((float)(Pb[c0 + 1] - Gs)) : 0.f;
     const uint32_t lane_off = (uint32_t)((p >> 5) * 32) << 16;
     const bool have_shared = nl > 0;
+    // each result through shared memory (the k and v stages, free once every
+    // product is done) and added to dk, dv as whole rows
+    float *tile = reinterpret_cast<float *>(s.k);
+    const int nrows = (int)min((long long)kKT, (long long)T - (long long)pair * kKT);
     for (int which = 0; which < 2; which++) {
         const uint32_t a_sh = which == 0 ? acc_k : acc_v, a_0 = which == 0 ? acc_k0 : acc_v0;
-        float *dst = (which == 0 ? dk : dv) + ((long long)bh * T + row) * kKD;
 #pragma unroll 1
         for (int cb = half * 64; cb < half * 64 + 64; cb += 16) {
             float x[16], y[16];
             tmem_ld16(a_sh + lane_off + cb, x);
             tmem_ld16(a_0 + lane_off + cb, y);
             tmem_ld_wait();
-            if (row < T) {
-                float4 *d4 = reinterpret_cast<float4 *>(dst + cb);
 #pragma unroll
-                for (int u = 0; u < 4; u++) {
-                    // an accumulator no level wrote holds no data: select, do not scale
-                    float a[4];
+            for (int u = 0; u < 4; u++) {
+                // an accumulator no level wrote holds no data: select, do not scale
+                float a[4];
 #pragma unroll
-                    for (int e = 0; e < 4; e++)
-                        a[e] = (have_shared ? rho * x[4 * u + e] : 0.f) + (lev0 ? f0 * y[4 * u + e] : 0.f);
-                    float4 o = d4[u];
-                    o.x += a[0];
-                    o.y += a[1];
-                    o.z += a[2];
-                    o.w += a[3];
-                    d4[u] = o;
-                }
+                for (int e = 0; e < 4; e++)
+                    a[e] = (have_shared ? rho * x[4 * u + e] : 0.f) + (lev0 ? f0 * y[4 * u + e] : 0.f);
+                *out_tile_piece(tile, p, cb / 4 + u) = make_float4(a[0], a[1], a[2], a[3]);
             }
         }
+        __syncthreads();
+        out_tile_store<kKThreads, true>((which == 0 ? dk : dv) + ((long long)bh * T + (long long)pair * kKT) * kKD,
+                                        tile, nrows);
+        __syncthreads();
     }
     tc_fence_before_sync();
     __syncthreads();

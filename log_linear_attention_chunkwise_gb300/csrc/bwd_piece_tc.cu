@@ -11,6 +11,7 @@
 // in order.
 #include "bwd_simt.cuh"
 #include "sm100.cuh"
+#include "split_stage.cuh"
 #include "tma_host.cuh"
 
 namespace lla {
@@ -148,8 +149,9 @@ bwd_piece_tc_kernel(const __grid_constant__ CUtensorMap map_q, const float *__re
     if (tid == 0) umma_commit(&s.bar_done);
     if (!mbar_wait(&s.bar_done, 0, kPWait)) atomicCAS(err, 0, 2);
     tc_fence_after_sync();
-    float4 *dst = reinterpret_cast<float4 *>(part + (((long long)bh * gridDim.x) + blockIdx.x) * kPDm * kPDm +
-                                             (long long)p * kPDm);
+    // the piece through shared memory (the q stages, free once every product
+    // is done) and out as whole rows
+    float *tile = reinterpret_cast<float *>(s.q[0]);
     const uint32_t lane_off = (uint32_t)((p >> 5) * 32) << 16;
 #pragma unroll 1
     for (int cb = 64 * half; cb < 64 * half + 64; cb += 16) {
@@ -157,8 +159,11 @@ bwd_piece_tc_kernel(const __grid_constant__ CUtensorMap map_q, const float *__re
         tmem_ld16(tm + lane_off + cb, x);
         tmem_ld_wait();
 #pragma unroll
-        for (int u = 0; u < 4; u++) dst[cb / 4 + u] = make_float4(x[4 * u], x[4 * u + 1], x[4 * u + 2], x[4 * u + 3]);
+        for (int u = 0; u < 4; u++)
+            *out_tile_piece(tile, p, cb / 4 + u) = make_float4(x[4 * u], x[4 * u + 1], x[4 * u + 2], x[4 * u + 3]);
     }
+    __syncthreads();
+    out_tile_store<kPThreads, false>(part + (((long long)bh * gridDim.x) + blockIdx.x) * kPDm * kPDm, tile, kPT);
     tc_fence_before_sync();
     __syncthreads();
     if (tid < 32) tmem_dealloc(tm, 128);

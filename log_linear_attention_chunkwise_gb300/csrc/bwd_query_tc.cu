@@ -185,18 +185,14 @@ bwd_query_tc_kernel(const Tin *__restrict__ q, const float *__restrict__ dout, c
         drain(n);  // contains a barrier of all threads: node n+1 is staged and U_{n-1} drained
         if (n + 1 < np && tid == 0) issue(n + 1);
     }
-    if (row_ok) {
-        float4 *d4 = reinterpret_cast<float4 *>(dq + tok * kQD + half * 64);
+    // dq through shared memory (the dO stages, free once every product is
+    // done) and added as whole rows
+    float *tile = reinterpret_cast<float *>(s.ohi);
 #pragma unroll
-        for (int u = 0; u < 16; u++) {
-            float4 o = d4[u];
-            o.x += dqa[4 * u];
-            o.y += dqa[4 * u + 1];
-            o.z += dqa[4 * u + 2];
-            o.w += dqa[4 * u + 3];
-            d4[u] = o;
-        }
-    }
+    for (int u = 0; u < 16; u++)
+        *out_tile_piece(tile, row, half * 16 + u) = make_float4(dqa[4 * u], dqa[4 * u + 1], dqa[4 * u + 2], dqa[4 * u + 3]);
+    __syncthreads();
+    out_tile_store<kQThreads, true>(dq + ((long long)bh * T + (long long)pair * kQT) * kQD, tile, nrows);
     tc_fence_before_sync();
     __syncthreads();
     if (tid < 32) tmem_dealloc(tm, 256);

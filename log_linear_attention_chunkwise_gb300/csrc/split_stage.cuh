@@ -73,3 +73,50 @@ __device__ __forceinline__ void stage_split_tile(uint8_t *const *dst, const floa
 }
 
 }  // namespace lla
+
+namespace lla {
+
+// A [128][128] fp32 tile in shared memory (64 KB) on its way to global
+// memory: piece j (16 bytes, columns 4j..4j+3) of row r is kept at piece
+// j ^ (r & 7) of the row, so a thread writing pieces of its own row and a
+// warp reading one whole row both touch every bank once.
+__device__ __forceinline__ float4 *out_tile_piece(float *tile, int r, int j)
+{
+    return reinterpret_cast<float4 *>(tile + r * 128 + ((j ^ (r & 7)) << 2));
+}
+
+// The staged tile to rows [0, nrows) of dst (row stride 128 floats), whole
+// rows per warp: dst = tile, or dst += tile when ADD (the loads of eight
+// pieces per thread are issued before their stores).  NTHREADS threads call
+// it together after a barrier that follows the staging.
+template <int NTHREADS, bool ADD>
+__device__ __forceinline__ void out_tile_store(float *dst, float *tile, int nrows)
+{
+    constexpr int kPer = 128 * 32 / NTHREADS;  // pieces per thread
+    static_assert(kPer % 8 == 0, "whole groups of eight pieces");
+#pragma unroll 1
+    for (int g0 = 0; g0 < kPer; g0 += 8) {
+        float4 o[8];
+#pragma unroll
+        for (int u = 0; u < 8; u++) {
+            const int e = threadIdx.x + (g0 + u) * NTHREADS;
+            const int r = e >> 5, j = e & 31;
+            o[u] = *out_tile_piece(tile, r, j);
+            if (ADD && r < nrows) {
+                const float4 x = reinterpret_cast<const float4 *>(dst + (long long)r * 128)[j];
+                o[u].x += x.x;
+                o[u].y += x.y;
+                o[u].z += x.z;
+                o[u].w += x.w;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; u++) {
+            const int e = threadIdx.x + (g0 + u) * NTHREADS;
+            const int r = e >> 5, j = e & 31;
+            if (r < nrows) reinterpret_cast<float4 *>(dst + (long long)r * 128)[j] = o[u];
+        }
+    }
+}
+
+}  // namespace lla
