@@ -223,7 +223,9 @@ lla_status lla_fwd_host(const void *q, const void *k, const void *v, const float
  * T = (I + strict_lower(diag(beta) K K^T))^{-1} diag(beta), so the
  * intra-chunk output, the read-out of earlier states and the chunk's
  * transition are small matrix products; the chunk-level Fenwick states are
- * then carried across chunks in order.  fp32 on CUDA cores, two launches.
+ * then carried across chunks in order.  Two launches; the products run on
+ * the tensor cores as TF32 with every fp32 operand split into a high part
+ * and a remainder (about 21 bits; bf16 inputs are exact), accumulation fp32.
  *   q, k [B,H,T,dk], v [B,H,T,dv] in in_dt; g, beta [B,H,T] fp32;
  *   lambda [B,H,T,L] fp32 with L = lla_num_levels(T); out [B,H,T,dv] fp32.
  *   q, k, v and out must be 16-byte aligned (read and written in 16-byte pieces).
