@@ -16,15 +16,17 @@
 //   * the chunk's own contribution at its end: H = K^T T diag(exp(gam_{C-1} - gam)) V;
 //   * intra-chunk output: o_a = sum_{s <= a} lambda_a[l(a,s)] exp(gam_a - gam_s) Cm[a,s] v_s,
 //     Cm = inclusive_lower(Q K^T) T  (Cm[a,a] = beta_a q_a.k_a: level 0).
-// Two launches: gdn_chunk_prep_kernel does everything that is local to a
-// chunk for all chunks at once (one CTA per chunk; the products on TF32
-// tensor-core fragments with split operands, the inverse by 16 x 16 diagonal
-// blocks and block substitution on CUDA cores), writing the intra-chunk
-// output, the rows of q~ and W, H and exp(gam_{C-1}); gdn_chunk_scan_kernel walks the chunks of one
+// Two launches.  gdn_chunk_prep_kernel does everything that is local to a
+// chunk, for all chunks at once (one CTA per chunk; the 16 x 16 diagonal
+// blocks of the inverse by forward substitution and the blocks below them by
+// block substitution), writing the intra-chunk output, the rows of q~ and W,
+// H and exp(gam_{C-1}).  gdn_chunk_scan_kernel walks the chunks of one
 // (batch, head) in order for 8 value columns (a state column only mixes with
 // itself), keeping the chunk-level Fenwick states in shared memory: read-out
-// added to the output, transition, and the fold of H into the new level.
-// The next chunk's operands are prefetched with cp.async while one is worked.
+// added to the output, transition, and the fold of H into the new level; the
+// next chunk's operands are prefetched with cp.async while one is worked.
+// Both run their products as warp-level TF32 tensor-core tiles with every
+// fp32 operand split into a high part and a remainder.
 #include "gdn.cuh"
 
 namespace lla {
