@@ -9,9 +9,10 @@
 // S and dP come from the tensor cores (dO, fp32, split into bf16 high and
 // remainder parts); thread = row reads its chunk's 64 columns of both, forms
 // W1, W2 and the level gradients in fp32, and writes W1 (then W2) split into
-// bf16 parts; the products dq, dk (and dv) follow on the tensor cores, read
-// back row by row and written out.  dq, dk, dv and dlambda rows are fully
-// written here (the node and block-state parts add to them afterwards).
+// bf16 parts; the products dq, dk (and dv) follow on the tensor cores, are
+// read back by rows into a shared tile and written out as whole rows.  dq, dk,
+// dv and dlambda rows are fully written here (the node and block-state parts
+// add to them afterwards).
 #include "bwd_simt.cuh"
 #include "sm100.cuh"
 #include "split_stage.cuh"
