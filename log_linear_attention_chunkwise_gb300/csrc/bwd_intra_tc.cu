@@ -27,7 +27,7 @@ constexpr int kIT = 128;
 constexpr int kID = 128;
 constexpr uint32_t kIB = kIT * kID * 2;  // 32 KB
 constexpr uint32_t kIH = kIB / 2;
-constexpr int kIThreads = 128;
+constexpr int kIThreads = 256;  // two threads per tile row: each takes half of the row's chunk columns
 constexpr uint32_t kIWait = 1u << 22;
 
 struct __align__(1024) IntraSmem {
@@ -55,12 +55,14 @@ __device__ __forceinline__ void mma8x(uint32_t d, const uint8_t *a, bool a_mn, c
     }
 }
 
-// 64 fp32 values of row `row` at columns [c0, c0 + 64) of a 128-wide tile in
-// three bf16 parts (high, middle, low: about 24 bits together), 128-byte swizzle.
-__device__ __forceinline__ void put_split64x3(uint8_t *hi, uint8_t *mid, uint8_t *lo, int row, int c0, const float *x)
+// 8 NCH fp32 values of row `row` at columns [c0, c0 + 8 NCH) of a 128-wide
+// tile (c0 a multiple of 8, inside one 64-column block) in three bf16 parts
+// (high, middle, low: about 24 bits together), 128-byte swizzle.
+template <int NCH>
+__device__ __forceinline__ void put_split_x3(uint8_t *hi, uint8_t *mid, uint8_t *lo, int row, int c0, const float *x)
 {
 #pragma unroll
-    for (int ch = 0; ch < 8; ch++) {
+    for (int ch = 0; ch < NCH; ch++) {
         uint4 h, m, l;
         __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&h);
         __nv_bfloat162 *m2 = reinterpret_cast<__nv_bfloat162 *>(&m);
@@ -78,21 +80,23 @@ __device__ __forceinline__ void put_split64x3(uint8_t *hi, uint8_t *mid, uint8_t
             m2[u] = mv;
             l2[u] = __floats2bfloat162_rn(a - f.x, b - f.y);
         }
-        const uint32_t off = (c0 >> 6) * kIH + sw128_offset(row, ch);
+        const uint32_t off = (c0 >> 6) * kIH + sw128_offset(row, ((c0 & 63) >> 3) + ch);
         *reinterpret_cast<uint4 *>(hi + off) = h;
         *reinterpret_cast<uint4 *>(mid + off) = m;
         *reinterpret_cast<uint4 *>(lo + off) = l;
     }
 }
 
-__device__ __forceinline__ void put_zero64(uint8_t *hi, uint8_t *lo, int row, int c0)
+// Zeros at columns [c0, c0 + 8 NCH) of row `row` in two tiles.
+template <int NCH>
+__device__ __forceinline__ void put_zero_x(uint8_t *a, uint8_t *b, int row, int c0)
 {
     const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
-    for (int ch = 0; ch < 8; ch++) {
-        const uint32_t off = (c0 >> 6) * kIH + sw128_offset(row, ch);
-        *reinterpret_cast<uint4 *>(hi + off) = z;
-        *reinterpret_cast<uint4 *>(lo + off) = z;
+    for (int ch = 0; ch < NCH; ch++) {
+        const uint32_t off = (c0 >> 6) * kIH + sw128_offset(row, ((c0 & 63) >> 3) + ch);
+        *reinterpret_cast<uint4 *>(a + off) = z;
+        *reinterpret_cast<uint4 *>(b + off) = z;
     }
 }
 
@@ -105,13 +109,15 @@ bwd_intra_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
 {
     extern __shared__ uint8_t smem_raw[];
     IntraSmem &s = *reinterpret_cast<IntraSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int t = threadIdx.x;  // tile row
+    const int tid = threadIdx.x;
+    const int t = tid & (kIT - 1), hh = tid >> 7;  // tile row, half of the row's chunk columns
     const int pair = blockIdx.x, bh = blockIdx.y;
     const long long trow = (long long)pair * kIT + t;
     const bool row_ok = trow < T;
     const long long tok = (long long)bh * T + trow;
-    const int cb = t & 64;  // first column of this row's chunk in the tile
-    if (t == 0) {
+    const int cb = t & 64;         // first column of this row's chunk in the tile
+    const int ch0 = cb + 32 * hh;  // first of this thread's 32 columns of it
+    if (tid == 0) {
         mbar_init(&s.bar_load, 1);
         mbar_init(&s.bar_mma, 1);
         fence_mbar_init();
@@ -125,7 +131,7 @@ bwd_intra_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
             tma_load_3d(s.v + h * kIH, &map_v, &s.bar_load, h * 64, pair * kIT, bh);
         }
     }
-    if (t < 32) {
+    if (tid < 32) {
         tmem_alloc(&s.tmem, 512);
         tmem_relinquish();
     }
@@ -136,7 +142,7 @@ bwd_intra_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                             (int)min((long long)kIT, (long long)T - (long long)pair * kIT));
     }
     const float gam_t = row_ok ? gamma[tok] : 0.f;
-    s.gam[t] = gam_t;
+    if (hh == 0) s.gam[t] = gam_t;
     fence_proxy_async_smem();
     tc_fence_before_sync();
     __syncthreads();
@@ -148,7 +154,7 @@ bwd_intra_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
     const uint32_t id_kmn = idesc_bf16_f32(128, 128, false, true);
     const uint32_t id_mnmn = idesc_bf16_f32(128, 128, true, true);
     if (!mbar_wait(&s.bar_load, 0, kIWait)) atomicCAS(err, 0, 1);
-    if (t == 0) {
+    if (tid == 0) {
         tc_fence_after_sync();
         mma8x(tS, s.q, false, s.k, false, id_kk, false);    // S = Q K^T
         mma8x(tP, s.ohi, false, s.v, false, id_kk, false);  // dP = dO V^T
@@ -157,8 +163,9 @@ bwd_intra_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
     }
     if (!mbar_wait(&s.bar_mma, 0, kIWait)) atomicCAS(err, 0, 2);
     tc_fence_after_sync();
-    // the row's chunk block: W1, W2 and the level gradients
-    float w1[64], w2[64];
+    // this thread's 32 columns of the row's chunk block: W1, W2 and the level
+    // gradients (partial sums; the two halves meet before dlambda is written)
+    float w1[32], w2[32];
     float dl[7];
 #pragma unroll
     for (int l = 0; l < 7; l++) dl[l] = 0.f;
@@ -169,14 +176,14 @@ bwd_intra_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
 #pragma unroll
         for (int l = 0; l < 7; l++) lamv[l] = (row_ok && l < L) ? lam_t[l] : 0.f;
 #pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 16) {
+        for (int c0 = 0; c0 < 32; c0 += 16) {
             float sv[16], pv[16];
-            tmem_ld16(tS + lane_off + cb + c0, sv);
-            tmem_ld16(tP + lane_off + cb + c0, pv);
+            tmem_ld16(tS + lane_off + ch0 + c0, sv);
+            tmem_ld16(tP + lane_off + ch0 + c0, pv);
             tmem_ld_wait();
 #pragma unroll
             for (int e = 0; e < 16; e++) {
-                const int b = c0 + e;
+                const int b = 32 * hh + c0 + e;  // key column inside the chunk
                 float x1 = 0.f, x2 = 0.f;
                 if (b <= a && row_ok) {
                     const float dec = __expf(gam_t - s.gam[cb + b]);
@@ -188,19 +195,19 @@ bwd_intra_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                     for (int l = 0; l < 7; l++)
                         if (l == lev) dl[l] = fmaf(dec * sv[e], pv[e], dl[l]);
                 }
-                w1[b] = x1;
-                w2[b] = x2;
+                w1[c0 + e] = x1;
+                w2[c0 + e] = x2;
             }
         }
     }
     tc_fence_before_sync();
     // W1 (three parts) into the (now free) V stage and the two part stages
-    put_split64x3(s.v, s.wmid, s.wlo, t, cb, w1);
-    put_zero64(s.v, s.wmid, t, cb ^ 64);
-    put_zero64(s.wlo, s.wlo, t, cb ^ 64);
+    put_split_x3<4>(s.v, s.wmid, s.wlo, t, ch0, w1);
+    put_zero_x<4>(s.v, s.wmid, t, ch0 ^ 64);
+    put_zero_x<4>(s.wlo, s.wlo, t, ch0 ^ 64);
     fence_proxy_async_smem();
     __syncthreads();
-    if (t == 0) {
+    if (tid == 0) {
         tc_fence_after_sync();
         mma8x(tQ, s.v, false, s.k, true, id_kmn, false);    // dq = W1 K   (B = K, MN-major)
         mma8x(tQ, s.wmid, false, s.k, true, id_kmn, true);
@@ -213,12 +220,12 @@ bwd_intra_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
     if (!mbar_wait(&s.bar_mma, 1, kIWait)) atomicCAS(err, 0, 2);
     tc_fence_after_sync();
     // W2 replaces W1
-    put_split64x3(s.v, s.wmid, s.wlo, t, cb, w2);
-    put_zero64(s.v, s.wmid, t, cb ^ 64);
-    put_zero64(s.wlo, s.wlo, t, cb ^ 64);
+    put_split_x3<4>(s.v, s.wmid, s.wlo, t, ch0, w2);
+    put_zero_x<4>(s.v, s.wmid, t, ch0 ^ 64);
+    put_zero_x<4>(s.wlo, s.wlo, t, ch0 ^ 64);
     fence_proxy_async_smem();
     __syncthreads();
-    if (t == 0) {
+    if (tid == 0) {
         tc_fence_after_sync();
         mma8x(tV, s.v, true, s.ohi, true, id_mnmn, false);  // dv = W2^T dO
         mma8x(tV, s.v, true, s.olo, true, id_mnmn, true);
@@ -232,9 +239,9 @@ bwd_intra_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
     float *tile = reinterpret_cast<float *>(s.q);
     const int nrows = (int)min((long long)kIT, (long long)T - (long long)pair * kIT);
     const long long row0 = (long long)bh * T + (long long)pair * kIT;
-    auto put = [&](uint32_t src) {
+    auto put = [&](uint32_t src) {  // row t, columns [64 hh, 64 hh + 64)
 #pragma unroll 1
-        for (int c0 = 0; c0 < kID; c0 += 16) {
+        for (int c0 = 64 * hh; c0 < 64 * hh + 64; c0 += 16) {
             float x[16];
             tmem_ld16(src + lane_off + c0, x);
             tmem_ld_wait();
@@ -249,10 +256,16 @@ bwd_intra_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
         out_tile_store<kIThreads, false>((o == 0 ? dq : dk) + row0 * kID, tile, nrows);
         __syncthreads();
     }
-    if (row_ok) {
+    // the level gradients: the second half's partial sums through the (free) tile
+    if (hh == 1)
+#pragma unroll
+        for (int l = 0; l < 7; l++) tile[t * 8 + l] = dl[l];
+    __syncthreads();
+    if (hh == 0 && row_ok) {
         float *dlr = dlam + tok * L;
-        for (int l = 0; l < L; l++) dlr[l] = l < 7 ? dl[l] : 0.f;
+        for (int l = 0; l < L; l++) dlr[l] = l < 7 ? dl[l] + tile[t * 8 + l] : 0.f;
     }
+    __syncthreads();  // the tile is staged again below
     if (!mbar_wait(&s.bar_mma, 0, kIWait)) atomicCAS(err, 0, 2);
     tc_fence_after_sync();
     put(tV);
@@ -260,7 +273,7 @@ bwd_intra_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
     out_tile_store<kIThreads, false>(dv + row0 * kID, tile, nrows);
     tc_fence_before_sync();
     __syncthreads();
-    if (t < 32) tmem_dealloc(tm, 512);
+    if (tid < 32) tmem_dealloc(tm, 512);
 }
 
 }  // namespace
