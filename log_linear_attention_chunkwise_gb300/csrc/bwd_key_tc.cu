@@ -109,7 +109,7 @@ bwd_key_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_consta
     // stage c * R (fp32 [128][128]) as bf16 high and remainder parts, 128-byte swizzled
     auto stage = [&](int buf, const float *Rm, float c) {
         uint8_t *dst[2] = {s.rhi[buf], s.rlo[buf]};
-        stage_split_tile<2, kKThreads>(dst, Rm, kKD, nullptr, c, kKD);
+        stage_split_tile<2, kKThreads, 8>(dst, Rm, kKD, nullptr, c, kKD);
     };
     // the level sequence: level 0 first (if any), then the shared levels
     const int total = (lev0 ? 1 : 0) + nl;
