@@ -242,7 +242,9 @@ def bwd(q, k, v, g, lam, dout, chunk: int = 64, workspace=None, stream=None):
 
 def gdn_fwd(q, k, v, g, beta, lam, out=None, state_Ls: int = 0, workspace=None, stream=None):
     """lla_gdn_fwd: Log-Linear Gated DeltaNet over whole sequences.  Returns
-    out [B,H,T,dv], or (out, state [B,H,state_Ls,dk,dv]) when state_Ls > 0."""
+    out [B,H,T,dv], or (out, state [B,H,state_Ls,dk,dv]) when state_Ls > 0.
+    workspace: a uint8 device tensor of at least
+    lla_gdn_fwd_workspace_bytes(B, H, T, dk, dv) bytes (allocated here when None)."""
     lib = load()
     for n, t in (("q", q), ("k", k), ("v", v)):
         _need(t, n, q.dtype, 4)
