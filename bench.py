@@ -429,8 +429,10 @@ def run_next_rows(dev, x, cfg, args):
         "ms": ms, "tokens_per_s": gcfg.B * gcfg.T / (ms / 1e3),
         "roofline": {"bound": "alu", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
                      "algorithmic_flops": flops,
-                     "note": "fp32 CUDA cores: a parallel per-chunk launch, then a scan over the chunks "
-                             "of each (batch, head, 8 value columns)"}}
+                     "note": "a per-chunk launch, then a scan over the chunks of each (batch, head, 8 value "
+                             "columns); products as TF32 tensor-core fragments with fp32 operands split in "
+                             "two (three MMAs per product); peak: the fp32 CUDA-core rate those flops would "
+                             "need without the tensor cores"}}
     del gx, gout, gws
     dc = W.DECODE_CONFIG
     pos = W.make_decode_positions(dc).to(dev)
