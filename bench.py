@@ -357,6 +357,8 @@ def run_lla(args, rank, world, local_rank):
         "clocks": clk.summary(),
     }
     del hx, hout
+    if rank == 0 and not args.skip_configs:
+        res["fwd_lines"] = run_fwd_lines(dev, xd, cfg, ws, stream, hbm_peak, bf16_peak)
     if rank == 0 and not args.skip_decode:
         res["decode"] = run_decode(dev, args)
     if rank == 0 and not args.skip_next:
@@ -366,6 +368,78 @@ def run_lla(args, rank, world, local_rank):
     res["context"] = ("pages: a Triton kernel overtakes FlashAttention-2 from about 8K tokens "
                       "(hardware not named)")
     return res
+
+
+def time_fwd_calls(call, stream, dev, reps, flush_buf=None):
+    """Mean ms of one forward call over reps calls, CUDA events on the
+    launching stream around each call; with flush_buf, a write of a buffer
+    larger than L2 runs before every call, outside the timed pair."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        for a, b in evs:
+            if flush_buf is not None:
+                flush_buf.add_(1)
+            a.record(stream)
+            call()
+            b.record(stream)
+    torch.cuda.synchronize(dev)
+    return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+
+def fwd_line(name, cfg, ms, out_bytes, hbm_peak, bf16_peak, extra=None):
+    nbytes = fwd_bytes(cfg, out_bytes)
+    flops = fwd_flops(cfg)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    tf = flops / (ms / 1e3) / 1e12
+    line = {"workload": name, "ms": ms, "tokens_per_s": cfg.tokens / (ms / 1e3), "tflops": tf,
+            "tflops_frac_of_bf16_peak": tf / bf16_peak,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": gbs / hbm_peak, "algorithmic_bytes": nbytes,
+                         "algorithmic_flops": flops}}
+    if extra:
+        line.update(extra)
+    return line
+
+
+def run_fwd_lines(dev, xd, cfg, ws, stream, hbm_peak, bf16_peak):
+    """The forward on the other forward workloads and with bf16 output: the
+    T=32768 workload with a bf16 out, the T=8192 workload (B2 H16 d128) and
+    the T=2048 workload (B4 H8 d64), whose 45 MB fit in L2, timed both warm
+    and with L2 flushed before every call."""
+    from log_linear_attention_chunkwise_gb300 import binding
+    lines = {}
+    out16 = torch.empty((cfg.B, cfg.H, cfg.T, cfg.dv), dtype=torch.bfloat16, device=dev)
+    ms = time_fwd_calls(lambda: binding.fwd(xd["q"], xd["k"], xd["v"], xd["g"], xd["lam"], chunk=cfg.chunk,
+                                            out=out16, workspace=ws, stream=stream), stream, dev, 20)
+    lines["bf16_out"] = fwd_line(f"{cfg.name} with bf16 out", cfg, ms, 2, hbm_peak, bf16_peak,
+                                 {"l2": "inputs (436 MB) larger than L2, no flush"})
+    del out16
+    flush = torch.zeros(64 << 20, dtype=torch.float32, device=dev)  # 256 MB, about twice L2
+    for wname, reps in (("bf16_T8192_lam1", 20), ("bf16_T2048", 50)):
+        c = W.FWD_CONFIGS[wname]
+        x = {n: t.to(dev) for n, t in W.make_fwd_inputs(c).items()}
+        o = torch.empty((c.B, c.H, c.T, c.dv), dtype=torch.float32, device=dev)
+        need = binding.fwd_workspace_bytes(c.B, c.H, c.T, c.dk, c.dv, c.chunk, c.dtype)
+        w = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+        call = lambda: binding.fwd(x["q"], x["k"], x["v"], x["g"], x["lam"], chunk=c.chunk,  # noqa: E731
+                                   out=o, workspace=w, stream=stream)
+        desc = f"{wname}: B={c.B} H={c.H} T={c.T} dk=dv={c.dk} chunk={c.chunk} bf16 in, fp32 out"
+        ms_cold = time_fwd_calls(call, stream, dev, reps, flush_buf=flush)
+        line = fwd_line(desc, c, ms_cold, 4, hbm_peak, bf16_peak, {"l2": "flushed before every call"})
+        line["launches_per_call"] = binding.load().lla_fwd_launches(c.B, c.H, c.T, c.dk, c.dv, c.chunk,
+                                                                    binding.LLA_BF16, binding.LLA_F32)
+        if fwd_bytes(c) < 100e6:
+            ms_warm = time_fwd_calls(call, stream, dev, reps)
+            line["warm"] = fwd_line(desc, c, ms_warm, 4, hbm_peak, bf16_peak,
+                                    {"l2": "warm (the inputs stay in L2 between calls)"})
+        lines[wname] = line
+        del x, o, w
+    del flush
+    return lines
 
 
 def run_next_rows(dev, x, cfg, args):
@@ -614,6 +688,8 @@ def main():
     ap.add_argument("--skip-next", action="store_true",
                     help="skip the prefill / lambda-MLP / backward timings")
     ap.add_argument("--skip-bwd", action="store_true", help="skip the backward timing")
+    ap.add_argument("--skip-configs", action="store_true",
+                    help="skip the bf16-out and T=8192 / T=2048 forward lines")
     ap.add_argument("--cpu-tokens", type=int, default=32768)
     ap.add_argument("--ref-tokens", type=int, default=2048)
     ap.add_argument("--heads", type=int, default=0, help="override H (smaller profiling case)")

@@ -32,6 +32,16 @@
  *     launch was rejected by the CUDA runtime (the runtime's last error is
  *     left for the caller to inspect with cudaGetLastError).
  *   - The current CUDA device must be the device that owns the pointers.
+ *   - Errors found while the kernels run.  The tensor-core kernels hand work
+ *     between warps and copy engines through shared-memory barriers; every
+ *     wait on one is bounded (about half a second).  A wait that runs out
+ *     records an lla_device_error code and the kernel carries on to its end
+ *     (every later wait is bounded too), so the GPU never hangs; the output
+ *     of that call is then invalid.  Entry points with such waits
+ *     take `int32_t *device_error`: NULL, or one int32 of device memory owned
+ *     by the caller that the kernels set (atomically, first code wins) and
+ *     never clear.  Zero it before the calls it should cover and read it
+ *     with lla_device_error_check once they are done.
  */
 #ifndef LLA_H
 #define LLA_H
@@ -54,14 +64,39 @@ typedef enum {
     LLA_ERR_UNSUPPORTED_SHAPE = 2,   /* a size outside the supported set          */
     LLA_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < the query's answer       */
     LLA_ERR_CUDA = 4,                /* a kernel launch failed                     */
-    LLA_ERR_DEVICE_REPORTED = 5      /* reserved for errors read back from device */
+    LLA_ERR_DEVICE_REPORTED = 5      /* a kernel recorded an error (device_error) */
 } lla_status;
+
+/* Codes the kernels store in a caller's device_error word (forward, backward,
+ * prefill, lambda producer; the decode steps store 1 + b instead, see there). */
+typedef enum {
+    LLA_DEVERR_NONE = 0,
+    LLA_DEVERR_COPY_TIMEOUT = 1,  /* a bulk copy into shared memory did not land in time     */
+    LLA_DEVERR_SYNC_TIMEOUT = 2   /* a tensor-core product or a warp hand-off did not finish */
+} lla_device_error;
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *lla_status_string(lla_status s);
 
 /* Library version as 10000*major + 100*minor + patch. */
 int lla_version(void);
+
+/* Reads a device_error word after the work it covers: synchronises `stream`,
+ * copies the int32 at device address device_error to the host and returns
+ * LLA_OK when it is 0, LLA_ERR_DEVICE_REPORTED otherwise (the code is stored
+ * in *code when code is non-NULL).  The word is left as it is.  NULL
+ * device_error: LLA_ERR_INVALID_ARGUMENT; a failed copy: LLA_ERR_CUDA.
+ * This is the one call of the library that blocks the host. */
+lla_status lla_device_error_check(const int32_t *device_error, int32_t *code, void *stream);
+
+/* Test hook for the reporting path above (the pages have no counterpart).
+ * While enabled (nonzero), every tensor-core forward launch withholds the
+ * first product of each tile (the intra-tile Q K^T: neither the product nor
+ * its completion signal is issued, so no copy or product is left in flight)
+ * and bounds its waits at a few thousand polls: the waits on that product
+ * run out, LLA_DEVERR_SYNC_TIMEOUT is recorded and the launch finishes with
+ * an invalid output.  Process-wide; 0 restores normal operation. */
+void lla_debug_withhold_first_product(int enable);
 
 /* L = 1 + bit_length(T-1): lambda entries per token for a length-T forward
  * (level 0 plus the Fenwick levels of the longest prefix).  0 for T <= 0. */
@@ -88,6 +123,10 @@ int lla_num_levels(int T);
  * 256-byte aligned; its contents on entry do not matter and are undefined on
  * return.  Calls that share a workspace must not overlap on the GPU.
  * q, k, v, g, lambda are read only; out must not alias an input.
+ * device_error: NULL or a caller-owned device int32 (see the conventions
+ * above); the tensor-core path (bf16, dk = dv = 128) may set it to
+ * LLA_DEVERR_COPY_TIMEOUT or LLA_DEVERR_SYNC_TIMEOUT; the CUDA-core path has
+ * no waits and never writes it.
  */
 size_t lla_fwd_workspace_bytes(int B, int H, int T, int dk, int dv, int chunk,
                                lla_dtype in_dt);
@@ -101,7 +140,8 @@ lla_status lla_fwd(const void *q, const void *k, const void *v,
                    const float *g, const float *lambda, void *out,
                    int B, int H, int T, int dk, int dv, int chunk,
                    lla_dtype in_dt, lla_dtype out_dt,
-                   void *workspace, size_t workspace_bytes, void *stream);
+                   void *workspace, size_t workspace_bytes, int32_t *device_error,
+                   void *stream);
 
 /*
  * lla_fwd for callers that cannot allocate device memory.  The pages have
@@ -112,11 +152,16 @@ lla_status lla_fwd(const void *q, const void *k, const void *v,
  * Same arguments, layouts and results as lla_fwd, without the workspace:
  * the scratch is one fixed array of lla_fwd_noalloc_max_scratch_bytes()
  * bytes (64 MiB) compiled into the library, present on every GPU that loads
- * it until the process exits.  A call that needs more scratch than that
+ * it until the process exits.  Arguments are checked in lla_fwd's order
+ * (shape and dtype, pointers and alignment, the stream's device); then a
+ * call that needs more scratch than the array holds
  * (lla_fwd_workspace_bytes(...) > the maximum) returns
- * LLA_ERR_WORKSPACE_TOO_SMALL and enqueues nothing.  The first call on a
- * device looks up the array's address with that device current; make it
- * before any stream capture.  All calls share the array: calls that may
+ * LLA_ERR_WORKSPACE_TOO_SMALL.  Nothing is enqueued on any error.
+ * `stream` must belong to the current device (LLA_ERR_INVALID_ARGUMENT
+ * otherwise): the array's address is looked up per device.  The first call
+ * on a device looks that address up with the device current; make it before
+ * any stream capture.  A failed look-up returns LLA_ERR_CUDA and is tried
+ * again by the next call.  All calls share the array: calls that may
  * overlap on the GPU race and must be ordered by the caller.  The library
  * allocates nothing and nothing needs clearing between calls.
  */
@@ -125,7 +170,8 @@ size_t lla_fwd_noalloc_max_scratch_bytes(void);
 lla_status lla_fwd_noalloc(const void *q, const void *k, const void *v,
                            const float *g, const float *lambda, void *out,
                            int B, int H, int T, int dk, int dv, int chunk,
-                           lla_dtype in_dt, lla_dtype out_dt, void *stream);
+                           lla_dtype in_dt, lla_dtype out_dt, int32_t *device_error,
+                           void *stream);
 
 /*
  * Decode state (the recurrent form of "Log-Linear Attention" §2.3: O(log T)
@@ -174,6 +220,8 @@ lla_status lla_decode_step(float *state_levels, float *state_logdecay,
  * state_levels [B,H,Ls,dk,dv] fp32 and state_logdecay [B,H,Ls] fp32 are
  * fully overwritten.  Requires bit_length(T) <= Ls <= 40, T <= 2^30.
  * workspace: at least lla_prefill_workspace_bytes(B,H,T) bytes.
+ * device_error: NULL or a caller-owned device int32, set by the tensor-core
+ * path (bf16, dk = dv = 128) as for lla_fwd.
  */
 size_t lla_prefill_workspace_bytes(int B, int H, int T);
 
@@ -181,7 +229,7 @@ lla_status lla_prefill_state(const void *k, const void *v, const float *g,
                              float *state_levels, float *state_logdecay,
                              int B, int H, int T, int dk, int dv, int Ls,
                              lla_dtype in_dt, void *workspace,
-                             size_t workspace_bytes, void *stream);
+                             size_t workspace_bytes, int32_t *device_error, void *stream);
 
 /*
  * lla_fwd on inputs and outputs in host memory (same layouts and dtypes as
@@ -196,7 +244,8 @@ lla_status lla_prefill_state(const void *k, const void *v, const float *g,
  * makes the host output valid.  Results are identical to lla_fwd.
  * workspace: device memory of at least lla_fwd_host_workspace_bytes(...)
  * bytes (two slots of group-sized copies plus the forward's workspace),
- * 256-byte aligned.  Errors as lla_fwd, all before the first copy.
+ * 256-byte aligned.  Errors as lla_fwd, all before the first copy;
+ * device_error (device memory, nullable) as for lla_fwd, covering every group.
  */
 size_t lla_fwd_host_workspace_bytes(int B, int H, int T, int dk, int dv, int chunk,
                                     lla_dtype in_dt, lla_dtype out_dt, int group);
@@ -204,7 +253,8 @@ size_t lla_fwd_host_workspace_bytes(int B, int H, int T, int dk, int dv, int chu
 lla_status lla_fwd_host(const void *q, const void *k, const void *v, const float *g,
                         const float *lambda, void *out, int B, int H, int T, int dk,
                         int dv, int chunk, lla_dtype in_dt, lla_dtype out_dt, int group,
-                        void *workspace, size_t workspace_bytes, void *stream);
+                        void *workspace, size_t workspace_bytes, int32_t *device_error,
+                        void *stream);
 
 /*
  * Log-Linear Gated DeltaNet ("Log-Linear Attention" §3 names it: the Gated
@@ -293,6 +343,8 @@ lla_status lla_gdn_decode_step(float *state, const void *q, const void *k,
  * LLA_ERR_UNSUPPORTED_SHAPE, a NULL pointer or misaligned workspace
  * LLA_ERR_INVALID_ARGUMENT, a short workspace LLA_ERR_WORKSPACE_TOO_SMALL,
  * all before any launch; a failed launch returns LLA_ERR_CUDA.
+ * device_error: NULL or a caller-owned device int32, set by the tensor-core
+ * parts as for lla_fwd.
  */
 size_t lla_bwd_workspace_bytes(int B, int H, int T, int dk, int dv, int chunk,
                                lla_dtype in_dt);
@@ -301,7 +353,8 @@ lla_status lla_bwd(const void *q, const void *k, const void *v, const float *g,
                    const float *lambda, const float *dout, float *dq, float *dk,
                    float *dv, float *dg, float *dlambda, int B, int H, int T,
                    int dk_dim, int dv_dim, int chunk, lla_dtype in_dt,
-                   void *workspace, size_t workspace_bytes, void *stream);
+                   void *workspace, size_t workspace_bytes, int32_t *device_error,
+                   void *stream);
 
 /*
  * Level weights from a two-layer MLP ("Adaptive memory decay for Log-Linear
@@ -313,10 +366,13 @@ lla_status lla_bwd(const void *q, const void *k, const void *v, const float *g,
  *   W1     [Dd, 2L]  fp32     W2 [2L, L] fp32     b [L] fp32 (shared by heads)
  *   lambda [B,H,T,L] fp32     output, the layout lla_fwd reads
  * Supported: 1 <= Dd <= 256, 1 <= L <= 32 (shared memory holds the weights).
+ * device_error: NULL or a caller-owned device int32, set by the tensor-core
+ * path (bf16 d, Dd a multiple of 64) as for lla_fwd.
  */
 lla_status lla_lambda_mlp(const void *d, const float *W1, const float *W2,
                           const float *b, float *lambda, int B, int H, int T,
-                          int Dd, int L, lla_dtype in_dt, void *stream);
+                          int Dd, int L, lla_dtype in_dt, int32_t *device_error,
+                          void *stream);
 
 #ifdef __cplusplus
 }

@@ -28,21 +28,23 @@ SIGNATURES = {
     "lla_num_levels": (_I, [_I]),
     "lla_fwd_workspace_bytes": (_Z, [_I] * 6 + [_I]),
     "lla_fwd_launches": (_I, [_I] * 8),
-    "lla_fwd": (_I, [_P] * 6 + [_I] * 6 + [_I, _I] + [_P, _Z, _P]),
+    "lla_fwd": (_I, [_P] * 6 + [_I] * 6 + [_I, _I] + [_P, _Z, _P, _P]),
     "lla_fwd_noalloc_max_scratch_bytes": (_Z, []),
-    "lla_fwd_noalloc": (_I, [_P] * 6 + [_I] * 6 + [_I, _I] + [_P]),
+    "lla_fwd_noalloc": (_I, [_P] * 6 + [_I] * 6 + [_I, _I] + [_P, _P]),
     "lla_decode_state_bytes": (_Z, [_I] * 5),
     "lla_decode_step": (_I, [_P] * 9 + [_I] * 5 + [_I, _P, _P]),
     "lla_prefill_workspace_bytes": (_Z, [_I] * 3),
-    "lla_prefill_state": (_I, [_P] * 5 + [_I] * 6 + [_I, _P, _Z, _P]),
-    "lla_lambda_mlp": (_I, [_P] * 5 + [_I] * 5 + [_I, _P]),
+    "lla_prefill_state": (_I, [_P] * 5 + [_I] * 6 + [_I, _P, _Z, _P, _P]),
+    "lla_lambda_mlp": (_I, [_P] * 5 + [_I] * 5 + [_I, _P, _P]),
     "lla_bwd_workspace_bytes": (_Z, [_I] * 7),
-    "lla_bwd": (_I, [_P] * 11 + [_I] * 7 + [_P, _Z, _P]),
+    "lla_bwd": (_I, [_P] * 11 + [_I] * 7 + [_P, _Z, _P, _P]),
     "lla_gdn_fwd_workspace_bytes": (_Z, [_I] * 5),
     "lla_gdn_fwd": (_I, [_P] * 8 + [_I] * 6 + [_I, _P, _Z, _P]),
     "lla_fwd_host_workspace_bytes": (_Z, [_I] * 9),
-    "lla_fwd_host": (_I, [_P] * 6 + [_I] * 6 + [_I, _I, _I, _P, _Z, _P]),
+    "lla_fwd_host": (_I, [_P] * 6 + [_I] * 6 + [_I, _I, _I, _P, _Z, _P, _P]),
     "lla_gdn_decode_step": (_I, [_P] * 9 + [_I] * 5 + [_I, _P, _P]),
+    "lla_device_error_check": (_I, [_P, _P, _P]),
+    "lla_debug_withhold_first_product": (None, [_I]),
 }
 
 _lib = None
@@ -91,6 +93,30 @@ def _check(name, code):
         raise LLAError(name, code)
 
 
+def _err_ptr(device_error):
+    if device_error is None:
+        return None
+    _need(device_error, "device_error", torch.int32, None)
+    if device_error.numel() < 1:
+        raise ValueError("device_error needs one int32 element")
+    return ctypes.c_void_p(device_error.data_ptr())
+
+
+def device_error_check(device_error, stream=None):
+    """lla_device_error_check: synchronise the stream and return the code in
+    device_error (0 when no kernel reported anything)."""
+    code = ctypes.c_int32(0)
+    rc = load().lla_device_error_check(_err_ptr(device_error), ctypes.byref(code), _stream(stream))
+    if rc not in (0, 5):
+        raise LLAError("lla_device_error_check", rc)
+    return int(code.value)
+
+
+def debug_withhold_first_product(enable: bool):
+    """lla_debug_withhold_first_product: the test hook of the reporting path."""
+    load().lla_debug_withhold_first_product(1 if enable else 0)
+
+
 def _need(t, name, dtype=None, ndim=None):
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
@@ -111,9 +137,11 @@ def fwd_workspace_bytes(B, H, T, dk, dv, chunk, in_dtype) -> int:
 
 
 def fwd(q, k, v, g, lam, chunk: int = 64, out_dtype=torch.float32, out=None, workspace=None,
-        stream=None):
+        device_error=None, stream=None):
     """lla_fwd on torch tensors: q,k [B,H,T,dk], v [B,H,T,dv] (fp32 or bf16),
-    g [B,H,T] fp32, lam [B,H,T,L] fp32.  Returns out [B,H,T,dv]."""
+    g [B,H,T] fp32, lam [B,H,T,L] fp32.  Returns out [B,H,T,dv].
+    device_error: optional int32 CUDA tensor of one element (see
+    device_error_check)."""
     lib = load()
     for n, t in (("q", q), ("k", k), ("v", v)):
         _need(t, n, q.dtype, 4)
@@ -132,7 +160,8 @@ def fwd(q, k, v, g, lam, chunk: int = 64, out_dtype=torch.float32, out=None, wor
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     rc = lib.lla_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(lam), _ptr(out), B, H, T, dk, dv,
-                     chunk, in_dt, _dt(out), _ptr(workspace), workspace.numel(), _stream(stream))
+                     chunk, in_dt, _dt(out), _ptr(workspace), workspace.numel(),
+                     _err_ptr(device_error), _stream(stream))
     _check("lla_fwd", rc)
     return out
 
@@ -168,7 +197,8 @@ def decode_step(state, logdecay, q, k, v, g, lam, pos, out=None, device_error=No
     return out
 
 
-def prefill_state(k, v, g, Ls: int, state=None, logdecay=None, workspace=None, stream=None):
+def prefill_state(k, v, g, Ls: int, state=None, logdecay=None, workspace=None, device_error=None,
+                  stream=None):
     """lla_prefill_state: decode state after the prefix k,v [B,H,T,d], g [B,H,T]."""
     lib = load()
     _need(k, "k", None, 4)
@@ -185,12 +215,12 @@ def prefill_state(k, v, g, Ls: int, state=None, logdecay=None, workspace=None, s
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=k.device)
     rc = lib.lla_prefill_state(_ptr(k), _ptr(v), _ptr(g), _ptr(state), _ptr(logdecay), B, H, T,
                                dk, dv, Ls, _dt(k), _ptr(workspace), workspace.numel(),
-                               _stream(stream))
+                               _err_ptr(device_error), _stream(stream))
     _check("lla_prefill_state", rc)
     return state, logdecay
 
 
-def lambda_mlp(d, W1, W2, b, out=None, stream=None):
+def lambda_mlp(d, W1, W2, b, out=None, device_error=None, stream=None):
     """lla_lambda_mlp: lambda [B,H,T,L] = softplus((d W1) W2 + b) for
     d [B,H,T,Dd] (fp32 or bf16), W1 [Dd,2L], W2 [2L,L], b [L] fp32."""
     lib = load()
@@ -204,12 +234,12 @@ def lambda_mlp(d, W1, W2, b, out=None, stream=None):
     if out is None:
         out = torch.empty((B, H, T, L), dtype=torch.float32, device=d.device)
     rc = lib.lla_lambda_mlp(_ptr(d), _ptr(W1), _ptr(W2), _ptr(b), _ptr(out), B, H, T, Dd, L,
-                            _dt(d), _stream(stream))
+                            _dt(d), _err_ptr(device_error), _stream(stream))
     _check("lla_lambda_mlp", rc)
     return out
 
 
-def bwd(q, k, v, g, lam, dout, chunk: int = 64, workspace=None, stream=None):
+def bwd(q, k, v, g, lam, dout, chunk: int = 64, workspace=None, device_error=None, stream=None):
     """lla_bwd: gradients (dq, dk, dv, dg, dlam) of sum(dout * lla_fwd(q, k, v, g, lam))."""
     lib = load()
     for n, t in (("q", q), ("k", k), ("v", v)):
@@ -235,7 +265,7 @@ def bwd(q, k, v, g, lam, dout, chunk: int = 64, workspace=None, stream=None):
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     rc = lib.lla_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(lam), _ptr(dout), _ptr(dq), _ptr(dkk),
                      _ptr(dvv), _ptr(dg), _ptr(dl), B, H, T, dk, dv, chunk, in_dt, _ptr(workspace),
-                     workspace.numel(), _stream(stream))
+                     workspace.numel(), _err_ptr(device_error), _stream(stream))
     _check("lla_bwd", rc)
     return dq, dkk, dvv, dg, dl
 
@@ -299,7 +329,7 @@ def gdn_decode_step(state, q, k, v, g, beta, lam, pos, out=None, device_error=No
 
 
 def fwd_host(q, k, v, g, lam, out=None, chunk: int = 64, out_dtype=torch.float32, group: int = 0,
-             workspace=None, stream=None, device=None):
+             workspace=None, device_error=None, stream=None, device=None):
     """lla_fwd_host: the forward on CPU tensors (pin them for overlap), run on
     `device`; returns the CPU output (valid once `stream` is synchronised)."""
     lib = load()
@@ -317,6 +347,6 @@ def fwd_host(q, k, v, g, lam, out=None, chunk: int = 64, out_dtype=torch.float32
     with torch.cuda.device(device):
         rc = lib.lla_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(lam), _ptr(out), B, H, T, dk, dv,
                               chunk, _dt(q), _dt(out), group, _ptr(workspace), workspace.numel(),
-                              _stream(stream))
+                              _err_ptr(device_error), _stream(stream))
     _check("lla_fwd_host", rc)
     return out

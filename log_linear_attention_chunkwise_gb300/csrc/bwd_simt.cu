@@ -712,12 +712,15 @@ cudaError_t launch_bwd(const BwdArgs &A)
     float *R = (float *)(ws + lay.R);
     float *parts = (float *)(ws + lay.parts);
     double *dG = (double *)(ws + lay.dG);
+    // bounded waits of the tensor-core parts report into the caller's word,
+    // else into a workspace word cleared before each part
+    int *const err = A.device_error ? (int *)A.device_error : (int *)(ws + lay.err);
+    auto clear_err = [&]() { return A.device_error ? cudaSuccess : cudaMemsetAsync(err, 0, sizeof(int), st); };
     bwd_gamma_kernel<<<dim3(N, BH), 32, 0, st>>>(A.g, gamma, A.T, A.C);
     cudaError_t e;
     if (bwd_state_tc_supported(A)) {
         // the forward's chunk states on the tensor cores, then its prefix and scan
-        int *err = (int *)(ws + lay.err);
-        e = cudaMemsetAsync(err, 0, sizeof(int), st);
+        e = clear_err();
         if (e != cudaSuccess) return e;
         e = bwd_state_tc(A, gamma, (float *)ws, nodes, err);
         if (e != cudaSuccess) return e;
@@ -727,8 +730,7 @@ cudaError_t launch_bwd(const BwdArgs &A)
     }
     if (e != cudaSuccess) return e;
     if (bwd_intra_tc_supported(A)) {
-        int *err = (int *)(ws + lay.err);
-        e = cudaMemsetAsync(err, 0, sizeof(int), st);
+        e = clear_err();
         if (e != cudaSuccess) return e;
         e = bwd_intra_tc(A, gamma, err);
         if (e != cudaSuccess) return e;
@@ -741,8 +743,7 @@ cudaError_t launch_bwd(const BwdArgs &A)
             A.dkey, A.dval, A.dlam, A.T, A.dk, A.dv, A.C, cbits, N, A.L, bwd_query_tc_supported(A) ? 0 : 1);
     }
     if (bwd_query_tc_supported(A) && N > 1) {
-        int *err = (int *)(ws + lay.err);
-        e = cudaMemsetAsync(err, 0, sizeof(int), st);
+        e = clear_err();
         if (e != cudaSuccess) return e;
         e = bwd_query_tc(A, gamma, P, nodes, err);
         if (e != cudaSuccess) return e;
@@ -751,7 +752,7 @@ cudaError_t launch_bwd(const BwdArgs &A)
     const int Pc = piece_chunks(A.C), nitems = total_items(N, Pc);
     if (nitems > 0) {
         if (bwd_piece_tc_supported(A)) {
-            e = bwd_piece_tc(A, gamma, P, parts, nlev, Pc, nitems, (int *)(ws + lay.err));
+            e = bwd_piece_tc(A, gamma, P, parts, nlev, Pc, nitems, err);
             if (e != cudaSuccess) return e;
         } else {
             bwd_block_piece_kernel<Tin><<<dim3(nitems, BH), kThreads, 0, st>>>(
@@ -763,8 +764,7 @@ cudaError_t launch_bwd(const BwdArgs &A)
             bwd_block_reduce_kernel<<<dim3(nred, BH), kThreads, 0, st>>>(parts, R, A.dk, A.dv, N, nlev, Pc, nitems,
                                                                          nblocks);
         if (bwd_key_tc_supported(A)) {
-            int *err = (int *)(ws + lay.err);
-            e = cudaMemsetAsync(err, 0, sizeof(int), st);
+            e = clear_err();
             if (e != cudaSuccess) return e;
             e = bwd_key_tc(A, gamma, P, R, parts, nlev, nblocks, Pc, nitems, err);
             if (e != cudaSuccess) return e;

@@ -14,6 +14,7 @@ struct BwdArgs {
     int B, H, T, dk, dv, C, L;
     lla_dtype in_dt;
     void *workspace;
+    int32_t *device_error;  // caller's word, or nullptr (the workspace word is used)
     void *stream;
 };
 

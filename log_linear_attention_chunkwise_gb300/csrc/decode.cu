@@ -340,9 +340,12 @@ cudaError_t launch_prefill(const PrefillArgs &A)
     prefill_chunk_carry_kernel<<<(unsigned)BH, 32, 0, st>>>(csum, carry, nchunk);
     prefill_tail_kernel<<<dim3(nchunk, (unsigned)BH), kTailChunk, 0, st>>>(A.g, carry, tail, A.T, nchunk);
     if (prefill_tc_supported(A)) {
-        int *dev_err = (int *)((char *)(carry + align_up((size_t)BH * nchunk, 32)));
-        err = cudaMemsetAsync(dev_err, 0, sizeof(int), st);
-        if (err != cudaSuccess) return err;
+        int *dev_err = A.device_error ? (int *)A.device_error
+                                      : (int *)((char *)(carry + align_up((size_t)BH * nchunk, 32)));
+        if (!A.device_error) {
+            err = cudaMemsetAsync(dev_err, 0, sizeof(int), st);
+            if (err != cudaSuccess) return err;
+        }
         return prefill_tc(A, tail, dev_err);
     }
     prefill_bucket_kernel<Tin><<<dim3(nseg, (unsigned)BH), kThreads, 0, st>>>(

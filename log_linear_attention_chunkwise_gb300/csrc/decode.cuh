@@ -26,6 +26,7 @@ struct PrefillArgs {
     int B, H, T, dk, dv, Ls;
     lla_dtype in_dt;
     void *workspace;
+    int32_t *device_error;  // caller's word, or nullptr (a workspace word is used)
     void *stream;
 };
 

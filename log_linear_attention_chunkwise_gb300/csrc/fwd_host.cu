@@ -10,8 +10,9 @@
 // two directions instead of their sum.
 //
 // The two internal streams and the ordering events are created once per
-// device on the first call (with that device current) and kept until exit;
-// a mutex per device serialises the enqueueing of concurrent calls.  The
+// device on the first call (with that device current) and kept until exit
+// (a creation that fails is undone and tried again by the next call); a
+// mutex per device serialises the enqueueing of concurrent calls.  The
 // call is ordered on the caller's stream: work already on it completes
 // before any copy starts, and the caller's stream waits for the last output
 // copy.  Host buffers should be pinned (page-locked) for the copies to run
@@ -29,28 +30,49 @@ struct Pipe {
     cudaEvent_t entry = nullptr, done = nullptr;
     cudaEvent_t in_ready[2] = {nullptr, nullptr}, comp_done[2] = {nullptr, nullptr},
                 out_done[2] = {nullptr, nullptr};
-    cudaError_t err = cudaSuccess;
-    std::mutex mu;
+    bool ready = false;
+    std::mutex mu;  // guards the set-up and serialises the enqueueing
 };
 
 Pipe g_pipe[kMaxDevices];
-std::once_flag g_pipe_once[kMaxDevices];
 
-Pipe *pipe_for_current_device()
+void destroy_pipe(Pipe *p)
+{
+    cudaEvent_t *evs[] = {&p->entry, &p->done, &p->in_ready[0], &p->in_ready[1], &p->comp_done[0],
+                          &p->comp_done[1], &p->out_done[0], &p->out_done[1]};
+    for (cudaEvent_t *ev : evs)
+        if (*ev) {
+            cudaEventDestroy(*ev);
+            *ev = nullptr;
+        }
+    if (p->h2d) cudaStreamDestroy(p->h2d);
+    if (p->d2h) cudaStreamDestroy(p->d2h);
+    p->h2d = p->d2h = nullptr;
+}
+
+// The current device's pipe with p->mu held (streams and events created on
+// first use); nullptr if they cannot be created.
+Pipe *lock_pipe_for_current_device(std::unique_lock<std::mutex> *lock)
 {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
     Pipe *p = &g_pipe[dev];
-    std::call_once(g_pipe_once[dev], [p]() {
+    *lock = std::unique_lock<std::mutex>(p->mu);
+    if (!p->ready) {
         cudaError_t e = cudaStreamCreateWithFlags(&p->h2d, cudaStreamNonBlocking);
         if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->d2h, cudaStreamNonBlocking);
         cudaEvent_t *evs[] = {&p->entry, &p->done, &p->in_ready[0], &p->in_ready[1], &p->comp_done[0],
                               &p->comp_done[1], &p->out_done[0], &p->out_done[1]};
         for (cudaEvent_t *ev : evs)
             if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
-        p->err = e;
-    });
-    return p->err == cudaSuccess ? p : nullptr;
+        if (e != cudaSuccess) {
+            destroy_pipe(p);
+            cudaGetLastError();
+            return nullptr;
+        }
+        p->ready = true;
+    }
+    return p;
 }
 
 size_t dt_size(lla_dtype dt) { return dt == LLA_BF16 ? 2 : 4; }
@@ -102,20 +124,23 @@ size_t lla_fwd_host_workspace_bytes(int B, int H, int T, int dk, int dv, int chu
 
 lla_status lla_fwd_host(const void *q, const void *k, const void *v, const float *g, const float *lambda,
                         void *out, int B, int H, int T, int dk, int dv, int chunk, lla_dtype in_dt,
-                        lla_dtype out_dt, int group, void *workspace, size_t workspace_bytes, void *stream)
+                        lla_dtype out_dt, int group, void *workspace, size_t workspace_bytes,
+                        int32_t *device_error, void *stream)
 {
     // shapes, dtypes and the empty case exactly as lla_fwd decides them
     if (B < 0 || H < 0 || T < 0 || group < 0) return LLA_ERR_INVALID_ARGUMENT;
     if (out_dt != LLA_F32 && out_dt != LLA_BF16) return LLA_ERR_INVALID_ARGUMENT;
     if ((long long)B * H * T == 0)
-        return lla_fwd(q, k, v, g, lambda, out, B, H, T, dk, dv, chunk, in_dt, out_dt, nullptr, 0, stream);
+        return lla_fwd(q, k, v, g, lambda, out, B, H, T, dk, dv, chunk, in_dt, out_dt, nullptr, 0,
+                       device_error, stream);
     if (lla_fwd_workspace_bytes(1, 1, T, dk, dv, chunk, in_dt) == 0) return LLA_ERR_UNSUPPORTED_SHAPE;
     if (in_dt == LLA_F32 && out_dt != LLA_F32) return LLA_ERR_UNSUPPORTED_SHAPE;
     if (!q || !k || !v || !g || !lambda || !out) return LLA_ERR_INVALID_ARGUMENT;
     const size_t need = lla_fwd_host_workspace_bytes(B, H, T, dk, dv, chunk, in_dt, out_dt, group);
     if (workspace_bytes < need) return LLA_ERR_WORKSPACE_TOO_SMALL;
     if (workspace == nullptr || ((uintptr_t)workspace & 255u) != 0) return LLA_ERR_INVALID_ARGUMENT;
-    Pipe *p = pipe_for_current_device();
+    std::unique_lock<std::mutex> lock;
+    Pipe *p = lock_pipe_for_current_device(&lock);
     if (!p) return LLA_ERR_CUDA;
     const long long BH = (long long)B * H;
     const int G = resolve_group(BH, group);
@@ -125,7 +150,6 @@ lla_status lla_fwd_host(const void *q, const void *k, const void *v, const float
     void *fws = ws + 2 * sb;
     const size_t fws_bytes = workspace_bytes - 2 * sb;
     cudaStream_t cs = (cudaStream_t)stream;
-    std::lock_guard<std::mutex> lock(p->mu);
 #define LLA_TRY(x)                                       \
     do {                                                 \
         if ((x) != cudaSuccess) return LLA_ERR_CUDA;     \
@@ -158,7 +182,7 @@ lla_status lla_fwd_host(const void *q, const void *k, const void *v, const float
         LLA_TRY(cudaStreamWaitEvent(cs, p->in_ready[sl], 0));
         LLA_TRY(cudaStreamWaitEvent(cs, p->out_done[sl], 0));
         lla_status st = lla_fwd(dq, dk_, dv_, (const float *)dg, (const float *)dl, dout, 1, n, T, dk, dv,
-                                chunk, in_dt, out_dt, fws, fws_bytes, stream);
+                                chunk, in_dt, out_dt, fws, fws_bytes, device_error, stream);
         if (st != LLA_OK) return st;
         LLA_TRY(cudaEventRecord(p->comp_done[sl], cs));
         // its output back to the host

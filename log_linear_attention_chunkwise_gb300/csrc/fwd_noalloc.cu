@@ -11,6 +11,9 @@
 // library, held until the process exits.  The first call on a device looks
 // up the array's device address (cudaGetSymbolAddress, with that device
 // current) and caches it; make that first call before any stream capture.
+// A look-up that fails is not cached: the call returns LLA_ERR_CUDA and the
+// next call tries again.  The address belongs to the current device, so the
+// stream must belong to it too (checked where the runtime can tell).
 // All calls share the one array and it keeps the last call's contents, so
 // calls that overlap on the GPU (different streams, no ordering between
 // them) race and must not be issued.  The forward resets every piece of the
@@ -30,20 +33,21 @@ constexpr int kMaxDevices = 64;
 __device__ __align__(256) unsigned char lla_noalloc_scratch[kNoAllocScratchBytes];
 
 void *g_scratch_ptr[kMaxDevices];
-cudaError_t g_setup_err[kMaxDevices];
-std::once_flag g_setup_once[kMaxDevices];
+std::mutex g_setup_mu;
 
-// Device address of the scratch array on the current device (set up once).
-lla_status scratch_for_current_device(void **ptr)
+// Device address of the scratch array on device `dev` (the current device);
+// only a successful look-up is kept.
+lla_status scratch_for_device(int dev, void **ptr)
 {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LLA_ERR_CUDA;
-    std::call_once(g_setup_once[dev], [dev]() {
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    if (g_scratch_ptr[dev] == nullptr) {
         void *p = nullptr;
-        g_setup_err[dev] = cudaGetSymbolAddress(&p, lla_noalloc_scratch);
+        if (cudaGetSymbolAddress(&p, lla_noalloc_scratch) != cudaSuccess || p == nullptr) {
+            cudaGetLastError();  // leave no sticky-looking error behind for the caller
+            return LLA_ERR_CUDA;
+        }
         g_scratch_ptr[dev] = p;
-    });
-    if (g_setup_err[dev] != cudaSuccess || g_scratch_ptr[dev] == nullptr) return LLA_ERR_CUDA;
+    }
     *ptr = g_scratch_ptr[dev];
     return LLA_OK;
 }
@@ -56,19 +60,30 @@ size_t lla_fwd_noalloc_max_scratch_bytes(void) { return kNoAllocScratchBytes; }
 
 lla_status lla_fwd_noalloc(const void *q, const void *k, const void *v, const float *g,
                            const float *lambda, void *out, int B, int H, int T, int dk, int dv,
-                           int chunk, lla_dtype in_dt, lla_dtype out_dt, void *stream)
+                           int chunk, lla_dtype in_dt, lla_dtype out_dt, int32_t *device_error,
+                           void *stream)
 {
-    // shape and dtype errors come back from lla_fwd itself, before any launch
+    // lla_fwd's own checks first, in its order, so that the status of a bad
+    // call does not depend on which entry point it came through
+    bool empty = false;
+    lla_status st = lla::fwd_args_status(q, k, v, g, lambda, out, B, H, T, dk, dv, chunk, in_dt,
+                                         out_dt, &empty);
+    if (st != LLA_OK || empty) return st;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LLA_ERR_CUDA;
+    int stream_dev = -1;
+    if (cudaStreamGetDevice((cudaStream_t)stream, &stream_dev) == cudaSuccess) {
+        if (stream_dev != dev) return LLA_ERR_INVALID_ARGUMENT;
+    } else {
+        cudaGetLastError();  // a runtime without the query: the documented duty stays the caller's
+    }
     const size_t need = lla_fwd_workspace_bytes(B, H, T, dk, dv, chunk, in_dt);
     if (need > kNoAllocScratchBytes) return LLA_ERR_WORKSPACE_TOO_SMALL;
-    if (need == 0)  // empty or rejected: lla_fwd decides which, with no scratch
-        return lla_fwd(q, k, v, g, lambda, out, B, H, T, dk, dv, chunk, in_dt, out_dt, nullptr, 0,
-                       stream);
     void *scratch = nullptr;
-    lla_status st = scratch_for_current_device(&scratch);
+    st = scratch_for_device(dev, &scratch);
     if (st != LLA_OK) return st;
     return lla_fwd(q, k, v, g, lambda, out, B, H, T, dk, dv, chunk, in_dt, out_dt, scratch,
-                   kNoAllocScratchBytes, stream);
+                   kNoAllocScratchBytes, device_error, stream);
 }
 
 }  // extern "C"

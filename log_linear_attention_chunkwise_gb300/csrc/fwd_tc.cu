@@ -29,6 +29,8 @@
 // 128-byte-swizzled shared memory, fp32 accumulators in tensor memory.  The
 // read-out forms U_j = Q Node_j per path node in tensor memory and applies
 // the per-row weights in fp32 while draining it.
+#include <atomic>
+
 #include "fwd_tc.cuh"
 #include "sm100.cuh"
 #include "tma_host.cuh"
@@ -44,22 +46,25 @@ constexpr int kTileLevels = 7;   // levels inside a tile: bit_length(a ^ b) <= 7
 constexpr uint32_t kBuf = kTile * kD * 2;  // one bf16 128x128 operand: 32 KB
 constexpr uint32_t kHalf = kBuf / 2;       // one 64-column swizzled block
 constexpr uint32_t kWaitIters = 1u << 22;  // bounded waits (~0.5 s with back-off)
+constexpr uint32_t kWithheldWaitIters = 4096;  // the waits while the test hook withholds a product
 constexpr int kLamLd = 9;                  // padded row of the in-tile lambdas
 constexpr int kMaxPath = 17;               // levels of a tile index (T <= 2^24, so NT <= 2^17)
 
-// Error codes written to the workspace error word.
-constexpr int kErrLoadTimeout = 1;
-constexpr int kErrMmaTimeout = 2;
+// Error codes (lla_device_error) written to the error word.
+constexpr int kErrLoadTimeout = LLA_DEVERR_COPY_TIMEOUT;
+constexpr int kErrMmaTimeout = LLA_DEVERR_SYNC_TIMEOUT;
 
 struct TcParams {
     const float *g, *lam;
     void *out;
     const double *P;        // [BH][NT+1] tile-gate prefix sums
     float *gamma;           // [BH][T] inclusive gate sum inside each tile (fp32)
-    int *err;               // first bounded wait that gave up (0: none)
+    int *err;               // first bounded wait that gave up (0: none): the caller's word or the workspace's
     float *segtot;          // [BH][nseg_full][128][128] decayed segment totals
     __nv_bfloat16 *node16;  // [BH][NT][128][128] Fenwick nodes (index 0 unused)
     int T, NT, BH, L, nseg_full;
+    uint32_t wait_iters;    // polls before a wait gives up
+    int withhold;           // test hook: the consumer issues no S = Q K^T and no signal for it
 };
 
 __device__ __forceinline__ void set_err(int *err, int code) { atomicCAS(err, 0, code); }
@@ -188,10 +193,10 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
             const int ls = n % kWalkStages, hb = n & 1;
             if (p == 0 && n >= 1 && n - 1 + kWalkStages < ntiles) {
                 // stage of tile n-1 is free once its product is done
-                if (!mbar_wait(&s.bar_h[(n - 1) & 1], ((n - 1) >> 1) & 1, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
+                if (!mbar_wait(&s.bar_h[(n - 1) & 1], ((n - 1) >> 1) & 1, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
                 issue_load(n - 1 + kWalkStages);
             }
-            if (!mbar_wait(&s.bar_load[ls], (n / kWalkStages) & 1, kWaitIters)) set_err(prm.err, kErrLoadTimeout);
+            if (!mbar_wait(&s.bar_load[ls], (n / kWalkStages) & 1, prm.wait_iters)) set_err(prm.err, kErrLoadTimeout);
             const float Gam = s.gm[ls][kTile - 1];
             const float gam_a = s.gm[ls][p];
             {   // V row p of the slice, scaled in place by exp(Gam - gamma)
@@ -212,7 +217,7 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
             fence_proxy_async_smem();
             prep_sync();
             if (p == 0) {
-                if (n >= 2 && !mbar_wait(&s.bar_hfree[hb], ((n - 2) >> 1) & 1, kWaitIters))
+                if (n >= 2 && !mbar_wait(&s.bar_hfree[hb], ((n - 2) >> 1) & 1, prm.wait_iters))
                     set_err(prm.err, kErrMmaTimeout);
                 tc_fence_after_sync();
                 // H slice = K^T Vs: A = K^T (M = dk, MN-major), B = Vs slice (N = 32, MN-major)
@@ -236,7 +241,7 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
             const int z = __ffs(J) - 1;
             const bool cross = (J == i0 + kSeg);  // closes a full segment
             const int mlim = cross ? kSegLog : z;
-            if (!mbar_wait(&s.bar_h[hb], (n >> 1) & 1, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
+            if (!mbar_wait(&s.bar_h[hb], (n >> 1) & 1, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
             tc_fence_after_sync();
             float acc[32];
             tmem_ld16(tm_h0 + hb * kSliceW + lane_off, *reinterpret_cast<float(*)[16]>(acc));
@@ -476,14 +481,16 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
                 tma_load_3d(nd[st] + kHalf, &map_node, &s.bar_node[st], 64, 0, bh * NT + j);
             };
             const uint32_t id_kmn = idesc_bf16_f32(128, 128, false, true);
-            if (!mbar_wait(&s.bar_load, 0, kWaitIters)) set_err(prm.err, kErrLoadTimeout);
+            if (!mbar_wait(&s.bar_load, 0, prm.wait_iters)) set_err(prm.err, kErrLoadTimeout);
             tc_fence_after_sync();
-            mma_kk(slot[0], s.q, s.k, idesc_bf16_f32(128, 128, false, false));
-            umma_commit(&s.bar_s);
+            if (!prm.withhold) {  // withheld: nothing is left in flight, the waits on bar_s run out
+                mma_kk(slot[0], s.q, s.k, idesc_bf16_f32(128, 128, false, false));
+                umma_commit(&s.bar_s);
+            }
             // path nodes in order: jn[n] computed on the fly
             int jnext = i;
             if (npath > 0) {
-                if (!mbar_wait(&s.bar_s, 0, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
+                if (!mbar_wait(&s.bar_s, 0, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
                 // the nodes come from the previous launches; everything before this
                 // point reads only inputs and the gate sums
                 grid_dependency_wait();
@@ -491,7 +498,7 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
                 jnext -= (jnext & -jnext);
             }
             // O = P V: P from tensor memory once the epilogue has stored it
-            if (!mbar_wait(&s.bar_pready, 0, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
+            if (!mbar_wait(&s.bar_pready, 0, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
             tc_fence_after_sync();
 #pragma unroll
             for (int kk = 0; kk < 8; kk++)
@@ -499,13 +506,13 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
                                  desc_sw128(smem_u32(s.v) + kk * 2048, kHalf, 1024), id_kmn, kk > 0 ? 1u : 0u);
             umma_commit(&s.bar_pv);
             if (npath > 0) {
-                if (!mbar_wait(&s.bar_pv, 0, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
+                if (!mbar_wait(&s.bar_pv, 0, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
                 if (npath > 1) {
                     load_node(1, jnext);  // the V buffer is free once P V is done
                     jnext -= (jnext & -jnext);
                 }
                 // level 0 into slot 0 (P has been consumed)
-                if (!mbar_wait(&s.bar_node[0], 0, kWaitIters)) set_err(prm.err, kErrLoadTimeout);
+                if (!mbar_wait(&s.bar_node[0], 0, prm.wait_iters)) set_err(prm.err, kErrLoadTimeout);
                 tc_fence_after_sync();
                 mma_kmn(slot[0], s.q, nd[0], id_kmn);
                 umma_commit(&s.bar_u[0]);
@@ -515,19 +522,19 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
                 if (n + 1 < npath) {
                     // slot st1 is free once level n-1 (or, for level 1, P V) is drained
                     if (n == 0) {
-                        if (!mbar_wait(&s.bar_pvfree, 0, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
+                        if (!mbar_wait(&s.bar_pvfree, 0, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
                     } else {
-                        if (!mbar_wait(&s.bar_ufree[st1], ((n - 1) >> 1) & 1, kWaitIters))
+                        if (!mbar_wait(&s.bar_ufree[st1], ((n - 1) >> 1) & 1, prm.wait_iters))
                             set_err(prm.err, kErrMmaTimeout);
                     }
-                    if (!mbar_wait(&s.bar_node[st1], ((n + 1) >> 1) & 1, kWaitIters)) set_err(prm.err, kErrLoadTimeout);
+                    if (!mbar_wait(&s.bar_node[st1], ((n + 1) >> 1) & 1, prm.wait_iters)) set_err(prm.err, kErrLoadTimeout);
                     tc_fence_after_sync();
                     mma_kmn(slot[st1], s.q, nd[st1], id_kmn);
                     umma_commit(&s.bar_u[st1]);
                 }
                 if (n + 2 < npath) {
                     // node buffer st is free once level n's product is done
-                    if (!mbar_wait(&s.bar_u[st], (n >> 1) & 1, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
+                    if (!mbar_wait(&s.bar_u[st], (n >> 1) & 1, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
                     load_node(st, jnext);
                     jnext -= (jnext & -jnext);
                 }
@@ -536,7 +543,7 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
     } else {
         // ---------------- epilogue warps
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-        if (!mbar_wait(&s.bar_s, 0, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
+        if (!mbar_wait(&s.bar_s, 0, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
         tc_fence_after_sync();
         // P = S . M  (thread = query row, 64 keys), packed bf16 pairs in registers
         uint32_t pk[32];
@@ -601,7 +608,7 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
         tc_fence_before_sync();
         mbar_arrive(&s.bar_pready);
 
-        if (!mbar_wait(&s.bar_pv, 0, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
+        if (!mbar_wait(&s.bar_pv, 0, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
         tc_fence_after_sync();
         float o[64];
         {
@@ -625,7 +632,7 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
         for (int n = 0; n < npath; n++) {
             const int st = n & 1;
             const float w = s.wgt[n * kTile + row];
-            if (!mbar_wait(&s.bar_u[st], (n >> 1) & 1, kWaitIters)) set_err(prm.err, kErrMmaTimeout);
+            if (!mbar_wait(&s.bar_u[st], (n >> 1) & 1, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
             tc_fence_after_sync();
             float r2[2][16];
 #pragma unroll
@@ -681,7 +688,8 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
 
 // Gate sums, in two small launches.  First, a warp per tile: Gam_i in fp64
 // from one coalesced float4 load per lane, stored in the P array shifted by
-// one (P[i+1] = Gam_i); the workspace error word is reset here too.
+// one (P[i+1] = Gam_i); the workspace error word is reset here too (err is
+// null when the caller passed a word of its own, which is never cleared).
 // Then one CTA per (batch*head) turns the tile sums into the prefix
 // P_i = Gam_0 + ... + Gam_{i-1} in place.
 constexpr int kScanThreads = 1024;
@@ -726,7 +734,7 @@ lla_tile_gate_sum_kernel(const float *__restrict__ g, double *__restrict__ P, fl
     }
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         Pb[0] = 0.0;
-        if (bh == 0) *err = 0;
+        if (bh == 0 && err != nullptr) *err = 0;
     }
 }
 
@@ -836,6 +844,10 @@ static cudaError_t launch_consumer(const CUtensorMap &mq, const CUtensorMap &mk,
     return cudaLaunchKernelEx(&cfg, lla_readout_consumer_kernel<OutT>, mq, mk, mv, mn, mo, prm);
 }
 
+static std::atomic<int> g_withhold_first_product{0};
+
+void tc_set_withhold_first_product(int enable) { g_withhold_first_product.store(enable ? 1 : 0); }
+
 cudaError_t tc_fwd(const TcFwdArgs &A)
 {
     const int BH = A.B * A.H, NT = (A.T + kTile - 1) / kTile;
@@ -845,7 +857,8 @@ cudaError_t tc_fwd(const TcFwdArgs &A)
     prm.lam = A.lam;
     prm.out = A.out;
     prm.P = (const double *)ws;
-    prm.err = (int *)(ws + off_err(BH, NT));
+    int *const ws_err = (int *)(ws + off_err(BH, NT));
+    prm.err = A.device_error ? (int *)A.device_error : ws_err;
     prm.gamma = (float *)(ws + off_gamma(BH, NT));
     prm.segtot = (float *)(ws + off_segtot(BH, NT));
     prm.node16 = (__nv_bfloat16 *)(ws + off_node16(BH, NT));
@@ -854,6 +867,8 @@ cudaError_t tc_fwd(const TcFwdArgs &A)
     prm.BH = BH;
     prm.L = A.L;
     prm.nseg_full = nseg_full_of(NT);
+    prm.withhold = g_withhold_first_product.load();
+    prm.wait_iters = prm.withhold ? kWithheldWaitIters : kWaitIters;
     CUtensorMap mq, mk, mv, mn, mo;
     const bool out32 = A.out_dt == LLA_F32;
     if (!make_map_bf16_3d(&mq, A.q, kD, A.T, BH, 64, kTile) ||
@@ -865,7 +880,8 @@ cudaError_t tc_fwd(const TcFwdArgs &A)
         return cudaErrorInvalidValue;
     cudaStream_t st = (cudaStream_t)A.stream;
     lla_tile_gate_sum_kernel<<<dim3((NT + 31) / 32, BH), 1024, 0, st>>>(A.g, (double *)prm.P, prm.gamma,
-                                                                          prm.err, A.T, NT);
+                                                                          A.device_error ? nullptr : ws_err,
+                                                                          A.T, NT);
     lla_tile_gate_scan_kernel<<<BH, kScanThreads, 0, st>>>((double *)prm.P, NT);
     cudaError_t e;
     if (NT > 1) {

@@ -14,6 +14,7 @@ struct TcFwdArgs {
     int B, H, T, L;
     lla_dtype out_dt;
     void *workspace;
+    int32_t *device_error;  // caller's word, or nullptr (the workspace word is used)
     void *stream;
 };
 
@@ -22,5 +23,7 @@ size_t tc_workspace_bytes(int B, int H, int T);
 size_t tc_smem_bytes();
 int tc_launches(int T);
 cudaError_t tc_fwd(const TcFwdArgs &A);
+// Test hook: withhold each tile's first product and shorten the waits.
+void tc_set_withhold_first_product(int enable);
 
 }  // namespace lla

@@ -164,8 +164,9 @@ constexpr uint32_t kTcWait = 1u << 22;
 
 using namespace sm100;
 
-// Sticky record of a bounded wait that gave up (1: load, 2: product); the
-// kernel carries on, so the results of that call are not to be trusted.
+// Sticky record of a bounded wait that gave up (1: load, 2: product) for
+// calls that pass no device_error word; the kernel carries on, so the
+// results of that call are not to be trusted.
 __device__ int lla_lambda_tc_wait_err;
 
 __host__ __device__ constexpr int tc_tmem_cols(int NP) { return NP <= 16 ? 32 : NP <= 32 ? 64 : 128; }
@@ -194,9 +195,9 @@ template <int NP>
 __global__ void __launch_bounds__(kTcThreads, 1)
 lambda_tc_kernel(const __grid_constant__ CUtensorMap map_d, const float *__restrict__ W1,
                  const float *__restrict__ W2, const float *__restrict__ bias, float *__restrict__ lam,
-                 long long N, int Dd, int L)
+                 long long N, int Dd, int L, int *err)
 {
-    int *err = &lla_lambda_tc_wait_err;
+    if (err == nullptr) err = &lla_lambda_tc_wait_err;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const TcLayout lay = tc_layout(Dd, NP, L);
@@ -337,7 +338,8 @@ cudaError_t launch_tc_np(const LambdaMlpArgs &A)
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
     const long long ntiles = (N + kTcRows - 1) / kTcRows;
     const int grid = (int)(ntiles < nsm ? ntiles : nsm);
-    kern<<<grid, kTcThreads, smem, (cudaStream_t)A.stream>>>(md, A.W1, A.W2, A.bias, A.lam, N, A.Dd, A.L);
+    kern<<<grid, kTcThreads, smem, (cudaStream_t)A.stream>>>(md, A.W1, A.W2, A.bias, A.lam, N, A.Dd, A.L,
+                                                          (int *)A.device_error);
     return cudaPeekAtLastError();
 }
 

@@ -11,6 +11,7 @@ struct LambdaMlpArgs {
     float *lam;
     int B, H, T, Dd, L;
     lla_dtype in_dt;
+    int32_t *device_error;  // caller's word, or nullptr (a library word is used)
     void *stream;
 };
 

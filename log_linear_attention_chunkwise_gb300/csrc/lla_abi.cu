@@ -30,6 +30,36 @@ lla_status fwd_shape_status(int B, int H, int T, int dk, int dv, int chunk, lla_
     return LLA_OK;
 }
 
+}  // namespace
+
+namespace lla {
+
+// Every check lla_fwd makes before it looks at the workspace: shape and
+// dtype, the empty case (LLA_OK with *empty set), pointers and alignment.
+lla_status fwd_args_status(const void *q, const void *k, const void *v, const float *g,
+                           const float *lambda, const void *out, int B, int H, int T, int dk,
+                           int dv, int chunk, lla_dtype in_dt, lla_dtype out_dt, bool *empty)
+{
+    *empty = false;
+    lla_status st = fwd_shape_status(B, H, T, dk, dv, chunk, in_dt);
+    if (st != LLA_OK) return st;
+    if (out_dt != LLA_F32 && out_dt != LLA_BF16) return LLA_ERR_INVALID_ARGUMENT;
+    if (in_dt == LLA_F32 && out_dt != LLA_F32) return LLA_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)B * H * T == 0) {
+        *empty = true;
+        return LLA_OK;
+    }
+    if (!q || !k || !v || !g || !lambda || !out) return LLA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(lambda) ||
+        !aligned16(out))
+        return LLA_ERR_INVALID_ARGUMENT;
+    return LLA_OK;
+}
+
+}  // namespace lla
+
+namespace {
+
 SimtFwdArgs simt_args(const void *q, const void *k, const void *v, const float *g,
                       const float *lambda, void *out, int B, int H, int T, int dk, int dv,
                       int chunk, lla_dtype in_dt, lla_dtype out_dt, void *ws, void *stream)
@@ -88,20 +118,29 @@ int lla_fwd_launches(int B, int H, int T, int dk, int dv, int chunk, lla_dtype i
     return T / chunk > 1 ? 4 : 3;
 }
 
+lla_status lla_device_error_check(const int32_t *device_error, int32_t *code, void *stream)
+{
+    if (device_error == nullptr) return LLA_ERR_INVALID_ARGUMENT;
+    int32_t h = 0;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaMemcpyAsync(&h, device_error, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return LLA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return LLA_ERR_CUDA;
+    if (code) *code = h;
+    return h == 0 ? LLA_OK : LLA_ERR_DEVICE_REPORTED;
+}
+
+void lla_debug_withhold_first_product(int enable) { lla::tc_set_withhold_first_product(enable); }
+
 lla_status lla_fwd(const void *q, const void *k, const void *v, const float *g,
                    const float *lambda, void *out, int B, int H, int T, int dk, int dv,
                    int chunk, lla_dtype in_dt, lla_dtype out_dt, void *workspace,
-                   size_t workspace_bytes, void *stream)
+                   size_t workspace_bytes, int32_t *device_error, void *stream)
 {
-    lla_status st = fwd_shape_status(B, H, T, dk, dv, chunk, in_dt);
-    if (st != LLA_OK) return st;
-    if (out_dt != LLA_F32 && out_dt != LLA_BF16) return LLA_ERR_INVALID_ARGUMENT;
-    if (in_dt == LLA_F32 && out_dt != LLA_F32) return LLA_ERR_UNSUPPORTED_SHAPE;
-    if ((long long)B * H * T == 0) return LLA_OK;
-    if (!q || !k || !v || !g || !lambda || !out) return LLA_ERR_INVALID_ARGUMENT;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(lambda) ||
-        !aligned16(out))
-        return LLA_ERR_INVALID_ARGUMENT;
+    bool empty = false;
+    lla_status st = fwd_args_status(q, k, v, g, lambda, out, B, H, T, dk, dv, chunk, in_dt,
+                                    out_dt, &empty);
+    if (st != LLA_OK || empty) return st;
     const size_t need = lla_fwd_workspace_bytes(B, H, T, dk, dv, chunk, in_dt);
     if (workspace_bytes < need) return LLA_ERR_WORKSPACE_TOO_SMALL;
     if (need > 0 && (workspace == nullptr || ((uintptr_t)workspace & 255u) != 0))
@@ -110,7 +149,7 @@ lla_status lla_fwd(const void *q, const void *k, const void *v, const float *g,
         TcFwdArgs A;
         A.q = q; A.k = k; A.v = v; A.g = g; A.lam = lambda; A.out = out;
         A.B = B; A.H = H; A.T = T; A.L = lla_num_levels(T); A.out_dt = out_dt;
-        A.workspace = workspace; A.stream = stream;
+        A.workspace = workspace; A.device_error = device_error; A.stream = stream;
         return tc_fwd(A) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
     }
     SimtFwdArgs A = simt_args(q, k, v, g, lambda, out, B, H, T, dk, dv, chunk, in_dt, out_dt,
@@ -156,7 +195,7 @@ size_t lla_prefill_workspace_bytes(int B, int H, int T)
 lla_status lla_prefill_state(const void *k, const void *v, const float *g, float *state_levels,
                              float *state_logdecay, int B, int H, int T, int dk, int dv, int Ls,
                              lla_dtype in_dt, void *workspace, size_t workspace_bytes,
-                             void *stream)
+                             int32_t *device_error, void *stream)
 {
     if (B < 0 || H < 0 || T < 0) return LLA_ERR_INVALID_ARGUMENT;
     if (in_dt != LLA_F32 && in_dt != LLA_BF16) return LLA_ERR_INVALID_ARGUMENT;
@@ -172,13 +211,13 @@ lla_status lla_prefill_state(const void *k, const void *v, const float *g, float
     PrefillArgs A;
     A.k = k; A.v = v; A.g = g; A.S = state_levels; A.D = state_logdecay;
     A.B = B; A.H = H; A.T = T; A.dk = dk; A.dv = dv; A.Ls = Ls; A.in_dt = in_dt;
-    A.workspace = workspace; A.stream = stream;
+    A.workspace = workspace; A.device_error = device_error; A.stream = stream;
     return prefill_state(A) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
 }
 
 lla_status lla_lambda_mlp(const void *d, const float *W1, const float *W2, const float *b,
                           float *lambda, int B, int H, int T, int Dd, int L, lla_dtype in_dt,
-                          void *stream)
+                          int32_t *device_error, void *stream)
 {
     if (B < 0 || H < 0 || T < 0) return LLA_ERR_INVALID_ARGUMENT;
     if (in_dt != LLA_F32 && in_dt != LLA_BF16) return LLA_ERR_INVALID_ARGUMENT;
@@ -188,7 +227,8 @@ lla_status lla_lambda_mlp(const void *d, const float *W1, const float *W2, const
     if (!d || !W1 || !W2 || !b || !lambda) return LLA_ERR_INVALID_ARGUMENT;
     LambdaMlpArgs A;
     A.d = d; A.W1 = W1; A.W2 = W2; A.bias = b; A.lam = lambda;
-    A.B = B; A.H = H; A.T = T; A.Dd = Dd; A.L = L; A.in_dt = in_dt; A.stream = stream;
+    A.B = B; A.H = H; A.T = T; A.Dd = Dd; A.L = L; A.in_dt = in_dt;
+    A.device_error = device_error; A.stream = stream;
     return lambda_mlp(A) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
 }
 
@@ -205,7 +245,7 @@ size_t lla_bwd_workspace_bytes(int B, int H, int T, int dk, int dv, int chunk, l
 lla_status lla_bwd(const void *q, const void *k, const void *v, const float *g, const float *lambda,
                    const float *dout, float *dq, float *dk, float *dv, float *dg, float *dlambda,
                    int B, int H, int T, int dk_dim, int dv_dim, int chunk, lla_dtype in_dt,
-                   void *workspace, size_t workspace_bytes, void *stream)
+                   void *workspace, size_t workspace_bytes, int32_t *device_error, void *stream)
 {
     lla_status st = fwd_shape_status(B, H, T, dk_dim, dv_dim, chunk, in_dt);
     if (st != LLA_OK) return st;
@@ -221,7 +261,7 @@ lla_status lla_bwd(const void *q, const void *k, const void *v, const float *g, 
     if (lla::bwd_smem_bytes(A) > 227 * 1024) return LLA_ERR_UNSUPPORTED_SHAPE;
     A.q = q; A.k = k; A.v = v; A.g = g; A.lam = lambda; A.dout = dout;
     A.dq = dq; A.dkey = dk; A.dval = dv; A.dg = dg; A.dlam = dlambda;
-    A.workspace = workspace; A.stream = stream;
+    A.workspace = workspace; A.device_error = device_error; A.stream = stream;
     return lla::bwd(A) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
 }
 

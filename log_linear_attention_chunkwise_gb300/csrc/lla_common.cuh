@@ -74,4 +74,10 @@ __host__ __device__ __forceinline__ size_t align_up(size_t x, size_t a)
     return (x + a - 1) / a * a;
 }
 
+// lla_fwd's checks before the workspace (shape, dtypes, the empty case,
+// pointers, alignment); *empty is set for a valid B*H*T == 0 call.
+lla_status fwd_args_status(const void *q, const void *k, const void *v, const float *g,
+                           const float *lambda, const void *out, int B, int H, int T, int dk,
+                           int dv, int chunk, lla_dtype in_dt, lla_dtype out_dt, bool *empty);
+
 }  // namespace lla

@@ -18,6 +18,10 @@ bound cannot hold for outputs of arbitrary magnitude.
 import numpy as np
 import torch
 
+# (what, max_abs, rel_fro, max |oracle|, stress) of every comparison made in
+# this process; conftest prints them at the end of the run
+RECORDS = []
+
 BF16_MAX_ABS = 2e-2
 BF16_REL_FRO = 5e-3
 F32_REL_FRO = 1e-4
@@ -38,6 +42,7 @@ def errors(gpu, ref):
 
 def assert_parity(gpu, ref, in_dtype, what="", stress=False):
     max_abs, rel_fro, ref_max = errors(gpu, ref)
+    RECORDS.append((what, max_abs, rel_fro, ref_max, stress, in_dtype == torch.bfloat16))
     if in_dtype == torch.bfloat16:
         amax = max(BF16_MAX_ABS, BF16_REL_FRO * ref_max) if stress else BF16_MAX_ABS
         ok = max_abs <= amax and rel_fro <= BF16_REL_FRO

@@ -61,7 +61,8 @@ NULL = None
 def fwd(lib, B=1, H=1, T=64, dk=64, dv=64, chunk=64, in_dt=1, out_dt=0, ws_bytes=1 << 30,
         ptr=ctypes.c_void_p(256)):
     p = ptr
-    return lib.lla_fwd(p, p, p, p, p, p, B, H, T, dk, dv, chunk, in_dt, out_dt, p, ws_bytes, NULL)
+    return lib.lla_fwd(p, p, p, p, p, p, B, H, T, dk, dv, chunk, in_dt, out_dt, p, ws_bytes, NULL,
+                       NULL)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -94,8 +95,8 @@ def test_decode_validation(lib):
 def test_prefill_validation(lib):
     p = ctypes.c_void_p(256)
     # bit_length(T) must fit in Ls slots
-    assert lib.lla_prefill_state(p, p, p, p, p, 1, 1, 8, 64, 64, 3, 1, p, 1 << 20, NULL) == 2
-    assert lib.lla_prefill_state(p, p, p, p, p, 1, 1, 8, 64, 64, 4, 1, p, 0, NULL) == 3
+    assert lib.lla_prefill_state(p, p, p, p, p, 1, 1, 8, 64, 64, 3, 1, p, 1 << 20, NULL, NULL) == 2
+    assert lib.lla_prefill_state(p, p, p, p, p, 1, 1, 8, 64, 64, 4, 1, p, 0, NULL, NULL) == 3
 
 
 def test_bwd_validation(lib):
@@ -103,7 +104,7 @@ def test_bwd_validation(lib):
 
     def bwd(B=1, T=256, dk=64, chunk=64, dt=1, ws=1 << 30, ptr=p):
         return lib.lla_bwd(ptr, p, p, p, p, p, p, p, p, p, p, B, 1, T, dk, 64, chunk, dt,
-                           p, ws, NULL)
+                           p, ws, NULL, NULL)
     assert bwd(chunk=128) == 2          # the backward takes chunks up to 64
     assert bwd(dk=48) == 2
     assert bwd(T=100) == 2
@@ -139,3 +140,25 @@ def test_gdn_validation(lib):
     assert lib.lla_gdn_fwd_workspace_bytes(0, 3, 130, 32, 16) == 0
     assert lib.lla_gdn_decode_step(p, p, p, p, p, p, p, p, p, 1, 1, 64, 64, 41, 1, NULL, NULL) == 2
     assert lib.lla_gdn_decode_step(NULL, p, p, p, p, p, p, p, p, 1, 1, 64, 64, 17, 1, NULL, NULL) == 1
+
+
+def test_device_error_check_rejects_null(lib):
+    code = ctypes.c_int32(7)
+    assert lib.lla_device_error_check(NULL, ctypes.byref(code), NULL) == 1
+    assert code.value == 7   # untouched: nothing was read
+
+
+def test_noalloc_checks_arguments_in_lla_fwd_order(lib):
+    """A bad call gets the status lla_fwd would give it, whatever its size:
+    shape and pointer errors come before the scratch-size refusal."""
+    p = ctypes.c_void_p(256)
+    big = dict(B=1, H=16, T=32768)
+
+    def noalloc(ptr=p, chunk=64, B=1, H=1, T=64, d=64, in_dt=1, out_dt=0):
+        return lib.lla_fwd_noalloc(ptr, p, p, p, p, p, B, H, T, d, d, chunk, in_dt, out_dt, NULL,
+                                   NULL)
+    assert noalloc(chunk=48, **big) == 2
+    assert noalloc(ptr=ctypes.c_void_p(0), d=128, **big) == 1
+    assert noalloc(ptr=ctypes.c_void_p(8), d=128, **big) == 1
+    assert noalloc(out_dt=9, d=128, **big) == 1
+    assert noalloc(B=0, ptr=ctypes.c_void_p(0)) == 0

@@ -145,7 +145,13 @@ def test_decode_workload_sampled_pairs():
     S_end = S.cpu()
     D_end = D.cpu()
     torch.cuda.synchronize()
-    pairs = [(int(np.argmax(pos0)), 0), (int(np.argmin(pos0)), 5), (7, 11), (33, 15)]
+    # 16 (sequence, head) pairs: the longest and shortest prefixes, then a
+    # seeded draw over the other sequences, every head at least once
+    rng = np.random.default_rng(44)
+    seqs = [int(np.argmax(pos0)), int(np.argmin(pos0))]
+    seqs += [int(b) for b in rng.permutation(Bn) if int(b) not in seqs][:14]
+    pairs = [(b, i % H) for i, b in enumerate(seqs)]
+    assert len(set(pairs)) == 16 and {h for _, h in pairs} == set(range(H))
     for (b, h) in pairs:
         n = int(pos0[b])
         pre = W.make_decode_prefix(cfg, pos0, n, device="cuda", seqs=[b], heads=[h])

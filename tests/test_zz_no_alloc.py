@@ -29,7 +29,7 @@ def noalloc_fwd(lib, x, chunk, out):
     in_dt = binding.LLA_BF16 if x["q"].dtype == torch.bfloat16 else binding.LLA_F32
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     return lib.lla_fwd_noalloc(_p(x["q"]), _p(x["k"]), _p(x["v"]), _p(x["g"]), _p(x["lam"]),
-                               _p(out), B, H, T, dk, dv, chunk, in_dt, binding.LLA_F32, stream)
+                               _p(out), B, H, T, dk, dv, chunk, in_dt, binding.LLA_F32, None, stream)
 
 
 @pytest.mark.parametrize("B,H,T,d,chunk,dtype", [
@@ -57,8 +57,16 @@ def test_noalloc_refuses_more_than_its_scratch():
     limit = lib.lla_fwd_noalloc_max_scratch_bytes()
     assert limit == 64 << 20
     # 16 heads x 32768 tokens at d = 128 needs far more than 64 MiB
-    assert lib.lla_fwd_workspace_bytes(1, 16, 32768, 128, 128, 64, 1) > limit
-    null = ctypes.c_void_p(256)
-    rc = lib.lla_fwd_noalloc(null, null, null, null, null, null, 1, 16, 32768, 128, 128, 64, 1, 0,
-                             None)
-    assert rc == 3  # LLA_ERR_WORKSPACE_TOO_SMALL, nothing enqueued
+    B, H, T, d = 1, 16, 32768, 128
+    assert lib.lla_fwd_workspace_bytes(B, H, T, d, d, 64, 1) > limit
+    # real, aligned device buffers, so only the scratch size can be refused
+    q = torch.zeros((B, H, T, d), dtype=torch.bfloat16, device="cuda")
+    g = torch.zeros((B, H, T), dtype=torch.float32, device="cuda")
+    lam = torch.zeros((B, H, T, lib.lla_num_levels(T)), dtype=torch.float32, device="cuda")
+    out = torch.full((B, H, T, d), 7.0, dtype=torch.float32, device="cuda")
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    rc = lib.lla_fwd_noalloc(_p(q), _p(q), _p(q), _p(g), _p(lam), _p(out), B, H, T, d, d, 64, 1, 0,
+                             None, stream)
+    assert rc == 3  # LLA_ERR_WORKSPACE_TOO_SMALL
+    torch.cuda.synchronize()
+    assert bool((out == 7.0).all())  # nothing was enqueued
