@@ -93,9 +93,9 @@ lla_status lla_device_error_check(const int32_t *device_error, int32_t *code, vo
  * While enabled (nonzero), every tensor-core forward launch withholds the
  * first product of each tile (the intra-tile Q K^T: neither the product nor
  * its completion signal is issued, so no copy or product is left in flight)
- * and bounds its waits at a few thousand polls: the waits on that product
- * run out, LLA_DEVERR_SYNC_TIMEOUT is recorded and the launch finishes with
- * an invalid output.  Process-wide; 0 restores normal operation. */
+ * and bounds the waits on that product at a few thousand polls: they run
+ * out, LLA_DEVERR_SYNC_TIMEOUT is recorded and the launch finishes with an
+ * invalid output.  Process-wide; 0 restores normal operation. */
 void lla_debug_withhold_first_product(int enable);
 
 /* L = 1 + bit_length(T-1): lambda entries per token for a length-T forward

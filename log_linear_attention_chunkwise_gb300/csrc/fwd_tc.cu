@@ -64,6 +64,7 @@ struct TcParams {
     __nv_bfloat16 *node16;  // [BH][NT][128][128] Fenwick nodes (index 0 unused)
     int T, NT, BH, L, nseg_full;
     uint32_t wait_iters;    // polls before a wait gives up
+    uint32_t s_wait_iters;  // the same for the waits on S = Q K^T (short while it is withheld)
     int withhold;           // test hook: the consumer issues no S = Q K^T and no signal for it
 };
 
@@ -490,7 +491,7 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
             // path nodes in order: jn[n] computed on the fly
             int jnext = i;
             if (npath > 0) {
-                if (!mbar_wait(&s.bar_s, 0, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
+                if (!mbar_wait(&s.bar_s, 0, prm.s_wait_iters)) set_err(prm.err, kErrMmaTimeout);
                 // the nodes come from the previous launches; everything before this
                 // point reads only inputs and the gate sums
                 grid_dependency_wait();
@@ -543,7 +544,7 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
     } else {
         // ---------------- epilogue warps
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-        if (!mbar_wait(&s.bar_s, 0, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
+        if (!mbar_wait(&s.bar_s, 0, prm.s_wait_iters)) set_err(prm.err, kErrMmaTimeout);
         tc_fence_after_sync();
         // P = S . M  (thread = query row, 64 keys), packed bf16 pairs in registers
         uint32_t pk[32];
@@ -868,7 +869,8 @@ cudaError_t tc_fwd(const TcFwdArgs &A)
     prm.L = A.L;
     prm.nseg_full = nseg_full_of(NT);
     prm.withhold = g_withhold_first_product.load();
-    prm.wait_iters = prm.withhold ? kWithheldWaitIters : kWaitIters;
+    prm.wait_iters = kWaitIters;
+    prm.s_wait_iters = prm.withhold ? kWithheldWaitIters : kWaitIters;
     CUtensorMap mq, mk, mv, mn, mo;
     const bool out32 = A.out_dt == LLA_F32;
     if (!make_map_bf16_3d(&mq, A.q, kD, A.T, BH, 64, kTile) ||
