@@ -1,5 +1,5 @@
 // Chunked forward on the 5th-generation tensor cores (tcgen05, TMEM, TMA),
-// bf16 q/k/v with fp32 accumulation, dk = dv = 128.
+// bf16 q/k/v with fp32 accumulation, dk = dv = D for D = 64 or 128.
 //
 // Page "Log-Linear Attention" (gist.science 2506.04761), technical summary
 // §2.2 (Fenwick buckets of [0,t), one state per bucket, lambda-weighted
@@ -9,11 +9,12 @@
 // walkers (one CTA per head, dv slice and segment of tiles, walking in order
 // with the Fenwick stack in tensor memory) compute each tile's state and
 // publish the tile-level Fenwick nodes; a fix-up kernel chains the nodes that
-// span segments.  The read-out consumer (one CTA per tile, no waits: every
-// node exists when it starts) forms the masked intra-tile product and the
-// lambda-weighted read-out of the nodes.  With Gam_i the gate sum
-// of tile i and P_i = Gam_0 + ... + Gam_{i-1} (fp64, from the prefix kernels),
-// the earlier tiles of tile i form the tile-level Fenwick buckets ending at
+// span segments.  The read-out consumer (persistent: one CTA per SM taking
+// tiles from a queue, the next tile's inputs loading while the current one
+// computes) forms the masked intra-tile product and the lambda-weighted
+// read-out of the nodes.  With Gam_i the gate sum of tile i and
+// P_i = Gam_0 + ... + Gam_{i-1} (fp64, from the prefix kernels), the earlier
+// tiles of tile i form the tile-level Fenwick buckets ending at
 // j = i, i - lowbit(i), ...; bucket j (level m = ctz(j)) holds the tiles
 // [j - 2^m, j) decayed to the end of tile j-1:
 //     Node_j = sum over those tiles' keys s of exp(P_j - G_s) k_s v_s^T.
@@ -25,10 +26,11 @@
 //        j_m = i + 1 - 2^m, published to global memory in bf16
 //   P  = S . M,  M[a][b] = lambda_a[bit_length(a^b)] exp(gamma_a - gamma_b), b <= a
 //   O  = P V + sum_{path j} diag(lambda_.[8+m] exp(gamma_. + P_i - P_j)) (Q Node_j)
-// Every product above is a tcgen05 MMA of M = N = 128, bf16 operands in
-// 128-byte-swizzled shared memory, fp32 accumulators in tensor memory.  The
-// read-out forms U_j = Q Node_j per path node in tensor memory and applies
-// the per-row weights in fp32 while draining it.
+// Every product above is a tcgen05 MMA of M = 128 (tokens, or dk padded to
+// 128 rows for D = 64), bf16 operands in 128-byte-swizzled shared memory,
+// fp32 accumulators in tensor memory.  The read-out forms U_j = Q Node_j per
+// path node in tensor memory and applies the per-row weights in fp32 while
+// draining it.
 #include <atomic>
 
 #include "fwd_tc.cuh"
@@ -41,14 +43,12 @@ namespace {
 using namespace sm100;
 
 constexpr int kTile = 128;       // tokens per tile (MMA M)
-constexpr int kD = 128;          // dk = dv
 constexpr int kTileLevels = 7;   // levels inside a tile: bit_length(a ^ b) <= 7
-constexpr uint32_t kBuf = kTile * kD * 2;  // one bf16 128x128 operand: 32 KB
-constexpr uint32_t kHalf = kBuf / 2;       // one 64-column swizzled block
+constexpr uint32_t kBlk = kTile * 128;  // one 64-column swizzled block of a 128-row bf16 tile: 16 KB
 constexpr uint32_t kWaitIters = 1u << 22;  // bounded waits (~0.5 s with back-off)
 constexpr uint32_t kWithheldWaitIters = 4096;  // the waits while the test hook withholds a product
-constexpr int kLamLd = 9;                  // padded row of the in-tile lambdas
 constexpr int kMaxPath = 17;               // levels of a tile index (T <= 2^24, so NT <= 2^17)
+constexpr int kLamMax = 25;                // lambda entries per token: L <= 1 + bit_length(2^24 - 1)
 
 // Error codes (lla_device_error) written to the error word.
 constexpr int kErrLoadTimeout = LLA_DEVERR_COPY_TIMEOUT;
@@ -58,10 +58,11 @@ struct TcParams {
     const float *g, *lam;
     void *out;
     const double *P;        // [BH][NT+1] tile-gate prefix sums
-    float *gamma;           // [BH][T] inclusive gate sum inside each tile (fp32)
+    float *gamma;           // [BH][NT][128] inclusive gate sum inside each tile (fp32)
     int *err;               // first bounded wait that gave up (0: none): the caller's word or the workspace's
-    float *segtot;          // [BH][nseg_full][128][128] decayed segment totals
-    __nv_bfloat16 *node16;  // [BH][NT][128][128] Fenwick nodes (index 0 unused)
+    int *queue;             // next work item of the read-out consumer (reset to 0 by the gate-sum kernel)
+    float *segtot;          // [BH][nseg_full][D][D] decayed segment totals
+    __nv_bfloat16 *node16;  // [BH][NT][D][D] Fenwick nodes (index 0 unused)
     int T, NT, BH, L, nseg_full;
     uint32_t wait_iters;    // polls before a wait gives up
     uint32_t s_wait_iters;  // the same for the waits on S = Q K^T (short while it is withheld)
@@ -70,32 +71,35 @@ struct TcParams {
 
 __device__ __forceinline__ void set_err(int *err, int code) { atomicCAS(err, 0, code); }
 
-// 8 MMAs over K = 128: A and B K-major (rows of 128 B, K split in two blocks).
+// MMAs over K = D with A and B K-major (rows of 128 B, K split in 64-column blocks).
+template <int D>
 __device__ __forceinline__ void mma_kk(uint32_t d, const uint8_t *a, const uint8_t *b, uint32_t idesc)
 {
 #pragma unroll
-    for (int kk = 0; kk < 8; kk++) {
-        const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+    for (int kk = 0; kk < D / 16; kk++) {
+        const uint32_t off = (kk >> 2) * kBlk + (kk & 3) * 32;
         umma_bf16(d, desc_sw128(smem_u32(a) + off, 16, 1024), desc_sw128(smem_u32(b) + off, 16, 1024),
                   idesc, kk > 0 ? 1u : 0u);
     }
 }
 
-// 8 MMAs over K = 128 with A K-major and B MN-major (rows = K index).
+// MMAs over K = D with A K-major and B MN-major (rows = K index, N in
+// 64-column blocks of D rows each).
+template <int D>
 __device__ __forceinline__ void mma_kmn(uint32_t d, const uint8_t *a, const uint8_t *b, uint32_t idesc)
 {
 #pragma unroll
-    for (int kk = 0; kk < 8; kk++) {
-        const uint32_t offa = (kk >> 2) * kHalf + (kk & 3) * 32;
+    for (int kk = 0; kk < D / 16; kk++) {
+        const uint32_t offa = (kk >> 2) * kBlk + (kk & 3) * 32;
         const uint32_t offb = kk * 2048;
         umma_bf16(d, desc_sw128(smem_u32(a) + offa, 16, 1024),
-                  desc_sw128(smem_u32(b) + offb, kHalf, 1024), idesc, kk > 0 ? 1u : 0u);
+                  desc_sw128(smem_u32(b) + offb, (uint32_t)D * 128, 1024), idesc, kk > 0 ? 1u : 0u);
     }
 }
 
 // ======================================================= node walkers
 // The tile-level Fenwick nodes Node_j (j = 1 .. NT-1) are built by walkers:
-// one CTA per (batch*head, 32-column slice of dv, segment of 64 tiles) goes
+// one CTA per (batch*head, 32-column slice of dv, segment of 32 tiles) goes
 // through its segment in order.  For tile i it forms H_i's slice on the
 // tensor cores and closes Node_{i+1}:
 //     Node_{i+1} = H_i + sum_{m < ctz(i+1)} exp(P_{i+1} - P_{i+1-2^m}) Node_{i+1-2^m},
@@ -104,9 +108,11 @@ __device__ __forceinline__ void mma_kmn(uint32_t d, const uint8_t *a, const uint
 // that closes a full segment reaches back before the segment; the walker
 // writes that segment's decayed total instead, and the fix-up kernel chains
 // the totals at segment granularity.  Nodes are published in bf16, the
-// read-out's MMA operand.
+// read-out's MMA operand.  For D = 64 the product's M (= dk) is padded to
+// 128: the second 64-row block of the K^T operand reads whatever shared
+// memory follows the tile, and those rows of H are never read.
 
-// fp32 128x128 tile staged as four 32-column boxes of 128 rows x 128 B:
+// fp32 tile of 128 rows staged as 32-column boxes of 128 rows x 128 B:
 // byte offset of the 4-float chunk holding columns [4c, 4c+4) of row r.
 __device__ __forceinline__ uint32_t f32_stage_off(int r, int c)
 {
@@ -114,17 +120,17 @@ __device__ __forceinline__ uint32_t f32_stage_off(int r, int c)
 }
 
 constexpr int kSliceW = 32;              // dv columns per walker
-constexpr int kSlices = kD / kSliceW;
 constexpr int kSegLog = 5;
 constexpr int kSeg = 1 << kSegLog;       // tiles per segment
 constexpr int kWalkStages = 2;           // K/V tiles in flight per walker (2 walkers per SM)
 constexpr int kWalkThreads = 256;        // warps 0-3: node epilogue; warps 4-7: tile preparation
 
+template <int D>
 struct __align__(1024) WalkSmem {
-    uint8_t k[kWalkStages][kBuf];   // K tiles
-    uint8_t v[kWalkStages][kHalf];  // the 64-column V block holding the slice
-    float gm[kWalkStages][kTile];   // the tile's inclusive gate sums gamma
-    double P[kSeg + 1];             // P_{i0} .. P_{i0+kSeg}
+    uint8_t k[kWalkStages][kTile * D * 2];  // K tiles
+    uint8_t v[kWalkStages][kBlk];           // the 64-column V block holding the slice
+    float gm[kWalkStages][kTile];           // the tile's inclusive gate sums gamma
+    double P[kSeg + 1];                     // P_{i0} .. P_{i0+kSeg}
     uint64_t bar_load[kWalkStages], bar_h[2], bar_hfree[2];
     uint32_t tmem;
 };
@@ -135,13 +141,14 @@ __device__ __forceinline__ void prep_sync() { asm volatile("bar.sync 1, 128;" ::
 // scale the V slice by exp(Gam - gamma) and issue the state product of tile
 // n while the epilogue warps (thread = dk row) fold tile n-1's state into
 // the Fenwick stack; TMA keeps kWalkStages tiles in flight.
+template <int D>
 __global__ void __launch_bounds__(kWalkThreads, 2)
 lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                        const TcParams prm)
 {
     extern __shared__ uint8_t smem_raw[];
-    WalkSmem &s = *reinterpret_cast<WalkSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~uintptr_t(1023));
+    WalkSmem<D> &s = *reinterpret_cast<WalkSmem<D> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                      ~uintptr_t(1023));
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int seg = blockIdx.x, slice = blockIdx.y, bh = blockIdx.z;
@@ -157,7 +164,7 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
         for (int b = 0; b < kWalkStages; b++) mbar_init(&s.bar_load[b], 1);
         for (int b = 0; b < 2; b++) {
             mbar_init(&s.bar_h[b], 1);
-            mbar_init(&s.bar_hfree[b], 128);
+            mbar_init(&s.bar_hfree[b], D);
         }
         fence_mbar_init();
         tma_prefetch_map(&map_k);
@@ -178,9 +185,9 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
     // a tile's 128 gamma values are one aligned 512-byte run
     auto issue_load = [&](int n) {
         const int ls = n % kWalkStages, i = i0 + n;
-        mbar_arrive_expect_tx(&s.bar_load[ls], kBuf + kHalf + kTile * 4);
-        tma_load_3d(s.k[ls], &map_k, &s.bar_load[ls], 0, i * kTile, bh);
-        tma_load_3d(s.k[ls] + kHalf, &map_k, &s.bar_load[ls], 64, i * kTile, bh);
+        mbar_arrive_expect_tx(&s.bar_load[ls], kTile * D * 2 + kBlk + kTile * 4);
+#pragma unroll
+        for (int h = 0; h < D / 64; h++) tma_load_3d(s.k[ls] + h * kBlk, &map_k, &s.bar_load[ls], h * 64, i * kTile, bh);
         tma_load_3d(s.v[ls], &map_v, &s.bar_load[ls], vblk * 64, i * kTile, bh);
         bulk_load(s.gm[ls], prm.gamma + ((long long)bh * NT + i) * kTile, kTile * 4, &s.bar_load[ls]);
     };
@@ -221,19 +228,19 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
                 if (n >= 2 && !mbar_wait(&s.bar_hfree[hb], ((n - 2) >> 1) & 1, prm.wait_iters))
                     set_err(prm.err, kErrMmaTimeout);
                 tc_fence_after_sync();
-                // H slice = K^T Vs: A = K^T (M = dk, MN-major), B = Vs slice (N = 32, MN-major)
+                // H slice = K^T Vs: A = K^T (M = 128 >= dk, MN-major), B = Vs slice (N = 32, MN-major)
                 const uint32_t idesc = idesc_bf16_f32(128, kSliceW, true, true);
 #pragma unroll
                 for (int kk = 0; kk < 8; kk++) {
                     const uint32_t off = kk * 2048;
-                    umma_bf16(tm_h0 + hb * kSliceW, desc_sw128(smem_u32(s.k[ls]) + off, kHalf, 1024),
-                              desc_sw128(smem_u32(s.v[ls]) + voff + off, kHalf, 1024), idesc,
+                    umma_bf16(tm_h0 + hb * kSliceW, desc_sw128(smem_u32(s.k[ls]) + off, kBlk, 1024),
+                              desc_sw128(smem_u32(s.v[ls]) + voff + off, kBlk, 1024), idesc,
                               kk > 0 ? 1u : 0u);
                 }
                 umma_commit(&s.bar_h[hb]);
             }
         }
-    } else {
+    } else if (tid < D) {
         // ---------------- epilogue warps: thread = dk row `tid`, the slice's 32 columns
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
         for (int n = 0; n < ntiles; n++) {
@@ -270,13 +277,13 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
                 __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(w);
 #pragma unroll
                 for (int u = 0; u < 16; u++) h[u] = __floats2bfloat162_rn(acc[2 * u], acc[2 * u + 1]);
-                uint4 *dst = reinterpret_cast<uint4 *>(prm.node16 + (((long long)bh * NT + J) * kD + tid) * kD +
+                uint4 *dst = reinterpret_cast<uint4 *>(prm.node16 + (((long long)bh * NT + J) * D + tid) * D +
                                                        slice * kSliceW);
 #pragma unroll
                 for (int u = 0; u < 4; u++) dst[u] = w[u];
             } else {
                 float4 *dst = reinterpret_cast<float4 *>(
-                    prm.segtot + ((((long long)bh * prm.nseg_full + seg) * kD + tid) * kD + slice * kSliceW));
+                    prm.segtot + ((((long long)bh * prm.nseg_full + seg) * D + tid) * D + slice * kSliceW));
 #pragma unroll
                 for (int u = 0; u < 8; u++)
                     dst[u] = make_float4(acc[4 * u], acc[4 * u + 1], acc[4 * u + 2], acc[4 * u + 3]);
@@ -293,8 +300,9 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
 // eight state elements per thread, the open node of each level in
 // registers, the decay factors in shared memory.
 constexpr int kFixThreads = 256;
-constexpr int kFixMaxZ = 12;    // levels of a segment index: (2^24/128)/64 segments < 2^12
-constexpr int kFixMaxSeg = 2048;
+constexpr int kFixMaxZ = 12;    // levels of a segment index: (2^24/128)/32 segments < 2^12
+constexpr int kFixMaxSeg = 4096;
+template <int D>
 __global__ void __launch_bounds__(kFixThreads)
 lla_node_fixup_kernel(const TcParams prm)
 {
@@ -307,7 +315,7 @@ lla_node_fixup_kernel(const TcParams prm)
     for (int u = threadIdx.x; u <= nseg; u += kFixThreads) pseg[u] = Pb[u * kSeg];
     __syncthreads();
     const int e0 = (blockIdx.x * kFixThreads + threadIdx.x) * 8;  // 8 consecutive elements
-    if (e0 >= kD * kD) return;
+    if (e0 >= D * D) return;
     float stack[kFixMaxZ][8];
 #pragma unroll
     for (int k = 0; k < kFixMaxZ; k++)
@@ -315,7 +323,7 @@ lla_node_fixup_kernel(const TcParams prm)
         for (int c = 0; c < 8; c++) stack[k][c] = 0.f;
     for (int u = 1; u <= nseg; u++) {
         const int z = __ffs(u) - 1;
-        const float4 *src = reinterpret_cast<const float4 *>(prm.segtot + ((bh * nseg) + (u - 1)) * (kD * kD) + e0);
+        const float4 *src = reinterpret_cast<const float4 *>(prm.segtot + ((bh * nseg) + (u - 1)) * (D * D) + e0);
         const float4 a = src[0], b = src[1];
         float val[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
@@ -336,367 +344,438 @@ lla_node_fixup_kernel(const TcParams prm)
         __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&w);
 #pragma unroll
         for (int c = 0; c < 4; c++) h[c] = __floats2bfloat162_rn(val[2 * c], val[2 * c + 1]);
-        *reinterpret_cast<uint4 *>(prm.node16 + (bh * NT + (long long)u * kSeg) * (kD * kD) + e0) = w;
+        *reinterpret_cast<uint4 *>(prm.node16 + (bh * NT + (long long)u * kSeg) * (D * D) + e0) = w;
     }
 }
 
 // ======================================================= read-out consumer
-// CTA per tile; every node is published before this kernel starts.  Warps
-// 0-7 (thread = (row, 64 columns)) drain tensor memory; warp 8 issues the
-// TMA loads and the MMAs.  The two hand off through mbarriers only, so a node
-// buffer is refilled as soon as the MMA reading it completes.
+// Persistent: one CTA per SM takes tiles from a queue (a counter in the
+// workspace) in order, last tiles first and tile-major across heads, so
+// co-running tiles share their deep nodes and the nodes written last are
+// still in L2.  Ten warps:
+//   warps 0-7  epilogue (thread = (row, half of the columns)): the mask P,
+//              the drains of P V and of every U = Q Node_j with its fp32
+//              per-row weight, the output staged in shared memory and
+//              written by TMA;
+//   warp 8     producer: takes the next tile and brings its q, k, v, gamma,
+//              lambda and path P values into the free stage (two stages);
+//   warp 9     MMA issuer (one lane): S, P V, the node loads and the U's.
+// Tile n uses stage n & 1 and tensor-memory region n & 1, so the MMAs and
+// loads of tile n+1 proceed while the epilogue drains tile n.  The roles
+// hand off through mbarriers only; the barriers used a variable number of
+// times per tile are waited with running completion counts.
 
-constexpr int kConsThreads = 288;  // 8 epilogue warps + 1 control warp
+constexpr int kConsThreads = 320;  // 8 epilogue warps, a producer warp, an MMA warp
 constexpr int kEpiThreads = 256;
+constexpr int kProdWarp = 8, kMmaWarp = 9;
 
+template <int D>
+struct __align__(1024) ConsStage {
+    uint8_t q[kTile * D * 2];
+    uint8_t k[kTile * D * 2];  // K, then path node 0, 2, ...; with q the fp32 output staging
+    uint8_t v[kTile * D * 2];  // V, then path node 1, 3, ...
+};
+
+template <int D>
 struct __align__(1024) ConsSmem {
-    uint8_t q[kBuf];
-    uint8_t k[kBuf];   // K, then node stage 0, then (with q) the output staging
-    uint8_t v[kBuf];   // V, then node stage 1
-    float gam[kTile];
-    float kf[kTile];              // exp(gamma_e - gamma_b), e = last key of b's 16-key chunk
-    float lam[kTile * kLamLd];
-    float wgt[kMaxPath * kTile];  // read-out weight of each path level per row
-    double pj[kMaxPath + 1];      // P at the path nodes, then P_i
-    uint64_t bar_load, bar_s, bar_pready, bar_pv, bar_pvfree, bar_node[2], bar_u[2], bar_ufree[2];
+    ConsStage<D> st[2];
+    float gam[2][kTile];
+    float lam[2][kTile * kLamMax];  // the tile's lambda rows, [128][L] dense
+    float kf[kTile];                // exp(gamma_e - gamma_b), e = last key of b's 16-key chunk
+    double pj[2][kMaxPath + 1];     // P at the path nodes of the stage's tile, then P_i
+    int item[2];                    // the stage's work item, -1 when the queue is empty
+    uint64_t bar_load[2], bar_sfree[2], bar_tfree[2];
+    uint64_t bar_s, bar_pready, bar_pv, bar_pvfree;
+    uint64_t bar_node[2], bar_u[2], bar_ufree[2];
     uint32_t tmem;
 };
 
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-template <typename OutT>
-__global__ void __launch_bounds__(kConsThreads, 2)
+// Work item w -> tile (i, bh): tile-major, last tiles first.
+__device__ __forceinline__ void item_tile(int w, int NT, int BH, int *i, int *bh)
+{
+    const int rev = NT * BH - 1 - w;
+    *i = rev / BH;
+    *bh = rev - *i * BH;
+}
+
+template <int D, typename OutT>
+__global__ void __launch_bounds__(kConsThreads, 1)
 lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                             const __grid_constant__ CUtensorMap map_v,
                             const __grid_constant__ CUtensorMap map_node,
                             const __grid_constant__ CUtensorMap map_out, const TcParams prm)
 {
+    constexpr uint32_t kT = kTile * D * 2;  // bytes of one bf16 tile
+    constexpr uint32_t kRegion = 128 + D;   // tensor-memory columns per tile: S / P / U even, then P V / U odd
     extern __shared__ uint8_t smem_raw[];
-    ConsSmem &s = *reinterpret_cast<ConsSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~uintptr_t(1023));
+    ConsSmem<D> &s = *reinterpret_cast<ConsSmem<D> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                      ~uintptr_t(1023));
     const int tid = threadIdx.x;
-    const int warp = tid >> 5;
-    const int NT = prm.NT, BH = prm.BH;
-    // tile-major, last tiles first: co-resident tiles share their deep nodes,
-    // and the nodes written last are still in L2
-    const int rev = NT * BH - 1 - (int)blockIdx.x;
-    const int i = rev / BH;
-    const int bh = rev - i * BH;
-    const double *Pb = prm.P + (long long)bh * (NT + 1);
-    int npath = 0;
-    for (int j = i; j > 0; j -= (j & -j)) npath++;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int NT = prm.NT, BH = prm.BH, L = prm.L;
+    const int total = NT * BH;
 
     if (tid == kEpiThreads) {
-        mbar_init(&s.bar_load, 1);
-        mbar_init(&s.bar_s, 1);
-        mbar_init(&s.bar_pready, kEpiThreads);
-        mbar_init(&s.bar_pv, 1);
-        mbar_init(&s.bar_pvfree, kEpiThreads);
         for (int b = 0; b < 2; b++) {
+            mbar_init(&s.bar_load[b], 1);
+            mbar_init(&s.bar_sfree[b], 1);
+            mbar_init(&s.bar_tfree[b], kEpiThreads);
             mbar_init(&s.bar_node[b], 1);
             mbar_init(&s.bar_u[b], 1);
             mbar_init(&s.bar_ufree[b], kEpiThreads);
         }
+        mbar_init(&s.bar_s, 1);
+        mbar_init(&s.bar_pready, kEpiThreads);
+        mbar_init(&s.bar_pv, 1);
+        mbar_init(&s.bar_pvfree, kEpiThreads);
         fence_mbar_init();
         tma_prefetch_map(&map_q);
         tma_prefetch_map(&map_k);
         tma_prefetch_map(&map_v);
         tma_prefetch_map(&map_node);
         tma_prefetch_map(&map_out);
-        mbar_arrive_expect_tx(&s.bar_load, 3 * kBuf);
-#pragma unroll
-        for (int h = 0; h < 2; h++) {
-            tma_load_3d(s.q + h * kHalf, &map_q, &s.bar_load, h * 64, i * kTile, bh);
-            tma_load_3d(s.k + h * kHalf, &map_k, &s.bar_load, h * 64, i * kTile, bh);
-            tma_load_3d(s.v + h * kHalf, &map_v, &s.bar_load, h * 64, i * kTile, bh);
-        }
     }
     if (warp == 0) {
-        tmem_alloc(&s.tmem, 256);
+        tmem_alloc(&s.tmem, 512);
         tmem_relinquish();
-    }
-    const int row = tid & (kTile - 1);
-    const int half = (tid >> 7) & 1;
-    const int tile_rows = min(kTile, prm.T - i * kTile);
-    const bool row_ok = row < tile_rows;
-    const long long tok = (long long)bh * prm.T + (long long)i * kTile + row;
-    const float *lam_row = prm.lam + tok * prm.L;
-    float gam_a = 0.f;
-    if (tid < kEpiThreads) {
-        // every global load first, then the stores that depend on them
-        gam_a = prm.gamma[((long long)bh * NT + i) * kTile + row];
-        float lv[kTileLevels + 1];
-        if (half == 0) {
-#pragma unroll
-            for (int l = 0; l <= kTileLevels; l++) lv[l] = (row_ok && l < prm.L) ? lam_row[l] : 0.f;
-        }
-        // read-out weights: path level n (node j_n, level m_n = ctz(j_n)):
-        //   lambda_a[8 + m_n] * exp(gamma_a + P_i - P_{j_n}); the halves split the levels
-        float lw[kMaxPath];
-        {
-            int j = i;
-#pragma unroll
-            for (int n = 0; n < kMaxPath; n++) {
-                lw[n] = 0.f;
-                if (j > 0) {
-                    if ((n & 1) == half && row_ok) lw[n] = lam_row[kTileLevels + 1 + (__ffs(j) - 1)];
-                    j -= (j & -j);
-                }
-            }
-        }
-        if (tid < npath) {  // P at the path nodes: thread n clears the n lowest set bits of i
-            int j = i;
-            for (int c = 0; c < tid; c++) j -= (j & -j);
-            s.pj[tid] = Pb[j];
-        }
-        if (tid == 0) s.pj[kMaxPath] = Pb[i];
-        if (half == 0) {
-            s.gam[row] = gam_a;
-#pragma unroll
-            for (int l = 0; l <= kTileLevels; l++) s.lam[row * kLamLd + l] = lv[l];
-        }
-        epi_sync();
-        {
-            const double Pi = s.pj[kMaxPath];
-#pragma unroll
-            for (int n = 0; n < kMaxPath; n++)
-                if (n < npath && (n & 1) == half)
-                    s.wgt[n * kTile + row] = lw[n] * __expf(gam_a + (float)(Pi - s.pj[n]));
-        }
-        epi_sync();
-        if (half == 0) s.kf[row] = __expf(s.gam[row | 15] - gam_a);
     }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tm = s.tmem;
-    const uint32_t slot[2] = {tm, tm + 128};
-    uint8_t *const nd[2] = {s.k, s.v};
 
-    if (warp == 8) {
-        // ---------------- control warp (one lane issues)
-        if ((tid & 31) == 0) {
-            auto load_node = [&](int st, int j) {
-                mbar_arrive_expect_tx(&s.bar_node[st], kBuf);
-                tma_load_3d(nd[st], &map_node, &s.bar_node[st], 0, 0, bh * NT + j);
-                tma_load_3d(nd[st] + kHalf, &map_node, &s.bar_node[st], 64, 0, bh * NT + j);
-            };
-            const uint32_t id_kmn = idesc_bf16_f32(128, 128, false, true);
-            if (!mbar_wait(&s.bar_load, 0, prm.wait_iters)) set_err(prm.err, kErrLoadTimeout);
-            tc_fence_after_sync();
-            if (!prm.withhold) {  // withheld: nothing is left in flight, the waits on bar_s run out
-                mma_kk(slot[0], s.q, s.k, idesc_bf16_f32(128, 128, false, false));
-                umma_commit(&s.bar_s);
+    if (warp == kProdWarp) {
+        // ---------------- producer
+        for (int n = 0;; n++) {
+            const int sg = n & 1;
+            if (n >= 2 && lane == 0 && !mbar_wait(&s.bar_sfree[sg], ((n - 2) >> 1) & 1, prm.wait_iters))
+                set_err(prm.err, kErrMmaTimeout);
+            __syncwarp();
+            int w = 0;
+            if (lane == 0) w = atomicAdd(prm.queue, 1);
+            w = __shfl_sync(0xffffffffu, w, 0);
+            if (w >= total) {
+                if (lane == 0) {
+                    s.item[sg] = -1;
+                    mbar_arrive(&s.bar_load[sg]);
+                }
+                break;
             }
-            // path nodes in order: jn[n] computed on the fly
-            int jnext = i;
-            if (npath > 0) {
-                if (!mbar_wait(&s.bar_s, 0, prm.s_wait_iters)) set_err(prm.err, kErrMmaTimeout);
-                // the nodes come from the previous launches; everything before this
-                // point reads only inputs and the gate sums
-                grid_dependency_wait();
-                load_node(0, jnext);  // the K buffer is free once S is done
-                jnext -= (jnext & -jnext);
-            }
-            // O = P V: P from tensor memory once the epilogue has stored it
-            if (!mbar_wait(&s.bar_pready, 0, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
-            tc_fence_after_sync();
+            int i, bh;
+            item_tile(w, NT, BH, &i, &bh);
+            const double *Pb = prm.P + (long long)bh * (NT + 1);
+            // P at the path nodes: lane c clears the c lowest set bits of i
+            int j = i;
+            for (int c = 0; c < lane && j > 0; c++) j -= (j & -j);
+            if (lane < kMaxPath && j > 0) s.pj[sg][lane] = Pb[j];
+            if (lane == 31) s.pj[sg][kMaxPath] = Pb[i];
+            if (lane == 0) s.item[sg] = w;
+            __syncwarp();
+            if (lane == 0) {
+                const int rows = min(kTile, prm.T - i * kTile);
+                const uint32_t lam_bytes = (uint32_t)rows * L * 4;
+                uint64_t *bar = &s.bar_load[sg];
+                mbar_arrive_expect_tx(bar, 3 * kT + lam_bytes + kTile * 4);
+                ConsStage<D> &t = s.st[sg];
 #pragma unroll
-            for (int kk = 0; kk < 8; kk++)
-                umma_bf16_tmem_a(slot[1], slot[0] + kk * 8,
-                                 desc_sw128(smem_u32(s.v) + kk * 2048, kHalf, 1024), id_kmn, kk > 0 ? 1u : 0u);
-            umma_commit(&s.bar_pv);
-            if (npath > 0) {
-                if (!mbar_wait(&s.bar_pv, 0, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
-                if (npath > 1) {
-                    load_node(1, jnext);  // the V buffer is free once P V is done
-                    jnext -= (jnext & -jnext);
+                for (int h = 0; h < D / 64; h++) {
+                    tma_load_3d(t.q + h * kBlk, &map_q, bar, h * 64, i * kTile, bh);
+                    tma_load_3d(t.k + h * kBlk, &map_k, bar, h * 64, i * kTile, bh);
+                    tma_load_3d(t.v + h * kBlk, &map_v, bar, h * 64, i * kTile, bh);
                 }
-                // level 0 into slot 0 (P has been consumed)
-                if (!mbar_wait(&s.bar_node[0], 0, prm.wait_iters)) set_err(prm.err, kErrLoadTimeout);
-                tc_fence_after_sync();
-                mma_kmn(slot[0], s.q, nd[0], id_kmn);
-                umma_commit(&s.bar_u[0]);
+                const long long tok0 = (long long)bh * prm.T + (long long)i * kTile;
+                bulk_load(s.lam[sg], prm.lam + tok0 * L, lam_bytes, bar);
+                bulk_load(s.gam[sg], prm.gamma + ((long long)bh * NT + i) * kTile, kTile * 4, bar);
             }
-            for (int n = 0; n < npath; n++) {
-                const int st = n & 1, st1 = st ^ 1;
-                if (n + 1 < npath) {
-                    // slot st1 is free once level n-1 (or, for level 1, P V) is drained
-                    if (n == 0) {
-                        if (!mbar_wait(&s.bar_pvfree, 0, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
-                    } else {
-                        if (!mbar_wait(&s.bar_ufree[st1], ((n - 1) >> 1) & 1, prm.wait_iters))
-                            set_err(prm.err, kErrMmaTimeout);
-                    }
-                    if (!mbar_wait(&s.bar_node[st1], ((n + 1) >> 1) & 1, prm.wait_iters)) set_err(prm.err, kErrLoadTimeout);
+        }
+    } else if (warp == kMmaWarp) {
+        // ---------------- MMA issuer (one lane)
+        if (lane == 0) {
+            const uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
+            const uint32_t id_kmn = idesc_bf16_f32(128, D, false, true);
+            // parities of the completions so far of bar_node[b] and bar_u[b] (bit b):
+            // only parities are ever waited on
+            uint32_t par_node = 0, par_u = 0;
+            bool dep_done = false;
+            for (int n = 0;; n++) {
+                const int sg = n & 1;
+                if (!mbar_wait(&s.bar_load[sg], (n >> 1) & 1, prm.wait_iters)) set_err(prm.err, kErrLoadTimeout);
+                const int w = s.item[sg];
+                if (w < 0) break;
+                int i, bh;
+                item_tile(w, NT, BH, &i, &bh);
+                const int npath = __popc(i);
+                if (n >= 2 && !mbar_wait(&s.bar_tfree[sg], ((n - 2) >> 1) & 1, prm.wait_iters))
+                    set_err(prm.err, kErrMmaTimeout);
+                tc_fence_after_sync();
+                // slot b at slot0 + 128 b; node buffer b is k (b = 0) or v (b = 1)
+                const uint32_t slot0 = tm + sg * kRegion;
+                ConsStage<D> &t = s.st[sg];
+                auto nd = [&](int b) { return t.k + b * kT; };
+                auto load_node = [&](int b, int jn) {  // a D x D bf16 node, D/64 boxes of 64 columns
+                    mbar_arrive_expect_tx(&s.bar_node[b], (uint32_t)D * D * 2);
+#pragma unroll
+                    for (int h = 0; h < D / 64; h++)
+                        tma_load_3d(nd(b) + h * (D * 128), &map_node, &s.bar_node[b], h * 64, 0, bh * NT + jn);
+                };
+                auto wait_node = [&](int b) {
+                    if (!mbar_wait(&s.bar_node[b], (par_node >> b) & 1, prm.wait_iters))
+                        set_err(prm.err, kErrLoadTimeout);
+                    par_node ^= 1u << b;
+                };
+                auto issue_u = [&](int b) {
                     tc_fence_after_sync();
-                    mma_kmn(slot[st1], s.q, nd[st1], id_kmn);
-                    umma_commit(&s.bar_u[st1]);
+                    mma_kmn<D>(slot0 + 128 * b, t.q, nd(b), id_kmn);
+                    umma_commit(&s.bar_u[b]);
+                    par_u ^= 1u << b;
+                };
+                // parity of the completion of the latest U issued into slot b
+                auto last_u_par = [&](int b) { return ((par_u >> b) & 1) ^ 1; };
+                if (!prm.withhold) {  // withheld: nothing is left in flight, the waits on bar_s run out
+                    mma_kk<D>(slot0, t.q, t.k, id_s);
+                    umma_commit(&s.bar_s);
                 }
-                if (n + 2 < npath) {
-                    // node buffer st is free once level n's product is done
-                    if (!mbar_wait(&s.bar_u[st], (n >> 1) & 1, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
-                    load_node(st, jnext);
+                int jnext = i;
+                if (npath > 0) {
+                    if (!mbar_wait(&s.bar_s, n & 1, prm.s_wait_iters)) set_err(prm.err, kErrMmaTimeout);
+                    if (!dep_done) {
+                        // the nodes come from the previous launches; everything before this
+                        // point reads only inputs and the gate sums
+                        grid_dependency_wait();
+                        dep_done = true;
+                    }
+                    load_node(0, jnext);  // the K buffer is free once S is done
                     jnext -= (jnext & -jnext);
+                }
+                // O = P V: P from tensor memory once the epilogue has stored it
+                if (!mbar_wait(&s.bar_pready, n & 1, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
+                tc_fence_after_sync();
+#pragma unroll
+                for (int kk = 0; kk < 8; kk++)
+                    umma_bf16_tmem_a(slot0 + 128, slot0 + kk * 8, desc_sw128(smem_u32(t.v) + kk * 2048, kBlk, 1024),
+                                     id_kmn, kk > 0 ? 1u : 0u);
+                umma_commit(&s.bar_pv);
+                if (npath > 0) {
+                    if (!mbar_wait(&s.bar_pv, n & 1, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
+                    if (npath > 1) {
+                        load_node(1, jnext);  // the V buffer is free once P V is done
+                        jnext -= (jnext & -jnext);
+                    }
+                    // path node 0 into slot 0 (P has been consumed)
+                    wait_node(0);
+                    issue_u(0);
+                }
+                for (int k = 0; k < npath; k++) {
+                    const int b = k & 1, b1 = b ^ 1;
+                    if (k + 1 < npath) {
+                        // slot b1 is free once U_{k-1} (or, for k = 0, P V) is drained
+                        if (k == 0) {
+                            if (!mbar_wait(&s.bar_pvfree, n & 1, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
+                        } else {
+                            // the drain of U_{k-1}, the latest U in slot b1
+                            if (!mbar_wait(&s.bar_ufree[b1], last_u_par(b1), prm.wait_iters))
+                                set_err(prm.err, kErrMmaTimeout);
+                        }
+                        wait_node(b1);
+                        issue_u(b1);
+                    }
+                    if (k + 2 < npath) {
+                        // node buffer b is free once U_k's product is done
+                        if (!mbar_wait(&s.bar_u[b], last_u_par(b), prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
+                        load_node(b, jnext);
+                        jnext -= (jnext & -jnext);
+                    }
                 }
             }
         }
+        __syncwarp();
     } else {
         // ---------------- epilogue warps
+        const int row = tid & (kTile - 1);
+        const int half = tid >> 7;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-        if (!mbar_wait(&s.bar_s, 0, prm.s_wait_iters)) set_err(prm.err, kErrMmaTimeout);
-        tc_fence_after_sync();
-        // P = S . M  (thread = query row, 64 keys), packed bf16 pairs in registers
-        uint32_t pk[32];
-        {
-            const int a = row;
-            const float *lam_a = s.lam + a * kLamLd;
-#pragma unroll
-            for (int cc = 0; cc < 4; cc += 2) {
-                const int c0 = half * 64 + cc * 16;
-                // the loads are warp-collective: every lane issues them, whatever its row
-                float r2[2][16];
-                tmem_ld16(slot[0] + lane_off + c0, r2[0]);
-                tmem_ld16(slot[0] + lane_off + c0 + 16, r2[1]);
-                tmem_ld_wait();
-#pragma unroll
-                for (int q2 = 0; q2 < 2; q2++) {
-                    const int cb = c0 + q2 * 16;
-                    const float *r = r2[q2];
-                    __nv_bfloat162 h[8];
-                    if (cb > a || !row_ok) {  // strictly above the diagonal, or a row past T
-#pragma unroll
-                        for (int u = 0; u < 8; u++) h[u] = __floats2bfloat162_rn(0.f, 0.f);
-                    } else if (cb + 16 <= a) {
-                        // a whole 16-key chunk below the row: one level, and the decay
-                        // exp(gamma_a - gamma_b) = exp(gamma_a - gamma_e) exp(gamma_e - gamma_b)
-                        // with e = cb + 15, both factors <= 1
-                        const int lev = 32 - __clz(a ^ cb);
-                        const float ra = lam_a[lev] * __expf(gam_a - s.gam[cb + 15]);
-#pragma unroll
-                        for (int u = 0; u < 8; u++)
-                            h[u] = __floats2bfloat162_rn(r[2 * u] * ra * s.kf[cb + 2 * u],
-                                                         r[2 * u + 1] * ra * s.kf[cb + 2 * u + 1]);
-                    } else {
-#pragma unroll
-                        for (int u = 0; u < 8; u++) {
-                            float x[2];
-#pragma unroll
-                            for (int e = 0; e < 2; e++) {
-                                const int b = cb + 2 * u + e;
-                                x[e] = 0.f;
-                                if (b <= a) {
-                                    const int lev = 32 - __clz(a ^ b);
-                                    x[e] = r[2 * u + e] * lam_a[lev] * __expf(gam_a - s.gam[b]);
-                                }
-                            }
-                            h[u] = __floats2bfloat162_rn(x[0], x[1]);
-                        }
-                    }
-#pragma unroll
-                    for (int u = 0; u < 8; u++) pk[(cc + q2) * 8 + u] = *reinterpret_cast<uint32_t *>(&h[u]);
-                }
-            }
-        }
-        // P replaces S in tensor memory (keys 2c, 2c+1 in column c) once every
-        // epilogue thread has read its S columns
-        tc_fence_before_sync();
-        epi_sync();
-        tc_fence_after_sync();
-        tmem_st16(slot[0] + lane_off + half * 32, *reinterpret_cast<const float(*)[16]>(pk));
-        tmem_st16(slot[0] + lane_off + half * 32 + 16, *reinterpret_cast<const float(*)[16]>(pk + 16));
-        tmem_st_wait();
-        tc_fence_before_sync();
-        mbar_arrive(&s.bar_pready);
-
-        if (!mbar_wait(&s.bar_pv, 0, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
-        tc_fence_after_sync();
-        float o[64];
-        {
-            float r2[2][16];
-#pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 32) {
-                tmem_ld16(slot[1] + lane_off + half * 64 + c0, r2[0]);
-                tmem_ld16(slot[1] + lane_off + half * 64 + c0 + 16, r2[1]);
-                tmem_ld_wait();
-#pragma unroll
-                for (int u = 0; u < 16; u++) {
-                    o[c0 + u] = r2[0][u];
-                    o[c0 + 16 + u] = r2[1][u];
-                }
-            }
-        }
-        tc_fence_before_sync();
-        mbar_arrive(&s.bar_pvfree);
-
-        // read-out: U_n = Q Node_{j_n} in slot n&1, drained with the fp32 weights
-        for (int n = 0; n < npath; n++) {
-            const int st = n & 1;
-            const float w = s.wgt[n * kTile + row];
-            if (!mbar_wait(&s.bar_u[st], (n >> 1) & 1, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
+        constexpr int kCols = D / 2;  // output columns per thread
+        uint32_t par_u = 0;  // parity of the completions of bar_u[b] consumed so far (bit b)
+        for (int n = 0;; n++) {
+            const int sg = n & 1;
+            if (!mbar_wait(&s.bar_load[sg], (n >> 1) & 1, prm.wait_iters)) set_err(prm.err, kErrLoadTimeout);
+            const int w = s.item[sg];
+            if (w < 0) break;
+            int i, bh;
+            item_tile(w, NT, BH, &i, &bh);
+            const int npath = __popc(i);
+            const bool row_ok = row < prm.T - i * kTile;
+            const float gam_a = s.gam[sg][row];
+            const float *lam_a = s.lam[sg] + row * L;
+            const uint32_t slot0 = tm + sg * kRegion, slot1 = slot0 + 128;
+            if (half == 0) s.kf[row] = __expf(s.gam[sg][row | 15] - gam_a);
+            epi_sync();
+            if (!mbar_wait(&s.bar_s, n & 1, prm.s_wait_iters)) set_err(prm.err, kErrMmaTimeout);
             tc_fence_after_sync();
-            float r2[2][16];
+            // P = S . M  (thread = query row, 64 keys), packed bf16 pairs in registers
+            uint32_t pk[32];
+            {
+                const int a = row;
 #pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 32) {
-                tmem_ld16(slot[st] + lane_off + half * 64 + c0, r2[0]);
-                tmem_ld16(slot[st] + lane_off + half * 64 + c0 + 16, r2[1]);
+                for (int cc = 0; cc < 4; cc += 2) {
+                    const int c0 = half * 64 + cc * 16;
+                    // the loads are warp-collective: every lane issues them, whatever its row
+                    float r2[2][16];
+                    tmem_ld16(slot0 + lane_off + c0, r2[0]);
+                    tmem_ld16(slot0 + lane_off + c0 + 16, r2[1]);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int q2 = 0; q2 < 2; q2++) {
+                        const int cb = c0 + q2 * 16;
+                        const float *r = r2[q2];
+                        __nv_bfloat162 h[8];
+                        if (cb > a || !row_ok) {  // strictly above the diagonal, or a row past T
+#pragma unroll
+                            for (int u = 0; u < 8; u++) h[u] = __floats2bfloat162_rn(0.f, 0.f);
+                        } else if (cb + 16 <= a) {
+                            // a whole 16-key chunk below the row: one level, and the decay
+                            // exp(gamma_a - gamma_b) = exp(gamma_a - gamma_e) exp(gamma_e - gamma_b)
+                            // with e = cb + 15, both factors <= 1
+                            const int lev = 32 - __clz(a ^ cb);
+                            const float ra = lam_a[lev] * __expf(gam_a - s.gam[sg][cb + 15]);
+#pragma unroll
+                            for (int u = 0; u < 8; u++)
+                                h[u] = __floats2bfloat162_rn(r[2 * u] * ra * s.kf[cb + 2 * u],
+                                                             r[2 * u + 1] * ra * s.kf[cb + 2 * u + 1]);
+                        } else {
+#pragma unroll
+                            for (int u = 0; u < 8; u++) {
+                                float x[2];
+#pragma unroll
+                                for (int e = 0; e < 2; e++) {
+                                    const int b = cb + 2 * u + e;
+                                    x[e] = 0.f;
+                                    if (b <= a) {
+                                        const int lev = 32 - __clz(a ^ b);
+                                        x[e] = r[2 * u + e] * lam_a[lev] * __expf(gam_a - s.gam[sg][b]);
+                                    }
+                                }
+                                h[u] = __floats2bfloat162_rn(x[0], x[1]);
+                            }
+                        }
+#pragma unroll
+                        for (int u = 0; u < 8; u++) pk[(cc + q2) * 8 + u] = *reinterpret_cast<uint32_t *>(&h[u]);
+                    }
+                }
+            }
+            // P replaces S in tensor memory (keys 2c, 2c+1 in column c) once every
+            // epilogue thread has read its S columns
+            tc_fence_before_sync();
+            epi_sync();
+            tc_fence_after_sync();
+            tmem_st16(slot0 + lane_off + half * 32, *reinterpret_cast<const float(*)[16]>(pk));
+            tmem_st16(slot0 + lane_off + half * 32 + 16, *reinterpret_cast<const float(*)[16]>(pk + 16));
+            tmem_st_wait();
+            tc_fence_before_sync();
+            mbar_arrive(&s.bar_pready);
+
+            if (!mbar_wait(&s.bar_pv, n & 1, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
+            tc_fence_after_sync();
+            float o[kCols];
+#pragma unroll
+            for (int c0 = 0; c0 < kCols; c0 += 16) {
+                float r[16];
+                tmem_ld16(slot1 + lane_off + half * kCols + c0, r);
                 tmem_ld_wait();
 #pragma unroll
-                for (int u = 0; u < 16; u++) {
-                    o[c0 + u] = fmaf(w, r2[0][u], o[c0 + u]);
-                    o[c0 + 16 + u] = fmaf(w, r2[1][u], o[c0 + 16 + u]);
-                }
+                for (int u = 0; u < 16; u++) o[c0 + u] = r[u];
             }
             tc_fence_before_sync();
-            mbar_arrive(&s.bar_ufree[st]);
-        }
+            mbar_arrive(&s.bar_pvfree);
 
-        // ---- store: stage the tile in the Q/K buffers (every product that read
-        // them is complete), then TMA; rows past T are clipped by the tensor map
-        if (sizeof(OutT) == 4) {
+            // read-out: U_k = Q Node_{j_k} in slot k & 1, drained with the fp32 weight
+            //   lambda_a[8 + m_k] exp(gamma_a + P_i - P_{j_k}),  m_k = ctz(j_k)
+            {
+                const double Pi = s.pj[sg][kMaxPath];
+                int j = i;
+                for (int k = 0; k < npath; k++) {
+                    const int b = k & 1;
+                    const int m = __ffs(j) - 1;
+                    j -= (j & -j);
+                    const float wk = row_ok ? lam_a[kTileLevels + 1 + m] * __expf(gam_a + (float)(Pi - s.pj[sg][k]))
+                                            : 0.f;
+                    if (!mbar_wait(&s.bar_u[b], (par_u >> b) & 1, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
+                    par_u ^= 1u << b;
+                    tc_fence_after_sync();
+                    const uint32_t sl = slot0 + 128 * b;
 #pragma unroll
-            for (int c = 0; c < 16; c++)
-                *reinterpret_cast<float4 *>(s.q + f32_stage_off(row, half * 16 + c)) =
-                    make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
-        } else {
+                    for (int c0 = 0; c0 < kCols; c0 += 16) {
+                        float r[16];
+                        tmem_ld16(sl + lane_off + half * kCols + c0, r);
+                        tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < 8; c++) {
-                uint4 w4;
-                __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&w4);
-#pragma unroll
-                for (int u = 0; u < 4; u++) h[u] = __floats2bfloat162_rn(o[8 * c + 2 * u], o[8 * c + 2 * u + 1]);
-                *reinterpret_cast<uint4 *>(s.q + half * kHalf + sw128_offset(row, c)) = w4;
+                        for (int u = 0; u < 16; u++) o[c0 + u] = fmaf(wk, r[u], o[c0 + u]);
+                    }
+                    tc_fence_before_sync();
+                    mbar_arrive(&s.bar_ufree[b]);
+                }
             }
-        }
-        fence_proxy_async_smem();
-        epi_sync();
-        if (tid == 0) {
+            // every tensor-memory read of this tile is done: its region may take tile n+2
+            tc_fence_before_sync();
+            mbar_arrive(&s.bar_tfree[sg]);
+
+            // ---- store: stage the tile in the q/k buffers (every product that read
+            // them is complete), then TMA; rows past T are clipped by the tensor map
+            ConsStage<D> &t = s.st[sg];
             if (sizeof(OutT) == 4) {
+                // fp32: D/32 boxes of 32 columns x 128 rows, in q then k
 #pragma unroll
-                for (int b = 0; b < 4; b++) tma_store_3d(&map_out, s.q + b * (kTile * 128), b * 32, i * kTile, bh);
+                for (int c = 0; c < kCols / 4; c++) {
+                    const int cg = half * (kCols / 4) + c;  // 4-float chunk of the row
+                    *reinterpret_cast<float4 *>(t.q + f32_stage_off(row, cg)) =
+                        make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+                }
             } else {
+                // bf16: D/64 blocks of 64 columns
 #pragma unroll
-                for (int h = 0; h < 2; h++) tma_store_3d(&map_out, s.q + h * kHalf, h * 64, i * kTile, bh);
+                for (int c = 0; c < kCols / 8; c++) {
+                    const int cg = half * (kCols / 8) + c;  // 8-element chunk of the row
+                    uint4 w4;
+                    __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&w4);
+#pragma unroll
+                    for (int u = 0; u < 4; u++) h[u] = __floats2bfloat162_rn(o[8 * c + 2 * u], o[8 * c + 2 * u + 1]);
+                    *reinterpret_cast<uint4 *>(t.q + (cg >> 3) * kBlk + sw128_offset(row, cg & 7)) = w4;
+                }
             }
-            tma_store_commit();
-            tma_store_wait_read();  // shared memory may be released; the writes finish with the kernel
+            fence_proxy_async_smem();
+            epi_sync();
+            if (tid == 0) {
+                if (sizeof(OutT) == 4) {
+#pragma unroll
+                    for (int b = 0; b < D / 32; b++) tma_store_3d(&map_out, t.q + b * (kTile * 128), b * 32, i * kTile, bh);
+                } else {
+#pragma unroll
+                    for (int h = 0; h < D / 64; h++) tma_store_3d(&map_out, t.q + h * kBlk, h * 64, i * kTile, bh);
+                }
+                tma_store_commit();
+                tma_store_wait_read();  // the stage may be refilled; the writes finish with the kernel
+                mbar_arrive(&s.bar_sfree[sg]);
+            }
         }
     }
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tm, 256);
+    if (warp == 0) tmem_dealloc(tm, 512);
 }
 
 // Gate sums, in two small launches.  First, a warp per tile: Gam_i in fp64
 // from one coalesced float4 load per lane, stored in the P array shifted by
-// one (P[i+1] = Gam_i); the workspace error word is reset here too (err is
-// null when the caller passed a word of its own, which is never cleared).
+// one (P[i+1] = Gam_i); the consumer's queue counter and the workspace error
+// word are reset here too (err is null when the caller passed a word of its
+// own, which is never cleared).
 // Then one CTA per (batch*head) turns the tile sums into the prefix
 // P_i = Gam_0 + ... + Gam_{i-1} in place.
 constexpr int kScanThreads = 1024;
 __global__ void __launch_bounds__(1024)
 lla_tile_gate_sum_kernel(const float *__restrict__ g, double *__restrict__ P, float *__restrict__ gamma,
-                         int *__restrict__ err, int T, int NT)
+                         int *__restrict__ err, int *__restrict__ queue, int T, int NT)
 {
     const long long bh = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -735,7 +814,10 @@ lla_tile_gate_sum_kernel(const float *__restrict__ g, double *__restrict__ P, fl
     }
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         Pb[0] = 0.0;
-        if (bh == 0 && err != nullptr) *err = 0;
+        if (bh == 0) {
+            if (err != nullptr) *err = 0;
+            *queue = 0;
+        }
     }
 }
 
@@ -780,28 +862,28 @@ lla_tile_gate_scan_kernel(double *__restrict__ P, int NT)
 
 }  // namespace
 
-// Workspace: [P fp64 BH*(NT+1)] [gamma fp32 BH*NT*128] [err word] [segment totals fp32] [nodes bf16]
+// Workspace: [P fp64 BH*(NT+1)] [gamma fp32 BH*NT*128] [err word, queue counter]
+// [segment totals fp32] [nodes bf16]
 static int nseg_full_of(int NT) { return NT > 1 ? (NT - 1) / kSeg : 0; }
 static size_t off_gamma(int BH, int NT) { return align_up((size_t)BH * (NT + 1) * 8, 256); }
 static size_t off_err(int BH, int NT) { return off_gamma(BH, NT) + align_up((size_t)BH * NT * kTile * 4, 256); }
+static size_t off_queue(int BH, int NT) { return off_err(BH, NT) + 128; }
 static size_t off_segtot(int BH, int NT) { return off_err(BH, NT) + 256; }
-static size_t off_node16(int BH, int NT)
+static size_t off_node16(int BH, int NT, int D)
 {
-    return off_segtot(BH, NT) + align_up((size_t)BH * nseg_full_of(NT) * kD * kD * 4, 1024);
+    return off_segtot(BH, NT) + align_up((size_t)BH * nseg_full_of(NT) * D * D * 4, 1024);
 }
 
-size_t tc_workspace_bytes(int B, int H, int T)
+size_t tc_workspace_bytes(int B, int H, int T, int D)
 {
     const int BH = B * H, NT = (T + kTile - 1) / kTile;
-    return off_node16(BH, NT) + align_up((size_t)BH * NT * kD * kD * 2, 1024);
+    return off_node16(BH, NT, D) + align_up((size_t)BH * NT * D * D * 2, 1024);
 }
 
 bool tc_supported(int dk, int dv, lla_dtype in_dt)
 {
-    return in_dt == LLA_BF16 && dk == kD && dv == kD;
+    return in_dt == LLA_BF16 && dk == dv && (dk == 64 || dk == 128);
 }
-
-size_t tc_smem_bytes() { return sizeof(ConsSmem) + 1024; }
 
 int tc_launches(int T)
 {
@@ -810,8 +892,8 @@ int tc_launches(int T)
     return 4 + (nseg_full_of(NT) > 0 ? 1 : 0);      // + walkers (+ segment fix-up)
 }
 
-static_assert(sizeof(WalkSmem) + 1024 <= 113 * 1024, "walker must fit two CTAs per SM");
-static_assert(sizeof(ConsSmem) + 1024 <= 113 * 1024, "consumer must fit two CTAs per SM");
+static_assert(sizeof(WalkSmem<128>) + 1024 <= 113 * 1024, "walker must fit two CTAs per SM");
+static_assert(sizeof(ConsSmem<128>) + 1024 <= 227 * 1024, "consumer must fit the shared memory of an SM");
 
 // Launch configuration, optionally as a programmatic dependent of the
 // previous kernel in the stream (it may start before that one finishes and
@@ -831,25 +913,35 @@ static cudaLaunchConfig_t launch_cfg(dim3 grid, dim3 block, size_t smem, cudaStr
     return cfg;
 }
 
-template <typename OutT>
+static int sm_count()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        n = 148;
+    return n;
+}
+
+template <int D, typename OutT>
 static cudaError_t launch_consumer(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                                    const CUtensorMap &mn, const CUtensorMap &mo, const TcParams &prm,
                                    int grid, cudaStream_t st, bool dependent)
 {
-    const size_t smem = sizeof(ConsSmem) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(lla_readout_consumer_kernel<OutT>,
+    const size_t smem = sizeof(ConsSmem<D>) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(lla_readout_consumer_kernel<D, OutT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr;
     cudaLaunchConfig_t cfg = launch_cfg(dim3(grid), dim3(kConsThreads), smem, st, dependent, &attr);
-    return cudaLaunchKernelEx(&cfg, lla_readout_consumer_kernel<OutT>, mq, mk, mv, mn, mo, prm);
+    return cudaLaunchKernelEx(&cfg, lla_readout_consumer_kernel<D, OutT>, mq, mk, mv, mn, mo, prm);
 }
 
 static std::atomic<int> g_withhold_first_product{0};
 
 void tc_set_withhold_first_product(int enable) { g_withhold_first_product.store(enable ? 1 : 0); }
 
-cudaError_t tc_fwd(const TcFwdArgs &A)
+template <int D>
+static cudaError_t tc_fwd_d(const TcFwdArgs &A)
 {
     const int BH = A.B * A.H, NT = (A.T + kTile - 1) / kTile;
     char *ws = (char *)A.workspace;
@@ -860,9 +952,10 @@ cudaError_t tc_fwd(const TcFwdArgs &A)
     prm.P = (const double *)ws;
     int *const ws_err = (int *)(ws + off_err(BH, NT));
     prm.err = A.device_error ? (int *)A.device_error : ws_err;
+    prm.queue = (int *)(ws + off_queue(BH, NT));
     prm.gamma = (float *)(ws + off_gamma(BH, NT));
     prm.segtot = (float *)(ws + off_segtot(BH, NT));
-    prm.node16 = (__nv_bfloat16 *)(ws + off_node16(BH, NT));
+    prm.node16 = (__nv_bfloat16 *)(ws + off_node16(BH, NT, D));
     prm.T = A.T;
     prm.NT = NT;
     prm.BH = BH;
@@ -873,39 +966,47 @@ cudaError_t tc_fwd(const TcFwdArgs &A)
     prm.s_wait_iters = prm.withhold ? kWithheldWaitIters : kWaitIters;
     CUtensorMap mq, mk, mv, mn, mo;
     const bool out32 = A.out_dt == LLA_F32;
-    if (!make_map_bf16_3d(&mq, A.q, kD, A.T, BH, 64, kTile) ||
-        !make_map_bf16_3d(&mk, A.k, kD, A.T, BH, 64, kTile) ||
-        !make_map_bf16_3d(&mv, A.v, kD, A.T, BH, 64, kTile) ||
-        !make_map_bf16_3d(&mn, prm.node16, kD, kD, (uint64_t)BH * NT, 64, kTile) ||
-        !(out32 ? make_map_f32_3d(&mo, A.out, kD, A.T, BH, 32, kTile)
-                : make_map_bf16_3d(&mo, A.out, kD, A.T, BH, 64, kTile)))
+    if (!make_map_bf16_3d(&mq, A.q, D, A.T, BH, 64, kTile) ||
+        !make_map_bf16_3d(&mk, A.k, D, A.T, BH, 64, kTile) ||
+        !make_map_bf16_3d(&mv, A.v, D, A.T, BH, 64, kTile) ||
+        !make_map_bf16_3d(&mn, prm.node16, D, D, (uint64_t)BH * NT, 64, D) ||
+        !(out32 ? make_map_f32_3d(&mo, A.out, D, A.T, BH, 32, kTile)
+                : make_map_bf16_3d(&mo, A.out, D, A.T, BH, 64, kTile)))
         return cudaErrorInvalidValue;
     cudaStream_t st = (cudaStream_t)A.stream;
-    lla_tile_gate_sum_kernel<<<dim3((NT + 31) / 32, BH), 1024, 0, st>>>(A.g, (double *)prm.P, prm.gamma,
-                                                                          A.device_error ? nullptr : ws_err,
-                                                                          A.T, NT);
+    lla_tile_gate_sum_kernel<<<dim3((NT + 31) / 32, BH), 1024, 0, st>>>(
+        A.g, (double *)prm.P, prm.gamma, A.device_error ? nullptr : ws_err, prm.queue, A.T, NT);
     lla_tile_gate_scan_kernel<<<BH, kScanThreads, 0, st>>>((double *)prm.P, NT);
     cudaError_t e;
     if (NT > 1) {
-        const size_t wsmem = sizeof(WalkSmem) + 1024;
-        e = cudaFuncSetAttribute(lla_node_walker_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        const size_t wsmem = sizeof(WalkSmem<D>) + 1024;
+        e = cudaFuncSetAttribute(lla_node_walker_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)wsmem);
         if (e != cudaSuccess) return e;
         const int nseg = (NT - 1 + kSeg - 1) / kSeg;
-        lla_node_walker_kernel<<<dim3(nseg, kSlices, BH), kWalkThreads, wsmem, st>>>(mk, mv, prm);
+        lla_node_walker_kernel<D><<<dim3(nseg, D / kSliceW, BH), kWalkThreads, wsmem, st>>>(mk, mv, prm);
         if (prm.nseg_full > 0) {
             cudaLaunchAttribute attr;
             cudaLaunchConfig_t cfg =
-                launch_cfg(dim3(kD * kD / 8 / kFixThreads, BH), dim3(kFixThreads), 0, st, true, &attr);
-            e = cudaLaunchKernelEx(&cfg, lla_node_fixup_kernel, prm);
+                launch_cfg(dim3((D * D / 8 + kFixThreads - 1) / kFixThreads, BH), dim3(kFixThreads), 0, st, true, &attr);
+            e = cudaLaunchKernelEx(&cfg, lla_node_fixup_kernel<D>, prm);
             if (e != cudaSuccess) return e;
         }
     }
-    // with nodes to read, the read-out starts in the tail of the node launches
-    e = out32 ? launch_consumer<float>(mq, mk, mv, mn, mo, prm, NT * BH, st, NT > 1)
-              : launch_consumer<__nv_bfloat16>(mq, mk, mv, mn, mo, prm, NT * BH, st, NT > 1);
+    // persistent read-out: one CTA per SM (or per tile when there are fewer);
+    // with nodes to read it starts in the tail of the node launches
+    const long long items = (long long)NT * BH;
+    const int grid = (int)(items < sm_count() ? items : sm_count());
+    e = out32 ? launch_consumer<D, float>(mq, mk, mv, mn, mo, prm, grid, st, NT > 1)
+              : launch_consumer<D, __nv_bfloat16>(mq, mk, mv, mn, mo, prm, grid, st, NT > 1);
     if (e != cudaSuccess) return e;
     return cudaPeekAtLastError();
+}
+
+cudaError_t tc_fwd(const TcFwdArgs &A)
+{
+    if (A.dk == 64) return tc_fwd_d<64>(A);
+    return tc_fwd_d<128>(A);
 }
 
 }  // namespace lla

@@ -12,6 +12,7 @@ struct TcFwdArgs {
     const float *g, *lam;
     void *out;
     int B, H, T, L;
+    int dk;  // = dv, 64 or 128
     lla_dtype out_dt;
     void *workspace;
     int32_t *device_error;  // caller's word, or nullptr (the workspace word is used)
@@ -19,8 +20,7 @@ struct TcFwdArgs {
 };
 
 bool tc_supported(int dk, int dv, lla_dtype in_dt);
-size_t tc_workspace_bytes(int B, int H, int T);
-size_t tc_smem_bytes();
+size_t tc_workspace_bytes(int B, int H, int T, int D);
 int tc_launches(int T);
 cudaError_t tc_fwd(const TcFwdArgs &A);
 // Test hook: withhold each tile's first product and shorten the waits.

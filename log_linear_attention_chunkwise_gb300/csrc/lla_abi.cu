@@ -101,7 +101,7 @@ size_t lla_fwd_workspace_bytes(int B, int H, int T, int dk, int dv, int chunk, l
 {
     if (fwd_shape_status(B, H, T, dk, dv, chunk, in_dt) != LLA_OK) return 0;
     if ((long long)B * H * T == 0) return 0;
-    if (tc_supported(dk, dv, in_dt)) return tc_workspace_bytes(B, H, T);
+    if (tc_supported(dk, dv, in_dt)) return tc_workspace_bytes(B, H, T, dk);
     SimtFwdArgs A = simt_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, B, H, T,
                               dk, dv, chunk, in_dt, LLA_F32, nullptr, nullptr);
     return simt_workspace_bytes(A);
@@ -148,7 +148,7 @@ lla_status lla_fwd(const void *q, const void *k, const void *v, const float *g,
     if (tc_supported(dk, dv, in_dt)) {
         TcFwdArgs A;
         A.q = q; A.k = k; A.v = v; A.g = g; A.lam = lambda; A.out = out;
-        A.B = B; A.H = H; A.T = T; A.L = lla_num_levels(T); A.out_dt = out_dt;
+        A.B = B; A.H = H; A.T = T; A.L = lla_num_levels(T); A.dk = dk; A.out_dt = out_dt;
         A.workspace = workspace; A.device_error = device_error; A.stream = stream;
         return tc_fwd(A) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
     }

@@ -162,6 +162,16 @@ def test_bf16_T32768_stress_no_decay_heads():
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("T,d", [(4224, 64), (12288, 64), (12288, 128)])
+def test_multi_segment_fixup_chain_stress(T, d):
+    """Zero-gate heads at lengths with one, two or three full 32-tile
+    segments, so the fix-up chain of segment totals (Node_32, Node_64, ...)
+    carries most of the output, for both tensor-core widths."""
+    cfg = W.small_fwd_config(1, 2, T, d, d, 64, torch.bfloat16, seed=T + 3 * d + 1, g_zero_head_frac=0.5)
+    assert (W.make_fwd_inputs(cfg)["g"][0].abs().sum(-1) == 0).any()  # a head without decay
+    check_full_size(cfg, pairs_rows=[], n_rows=0)
+
+
 def test_bf16_T8192_stress_reduced():
     cfg = W.FWD_CONFIGS["bf16_T8192_lam1"].with_(B=1, H=4, g_zero_head_frac=0.5, seed=12)
     check_full_size(cfg, pairs_rows=[], n_rows=0)
