@@ -251,6 +251,42 @@ class ClockSampler:
 
 # ------------------------------------------------------------- our arm
 
+def run_e2e(args, x, cfg, out, dev, stream, tokens):
+    """The same metric end to end through the C-ABI host-buffer call
+    lla_fwd_host: pinned host inputs copied in, the forward, the output
+    copied back, every step."""
+    from log_linear_attention_chunkwise_gb300 import binding
+    hx = {n: t.pin_memory() for n, t in x.items()}
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in hx.values())
+    d2h = hout.numel() * hout.element_size()
+    hneed = binding.load().lla_fwd_host_workspace_bytes(
+        cfg.B, cfg.H, cfg.T, cfg.dk, cfg.dv, cfg.chunk, binding.LLA_BF16, binding.LLA_F32, 0)
+    hws = torch.empty(hneed, dtype=torch.uint8, device=dev)
+
+    def e2e_step():
+        binding.fwd_host(hx["q"], hx["k"], hx["v"], hx["g"], hx["lam"], out=hout, chunk=cfg.chunk,
+                         workspace=hws, stream=stream, device=dev)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_steps = max(3, min(args.steps, 10))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = a.elapsed_time(b) / e2e_steps
+    e2e_ms = max_over_ranks(e2e_ms, dev)
+    del hws
+
+    return {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+            "call": "lla_fwd_host (host buffers, copies pipelined with the forward)"}
+
+
 def run_lla(args, rank, world, local_rank):
     from log_linear_attention_chunkwise_gb300 import binding
     binding.load()
@@ -301,31 +337,7 @@ def run_lla(args, rank, world, local_rank):
 
     # end to end through the C-ABI host-buffer call (lla_fwd_host): pinned host
     # inputs copied in, the forward, the output copied back, every step
-    hx = {n: t.pin_memory() for n, t in x.items()}
-    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in hx.values())
-    d2h = hout.numel() * hout.element_size()
-    hneed = binding.load().lla_fwd_host_workspace_bytes(
-        cfg.B, cfg.H, cfg.T, cfg.dk, cfg.dv, cfg.chunk, binding.LLA_BF16, binding.LLA_F32, 0)
-    hws = torch.empty(hneed, dtype=torch.uint8, device=dev)
-
-    def e2e_step():
-        binding.fwd_host(hx["q"], hx["k"], hx["v"], hx["g"], hx["lam"], out=hout, chunk=cfg.chunk,
-                         workspace=hws, stream=stream, device=dev)
-
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    e2e_steps = max(3, min(args.steps, 10))
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    b.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = a.elapsed_time(b) / e2e_steps
-    e2e_ms = max_over_ranks(e2e_ms, dev)
-    del hws
+    e2e = run_e2e(args, x, cfg, out, dev, stream, tokens) if not args.skip_e2e else None
 
     hbm_peak, bf16_peak, bf16_sus, peak_src = load_peaks()
     nbytes = fwd_bytes(cfg)
@@ -350,13 +362,10 @@ def run_lla(args, rank, world, local_rank):
                      "algorithmic_bytes_per_launch": nbytes, "algorithmic_flops_per_launch": flops,
                      "per_launch_ms": per_launch_ms,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"},
-        "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "call": "lla_fwd_host (host buffers, copies pipelined with the forward)"},
+        "e2e": e2e,
         "gpu_launches": launches_per_call * args.steps,
         "clocks": clk.summary(),
     }
-    del hx, hout
     if rank == 0 and not args.skip_configs:
         res["fwd_lines"] = run_fwd_lines(dev, xd, cfg, ws, stream, hbm_peak, bf16_peak)
     if rank == 0 and not args.skip_decode:
@@ -688,6 +697,7 @@ def main():
     ap.add_argument("--skip-next", action="store_true",
                     help="skip the prefill / lambda-MLP / backward timings")
     ap.add_argument("--skip-bwd", action="store_true", help="skip the backward timing")
+    ap.add_argument("--skip-e2e", action="store_true", help="skip the host-buffer (end-to-end) timing")
     ap.add_argument("--skip-configs", action="store_true",
                     help="skip the bf16-out and T=8192 / T=2048 forward lines")
     ap.add_argument("--cpu-tokens", type=int, default=32768)
