@@ -448,6 +448,7 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
 
     if (warp == kProdWarp) {
         // ---------------- producer
+        bool dep_done = false;
         for (int n = 0;; n++) {
             const int sg = n & 1;
             if (n >= 2 && lane == 0 && !mbar_wait(&s.bar_sfree[sg], ((n - 2) >> 1) & 1, prm.wait_iters))
@@ -489,6 +490,16 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
                 bulk_load(s.lam[sg], prm.lam + tok0 * L, lam_bytes, bar);
                 bulk_load(s.gam[sg], prm.gamma + ((long long)bh * NT + i) * kTile, kTile * 4, bar);
             }
+            // the tile's path nodes into L2 ahead of their loads (lane c: node c);
+            // they come from the previous launches, so wait for those once
+            if (i > 0) {
+                if (!dep_done) {
+                    grid_dependency_wait();
+                    dep_done = true;
+                }
+                if (lane < kMaxPath && j > 0)
+                    bulk_prefetch_l2(prm.node16 + ((long long)bh * NT + j) * (D * D), (uint32_t)D * D * 2);
+            }
         }
     } else if (warp == kMmaWarp) {
         // ---------------- MMA issuer (one lane)
@@ -499,6 +510,7 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
             // only parities are ever waited on
             uint32_t par_node = 0, par_u = 0;
             bool dep_done = false;
+            bool s_early = false;  // this tile's S was issued while the previous tile read out
             for (int n = 0;; n++) {
                 const int sg = n & 1;
                 if (!mbar_wait(&s.bar_load[sg], (n >> 1) & 1, prm.wait_iters)) set_err(prm.err, kErrLoadTimeout);
@@ -507,7 +519,7 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
                 int i, bh;
                 item_tile(w, NT, BH, &i, &bh);
                 const int npath = __popc(i);
-                if (n >= 2 && !mbar_wait(&s.bar_tfree[sg], ((n - 2) >> 1) & 1, prm.wait_iters))
+                if (!s_early && n >= 2 && !mbar_wait(&s.bar_tfree[sg], ((n - 2) >> 1) & 1, prm.wait_iters))
                     set_err(prm.err, kErrMmaTimeout);
                 tc_fence_after_sync();
                 // slot b at slot0 + 128 b; node buffer b is k (b = 0) or v (b = 1)
@@ -533,10 +545,11 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
                 };
                 // parity of the completion of the latest U issued into slot b
                 auto last_u_par = [&](int b) { return ((par_u >> b) & 1) ^ 1; };
-                if (!prm.withhold) {  // withheld: nothing is left in flight, the waits on bar_s run out
+                if (!s_early && !prm.withhold) {  // withheld: nothing is left in flight, the waits on bar_s run out
                     mma_kk<D>(slot0, t.q, t.k, id_s);
                     umma_commit(&s.bar_s);
                 }
+                s_early = false;
                 int jnext = i;
                 if (npath > 0) {
                     if (!mbar_wait(&s.bar_s, n & 1, prm.s_wait_iters)) set_err(prm.err, kErrMmaTimeout);
@@ -552,10 +565,11 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
                 // O = P V: P from tensor memory once the epilogue has stored it
                 if (!mbar_wait(&s.bar_pready, n & 1, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
                 tc_fence_after_sync();
+                // P of keys [64h, 64h+64) sits packed in columns [64h, 64h+32)
 #pragma unroll
                 for (int kk = 0; kk < 8; kk++)
-                    umma_bf16_tmem_a(slot0 + 128, slot0 + kk * 8, desc_sw128(smem_u32(t.v) + kk * 2048, kBlk, 1024),
-                                     id_kmn, kk > 0 ? 1u : 0u);
+                    umma_bf16_tmem_a(slot0 + 128, slot0 + (kk >> 2) * 64 + (kk & 3) * 8,
+                                     desc_sw128(smem_u32(t.v) + kk * 2048, kBlk, 1024), id_kmn, kk > 0 ? 1u : 0u);
                 umma_commit(&s.bar_pv);
                 if (npath > 0) {
                     if (!mbar_wait(&s.bar_pv, n & 1, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
@@ -566,6 +580,19 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
                     // path node 0 into slot 0 (P has been consumed)
                     wait_node(0);
                     issue_u(0);
+                }
+                {   // the next tile's S, if its inputs have landed and its region is free,
+                    // so that the epilogue finds it done when it gets there
+                    const int n1 = n + 1, sg1 = n1 & 1;
+                    if (mbar_test(&s.bar_load[sg1], (n1 >> 1) & 1) && s.item[sg1] >= 0 &&
+                        (n1 < 2 || mbar_test(&s.bar_tfree[sg1], ((n1 - 2) >> 1) & 1))) {
+                        tc_fence_after_sync();
+                        if (!prm.withhold) {
+                            mma_kk<D>(tm + sg1 * kRegion, s.st[sg1].q, s.st[sg1].k, id_s);
+                            umma_commit(&s.bar_s);
+                        }
+                        s_early = true;
+                    }
                 }
                 for (int k = 0; k < npath; k++) {
                     const int b = k & 1, b1 = b ^ 1;
@@ -614,12 +641,15 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
             epi_sync();
             if (!mbar_wait(&s.bar_s, n & 1, prm.s_wait_iters)) set_err(prm.err, kErrMmaTimeout);
             tc_fence_after_sync();
-            // P = S . M  (thread = query row, 64 keys), packed bf16 pairs in registers
-            uint32_t pk[32];
+            // P = S . M  (thread = query row, keys [64 half, 64 half + 64)), written
+            // back packed (keys 2c, 2c+1 in one column) into columns
+            // [64 half, 64 half + 32): columns this thread has already read, so no
+            // other thread's S is overwritten
             {
                 const int a = row;
 #pragma unroll
                 for (int cc = 0; cc < 4; cc += 2) {
+                    uint32_t pk[16];
                     const int c0 = half * 64 + cc * 16;
                     // the loads are warp-collective: every lane issues them, whatever its row
                     float r2[2][16];
@@ -661,17 +691,11 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
                             }
                         }
 #pragma unroll
-                        for (int u = 0; u < 8; u++) pk[(cc + q2) * 8 + u] = *reinterpret_cast<uint32_t *>(&h[u]);
+                        for (int u = 0; u < 8; u++) pk[q2 * 8 + u] = *reinterpret_cast<uint32_t *>(&h[u]);
                     }
+                    tmem_st16(slot0 + lane_off + half * 64 + cc * 8, *reinterpret_cast<const float(*)[16]>(pk));
                 }
             }
-            // P replaces S in tensor memory (keys 2c, 2c+1 in column c) once every
-            // epilogue thread has read its S columns
-            tc_fence_before_sync();
-            epi_sync();
-            tc_fence_after_sync();
-            tmem_st16(slot0 + lane_off + half * 32, *reinterpret_cast<const float(*)[16]>(pk));
-            tmem_st16(slot0 + lane_off + half * 32 + 16, *reinterpret_cast<const float(*)[16]>(pk + 16));
             tmem_st_wait();
             tc_fence_before_sync();
             mbar_arrive(&s.bar_pready);
@@ -680,13 +704,11 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
             tc_fence_after_sync();
             float o[kCols];
 #pragma unroll
-            for (int c0 = 0; c0 < kCols; c0 += 16) {
-                float r[16];
-                tmem_ld16(slot1 + lane_off + half * kCols + c0, r);
-                tmem_ld_wait();
-#pragma unroll
-                for (int u = 0; u < 16; u++) o[c0 + u] = r[u];
+            for (int c0 = 0; c0 < kCols; c0 += 32) {
+                tmem_ld16(slot1 + lane_off + half * kCols + c0, *reinterpret_cast<float(*)[16]>(o + c0));
+                tmem_ld16(slot1 + lane_off + half * kCols + c0 + 16, *reinterpret_cast<float(*)[16]>(o + c0 + 16));
             }
+            tmem_ld_wait();
             tc_fence_before_sync();
             mbar_arrive(&s.bar_pvfree);
 
@@ -706,12 +728,16 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
                     tc_fence_after_sync();
                     const uint32_t sl = slot0 + 128 * b;
 #pragma unroll
-                    for (int c0 = 0; c0 < kCols; c0 += 16) {
-                        float r[16];
-                        tmem_ld16(sl + lane_off + half * kCols + c0, r);
+                    for (int c0 = 0; c0 < kCols; c0 += 32) {
+                        float r2[2][16];
+                        tmem_ld16(sl + lane_off + half * kCols + c0, r2[0]);
+                        tmem_ld16(sl + lane_off + half * kCols + c0 + 16, r2[1]);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int u = 0; u < 16; u++) o[c0 + u] = fmaf(wk, r[u], o[c0 + u]);
+                        for (int u = 0; u < 16; u++) {
+                            o[c0 + u] = fmaf(wk, r2[0][u], o[c0 + u]);
+                            o[c0 + 16 + u] = fmaf(wk, r2[1][u], o[c0 + 16 + u]);
+                        }
                     }
                     tc_fence_before_sync();
                     mbar_arrive(&s.bar_ufree[b]);

@@ -92,6 +92,30 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint
         : "memory");
 }
 
+// Bring `bytes` (multiple of 16, 16-byte aligned address) of global memory
+// into L2 ahead of use; no completion to wait for.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *gsrc, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(gsrc)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// Non-blocking test of a phase (see mbar_try_wait), for issuers that have
+// other work to do when the phase has not completed yet.
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // 3-D tiled store shared -> global (bulk async group of this thread).  Rows
 // or columns outside the tensor are not written.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *smem_src, int c0, int c1,
