@@ -352,22 +352,25 @@ lla_node_fixup_kernel(const TcParams prm)
 // Persistent: one CTA per SM takes tiles from a queue (a counter in the
 // workspace) in order, last tiles first and tile-major across heads, so
 // co-running tiles share their deep nodes and the nodes written last are
-// still in L2.  Ten warps:
-//   warps 0-7  epilogue (thread = (row, half of the columns)): the mask P,
-//              the drains of P V and of every U = Q Node_j with its fp32
+// still in L2.  Eighteen warps:
+//   warps 0-15 epilogue (thread = (row, quarter of the columns)): the mask
+//              P, the drains of P V and of every U = Q Node_j with its fp32
 //              per-row weight, the output staged in shared memory and
-//              written by TMA;
-//   warp 8     producer: takes the next tile and brings its q, k, v, gamma,
-//              lambda and path P values into the free stage (two stages);
-//   warp 9     MMA issuer (one lane): S, P V, the node loads and the U's.
+//              written by TMA; four threads per row keep enough warps in
+//              flight to hide the tensor-memory and barrier latencies;
+//   warp 16    producer: takes the next tile and brings its q, k, v, gamma,
+//              lambda and path P values into the free stage (two stages),
+//              and its path nodes into L2;
+//   warp 17    MMA issuer (one lane): S, P V, the node loads and the U's.
 // Tile n uses stage n & 1 and tensor-memory region n & 1, so the MMAs and
 // loads of tile n+1 proceed while the epilogue drains tile n.  The roles
 // hand off through mbarriers only; the barriers used a variable number of
 // times per tile are waited with running completion counts.
 
-constexpr int kConsThreads = 320;  // 8 epilogue warps, a producer warp, an MMA warp
-constexpr int kEpiThreads = 256;
-constexpr int kProdWarp = 8, kMmaWarp = 9;
+constexpr int kEpiThreads = 512;   // 16 epilogue warps: 4 threads per row
+constexpr int kConsThreads = kEpiThreads + 64;  // plus a producer warp and an MMA warp
+constexpr int kProdWarp = kEpiThreads / 32, kMmaWarp = kProdWarp + 1;
+constexpr int kParts = kEpiThreads / kTile;  // threads per row
 
 template <int D>
 struct __align__(1024) ConsStage {
@@ -390,7 +393,7 @@ struct __align__(1024) ConsSmem {
     uint32_t tmem;
 };
 
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
 
 // Work item w -> tile (i, bh): tile-major, last tiles first.
 __device__ __forceinline__ void item_tile(int w, int NT, int BH, int *i, int *bh)
@@ -565,10 +568,10 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
                 // O = P V: P from tensor memory once the epilogue has stored it
                 if (!mbar_wait(&s.bar_pready, n & 1, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
                 tc_fence_after_sync();
-                // P of keys [64h, 64h+64) sits packed in columns [64h, 64h+32)
+                // P of keys [32p, 32p+32) sits packed in columns [32p, 32p+16)
 #pragma unroll
                 for (int kk = 0; kk < 8; kk++)
-                    umma_bf16_tmem_a(slot0 + 128, slot0 + (kk >> 2) * 64 + (kk & 3) * 8,
+                    umma_bf16_tmem_a(slot0 + 128, slot0 + (kk >> 1) * 32 + (kk & 1) * 8,
                                      desc_sw128(smem_u32(t.v) + kk * 2048, kBlk, 1024), id_kmn, kk > 0 ? 1u : 0u);
                 umma_commit(&s.bar_pv);
                 if (npath > 0) {
@@ -621,9 +624,9 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
     } else {
         // ---------------- epilogue warps
         const int row = tid & (kTile - 1);
-        const int half = tid >> 7;
+        const int part = tid >> 7;                      // keys [32 part, +32), columns [kCols part, +kCols)
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-        constexpr int kCols = D / 2;  // output columns per thread
+        constexpr int kCols = D / kParts;               // output columns per thread
         uint32_t par_u = 0;  // parity of the completions of bar_u[b] consumed so far (bit b)
         for (int n = 0;; n++) {
             const int sg = n & 1;
@@ -634,67 +637,65 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
             item_tile(w, NT, BH, &i, &bh);
             const int npath = __popc(i);
             const bool row_ok = row < prm.T - i * kTile;
-            const float gam_a = s.gam[sg][row];
+            const float *gam = s.gam[sg];
+            const float gam_a = gam[row];
             const float *lam_a = s.lam[sg] + row * L;
             const uint32_t slot0 = tm + sg * kRegion, slot1 = slot0 + 128;
-            if (half == 0) s.kf[row] = __expf(s.gam[sg][row | 15] - gam_a);
+            if (part == 0) s.kf[row] = __expf(gam[row | 15] - gam_a);
             epi_sync();
             if (!mbar_wait(&s.bar_s, n & 1, prm.s_wait_iters)) set_err(prm.err, kErrMmaTimeout);
             tc_fence_after_sync();
-            // P = S . M  (thread = query row, keys [64 half, 64 half + 64)), written
+            // P = S . M  (thread = query row, keys [32 part, 32 part + 32)), written
             // back packed (keys 2c, 2c+1 in one column) into columns
-            // [64 half, 64 half + 32): columns this thread has already read, so no
+            // [32 part, 32 part + 16): columns this thread has already read, so no
             // other thread's S is overwritten
             {
                 const int a = row;
+                uint32_t pk[16];
 #pragma unroll
-                for (int cc = 0; cc < 4; cc += 2) {
-                    uint32_t pk[16];
-                    const int c0 = half * 64 + cc * 16;
+                for (int q2 = 0; q2 < 2; q2++) {
+                    const int cb = part * 32 + q2 * 16;
                     // the loads are warp-collective: every lane issues them, whatever its row
-                    float r2[2][16];
-                    tmem_ld16(slot0 + lane_off + c0, r2[0]);
-                    tmem_ld16(slot0 + lane_off + c0 + 16, r2[1]);
+                    float r[16];
+                    tmem_ld16(slot0 + lane_off + cb, r);
                     tmem_ld_wait();
+                    __nv_bfloat162 h[8];
+                    if (cb > a || !row_ok) {  // strictly above the diagonal, or a row past T
 #pragma unroll
-                    for (int q2 = 0; q2 < 2; q2++) {
-                        const int cb = c0 + q2 * 16;
-                        const float *r = r2[q2];
-                        __nv_bfloat162 h[8];
-                        if (cb > a || !row_ok) {  // strictly above the diagonal, or a row past T
+                        for (int u = 0; u < 8; u++) h[u] = __floats2bfloat162_rn(0.f, 0.f);
+                    } else if (cb + 16 <= a) {
+                        // a whole 16-key chunk below the row: one level, and the decay
+                        // exp(gamma_a - gamma_b) = exp(gamma_a - gamma_e) exp(gamma_e - gamma_b)
+                        // with e = cb + 15, both factors <= 1
+                        const int lev = 32 - __clz(a ^ cb);
+                        const float ra = lam_a[lev] * __expf(gam_a - gam[cb + 15]);
+                        const float4 *kf4 = reinterpret_cast<const float4 *>(s.kf + cb);
 #pragma unroll
-                            for (int u = 0; u < 8; u++) h[u] = __floats2bfloat162_rn(0.f, 0.f);
-                        } else if (cb + 16 <= a) {
-                            // a whole 16-key chunk below the row: one level, and the decay
-                            // exp(gamma_a - gamma_b) = exp(gamma_a - gamma_e) exp(gamma_e - gamma_b)
-                            // with e = cb + 15, both factors <= 1
-                            const int lev = 32 - __clz(a ^ cb);
-                            const float ra = lam_a[lev] * __expf(gam_a - s.gam[sg][cb + 15]);
-#pragma unroll
-                            for (int u = 0; u < 8; u++)
-                                h[u] = __floats2bfloat162_rn(r[2 * u] * ra * s.kf[cb + 2 * u],
-                                                             r[2 * u + 1] * ra * s.kf[cb + 2 * u + 1]);
-                        } else {
-#pragma unroll
-                            for (int u = 0; u < 8; u++) {
-                                float x[2];
-#pragma unroll
-                                for (int e = 0; e < 2; e++) {
-                                    const int b = cb + 2 * u + e;
-                                    x[e] = 0.f;
-                                    if (b <= a) {
-                                        const int lev = 32 - __clz(a ^ b);
-                                        x[e] = r[2 * u + e] * lam_a[lev] * __expf(gam_a - s.gam[sg][b]);
-                                    }
-                                }
-                                h[u] = __floats2bfloat162_rn(x[0], x[1]);
-                            }
+                        for (int u = 0; u < 4; u++) {
+                            const float4 f = kf4[u];
+                            h[2 * u] = __floats2bfloat162_rn(r[4 * u] * ra * f.x, r[4 * u + 1] * ra * f.y);
+                            h[2 * u + 1] = __floats2bfloat162_rn(r[4 * u + 2] * ra * f.z, r[4 * u + 3] * ra * f.w);
                         }
+                    } else {
 #pragma unroll
-                        for (int u = 0; u < 8; u++) pk[q2 * 8 + u] = *reinterpret_cast<uint32_t *>(&h[u]);
+                        for (int u = 0; u < 8; u++) {
+                            float x[2];
+#pragma unroll
+                            for (int e = 0; e < 2; e++) {
+                                const int b = cb + 2 * u + e;
+                                x[e] = 0.f;
+                                if (b <= a) {
+                                    const int lev = 32 - __clz(a ^ b);
+                                    x[e] = r[2 * u + e] * lam_a[lev] * __expf(gam_a - gam[b]);
+                                }
+                            }
+                            h[u] = __floats2bfloat162_rn(x[0], x[1]);
+                        }
                     }
-                    tmem_st16(slot0 + lane_off + half * 64 + cc * 8, *reinterpret_cast<const float(*)[16]>(pk));
+#pragma unroll
+                    for (int u = 0; u < 8; u++) pk[q2 * 8 + u] = *reinterpret_cast<uint32_t *>(&h[u]);
                 }
+                tmem_st16(slot0 + lane_off + part * 32, *reinterpret_cast<const float(*)[16]>(pk));
             }
             tmem_st_wait();
             tc_fence_before_sync();
@@ -704,10 +705,8 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
             tc_fence_after_sync();
             float o[kCols];
 #pragma unroll
-            for (int c0 = 0; c0 < kCols; c0 += 32) {
-                tmem_ld16(slot1 + lane_off + half * kCols + c0, *reinterpret_cast<float(*)[16]>(o + c0));
-                tmem_ld16(slot1 + lane_off + half * kCols + c0 + 16, *reinterpret_cast<float(*)[16]>(o + c0 + 16));
-            }
+            for (int c0 = 0; c0 < kCols; c0 += 16)
+                tmem_ld16(slot1 + lane_off + part * kCols + c0, *reinterpret_cast<float(*)[16]>(o + c0));
             tmem_ld_wait();
             tc_fence_before_sync();
             mbar_arrive(&s.bar_pvfree);
@@ -727,20 +726,15 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
                     par_u ^= 1u << b;
                     tc_fence_after_sync();
                     const uint32_t sl = slot0 + 128 * b;
+                    float r[kCols];
 #pragma unroll
-                    for (int c0 = 0; c0 < kCols; c0 += 32) {
-                        float r2[2][16];
-                        tmem_ld16(sl + lane_off + half * kCols + c0, r2[0]);
-                        tmem_ld16(sl + lane_off + half * kCols + c0 + 16, r2[1]);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int u = 0; u < 16; u++) {
-                            o[c0 + u] = fmaf(wk, r2[0][u], o[c0 + u]);
-                            o[c0 + 16 + u] = fmaf(wk, r2[1][u], o[c0 + 16 + u]);
-                        }
-                    }
+                    for (int c0 = 0; c0 < kCols; c0 += 16)
+                        tmem_ld16(sl + lane_off + part * kCols + c0, *reinterpret_cast<float(*)[16]>(r + c0));
+                    tmem_ld_wait();
                     tc_fence_before_sync();
                     mbar_arrive(&s.bar_ufree[b]);
+#pragma unroll
+                    for (int u = 0; u < kCols; u++) o[u] = fmaf(wk, r[u], o[u]);
                 }
             }
             // every tensor-memory read of this tile is done: its region may take tile n+2
@@ -754,7 +748,7 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
                 // fp32: D/32 boxes of 32 columns x 128 rows, in q then k
 #pragma unroll
                 for (int c = 0; c < kCols / 4; c++) {
-                    const int cg = half * (kCols / 4) + c;  // 4-float chunk of the row
+                    const int cg = part * (kCols / 4) + c;  // 4-float chunk of the row
                     *reinterpret_cast<float4 *>(t.q + f32_stage_off(row, cg)) =
                         make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
                 }
@@ -762,7 +756,7 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
                 // bf16: D/64 blocks of 64 columns
 #pragma unroll
                 for (int c = 0; c < kCols / 8; c++) {
-                    const int cg = half * (kCols / 8) + c;  // 8-element chunk of the row
+                    const int cg = part * (kCols / 8) + c;  // 8-element chunk of the row
                     uint4 w4;
                     __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&w4);
 #pragma unroll
