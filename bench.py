@@ -426,7 +426,38 @@ def run_fwd_lines(dev, xd, cfg, ws, stream, hbm_peak, bf16_peak):
                                             out=out16, workspace=ws, stream=stream), stream, dev, 20)
     lines["bf16_out"] = fwd_line(f"{cfg.name} with bf16 out", cfg, ms, 2, hbm_peak, bf16_peak,
                                  {"l2": "inputs (436 MB) larger than L2, no flush"})
-    del out16
+    # lambda from the MLP (LambdaMLPSoftplus, d = k): in the read-out, against
+    # the two launches (producer writing lambda, then the forward reading it)
+    L = cfg.L
+    gw = torch.Generator().manual_seed(5)
+    W1 = (torch.randn((cfg.dk, 2 * L), generator=gw) / math.sqrt(cfg.dk)).to(dev)
+    W2 = (torch.randn((2 * L, L), generator=gw) / math.sqrt(2 * L)).to(dev)
+    bias = torch.full((L,), 0.54, device=dev)
+    out32 = torch.empty((cfg.B, cfg.H, cfg.T, cfg.dv), dtype=torch.float32, device=dev)
+    mws = torch.empty(binding.load().lla_fwd_lambda_mlp_workspace_bytes(
+        cfg.B, cfg.H, cfg.T, cfg.dk, cfg.dv, cfg.dk, cfg.chunk, binding.LLA_BF16), dtype=torch.uint8, device=dev)
+    ms_fused = time_fwd_calls(lambda: binding.fwd_lambda_mlp(
+        xd["q"], xd["k"], xd["v"], xd["g"], xd["k"], W1, W2, bias, chunk=cfg.chunk, out=out32, workspace=mws,
+        stream=stream), stream, dev, 20)
+    lam_buf = torch.empty((cfg.B, cfg.H, cfg.T, L), device=dev)
+
+    def pair():
+        binding.lambda_mlp(xd["k"], W1, W2, bias, out=lam_buf, stream=stream)
+        binding.fwd(xd["q"], xd["k"], xd["v"], xd["g"], lam_buf, chunk=cfg.chunk, out=out32, workspace=ws,
+                    stream=stream)
+    ms_pair = time_fwd_calls(pair, stream, dev, 20)
+    # compulsory bytes of the fused call: q, k, v, g in, out; no lambda in memory
+    per_tok = 3 * cfg.dk * 2 + 4 + cfg.dv * 4
+    nbytes = cfg.B * cfg.H * cfg.T * per_tok
+    gbs = nbytes / (ms_fused / 1e3) / 1e9
+    lines["lambda_mlp_fused"] = {
+        "workload": f"{cfg.name}, lambda = softplus((k W1) W2 + b) with hidden {2 * L}, fp32 out",
+        "ms": ms_fused, "tokens_per_s": cfg.tokens / (ms_fused / 1e3),
+        "ms_two_launches": ms_pair,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": gbs / hbm_peak, "algorithmic_bytes": nbytes},
+        "l2": "inputs larger than L2, no flush"}
+    del out32, mws, lam_buf
     flush = torch.zeros(64 << 20, dtype=torch.float32, device=dev)  # 256 MB, about twice L2
     for wname, reps in (("bf16_T8192_lam1", 20), ("bf16_T2048", 50)):
         c = W.FWD_CONFIGS[wname]

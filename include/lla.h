@@ -174,6 +174,33 @@ lla_status lla_fwd_noalloc(const void *q, const void *k, const void *v,
                            void *stream);
 
 /*
+ * lla_fwd with lambda produced by the two-layer MLP of "Adaptive memory decay
+ * for Log-Linear Attention" (§Method, LambdaMLPSoftplus) instead of passed in:
+ *     lambda_t = softplus((d_t W1) W2 + b),   width 2L hidden, L = lla_num_levels(T),
+ * then out = lla_fwd(q, k, v, g, lambda).  The same MLP as lla_lambda_mlp.
+ *   d  [B,H,T,Dd] in_dt     W1 [Dd,2L], W2 [2L,L], b [L] fp32 (shared by heads)
+ * Other arguments, layouts and errors as lla_fwd and lla_lambda_mlp.
+ * When d is the key tensor itself (d == k, Dd == dk) on the tensor-core
+ * shapes (bf16, dk = dv in {64,128}) with 2L <= 32 (T <= 32768), lambda is
+ * computed inside the read-out, from the key tile it already holds in shared
+ * memory (the first layer on the tensor cores with W1 split into two bf16
+ * parts, the second layer and softplus in fp32), and never goes to device
+ * memory.  Any other call runs lla_lambda_mlp into the workspace and then
+ * lla_fwd (the same results up to rounding, two passes over lambda).
+ * workspace: at least lla_fwd_lambda_mlp_workspace_bytes(...) bytes, enough
+ * for either way.
+ */
+size_t lla_fwd_lambda_mlp_workspace_bytes(int B, int H, int T, int dk, int dv, int Dd,
+                                          int chunk, lla_dtype in_dt);
+
+lla_status lla_fwd_lambda_mlp(const void *q, const void *k, const void *v, const float *g,
+                              const void *d, const float *W1, const float *W2,
+                              const float *b, void *out, int B, int H, int T, int dk, int dv,
+                              int Dd, int chunk, lla_dtype in_dt, lla_dtype out_dt,
+                              void *workspace, size_t workspace_bytes,
+                              int32_t *device_error, void *stream);
+
+/*
  * Decode state (the recurrent form of "Log-Linear Attention" §2.3: O(log T)
  * states, each step reads and updates O(log T) of them).  For one (b,h) at
  * token index t the state holds the Fenwick buckets of the prefix [0,t):

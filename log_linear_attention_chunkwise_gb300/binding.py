@@ -44,6 +44,8 @@ SIGNATURES = {
     "lla_fwd_host": (_I, [_P] * 6 + [_I] * 6 + [_I, _I, _I, _P, _Z, _P, _P]),
     "lla_gdn_decode_step": (_I, [_P] * 9 + [_I] * 5 + [_I, _P, _P]),
     "lla_device_error_check": (_I, [_P, _P, _P]),
+    "lla_fwd_lambda_mlp_workspace_bytes": (_Z, [_I] * 8),
+    "lla_fwd_lambda_mlp": (_I, [_P] * 9 + [_I] * 8 + [_I, _P, _Z, _P, _P]),
     "lla_debug_withhold_first_product": (None, [_I]),
 }
 
@@ -163,6 +165,39 @@ def fwd(q, k, v, g, lam, chunk: int = 64, out_dtype=torch.float32, out=None, wor
                      chunk, in_dt, _dt(out), _ptr(workspace), workspace.numel(),
                      _err_ptr(device_error), _stream(stream))
     _check("lla_fwd", rc)
+    return out
+
+
+def fwd_lambda_mlp(q, k, v, g, d, W1, W2, b, chunk: int = 64, out_dtype=torch.float32, out=None,
+                   workspace=None, device_error=None, stream=None):
+    """lla_fwd_lambda_mlp: the forward with lambda = softplus((d W1) W2 + b)
+    computed from d [B,H,T,Dd] (pass d = k for the in-kernel path);
+    W1 [Dd,2L], W2 [2L,L], b [L] fp32.  Returns out [B,H,T,dv]."""
+    lib = load()
+    for n, t in (("q", q), ("k", k), ("v", v), ("d", d)):
+        _need(t, n, q.dtype, 4)
+    _need(g, "g", torch.float32, 3)
+    for n, t in (("W1", W1), ("W2", W2), ("b", b)):
+        _need(t, n, torch.float32, None)
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    Dd = d.shape[-1]
+    L = lib.lla_num_levels(T)
+    if k.shape != q.shape or v.shape[:3] != (B, H, T) or g.shape != (B, H, T) or \
+            d.shape[:3] != (B, H, T) or W1.shape != (Dd, 2 * L) or W2.shape != (2 * L, L) or \
+            b.shape != (L,):
+        raise ValueError("inconsistent shapes")
+    if out is None:
+        out = torch.empty((B, H, T, dv), dtype=out_dtype, device=q.device)
+    _need(out, "out", None, 4)
+    in_dt = _dt(q)
+    need = lib.lla_fwd_lambda_mlp_workspace_bytes(B, H, T, dk, dv, Dd, chunk, in_dt)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    rc = lib.lla_fwd_lambda_mlp(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(d), _ptr(W1), _ptr(W2), _ptr(b),
+                                _ptr(out), B, H, T, dk, dv, Dd, chunk, in_dt, _dt(out), _ptr(workspace),
+                                workspace.numel(), _err_ptr(device_error), _stream(stream))
+    _check("lla_fwd_lambda_mlp", rc)
     return out
 
 

@@ -49,6 +49,7 @@ constexpr uint32_t kWaitIters = 1u << 22;  // bounded waits (~0.5 s with back-of
 constexpr uint32_t kWithheldWaitIters = 4096;  // the waits while the test hook withholds a product
 constexpr int kMaxPath = 17;               // levels of a tile index (T <= 2^24, so NT <= 2^17)
 constexpr int kLamMax = 25;                // lambda entries per token: L <= 1 + bit_length(2^24 - 1)
+constexpr int kMlpHidden = 32;             // hidden width of the in-kernel lambda MLP (2L <= 32)
 
 // Error codes (lla_device_error) written to the error word.
 constexpr int kErrLoadTimeout = LLA_DEVERR_COPY_TIMEOUT;
@@ -64,6 +65,10 @@ struct TcParams {
     float *segtot;          // [BH][nseg_full][D][D] decayed segment totals
     __nv_bfloat16 *node16;  // [BH][NT][D][D] Fenwick nodes (index 0 unused)
     int T, NT, BH, L, nseg_full;
+    // lambda from the two-layer MLP on the key tile ("Adaptive memory decay for
+    // Log-Linear Attention", LambdaMLPSoftplus) instead of a lambda input
+    const float *W1, *W2, *bmlp;  // [D][2L], [2L][L], [L] fp32
+    int mlp;
     uint32_t wait_iters;    // polls before a wait gives up
     uint32_t s_wait_iters;  // the same for the waits on S = Q K^T (short while it is withheld)
     int withhold;           // test hook: the consumer issues no S = Q K^T and no signal for it
@@ -379,16 +384,36 @@ struct __align__(1024) ConsStage {
     uint8_t v[kTile * D * 2];  // V, then path node 1, 3, ...
 };
 
+// Shared memory after the stages: either the lambda rows of each stage
+// ([128][L] fp32, loaded with the tile), or, with the in-kernel lambda MLP,
+// the first layer's weights as bf16 high and low parts in the K-major
+// swizzled layout of an MMA operand ([2][32 hidden][D]), the second layer
+// and bias (fp32) and one [128][L] staging of the tile's lambdas.
+template <int D>
+struct MlpLayout {
+    static constexpr uint32_t kW1Part = kMlpHidden * D * 2;
+    static constexpr uint32_t kW2 = 2 * kW1Part;                        // [2L][L] fp32
+    static constexpr uint32_t kBias = kW2 + kMlpHidden * 16 * 4;        // L <= 16
+    static constexpr uint32_t kLam = kBias + 16 * 4;                    // [128][L] fp32
+    static constexpr uint32_t kEnd = kLam + kTile * 16 * 4;
+};
+constexpr uint32_t kLamStage = kTile * kLamMax * 4;
+template <int D>
+constexpr uint32_t aux_bytes()
+{
+    return MlpLayout<D>::kEnd > 2 * kLamStage ? MlpLayout<D>::kEnd : 2 * kLamStage;
+}
+
 template <int D>
 struct __align__(1024) ConsSmem {
     ConsStage<D> st[2];
+    uint8_t aux[aux_bytes<D>()];    // lambda stages, or the MLP's weights and lambda staging
     float gam[2][kTile];
-    float lam[2][kTile * kLamMax];  // the tile's lambda rows, [128][L] dense
     float kf[kTile];                // exp(gamma_e - gamma_b), e = last key of b's 16-key chunk
     double pj[2][kMaxPath + 1];     // P at the path nodes of the stage's tile, then P_i
     int item[2];                    // the stage's work item, -1 when the queue is empty
     uint64_t bar_load[2], bar_sfree[2], bar_tfree[2];
-    uint64_t bar_s, bar_pready, bar_pv, bar_pvfree;
+    uint64_t bar_s, bar_pready, bar_pv, bar_pvfree, bar_h;
     uint64_t bar_node[2], bar_u[2], bar_ufree[2];
     uint32_t tmem;
 };
@@ -433,6 +458,7 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
         mbar_init(&s.bar_pready, kEpiThreads);
         mbar_init(&s.bar_pv, 1);
         mbar_init(&s.bar_pvfree, kEpiThreads);
+        mbar_init(&s.bar_h, 1);
         fence_mbar_init();
         tma_prefetch_map(&map_q);
         tma_prefetch_map(&map_k);
@@ -443,6 +469,27 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
     if (warp == 0) {
         tmem_alloc(&s.tmem, 512);
         tmem_relinquish();
+    }
+    using ML = MlpLayout<D>;
+    if (prm.mlp) {
+        // W1 split into bf16 high and low parts (together about 16 bits of every
+        // weight; the keys are exact in bf16), transposed into the K-major
+        // operand layout, hidden columns past 2L zero; W2 and the bias in fp32
+        const int Hd = 2 * L;
+        for (int e = tid; e < kMlpHidden * D; e += kConsThreads) {
+            const int n = e / D, kx = e % D;
+            const float w = n < Hd ? prm.W1[kx * Hd + n] : 0.f;
+            const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(w - __bfloat162float(hi));
+            const uint32_t off = (uint32_t)(kx >> 6) * (kMlpHidden * 128) + sw128_offset(n, (kx & 63) >> 3) +
+                                 (kx & 7) * 2;
+            *reinterpret_cast<__nv_bfloat16 *>(s.aux + off) = hi;
+            *reinterpret_cast<__nv_bfloat16 *>(s.aux + ML::kW1Part + off) = lo;
+        }
+        float *w2 = reinterpret_cast<float *>(s.aux + ML::kW2);  // [32][L], rows past 2L zero
+        for (int e = tid; e < kMlpHidden * L; e += kConsThreads) w2[e] = e < Hd * L ? prm.W2[e] : 0.f;
+        for (int e = tid; e < L; e += kConsThreads) reinterpret_cast<float *>(s.aux + ML::kBias)[e] = prm.bmlp[e];
+        fence_proxy_async_smem();
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -479,7 +526,7 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
             __syncwarp();
             if (lane == 0) {
                 const int rows = min(kTile, prm.T - i * kTile);
-                const uint32_t lam_bytes = (uint32_t)rows * L * 4;
+                const uint32_t lam_bytes = prm.mlp ? 0u : (uint32_t)rows * L * 4;
                 uint64_t *bar = &s.bar_load[sg];
                 mbar_arrive_expect_tx(bar, 3 * kT + lam_bytes + kTile * 4);
                 ConsStage<D> &t = s.st[sg];
@@ -490,7 +537,8 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
                     tma_load_3d(t.v + h * kBlk, &map_v, bar, h * 64, i * kTile, bh);
                 }
                 const long long tok0 = (long long)bh * prm.T + (long long)i * kTile;
-                bulk_load(s.lam[sg], prm.lam + tok0 * L, lam_bytes, bar);
+                if (!prm.mlp)
+                    bulk_load(s.aux + sg * kLamStage, prm.lam + tok0 * L, lam_bytes, bar);
                 bulk_load(s.gam[sg], prm.gamma + ((long long)bh * NT + i) * kTile, kTile * 4, bar);
             }
             // the tile's path nodes into L2 ahead of their loads (lane c: node c);
@@ -509,6 +557,20 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
         if (lane == 0) {
             const uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
             const uint32_t id_kmn = idesc_bf16_f32(128, D, false, true);
+            const uint32_t id_h = idesc_bf16_f32(128, kMlpHidden, false, false);
+            // h = K W1 (both parts, one accumulator) into slot 1 of the tile's region
+            auto issue_h = [&](uint32_t slot1, const uint8_t *kt) {
+#pragma unroll
+                for (int p = 0; p < 2; p++)
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; kk++) {
+                        const uint32_t offa = (kk >> 2) * kBlk + (kk & 3) * 32;
+                        const uint32_t offb = p * ML::kW1Part + (kk >> 2) * (kMlpHidden * 128) + (kk & 3) * 32;
+                        umma_bf16(slot1, desc_sw128(smem_u32(kt) + offa, 16, 1024),
+                                  desc_sw128(smem_u32(s.aux) + offb, 16, 1024), id_h, (p | kk) ? 1u : 0u);
+                    }
+                umma_commit(&s.bar_h);
+            };
             // parities of the completions so far of bar_node[b] and bar_u[b] (bit b):
             // only parities are ever waited on
             uint32_t par_node = 0, par_u = 0;
@@ -548,9 +610,12 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
                 };
                 // parity of the completion of the latest U issued into slot b
                 auto last_u_par = [&](int b) { return ((par_u >> b) & 1) ^ 1; };
-                if (!s_early && !prm.withhold) {  // withheld: nothing is left in flight, the waits on bar_s run out
-                    mma_kk<D>(slot0, t.q, t.k, id_s);
-                    umma_commit(&s.bar_s);
+                if (!s_early) {
+                    if (!prm.withhold) {  // withheld: nothing is left in flight, the waits on bar_s run out
+                        mma_kk<D>(slot0, t.q, t.k, id_s);
+                        umma_commit(&s.bar_s);
+                    }
+                    if (prm.mlp) issue_h(slot0 + 128, t.k);
                 }
                 s_early = false;
                 int jnext = i;
@@ -594,6 +659,7 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
                             mma_kk<D>(tm + sg1 * kRegion, s.st[sg1].q, s.st[sg1].k, id_s);
                             umma_commit(&s.bar_s);
                         }
+                        if (prm.mlp) issue_h(tm + sg1 * kRegion + 128, s.st[sg1].k);
                         s_early = true;
                     }
                 }
@@ -639,8 +705,30 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
             const bool row_ok = row < prm.T - i * kTile;
             const float *gam = s.gam[sg];
             const float gam_a = gam[row];
-            const float *lam_a = s.lam[sg] + row * L;
             const uint32_t slot0 = tm + sg * kRegion, slot1 = slot0 + 128;
+            const float *lam_a;
+            if (prm.mlp) {
+                // lambda_l = softplus(b_l + sum_j h_j W2[j][l]) for l = part, part + 4, ...;
+                // h (the row's 2L hidden values) from tensor memory
+                if (!mbar_wait(&s.bar_h, n & 1, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
+                tc_fence_after_sync();
+                float h[kMlpHidden];
+                tmem_ld16(slot1 + lane_off, *reinterpret_cast<float(*)[16]>(h));
+                tmem_ld16(slot1 + lane_off + 16, *reinterpret_cast<float(*)[16]>(h + 16));
+                tmem_ld_wait();
+                const float *w2 = reinterpret_cast<const float *>(s.aux + ML::kW2);
+                const float *bs = reinterpret_cast<const float *>(s.aux + ML::kBias);
+                float *lst = reinterpret_cast<float *>(s.aux + ML::kLam);
+                for (int l = part; l < L; l += kParts) {
+                    float z = bs[l];
+#pragma unroll
+                    for (int jh = 0; jh < kMlpHidden; jh++) z = fmaf(h[jh], w2[jh * L + l], z);
+                    lst[row * L + l] = fmaxf(z, 0.f) + log1pf(__expf(-fabsf(z)));
+                }
+                lam_a = lst + row * L;
+            } else {
+                lam_a = reinterpret_cast<const float *>(s.aux + sg * kLamStage) + row * L;
+            }
             if (part == 0) s.kf[row] = __expf(gam[row | 15] - gam_a);
             epi_sync();
             if (!mbar_wait(&s.bar_s, n & 1, prm.s_wait_iters)) set_err(prm.err, kErrMmaTimeout);
@@ -905,6 +993,11 @@ bool tc_supported(int dk, int dv, lla_dtype in_dt)
     return in_dt == LLA_BF16 && dk == dv && (dk == 64 || dk == 128);
 }
 
+bool tc_mlp_supported(int dk, int dv, lla_dtype in_dt, int L)
+{
+    return tc_supported(dk, dv, in_dt) && 2 * L <= kMlpHidden;
+}
+
 int tc_launches(int T)
 {
     const int NT = (T + kTile - 1) / kTile;
@@ -914,6 +1007,7 @@ int tc_launches(int T)
 
 static_assert(sizeof(WalkSmem<128>) + 1024 <= 113 * 1024, "walker must fit two CTAs per SM");
 static_assert(sizeof(ConsSmem<128>) + 1024 <= 227 * 1024, "consumer must fit the shared memory of an SM");
+static_assert(MlpLayout<128>::kW2 % 1024 == 0, "the MLP's weight parts are whole swizzle atoms");
 
 // Launch configuration, optionally as a programmatic dependent of the
 // previous kernel in the stream (it may start before that one finishes and
@@ -981,6 +1075,10 @@ static cudaError_t tc_fwd_d(const TcFwdArgs &A)
     prm.BH = BH;
     prm.L = A.L;
     prm.nseg_full = nseg_full_of(NT);
+    prm.W1 = A.W1;
+    prm.W2 = A.W2;
+    prm.bmlp = A.bmlp;
+    prm.mlp = A.W1 != nullptr ? 1 : 0;
     prm.withhold = g_withhold_first_product.load();
     prm.wait_iters = kWaitIters;
     prm.s_wait_iters = prm.withhold ? kWithheldWaitIters : kWaitIters;

@@ -158,6 +158,50 @@ lla_status lla_fwd(const void *q, const void *k, const void *v, const float *g,
     return simt_fwd(A) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
 }
 
+size_t lla_fwd_lambda_mlp_workspace_bytes(int B, int H, int T, int dk, int dv, int Dd, int chunk,
+                                          lla_dtype in_dt)
+{
+    if (Dd < 1 || Dd > 256) return 0;
+    const size_t fwd = lla_fwd_workspace_bytes(B, H, T, dk, dv, chunk, in_dt);
+    if (fwd == 0) return 0;
+    // lambda staged in the workspace when it cannot be computed in the read-out
+    const size_t lam = align_up((size_t)B * H * T * lla_num_levels(T) * sizeof(float), 256);
+    return lam + fwd;
+}
+
+lla_status lla_fwd_lambda_mlp(const void *q, const void *k, const void *v, const float *g,
+                              const void *d, const float *W1, const float *W2, const float *b,
+                              void *out, int B, int H, int T, int dk, int dv, int Dd, int chunk,
+                              lla_dtype in_dt, lla_dtype out_dt, void *workspace,
+                              size_t workspace_bytes, int32_t *device_error, void *stream)
+{
+    // lla_fwd's checks with a stand-in lambda pointer (lambda is not an input here)
+    bool empty = false;
+    lla_status st = fwd_args_status(q, k, v, g, g, out, B, H, T, dk, dv, chunk, in_dt, out_dt,
+                                    &empty);
+    if (st != LLA_OK || empty) return st;
+    const int L = lla_num_levels(T);
+    if (Dd < 1 || Dd > 256 || L > 32) return LLA_ERR_UNSUPPORTED_SHAPE;
+    if (!d || !W1 || !W2 || !b || !aligned16(d)) return LLA_ERR_INVALID_ARGUMENT;
+    const size_t need = lla_fwd_lambda_mlp_workspace_bytes(B, H, T, dk, dv, Dd, chunk, in_dt);
+    if (workspace_bytes < need) return LLA_ERR_WORKSPACE_TOO_SMALL;
+    if (workspace == nullptr || ((uintptr_t)workspace & 255u) != 0) return LLA_ERR_INVALID_ARGUMENT;
+    if (d == k && Dd == dk && tc_mlp_supported(dk, dv, in_dt, L)) {
+        TcFwdArgs A;
+        A.q = q; A.k = k; A.v = v; A.g = g; A.lam = nullptr; A.out = out;
+        A.B = B; A.H = H; A.T = T; A.L = L; A.dk = dk; A.out_dt = out_dt;
+        A.W1 = W1; A.W2 = W2; A.bmlp = b;
+        A.workspace = workspace; A.device_error = device_error; A.stream = stream;
+        return tc_fwd(A) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+    }
+    float *lam = (float *)workspace;
+    const size_t lam_bytes = align_up((size_t)B * H * T * L * sizeof(float), 256);
+    st = lla_lambda_mlp(d, W1, W2, b, lam, B, H, T, Dd, L, in_dt, device_error, stream);
+    if (st != LLA_OK) return st;
+    return lla_fwd(q, k, v, g, lam, out, B, H, T, dk, dv, chunk, in_dt, out_dt,
+                   (char *)workspace + lam_bytes, workspace_bytes - lam_bytes, device_error, stream);
+}
+
 size_t lla_decode_state_bytes(int B, int H, int dk, int dv, int Ls)
 {
     if (B < 0 || H < 0 || dk < 0 || dv < 0 || Ls < 0) return 0;

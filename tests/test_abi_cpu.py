@@ -162,3 +162,23 @@ def test_noalloc_checks_arguments_in_lla_fwd_order(lib):
     assert noalloc(ptr=ctypes.c_void_p(8), d=128, **big) == 1
     assert noalloc(out_dt=9, d=128, **big) == 1
     assert noalloc(B=0, ptr=ctypes.c_void_p(0)) == 0
+
+
+def test_fwd_lambda_mlp_validation(lib):
+    p = ctypes.c_void_p(256)
+
+    def call(d=p, Dd=64, T=64, dk=64, ws=1 << 30, wsp=p, W1=p):
+        return lib.lla_fwd_lambda_mlp(p, p, p, p, d, W1, p, p, p, 1, 1, T, dk, dk, Dd, 64, 1, 0,
+                                      wsp, ws, NULL, NULL)
+    assert call(Dd=0) == 2
+    assert call(Dd=300) == 2
+    assert call(dk=48) == 2
+    assert call(d=NULL) == 1
+    assert call(W1=NULL) == 1
+    assert call(d=ctypes.c_void_p(256 + 8)) == 1
+    assert call(ws=0) == 3
+    assert call(wsp=ctypes.c_void_p(256 + 16)) == 1
+    # enough for lambda staged in the workspace plus the forward's own workspace
+    n = lib.lla_fwd_lambda_mlp_workspace_bytes(2, 3, 2048, 128, 128, 128, 64, 1)
+    assert n >= 2 * 3 * 2048 * 12 * 4 + lib.lla_fwd_workspace_bytes(2, 3, 2048, 128, 128, 64, 1)
+    assert lib.lla_fwd_lambda_mlp_workspace_bytes(2, 3, 2048, 128, 128, 0, 64, 1) == 0

@@ -95,3 +95,49 @@ def test_lambda_mlp_at_the_32k_workload_sampled_rows():
     flat = lam.reshape(-1, cfg.L).cpu()[rows]
     ref = oracle.lambda_mlp(k.reshape(-1, 128)[rows], W1, W2, b)
     np.testing.assert_allclose(flat.double().numpy(), ref, rtol=2e-5, atol=2e-6)
+
+
+def _fused_case(B, H, T, d, seed, separate_d=False, out_dtype=torch.float32):
+    cfg = W.small_fwd_config(B, H, T, d, d, 64, torch.bfloat16, seed=seed)
+    x = W.make_fwd_inputs(cfg)
+    L = cfg.L
+    W1, W2, b = weights(d, L, seed=seed + 1)
+    dd = x["k"].clone() if separate_d else x["k"]
+    lam_ref = oracle.lambda_mlp(dd, W1, W2, b)
+    ref = oracle.naive(x["q"], x["k"], x["v"], x["g"], lam_ref)
+    xd = {n: t.cuda() for n, t in x.items()}
+    d_dev = dd.cuda() if separate_d else xd["k"]
+    out = binding.fwd_lambda_mlp(xd["q"], xd["k"], xd["v"], xd["g"], d_dev, W1.cuda(), W2.cuda(), b.cuda(),
+                                 chunk=64, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    return out, ref
+
+
+@pytest.mark.parametrize("B,H,T,d", [(1, 2, 384, 128), (2, 2, 2048, 128), (1, 3, 1088, 64),
+                                     (2, 2, 256, 64), (1, 1, 64, 128), (1, 2, 4224, 128)])
+def test_fwd_lambda_mlp_in_the_read_out(B, H, T, d):
+    """d = k on the tensor-core shapes: lambda computed inside the read-out
+    from the key tile (never written to memory), against the oracle's MLP
+    followed by the oracle's double sum."""
+    out, ref = _fused_case(B, H, T, d, seed=T + d)
+    assert_parity(out, ref, torch.bfloat16, f"fused lambda MLP {(B, H, T, d)}")
+
+
+def test_fwd_lambda_mlp_two_pass_path_agrees():
+    """A separate d tensor (same values as k) takes the two-pass path; both
+    paths match the oracle, and each other to rounding."""
+    out_sep, ref = _fused_case(1, 2, 1024, 128, seed=9, separate_d=True)
+    out_fused, _ = _fused_case(1, 2, 1024, 128, seed=9)
+    assert_parity(out_sep, ref, torch.bfloat16, "two-pass lambda MLP")
+    assert_parity(out_fused, ref, torch.bfloat16, "fused lambda MLP")
+    assert float((out_sep - out_fused).abs().max()) <= 1e-2
+
+
+def test_fwd_lambda_mlp_bf16_out_and_cuda_core_shapes():
+    out, ref = _fused_case(1, 2, 640, 64, seed=3, out_dtype=torch.bfloat16)
+    assert out.dtype == torch.bfloat16
+    d = out.double().cpu().numpy() - ref
+    assert np.linalg.norm(d) / np.linalg.norm(ref) <= 5e-3
+    # dk = 32 has no tensor-core path: the MLP runs first, then the CUDA-core forward
+    out, ref = _fused_case(1, 2, 256, 32, seed=4)
+    assert_parity(out, ref, torch.bfloat16, "lambda MLP, CUDA-core forward")
