@@ -104,18 +104,20 @@ __device__ __forceinline__ void mma_kmn(uint32_t d, const uint8_t *a, const uint
 
 // ======================================================= node walkers
 // The tile-level Fenwick nodes Node_j (j = 1 .. NT-1) are built by walkers:
-// one CTA per (batch*head, 32-column slice of dv, segment of 32 tiles) goes
-// through its segment in order.  For tile i it forms H_i's slice on the
-// tensor cores and closes Node_{i+1}:
+// one CTA per (batch*head, segment of 8 tiles) goes through its segment in
+// order.  For tile i it forms the whole state H_i (D x D) on the tensor
+// cores and closes Node_{i+1}:
 //     Node_{i+1} = H_i + sum_{m < ctz(i+1)} exp(P_{i+1} - P_{i+1-2^m}) Node_{i+1-2^m},
-// keeping the latest node of each level (the Fenwick stack) in fp32 in
-// tensor memory, so nothing crosses CTAs and nothing waits.  Only the node
-// that closes a full segment reaches back before the segment; the walker
-// writes that segment's decayed total instead, and the fix-up kernel chains
-// the totals at segment granularity.  Nodes are published in bf16, the
-// read-out's MMA operand.  For D = 64 the product's M (= dk) is padded to
-// 128: the second 64-row block of the K^T operand reads whatever shared
-// memory follows the tile, and those rows of H are never read.
+// keeping the latest node of each level (the Fenwick stack, three levels) in
+// fp32 in tensor memory, so nothing crosses CTAs and nothing waits.  Only
+// the node that closes a full segment reaches back before the segment; the
+// walker writes that segment's decayed total instead, and the fix-up kernel
+// forms the nodes at segment granularity from the totals.  Nodes are
+// published in bf16, the read-out's MMA operand.  Each K and V tile is read
+// once; a ring of three tiles keeps the loads in flight.  For D = 64 the
+// product's M (= dk) is padded to 128: the second 64-row block of the K^T
+// operand reads whatever shared memory follows the tile, and those rows of
+// H are never read.
 
 // fp32 tile of 128 rows staged as 32-column boxes of 128 rows x 128 B:
 // byte offset of the 4-float chunk holding columns [4c, 4c+4) of row r.
@@ -124,59 +126,61 @@ __device__ __forceinline__ uint32_t f32_stage_off(int r, int c)
     return (uint32_t)(c >> 3) * (kTile * 128) + sw128_offset(r, c & 7);
 }
 
-constexpr int kSliceW = 32;              // dv columns per walker
-constexpr int kSegLog = 5;
+constexpr int kSegLog = 3;
 constexpr int kSeg = 1 << kSegLog;       // tiles per segment
-constexpr int kWalkStages = 2;           // K/V tiles in flight per walker (2 walkers per SM)
+constexpr int kWalkStages = 3;           // K/V tiles in flight per walker
 constexpr int kWalkThreads = 256;        // warps 0-3: node epilogue; warps 4-7: tile preparation
 
 template <int D>
 struct __align__(1024) WalkSmem {
     uint8_t k[kWalkStages][kTile * D * 2];  // K tiles
-    uint8_t v[kWalkStages][kBlk];           // the 64-column V block holding the slice
+    uint8_t v[kWalkStages][kTile * D * 2];  // V tiles, scaled in place by exp(Gam - gamma)
     float gm[kWalkStages][kTile];           // the tile's inclusive gate sums gamma
     double P[kSeg + 1];                     // P_{i0} .. P_{i0+kSeg}
-    uint64_t bar_load[kWalkStages], bar_h[2], bar_hfree[2];
+    uint64_t bar_load[kWalkStages], bar_h, bar_hfree;
     uint32_t tmem;
 };
 
+// tensor-memory columns of a walker: the stack's kSegLog levels and H, D each
+template <int D>
+constexpr uint32_t walk_tmem_cols()
+{
+    return (kSegLog + 1) * D <= 256 ? 256u : 512u;
+}
+
 __device__ __forceinline__ void prep_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-// Warp-specialised: the preparation warps (thread = token row) load gates,
-// scale the V slice by exp(Gam - gamma) and issue the state product of tile
-// n while the epilogue warps (thread = dk row) fold tile n-1's state into
-// the Fenwick stack; TMA keeps kWalkStages tiles in flight.
+// Warp-specialised: the preparation warps (thread = token row) scale V by
+// exp(Gam - gamma) and issue the state product of tile n while the epilogue
+// warps (thread = dk row) fold tile n-1's state into the Fenwick stack.
 template <int D>
-__global__ void __launch_bounds__(kWalkThreads, 2)
+__global__ void __launch_bounds__(kWalkThreads, 1)
 lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                        const TcParams prm)
 {
+    constexpr uint32_t kT = kTile * D * 2;
     extern __shared__ uint8_t smem_raw[];
     WalkSmem<D> &s = *reinterpret_cast<WalkSmem<D> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                       ~uintptr_t(1023));
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
-    const int seg = blockIdx.x, slice = blockIdx.y, bh = blockIdx.z;
+    const int seg = blockIdx.x, bh = blockIdx.y;
     const int NT = prm.NT;
     const int i0 = seg * kSeg, i1 = min(i0 + kSeg, NT - 1);  // tiles i0..i1-1 close Node_{i+1}
     const int ntiles = i1 - i0;
     const double *Pb = prm.P + (long long)bh * (NT + 1);
-    const int vblk = slice >> 1;                       // 64-column V block holding the slice
-    const uint32_t voff = (uint32_t)(slice & 1) * 64;  // the slice's byte offset in a block row
 
     grid_launch_dependents();  // the fix-up and read-out may start in this grid's tail
     if (tid == 0) {
         for (int b = 0; b < kWalkStages; b++) mbar_init(&s.bar_load[b], 1);
-        for (int b = 0; b < 2; b++) {
-            mbar_init(&s.bar_h[b], 1);
-            mbar_init(&s.bar_hfree[b], D);
-        }
+        mbar_init(&s.bar_h, 1);
+        mbar_init(&s.bar_hfree, D);
         fence_mbar_init();
         tma_prefetch_map(&map_k);
         tma_prefetch_map(&map_v);
     }
     if (warp == 0) {
-        tmem_alloc(&s.tmem, 256);
+        tmem_alloc(&s.tmem, walk_tmem_cols<D>());
         tmem_relinquish();
     }
     for (int j = tid; j <= kSeg; j += kWalkThreads) s.P[j] = (i0 + j <= NT) ? Pb[i0 + j] : 0.0;
@@ -184,16 +188,18 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tm = s.tmem;
-    // columns: stack level m at [32m, 32m+32) for m < kSegLog; two H buffers after it
-    const uint32_t tm_h0 = tm + kSegLog * kSliceW;
+    // columns: stack level m at [D m, D m + D) for m < kSegLog; H after it
+    const uint32_t tm_h = tm + kSegLog * D;
 
     // a tile's 128 gamma values are one aligned 512-byte run
     auto issue_load = [&](int n) {
         const int ls = n % kWalkStages, i = i0 + n;
-        mbar_arrive_expect_tx(&s.bar_load[ls], kTile * D * 2 + kBlk + kTile * 4);
+        mbar_arrive_expect_tx(&s.bar_load[ls], 2 * kT + kTile * 4);
 #pragma unroll
-        for (int h = 0; h < D / 64; h++) tma_load_3d(s.k[ls] + h * kBlk, &map_k, &s.bar_load[ls], h * 64, i * kTile, bh);
-        tma_load_3d(s.v[ls], &map_v, &s.bar_load[ls], vblk * 64, i * kTile, bh);
+        for (int h = 0; h < D / 64; h++) {
+            tma_load_3d(s.k[ls] + h * kBlk, &map_k, &s.bar_load[ls], h * 64, i * kTile, bh);
+            tma_load_3d(s.v[ls] + h * kBlk, &map_v, &s.bar_load[ls], h * 64, i * kTile, bh);
+        }
         bulk_load(s.gm[ls], prm.gamma + ((long long)bh * NT + i) * kTile, kTile * 4, &s.bar_load[ls]);
     };
 
@@ -203,20 +209,20 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
         if (p == 0)
             for (int n = 0; n < min(kWalkStages, ntiles); n++) issue_load(n);
         for (int n = 0; n < ntiles; n++) {
-            const int ls = n % kWalkStages, hb = n & 1;
+            const int ls = n % kWalkStages;
             if (p == 0 && n >= 1 && n - 1 + kWalkStages < ntiles) {
                 // stage of tile n-1 is free once its product is done
-                if (!mbar_wait(&s.bar_h[(n - 1) & 1], ((n - 1) >> 1) & 1, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
+                if (!mbar_wait(&s.bar_h, (n - 1) & 1, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
                 issue_load(n - 1 + kWalkStages);
             }
             if (!mbar_wait(&s.bar_load[ls], (n / kWalkStages) & 1, prm.wait_iters)) set_err(prm.err, kErrLoadTimeout);
             const float Gam = s.gm[ls][kTile - 1];
             const float gam_a = s.gm[ls][p];
-            {   // V row p of the slice, scaled in place by exp(Gam - gamma)
+            {   // V row p, scaled in place by exp(Gam - gamma)
                 const float w = __expf(Gam - gam_a);
 #pragma unroll
-                for (int c = 0; c < 4; c++) {
-                    uint4 *q4 = reinterpret_cast<uint4 *>(s.v[ls] + sw128_offset(p, (voff >> 4) + c));
+                for (int c = 0; c < D / 8; c++) {
+                    uint4 *q4 = reinterpret_cast<uint4 *>(s.v[ls] + (c >> 3) * kBlk + sw128_offset(p, c & 7));
                     uint4 raw = *q4;
                     __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&raw);
 #pragma unroll
@@ -230,127 +236,134 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
             fence_proxy_async_smem();
             prep_sync();
             if (p == 0) {
-                if (n >= 2 && !mbar_wait(&s.bar_hfree[hb], ((n - 2) >> 1) & 1, prm.wait_iters))
+                // H (one accumulator) is free once the epilogue has drained tile n-1's
+                if (n >= 1 && !mbar_wait(&s.bar_hfree, (n - 1) & 1, prm.wait_iters))
                     set_err(prm.err, kErrMmaTimeout);
                 tc_fence_after_sync();
-                // H slice = K^T Vs: A = K^T (M = 128 >= dk, MN-major), B = Vs slice (N = 32, MN-major)
-                const uint32_t idesc = idesc_bf16_f32(128, kSliceW, true, true);
+                // H = K^T Vs: A = K^T (M = 128 >= dk, MN-major), B = Vs (N = D, MN-major)
+                const uint32_t idesc = idesc_bf16_f32(128, D, true, true);
 #pragma unroll
                 for (int kk = 0; kk < 8; kk++) {
                     const uint32_t off = kk * 2048;
-                    umma_bf16(tm_h0 + hb * kSliceW, desc_sw128(smem_u32(s.k[ls]) + off, kBlk, 1024),
-                              desc_sw128(smem_u32(s.v[ls]) + voff + off, kBlk, 1024), idesc,
-                              kk > 0 ? 1u : 0u);
+                    umma_bf16(tm_h, desc_sw128(smem_u32(s.k[ls]) + off, kBlk, 1024),
+                              desc_sw128(smem_u32(s.v[ls]) + off, kBlk, 1024), idesc, kk > 0 ? 1u : 0u);
                 }
-                umma_commit(&s.bar_h[hb]);
+                umma_commit(&s.bar_h);
             }
         }
     } else if (tid < D) {
-        // ---------------- epilogue warps: thread = dk row `tid`, the slice's 32 columns
+        // ---------------- epilogue warps: thread = dk row `tid`, all D columns
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
         for (int n = 0; n < ntiles; n++) {
-            const int hb = n & 1;
             const int J = i0 + n + 1;
             const int z = __ffs(J) - 1;
             const bool cross = (J == i0 + kSeg);  // closes a full segment
             const int mlim = cross ? kSegLog : z;
-            if (!mbar_wait(&s.bar_h[hb], (n >> 1) & 1, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
+            if (!mbar_wait(&s.bar_h, n & 1, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
             tc_fence_after_sync();
-            float acc[32];
-            tmem_ld16(tm_h0 + hb * kSliceW + lane_off, *reinterpret_cast<float(*)[16]>(acc));
-            tmem_ld16(tm_h0 + hb * kSliceW + lane_off + 16, *reinterpret_cast<float(*)[16]>(acc + 16));
+            float acc[D];
+#pragma unroll
+            for (int c = 0; c < D; c += 16) tmem_ld16(tm_h + lane_off + c, *reinterpret_cast<float(*)[16]>(acc + c));
             tmem_ld_wait();
             tc_fence_before_sync();
-            mbar_arrive(&s.bar_hfree[hb]);
+            mbar_arrive(&s.bar_hfree);  // the next tile's product may overwrite H
             const double PJ = s.P[J - i0];
             for (int m = 0; m < mlim; m++) {
                 const float f = __expf((float)(PJ - s.P[J - (1 << m) - i0]));
-                float x[32];
-                tmem_ld16(tm + m * kSliceW + lane_off, *reinterpret_cast<float(*)[16]>(x));
-                tmem_ld16(tm + m * kSliceW + lane_off + 16, *reinterpret_cast<float(*)[16]>(x + 16));
-                tmem_ld_wait();
 #pragma unroll
-                for (int u = 0; u < 32; u++) acc[u] = fmaf(f, x[u], acc[u]);
+                for (int c = 0; c < D; c += 32) {
+                    float x[32];
+                    tmem_ld16(tm + m * D + lane_off + c, *reinterpret_cast<float(*)[16]>(x));
+                    tmem_ld16(tm + m * D + lane_off + c + 16, *reinterpret_cast<float(*)[16]>(x + 16));
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int u = 0; u < 32; u++) acc[c + u] = fmaf(f, x[u], acc[c + u]);
+                }
             }
             if (!cross) {
                 if (z < kSegLog) {
-                    tmem_st16(tm + z * kSliceW + lane_off, *reinterpret_cast<float(*)[16]>(acc));
-                    tmem_st16(tm + z * kSliceW + lane_off + 16, *reinterpret_cast<float(*)[16]>(acc + 16));
+#pragma unroll
+                    for (int c = 0; c < D; c += 16)
+                        tmem_st16(tm + z * D + lane_off + c, *reinterpret_cast<float(*)[16]>(acc + c));
                     tmem_st_wait();
                 }
-                uint4 w[4];
-                __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(w);
+                uint4 *dst = reinterpret_cast<uint4 *>(prm.node16 + (((long long)bh * NT + J) * D + tid) * D);
 #pragma unroll
-                for (int u = 0; u < 16; u++) h[u] = __floats2bfloat162_rn(acc[2 * u], acc[2 * u + 1]);
-                uint4 *dst = reinterpret_cast<uint4 *>(prm.node16 + (((long long)bh * NT + J) * D + tid) * D +
-                                                       slice * kSliceW);
+                for (int c = 0; c < D / 8; c++) {
+                    uint4 w;
+                    __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&w);
 #pragma unroll
-                for (int u = 0; u < 4; u++) dst[u] = w[u];
+                    for (int u = 0; u < 4; u++) h[u] = __floats2bfloat162_rn(acc[8 * c + 2 * u], acc[8 * c + 2 * u + 1]);
+                    dst[c] = w;
+                }
             } else {
                 float4 *dst = reinterpret_cast<float4 *>(
-                    prm.segtot + ((((long long)bh * prm.nseg_full + seg) * D + tid) * D + slice * kSliceW));
+                    prm.segtot + (((long long)bh * prm.nseg_full + seg) * D + tid) * D);
 #pragma unroll
-                for (int u = 0; u < 8; u++)
+                for (int u = 0; u < D / 4; u++)
                     dst[u] = make_float4(acc[4 * u], acc[4 * u + 1], acc[4 * u + 2], acc[4 * u + 3]);
             }
         }
     }
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tm, 256);
+    if (warp == 0) tmem_dealloc(tm, walk_tmem_cols<D>());
 }
 
-// Nodes that close full segments: Fenwick chain over the segment totals,
-//   Node_{(u)SEG} = Tot_{u-1} + sum_{k < ctz(u)} exp(P_{uSEG} - P_{(u-2^k)SEG}) Node_{(u-2^k)SEG},
-// eight state elements per thread, the open node of each level in
-// registers, the decay factors in shared memory.
+// Nodes that close full segments, each on its own from the segment totals:
+// node u SEG covers segments [u - lowbit(u), u), so
+//   Node_{u SEG} = sum_{sigma in [u - lowbit(u), u)} exp(P_{u SEG} - P_{(sigma+1) SEG}) Tot_sigma.
+// One CTA per (256 x 8 state elements, u, batch*head); the totals' loads of a
+// thread are all issued before they are summed.
 constexpr int kFixThreads = 256;
-constexpr int kFixMaxZ = 12;    // levels of a segment index: (2^24/128)/32 segments < 2^12
-constexpr int kFixMaxSeg = 4096;
 template <int D>
 __global__ void __launch_bounds__(kFixThreads)
 lla_node_fixup_kernel(const TcParams prm)
 {
-    __shared__ double pseg[kFixMaxSeg + 1];  // P at segment boundaries
     grid_launch_dependents();
     grid_dependency_wait();  // the walkers' segment totals
-    const long long bh = blockIdx.y;
+    const long long bh = blockIdx.z;
+    const int u = blockIdx.y + 1;
     const int NT = prm.NT, nseg = prm.nseg_full;
-    const double *Pb = prm.P + bh * (NT + 1);
-    for (int u = threadIdx.x; u <= nseg; u += kFixThreads) pseg[u] = Pb[u * kSeg];
-    __syncthreads();
     const int e0 = (blockIdx.x * kFixThreads + threadIdx.x) * 8;  // 8 consecutive elements
     if (e0 >= D * D) return;
-    float stack[kFixMaxZ][8];
+    const double *Pb = prm.P + bh * (NT + 1);
+    const double Pu = Pb[u * kSeg];
+    const int first = u - (u & -u);
+    float val[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int s0 = first; s0 < u; s0 += 8) {
+        float4 a[8], b[8];
+        float f[8];
 #pragma unroll
-    for (int k = 0; k < kFixMaxZ; k++)
-#pragma unroll
-        for (int c = 0; c < 8; c++) stack[k][c] = 0.f;
-    for (int u = 1; u <= nseg; u++) {
-        const int z = __ffs(u) - 1;
-        const float4 *src = reinterpret_cast<const float4 *>(prm.segtot + ((bh * nseg) + (u - 1)) * (D * D) + e0);
-        const float4 a = src[0], b = src[1];
-        float val[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-        for (int k = 0; k < kFixMaxZ; k++) {
-            if (k < z) {
-                const float f = __expf((float)(pseg[u] - pseg[u - (1 << k)]));
-#pragma unroll
-                for (int c = 0; c < 8; c++) val[c] = fmaf(f, stack[k][c], val[c]);
+        for (int q = 0; q < 8; q++) {
+            const int sg = s0 + q;
+            if (sg < u) {
+                const float4 *src = reinterpret_cast<const float4 *>(prm.segtot + ((bh * nseg) + sg) * (D * D) + e0);
+                a[q] = src[0];
+                b[q] = src[1];
+                f[q] = __expf((float)(Pu - Pb[(sg + 1) * kSeg]));
+            } else {
+                a[q] = b[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+                f[q] = 0.f;
             }
         }
 #pragma unroll
-        for (int k = 0; k < kFixMaxZ; k++)
-            if (k == z) {
-#pragma unroll
-                for (int c = 0; c < 8; c++) stack[k][c] = val[c];
-            }
-        uint4 w;
-        __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&w);
-#pragma unroll
-        for (int c = 0; c < 4; c++) h[c] = __floats2bfloat162_rn(val[2 * c], val[2 * c + 1]);
-        *reinterpret_cast<uint4 *>(prm.node16 + (bh * NT + (long long)u * kSeg) * (D * D) + e0) = w;
+        for (int q = 0; q < 8; q++) {
+            val[0] = fmaf(f[q], a[q].x, val[0]);
+            val[1] = fmaf(f[q], a[q].y, val[1]);
+            val[2] = fmaf(f[q], a[q].z, val[2]);
+            val[3] = fmaf(f[q], a[q].w, val[3]);
+            val[4] = fmaf(f[q], b[q].x, val[4]);
+            val[5] = fmaf(f[q], b[q].y, val[5]);
+            val[6] = fmaf(f[q], b[q].z, val[6]);
+            val[7] = fmaf(f[q], b[q].w, val[7]);
+        }
     }
+    uint4 w;
+    __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&w);
+#pragma unroll
+    for (int c = 0; c < 4; c++) h[c] = __floats2bfloat162_rn(val[2 * c], val[2 * c + 1]);
+    *reinterpret_cast<uint4 *>(prm.node16 + (bh * NT + (long long)u * kSeg) * (D * D) + e0) = w;
 }
 
 // ======================================================= read-out consumer
@@ -1005,7 +1018,8 @@ int tc_launches(int T)
     return 4 + (nseg_full_of(NT) > 0 ? 1 : 0);      // + walkers (+ segment fix-up)
 }
 
-static_assert(sizeof(WalkSmem<128>) + 1024 <= 113 * 1024, "walker must fit two CTAs per SM");
+static_assert(sizeof(WalkSmem<128>) + 1024 <= 227 * 1024, "walker must fit the shared memory of an SM");
+static_assert(sizeof(WalkSmem<64>) + 1024 <= 113 * 1024, "walker (D = 64) must fit two CTAs per SM");
 static_assert(sizeof(ConsSmem<128>) + 1024 <= 227 * 1024, "consumer must fit the shared memory of an SM");
 static_assert(MlpLayout<128>::kW2 % 1024 == 0, "the MLP's weight parts are whole swizzle atoms");
 
@@ -1102,11 +1116,11 @@ static cudaError_t tc_fwd_d(const TcFwdArgs &A)
                                  (int)wsmem);
         if (e != cudaSuccess) return e;
         const int nseg = (NT - 1 + kSeg - 1) / kSeg;
-        lla_node_walker_kernel<D><<<dim3(nseg, D / kSliceW, BH), kWalkThreads, wsmem, st>>>(mk, mv, prm);
+        lla_node_walker_kernel<D><<<dim3(nseg, BH), kWalkThreads, wsmem, st>>>(mk, mv, prm);
         if (prm.nseg_full > 0) {
             cudaLaunchAttribute attr;
-            cudaLaunchConfig_t cfg =
-                launch_cfg(dim3((D * D / 8 + kFixThreads - 1) / kFixThreads, BH), dim3(kFixThreads), 0, st, true, &attr);
+            cudaLaunchConfig_t cfg = launch_cfg(dim3((D * D / 8 + kFixThreads - 1) / kFixThreads, prm.nseg_full, BH),
+                                                dim3(kFixThreads), 0, st, true, &attr);
             e = cudaLaunchKernelEx(&cfg, lla_node_fixup_kernel<D>, prm);
             if (e != cudaSuccess) return e;
         }
