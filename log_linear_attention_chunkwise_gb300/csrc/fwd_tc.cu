@@ -129,7 +129,8 @@ __device__ __forceinline__ uint32_t f32_stage_off(int r, int c)
 constexpr int kSegLog = 3;
 constexpr int kSeg = 1 << kSegLog;       // tiles per segment
 constexpr int kWalkStages = 3;           // K/V tiles in flight per walker
-constexpr int kWalkThreads = 256;        // warps 0-3: node epilogue; warps 4-7: tile preparation
+constexpr int kWalkEpi = 512;            // warps 0-15: node epilogue, four threads per dk row
+constexpr int kWalkThreads = kWalkEpi + 128;  // warps 16-19: tile preparation (thread = token row)
 
 template <int D>
 struct __align__(1024) WalkSmem {
@@ -149,6 +150,7 @@ constexpr uint32_t walk_tmem_cols()
 }
 
 __device__ __forceinline__ void prep_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void wepi_sync() { asm volatile("bar.sync 2, 512;" ::: "memory"); }
 
 // Warp-specialised: the preparation warps (thread = token row) scale V by
 // exp(Gam - gamma) and issue the state product of tile n while the epilogue
@@ -174,7 +176,7 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
     if (tid == 0) {
         for (int b = 0; b < kWalkStages; b++) mbar_init(&s.bar_load[b], 1);
         mbar_init(&s.bar_h, 1);
-        mbar_init(&s.bar_hfree, D);
+        mbar_init(&s.bar_hfree, 4 * D);
         fence_mbar_init();
         tma_prefetch_map(&map_k);
         tma_prefetch_map(&map_v);
@@ -203,9 +205,9 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
         bulk_load(s.gm[ls], prm.gamma + ((long long)bh * NT + i) * kTile, kTile * 4, &s.bar_load[ls]);
     };
 
-    if (warp >= 4) {
+    if (tid >= kWalkEpi) {
         // ---------------- preparation warps
-        const int p = tid - 128;
+        const int p = tid - kWalkEpi;
         if (p == 0)
             for (int n = 0; n < min(kWalkStages, ntiles); n++) issue_load(n);
         for (int n = 0; n < ntiles; n++) {
@@ -251,9 +253,12 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
                 umma_commit(&s.bar_h);
             }
         }
-    } else if (tid < D) {
-        // ---------------- epilogue warps: thread = dk row `tid`, all D columns
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    } else if ((tid & 127) < D) {
+        // ---------------- epilogue warps: thread = (dk row, quarter of the columns)
+        constexpr int kC = D / 4;  // columns per thread
+        const int r = tid & 127, q = tid >> 7;
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t c0 = q * kC;
         for (int n = 0; n < ntiles; n++) {
             const int J = i0 + n + 1;
             const int z = __ffs(J) - 1;
@@ -261,35 +266,33 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
             const int mlim = cross ? kSegLog : z;
             if (!mbar_wait(&s.bar_h, n & 1, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
             tc_fence_after_sync();
-            float acc[D];
+            float acc[kC];
 #pragma unroll
-            for (int c = 0; c < D; c += 16) tmem_ld16(tm_h + lane_off + c, *reinterpret_cast<float(*)[16]>(acc + c));
+            for (int c = 0; c < kC; c += 16) tmem_ld16(tm_h + lane_off + c0 + c, *reinterpret_cast<float(*)[16]>(acc + c));
             tmem_ld_wait();
             tc_fence_before_sync();
             mbar_arrive(&s.bar_hfree);  // the next tile's product may overwrite H
             const double PJ = s.P[J - i0];
             for (int m = 0; m < mlim; m++) {
                 const float f = __expf((float)(PJ - s.P[J - (1 << m) - i0]));
+                float x[kC];
 #pragma unroll
-                for (int c = 0; c < D; c += 32) {
-                    float x[32];
-                    tmem_ld16(tm + m * D + lane_off + c, *reinterpret_cast<float(*)[16]>(x));
-                    tmem_ld16(tm + m * D + lane_off + c + 16, *reinterpret_cast<float(*)[16]>(x + 16));
-                    tmem_ld_wait();
+                for (int c = 0; c < kC; c += 16)
+                    tmem_ld16(tm + m * D + lane_off + c0 + c, *reinterpret_cast<float(*)[16]>(x + c));
+                tmem_ld_wait();
 #pragma unroll
-                    for (int u = 0; u < 32; u++) acc[c + u] = fmaf(f, x[u], acc[c + u]);
-                }
+                for (int u = 0; u < kC; u++) acc[u] = fmaf(f, x[u], acc[u]);
             }
             if (!cross) {
                 if (z < kSegLog) {
 #pragma unroll
-                    for (int c = 0; c < D; c += 16)
-                        tmem_st16(tm + z * D + lane_off + c, *reinterpret_cast<float(*)[16]>(acc + c));
+                    for (int c = 0; c < kC; c += 16)
+                        tmem_st16(tm + z * D + lane_off + c0 + c, *reinterpret_cast<float(*)[16]>(acc + c));
                     tmem_st_wait();
                 }
-                uint4 *dst = reinterpret_cast<uint4 *>(prm.node16 + (((long long)bh * NT + J) * D + tid) * D);
+                uint4 *dst = reinterpret_cast<uint4 *>(prm.node16 + (((long long)bh * NT + J) * D + r) * D + c0);
 #pragma unroll
-                for (int c = 0; c < D / 8; c++) {
+                for (int c = 0; c < kC / 8; c++) {
                     uint4 w;
                     __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&w);
 #pragma unroll
@@ -298,9 +301,9 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
                 }
             } else {
                 float4 *dst = reinterpret_cast<float4 *>(
-                    prm.segtot + (((long long)bh * prm.nseg_full + seg) * D + tid) * D);
+                    prm.segtot + (((long long)bh * prm.nseg_full + seg) * D + r) * D + c0);
 #pragma unroll
-                for (int u = 0; u < D / 4; u++)
+                for (int u = 0; u < kC / 4; u++)
                     dst[u] = make_float4(acc[4 * u], acc[4 * u + 1], acc[4 * u + 2], acc[4 * u + 3]);
             }
         }
@@ -313,9 +316,11 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
 // Nodes that close full segments, each on its own from the segment totals:
 // node u SEG covers segments [u - lowbit(u), u), so
 //   Node_{u SEG} = sum_{sigma in [u - lowbit(u), u)} exp(P_{u SEG} - P_{(sigma+1) SEG}) Tot_sigma.
-// One CTA per (256 x 8 state elements, u, batch*head); the totals' loads of a
-// thread are all issued before they are summed.
+// One CTA per (2048 state elements, u, batch*head): a thread owns 8 elements
+// (two float4 at a 1024-element stride, so the CTA's loads are coalesced) and
+// the totals are summed two segments at a time with all loads in flight.
 constexpr int kFixThreads = 256;
+constexpr int kFixElems = kFixThreads * 8;
 template <int D>
 __global__ void __launch_bounds__(kFixThreads)
 lla_node_fixup_kernel(const TcParams prm)
@@ -325,45 +330,37 @@ lla_node_fixup_kernel(const TcParams prm)
     const long long bh = blockIdx.z;
     const int u = blockIdx.y + 1;
     const int NT = prm.NT, nseg = prm.nseg_full;
-    const int e0 = (blockIdx.x * kFixThreads + threadIdx.x) * 8;  // 8 consecutive elements
-    if (e0 >= D * D) return;
+    const int e0 = blockIdx.x * kFixElems + threadIdx.x * 4;  // elements [e0, e0+4) and [e0+1024, e0+1028)
     const double *Pb = prm.P + bh * (NT + 1);
     const double Pu = Pb[u * kSeg];
     const int first = u - (u & -u);
-    float val[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int s0 = first; s0 < u; s0 += 8) {
-        float4 a[8], b[8];
-        float f[8];
-#pragma unroll
-        for (int q = 0; q < 8; q++) {
-            const int sg = s0 + q;
-            if (sg < u) {
-                const float4 *src = reinterpret_cast<const float4 *>(prm.segtot + ((bh * nseg) + sg) * (D * D) + e0);
-                a[q] = src[0];
-                b[q] = src[1];
-                f[q] = __expf((float)(Pu - Pb[(sg + 1) * kSeg]));
-            } else {
-                a[q] = b[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-                f[q] = 0.f;
-            }
+    float4 va = make_float4(0.f, 0.f, 0.f, 0.f), vb = va;
+    for (int sg = first; sg < u; sg += 2) {
+        const bool two = sg + 1 < u;
+        const float *t0 = prm.segtot + ((bh * nseg) + sg) * (D * D);
+        const float4 a0 = *reinterpret_cast<const float4 *>(t0 + e0);
+        const float4 b0 = *reinterpret_cast<const float4 *>(t0 + e0 + 1024);
+        float4 a1 = make_float4(0.f, 0.f, 0.f, 0.f), b1 = a1;
+        if (two) {
+            a1 = *reinterpret_cast<const float4 *>(t0 + D * D + e0);
+            b1 = *reinterpret_cast<const float4 *>(t0 + D * D + e0 + 1024);
         }
-#pragma unroll
-        for (int q = 0; q < 8; q++) {
-            val[0] = fmaf(f[q], a[q].x, val[0]);
-            val[1] = fmaf(f[q], a[q].y, val[1]);
-            val[2] = fmaf(f[q], a[q].z, val[2]);
-            val[3] = fmaf(f[q], a[q].w, val[3]);
-            val[4] = fmaf(f[q], b[q].x, val[4]);
-            val[5] = fmaf(f[q], b[q].y, val[5]);
-            val[6] = fmaf(f[q], b[q].z, val[6]);
-            val[7] = fmaf(f[q], b[q].w, val[7]);
-        }
+        const float f0 = __expf((float)(Pu - Pb[(sg + 1) * kSeg]));
+        const float f1 = two ? __expf((float)(Pu - Pb[(sg + 2) * kSeg])) : 0.f;
+        va.x = fmaf(f0, a0.x, fmaf(f1, a1.x, va.x));
+        va.y = fmaf(f0, a0.y, fmaf(f1, a1.y, va.y));
+        va.z = fmaf(f0, a0.z, fmaf(f1, a1.z, va.z));
+        va.w = fmaf(f0, a0.w, fmaf(f1, a1.w, va.w));
+        vb.x = fmaf(f0, b0.x, fmaf(f1, b1.x, vb.x));
+        vb.y = fmaf(f0, b0.y, fmaf(f1, b1.y, vb.y));
+        vb.z = fmaf(f0, b0.z, fmaf(f1, b1.z, vb.z));
+        vb.w = fmaf(f0, b0.w, fmaf(f1, b1.w, vb.w));
     }
-    uint4 w;
-    __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&w);
-#pragma unroll
-    for (int c = 0; c < 4; c++) h[c] = __floats2bfloat162_rn(val[2 * c], val[2 * c + 1]);
-    *reinterpret_cast<uint4 *>(prm.node16 + (bh * NT + (long long)u * kSeg) * (D * D) + e0) = w;
+    __nv_bfloat16 *dst = prm.node16 + (bh * NT + (long long)u * kSeg) * (D * D);
+    *reinterpret_cast<__nv_bfloat162 *>(dst + e0) = __floats2bfloat162_rn(va.x, va.y);
+    *reinterpret_cast<__nv_bfloat162 *>(dst + e0 + 2) = __floats2bfloat162_rn(va.z, va.w);
+    *reinterpret_cast<__nv_bfloat162 *>(dst + e0 + 1024) = __floats2bfloat162_rn(vb.x, vb.y);
+    *reinterpret_cast<__nv_bfloat162 *>(dst + e0 + 1026) = __floats2bfloat162_rn(vb.z, vb.w);
 }
 
 // ======================================================= read-out consumer
@@ -1119,8 +1116,8 @@ static cudaError_t tc_fwd_d(const TcFwdArgs &A)
         lla_node_walker_kernel<D><<<dim3(nseg, BH), kWalkThreads, wsmem, st>>>(mk, mv, prm);
         if (prm.nseg_full > 0) {
             cudaLaunchAttribute attr;
-            cudaLaunchConfig_t cfg = launch_cfg(dim3((D * D / 8 + kFixThreads - 1) / kFixThreads, prm.nseg_full, BH),
-                                                dim3(kFixThreads), 0, st, true, &attr);
+            cudaLaunchConfig_t cfg = launch_cfg(dim3(D * D / kFixElems, prm.nseg_full, BH), dim3(kFixThreads), 0,
+                                                st, true, &attr);
             e = cudaLaunchKernelEx(&cfg, lla_node_fixup_kernel<D>, prm);
             if (e != cudaSuccess) return e;
         }
