@@ -129,8 +129,9 @@ __device__ __forceinline__ uint32_t f32_stage_off(int r, int c)
 constexpr int kSegLog = 3;
 constexpr int kSeg = 1 << kSegLog;       // tiles per segment
 constexpr int kWalkStages = 3;           // K/V tiles in flight per walker
-constexpr int kWalkEpi = 512;            // warps 0-15: node epilogue, four threads per dk row
-constexpr int kWalkThreads = kWalkEpi + 128;  // warps 16-19: tile preparation (thread = token row)
+constexpr int kWalkEpi = 256;            // warps 0-7: node epilogue, two threads per dk row
+constexpr int kWalkPrep = 256;           // warps 8-15: tile preparation, two threads per token row
+constexpr int kWalkThreads = kWalkEpi + kWalkPrep + 32;  // warp 16: loader
 
 template <int D>
 struct __align__(1024) WalkSmem {
@@ -149,12 +150,12 @@ constexpr uint32_t walk_tmem_cols()
     return (kSegLog + 1) * D <= 256 ? 256u : 512u;
 }
 
-__device__ __forceinline__ void prep_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-__device__ __forceinline__ void wepi_sync() { asm volatile("bar.sync 2, 512;" ::: "memory"); }
+__device__ __forceinline__ void prep_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-// Warp-specialised: the preparation warps (thread = token row) scale V by
-// exp(Gam - gamma) and issue the state product of tile n while the epilogue
-// warps (thread = dk row) fold tile n-1's state into the Fenwick stack.
+// Warp-specialised: a loader warp keeps the ring of K/V tiles full (tile
+// n+3 as soon as tile n's product is done), the preparation warps scale V by
+// exp(Gam - gamma) and issue the state product of tile n, and the epilogue
+// warps fold tile n-1's state into the Fenwick stack and publish the node.
 template <int D>
 __global__ void __launch_bounds__(kWalkThreads, 1)
 lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
@@ -176,7 +177,7 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
     if (tid == 0) {
         for (int b = 0; b < kWalkStages; b++) mbar_init(&s.bar_load[b], 1);
         mbar_init(&s.bar_h, 1);
-        mbar_init(&s.bar_hfree, 4 * D);
+        mbar_init(&s.bar_hfree, 2 * D);
         fence_mbar_init();
         tma_prefetch_map(&map_k);
         tma_prefetch_map(&map_v);
@@ -205,26 +206,30 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
         bulk_load(s.gm[ls], prm.gamma + ((long long)bh * NT + i) * kTile, kTile * 4, &s.bar_load[ls]);
     };
 
-    if (tid >= kWalkEpi) {
-        // ---------------- preparation warps
+    if (tid >= kWalkEpi + kWalkPrep) {
+        // ---------------- loader (one lane): a stage is refilled once the
+        // product of the tile it held is done
+        if ((tid & 31) == 0)
+            for (int n = 0; n < ntiles; n++) {
+                if (n >= kWalkStages && !mbar_wait(&s.bar_h, (n - kWalkStages) & 1, prm.wait_iters))
+                    set_err(prm.err, kErrMmaTimeout);
+                issue_load(n);
+            }
+    } else if (tid >= kWalkEpi) {
+        // ---------------- preparation warps: thread = (token row, half of the columns)
         const int p = tid - kWalkEpi;
-        if (p == 0)
-            for (int n = 0; n < min(kWalkStages, ntiles); n++) issue_load(n);
+        const int prow = p & 127, ph = p >> 7;
         for (int n = 0; n < ntiles; n++) {
             const int ls = n % kWalkStages;
-            if (p == 0 && n >= 1 && n - 1 + kWalkStages < ntiles) {
-                // stage of tile n-1 is free once its product is done
-                if (!mbar_wait(&s.bar_h, (n - 1) & 1, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
-                issue_load(n - 1 + kWalkStages);
-            }
             if (!mbar_wait(&s.bar_load[ls], (n / kWalkStages) & 1, prm.wait_iters)) set_err(prm.err, kErrLoadTimeout);
             const float Gam = s.gm[ls][kTile - 1];
-            const float gam_a = s.gm[ls][p];
-            {   // V row p, scaled in place by exp(Gam - gamma)
+            const float gam_a = s.gm[ls][prow];
+            {   // V row prow, columns [half D/2, +D/2), scaled in place by exp(Gam - gamma)
                 const float w = __expf(Gam - gam_a);
 #pragma unroll
-                for (int c = 0; c < D / 8; c++) {
-                    uint4 *q4 = reinterpret_cast<uint4 *>(s.v[ls] + (c >> 3) * kBlk + sw128_offset(p, c & 7));
+                for (int cc = 0; cc < D / 16; cc++) {
+                    const int c = ph * (D / 16) + cc;  // 16-byte chunk of the row
+                    uint4 *q4 = reinterpret_cast<uint4 *>(s.v[ls] + (c >> 3) * kBlk + sw128_offset(prow, c & 7));
                     uint4 raw = *q4;
                     __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&raw);
 #pragma unroll
@@ -244,18 +249,17 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
                 tc_fence_after_sync();
                 // H = K^T Vs: A = K^T (M = 128 >= dk, MN-major), B = Vs (N = D, MN-major)
                 const uint32_t idesc = idesc_bf16_f32(128, D, true, true);
+                const uint64_t da = desc_sw128(smem_u32(s.k[ls]), kBlk, 1024);
+                const uint64_t db = desc_sw128(smem_u32(s.v[ls]), kBlk, 1024);
 #pragma unroll
-                for (int kk = 0; kk < 8; kk++) {
-                    const uint32_t off = kk * 2048;
-                    umma_bf16(tm_h, desc_sw128(smem_u32(s.k[ls]) + off, kBlk, 1024),
-                              desc_sw128(smem_u32(s.v[ls]) + off, kBlk, 1024), idesc, kk > 0 ? 1u : 0u);
-                }
+                for (int kk = 0; kk < 8; kk++)  // K step of 16 rows = 2048 bytes = 128 in the address field
+                    umma_bf16(tm_h, da + kk * 128, db + kk * 128, idesc, kk > 0 ? 1u : 0u);
                 umma_commit(&s.bar_h);
             }
         }
     } else if ((tid & 127) < D) {
-        // ---------------- epilogue warps: thread = (dk row, quarter of the columns)
-        constexpr int kC = D / 4;  // columns per thread
+        // ---------------- epilogue warps: thread = (dk row, half of the columns)
+        constexpr int kC = D / 2;  // columns per thread
         const int r = tid & 127, q = tid >> 7;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t c0 = q * kC;
@@ -275,13 +279,15 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
             const double PJ = s.P[J - i0];
             for (int m = 0; m < mlim; m++) {
                 const float f = __expf((float)(PJ - s.P[J - (1 << m) - i0]));
-                float x[kC];
 #pragma unroll
-                for (int c = 0; c < kC; c += 16)
-                    tmem_ld16(tm + m * D + lane_off + c0 + c, *reinterpret_cast<float(*)[16]>(x + c));
-                tmem_ld_wait();
+                for (int c = 0; c < kC; c += 32) {
+                    float x[32];
+                    tmem_ld16(tm + m * D + lane_off + c0 + c, *reinterpret_cast<float(*)[16]>(x));
+                    if (kC > 16) tmem_ld16(tm + m * D + lane_off + c0 + c + 16, *reinterpret_cast<float(*)[16]>(x + 16));
+                    tmem_ld_wait();
 #pragma unroll
-                for (int u = 0; u < kC; u++) acc[u] = fmaf(f, x[u], acc[u]);
+                    for (int u = 0; u < (kC > 16 ? 32 : 16); u++) acc[c + u] = fmaf(f, x[u], acc[c + u]);
+                }
             }
             if (!cross) {
                 if (z < kSegLog) {
