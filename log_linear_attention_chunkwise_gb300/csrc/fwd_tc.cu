@@ -130,8 +130,8 @@ constexpr int kSegLog = 3;
 constexpr int kSeg = 1 << kSegLog;       // tiles per segment
 constexpr int kWalkStages = 3;           // K/V tiles in flight per walker
 constexpr int kWalkEpi = 256;            // warps 0-7: node epilogue, two threads per dk row
-constexpr int kWalkPrep = 256;           // warps 8-15: tile preparation, two threads per token row
-constexpr int kWalkThreads = kWalkEpi + kWalkPrep + 32;  // warp 16: loader
+constexpr int kWalkPrep = 128;           // warps 8-11: tile preparation, thread = token row
+constexpr int kWalkThreads = kWalkEpi + kWalkPrep + 64;  // warp 16: loader, warp 17: MMA issuer
 
 template <int D>
 struct __align__(1024) WalkSmem {
@@ -139,7 +139,7 @@ struct __align__(1024) WalkSmem {
     uint8_t v[kWalkStages][kTile * D * 2];  // V tiles, scaled in place by exp(Gam - gamma)
     float gm[kWalkStages][kTile];           // the tile's inclusive gate sums gamma
     double P[kSeg + 1];                     // P_{i0} .. P_{i0+kSeg}
-    uint64_t bar_load[kWalkStages], bar_h, bar_hfree;
+    uint64_t bar_load[kWalkStages], bar_scaled[kWalkStages], bar_h, bar_hfree;
     uint32_t tmem;
 };
 
@@ -150,12 +150,12 @@ constexpr uint32_t walk_tmem_cols()
     return (kSegLog + 1) * D <= 256 ? 256u : 512u;
 }
 
-__device__ __forceinline__ void prep_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-// Warp-specialised: a loader warp keeps the ring of K/V tiles full (tile
-// n+3 as soon as tile n's product is done), the preparation warps scale V by
-// exp(Gam - gamma) and issue the state product of tile n, and the epilogue
-// warps fold tile n-1's state into the Fenwick stack and publish the node.
+// Warp-specialised, every hand-off through an mbarrier: a loader warp keeps
+// the ring of K/V tiles full (tile n+3 as soon as tile n's product is done),
+// the preparation warps scale V by exp(Gam - gamma), an MMA warp issues the
+// state product of each scaled tile, and the epilogue warps fold tile n-1's
+// state into the Fenwick stack and publish the node.
 template <int D>
 __global__ void __launch_bounds__(kWalkThreads, 1)
 lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
@@ -175,7 +175,10 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
 
     grid_launch_dependents();  // the fix-up and read-out may start in this grid's tail
     if (tid == 0) {
-        for (int b = 0; b < kWalkStages; b++) mbar_init(&s.bar_load[b], 1);
+        for (int b = 0; b < kWalkStages; b++) {
+            mbar_init(&s.bar_load[b], 1);
+            mbar_init(&s.bar_scaled[b], kWalkPrep);
+        }
         mbar_init(&s.bar_h, 1);
         mbar_init(&s.bar_hfree, 2 * D);
         fence_mbar_init();
@@ -206,7 +209,28 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
         bulk_load(s.gm[ls], prm.gamma + ((long long)bh * NT + i) * kTile, kTile * 4, &s.bar_load[ls]);
     };
 
-    if (tid >= kWalkEpi + kWalkPrep) {
+    if (tid >= kWalkEpi + kWalkPrep + 32) {
+        // ---------------- MMA issuer (one lane): tile n's product once its V is
+        // scaled and tile n-1's state has been drained from the accumulator
+        if ((tid & 31) == 0) {
+            const uint32_t idesc = idesc_bf16_f32(128, D, true, true);
+            for (int n = 0; n < ntiles; n++) {
+                const int ls = n % kWalkStages;
+                if (!mbar_wait(&s.bar_scaled[ls], (n / kWalkStages) & 1, prm.wait_iters))
+                    set_err(prm.err, kErrMmaTimeout);
+                if (n >= 1 && !mbar_wait(&s.bar_hfree, (n - 1) & 1, prm.wait_iters))
+                    set_err(prm.err, kErrMmaTimeout);
+                tc_fence_after_sync();
+                // H = K^T Vs: A = K^T (M = 128 >= dk, MN-major), B = Vs (N = D, MN-major)
+                const uint64_t da = desc_sw128(smem_u32(s.k[ls]), kBlk, 1024);
+                const uint64_t db = desc_sw128(smem_u32(s.v[ls]), kBlk, 1024);
+#pragma unroll
+                for (int kk = 0; kk < 8; kk++)  // K step of 16 rows = 2048 bytes = 128 in the address field
+                    umma_bf16(tm_h, da + kk * 128, db + kk * 128, idesc, kk > 0 ? 1u : 0u);
+                umma_commit(&s.bar_h);
+            }
+        }
+    } else if (tid >= kWalkEpi + kWalkPrep) {
         // ---------------- loader (one lane): a stage is refilled once the
         // product of the tile it held is done
         if ((tid & 31) == 0)
@@ -216,46 +240,35 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
                 issue_load(n);
             }
     } else if (tid >= kWalkEpi) {
-        // ---------------- preparation warps: thread = (token row, half of the columns)
-        const int p = tid - kWalkEpi;
-        const int prow = p & 127, ph = p >> 7;
+        // ---------------- preparation warps: thread = token row
+        const int prow = tid - kWalkEpi;
         for (int n = 0; n < ntiles; n++) {
             const int ls = n % kWalkStages;
             if (!mbar_wait(&s.bar_load[ls], (n / kWalkStages) & 1, prm.wait_iters)) set_err(prm.err, kErrLoadTimeout);
-            const float Gam = s.gm[ls][kTile - 1];
-            const float gam_a = s.gm[ls][prow];
-            {   // V row prow, columns [half D/2, +D/2), scaled in place by exp(Gam - gamma)
-                const float w = __expf(Gam - gam_a);
+            const float w = __expf(s.gm[ls][kTile - 1] - s.gm[ls][prow]);
+            // V row prow scaled in place by exp(Gam - gamma): all loads first, then
+            // the products, then the stores
+            constexpr int kCh = D / 8;  // 16-byte chunks of the row
+            uint4 raw[kCh];
+            uint4 *q4[kCh];
 #pragma unroll
-                for (int cc = 0; cc < D / 16; cc++) {
-                    const int c = ph * (D / 16) + cc;  // 16-byte chunk of the row
-                    uint4 *q4 = reinterpret_cast<uint4 *>(s.v[ls] + (c >> 3) * kBlk + sw128_offset(prow, c & 7));
-                    uint4 raw = *q4;
-                    __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&raw);
+            for (int c = 0; c < kCh; c++) {
+                q4[c] = reinterpret_cast<uint4 *>(s.v[ls] + (c >> 3) * kBlk + sw128_offset(prow, c & 7));
+                raw[c] = *q4[c];
+            }
 #pragma unroll
-                    for (int u = 0; u < 4; u++) {
-                        float2 f = __bfloat1622float2(h[u]);
-                        h[u] = __floats2bfloat162_rn(f.x * w, f.y * w);
-                    }
-                    *q4 = raw;
+            for (int cc = 0; cc < kCh; cc++) {
+                __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&raw[cc]);
+#pragma unroll
+                for (int u = 0; u < 4; u++) {
+                    const float2 f = __bfloat1622float2(h[u]);
+                    h[u] = __floats2bfloat162_rn(f.x * w, f.y * w);
                 }
             }
-            fence_proxy_async_smem();
-            prep_sync();
-            if (p == 0) {
-                // H (one accumulator) is free once the epilogue has drained tile n-1's
-                if (n >= 1 && !mbar_wait(&s.bar_hfree, (n - 1) & 1, prm.wait_iters))
-                    set_err(prm.err, kErrMmaTimeout);
-                tc_fence_after_sync();
-                // H = K^T Vs: A = K^T (M = 128 >= dk, MN-major), B = Vs (N = D, MN-major)
-                const uint32_t idesc = idesc_bf16_f32(128, D, true, true);
-                const uint64_t da = desc_sw128(smem_u32(s.k[ls]), kBlk, 1024);
-                const uint64_t db = desc_sw128(smem_u32(s.v[ls]), kBlk, 1024);
 #pragma unroll
-                for (int kk = 0; kk < 8; kk++)  // K step of 16 rows = 2048 bytes = 128 in the address field
-                    umma_bf16(tm_h, da + kk * 128, db + kk * 128, idesc, kk > 0 ? 1u : 0u);
-                umma_commit(&s.bar_h);
-            }
+            for (int cc = 0; cc < kCh; cc++) *q4[cc] = raw[cc];
+            fence_proxy_async_smem();
+            mbar_arrive(&s.bar_scaled[ls]);
         }
     } else if ((tid & 127) < D) {
         // ---------------- epilogue warps: thread = (dk row, half of the columns)
