@@ -129,7 +129,7 @@ __device__ __forceinline__ uint32_t f32_stage_off(int r, int c)
 constexpr int kSegLog = 3;
 constexpr int kSeg = 1 << kSegLog;       // tiles per segment
 constexpr int kWalkStages = 3;           // K/V tiles in flight per walker
-constexpr int kWalkEpi = 256;            // warps 0-7: node epilogue, two threads per dk row
+constexpr int kWalkEpi = 512;            // warps 0-15: node epilogue, four threads per dk row
 constexpr int kWalkPrep = 128;           // warps 8-11: tile preparation, thread = token row
 constexpr int kWalkThreads = kWalkEpi + kWalkPrep + 64;  // warp 16: loader, warp 17: MMA issuer
 
@@ -180,7 +180,7 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
             mbar_init(&s.bar_scaled[b], kWalkPrep);
         }
         mbar_init(&s.bar_h, 1);
-        mbar_init(&s.bar_hfree, 2 * D);
+        mbar_init(&s.bar_hfree, (kWalkEpi / 128) * D);
         fence_mbar_init();
         tma_prefetch_map(&map_k);
         tma_prefetch_map(&map_v);
@@ -246,33 +246,35 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
             const int ls = n % kWalkStages;
             if (!mbar_wait(&s.bar_load[ls], (n / kWalkStages) & 1, prm.wait_iters)) set_err(prm.err, kErrLoadTimeout);
             const float w = __expf(s.gm[ls][kTile - 1] - s.gm[ls][prow]);
-            // V row prow scaled in place by exp(Gam - gamma): all loads first, then
-            // the products, then the stores
-            constexpr int kCh = D / 8;  // 16-byte chunks of the row
-            uint4 raw[kCh];
-            uint4 *q4[kCh];
+            // V row prow scaled in place by exp(Gam - gamma), eight 16-byte chunks at a
+            // time: all loads first, then the products, then the stores
+            uint8_t *const vrow = s.v[ls] + prow * 128;
+            const uint32_t sw = (uint32_t)(prow & 7);
 #pragma unroll
-            for (int c = 0; c < kCh; c++) {
-                q4[c] = reinterpret_cast<uint4 *>(s.v[ls] + (c >> 3) * kBlk + sw128_offset(prow, c & 7));
-                raw[c] = *q4[c];
-            }
+            for (int c0 = 0; c0 < D / 8; c0 += 8) {
+                uint4 raw[8];
 #pragma unroll
-            for (int cc = 0; cc < kCh; cc++) {
-                __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&raw[cc]);
+                for (int c = 0; c < 8; c++)
+                    raw[c] = *reinterpret_cast<const uint4 *>(vrow + ((c0 + c) >> 3) * kBlk + ((c ^ sw) << 4));
 #pragma unroll
-                for (int u = 0; u < 4; u++) {
-                    const float2 f = __bfloat1622float2(h[u]);
-                    h[u] = __floats2bfloat162_rn(f.x * w, f.y * w);
+                for (int c = 0; c < 8; c++) {
+                    __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&raw[c]);
+#pragma unroll
+                    for (int u = 0; u < 4; u++) {
+                        const float2 f = __bfloat1622float2(h[u]);
+                        h[u] = __floats2bfloat162_rn(f.x * w, f.y * w);
+                    }
                 }
-            }
 #pragma unroll
-            for (int cc = 0; cc < kCh; cc++) *q4[cc] = raw[cc];
+                for (int c = 0; c < 8; c++)
+                    *reinterpret_cast<uint4 *>(vrow + ((c0 + c) >> 3) * kBlk + ((c ^ sw) << 4)) = raw[c];
+            }
             fence_proxy_async_smem();
             mbar_arrive(&s.bar_scaled[ls]);
         }
     } else if ((tid & 127) < D) {
-        // ---------------- epilogue warps: thread = (dk row, half of the columns)
-        constexpr int kC = D / 2;  // columns per thread
+        // ---------------- epilogue warps: thread = (dk row, quarter of the columns)
+        constexpr int kC = D / (kWalkEpi / 128);  // columns per thread
         const int r = tid & 127, q = tid >> 7;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t c0 = q * kC;
@@ -293,13 +295,12 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
             for (int m = 0; m < mlim; m++) {
                 const float f = __expf((float)(PJ - s.P[J - (1 << m) - i0]));
 #pragma unroll
-                for (int c = 0; c < kC; c += 32) {
-                    float x[32];
-                    tmem_ld16(tm + m * D + lane_off + c0 + c, *reinterpret_cast<float(*)[16]>(x));
-                    if (kC > 16) tmem_ld16(tm + m * D + lane_off + c0 + c + 16, *reinterpret_cast<float(*)[16]>(x + 16));
+                for (int c = 0; c < kC; c += 16) {
+                    float x[16];
+                    tmem_ld16(tm + m * D + lane_off + c0 + c, x);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int u = 0; u < (kC > 16 ? 32 : 16); u++) acc[c + u] = fmaf(f, x[u], acc[c + u]);
+                    for (int u = 0; u < 16; u++) acc[c + u] = fmaf(f, x[u], acc[c + u]);
                 }
             }
             if (!cross) {
