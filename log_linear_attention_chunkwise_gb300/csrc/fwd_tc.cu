@@ -128,7 +128,7 @@ __device__ __forceinline__ uint32_t f32_stage_off(int r, int c)
 
 constexpr int kSegLog = 3;
 constexpr int kSeg = 1 << kSegLog;       // tiles per segment
-constexpr int kWalkStages = 3;           // K/V tiles in flight per walker
+constexpr int kWalkStages = 2;           // K/V tiles in flight per walker
 constexpr int kWalkEpi = 512;            // warps 0-15: node epilogue, four threads per dk row
 constexpr int kWalkPrep = 128;           // warps 8-11: tile preparation, thread = token row
 constexpr int kWalkThreads = kWalkEpi + kWalkPrep + 64;  // warp 16: loader, warp 17: MMA issuer
@@ -137,11 +137,19 @@ template <int D>
 struct __align__(1024) WalkSmem {
     uint8_t k[kWalkStages][kTile * D * 2];  // K tiles
     uint8_t v[kWalkStages][kTile * D * 2];  // V tiles, scaled in place by exp(Gam - gamma)
+    uint8_t nst[D * D * 2];                 // a closed node in bf16, staged for its TMA store
     float gm[kWalkStages][kTile];           // the tile's inclusive gate sums gamma
     double P[kSeg + 1];                     // P_{i0} .. P_{i0+kSeg}
     uint64_t bar_load[kWalkStages], bar_scaled[kWalkStages], bar_h, bar_hfree;
     uint32_t tmem;
 };
+
+// the epilogue threads of a walker: four per dk row
+template <int D>
+__device__ __forceinline__ void wepi_sync()
+{
+    asm volatile("bar.sync 2, %0;" ::"n"((kWalkEpi / 128) * D) : "memory");
+}
 
 // tensor-memory columns of a walker: the stack's kSegLog levels and H, D each
 template <int D>
@@ -159,7 +167,7 @@ constexpr uint32_t walk_tmem_cols()
 template <int D>
 __global__ void __launch_bounds__(kWalkThreads, 1)
 lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
-                       const TcParams prm)
+                       const __grid_constant__ CUtensorMap map_node, const TcParams prm)
 {
     constexpr uint32_t kT = kTile * D * 2;
     extern __shared__ uint8_t smem_raw[];
@@ -184,6 +192,7 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
         fence_mbar_init();
         tma_prefetch_map(&map_k);
         tma_prefetch_map(&map_v);
+        tma_prefetch_map(&map_node);
     }
     if (warp == 0) {
         tmem_alloc(&s.tmem, walk_tmem_cols<D>());
@@ -310,14 +319,27 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
                         tmem_st16(tm + z * D + lane_off + c0 + c, *reinterpret_cast<float(*)[16]>(acc + c));
                     tmem_st_wait();
                 }
-                uint4 *dst = reinterpret_cast<uint4 *>(prm.node16 + (((long long)bh * NT + J) * D + r) * D + c0);
+                // the node in bf16 through shared memory (the layout of its TMA box:
+                // 64-column blocks of D rows, 128-byte swizzle) and one TMA store;
+                // the staging is reused once the previous node's store has read it
+                if (tid == 0) tma_store_wait_read();
+                wepi_sync<D>();
 #pragma unroll
                 for (int c = 0; c < kC / 8; c++) {
+                    const int cg = (c0 >> 3) + c;  // 8-column chunk of the row
                     uint4 w;
                     __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&w);
 #pragma unroll
                     for (int u = 0; u < 4; u++) h[u] = __floats2bfloat162_rn(acc[8 * c + 2 * u], acc[8 * c + 2 * u + 1]);
-                    dst[c] = w;
+                    *reinterpret_cast<uint4 *>(s.nst + (cg >> 3) * (D * 128) + sw128_offset(r, cg & 7)) = w;
+                }
+                fence_proxy_async_smem();
+                wepi_sync<D>();
+                if (tid == 0) {
+#pragma unroll
+                    for (int h = 0; h < D / 64; h++)
+                        tma_store_3d(&map_node, s.nst + h * (D * 128), h * 64, 0, bh * NT + J);
+                    tma_store_commit();
                 }
             } else {
                 float4 *dst = reinterpret_cast<float4 *>(
@@ -327,6 +349,7 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
                     dst[u] = make_float4(acc[4 * u], acc[4 * u + 1], acc[4 * u + 2], acc[4 * u + 3]);
             }
         }
+        if (tid == 0) tma_store_wait_all();  // the staging is read before the CTA ends
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -1133,7 +1156,7 @@ static cudaError_t tc_fwd_d(const TcFwdArgs &A)
                                  (int)wsmem);
         if (e != cudaSuccess) return e;
         const int nseg = (NT - 1 + kSeg - 1) / kSeg;
-        lla_node_walker_kernel<D><<<dim3(nseg, BH), kWalkThreads, wsmem, st>>>(mk, mv, prm);
+        lla_node_walker_kernel<D><<<dim3(nseg, BH), kWalkThreads, wsmem, st>>>(mk, mv, mn, prm);
         if (prm.nseg_full > 0) {
             cudaLaunchAttribute attr;
             cudaLaunchConfig_t cfg = launch_cfg(dim3(D * D / kFixElems, prm.nseg_full, BH), dim3(kFixThreads), 0,
