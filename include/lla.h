@@ -228,7 +228,9 @@ size_t lla_decode_state_bytes(int B, int H, int dk, int dv, int Ls);
  * A sequence with pos < 0 or bit_length(pos+1) > Ls is skipped (its out and
  * state are left untouched) and, if device_error is non-NULL, the kernel
  * stores 1 + b into *device_error (one of the offending b when several).
- * The kernel never traps.  device_error is device memory owned by the caller;
+ * The live slots stream into shared memory by bulk copies whose waits are
+ * bounded; one that runs out stores -1 (if nothing was stored before) and
+ * that step's output is invalid.  The kernel never traps.  device_error is device memory owned by the caller;
  * the library only ever writes a nonzero value into it.
  */
 lla_status lla_decode_step(float *state_levels, float *state_logdecay,

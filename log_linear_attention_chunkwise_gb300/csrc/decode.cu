@@ -12,6 +12,7 @@
 
 #include "decode.cuh"
 #include "outer_simt.cuh"
+#include "sm100.cuh"
 
 namespace lla {
 namespace {
@@ -20,15 +21,22 @@ constexpr int kThreads = 256;
 constexpr int kMaxLs = 40;
 
 // One cluster of kParts CTAs per (head, sequence); CTA `part` owns rows
-// [part*dk/kParts, (part+1)*dk/kParts) of every slot, all dv columns.  Thread
-// layout inside a CTA: cg = column group of 4 (float4), rg = row group; a
-// thread owns rows rg, rg+R, ... of its 4 columns.  The partial read-outs
-// are summed through distributed shared memory by CTA 0, which also writes
-// the slot log-decays once every CTA of the cluster has read them.
+// [part*dk/kParts, (part+1)*dk/kParts) of every slot, all dv columns: one
+// contiguous chunk of each slot (16 KB at dk = dv = 128).  The live slots'
+// chunks stream into shared memory by bulk copies through a ring of
+// kRing buffers, issued as soon as the position is known (before the small
+// vector loads), so each SM keeps about three CTAs x kRing chunks in
+// flight.  Thread layout inside a CTA: cg = column group of 4 (float4),
+// rg = row group; a thread owns rows rg, rg+R, ... of its 4 columns.  The
+// partial read-outs are summed through distributed shared memory by CTA 0,
+// which also writes the slot log-decays once every CTA of the cluster has
+// read them.
 constexpr int kParts = 4;
+constexpr int kRing = 4;
+constexpr uint32_t kCopyWait = 1u << 22;  // bounded waits on the slot copies
 
 template <typename Tin, int DV>
-__global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kThreads, 4)
+__global__ void __cluster_dims__(kParts, 1, 1) __launch_bounds__(kThreads, 3)
 decode_step_kernel(float *__restrict__ S, float *__restrict__ D, const Tin *__restrict__ q,
                    const Tin *__restrict__ k, const Tin *__restrict__ v,
                    const float *__restrict__ g, const float *__restrict__ lam,
@@ -36,15 +44,18 @@ decode_step_kernel(float *__restrict__ S, float *__restrict__ D, const Tin *__re
                    int Ls, int32_t *__restrict__ err)
 {
     namespace cg = cooperative_groups;
+    using namespace sm100;
     constexpr int dv = DV;
     constexpr int NC4 = DV / 4;                 // column groups
     constexpr int R = kThreads / NC4;           // row groups
     constexpr int RPT = (128 / kParts + R - 1) / R;  // rows per thread (dk <= 128)
+    extern __shared__ __align__(128) uint8_t ring[];  // kRing chunks of rows x DV fp32
     __shared__ float qs[128], kss[128], vs[DV];
     __shared__ float wl[kMaxLs], el[kMaxLs], dnew[kMaxLs];
     __shared__ float red[R][DV];
     __shared__ float part_out[DV];
     __shared__ float qk_sh;
+    __shared__ uint64_t bar[kRing];
 
     cg::cluster_group cluster = cg::this_cluster();
     const int part = (int)cluster.block_rank();
@@ -58,6 +69,25 @@ decode_step_kernel(float *__restrict__ S, float *__restrict__ D, const Tin *__re
     }
     const int tid = threadIdx.x;
     const int rows = dk / kParts, row0 = part * rows;
+    const uint32_t chunk = (uint32_t)rows * DV * 4;  // bytes of this CTA's part of a slot
+    const uint64_t live_all = (uint64_t)t & ((Ls >= 64) ? ~0ull : ((1ull << Ls) - 1));
+    const int nlive = __popcll(live_all);
+    // the k-th live slot's chunk into ring buffer k % kRing
+    auto issue = [&](int kk, uint64_t rest) {
+        const int l = ctz_u64(rest);
+        uint64_t *bb = &bar[kk % kRing];
+        mbar_arrive_expect_tx(bb, chunk);
+        bulk_load(ring + (kk % kRing) * chunk, S + ((bh * Ls + l) * (long long)dk + row0) * dv, chunk, bb);
+    };
+    if (tid == 0) {
+        for (int i = 0; i < kRing; i++) mbar_init(&bar[i], 1);
+        fence_mbar_init();
+        uint64_t rest = live_all;
+        for (int kk = 0; kk < kRing && rest; kk++) {
+            issue(kk, rest);
+            rest &= rest - 1;
+        }
+    }
     for (int r = tid; r < dk; r += kThreads) {
         qs[r] = to_f32(q[bh * dk + r]);
         kss[r] = to_f32(k[bh * dk + r]);
@@ -90,39 +120,41 @@ decode_step_kernel(float *__restrict__ S, float *__restrict__ D, const Tin *__re
     for (int i = 0; i < RPT; i++) mrg[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 
-    // live slots, two per iteration so that two slots' loads are in flight
-    uint64_t live = (uint64_t)t & ((Ls >= 64) ? ~0ull : ((1ull << Ls) - 1));
-    while (live) {
+    // live slots in order, each from its ring buffer once its copy has landed;
+    // a buffer is refilled with the slot kRing later once every thread is done
+    uint64_t live = live_all, ahead = live_all;
+    for (int i = 0; i < kRing && ahead; i++) ahead &= ahead - 1;  // the slots not yet issued
+    for (int kk = 0; kk < nlive; kk++) {
         const int l0 = ctz_u64(live);
         live &= live - 1;
-        const int l1 = live ? ctz_u64(live) : -1;
-        if (live) live &= live - 1;
-        const float4 *S0 = reinterpret_cast<const float4 *>(S + ((bh * Ls + l0) * (long long)dk) * dv);
-        const float4 *S1 = reinterpret_cast<const float4 *>(S + ((bh * Ls + (l1 < 0 ? l0 : l1)) * (long long)dk) * dv);
-        float4 sv0[RPT], sv1[RPT];
+        if (!mbar_wait(&bar[kk % kRing], (kk / kRing) & 1, kCopyWait) && err != nullptr) atomicCAS(err, 0, -1);
+        const float4 *S0 = reinterpret_cast<const float4 *>(ring + (kk % kRing) * chunk);
+        float4 sv0[RPT];
 #pragma unroll
         for (int i = 0; i < RPT; i++) {
             const int r = rg + R * i;
-            const long long idx = (long long)(row0 + r) * ncol4 + cg4;
-            sv0[i] = (r < rows) ? __ldcs(S0 + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
-            sv1[i] = (r < rows && l1 >= 0) ? __ldcs(S1 + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
+            sv0[i] = (r < rows) ? S0[r * NC4 + cg4] : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         const float w0 = wl[l0], e0 = (l0 < m) ? el[l0] : 0.f;
-        const float w1 = l1 >= 0 ? wl[l1] : 0.f, e1 = (l1 >= 0 && l1 < m) ? el[l1] : 0.f;
 #pragma unroll
         for (int i = 0; i < RPT; i++) {
             const int r = rg + R * i;
             const float qr = (r < rows) ? qs[row0 + r] : 0.f;
-            const float a0 = qr * w0, a1 = qr * w1;
-            acc.x = fmaf(a1, sv1[i].x, fmaf(a0, sv0[i].x, acc.x));
-            acc.y = fmaf(a1, sv1[i].y, fmaf(a0, sv0[i].y, acc.y));
-            acc.z = fmaf(a1, sv1[i].z, fmaf(a0, sv0[i].z, acc.z));
-            acc.w = fmaf(a1, sv1[i].w, fmaf(a0, sv0[i].w, acc.w));
+            const float a0 = qr * w0;
+            acc.x = fmaf(a0, sv0[i].x, acc.x);
+            acc.y = fmaf(a0, sv0[i].y, acc.y);
+            acc.z = fmaf(a0, sv0[i].z, acc.z);
+            acc.w = fmaf(a0, sv0[i].w, acc.w);
             // slots below m are carried into the new slot (e = 0 for the others)
-            mrg[i].x = fmaf(e1, sv1[i].x, fmaf(e0, sv0[i].x, mrg[i].x));
-            mrg[i].y = fmaf(e1, sv1[i].y, fmaf(e0, sv0[i].y, mrg[i].y));
-            mrg[i].z = fmaf(e1, sv1[i].z, fmaf(e0, sv0[i].z, mrg[i].z));
-            mrg[i].w = fmaf(e1, sv1[i].w, fmaf(e0, sv0[i].w, mrg[i].w));
+            mrg[i].x = fmaf(e0, sv0[i].x, mrg[i].x);
+            mrg[i].y = fmaf(e0, sv0[i].y, mrg[i].y);
+            mrg[i].z = fmaf(e0, sv0[i].z, mrg[i].z);
+            mrg[i].w = fmaf(e0, sv0[i].w, mrg[i].w);
+        }
+        if (kk + kRing < nlive) {
+            __syncthreads();  // every thread has read buffer kk % kRing
+            if (tid == 0) issue(kk + kRing, ahead);
+            ahead &= ahead - 1;
         }
     }
     red[rg][col + 0] = acc.x;
@@ -290,7 +322,10 @@ prefill_bucket_kernel(const Tin *__restrict__ k, const Tin *__restrict__ v,
 template <typename Tin, int DV>
 void launch_decode_dv(const DecodeArgs &A)
 {
-    decode_step_kernel<Tin, DV><<<dim3(A.H * kParts, A.B), kThreads, 0, (cudaStream_t)A.stream>>>(
+    const size_t smem = (size_t)kRing * (A.dk / kParts) * DV * 4;
+    if (smem > 48 * 1024)
+        cudaFuncSetAttribute(decode_step_kernel<Tin, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    decode_step_kernel<Tin, DV><<<dim3(A.H * kParts, A.B), kThreads, smem, (cudaStream_t)A.stream>>>(
         A.S, A.D, (const Tin *)A.q, (const Tin *)A.k, (const Tin *)A.v, A.g, A.lam, A.out, A.pos,
         A.H, A.dk, A.Ls, A.err);
 }

@@ -137,7 +137,7 @@ template <int D>
 struct __align__(1024) WalkSmem {
     uint8_t k[kWalkStages][kTile * D * 2];  // K tiles
     uint8_t v[kWalkStages][kTile * D * 2];  // V tiles, scaled in place by exp(Gam - gamma)
-    uint8_t nst[D * D * 2];                 // a closed node in bf16, staged for its TMA store
+    uint8_t nst[2][D * D * 2];              // closed nodes in bf16, staged for their TMA stores (two in turn)
     float gm[kWalkStages][kTile];           // the tile's inclusive gate sums gamma
     double P[kSeg + 1];                     // P_{i0} .. P_{i0+kSeg}
     uint64_t bar_load[kWalkStages], bar_scaled[kWalkStages], bar_h, bar_hfree;
@@ -287,6 +287,7 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
         const int r = tid & 127, q = tid >> 7;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t c0 = q * kC;
+        int nstage = 0;  // nodes published so far: the staging buffer alternates
         for (int n = 0; n < ntiles; n++) {
             const int J = i0 + n + 1;
             const int z = __ffs(J) - 1;
@@ -321,8 +322,9 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
                 }
                 // the node in bf16 through shared memory (the layout of its TMA box:
                 // 64-column blocks of D rows, 128-byte swizzle) and one TMA store;
-                // the staging is reused once the previous node's store has read it
-                if (tid == 0) tma_store_wait_read();
+                // a staging buffer is reused once the store two nodes back has read it
+                uint8_t *const nst = s.nst[nstage & 1];
+                if (tid == 0) tma_store_wait_read_all_but_one();
                 wepi_sync<D>();
 #pragma unroll
                 for (int c = 0; c < kC / 8; c++) {
@@ -331,16 +333,17 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
                     __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&w);
 #pragma unroll
                     for (int u = 0; u < 4; u++) h[u] = __floats2bfloat162_rn(acc[8 * c + 2 * u], acc[8 * c + 2 * u + 1]);
-                    *reinterpret_cast<uint4 *>(s.nst + (cg >> 3) * (D * 128) + sw128_offset(r, cg & 7)) = w;
+                    *reinterpret_cast<uint4 *>(nst + (cg >> 3) * (D * 128) + sw128_offset(r, cg & 7)) = w;
                 }
                 fence_proxy_async_smem();
                 wepi_sync<D>();
                 if (tid == 0) {
 #pragma unroll
                     for (int h = 0; h < D / 64; h++)
-                        tma_store_3d(&map_node, s.nst + h * (D * 128), h * 64, 0, bh * NT + J);
+                        tma_store_3d(&map_node, nst + h * (D * 128), h * 64, 0, bh * NT + J);
                     tma_store_commit();
                 }
+                nstage++;
             } else {
                 float4 *dst = reinterpret_cast<float4 *>(
                     prm.segtot + (((long long)bh * prm.nseg_full + seg) * D + r) * D + c0);

@@ -144,6 +144,12 @@ __device__ __forceinline__ void tma_store_wait_read()
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// The same, leaving the most recently committed group still reading.
+__device__ __forceinline__ void tma_store_wait_read_all_but_one()
+{
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (tensor core operand reads, TMA).
 __device__ __forceinline__ void fence_proxy_async_smem()
