@@ -416,12 +416,13 @@ lla_node_fixup_kernel(const TcParams prm)
 // still in L2.  Eighteen warps:
 //   warps 0-15 epilogue (thread = (row, quarter of the columns)): the mask
 //              P, the drains of P V and of every U = Q Node_j with its fp32
-//              per-row weight, the output staged in shared memory and
-//              written by TMA; four threads per row keep enough warps in
-//              flight to hide the tensor-memory and barrier latencies;
-//   warp 16    producer: takes the next tile and brings its q, k, v, gamma,
-//              lambda and path P values into the free stage (two stages),
-//              and its path nodes into L2;
+//              per-row weight, the output staged in shared memory; four
+//              threads per row keep enough warps in flight to hide the
+//              tensor-memory and barrier latencies;
+//   warp 16    producer: writes out (TMA store) the output staged in a stage,
+//              then takes the next tile and brings its q, k, v, gamma,
+//              lambda and path P values into that stage (two stages), and
+//              its path nodes into L2;
 //   warp 17    MMA issuer (one lane): S, P V, the node loads and the U's.
 // Tile n uses stage n & 1 and tensor-memory region n & 1, so the MMAs and
 // loads of tile n+1 proceed while the epilogue drains tile n.  The roles
@@ -468,7 +469,7 @@ struct __align__(1024) ConsSmem {
     float kf[kTile];                // exp(gamma_e - gamma_b), e = last key of b's 16-key chunk
     double pj[2][kMaxPath + 1];     // P at the path nodes of the stage's tile, then P_i
     int item[2];                    // the stage's work item, -1 when the queue is empty
-    uint64_t bar_load[2], bar_sfree[2], bar_tfree[2];
+    uint64_t bar_load[2], bar_staged[2], bar_tfree[2];
     uint64_t bar_s, bar_pready, bar_pv, bar_pvfree, bar_h;
     uint64_t bar_node[2], bar_u[2], bar_ufree[2];
     uint32_t tmem;
@@ -504,7 +505,7 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
     if (tid == kEpiThreads) {
         for (int b = 0; b < 2; b++) {
             mbar_init(&s.bar_load[b], 1);
-            mbar_init(&s.bar_sfree[b], 1);
+            mbar_init(&s.bar_staged[b], 1);
             mbar_init(&s.bar_tfree[b], kEpiThreads);
             mbar_init(&s.bar_node[b], 1);
             mbar_init(&s.bar_u[b], 1);
@@ -554,11 +555,28 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
 
     if (warp == kProdWarp) {
         // ---------------- producer
+        // The output of the tile that last used a stage, staged there by the
+        // epilogue, is written out by TMA from here before the stage is
+        // refilled, so the epilogue never waits for the store.
+        auto store_out = [&](int sgx, int nx) {  // lane 0: tile nx of stage sgx
+            if (!mbar_wait(&s.bar_staged[sgx], (nx >> 1) & 1, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
+            int io, bho;
+            item_tile(s.item[sgx], NT, BH, &io, &bho);
+            const ConsStage<D> &t = s.st[sgx];
+            if (sizeof(OutT) == 4) {
+#pragma unroll
+                for (int b = 0; b < D / 32; b++) tma_store_3d(&map_out, t.q + b * (kTile * 128), b * 32, io * kTile, bho);
+            } else {
+#pragma unroll
+                for (int h = 0; h < D / 64; h++) tma_store_3d(&map_out, t.q + h * kBlk, h * 64, io * kTile, bho);
+            }
+            tma_store_commit();
+            tma_store_wait_read();  // the stage may be refilled; the writes finish with the kernel
+        };
         bool dep_done = false;
         for (int n = 0;; n++) {
             const int sg = n & 1;
-            if (n >= 2 && lane == 0 && !mbar_wait(&s.bar_sfree[sg], ((n - 2) >> 1) & 1, prm.wait_iters))
-                set_err(prm.err, kErrMmaTimeout);
+            if (n >= 2 && lane == 0) store_out(sg, n - 2);
             __syncwarp();
             int w = 0;
             if (lane == 0) w = atomicAdd(prm.queue, 1);
@@ -567,6 +585,7 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
                 if (lane == 0) {
                     s.item[sg] = -1;
                     mbar_arrive(&s.bar_load[sg]);
+                    if (n >= 1) store_out(sg ^ 1, n - 1);  // the last tile taken
                 }
                 break;
             }
@@ -885,8 +904,9 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
             tc_fence_before_sync();
             mbar_arrive(&s.bar_tfree[sg]);
 
-            // ---- store: stage the tile in the q/k buffers (every product that read
-            // them is complete), then TMA; rows past T are clipped by the tensor map
+            // ---- stage the tile in the q/k buffers (every product that read them is
+            // complete) for the producer's TMA store; rows past T are clipped by the
+            // tensor map
             ConsStage<D> &t = s.st[sg];
             if (sizeof(OutT) == 4) {
                 // fp32: D/32 boxes of 32 columns x 128 rows, in q then k
@@ -910,18 +930,7 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
             }
             fence_proxy_async_smem();
             epi_sync();
-            if (tid == 0) {
-                if (sizeof(OutT) == 4) {
-#pragma unroll
-                    for (int b = 0; b < D / 32; b++) tma_store_3d(&map_out, t.q + b * (kTile * 128), b * 32, i * kTile, bh);
-                } else {
-#pragma unroll
-                    for (int h = 0; h < D / 64; h++) tma_store_3d(&map_out, t.q + h * kBlk, h * 64, i * kTile, bh);
-                }
-                tma_store_commit();
-                tma_store_wait_read();  // the stage may be refilled; the writes finish with the kernel
-                mbar_arrive(&s.bar_sfree[sg]);
-            }
+            if (tid == 0) mbar_arrive(&s.bar_staged[sg]);  // the producer stores it
         }
     }
     tc_fence_before_sync();
