@@ -806,59 +806,84 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
             }
             if (part == 0) s.kf[row] = __expf(gam[row | 15] - gam_a);
             epi_sync();
-            if (!mbar_wait(&s.bar_s, n & 1, prm.s_wait_iters)) set_err(prm.err, kErrMmaTimeout);
-            tc_fence_after_sync();
-            // P = S . M  (thread = query row, keys [32 part, 32 part + 32)), written
+            // P = S . M  (thread = query row a, keys [32 part, 32 part + 32)), written
             // back packed (keys 2c, 2c+1 in one column) into columns
             // [32 part, 32 part + 16): columns this thread has already read, so no
-            // other thread's S is overwritten
+            // other thread's S is overwritten.  A warp's 32 rows form one 32-row
+            // block, so the case is uniform over the warp: keys all above its rows
+            // (part > a/32), all below them (two 16-key chunks of one level each),
+            // or the diagonal block, where each lane has the 16-key chunk holding
+            // its own row (the lower chunk for rows 0-15 of the block, the upper one
+            // for rows 16-31) and one chunk wholly below (or above) the row.
+            // Below the row, with e the last key of the chunk,
+            //   exp(gamma_a - gamma_b) = exp(gamma_a - gamma_e) exp(gamma_e - gamma_b),
+            // both factors <= 1; inside the row's own chunk one exp per key.
+            // The per-lane factors are formed before S is waited for.
             {
-                const int a = row;
+                const int a = row, rb = a >> 5, kb = part * 32;
+                const bool hi = (a & 16) != 0;
+                float cf0 = 0.f, cf1 = 0.f;  // lambda_a[level] exp(gamma_a - gamma_e) of each chunk
+                if (part < rb) {
+                    cf0 = lam_a[32 - __clz(a ^ kb)] * __expf(gam_a - gam[kb + 15]);
+                    cf1 = lam_a[32 - __clz(a ^ (kb + 16))] * __expf(gam_a - gam[kb + 31]);
+                } else if (part == rb && hi) {
+                    // rows 16-31 of the block: keys [kb, kb + 16) lie below, at level 5
+                    cf0 = lam_a[5] * __expf(gam_a - gam[kb + 15]);
+                }
+                if (!mbar_wait(&s.bar_s, n & 1, prm.s_wait_iters)) set_err(prm.err, kErrMmaTimeout);
+                tc_fence_after_sync();
                 uint32_t pk[16];
+                auto pack = [](float x0, float x1) {
+                    __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+                    return *reinterpret_cast<uint32_t *>(&h);
+                };
+                if (part > rb) {
 #pragma unroll
-                for (int q2 = 0; q2 < 2; q2++) {
-                    const int cb = part * 32 + q2 * 16;
-                    // the loads are warp-collective: every lane issues them, whatever its row
-                    float r[16];
-                    tmem_ld16(slot0 + lane_off + cb, r);
+                    for (int u = 0; u < 16; u++) pk[u] = 0u;
+                } else {
+                    // the loads are warp-collective: every lane of the warp issues them
+                    float r0[16], r1[16];
+                    tmem_ld16(slot0 + lane_off + kb, r0);
+                    tmem_ld16(slot0 + lane_off + kb + 16, r1);
                     tmem_ld_wait();
-                    __nv_bfloat162 h[8];
-                    if (cb > a || !row_ok) {  // strictly above the diagonal, or a row past T
-#pragma unroll
-                        for (int u = 0; u < 8; u++) h[u] = __floats2bfloat162_rn(0.f, 0.f);
-                    } else if (cb + 16 <= a) {
-                        // a whole 16-key chunk below the row: one level, and the decay
-                        // exp(gamma_a - gamma_b) = exp(gamma_a - gamma_e) exp(gamma_e - gamma_b)
-                        // with e = cb + 15, both factors <= 1
-                        const int lev = 32 - __clz(a ^ cb);
-                        const float ra = lam_a[lev] * __expf(gam_a - gam[cb + 15]);
-                        const float4 *kf4 = reinterpret_cast<const float4 *>(s.kf + cb);
+                    const float4 *kf4 = reinterpret_cast<const float4 *>(s.kf + kb);
+                    if (part < rb) {
 #pragma unroll
                         for (int u = 0; u < 4; u++) {
-                            const float4 f = kf4[u];
-                            h[2 * u] = __floats2bfloat162_rn(r[4 * u] * ra * f.x, r[4 * u + 1] * ra * f.y);
-                            h[2 * u + 1] = __floats2bfloat162_rn(r[4 * u + 2] * ra * f.z, r[4 * u + 3] * ra * f.w);
+                            const float4 f0 = kf4[u], f1 = kf4[4 + u];
+                            pk[2 * u] = pack(r0[4 * u] * cf0 * f0.x, r0[4 * u + 1] * cf0 * f0.y);
+                            pk[2 * u + 1] = pack(r0[4 * u + 2] * cf0 * f0.z, r0[4 * u + 3] * cf0 * f0.w);
+                            pk[8 + 2 * u] = pack(r1[4 * u] * cf1 * f1.x, r1[4 * u + 1] * cf1 * f1.y);
+                            pk[8 + 2 * u + 1] = pack(r1[4 * u + 2] * cf1 * f1.z, r1[4 * u + 3] * cf1 * f1.w);
                         }
                     } else {
+                        const int cd = kb + (hi ? 16 : 0);  // the row's own chunk
 #pragma unroll
                         for (int u = 0; u < 8; u++) {
-                            float x[2];
+                            float xd[2], xo[2];
 #pragma unroll
                             for (int e = 0; e < 2; e++) {
-                                const int b = cb + 2 * u + e;
-                                x[e] = 0.f;
-                                if (b <= a) {
-                                    const int lev = 32 - __clz(a ^ b);
-                                    x[e] = r[2 * u + e] * lam_a[lev] * __expf(gam_a - gam[b]);
-                                }
+                                const int j = 2 * u + e, b = cd + j;
+                                // the level (0..4) varies over the lanes: a shared-memory
+                                // lookup (a select chain over registers compiles to branches)
+                                const float lj = lam_a[32 - __clz(a ^ b)];
+                                const float ex = __expf(fminf(gam_a - gam[b], 0.f));
+                                xd[e] = b <= a ? (hi ? r1[j] : r0[j]) * lj * ex : 0.f;
+                                // the other chunk: below the row for rows 16-31 (cf0), above it
+                                // for rows 0-15 (cf0 = 0)
+                                xo[e] = (hi ? r0[j] : r1[j]) * cf0 * s.kf[kb + j];
                             }
-                            h[u] = __floats2bfloat162_rn(x[0], x[1]);
+                            const uint32_t pd = pack(xd[0], xd[1]), po = pack(xo[0], xo[1]);
+                            pk[u] = hi ? po : pd;
+                            pk[8 + u] = hi ? pd : po;
                         }
                     }
-#pragma unroll
-                    for (int u = 0; u < 8; u++) pk[q2 * 8 + u] = *reinterpret_cast<uint32_t *>(&h[u]);
                 }
-                tmem_st16(slot0 + lane_off + part * 32, *reinterpret_cast<const float(*)[16]>(pk));
+                if (!row_ok) {  // a row past T
+#pragma unroll
+                    for (int u = 0; u < 16; u++) pk[u] = 0u;
+                }
+                tmem_st16(slot0 + lane_off + kb, *reinterpret_cast<const float(*)[16]>(pk));
             }
             tmem_st_wait();
             tc_fence_before_sync();
