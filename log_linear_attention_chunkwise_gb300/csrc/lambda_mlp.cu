@@ -150,15 +150,20 @@ cudaError_t launch_t(const LambdaMlpArgs &A)
 // ------------------------------------------------ tensor-core path
 // bf16 d with Dd a multiple of 64 (<= 256): the first layer h = d W1 runs on
 // the tensor cores.  d is exact in bf16; W1 is split into three bf16 parts
-// (hi + mid + lo reproduce each fp32 weight to about 24 bits), so
-// h = d W1_hi + d W1_mid + d W1_lo accumulates in fp32 tensor memory with
-// the error of an fp32 dot product.  Per 128-row tile: TMA brings the d rows
-// (two-stage ring), one thread issues the products into one of two
-// tensor-memory accumulators, and four epilogue warps (thread = row) read
-// h, apply the second layer and softplus in fp32 and store the row's L
+// (hi + mid + lo reproduce each fp32 weight to about 24 bits), stacked along
+// N, so one product of N = 3 NP per K step gives d W1_hi, d W1_mid and
+// d W1_lo in three fp32 accumulators, which the epilogue adds as
+// hi + (mid + lo): h carries the error of an fp32 dot product, and a tile
+// takes Dd / 16 MMAs instead of three times as many.  Per 128-row tile: TMA
+// brings the d rows through a ring of up to four stages, one thread issues
+// the products into one of two accumulator sets, and eight epilogue warps
+// (two threads per row, each half of the row's float4 groups of L)
+// read h, apply the second layer and softplus in fp32 and store their
 // weights.  CTAs are persistent over the tiles.
 constexpr int kTcRows = 128;
-constexpr int kTcEpi = 128;             // epilogue threads (one per row)
+constexpr int kTcEpi = 256;             // epilogue threads (two per row)
+constexpr int kTcParts = kTcEpi / kTcRows;
+constexpr int kTcIssueWarp = kTcEpi / 32;
 constexpr int kTcThreads = kTcEpi + 32;  // plus one issuing warp
 constexpr uint32_t kTcWait = 1u << 22;
 
@@ -169,25 +174,31 @@ using namespace sm100;
 // results of that call are not to be trusted.
 __device__ int lla_lambda_tc_wait_err;
 
-__host__ __device__ constexpr int tc_tmem_cols(int NP) { return NP <= 16 ? 32 : NP <= 32 ? 64 : 128; }
+// tensor-memory columns of the two accumulator sets (3 NP columns each)
+__host__ __device__ constexpr int tc_tmem_cols(int NP) { return 6 * NP <= 128 ? 128 : 6 * NP <= 256 ? 256 : 512; }
+
+constexpr int kTcMaxStages = 4;
+constexpr uint32_t kTcSmemMax = 227 * 1024 - 1024;
 
 struct TcLayout {  // byte offsets in dynamic shared memory (1024-aligned base)
-    uint32_t w1, w2, d0, d1, bars, total;
+    uint32_t w1, w2, d0, dtile, bars, total;
+    int stages;
 };
 
 __host__ __device__ inline TcLayout tc_layout(int Dd, int NP, int L)
 {
     TcLayout t;
-    const uint32_t wblk = (uint32_t)NP * 128;              // one 64-wide K block of W1^T part
-    const uint32_t wpart = wblk * (uint32_t)(Dd / 64);     // one part
-    const uint32_t dtile = (uint32_t)kTcRows * 128 * (uint32_t)(Dd / 64);
-    t.w1 = 0;
-    t.d0 = (3 * wpart + 1023) & ~1023u;
-    t.d1 = t.d0 + dtile;
-    t.w2 = t.d1 + dtile;
+    const uint32_t w1bytes = 3u * (uint32_t)NP * 128 * (uint32_t)(Dd / 64);  // [Dd/64][3 NP rows][128 B]
+    t.dtile = (uint32_t)kTcRows * 128 * (uint32_t)(Dd / 64);
     const int Lp = (L + 3) & ~3;
+    const uint32_t tail = (((uint32_t)(NP * Lp + Lp) * 4 + 15) & ~15u) + (2 * kTcMaxStages + 4) * 8 + 16;
+    t.w1 = 0;
+    t.d0 = (w1bytes + 1023) & ~1023u;
+    t.stages = kTcMaxStages;
+    while (t.stages > 2 && t.d0 + t.stages * t.dtile + tail > kTcSmemMax) t.stages--;
+    t.w2 = t.d0 + t.stages * t.dtile;
     t.bars = (t.w2 + (uint32_t)(NP * Lp + Lp) * 4 + 15) & ~15u;
-    t.total = t.bars + 8 * 8 + 16;
+    t.total = t.bars + (2 * kTcMaxStages + 4) * 8 + 16;
     return t;
 }
 
@@ -203,26 +214,27 @@ lambda_tc_kernel(const __grid_constant__ CUtensorMap map_d, const float *__restr
     const TcLayout lay = tc_layout(Dd, NP, L);
     const int Hd = 2 * L;
     const int nb = Dd / 64;
-    const uint32_t wblk = (uint32_t)NP * 128, wpart = wblk * nb;
+    const int NS = lay.stages;
+    const uint32_t wblk = 3u * NP * 128;  // one 64-wide K block of the stacked W1^T parts
     const uint32_t dblk = (uint32_t)kTcRows * 128;
-    uint8_t *dbuf[2] = {sm + lay.d0, sm + lay.d1};
     const int Lp = (L + 3) & ~3;
     float *w2 = reinterpret_cast<float *>(sm + lay.w2);  // [NP][Lp] zero-padded, then bias [Lp]
     float *bs = w2 + NP * Lp;
-    uint64_t *bar_load = reinterpret_cast<uint64_t *>(sm + lay.bars);  // [2]
-    uint64_t *bar_mma = bar_load + 2;                                  // [2]
-    uint64_t *bar_free = bar_load + 4;                                 // [2]
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_load + 6);
+    uint64_t *bar_load = reinterpret_cast<uint64_t *>(sm + lay.bars);  // [NS]
+    uint64_t *bar_mma = bar_load + kTcMaxStages;                       // [2]
+    uint64_t *bar_free = bar_mma + 2;                                  // [2]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_free + 2);
     const int tid = threadIdx.x, warp = tid >> 5;
-    // W1^T split into three bf16 parts in the K-major 128-byte-swizzled layout
+    // W1^T split into three bf16 parts, stacked along N (rows part NP + n) in
+    // the K-major 128-byte-swizzled layout
     for (int e = tid; e < NP * Dd; e += kTcThreads) {
         const int n = e / Dd, k = e % Dd;
         float w = n < Hd ? W1[k * Hd + n] : 0.f;
-        const uint32_t off = (uint32_t)(k / 64) * wblk + sw128_offset(n, (k % 64) / 8) + (k % 8) * 2;
 #pragma unroll
         for (int part = 0; part < 3; part++) {
+            const uint32_t off = (uint32_t)(k / 64) * wblk + sw128_offset(part * NP + n, (k % 64) / 8) + (k % 8) * 2;
             const __nv_bfloat16 b = __float2bfloat16_rn(w);
-            *reinterpret_cast<__nv_bfloat16 *>(sm + lay.w1 + part * wpart + off) = b;
+            *reinterpret_cast<__nv_bfloat16 *>(sm + lay.w1 + off) = b;
             w -= __bfloat162float(b);
         }
     }
@@ -232,15 +244,15 @@ lambda_tc_kernel(const __grid_constant__ CUtensorMap map_d, const float *__restr
     }
     for (int e = tid; e < Lp; e += kTcThreads) bs[e] = e < L ? bias[e] : 0.f;
     if (tid == kTcEpi) {
+        for (int b = 0; b < NS; b++) mbar_init(&bar_load[b], 1);
         for (int b = 0; b < 2; b++) {
-            mbar_init(&bar_load[b], 1);
             mbar_init(&bar_mma[b], 1);
             mbar_init(&bar_free[b], kTcEpi);
         }
         fence_mbar_init();
         tma_prefetch_map(&map_d);
     }
-    if (warp == 4) {
+    if (warp == kTcIssueWarp) {
         tmem_alloc(tmem_slot, tc_tmem_cols(NP));
         tmem_relinquish();
     }
@@ -251,57 +263,68 @@ lambda_tc_kernel(const __grid_constant__ CUtensorMap map_d, const float *__restr
     const uint32_t tm = *tmem_slot;
     const long long ntiles = (N + kTcRows - 1) / kTcRows;
     const int my = (int)((ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x);  // tiles of this CTA
-    if (warp == 4) {
+    if (warp == kTcIssueWarp) {
         if (tid == kTcEpi) {
+            // tile i: load stage i % NS, accumulator set i % 2
             auto load = [&](int i) {
-                const int st = i & 1;
+                const int ls = i % NS;
                 const long long tile = blockIdx.x + (long long)i * gridDim.x;
-                mbar_arrive_expect_tx(&bar_load[st], dblk * nb);
+                uint8_t *dst = sm + lay.d0 + ls * lay.dtile;
+                mbar_arrive_expect_tx(&bar_load[ls], dblk * nb);
                 for (int b = 0; b < nb; b++)
-                    tma_load_3d(dbuf[st] + b * dblk, &map_d, &bar_load[st], 64 * b, (int)(tile * kTcRows), 0);
+                    tma_load_3d(dst + b * dblk, &map_d, &bar_load[ls], 64 * b, (int)(tile * kTcRows), 0);
             };
-            for (int i = 0; i < min(2, my); i++) load(i);
-            const uint32_t idesc = idesc_bf16_f32(128, NP, false, false);
+            for (int i = 0; i < min(NS, my); i++) load(i);
+            const uint32_t idesc = idesc_bf16_f32(128, 3 * NP, false, false);
             for (int i = 0; i < my; i++) {
-                const int st = i & 1;
-                if (!mbar_wait(&bar_load[st], (i >> 1) & 1, kTcWait)) atomicCAS(err, 0, 1);
+                const int ls = i % NS, st = i & 1;
+                if (!mbar_wait(&bar_load[ls], (i / NS) & 1, kTcWait)) atomicCAS(err, 0, 1);
                 if (i >= 2 && !mbar_wait(&bar_free[st], ((i - 2) >> 1) & 1, kTcWait)) atomicCAS(err, 0, 2);
                 tc_fence_after_sync();
-                const uint32_t acc = tm + (uint32_t)(st * NP);
-                int first = 1;
-                for (int part = 0; part < 3; part++)
-                    for (int kk = 0; kk < 4 * nb; kk++) {
-                        const uint32_t offa = (kk >> 2) * dblk + (kk & 3) * 32;
-                        const uint32_t offb = part * wpart + (kk >> 2) * wblk + (kk & 3) * 32;
-                        umma_bf16(acc, desc_sw128(smem_u32(dbuf[st]) + offa, 16, 1024),
-                                  desc_sw128(smem_u32(sm + lay.w1) + offb, 16, 1024), idesc, first ? 0u : 1u);
-                        first = 0;
-                    }
+                const uint32_t acc = tm + (uint32_t)(st * 3 * NP);
+                const uint8_t *dt = sm + lay.d0 + ls * lay.dtile;
+                for (int kk = 0; kk < 4 * nb; kk++) {
+                    const uint32_t offa = (kk >> 2) * dblk + (kk & 3) * 32;
+                    const uint32_t offb = (kk >> 2) * wblk + (kk & 3) * 32;
+                    umma_bf16(acc, desc_sw128(smem_u32(dt) + offa, 16, 1024),
+                              desc_sw128(smem_u32(sm + lay.w1) + offb, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+                }
                 umma_commit(&bar_mma[st]);
-                if (i + 2 < my) {  // the stage is free once this tile's products are done
+                if (i + NS < my) {  // the stage is free once this tile's products are done
                     if (!mbar_wait(&bar_mma[st], (i >> 1) & 1, kTcWait)) atomicCAS(err, 0, 2);
-                    load(i + 2);
+                    load(i + NS);
                 }
             }
         }
     } else {
-        // epilogue: thread = row of the tile = tensor-memory lane
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        // epilogue: kTcParts threads per row of the tile (= tensor-memory lane);
+        // part p takes the float4 groups g of lambda with g % kTcParts == p
+        const int row_t = tid & (kTcRows - 1), part = tid >> 7;
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const bool vec = (L & 3) == 0 && ((uintptr_t)lam & 15) == 0;  // every row 16-byte aligned
         for (int i = 0; i < my; i++) {
             const int st = i & 1;
-            const long long row = (blockIdx.x + (long long)i * gridDim.x) * kTcRows + tid;
+            const long long row = (blockIdx.x + (long long)i * gridDim.x) * kTcRows + row_t;
             if (!mbar_wait(&bar_mma[st], (i >> 1) & 1, kTcWait)) atomicCAS(err, 0, 2);
             tc_fence_after_sync();
+            // h = hi + (mid + lo) from the three accumulators of the set
             float h[NP];
+            const uint32_t acc = tm + (uint32_t)(st * 3 * NP) + lane_off;
 #pragma unroll
-            for (int c = 0; c < NP; c += 16)
-                tmem_ld16(tm + (uint32_t)(st * NP + c) + lane_off, *reinterpret_cast<float(*)[16]>(h + c));
-            tmem_ld_wait();
+            for (int c = 0; c < NP; c += 16) {
+                float m[16], l[16];
+                tmem_ld16(acc + c, *reinterpret_cast<float(*)[16]>(h + c));
+                tmem_ld16(acc + NP + c, m);
+                tmem_ld16(acc + 2 * NP + c, l);
+                tmem_ld_wait();
+#pragma unroll
+                for (int u = 0; u < 16; u++) h[c + u] += m[u] + l[u];
+            }
             tc_fence_before_sync();
             mbar_arrive(&bar_free[st]);
             if (row < N) {
                 float *out = lam + row * L;
-                for (int l0 = 0; l0 < L; l0 += 4) {
+                for (int l0 = 4 * part; l0 < L; l0 += 4 * kTcParts) {
                     float4 z = *reinterpret_cast<const float4 *>(bs + l0);
 #pragma unroll
                     for (int j = 0; j < NP; j++) {
@@ -311,17 +334,22 @@ lambda_tc_kernel(const __grid_constant__ CUtensorMap map_d, const float *__restr
                         z.z = fmaf(h[j], w.z, z.z);
                         z.w = fmaf(h[j], w.w, z.w);
                     }
-                    const float zz[4] = {z.x, z.y, z.z, z.w};
+                    const float4 y = make_float4(softplus_f(z.x), softplus_f(z.y), softplus_f(z.z), softplus_f(z.w));
+                    if (vec) {
+                        *reinterpret_cast<float4 *>(out + l0) = y;
+                    } else {
+                        const float yy[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
-                    for (int q = 0; q < 4; q++)
-                        if (l0 + q < L) out[l0 + q] = softplus_f(zz[q]);
+                        for (int q = 0; q < 4; q++)
+                            if (l0 + q < L) out[l0 + q] = yy[q];
+                    }
                 }
             }
         }
     }
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 4) tmem_dealloc(tm, tc_tmem_cols(NP));
+    if (warp == kTcIssueWarp) tmem_dealloc(tm, tc_tmem_cols(NP));
 }
 
 template <int NP>
