@@ -444,8 +444,9 @@ struct __align__(1024) ConsStage {
 // Shared memory after the stages: either the lambda rows of each stage
 // ([128][L] fp32, loaded with the tile), or, with the in-kernel lambda MLP,
 // the first layer's weights as bf16 high and low parts in the K-major
-// swizzled layout of an MMA operand ([2][32 hidden][D]), the second layer
-// and bias (fp32) and one [128][L] staging of the tile's lambdas.
+// swizzled layout of one N = 64 MMA operand (per 64-wide K block, the 32
+// hidden rows of the high part, then those of the low part), the second
+// layer and bias (fp32) and one [128][L] staging of the tile's lambdas.
 template <int D>
 struct MlpLayout {
     static constexpr uint32_t kW1Part = kMlpHidden * D * 2;
@@ -538,10 +539,10 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
             const float w = n < Hd ? prm.W1[kx * Hd + n] : 0.f;
             const __nv_bfloat16 hi = __float2bfloat16_rn(w);
             const __nv_bfloat16 lo = __float2bfloat16_rn(w - __bfloat162float(hi));
-            const uint32_t off = (uint32_t)(kx >> 6) * (kMlpHidden * 128) + sw128_offset(n, (kx & 63) >> 3) +
-                                 (kx & 7) * 2;
-            *reinterpret_cast<__nv_bfloat16 *>(s.aux + off) = hi;
-            *reinterpret_cast<__nv_bfloat16 *>(s.aux + ML::kW1Part + off) = lo;
+            // per 64-wide K block: rows [0, 32) the high part, [32, 64) the low part
+            const uint32_t blk = (uint32_t)(kx >> 6) * (2 * kMlpHidden * 128), in = (kx & 7) * 2;
+            *reinterpret_cast<__nv_bfloat16 *>(s.aux + blk + sw128_offset(n, (kx & 63) >> 3) + in) = hi;
+            *reinterpret_cast<__nv_bfloat16 *>(s.aux + blk + sw128_offset(kMlpHidden + n, (kx & 63) >> 3) + in) = lo;
         }
         float *w2 = reinterpret_cast<float *>(s.aux + ML::kW2);  // [32][L], rows past 2L zero
         for (int e = tid; e < kMlpHidden * L; e += kConsThreads) w2[e] = e < Hd * L ? prm.W2[e] : 0.f;
@@ -632,18 +633,16 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
         if (lane == 0) {
             const uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
             const uint32_t id_kmn = idesc_bf16_f32(128, D, false, true);
-            const uint32_t id_h = idesc_bf16_f32(128, kMlpHidden, false, false);
-            // h = K W1 (both parts, one accumulator) into slot 1 of the tile's region
+            const uint32_t id_h = idesc_bf16_f32(128, 2 * kMlpHidden, false, false);
+            // [K W1_hi | K W1_lo] (one N = 64 product per K step) into slot 1 of the tile's region
             auto issue_h = [&](uint32_t slot1, const uint8_t *kt) {
 #pragma unroll
-                for (int p = 0; p < 2; p++)
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; kk++) {
-                        const uint32_t offa = (kk >> 2) * kBlk + (kk & 3) * 32;
-                        const uint32_t offb = p * ML::kW1Part + (kk >> 2) * (kMlpHidden * 128) + (kk & 3) * 32;
-                        umma_bf16(slot1, desc_sw128(smem_u32(kt) + offa, 16, 1024),
-                                  desc_sw128(smem_u32(s.aux) + offb, 16, 1024), id_h, (p | kk) ? 1u : 0u);
-                    }
+                for (int kk = 0; kk < D / 16; kk++) {
+                    const uint32_t offa = (kk >> 2) * kBlk + (kk & 3) * 32;
+                    const uint32_t offb = (kk >> 2) * (2 * kMlpHidden * 128) + (kk & 3) * 32;
+                    umma_bf16(slot1, desc_sw128(smem_u32(kt) + offa, 16, 1024),
+                              desc_sw128(smem_u32(s.aux) + offb, 16, 1024), id_h, kk ? 1u : 0u);
+                }
                 umma_commit(&s.bar_h);
             };
             // parities of the completions so far of bar_node[b] and bar_u[b] (bit b):
@@ -787,10 +786,19 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
                 // h (the row's 2L hidden values) from tensor memory
                 if (!mbar_wait(&s.bar_h, n & 1, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
                 tc_fence_after_sync();
+                // h = K W1_hi + K W1_lo
                 float h[kMlpHidden];
-                tmem_ld16(slot1 + lane_off, *reinterpret_cast<float(*)[16]>(h));
-                tmem_ld16(slot1 + lane_off + 16, *reinterpret_cast<float(*)[16]>(h + 16));
-                tmem_ld_wait();
+                {
+                    float hl[16];
+#pragma unroll
+                    for (int c = 0; c < kMlpHidden; c += 16) {
+                        tmem_ld16(slot1 + lane_off + c, *reinterpret_cast<float(*)[16]>(h + c));
+                        tmem_ld16(slot1 + lane_off + kMlpHidden + c, hl);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int u = 0; u < 16; u++) h[c + u] += hl[u];
+                    }
+                }
                 const float *w2 = reinterpret_cast<const float *>(s.aux + ML::kW2);
                 const float *bs = reinterpret_cast<const float *>(s.aux + ML::kBias);
                 float *lst = reinterpret_cast<float *>(s.aux + ML::kLam);
