@@ -40,6 +40,16 @@ struct __align__(1024) IntraSmem {
     uint32_t tmem;
 };
 
+// c ? x : y as a predicated select (never a branch)
+__device__ __forceinline__ float selp_f(bool c, float x, float y)
+{
+    float r;
+    asm("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %3, 0;\n\tselp.f32 %0, %1, %2, p;\n\t}"
+        : "=f"(r)
+        : "f"(x), "f"(y), "r"((uint32_t)c));
+    return r;
+}
+
 // 8 MMAs over K = 128 with the given operand majors (A K-major or MN-major,
 // B K-major or MN-major; K-major rows are 128 B, MN-major K rows are 128 B).
 __device__ __forceinline__ void mma8x(uint32_t d, const uint8_t *a, bool a_mn, const uint8_t *b, bool b_mn,
@@ -183,20 +193,26 @@ bwd_intra_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
             tmem_ld_wait();
 #pragma unroll
             for (int e = 0; e < 16; e++) {
+                // branch-free: the level varies over the lanes, and a register
+                // array indexed by it (or a branch per level) serialises the warp
                 const int b = 32 * hh + c0 + e;  // key column inside the chunk
-                float x1 = 0.f, x2 = 0.f;
-                if (b <= a && row_ok) {
-                    const float dec = __expf(gam_t - s.gam[cb + b]);
-                    const int lev = 32 - __clz(a ^ b);
-                    const float m = lamv[lev] * dec;
-                    x1 = m * pv[e];
-                    x2 = m * sv[e];
+                const bool ok = b <= a && row_ok;
+                const float dec = __expf(fminf(gam_t - s.gam[cb + b], 0.f));
+                const uint32_t x = (uint32_t)(a ^ b);  // level = bit_length(x)
+                float lm = lamv[0];
+                lm = selp_f(x >= 1u, lamv[1], lm);
+                lm = selp_f(x >= 2u, lamv[2], lm);
+                lm = selp_f(x >= 4u, lamv[3], lm);
+                lm = selp_f(x >= 8u, lamv[4], lm);
+                lm = selp_f(x >= 16u, lamv[5], lm);
+                lm = selp_f(x >= 32u, lamv[6], lm);
+                const float m = selp_f(ok, lm * dec, 0.f);
+                w1[c0 + e] = m * pv[e];
+                w2[c0 + e] = m * sv[e];
+                const float ds = selp_f(ok, dec * sv[e], 0.f);
+                const int lev = 32 - __clz((int)x);
 #pragma unroll
-                    for (int l = 0; l < 7; l++)
-                        if (l == lev) dl[l] = fmaf(dec * sv[e], pv[e], dl[l]);
-                }
-                w1[c0 + e] = x1;
-                w2[c0 + e] = x2;
+                for (int l = 0; l < 7; l++) dl[l] = fmaf(selp_f(lev == l, ds, 0.f), pv[e], dl[l]);
             }
         }
     }
