@@ -113,13 +113,27 @@ bwd_key_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_consta
     };
     // the level sequence: level 0 first (if any), then the shared levels
     const int total = (lev0 ? 1 : 0) + nl;
+    auto level_of = [&](int n) { return (lev0 && n == 0) ? 0 : levs[n - (lev0 ? 1 : 0)]; };
+    // the block states are read from DRAM: each is prefetched into L2 two
+    // levels before it is staged
+    auto prefetch_state = [&](int n) {
+        if (tid == 0 && n < total) {
+            const int m = level_of(n);
+            const float *src = block_state(R, part, bh, m, (c0 >> m) + 1, N, Pc, nitems, nblocks, kKD * kKD);
+            bulk_prefetch_l2(src, kKD * kKD * 2);
+            bulk_prefetch_l2(src + kKD * kKD / 2, kKD * kKD * 2);
+        }
+    };
+    prefetch_state(0);
+    prefetch_state(1);
     bool acc_started = false;
     if (!mbar_wait(&s.bar_load, 0, kKWait)) key_err(err, 1);
     for (int n = 0; n < total; n++) {
         const int buf = n & 1;
         const bool is0 = lev0 && n == 0;
-        const int m = is0 ? 0 : levs[n - (lev0 ? 1 : 0)];
+        const int m = level_of(n);
         const int b = (c0 >> m) + 1;
+        prefetch_state(n + 2);
         const float *Rm = block_state(R, part, bh, m, b, N, Pc, nitems, nblocks, kKD * kKD);
         const float c = is0 ? 1.f : expf((float)(Pb[b << m] - Pend));
         if (n >= 2 && !mbar_wait(&s.bar_mma[buf], ((n - 2) >> 1) & 1, kKWait)) key_err(err, 2);

@@ -4,9 +4,11 @@
 // CUDA-core backward).  A CTA takes one piece (up to 16 chunks) in 128-token
 // tiles: TMA brings the q tile; two threads per token row scale half the dO
 // row each by w (0 for tokens outside the piece) and split it into bf16 high
-// and remainder parts;
-// one thread issues piece += Q^T (w dO)_hi + Q^T (w dO)_lo (M = dk, N = dv,
-// K = 128 tokens) into a tensor-memory accumulator.  The finished piece is
+// and remainder parts, stored side by side; one thread issues
+// [piece_hi | piece_lo] += Q^T [(w dO)_hi | (w dO)_lo] (M = dk, N = 2 dv,
+// K = 128 tokens: one MMA per K step) into two tensor-memory accumulators,
+// added when the piece is written.  The dO rows of a tile are prefetched
+// into L2 two tiles ahead.  The finished piece is
 // written to its own slot; the reduction that follows sums a block's pieces
 // in order.
 #include "bwd_simt.cuh"
@@ -28,7 +30,9 @@ constexpr uint32_t kPWait = 1u << 22;
 
 struct __align__(1024) PieceSmem {
     uint8_t q[2][kPB];
-    uint8_t bhi[2][kPB], blo[2][kPB];
+    struct __align__(1024) {
+        uint8_t hi[kPB], lo[kPB];  // the four 64-column blocks of one N = 256 operand
+    } b[2];
     uint64_t bar_load[2], bar_mma[2], bar_done;
     uint32_t tmem;
 };
@@ -78,7 +82,7 @@ bwd_piece_tc_kernel(const __grid_constant__ CUtensorMap map_q, const float *__re
         tma_prefetch_map(&map_q);
     }
     if (tid < 32) {
-        tmem_alloc(&s.tmem, 128);
+        tmem_alloc(&s.tmem, 256);
         tmem_relinquish();
     }
     tc_fence_before_sync();
@@ -91,11 +95,23 @@ bwd_piece_tc_kernel(const __grid_constant__ CUtensorMap map_q, const float *__re
         tma_load_3d(s.q[st], &map_q, &s.bar_load[st], 0, (int)(t_lo + (long long)n * kPT), bh);
         tma_load_3d(s.q[st] + kPH, &map_q, &s.bar_load[st], 64, (int)(t_lo + (long long)n * kPT), bh);
     };
+    auto prefetch_dout = [&](int n) {  // the dO rows of tile n (rows past the piece are not needed)
+        if (tid == 0 && n < ntiles) {
+            const long long r0 = t_lo + (long long)n * kPT;
+            const long long rows = min((long long)kPT, t_hi - r0);
+            const float *src = dout + ((long long)bh * T + r0) * kPDm;
+            for (long long r = 0; r < rows; r += 64)  // pieces of at most 32 KB
+                bulk_prefetch_l2(src + r * kPDm, (uint32_t)(min(64LL, rows - r) * kPDm * 4));
+        }
+    };
     if (tid == 0)
         for (int n = 0; n < min(2, ntiles); n++) load_q(n);
-    const uint32_t idesc = idesc_bf16_f32(128, 128, true, true);
+    prefetch_dout(0);
+    prefetch_dout(1);
+    const uint32_t idesc = idesc_bf16_f32(128, 256, true, true);
     for (int n = 0; n < ntiles; n++) {
         const int st = n & 1;
+        prefetch_dout(n + 2);
         if (tid == 0 && n >= 1 && n + 1 < ntiles) {  // q stage of tile n-1 is free once its product is done
             if (!mbar_wait(&s.bar_mma[(n - 1) & 1], ((n - 1) >> 1) & 1, kPWait)) atomicCAS(err, 0, 2);
             load_q(n + 1);
@@ -109,13 +125,20 @@ bwd_piece_tc_kernel(const __grid_constant__ CUtensorMap map_q, const float *__re
             w = lam[gi * L + lev] * __expf((float)(Pb[t >> cbits] - Pref) + gamma[gi]);
         }
         const float4 *src = reinterpret_cast<const float4 *>(dout + ((long long)bh * T + (t < t_hi ? t : t_lo)) * kPDm);
-#pragma unroll 4
-        for (int ch = 8 * half; ch < 8 * half + 8; ch++) {
-            float4 a = make_float4(0.f, 0.f, 0.f, 0.f), c = a;
+        float4 av[8], cv[8];  // all of the half row's loads first
+#pragma unroll
+        for (int q8 = 0; q8 < 8; q8++) {
+            const int ch = 8 * half + q8;
+            av[q8] = cv[q8] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (t < t_hi) {
-                a = src[2 * ch];
-                c = src[2 * ch + 1];
+                av[q8] = src[2 * ch];
+                cv[q8] = src[2 * ch + 1];
             }
+        }
+#pragma unroll
+        for (int q8 = 0; q8 < 8; q8++) {
+            const int ch = 8 * half + q8;
+            const float4 a = av[q8], c = cv[q8];
             const float x[8] = {a.x * w, a.y * w, a.z * w, a.w * w, c.x * w, c.y * w, c.z * w, c.w * w};
             uint4 h, l;
             __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&h);
@@ -128,8 +151,8 @@ bwd_piece_tc_kernel(const __grid_constant__ CUtensorMap map_q, const float *__re
                 l2[u] = __floats2bfloat162_rn(x[2 * u] - hf.x, x[2 * u + 1] - hf.y);
             }
             const uint32_t off = (ch >> 3) * kPH + sw128_offset(p, ch & 7);
-            *reinterpret_cast<uint4 *>(s.bhi[st] + off) = h;
-            *reinterpret_cast<uint4 *>(s.blo[st] + off) = l;
+            *reinterpret_cast<uint4 *>(s.b[st].hi + off) = h;
+            *reinterpret_cast<uint4 *>(s.b[st].lo + off) = l;
         }
         fence_proxy_async_smem();
         if (!mbar_wait(&s.bar_load[st], (n >> 1) & 1, kPWait)) atomicCAS(err, 0, 1);
@@ -137,12 +160,9 @@ bwd_piece_tc_kernel(const __grid_constant__ CUtensorMap map_q, const float *__re
         if (tid == 0) {
             tc_fence_after_sync();
 #pragma unroll
-            for (int kk = 0; kk < 8; kk++) {
-                const uint64_t a = desc_sw128(smem_u32(s.q[st]) + kk * 2048, kPH, 1024);
-                umma_bf16(tm, a, desc_sw128(smem_u32(s.bhi[st]) + kk * 2048, kPH, 1024), idesc,
-                          (n > 0 || kk > 0) ? 1u : 0u);
-                umma_bf16(tm, a, desc_sw128(smem_u32(s.blo[st]) + kk * 2048, kPH, 1024), idesc, 1u);
-            }
+            for (int kk = 0; kk < 8; kk++)
+                umma_bf16(tm, desc_sw128(smem_u32(s.q[st]) + kk * 2048, kPH, 1024),
+                          desc_sw128(smem_u32(s.b[st].hi) + kk * 2048, kPH, 1024), idesc, (n > 0 || kk > 0) ? 1u : 0u);
             umma_commit(&s.bar_mma[st]);
         }
     }
@@ -155,18 +175,20 @@ bwd_piece_tc_kernel(const __grid_constant__ CUtensorMap map_q, const float *__re
     const uint32_t lane_off = (uint32_t)((p >> 5) * 32) << 16;
 #pragma unroll 1
     for (int cb = 64 * half; cb < 64 * half + 64; cb += 16) {
-        float x[16];
+        float x[16], y[16];  // piece_hi + piece_lo
         tmem_ld16(tm + lane_off + cb, x);
+        tmem_ld16(tm + lane_off + kPDm + cb, y);
         tmem_ld_wait();
 #pragma unroll
         for (int u = 0; u < 4; u++)
-            *out_tile_piece(tile, p, cb / 4 + u) = make_float4(x[4 * u], x[4 * u + 1], x[4 * u + 2], x[4 * u + 3]);
+            *out_tile_piece(tile, p, cb / 4 + u) = make_float4(x[4 * u] + y[4 * u], x[4 * u + 1] + y[4 * u + 1],
+                                                               x[4 * u + 2] + y[4 * u + 2], x[4 * u + 3] + y[4 * u + 3]);
     }
     __syncthreads();
     out_tile_store<kPThreads, false>(part + (((long long)bh * gridDim.x) + blockIdx.x) * kPDm * kPDm, tile, kPT);
     tc_fence_before_sync();
     __syncthreads();
-    if (tid < 32) tmem_dealloc(tm, 128);
+    if (tid < 32) tmem_dealloc(tm, 256);
 }
 
 }  // namespace

@@ -106,13 +106,24 @@ bwd_query_tc_kernel(const Tin *__restrict__ q, const float *__restrict__ dout, c
     const int nrows = (int)min((long long)kQT, (long long)T - (long long)pair * kQT);
     {
         uint8_t *d0[2] = {s.ohi, s.olo};
-        stage_split_tile<2, kQThreads>(d0, dout + ((long long)bh * T + (long long)pair * kQT) * kQD, kQD, nullptr,
-                                       1.f, nrows);
+        stage_split_tile<2, kQThreads, 8>(d0, dout + ((long long)bh * T + (long long)pair * kQT) * kQD, kQD,
+                                          nullptr, 1.f, nrows);
     }
     const float *node_base = nodes + (long long)bh * N * kQD * kQD;
+    // the fp32 nodes come from DRAM: each is prefetched into L2 two nodes
+    // before it is staged
+    auto prefetch_node = [&](int n) {
+        if (tid == 0 && n < np) {
+            const float *src = node_base + (long long)js[n] * kQD * kQD;
+            bulk_prefetch_l2(src, kQD * kQD * 2);
+            bulk_prefetch_l2(src + kQD * kQD / 2, kQD * kQD * 2);
+        }
+    };
+    prefetch_node(1);
+    prefetch_node(2);
     {
         uint8_t *d1[2] = {s.nhi[0], s.nlo[0]};
-        stage_split_tile<2, kQThreads>(d1, node_base + (long long)js[0] * kQD * kQD, kQD, nullptr, 1.f, kQD);
+        stage_split_tile<2, kQThreads, 8>(d1, node_base + (long long)js[0] * kQD * kQD, kQD, nullptr, 1.f, kQD);
     }
     fence_proxy_async_smem();
     tc_fence_before_sync();
@@ -178,8 +189,10 @@ bwd_query_tc_kernel(const Tin *__restrict__ q, const float *__restrict__ dout, c
             // stage node n+1 into the other buffer once node n-1's product is done
             const int b1 = (n + 1) & 1;
             if (n >= 1 && !mbar_wait(&s.bar_mma[b1], ((n - 1) >> 1) & 1, kQWait)) q_err(err, 2);
+            prefetch_node(n + 3);
             uint8_t *d1[2] = {s.nhi[b1], s.nlo[b1]};
-            stage_split_tile<2, kQThreads>(d1, node_base + (long long)js[n + 1] * kQD * kQD, kQD, nullptr, 1.f, kQD);
+            stage_split_tile<2, kQThreads, 8>(d1, node_base + (long long)js[n + 1] * kQD * kQD, kQD, nullptr, 1.f,
+                                              kQD);
             fence_proxy_async_smem();
         }
         drain(n);  // contains a barrier of all threads: node n+1 is staged and U_{n-1} drained
