@@ -6,7 +6,7 @@
 // read-out) and §2.3 (the hierarchical mask computed chunkwise with matmuls).
 //
 // Five launches.  Two small kernels form the fp64 tile-gate prefix sums.  Node
-// walkers (one CTA per head, dv slice and segment of tiles, walking in order
+// walkers (one CTA per head and segment of tiles, the whole dv width, walking in order
 // with the Fenwick stack in tensor memory) compute each tile's state and
 // publish the tile-level Fenwick nodes; a fix-up kernel chains the nodes that
 // span segments.  The read-out consumer (persistent: one CTA per SM taking
