@@ -115,7 +115,8 @@ bwd_intra_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
                     const __grid_constant__ CUtensorMap map_v, const float *__restrict__ dout,
                     const float *__restrict__ gamma, const float *__restrict__ lam, float *__restrict__ dq,
                     float *__restrict__ dk, float *__restrict__ dv, float *__restrict__ dlam, int T, int L,
-                    int *__restrict__ err)
+                    const __nv_bfloat16 *__restrict__ q16, const __nv_bfloat16 *__restrict__ k16,
+                    const __nv_bfloat16 *__restrict__ v16, int nsm, int *__restrict__ err)
 {
     extern __shared__ uint8_t smem_raw[];
     IntraSmem &s = *reinterpret_cast<IntraSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -172,6 +173,21 @@ bwd_intra_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_cons
         umma_commit(&s.bar_mma);
     }
     if (!mbar_wait(&s.bar_mma, 0, kIWait)) atomicCAS(err, 0, 2);
+    if (tid == 0) {
+        // this tile's inputs are in: the CTA that will run next on this SM (one
+        // CTA per SM, launched in order) gets its q, k, v and dO rows into L2
+        // while this one computes, instead of all CTAs of a wave loading at once
+        const long long nxt = (long long)blockIdx.y * gridDim.x + blockIdx.x + nsm;
+        if (nxt < (long long)gridDim.x * gridDim.y) {
+            const long long r0 = (nxt % gridDim.x) * kIT, b2 = nxt / gridDim.x;
+            const long long rows = min((long long)kIT, (long long)T - r0);
+            const long long e0 = (b2 * T + r0) * kID;
+            prefetch_l2(dout + e0, rows * kID * 4);
+            prefetch_l2(q16 + e0, rows * kID * 2);
+            prefetch_l2(k16 + e0, rows * kID * 2);
+            prefetch_l2(v16 + e0, rows * kID * 2);
+        }
+    }
     tc_fence_after_sync();
     // this thread's 32 columns of the row's chunk block: W1, W2 and the level
     // gradients (partial sums; the two halves meet before dlambda is written)
@@ -312,7 +328,8 @@ cudaError_t bwd_intra_tc(const BwdArgs &A, const float *gamma, int *err)
     cudaError_t e = cudaFuncSetAttribute(bwd_intra_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     bwd_intra_tc_kernel<<<dim3((A.T + kIT - 1) / kIT, BH), kIThreads, smem, (cudaStream_t)A.stream>>>(
-        mq, mk, mv, A.dout, gamma, A.lam, A.dq, A.dkey, A.dval, A.dlam, A.T, A.L, err);
+        mq, mk, mv, A.dout, gamma, A.lam, A.dq, A.dkey, A.dval, A.dlam, A.T, A.L, (const __nv_bfloat16 *)A.q,
+        (const __nv_bfloat16 *)A.k, (const __nv_bfloat16 *)A.v, bwd_sm_count(), err);
     return cudaPeekAtLastError();
 }
 

@@ -61,4 +61,27 @@ bool bwd_piece_tc_supported(const BwdArgs &A);
 cudaError_t bwd_piece_tc(const BwdArgs &A, const float *gamma, const double *P, float *part, int nlev, int Pc,
                          int nitems, int *err);
 
+
+// Number of SMs of the current device (the tensor-core backward kernels run
+// one CTA per SM, so the CTA that follows CTA x on an SM is about x + this).
+inline int bwd_sm_count()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        n <= 0)
+        n = 148;
+    return n;
+}
+
+// Prefetch [p, p + bytes) into L2 (bytes a multiple of 16, p 16-byte aligned),
+// in pieces of at most 32 KB.
+__device__ __forceinline__ void prefetch_l2(const void *p, long long bytes)
+{
+    const char *c = static_cast<const char *>(p);
+    for (long long o = 0; o < bytes; o += 32768) {
+        const long long n = bytes - o < 32768 ? bytes - o : 32768;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(c + o), "r"((uint32_t)n) : "memory");
+    }
+}
+
 }  // namespace lla
