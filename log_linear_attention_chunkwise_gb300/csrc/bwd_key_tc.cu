@@ -32,6 +32,7 @@ constexpr int kKD = 128;                      // dk = dv
 constexpr uint32_t kKBuf = kKT * kKD * 2;     // bf16 128 x 128: 32 KB
 constexpr uint32_t kKHalf = kKBuf / 2;
 constexpr int kKThreads = 256;  // staging: twice the loads in flight; drain: a row's two column halves
+constexpr int kKAllThreads = kKThreads + 32;  // plus one warp whose lane 0 issues the products
 constexpr uint32_t kKWait = 1u << 22;
 
 struct __align__(1024) KeySmem {
@@ -39,9 +40,11 @@ struct __align__(1024) KeySmem {
     uint8_t v[kKBuf];
     uint8_t rhi[2][kKBuf];
     uint8_t rlo[2][kKBuf];
-    uint64_t bar_load, bar_mma[2], bar_done;
+    uint64_t bar_load, bar_mma[2], bar_done, bar_staged[2];
     uint32_t tmem;
 };
+
+__device__ __forceinline__ void work_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 __device__ __forceinline__ void key_err(int *err, int code) { atomicCAS(err, 0, code); }
 
@@ -58,7 +61,7 @@ __device__ __forceinline__ void mma8(uint32_t d, const uint8_t *a, const uint8_t
     }
 }
 
-__global__ void __launch_bounds__(kKThreads, 1)
+__global__ void __launch_bounds__(kKAllThreads, 1)
 bwd_key_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                   const float *__restrict__ gamma, const double *__restrict__ P, const float *__restrict__ R,
                   const float *__restrict__ part, float *__restrict__ dk, float *__restrict__ dv, int T, int N,
@@ -85,6 +88,8 @@ bwd_key_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_consta
         mbar_init(&s.bar_mma[0], 1);
         mbar_init(&s.bar_mma[1], 1);
         mbar_init(&s.bar_done, 1);
+        mbar_init(&s.bar_staged[0], kKThreads);
+        mbar_init(&s.bar_staged[1], kKThreads);
         fence_mbar_init();
         tma_prefetch_map(&map_k);
         tma_prefetch_map(&map_v);
@@ -126,8 +131,30 @@ bwd_key_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_consta
     };
     prefetch_state(0);
     prefetch_state(1);
-    bool acc_started = false;
-    if (!mbar_wait(&s.bar_load, 0, kKWait)) key_err(err, 1);
+    // The 256 staging threads stage level n into buffer n & 1 and signal it;
+    // one thread of the extra warp issues its products, so no staging thread
+    // waits for the issue.
+    if (tid >= kKThreads) {
+        if (tid == kKThreads) {
+            bool acc_started = false;
+            if (!mbar_wait(&s.bar_load, 0, kKWait)) key_err(err, 1);
+            for (int n = 0; n < total; n++) {
+                const int buf = n & 1;
+                const bool is0 = lev0 && n == 0;
+                if (!mbar_wait(&s.bar_staged[buf], (n >> 1) & 1, kKWait)) key_err(err, 2);
+                tc_fence_after_sync();
+                const uint32_t dk_acc = is0 ? acc_k0 : acc_k, dv_acc = is0 ? acc_v0 : acc_v;
+                const bool acc = is0 ? false : acc_started;
+                mma8(dk_acc, s.v, s.rhi[buf], id_kk, true, acc);
+                mma8(dk_acc, s.v, s.rlo[buf], id_kk, true, true);
+                mma8(dv_acc, s.k, s.rhi[buf], id_kmn, false, acc);
+                mma8(dv_acc, s.k, s.rlo[buf], id_kmn, false, true);
+                umma_commit(&s.bar_mma[buf]);
+                if (!is0) acc_started = true;
+            }
+            umma_commit(&s.bar_done);
+        }
+    } else {
     for (int n = 0; n < total; n++) {
         const int buf = n & 1;
         const bool is0 = lev0 && n == 0;
@@ -139,20 +166,8 @@ bwd_key_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_consta
         if (n >= 2 && !mbar_wait(&s.bar_mma[buf], ((n - 2) >> 1) & 1, kKWait)) key_err(err, 2);
         stage(buf, Rm, c);
         fence_proxy_async_smem();
-        __syncthreads();
-        if (tid == 0) {
-            tc_fence_after_sync();
-            const uint32_t dk_acc = is0 ? acc_k0 : acc_k, dv_acc = is0 ? acc_v0 : acc_v;
-            const bool acc = is0 ? false : acc_started;
-            mma8(dk_acc, s.v, s.rhi[buf], id_kk, true, acc);
-            mma8(dk_acc, s.v, s.rlo[buf], id_kk, true, true);
-            mma8(dv_acc, s.k, s.rhi[buf], id_kmn, false, acc);
-            mma8(dv_acc, s.k, s.rlo[buf], id_kmn, false, true);
-            umma_commit(&s.bar_mma[buf]);
-        }
-        if (!is0) acc_started = true;
+        mbar_arrive(&s.bar_staged[buf]);
     }
-    if (tid == 0) umma_commit(&s.bar_done);
     if (!mbar_wait(&s.bar_done, 0, kKWait)) key_err(err, 2);
     tc_fence_after_sync();
     // drain: row p; weights rho (shared levels) and f0 (level 0, first chunk)
@@ -186,11 +201,12 @@ bwd_key_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_consta
                 *out_tile_piece(tile, p, cb / 4 + u) = make_float4(a[0], a[1], a[2], a[3]);
             }
         }
-        __syncthreads();
+        work_sync();
         out_tile_store<kKThreads, true>((which == 0 ? dk : dv) + ((long long)bh * T + (long long)pair * kKT) * kKD,
                                         tile, nrows);
-        __syncthreads();
+        work_sync();
     }
+    }  // staging threads
     tc_fence_before_sync();
     __syncthreads();
     if (tid < 32) tmem_dealloc(tm, 512);
@@ -214,7 +230,7 @@ cudaError_t bwd_key_tc(const BwdArgs &A, const float *gamma, const double *P, co
     const size_t smem = sizeof(KeySmem) + 1024;
     cudaError_t e = cudaFuncSetAttribute(bwd_key_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    bwd_key_tc_kernel<<<dim3((N + 1) / 2, BH), kKThreads, smem, (cudaStream_t)A.stream>>>(
+    bwd_key_tc_kernel<<<dim3((N + 1) / 2, BH), kKAllThreads, smem, (cudaStream_t)A.stream>>>(
         mk, mv, gamma, P, R, part, A.dkey, A.dval, A.T, N, nlev, nblocks, Pc, nitems, err);
     return cudaPeekAtLastError();
 }
