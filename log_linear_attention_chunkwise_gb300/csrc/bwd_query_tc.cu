@@ -9,7 +9,9 @@
 // is one product over all 128 rows, with weight 0 on the rows it does not
 // concern.  U = dO Node^T runs on the tensor cores with dO and the node (both
 // fp32) split into bf16 high and remainder parts (three products: hi.hi,
-// hi.lo, lo.hi); a two-deep ring of node stages and of accumulators lets the
+// hi.lo, lo.hi: dO_hi times [Node_hi | Node_lo] as one N = 256 product into
+// two accumulators, then dO_lo times Node_hi into the first, and the drain
+// adds the two); a two-deep ring of node stages and of accumulator pairs lets the
 // staging of node n+1 and the product of node n overlap the drain of node
 // n-1.  Eight warps drain: thread = (row, half of the 128 columns); the two
 // halves' q.U partial sums meet in shared memory.  Results are added to dq
@@ -33,7 +35,8 @@ constexpr int kQMaxPath = 20;
 
 struct __align__(1024) QuerySmem {
     uint8_t ohi[kQBuf], olo[kQBuf];     // dO tile, high and remainder parts
-    uint8_t nhi[2][kQBuf], nlo[2][kQBuf];  // node stages
+    uint8_t nd[2][2 * kQBuf];           // node stages: per 64-column K block, the high part's
+                                        // 128 rows then the remainder's (one N = 256 operand)
     float part[2][kQT];                 // q.U partial sums of the second half
     float wt[kQMaxPath][kQT];           // per path node and row: exp(G_t - P_j) (0 where it does not apply)
     float lwt[kQMaxPath][kQT];          // the same times lambda_t at the node's level
@@ -44,17 +47,6 @@ struct __align__(1024) QuerySmem {
 __device__ __forceinline__ void q_err(int *err, int code) { atomicCAS(err, 0, code); }
 
 __device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
-
-// 8 MMAs over K = 128, A and B K-major.
-__device__ __forceinline__ void mma8k(uint32_t d, const uint8_t *a, const uint8_t *b, uint32_t idesc, bool acc)
-{
-#pragma unroll
-    for (int kk = 0; kk < 8; kk++) {
-        const uint32_t off = (kk >> 2) * kQHalf + (kk & 3) * 32;
-        umma_bf16(d, desc_sw128(smem_u32(a) + off, 16, 1024), desc_sw128(smem_u32(b) + off, 16, 1024), idesc,
-                  (acc || kk > 0) ? 1u : 0u);
-    }
-}
 
 template <typename Tin>
 __global__ void __launch_bounds__(kQThreads, 1)
@@ -86,7 +78,7 @@ bwd_query_tc_kernel(const Tin *__restrict__ q, const float *__restrict__ dout, c
         fence_mbar_init();
     }
     if (tid < 32) {
-        tmem_alloc(&s.tmem, 256);
+        tmem_alloc(&s.tmem, 512);
         tmem_relinquish();
     }
     // read-out weights of every path node for this row (the halves split the
@@ -122,8 +114,9 @@ bwd_query_tc_kernel(const Tin *__restrict__ q, const float *__restrict__ dout, c
     prefetch_node(1);
     prefetch_node(2);
     {
-        uint8_t *d1[2] = {s.nhi[0], s.nlo[0]};
-        stage_split_tile<2, kQThreads, 8>(d1, node_base + (long long)js[0] * kQD * kQD, kQD, nullptr, 1.f, kQD);
+        uint8_t *d1[2] = {s.nd[0], s.nd[0] + kQHalf};
+        stage_split_tile<2, kQThreads, 8, 2 * kQHalf>(d1, node_base + (long long)js[0] * kQD * kQD, kQD, nullptr, 1.f,
+                                                      kQD);
     }
     fence_proxy_async_smem();
     tc_fence_before_sync();
@@ -131,6 +124,7 @@ bwd_query_tc_kernel(const Tin *__restrict__ q, const float *__restrict__ dout, c
     tc_fence_after_sync();
     const uint32_t tm = s.tmem;
     const uint32_t idesc = idesc_bf16_f32(128, 128, false, false);
+    const uint32_t idesc2 = idesc_bf16_f32(128, 256, false, false);
     // this thread's q half row (16-byte loads), and G_t
     float qv[64];
     {
@@ -153,9 +147,19 @@ bwd_query_tc_kernel(const Tin *__restrict__ q, const float *__restrict__ dout, c
     auto issue = [&](int n) {
         const int b = n & 1;
         tc_fence_after_sync();
-        mma8k(tm + b * 128, s.ohi, s.nhi[b], idesc, false);
-        mma8k(tm + b * 128, s.ohi, s.nlo[b], idesc, true);
-        mma8k(tm + b * 128, s.olo, s.nhi[b], idesc, true);
+        const uint32_t acc = tm + b * 256;  // [dO_hi Node_hi^T + dO_lo Node_hi^T | dO_hi Node_lo^T]
+#pragma unroll
+        for (int kk = 0; kk < 8; kk++) {
+            const uint32_t offa = (kk >> 2) * kQHalf + (kk & 3) * 32, offb = (kk >> 2) * (2 * kQHalf) + (kk & 3) * 32;
+            umma_bf16(acc, desc_sw128(smem_u32(s.ohi) + offa, 16, 1024), desc_sw128(smem_u32(s.nd[b]) + offb, 16, 1024),
+                      idesc2, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; kk++) {
+            const uint32_t offa = (kk >> 2) * kQHalf + (kk & 3) * 32, offb = (kk >> 2) * (2 * kQHalf) + (kk & 3) * 32;
+            umma_bf16(acc, desc_sw128(smem_u32(s.olo) + offa, 16, 1024), desc_sw128(smem_u32(s.nd[b]) + offb, 16, 1024),
+                      idesc, 1u);
+        }
         umma_commit(&s.bar_mma[b]);
     };
     auto drain = [&](int n) {
@@ -169,9 +173,12 @@ bwd_query_tc_kernel(const Tin *__restrict__ q, const float *__restrict__ dout, c
         float dot = 0.f;
 #pragma unroll
         for (int c0c = 0; c0c < 64; c0c += 16) {
-            float u[16];
-            tmem_ld16(tm + b * 128 + lane_off + half * 64 + c0c, u);
+            float u[16], u2[16];
+            tmem_ld16(tm + b * 256 + lane_off + half * 64 + c0c, u);
+            tmem_ld16(tm + b * 256 + 128 + lane_off + half * 64 + c0c, u2);
             tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; e++) u[e] += u2[e];
 #pragma unroll
             for (int e = 0; e < 16; e++) {
                 dqa[c0c + e] = fmaf(lw, u[e], dqa[c0c + e]);
@@ -190,9 +197,9 @@ bwd_query_tc_kernel(const Tin *__restrict__ q, const float *__restrict__ dout, c
             const int b1 = (n + 1) & 1;
             if (n >= 1 && !mbar_wait(&s.bar_mma[b1], ((n - 1) >> 1) & 1, kQWait)) q_err(err, 2);
             prefetch_node(n + 3);
-            uint8_t *d1[2] = {s.nhi[b1], s.nlo[b1]};
-            stage_split_tile<2, kQThreads, 8>(d1, node_base + (long long)js[n + 1] * kQD * kQD, kQD, nullptr, 1.f,
-                                              kQD);
+            uint8_t *d1[2] = {s.nd[b1], s.nd[b1] + kQHalf};
+            stage_split_tile<2, kQThreads, 8, 2 * kQHalf>(d1, node_base + (long long)js[n + 1] * kQD * kQD, kQD,
+                                                          nullptr, 1.f, kQD);
             fence_proxy_async_smem();
         }
         drain(n);  // contains a barrier of all threads: node n+1 is staged and U_{n-1} drained
@@ -208,7 +215,7 @@ bwd_query_tc_kernel(const Tin *__restrict__ q, const float *__restrict__ dout, c
     out_tile_store<kQThreads, true>(dq + ((long long)bh * T + (long long)pair * kQT) * kQD, tile, nrows);
     tc_fence_before_sync();
     __syncthreads();
-    if (tid < 32) tmem_dealloc(tm, 256);
+    if (tid < 32) tmem_dealloc(tm, 512);
 }
 
 }  // namespace

@@ -16,9 +16,12 @@ namespace lla {
 
 // Rows [0, 128) of src (row stride ld floats); row r scaled by
 // all * scale[r] (scale nullptr: all) and rows >= nrows written as 0.  NPARTS = 2 or 3; part p goes
-// to dst[p].  NTHREADS threads (a multiple of 32) call it together; each
-// issues the loads of GROUP rows before converting them.
-template <int NPARTS, int NTHREADS, int GROUP = 4>
+// to dst[p], its second 64-column block BLK bytes after its first (16 KB:
+// the two blocks of one tile back to back; 32 KB: the blocks of two parts
+// interleaved, the layout of an N = 256 operand).  NTHREADS threads (a
+// multiple of 32) call it together; each issues the loads of GROUP rows
+// before converting them.
+template <int NPARTS, int NTHREADS, int GROUP = 4, uint32_t BLK = 128 * 128>
 __device__ __forceinline__ void stage_split_tile(uint8_t *const *dst, const float *src, long long ld,
                                                  const float *scale, float all, int nrows)
 {
@@ -65,7 +68,7 @@ __device__ __forceinline__ void stage_split_tile(uint8_t *const *dst, const floa
                 b -= f.y;
             }
         }
-        const uint32_t off = blk * (128 * 128) + sm100::sw128_offset(r, chunk);
+        const uint32_t off = blk * BLK + sm100::sw128_offset(r, chunk);
 #pragma unroll
         for (int p = 0; p < NPARTS; p++) *reinterpret_cast<uint4 *>(dst[p] + off) = part[p];
         }
