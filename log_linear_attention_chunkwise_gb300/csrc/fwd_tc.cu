@@ -695,13 +695,15 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
                 int jnext = i;
                 if (npath > 0) {
                     if (!mbar_wait(&s.bar_s, n & 1, prm.s_wait_iters)) set_err(prm.err, kErrMmaTimeout);
+                    // with the lambda MLP, h = K W1 was issued after S and reads K too
+                    if (prm.mlp && !mbar_wait(&s.bar_h, n & 1, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
                     if (!dep_done) {
                         // the nodes come from the previous launches; everything before this
                         // point reads only inputs and the gate sums
                         grid_dependency_wait();
                         dep_done = true;
                     }
-                    load_node(0, jnext);  // the K buffer is free once S is done
+                    load_node(0, jnext);  // the K buffer is free once S (and h) are done
                     jnext -= (jnext & -jnext);
                 }
                 // O = P V: P from tensor memory once the epilogue has stored it
@@ -737,8 +739,16 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
                         s_early = true;
                     }
                 }
+                // Node k+2 goes into buffer b as soon as U_k has read it, before U_{k+1}
+                // waits for its own node
                 for (int k = 0; k < npath; k++) {
                     const int b = k & 1, b1 = b ^ 1;
+                    if (k + 2 < npath) {
+                        // node buffer b is free once U_k's product is done
+                        if (!mbar_wait(&s.bar_u[b], last_u_par(b), prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
+                        load_node(b, jnext);
+                        jnext -= (jnext & -jnext);
+                    }
                     if (k + 1 < npath) {
                         // slot b1 is free once U_{k-1} (or, for k = 0, P V) is drained
                         if (k == 0) {
@@ -750,12 +760,6 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
                         }
                         wait_node(b1);
                         issue_u(b1);
-                    }
-                    if (k + 2 < npath) {
-                        // node buffer b is free once U_k's product is done
-                        if (!mbar_wait(&s.bar_u[b], last_u_par(b), prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
-                        load_node(b, jnext);
-                        jnext -= (jnext & -jnext);
                     }
                 }
             }
