@@ -559,7 +559,7 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
         // The output of the tile that last used a stage, staged there by the
         // epilogue, is written out by TMA from here before the stage is
         // refilled, so the epilogue never waits for the store.
-        auto store_out = [&](int sgx, int nx) {  // lane 0: tile nx of stage sgx
+        auto issue_store = [&](int sgx, int nx) {  // lane 0: tile nx of stage sgx
             if (!mbar_wait(&s.bar_staged[sgx], (nx >> 1) & 1, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
             int io, bho;
             item_tile(s.item[sgx], NT, BH, &io, &bho);
@@ -572,32 +572,40 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
                 for (int h = 0; h < D / 64; h++) tma_store_3d(&map_out, t.q + h * kBlk, h * 64, io * kTile, bho);
             }
             tma_store_commit();
-            tma_store_wait_read();  // the stage may be refilled; the writes finish with the kernel
         };
         bool dep_done = false;
         for (int n = 0;; n++) {
             const int sg = n & 1;
-            if (n >= 2 && lane == 0) store_out(sg, n - 2);
-            __syncwarp();
+            // the next work item and the P values at its path nodes, fetched while
+            // the tile that last used this stage may still be reading out
             int w = 0;
             if (lane == 0) w = atomicAdd(prm.queue, 1);
             w = __shfl_sync(0xffffffffu, w, 0);
-            if (w >= total) {
+            const bool have = w < total;
+            int i = 0, bh = 0, j = 0;
+            double pv = 0.0;
+            if (have) {
+                item_tile(w, NT, BH, &i, &bh);
+                const double *Pb = prm.P + (long long)bh * (NT + 1);
+                // lane c clears the c lowest set bits of i; lane 31 takes P_i
+                j = i;
+                for (int c = 0; c < lane && j > 0; c++) j -= (j & -j);
+                if (lane < kMaxPath && j > 0) pv = Pb[j];
+                if (lane == 31) pv = Pb[i];
+            }
+            if (n >= 2 && lane == 0) issue_store(sg, n - 2);
+            __syncwarp();
+            if (!have) {
                 if (lane == 0) {
                     s.item[sg] = -1;
                     mbar_arrive(&s.bar_load[sg]);
-                    if (n >= 1) store_out(sg ^ 1, n - 1);  // the last tile taken
+                    if (n >= 1) issue_store(sg ^ 1, n - 1);  // the last tile taken
+                    tma_store_wait_read();  // the stores read shared memory before the CTA ends
                 }
                 break;
             }
-            int i, bh;
-            item_tile(w, NT, BH, &i, &bh);
-            const double *Pb = prm.P + (long long)bh * (NT + 1);
-            // P at the path nodes: lane c clears the c lowest set bits of i
-            int j = i;
-            for (int c = 0; c < lane && j > 0; c++) j -= (j & -j);
-            if (lane < kMaxPath && j > 0) s.pj[sg][lane] = Pb[j];
-            if (lane == 31) s.pj[sg][kMaxPath] = Pb[i];
+            if (lane < kMaxPath && j > 0) s.pj[sg][lane] = pv;
+            if (lane == 31) s.pj[sg][kMaxPath] = pv;
             if (lane == 0) s.item[sg] = w;
             __syncwarp();
             if (lane == 0) {
@@ -606,16 +614,20 @@ lla_readout_consumer_kernel(const __grid_constant__ CUtensorMap map_q, const __g
                 uint64_t *bar = &s.bar_load[sg];
                 mbar_arrive_expect_tx(bar, 3 * kT + lam_bytes + kTile * 4);
                 ConsStage<D> &t = s.st[sg];
+                // V, lambda and gamma first; q and k once the store has read the
+                // output staged in their buffers
 #pragma unroll
-                for (int h = 0; h < D / 64; h++) {
-                    tma_load_3d(t.q + h * kBlk, &map_q, bar, h * 64, i * kTile, bh);
-                    tma_load_3d(t.k + h * kBlk, &map_k, bar, h * 64, i * kTile, bh);
-                    tma_load_3d(t.v + h * kBlk, &map_v, bar, h * 64, i * kTile, bh);
-                }
+                for (int h = 0; h < D / 64; h++) tma_load_3d(t.v + h * kBlk, &map_v, bar, h * 64, i * kTile, bh);
                 const long long tok0 = (long long)bh * prm.T + (long long)i * kTile;
                 if (!prm.mlp)
                     bulk_load(s.aux + sg * kLamStage, prm.lam + tok0 * L, lam_bytes, bar);
                 bulk_load(s.gam[sg], prm.gamma + ((long long)bh * NT + i) * kTile, kTile * 4, bar);
+                if (n >= 2) tma_store_wait_read();
+#pragma unroll
+                for (int h = 0; h < D / 64; h++) {
+                    tma_load_3d(t.q + h * kBlk, &map_q, bar, h * 64, i * kTile, bh);
+                    tma_load_3d(t.k + h * kBlk, &map_k, bar, h * 64, i * kTile, bh);
+                }
             }
             // the tile's path nodes into L2 ahead of their loads (lane c: node c);
             // they come from the previous launches, so wait for those once
