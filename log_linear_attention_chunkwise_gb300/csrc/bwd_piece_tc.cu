@@ -28,23 +28,28 @@ constexpr uint32_t kPH = kPB / 2;
 constexpr int kPThreads = 256;  // (token row, column half)
 constexpr uint32_t kPWait = 1u << 22;
 
+// S stages of (q tile, split dO tile).  With one stage (96 KB) two CTAs share
+// an SM, so one CTA's dO split and drain overlap the other's loads and
+// products; with two, one CTA overlaps its own next load.
+template <int S>
 struct __align__(1024) PieceSmem {
-    uint8_t q[2][kPB];
+    uint8_t q[S][kPB];
     struct __align__(1024) {
         uint8_t hi[kPB], lo[kPB];  // the four 64-column blocks of one N = 256 operand
-    } b[2];
-    uint64_t bar_load[2], bar_mma[2], bar_done;
+    } b[S];
+    uint64_t bar_load[S], bar_mma[S], bar_done;
     uint32_t tmem;
 };
 
-__global__ void __launch_bounds__(kPThreads, 1)
+template <int S>
+__global__ void __launch_bounds__(kPThreads, 3 - S)
 bwd_piece_tc_kernel(const __grid_constant__ CUtensorMap map_q, const float *__restrict__ dout,
                     const float *__restrict__ gamma, const float *__restrict__ lam, const double *__restrict__ P,
                     float *__restrict__ part, int T, int N, int L, int cbits, int nlev, int Pc,
                     int *__restrict__ err)
 {
     extern __shared__ uint8_t smem_raw[];
-    PieceSmem &s = *reinterpret_cast<PieceSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    PieceSmem<S> &s = *reinterpret_cast<PieceSmem<S> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x;
     const int p = tid & 127, half = tid >> 7;  // token row of a tile, half of its columns
     const int bh = blockIdx.y;
@@ -73,7 +78,7 @@ bwd_piece_tc_kernel(const __grid_constant__ CUtensorMap map_q, const float *__re
     const long long t_lo = (long long)p0 << cbits, t_hi = (long long)p1 << cbits;
     const int ntiles = (int)((t_hi - t_lo + kPT - 1) / kPT);
     if (tid == 0) {
-        for (int i = 0; i < 2; i++) {
+        for (int i = 0; i < S; i++) {
             mbar_init(&s.bar_load[i], 1);
             mbar_init(&s.bar_mma[i], 1);
         }
@@ -90,7 +95,7 @@ bwd_piece_tc_kernel(const __grid_constant__ CUtensorMap map_q, const float *__re
     tc_fence_after_sync();
     const uint32_t tm = s.tmem;
     auto load_q = [&](int n) {
-        const int st = n & 1;
+        const int st = n % S;
         mbar_arrive_expect_tx(&s.bar_load[st], kPB);
         tma_load_3d(s.q[st], &map_q, &s.bar_load[st], 0, (int)(t_lo + (long long)n * kPT), bh);
         tma_load_3d(s.q[st] + kPH, &map_q, &s.bar_load[st], 64, (int)(t_lo + (long long)n * kPT), bh);
@@ -105,18 +110,20 @@ bwd_piece_tc_kernel(const __grid_constant__ CUtensorMap map_q, const float *__re
         }
     };
     if (tid == 0)
-        for (int n = 0; n < min(2, ntiles); n++) load_q(n);
+        for (int n = 0; n < min(S, ntiles); n++) load_q(n);
     prefetch_dout(0);
     prefetch_dout(1);
     const uint32_t idesc = idesc_bf16_f32(128, 256, true, true);
     for (int n = 0; n < ntiles; n++) {
-        const int st = n & 1;
+        const int st = n % S;
         prefetch_dout(n + 2);
-        if (tid == 0 && n >= 1 && n + 1 < ntiles) {  // q stage of tile n-1 is free once its product is done
+        if (S == 2 && tid == 0 && n >= 1 && n + 1 < ntiles) {  // q stage of tile n-1 is free once its product is done
             if (!mbar_wait(&s.bar_mma[(n - 1) & 1], ((n - 1) >> 1) & 1, kPWait)) atomicCAS(err, 0, 2);
             load_q(n + 1);
         }
-        if (n >= 2 && !mbar_wait(&s.bar_mma[st], ((n - 2) >> 1) & 1, kPWait)) atomicCAS(err, 0, 2);
+        // the stage is free once the product of tile n - S is done
+        if (n >= S && !mbar_wait(&s.bar_mma[st], ((n - S) / S) & 1, kPWait)) atomicCAS(err, 0, 2);
+        if (S == 1 && tid == 0 && n >= 1) load_q(n);
         // token row p of the tile: w dO, split
         const long long t = t_lo + (long long)n * kPT + p;
         float w = 0.f;
@@ -155,7 +162,7 @@ bwd_piece_tc_kernel(const __grid_constant__ CUtensorMap map_q, const float *__re
             *reinterpret_cast<uint4 *>(s.b[st].lo + off) = l;
         }
         fence_proxy_async_smem();
-        if (!mbar_wait(&s.bar_load[st], (n >> 1) & 1, kPWait)) atomicCAS(err, 0, 1);
+        if (!mbar_wait(&s.bar_load[st], (n / S) & 1, kPWait)) atomicCAS(err, 0, 1);
         __syncthreads();
         if (tid == 0) {
             tc_fence_after_sync();
@@ -169,8 +176,8 @@ bwd_piece_tc_kernel(const __grid_constant__ CUtensorMap map_q, const float *__re
     if (tid == 0) umma_commit(&s.bar_done);
     if (!mbar_wait(&s.bar_done, 0, kPWait)) atomicCAS(err, 0, 2);
     tc_fence_after_sync();
-    // the piece through shared memory (the q stages, free once every product
-    // is done) and out as whole rows
+    // the piece through shared memory (64 KB from the first q stage on, free
+    // once every product is done) and out as whole rows
     float *tile = reinterpret_cast<float *>(s.q[0]);
     const uint32_t lane_off = (uint32_t)((p >> 5) * 32) << 16;
 #pragma unroll 1
@@ -205,10 +212,11 @@ cudaError_t bwd_piece_tc(const BwdArgs &A, const float *gamma, const double *P, 
     const int BH = A.B * A.H, N = A.T / A.C;
     CUtensorMap mq;
     if (!make_map_bf16_3d(&mq, A.q, kPDm, A.T, BH, 64, kPT)) return cudaErrorInvalidValue;
-    const size_t smem = sizeof(PieceSmem) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(bwd_piece_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    constexpr int S = 1;
+    const size_t smem = sizeof(PieceSmem<S>) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(bwd_piece_tc_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    bwd_piece_tc_kernel<<<dim3(nitems, BH), kPThreads, smem, (cudaStream_t)A.stream>>>(
+    bwd_piece_tc_kernel<S><<<dim3(nitems, BH), kPThreads, smem, (cudaStream_t)A.stream>>>(
         mq, A.dout, gamma, A.lam, P, part, A.T, N, A.L, ctz_u32((uint32_t)A.C), nlev, Pc, err);
     return cudaPeekAtLastError();
 }
