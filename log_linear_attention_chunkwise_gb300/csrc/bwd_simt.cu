@@ -592,21 +592,55 @@ bwd_gate_grad_kernel(const Tin *__restrict__ k, const float *__restrict__ lam,
     if (lane == 0) dG[gi] = (double)a;
 }
 
-// dg_r = sum_{u >= r} dG_u per (batch, head), fp64, one CTA of 1024 threads.
+// dg_r = sum_{u >= r} dG_u per (batch, head), fp64.  One CTA of 1024 threads
+// per block of kGateBlk tokens: first the sum of every token after the block
+// (coalesced loads, four in flight per thread; the later blocks are read
+// once per earlier block, from L2), then the suffix sums inside the block,
+// four consecutive tokens per thread.  Every sum runs in a fixed order.
+constexpr int kGateBlk = 4096;
+
+__device__ __forceinline__ double warp_sum_f64(double x)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    return x;
+}
+
 __global__ void __launch_bounds__(1024)
 bwd_gate_scan_kernel(const double *__restrict__ dG, float *__restrict__ dg, int T)
 {
-    __shared__ double part[1024];
     __shared__ double wsum[32];
-    const long long bh = blockIdx.x;
+    __shared__ double after_sh;
+    const long long bh = blockIdx.y;
     const double *src = dG + bh * T;
-    const int per = (T + 1023) / 1024;
-    const int lo = min(T, (int)threadIdx.x * per), hi = min(T, lo + per);
-    double s = 0.0;
-    for (int u = lo; u < hi; u++) s += src[u];
-    // exclusive suffix sum of the per-thread totals
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    double incl = s;  // inclusive suffix within the warp (lanes >= this one)
+    const int b0 = blockIdx.x * kGateBlk, b1 = min(T, b0 + kGateBlk);
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    // the tokens after the block
+    double a0 = 0.0, a1 = 0.0, a2 = 0.0, a3 = 0.0;
+    int u = b1 + tid;
+    for (; u + 3 * 1024 < T; u += 4 * 1024) {
+        a0 += src[u];
+        a1 += src[u + 1024];
+        a2 += src[u + 2048];
+        a3 += src[u + 3072];
+    }
+    for (; u < T; u += 1024) a0 += src[u];
+    const double a = warp_sum_f64((a0 + a1) + (a2 + a3));
+    if (lane == 0) wsum[w] = a;
+    __syncthreads();
+    if (w == 0) {
+        const double x = warp_sum_f64(wsum[lane]);
+        if (lane == 0) after_sh = x;
+    }
+    __syncthreads();
+    const double after = after_sh;
+    // the block
+    const int t0 = b0 + 4 * tid;
+    double x[4];
+#pragma unroll
+    for (int e = 0; e < 4; e++) x[e] = t0 + e < b1 ? src[t0 + e] : 0.0;
+    const double sum4 = (x[0] + x[1]) + (x[2] + x[3]);
+    double incl = sum4;  // inclusive suffix within the warp (lanes >= this one)
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
         const double y = __shfl_down_sync(0xffffffffu, incl, off);
@@ -615,20 +649,21 @@ bwd_gate_scan_kernel(const double *__restrict__ dG, float *__restrict__ dg, int 
     if (lane == 0) wsum[w] = incl;
     __syncthreads();
     if (w == 0) {
-        double x = wsum[lane], wi = x;
+        const double xw = wsum[lane];
+        double wi = xw;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             const double y = __shfl_down_sync(0xffffffffu, wi, off);
             if (lane + off < 32) wi += y;
         }
-        wsum[lane] = wi - x;  // sum over later warps
+        wsum[lane] = wi - xw;  // sum over later warps
     }
     __syncthreads();
-    part[threadIdx.x] = incl - s + wsum[w];  // sum over later threads
-    double run = part[threadIdx.x];
-    for (int u = hi - 1; u >= lo; u--) {
-        run += src[u];
-        dg[bh * T + u] = (float)run;
+    double run = after + (incl - sum4) + wsum[w];  // every token after this thread's four
+#pragma unroll
+    for (int e = 3; e >= 0; e--) {
+        run += x[e];
+        if (t0 + e < b1) dg[bh * T + t0 + e] = (float)run;
     }
 }
 
@@ -779,7 +814,7 @@ cudaError_t launch_bwd(const BwdArgs &A)
     }
     bwd_gate_grad_kernel<Tin><<<dim3((A.T + kThreads / 32 - 1) / (kThreads / 32), BH), kThreads, 0, st>>>(
         (const Tin *)A.k, A.lam, A.dlam, A.dkey, dG, A.T, A.dk, A.L);
-    bwd_gate_scan_kernel<<<BH, 1024, 0, st>>>(dG, A.dg, A.T);
+    bwd_gate_scan_kernel<<<dim3((A.T + kGateBlk - 1) / kGateBlk, BH), 1024, 0, st>>>(dG, A.dg, A.T);
     return cudaPeekAtLastError();
 }
 

@@ -97,24 +97,34 @@ simt_chunk_state_kernel(const Tin *__restrict__ k, const Tin *__restrict__ v,
 __global__ void __launch_bounds__(kThreads)
 simt_gate_prefix_kernel(const float *__restrict__ gam, double *__restrict__ P, int N)
 {
-    __shared__ double part[kThreads];
+    __shared__ double wsum[kThreads / 32];
     const long long bh = blockIdx.x;
     const int per = (N + kThreads - 1) / kThreads;
     const int lo = min(N, (int)threadIdx.x * per), hi = min(N, lo + per);
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     double s = 0.0;
     for (int j = lo; j < hi; j++) s += (double)gam[bh * N + j];
-    part[threadIdx.x] = s;
+    // exclusive prefix of the per-thread sums: within the warp, then over warps
+    double incl = s;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const double y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    if (lane == 31) wsum[w] = incl;
     __syncthreads();
-    if (threadIdx.x == 0) {
-        double run = 0.0;
-        for (int u = 0; u < kThreads; u++) {
-            double x = part[u];
-            part[u] = run;
-            run += x;
+    if (w == 0) {
+        const double xw = lane < kThreads / 32 ? wsum[lane] : 0.0;
+        double wi = xw;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const double y = __shfl_up_sync(0xffffffffu, wi, off);
+            if (lane >= off) wi += y;
         }
+        if (lane < kThreads / 32) wsum[lane] = wi - xw;  // sum over earlier warps
     }
     __syncthreads();
-    double run = part[threadIdx.x];
+    double run = (incl - s) + wsum[w];
     double *Pb = P + bh * (long long)(N + 1);
     for (int j = lo; j < hi; j++) {
         Pb[j] = run;
