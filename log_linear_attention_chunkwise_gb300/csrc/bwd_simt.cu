@@ -407,9 +407,10 @@ bwd_block_piece_kernel(const Tin *__restrict__ q, const float *__restrict__ dout
 }
 
 // R_{m,b} = sum of its pieces in piece order (bitwise reproducible).  One
-// CTA per odd block of the levels whose blocks span several pieces
-// (2^m > Pc); a ragged last block of one piece exits (block_state reads the
-// piece itself, as for every block of the lower levels).
+// CTA per (odd block, slice of its elements) of the levels whose blocks span
+// several pieces (2^m > Pc); a ragged last block of one piece exits
+// (block_state reads the piece itself, as for every block of the lower
+// levels).
 __global__ void __launch_bounds__(kThreads)
 bwd_block_reduce_kernel(const float *__restrict__ part, float *__restrict__ R, int Dk, int Dv, int N,
                         int nlev, int Pc, int nitems, int nblocks)
@@ -436,9 +437,23 @@ bwd_block_reduce_kernel(const float *__restrict__ part, float *__restrict__ R, i
                         ((bh * nitems) + first + (b / 2) * pp) * (long long)(Dk * Dv / 4);
     float4 *dst = reinterpret_cast<float4 *>(R) + ((bh * nblocks) + off + b) * (long long)(Dk * Dv / 4);
     const int E4 = Dk * Dv / 4;
-    for (int e = threadIdx.x; e < E4; e += kThreads) {
+    // slice blockIdx.z of the block's elements; the pieces are added in piece
+    // order, four loads issued before their additions
+    const int per = (E4 + gridDim.z - 1) / gridDim.z;
+    const int e_lo = blockIdx.z * per, e_hi = min(E4, e_lo + per);
+    for (int e = e_lo + threadIdx.x; e < e_hi; e += kThreads) {
         float4 acc = src[e];
-        for (int p = 1; p < npieces; p++) {
+        int p = 1;
+        for (; p + 3 < npieces; p += 4) {
+            float4 x[4];
+#pragma unroll
+            for (int u = 0; u < 4; u++) x[u] = src[(long long)(p + u) * E4 + e];
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                acc.x += x[u].x; acc.y += x[u].y; acc.z += x[u].z; acc.w += x[u].w;
+            }
+        }
+        for (; p < npieces; p++) {
             const float4 x = src[(long long)p * E4 + e];
             acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
         }
@@ -796,7 +811,7 @@ cudaError_t launch_bwd(const BwdArgs &A)
         }
         const int nred = multi_piece_blocks(N, Pc);
         if (nred > 0)
-            bwd_block_reduce_kernel<<<dim3(nred, BH), kThreads, 0, st>>>(parts, R, A.dk, A.dv, N, nlev, Pc, nitems,
+            bwd_block_reduce_kernel<<<dim3(nred, BH, 8), kThreads, 0, st>>>(parts, R, A.dk, A.dv, N, nlev, Pc, nitems,
                                                                          nblocks);
         if (bwd_key_tc_supported(A)) {
             e = clear_err();
