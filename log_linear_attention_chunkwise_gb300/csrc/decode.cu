@@ -200,8 +200,9 @@ decode_step_kernel(float *__restrict__ S, float *__restrict__ D, const Tin *__re
 }
 
 // tail[bh][s] = sum_{r=s+1}^{T-1} g[bh][r], accumulated in fp64 and stored
-// fp32, in three launches over chunks of kTailChunk tokens: chunk sums, the
-// chunks' exclusive suffix sums, then each chunk's suffix scan plus its carry.
+// fp32, in two launches over chunks of kTailChunk tokens: chunk sums, then
+// each chunk's suffix scan plus its carry (the sum of the later chunks' sums,
+// formed by one warp of the chunk's CTA).
 constexpr int kTailChunk = 1024;
 
 __global__ void __launch_bounds__(256)
@@ -226,27 +227,22 @@ prefill_chunk_sum_kernel(const float *__restrict__ g, double *__restrict__ csum,
     }
 }
 
-// carry[c] = sum of the chunk sums after c, per (batch, head); one thread walks them.
-__global__ void __launch_bounds__(32)
-prefill_chunk_carry_kernel(const double *__restrict__ csum, double *__restrict__ carry, int nchunk)
-{
-    if (threadIdx.x != 0) return;
-    const long long bh = blockIdx.x;
-    double run = 0.0;
-    for (int c = nchunk - 1; c >= 0; c--) {
-        carry[bh * nchunk + c] = run;
-        run += csum[bh * nchunk + c];
-    }
-}
-
 __global__ void __launch_bounds__(kTailChunk)
-prefill_tail_kernel(const float *__restrict__ g, const double *__restrict__ carry, float *__restrict__ tail,
+prefill_tail_kernel(const float *__restrict__ g, const double *__restrict__ csum, float *__restrict__ tail,
                     int T, int nchunk)
 {
     __shared__ double wsum[kTailChunk / 32];
+    __shared__ double carry_sh;
     const long long bh = blockIdx.y;
     const int c = blockIdx.x;
     const int i = threadIdx.x, lane = i & 31, w = i >> 5;
+    if (w == 0) {  // the carry: the sums of the chunks after c, in a fixed order
+        double a = 0.0;
+        for (int c2 = c + 1 + lane; c2 < nchunk; c2 += 32) a += csum[bh * nchunk + c2];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+        if (lane == 0) carry_sh = a;
+    }
     const long long r = (long long)c * kTailChunk + i;
     const double x = r < T ? (double)g[bh * T + r] : 0.0;
     double incl = x;  // sum over this lane and the later lanes of the warp
@@ -268,7 +264,7 @@ prefill_tail_kernel(const float *__restrict__ g, const double *__restrict__ carr
         wsum[lane] = s - own;  // later warps of the chunk
     }
     __syncthreads();
-    if (r < T) tail[bh * T + r] = (float)(carry[bh * nchunk + c] + wsum[w] + (incl - x));
+    if (r < T) tail[bh * T + r] = (float)(carry_sh + wsum[w] + (incl - x));
 }
 
 constexpr int kSeg = 1024;  // tokens per CTA of the bucket kernel
@@ -370,13 +366,11 @@ cudaError_t launch_prefill(const PrefillArgs &A)
     const int nchunk = (A.T + kTailChunk - 1) / kTailChunk;
     const size_t tail_bytes = align_up((size_t)BH * A.T * sizeof(float), 256);
     double *csum = (double *)((char *)A.workspace + tail_bytes);
-    double *carry = csum + align_up((size_t)BH * nchunk, 32);
     prefill_chunk_sum_kernel<<<dim3(nchunk, (unsigned)BH), 256, 0, st>>>(A.g, csum, A.T, nchunk);
-    prefill_chunk_carry_kernel<<<(unsigned)BH, 32, 0, st>>>(csum, carry, nchunk);
-    prefill_tail_kernel<<<dim3(nchunk, (unsigned)BH), kTailChunk, 0, st>>>(A.g, carry, tail, A.T, nchunk);
+    prefill_tail_kernel<<<dim3(nchunk, (unsigned)BH), kTailChunk, 0, st>>>(A.g, csum, tail, A.T, nchunk);
     if (prefill_tc_supported(A)) {
         int *dev_err = A.device_error ? (int *)A.device_error
-                                      : (int *)((char *)(carry + align_up((size_t)BH * nchunk, 32)));
+                                      : (int *)((char *)(csum + align_up((size_t)BH * nchunk, 32)));
         if (!A.device_error) {
             err = cudaMemsetAsync(dev_err, 0, sizeof(int), st);
             if (err != cudaSuccess) return err;
@@ -398,11 +392,11 @@ cudaError_t decode_step(const DecodeArgs &A)
 
 size_t prefill_workspace_bytes(int B, int H, int T)
 {
-    // per-token tails, chunk sums and carries (fp64), the tensor-core path's error word
+    // per-token tails, chunk sums (fp64), the tensor-core path's error word
     const size_t BH = (size_t)B * H;
     const size_t nchunk = (size_t)((T > 0 ? T : 1) + kTailChunk - 1) / kTailChunk;
     return align_up(BH * (size_t)(T > 0 ? T : 1) * sizeof(float), 256) +
-           2 * align_up(BH * nchunk, 32) * sizeof(double) + 256;
+           align_up(BH * nchunk, 32) * sizeof(double) + 256;
 }
 
 cudaError_t prefill_state(const PrefillArgs &A)
