@@ -181,7 +181,6 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
     const int ntiles = i1 - i0;
     const double *Pb = prm.P + (long long)bh * (NT + 1);
 
-    grid_launch_dependents();  // the fix-up and read-out may start in this grid's tail
     if (tid == 0) {
         for (int b = 0; b < kWalkStages; b++) {
             mbar_init(&s.bar_load[b], 1);
@@ -198,16 +197,9 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
         tmem_alloc(&s.tmem, walk_tmem_cols<D>());
         tmem_relinquish();
     }
-    for (int j = tid; j <= kSeg; j += kWalkThreads) s.P[j] = (i0 + j <= NT) ? Pb[i0 + j] : 0.0;
-    tc_fence_before_sync();
-    __syncthreads();
-    tc_fence_after_sync();
-    const uint32_t tm = s.tmem;
-    // columns: stack level m at [D m, D m + D) for m < kSegLog; H after it
-    const uint32_t tm_h = tm + kSegLog * D;
-
-    // a tile's 128 gamma values are one aligned 512-byte run
-    auto issue_load = [&](int n) {
+    // a tile's K and V (inputs), then its 128 gamma values (from the gate
+    // launches: one aligned 512-byte run), on one barrier
+    auto issue_kv = [&](int n) {
         const int ls = n % kWalkStages, i = i0 + n;
         mbar_arrive_expect_tx(&s.bar_load[ls], 2 * kT + kTile * 4);
 #pragma unroll
@@ -215,8 +207,32 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
             tma_load_3d(s.k[ls] + h * kBlk, &map_k, &s.bar_load[ls], h * 64, i * kTile, bh);
             tma_load_3d(s.v[ls] + h * kBlk, &map_v, &s.bar_load[ls], h * 64, i * kTile, bh);
         }
+    };
+    auto issue_gamma = [&](int n) {
+        const int ls = n % kWalkStages, i = i0 + n;
         bulk_load(s.gm[ls], prm.gamma + ((long long)bh * NT + i) * kTile, kTile * 4, &s.bar_load[ls]);
     };
+    auto issue_load = [&](int n) {
+        issue_kv(n);
+        issue_gamma(n);
+    };
+    constexpr int kLoader = kWalkEpi + kWalkPrep;  // the loader lane
+    __syncthreads();  // the barriers are initialised
+    // the first tiles' K and V load while the gate launches finish; gamma and
+    // P only after them
+    if (tid == kLoader)
+        for (int n = 0; n < kWalkStages && n < ntiles; n++) issue_kv(n);
+    grid_dependency_wait();
+    grid_launch_dependents();  // the fix-up and read-out may start in this grid's tail (after the gates)
+    if (tid == kLoader)
+        for (int n = 0; n < kWalkStages && n < ntiles; n++) issue_gamma(n);
+    for (int j = tid; j <= kSeg; j += kWalkThreads) s.P[j] = (i0 + j <= NT) ? Pb[i0 + j] : 0.0;
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tm = s.tmem;
+    // columns: stack level m at [D m, D m + D) for m < kSegLog; H after it
+    const uint32_t tm_h = tm + kSegLog * D;
 
     if (tid >= kWalkEpi + kWalkPrep + 32) {
         // ---------------- MMA issuer (one lane): tile n's product once its V is
@@ -243,9 +259,8 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
         // ---------------- loader (one lane): a stage is refilled once the
         // product of the tile it held is done
         if ((tid & 31) == 0)
-            for (int n = 0; n < ntiles; n++) {
-                if (n >= kWalkStages && !mbar_wait(&s.bar_h, (n - kWalkStages) & 1, prm.wait_iters))
-                    set_err(prm.err, kErrMmaTimeout);
+            for (int n = kWalkStages; n < ntiles; n++) {  // the first stages were issued above
+                if (!mbar_wait(&s.bar_h, (n - kWalkStages) & 1, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
                 issue_load(n);
             }
     } else if (tid >= kWalkEpi) {
@@ -999,6 +1014,7 @@ __global__ void __launch_bounds__(1024)
 lla_tile_gate_sum_kernel(const float *__restrict__ g, double *__restrict__ P, float *__restrict__ gamma,
                          int *__restrict__ err, int *__restrict__ queue, int T, int NT)
 {
+    grid_launch_dependents();  // the scan may launch now; it waits for this grid
     const long long bh = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = blockIdx.x * 32 + warp;
@@ -1046,6 +1062,8 @@ lla_tile_gate_sum_kernel(const float *__restrict__ g, double *__restrict__ P, fl
 __global__ void __launch_bounds__(kScanThreads)
 lla_tile_gate_scan_kernel(double *__restrict__ P, int NT)
 {
+    grid_dependency_wait();    // the tile sums
+    grid_launch_dependents();  // the walkers may launch now; they wait for this grid
     __shared__ double wsum[32];
     __shared__ double carry_sh;
     const long long bh = blockIdx.x;
@@ -1209,15 +1227,25 @@ static cudaError_t tc_fwd_d(const TcFwdArgs &A)
     cudaStream_t st = (cudaStream_t)A.stream;
     lla_tile_gate_sum_kernel<<<dim3((NT + 31) / 32, BH), 1024, 0, st>>>(
         A.g, (double *)prm.P, prm.gamma, A.device_error ? nullptr : ws_err, prm.queue, A.T, NT);
-    lla_tile_gate_scan_kernel<<<BH, kScanThreads, 0, st>>>((double *)prm.P, NT);
     cudaError_t e;
+    {
+        // programmatic launches: the scan and then the walkers start while the launch
+        // before them finishes, and wait for it before reading its results
+        cudaLaunchAttribute attr;
+        cudaLaunchConfig_t cfg = launch_cfg(dim3(BH), dim3(kScanThreads), 0, st, true, &attr);
+        e = cudaLaunchKernelEx(&cfg, lla_tile_gate_scan_kernel, (double *)prm.P, NT);
+        if (e != cudaSuccess) return e;
+    }
     if (NT > 1) {
         const size_t wsmem = sizeof(WalkSmem<D>) + 1024;
         e = cudaFuncSetAttribute(lla_node_walker_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)wsmem);
         if (e != cudaSuccess) return e;
         const int nseg = (NT - 1 + kSeg - 1) / kSeg;
-        lla_node_walker_kernel<D><<<dim3(nseg, BH), kWalkThreads, wsmem, st>>>(mk, mv, mn, prm);
+        cudaLaunchAttribute attr;
+        cudaLaunchConfig_t cfg = launch_cfg(dim3(nseg, BH), dim3(kWalkThreads), wsmem, st, true, &attr);
+        e = cudaLaunchKernelEx(&cfg, lla_node_walker_kernel<D>, mk, mv, mn, prm);
+        if (e != cudaSuccess) return e;
         if (prm.nseg_full > 0) {
             cudaLaunchAttribute attr;
             cudaLaunchConfig_t cfg = launch_cfg(dim3(D * D / kFixElems, prm.nseg_full, BH), dim3(kFixThreads), 0,
