@@ -298,17 +298,19 @@ lambda_tc_kernel(const __grid_constant__ CUtensorMap map_d, const float *__restr
         }
     } else {
         // epilogue: kTcParts threads per row of the tile (= tensor-memory lane);
-        // part p takes the float4 groups g of lambda with g % kTcParts == p
+        // part p takes the float4 groups g of lambda with g % kTcParts == p.
+        // Tiles are taken in pairs (i, i + 1: accumulator sets 0 and 1), so that
+        // every W2 load from shared memory serves two rows: those loads (about
+        // four wavefronts each, although all lanes read one address) bound the
+        // kernel.
         const int row_t = tid & (kTcRows - 1), part = tid >> 7;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const bool vec = (L & 3) == 0 && ((uintptr_t)lam & 15) == 0;  // every row 16-byte aligned
-        for (int i = 0; i < my; i++) {
+        // h = hi + (mid + lo) from the three accumulators of set st
+        auto drain = [&](int i, float (&h)[NP]) {
             const int st = i & 1;
-            const long long row = (blockIdx.x + (long long)i * gridDim.x) * kTcRows + row_t;
             if (!mbar_wait(&bar_mma[st], (i >> 1) & 1, kTcWait)) atomicCAS(err, 0, 2);
             tc_fence_after_sync();
-            // h = hi + (mid + lo) from the three accumulators of the set
-            float h[NP];
             const uint32_t acc = tm + (uint32_t)(st * 3 * NP) + lane_off;
 #pragma unroll
             for (int c = 0; c < NP; c += 16) {
@@ -322,28 +324,50 @@ lambda_tc_kernel(const __grid_constant__ CUtensorMap map_d, const float *__restr
             }
             tc_fence_before_sync();
             mbar_arrive(&bar_free[st]);
-            if (row < N) {
-                float *out = lam + row * L;
-                for (int l0 = 4 * part; l0 < L; l0 += 4 * kTcParts) {
-                    float4 z = *reinterpret_cast<const float4 *>(bs + l0);
+        };
+        auto store = [&](long long row, const float4 &y, int l0) {
+            float *out = lam + row * L;
+            if (vec) {
+                *reinterpret_cast<float4 *>(out + l0) = y;
+            } else {
+                const float yy[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
-                    for (int j = 0; j < NP; j++) {
-                        const float4 w = *reinterpret_cast<const float4 *>(w2 + j * Lp + l0);
-                        z.x = fmaf(h[j], w.x, z.x);
-                        z.y = fmaf(h[j], w.y, z.y);
-                        z.z = fmaf(h[j], w.z, z.z);
-                        z.w = fmaf(h[j], w.w, z.w);
-                    }
-                    const float4 y = make_float4(softplus_f(z.x), softplus_f(z.y), softplus_f(z.z), softplus_f(z.w));
-                    if (vec) {
-                        *reinterpret_cast<float4 *>(out + l0) = y;
-                    } else {
-                        const float yy[4] = {y.x, y.y, y.z, y.w};
+                for (int q = 0; q < 4; q++)
+                    if (l0 + q < L) out[l0 + q] = yy[q];
+            }
+        };
+        for (int i = 0; i < my; i += 2) {
+            const bool two = i + 1 < my;
+            const long long row0 = (blockIdx.x + (long long)i * gridDim.x) * kTcRows + row_t;
+            const long long row1 = row0 + (long long)gridDim.x * kTcRows;
+            float h0[NP], h1[NP];
+            drain(i, h0);
+            if (two) {
+                drain(i + 1, h1);
+            } else {
 #pragma unroll
-                        for (int q = 0; q < 4; q++)
-                            if (l0 + q < L) out[l0 + q] = yy[q];
-                    }
+                for (int j = 0; j < NP; j++) h1[j] = 0.f;
+            }
+            for (int l0 = 4 * part; l0 < L; l0 += 4 * kTcParts) {
+                float4 z0 = *reinterpret_cast<const float4 *>(bs + l0), z1 = z0;
+#pragma unroll
+                for (int j = 0; j < NP; j++) {
+                    const float4 w = *reinterpret_cast<const float4 *>(w2 + j * Lp + l0);
+                    z0.x = fmaf(h0[j], w.x, z0.x);
+                    z0.y = fmaf(h0[j], w.y, z0.y);
+                    z0.z = fmaf(h0[j], w.z, z0.z);
+                    z0.w = fmaf(h0[j], w.w, z0.w);
+                    z1.x = fmaf(h1[j], w.x, z1.x);
+                    z1.y = fmaf(h1[j], w.y, z1.y);
+                    z1.z = fmaf(h1[j], w.z, z1.z);
+                    z1.w = fmaf(h1[j], w.w, z1.w);
                 }
+                if (row0 < N)
+                    store(row0, make_float4(softplus_f(z0.x), softplus_f(z0.y), softplus_f(z0.z), softplus_f(z0.w)),
+                          l0);
+                if (two && row1 < N)
+                    store(row1, make_float4(softplus_f(z1.x), softplus_f(z1.y), softplus_f(z1.z), softplus_f(z1.w)),
+                          l0);
             }
         }
     }
