@@ -143,3 +143,15 @@ def test_bwd_at_the_32k_workload_sampled_rows_and_identities():
         scale = max(abs(s) for s in sums)
         assert max(sums) - min(sums) <= 1e-4 * scale, (h, sums)
         assert abs(float(dg[0, h, 0])) <= 1e-4 * scale + 1e-6 * float(dg[0, h].abs().max()), (h, float(dg[0, h, 0]))
+    # dg against its definition at every token: the reverse running sum of
+    # sum_l lambda dlambda - k . dk, formed here in fp64 from the returned
+    # dlambda and dk (this checks the gate-gradient launches, the blocked
+    # reverse scan over 4096-token blocks included, at the full size)
+    lam_dl = lam * dl
+    k_dk = k * dk
+    dG = lam_dl.sum(-1) - k_dk.sum(-1)
+    ref = torch.flip(torch.cumsum(torch.flip(dG, [-1]), -1), [-1])
+    terms = lam_dl.abs().sum(-1) + k_dk.abs().sum(-1)
+    for h in range(cfg.H):
+        err = float((dg[0, h] - ref[0, h]).abs().max())
+        assert err <= 1e-6 * float(terms[0, h].sum()), (h, err, float(terms[0, h].sum()))
