@@ -587,24 +587,64 @@ bwd_key_kernel(const Tin *__restrict__ k, const Tin *__restrict__ v, const float
     }
 }
 
-// dG_u = sum_l lam_u[l] dlam_u[l] - k_u . dk_u, one warp per token (fp32 sums;
-// the long running sum over tokens below is fp64).
-template <typename Tin>
+// dG_u = sum_l lam_u[l] dlam_u[l] - k_u . dk_u, a warp per pair of tokens (fp32
+// sums; the long running sum over tokens below is fp64).  With 16-byte aligned
+// k and dk (VEC) each lane reads four consecutive elements of a row per load;
+// both tokens' loads are issued before their sums.
+template <typename Tin> struct Vec4;
+template <> struct Vec4<float> {
+    using type = float4;
+    __device__ static void to_f32(const float4 &x, float (&f)[4]) { f[0] = x.x; f[1] = x.y; f[2] = x.z; f[3] = x.w; }
+};
+template <> struct Vec4<__nv_bfloat16> {
+    using type = uint2;
+    __device__ static void to_f32(const uint2 &x, float (&f)[4])
+    {
+        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&x);
+        const float2 a = __bfloat1622float2(h[0]), b = __bfloat1622float2(h[1]);
+        f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    }
+};
+
+template <typename Tin, bool VEC>
 __global__ void __launch_bounds__(kThreads)
 bwd_gate_grad_kernel(const Tin *__restrict__ k, const float *__restrict__ lam,
                      const float *__restrict__ dlam, const float *__restrict__ dk,
                      double *__restrict__ dG, int T, int Dk, int L)
 {
     const int lane = threadIdx.x & 31;
-    const int u = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
-    if (u >= T) return;
-    const long long gi = (long long)blockIdx.y * T + u;
-    float a = 0.f;  // at most 4 + 1 terms per lane; the token's dG is summed in fp32
-    for (int l = lane; l < L; l += 32) a = fmaf(lam[gi * L + l], dlam[gi * L + l], a);
-    for (int r = lane; r < Dk; r += 32) a = fmaf(-to_f32(k[gi * Dk + r]), dk[gi * Dk + r], a);
+    const int u0 = 2 * (blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5));
+    if (u0 >= T) return;
+    float a[2] = {0.f, 0.f};
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
-    if (lane == 0) dG[gi] = (double)a;
+    for (int e = 0; e < 2; e++) {
+        const int u = u0 + e;
+        if (u < T) {
+            const long long gi = (long long)blockIdx.y * T + u;
+            for (int l = lane; l < L; l += 32) a[e] = fmaf(lam[gi * L + l], dlam[gi * L + l], a[e]);
+            if (VEC) {
+                using V = typename Vec4<Tin>::type;
+                for (int r = 4 * lane; r < Dk; r += 128) {
+                    const V kv = *reinterpret_cast<const V *>(k + gi * Dk + r);
+                    const float4 dv = *reinterpret_cast<const float4 *>(dk + gi * Dk + r);
+                    float kf[4];
+                    Vec4<Tin>::to_f32(kv, kf);
+                    a[e] = fmaf(-kf[0], dv.x, a[e]);
+                    a[e] = fmaf(-kf[1], dv.y, a[e]);
+                    a[e] = fmaf(-kf[2], dv.z, a[e]);
+                    a[e] = fmaf(-kf[3], dv.w, a[e]);
+                }
+            } else {
+                for (int r = lane; r < Dk; r += 32) a[e] = fmaf(-to_f32(k[gi * Dk + r]), dk[gi * Dk + r], a[e]);
+            }
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 2; e++) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) a[e] += __shfl_xor_sync(0xffffffffu, a[e], off);
+    }
+    if (lane < 2 && u0 + lane < T) dG[(long long)blockIdx.y * T + u0 + lane] = (double)(lane ? a[1] : a[0]);
 }
 
 // dg_r = sum_{u >= r} dG_u per (batch, head), fp64.  One CTA of 1024 threads
@@ -827,8 +867,15 @@ cudaError_t launch_bwd(const BwdArgs &A)
                 nlev, nblocks, Pc, nitems);
         }
     }
-    bwd_gate_grad_kernel<Tin><<<dim3((A.T + kThreads / 32 - 1) / (kThreads / 32), BH), kThreads, 0, st>>>(
-        (const Tin *)A.k, A.lam, A.dlam, A.dkey, dG, A.T, A.dk, A.L);
+    {
+        const dim3 grid((A.T + kThreads / 16 - 1) / (kThreads / 16), BH);  // two tokens per warp
+        if ((((uintptr_t)A.k | (uintptr_t)A.dkey) & 15u) == 0)
+            bwd_gate_grad_kernel<Tin, true><<<grid, kThreads, 0, st>>>((const Tin *)A.k, A.lam, A.dlam, A.dkey, dG,
+                                                                       A.T, A.dk, A.L);
+        else
+            bwd_gate_grad_kernel<Tin, false><<<grid, kThreads, 0, st>>>((const Tin *)A.k, A.lam, A.dlam, A.dkey, dG,
+                                                                        A.T, A.dk, A.L);
+    }
     bwd_gate_scan_kernel<<<dim3((A.T + kGateBlk - 1) / kGateBlk, BH), 1024, 0, st>>>(dG, A.dg, A.T);
     return cudaPeekAtLastError();
 }
