@@ -1,8 +1,8 @@
 // lla_fwd_host: the forward on inputs and outputs in host memory.
 //
 // The (batch, head) pairs are independent and each pair's rows are one
-// contiguous span of every tensor, so the call cuts them into groups and
-// pipelines three stages over two device slots: the copy of group j+1's
+// contiguous span of every tensor, so the call cuts them into groups (half
+// size at both ends) and pipelines three stages over two device slots: the copy of group j+1's
 // inputs (host -> device), the forward of group j, and the copy of group
 // j-1's output (device -> host) run at the same time on a copy-in stream,
 // the caller's stream and a copy-out stream.  The two copy directions use
@@ -157,11 +157,20 @@ lla_status lla_fwd_host(const void *q, const void *k, const void *v, const float
     LLA_TRY(cudaEventRecord(p->entry, cs));
     LLA_TRY(cudaStreamWaitEvent(p->h2d, p->entry, 0));
     LLA_TRY(cudaStreamWaitEvent(p->d2h, p->entry, 0));
-    const long long ngroups = (BH + G - 1) / G;
-    for (long long j = 0; j < ngroups; j++) {
+    // G pairs per group in the middle, half as many in the first and the last
+    // group: the pipeline's fill (the first input copy, alone) and drain (the
+    // last output copy, alone) are the transfer time it cannot overlap
+    const int Gh = G > 1 ? G / 2 : 1;
+    long long b0 = 0;
+    for (long long j = 0; b0 < BH; j++) {
         const int sl = (int)(j & 1);
-        const long long b0 = j * G;
-        const int n = (int)((BH - b0) < G ? (BH - b0) : G);
+        const long long rem = BH - b0;
+        long long nn;
+        if (j == 0) nn = rem < Gh ? rem : Gh;
+        else if (rem <= Gh) nn = rem;             // the last group
+        else if (rem <= G + Gh) nn = rem - Gh;    // leaves a small last group
+        else nn = G;
+        const int n = (int)nn;
         char *base = ws + sl * sb;
         char *dq = base;
         char *dk_ = dq + lla::align_up(s.q * G, 256);
@@ -189,6 +198,7 @@ lla_status lla_fwd_host(const void *q, const void *k, const void *v, const float
         LLA_TRY(cudaStreamWaitEvent(p->d2h, p->comp_done[sl], 0));
         LLA_TRY(cudaMemcpyAsync((char *)out + b0 * s.out, dout, n * s.out, cudaMemcpyDeviceToHost, p->d2h));
         LLA_TRY(cudaEventRecord(p->out_done[sl], p->d2h));
+        b0 += n;
     }
     LLA_TRY(cudaEventRecord(p->done, p->d2h));
     LLA_TRY(cudaStreamWaitEvent(cs, p->done, 0));
