@@ -264,8 +264,10 @@ lla_status lla_prefill_state(const void *k, const void *v, const float *g,
  * lla_fwd on inputs and outputs in host memory (same layouts and dtypes as
  * lla_fwd, host pointers; pin them for asynchronous copies).  The pages have
  * no counterpart: this is the host-facing call of the library.  The
- * (batch, head) pairs are processed in groups of `group` pairs (0: about an
- * eighth of them), pipelined over two device slots so that copying group
+ * (batch, head) pairs are processed in groups of at most `group` pairs (0:
+ * about an eighth of them; the first and the last group hold half as many,
+ * which shortens the copies that cannot overlap), pipelined over two device
+ * slots so that copying group
  * j+1 in, computing group j and copying group j-1 out overlap (two internal
  * streams, created on the first call on a device and kept until exit).
  * Ordered on `stream`: earlier work on it completes before the first copy,
