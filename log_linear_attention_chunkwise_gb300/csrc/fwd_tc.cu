@@ -307,7 +307,11 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
             const int J = i0 + n + 1;
             const int z = __ffs(J) - 1;
             const bool cross = (J == i0 + kSeg);  // closes a full segment
-            const int mlim = cross ? kSegLog : z;
+            // the tile before a segment-closing one (whose epilogue folds nothing)
+            // combines the stack, decayed to the segment's end, into level 0, so
+            // the closing tile folds that one level instead of kSegLog
+            const bool pre = (J == i0 + kSeg - 1) && (ntiles == kSeg);
+            const int mlim = cross ? 1 : z;
             if (!mbar_wait(&s.bar_h, n & 1, prm.wait_iters)) set_err(prm.err, kErrMmaTimeout);
             tc_fence_after_sync();
             float acc[kC];
@@ -318,7 +322,7 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
             mbar_arrive(&s.bar_hfree);  // the next tile's product may overwrite H
             const double PJ = s.P[J - i0];
             for (int m = 0; m < mlim; m++) {
-                const float f = __expf((float)(PJ - s.P[J - (1 << m) - i0]));
+                const float f = cross ? 1.f : __expf((float)(PJ - s.P[J - (1 << m) - i0]));
 #pragma unroll
                 for (int c = 0; c < kC; c += 16) {
                     float x[16];
@@ -329,7 +333,7 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
                 }
             }
             if (!cross) {
-                if (z < kSegLog) {
+                if (z < kSegLog && !pre) {
 #pragma unroll
                     for (int c = 0; c < kC; c += 16)
                         tmem_st16(tm + z * D + lane_off + c0 + c, *reinterpret_cast<float(*)[16]>(acc + c));
@@ -359,6 +363,30 @@ lla_node_walker_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_c
                     tma_store_commit();
                 }
                 nstage++;
+                if (pre) {
+                    // this node and the stack levels above it, each decayed to the
+                    // segment's end P_{i0 + kSeg}: the segment total less the next
+                    // tile's state
+                    const double PE = s.P[kSeg];
+                    const float f0 = __expf((float)(PE - PJ));
+#pragma unroll
+                    for (int u = 0; u < kC; u++) acc[u] *= f0;
+                    for (int m = 1; m < kSegLog; m++) {
+                        const float f = __expf((float)(PE - s.P[kSeg - (1 << m)]));
+#pragma unroll
+                        for (int c = 0; c < kC; c += 16) {
+                            float x[16];
+                            tmem_ld16(tm + m * D + lane_off + c0 + c, x);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int u = 0; u < 16; u++) acc[c + u] = fmaf(f, x[u], acc[c + u]);
+                        }
+                    }
+#pragma unroll
+                    for (int c = 0; c < kC; c += 16)
+                        tmem_st16(tm + lane_off + c0 + c, *reinterpret_cast<float(*)[16]>(acc + c));
+                    tmem_st_wait();
+                }
             } else {
                 float4 *dst = reinterpret_cast<float4 *>(
                     prm.segtot + (((long long)bh * prm.nseg_full + seg) * D + r) * D + c0);
